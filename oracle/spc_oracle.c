@@ -1,0 +1,375 @@
+/*
+ * spc_oracle.c -- plain, slow CPU oracle of the SpeCache decode hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY (see spc_oracle.h): used by the tests, smoke() and
+ * the benchmark's CPU baseline, never by the product path.
+ *
+ * Every function follows the SpeCache page ("SpeCache: Speculative Key-Value
+ * Caching for Efficient Generation of LLMs", arXiv 2503.16163) step by step:
+ *   - quantisation: section 3, "Original KIVI quantisation" (Q(X) = round((X-z)/s),
+ *     X' = Q(X)*s + z, z = min X, s = (max X - min X)/(2^B - 1)) and "Improved
+ *     1-bit quantisation" (z = (3 min X + max X)/4, s = (max X - min X)/2);
+ *   - grouping: keys per channel, values per token (KIVI, as the SemKV page
+ *     section 2.1 describes it), group size 32 and a bf16 residual window
+ *     (page 1 section 4, software setup);
+ *   - attention: O = Attn([T_t, T'_{t+1}], C' U C_kappa) of section 3
+ *     ("Decoding") and Algorithm 3, where C' U C_kappa replaces the low-bit rows
+ *     C'_kappa by the 16-bit rows C_kappa;
+ *   - ArgTopK over the speculative token's attention row (Algorithm 3, and
+ *     Algorithm 2 for the pre-decoding step);
+ *   - Pre-fetch: an index copy of 16-bit rows (Algorithm 3).
+ * Readings where the pages are silent (tie rules, metadata format, GQA
+ * summation, residual split) are the ones listed in the design notes and are
+ * restated at each function below.
+ *
+ * Build: gcc -O2 -fPIC -shared -fopenmp -ffp-contract=off (no contraction, so
+ * binary32 steps round exactly as written).
+ */
+#include "spc_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+static float bf16_to_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* The bf16 pattern of a value that is itself a bf16 value (min/max of bf16
+ * inputs), with -0.0 stored as +0.0. */
+static uint16_t float_to_bf16_exact(float f) {
+  if (f == 0.0f) return 0;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+int32_t orc_nq(const orc_dims* d) {
+  /* Reading: the quantised part is a whole number of 32-token groups and the
+   * residual window holds at least R tokens (KIVI keeps the most recent tokens
+   * in 16 bits; page 1 section 4).  N_q = floor((N-R)/32)*32 when N >= R. */
+  if (d->N <= d->R) return 0;
+  return ((d->N - d->R) / 32) * 32;
+}
+
+void orc_quant_params(int32_t bits, int32_t mode, float lo, float hi, float* z, float* s) {
+  if (bits == 1 && mode == 0) {
+    /* Improved 1-bit rule: z = (3 min + max)/4, s = (max - min)/2. */
+    *z = (3.0f * lo + hi) * 0.25f;
+    *s = (hi - lo) * 0.5f;
+  } else if (bits == 1) {
+    /* Original KIVI at B = 1: z = min, s = (max - min)/(2^1 - 1). */
+    *z = lo;
+    *s = hi - lo;
+  } else {
+    /* Original KIVI at B = 2: z = min, s = (max - min)/(2^2 - 1). */
+    *z = lo;
+    *s = (hi - lo) / 3.0f;
+  }
+}
+
+uint8_t orc_quant_code(int32_t bits, float x, float z, float s) {
+  /* Q(X) = round((X - z)/s).  Reading: round half to even, then clamp to the
+   * code range (at 1 bit (X-z)/s spans [-0.5, 1.5]); a constant group (s = 0)
+   * gets code 0, whose dequantised value z is the group's value. */
+  if (s == 0.0f) return 0;
+  float t = (x - z) / s;
+  float c = rintf(t);
+  float cmax = (float)((1 << bits) - 1);
+  if (c < 0.0f) c = 0.0f;
+  if (c > cmax) c = cmax;
+  return (uint8_t)c;
+}
+
+double orc_dequant(int32_t bits, int32_t mode, uint16_t lo_b, uint16_t hi_b, int32_t code) {
+  /* X' = Q(X) * s + z, evaluated in fp64 from the stored min/max. */
+  double lo = (double)bf16_to_float(lo_b), hi = (double)bf16_to_float(hi_b);
+  double z, s;
+  if (bits == 1 && mode == 0) {
+    z = (3.0 * lo + hi) / 4.0;
+    s = (hi - lo) / 2.0;
+  } else if (bits == 1) {
+    z = lo;
+    s = hi - lo;
+  } else {
+    z = lo;
+    s = (hi - lo) / 3.0;
+  }
+  return (double)code * s + z;
+}
+
+void orc_quantize(const orc_dims* d, int32_t mode, const uint16_t* K, const uint16_t* V,
+                  uint8_t* kcode, uint16_t* kmm, uint8_t* vcode, uint16_t* vmm) {
+  const int32_t B = d->B, H = d->Hkv, N = d->N, D = d->D, nq = orc_nq(d);
+  const int32_t ng = nq / 32, ncg = D / 32;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int32_t b = 0; b < B; ++b) {
+    for (int32_t h = 0; h < H; ++h) {
+      const uint16_t* Kbh = K + ((int64_t)(b * H + h) * N) * D;
+      const uint16_t* Vbh = V + ((int64_t)(b * H + h) * N) * D;
+      /* Keys: one group per (32-token block g, channel c). */
+      for (int32_t g = 0; g < ng; ++g) {
+        for (int32_t c = 0; c < D; ++c) {
+          float lo = bf16_to_float(Kbh[(int64_t)(32 * g) * D + c]), hi = lo;
+          for (int32_t j = 1; j < 32; ++j) {
+            float x = bf16_to_float(Kbh[(int64_t)(32 * g + j) * D + c]);
+            if (x < lo) lo = x;
+            if (x > hi) hi = x;
+          }
+          float z, s;
+          orc_quant_params(d->bits, mode, lo, hi, &z, &s);
+          int64_t m = (((int64_t)(b * H + h) * ng + g) * D + c) * 2;
+          kmm[m] = float_to_bf16_exact(lo);
+          kmm[m + 1] = float_to_bf16_exact(hi);
+          for (int32_t j = 0; j < 32; ++j) {
+            int32_t n = 32 * g + j;
+            float x = bf16_to_float(Kbh[(int64_t)n * D + c]);
+            kcode[((int64_t)(b * H + h) * nq + n) * D + c] = orc_quant_code(d->bits, x, z, s);
+          }
+        }
+      }
+      /* Values: one group per (token n, 32-channel block cg). */
+      for (int32_t n = 0; n < nq; ++n) {
+        for (int32_t cg = 0; cg < ncg; ++cg) {
+          float lo = bf16_to_float(Vbh[(int64_t)n * D + 32 * cg]), hi = lo;
+          for (int32_t j = 1; j < 32; ++j) {
+            float x = bf16_to_float(Vbh[(int64_t)n * D + 32 * cg + j]);
+            if (x < lo) lo = x;
+            if (x > hi) hi = x;
+          }
+          float z, s;
+          orc_quant_params(d->bits, mode, lo, hi, &z, &s);
+          int64_t m = (((int64_t)(b * H + h) * nq + n) * ncg + cg) * 2;
+          vmm[m] = float_to_bf16_exact(lo);
+          vmm[m + 1] = float_to_bf16_exact(hi);
+          for (int32_t j = 0; j < 32; ++j) {
+            int32_t c = 32 * cg + j;
+            float x = bf16_to_float(Vbh[(int64_t)n * D + c]);
+            vcode[((int64_t)(b * H + h) * nq + n) * D + c] = orc_quant_code(d->bits, x, z, s);
+          }
+        }
+      }
+    }
+  }
+}
+
+int64_t orc_record_bytes(int32_t bits) { return 1024 * (int64_t)(bits + 1); }
+
+/*
+ * The library's byte layout of one 32-token group (D = 128), written out as a
+ * plain index rule.  A group record is, in order:
+ *   K codes  : `bits` planes of 128 u32 words (plane p holds bit p of each code)
+ *   K minmax : 128 u32 words, min in bits 0..15 and max in bits 16..31 (bf16)
+ *   V codes  : `bits` planes of 128 u32 words
+ *   V minmax : 128 u32 words
+ * With L = 4a + t (a in 0..7, t in 0..3), j in 0..3 and bit b in 0..31:
+ *   K code word 4L+j, bit b : token 8j + a,
+ *                             channel 16*((b&15)>>1) + 2t + 8*(b&1) + (b>>4)
+ *   K minmax word 32t+m     : channel 16*(m>>2) + 2t + 8*((m>>1)&1) + (m&1)
+ *   V code word 4L+j, bit b : token 16*(j>>1) + 8*(j&1) + 2t + (b>>4),
+ *                             channel 16*((b&15)>>1) + 8*(b&1) + a
+ *   V minmax word 32t+m     : token 16*(m>>4) + 8*((m>>3)&1) + 2t + ((m>>2)&1),
+ *                             channel group m&3
+ * The residual window is bf16 [resid_cap, 2, D] per (b,hkv): row j holds the
+ * key then the value of token N_q + j.
+ */
+void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
+              const uint8_t* vcode, const uint16_t* vmm,
+              const uint16_t* K, const uint16_t* V,
+              int32_t q_groups_cap, int32_t resid_cap,
+              uint8_t* records, uint16_t* resid) {
+  const int32_t B = d->B, H = d->Hkv, N = d->N, D = d->D, nq = orc_nq(d), bits = d->bits;
+  const int32_t ng = nq / 32, ncg = D / 32, r = N - nq;
+  const int64_t RB = orc_record_bytes(bits);
+  for (int32_t b = 0; b < B; ++b) {
+    for (int32_t h = 0; h < H; ++h) {
+      const int64_t bh = (int64_t)b * H + h;
+      for (int32_t g = 0; g < ng; ++g) {
+        uint32_t* rec = (uint32_t*)(records + (bh * q_groups_cap + g) * RB);
+        uint32_t* kc = rec;
+        uint32_t* kmw = rec + 128 * bits;
+        uint32_t* vc = kmw + 128;
+        uint32_t* vmw = vc + 128 * bits;
+        memset(rec, 0, (size_t)RB);
+        for (int32_t p = 0; p < bits; ++p) {
+          for (int32_t L = 0; L < 32; ++L) {
+            int32_t a = L >> 2, t = L & 3;
+            for (int32_t j = 0; j < 4; ++j) {
+              uint32_t wk = 0, wv = 0;
+              for (int32_t bit = 0; bit < 32; ++bit) {
+                int32_t ktok = 8 * j + a;
+                int32_t kch = 16 * ((bit & 15) >> 1) + 2 * t + 8 * (bit & 1) + (bit >> 4);
+                int32_t kcv = kcode[(bh * nq + 32 * g + ktok) * D + kch];
+                wk |= (uint32_t)((kcv >> p) & 1) << bit;
+                int32_t vtok = 16 * (j >> 1) + 8 * (j & 1) + 2 * t + (bit >> 4);
+                int32_t vch = 16 * ((bit & 15) >> 1) + 8 * (bit & 1) + a;
+                int32_t vcv = vcode[(bh * nq + 32 * g + vtok) * D + vch];
+                wv |= (uint32_t)((vcv >> p) & 1) << bit;
+              }
+              kc[128 * p + 4 * L + j] = wk;
+              vc[128 * p + 4 * L + j] = wv;
+            }
+          }
+        }
+        for (int32_t t = 0; t < 4; ++t) {
+          for (int32_t m = 0; m < 32; ++m) {
+            int32_t kch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1);
+            int64_t km = ((bh * ng + g) * D + kch) * 2;
+            kmw[32 * t + m] = (uint32_t)kmm[km] | ((uint32_t)kmm[km + 1] << 16);
+            int32_t vtok = 16 * (m >> 4) + 8 * ((m >> 3) & 1) + 2 * t + ((m >> 2) & 1);
+            int32_t cg = m & 3;
+            int64_t vm = ((bh * nq + 32 * g + vtok) * ncg + cg) * 2;
+            vmw[32 * t + m] = (uint32_t)vmm[vm] | ((uint32_t)vmm[vm + 1] << 16);
+          }
+        }
+      }
+      for (int32_t j = 0; j < r; ++j) {
+        const int64_t src = (bh * N + nq + j) * D;
+        uint16_t* dst = resid + ((bh * resid_cap + j) * 2) * D;
+        memcpy(dst, K + src, sizeof(uint16_t) * (size_t)D);
+        memcpy(dst + D, V + src, sizeof(uint16_t) * (size_t)D);
+      }
+    }
+  }
+}
+
+void orc_attention(const orc_dims* d, int32_t mode, const uint16_t* q,
+                   const uint8_t* kcode, const uint16_t* kmm,
+                   const uint8_t* vcode, const uint16_t* vmm,
+                   const uint16_t* K, const uint16_t* V,
+                   const int32_t* idx, int32_t k,
+                   double* o, double* lse, double* S) {
+  const int32_t B = d->B, H = d->Hkv, Hq = d->Hq, N = d->N, D = d->D, nq = orc_nq(d);
+  const int32_t G = Hq / H, ng = nq / 32, ncg = D / 32;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int32_t b = 0; b < B; ++b) {
+    for (int32_t hk = 0; hk < H; ++hk) {
+      const int64_t bh = (int64_t)b * H + hk;
+      /* Rows of K and V as this step sees them: C' U C_kappa plus the residual. */
+      double* kr = (double*)malloc(sizeof(double) * (size_t)N * D);
+      double* vr = (double*)malloc(sizeof(double) * (size_t)N * D);
+      char* sel = (char*)calloc((size_t)(nq > 0 ? nq : 1), 1);
+      if (idx != NULL) {
+        for (int32_t j = 0; j < k; ++j) {
+          int32_t n = idx[bh * k + j];
+          if (n >= 0 && n < nq) sel[n] = 1;
+        }
+      }
+      for (int32_t n = 0; n < N; ++n) {
+        for (int32_t c = 0; c < D; ++c) {
+          if (n < nq && !sel[n]) {
+            int64_t km = ((bh * ng + n / 32) * D + c) * 2;
+            int64_t vm = ((bh * nq + n) * ncg + c / 32) * 2;
+            kr[(int64_t)n * D + c] = orc_dequant(d->bits, mode, kmm[km], kmm[km + 1],
+                                                 kcode[(bh * nq + n) * D + c]);
+            vr[(int64_t)n * D + c] = orc_dequant(d->bits, mode, vmm[vm], vmm[vm + 1],
+                                                 vcode[(bh * nq + n) * D + c]);
+          } else {
+            kr[(int64_t)n * D + c] = (double)bf16_to_float(K[(bh * N + n) * D + c]);
+            vr[(int64_t)n * D + c] = (double)bf16_to_float(V[(bh * N + n) * D + c]);
+          }
+        }
+      }
+      double* logit = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+      if (S != NULL)
+        for (int32_t n = 0; n < nq; ++n) S[bh * nq + n] = 0.0;
+      for (int32_t gi = 0; gi < G; ++gi) {
+        const int32_t h = hk * G + gi;
+        for (int32_t i = 0; i < 2; ++i) {
+          const uint16_t* qv = q + (((int64_t)b * 2 + i) * Hq + h) * D;
+          double mx = -INFINITY;
+          for (int32_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int32_t c = 0; c < D; ++c)
+              acc += (double)bf16_to_float(qv[c]) * kr[(int64_t)n * D + c];
+            logit[n] = d->scale * acc;
+            if (logit[n] > mx) mx = logit[n];
+          }
+          double den = 0.0;
+          for (int32_t n = 0; n < N; ++n) den += exp(logit[n] - mx);
+          double* ov = o ? o + (((int64_t)b * 2 + i) * Hq + h) * D : NULL;
+          if (ov != NULL) {
+            for (int32_t c = 0; c < D; ++c) ov[c] = 0.0;
+            for (int32_t n = 0; n < N; ++n) {
+              double p = exp(logit[n] - mx) / den;
+              for (int32_t c = 0; c < D; ++c) ov[c] += p * vr[(int64_t)n * D + c];
+            }
+          }
+          if (lse != NULL) lse[((int64_t)b * 2 + i) * Hq + h] = (N > 0) ? mx + log(den) : -INFINITY;
+          /* Reading: the score of position n for ArgTopK is the speculative
+           * token's probability summed over the query heads sharing KV head hk. */
+          if (S != NULL && i == 1)
+            for (int32_t n = 0; n < nq; ++n) S[bh * nq + n] += exp(logit[n] - mx) / den;
+        }
+      }
+      free(logit);
+      free(sel);
+      free(kr);
+      free(vr);
+    }
+  }
+}
+
+typedef struct {
+  double s;
+  int32_t n;
+} scored_pos;
+
+static int by_score_then_index(const void* a, const void* b) {
+  const scored_pos* x = (const scored_pos*)a;
+  const scored_pos* y = (const scored_pos*)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  return (x->n < y->n) ? -1 : (x->n > y->n);
+}
+
+static int by_int(const void* a, const void* b) {
+  int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+  return (x < y) ? -1 : (x > y);
+}
+
+void orc_topk(const orc_dims* d, const double* S, int32_t k, int32_t* idx, uint32_t* bitmap) {
+  const int32_t B = d->B, H = d->Hkv, nq = orc_nq(d);
+  const int32_t nw = (nq + 31) / 32;
+  const int32_t keff = k < nq ? k : nq;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int32_t b = 0; b < B; ++b) {
+    for (int32_t h = 0; h < H; ++h) {
+      const int64_t bh = (int64_t)b * H + h;
+      scored_pos* all = (scored_pos*)malloc(sizeof(scored_pos) * (size_t)(nq > 0 ? nq : 1));
+      for (int32_t n = 0; n < nq; ++n) {
+        all[n].s = S[bh * nq + n];
+        all[n].n = n;
+      }
+      qsort(all, (size_t)nq, sizeof(scored_pos), by_score_then_index);
+      int32_t* out = idx + bh * k;
+      for (int32_t j = 0; j < keff; ++j) out[j] = all[j].n;
+      qsort(out, (size_t)keff, sizeof(int32_t), by_int);
+      for (int32_t j = keff; j < k; ++j) out[j] = -1;
+      if (bitmap != NULL) {
+        uint32_t* bm = bitmap + bh * nw;
+        for (int32_t w = 0; w < nw; ++w) bm[w] = 0;
+        for (int32_t j = 0; j < keff; ++j) bm[out[j] / 32] |= 1u << (out[j] % 32);
+      }
+      free(all);
+    }
+  }
+}
+
+void orc_gather(const orc_dims* d, const uint16_t* host, int64_t n_cap,
+                const int32_t* idx, int32_t k, uint16_t* staging) {
+  const int32_t B = d->B, H = d->Hkv, D = d->D;
+  for (int32_t b = 0; b < B; ++b)
+    for (int32_t h = 0; h < H; ++h) {
+      const int64_t bh = (int64_t)b * H + h;
+      for (int32_t j = 0; j < k; ++j) {
+        int32_t n = idx[bh * k + j];
+        if (n < 0) continue;
+        memcpy(staging + (bh * k + j) * 2 * D, host + (bh * n_cap + n) * 2 * D,
+               sizeof(uint16_t) * 2 * (size_t)D);
+      }
+    }
+}

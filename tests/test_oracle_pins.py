@@ -1,0 +1,361 @@
+"""Pins of the CPU oracle to what the pages and the mathematics fix.
+
+Each test ties an oracle function to something other than itself: the hand
+worked examples under tests/golden (from the SpeCache page's formulas), the
+half-interval geometry the page states, exact rational arithmetic, library
+routines (torch's scaled-dot-product attention and softmax in fp64, numpy's
+lexsort), closed-form byte counts the page prints, and invariants of softmax
+attention.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def f2b(x):
+    """Exact bf16 bits of a float that is representable in bf16."""
+    b = synth.f32_to_bf16_rne(np.asarray(x, np.float32))
+    assert np.all(synth.bf16_to_f32(b) == np.asarray(x, np.float32)), "not a bf16 value"
+    return b
+
+
+def b2f(b):
+    return synth.bf16_to_f32(np.asarray(b, np.uint16)).astype(np.float64)
+
+
+def read_golden(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        rows.append([s.split() for s in line.split("|")])
+    return rows
+
+
+def quantize_key_group(bits, values, mode=0):
+    """Quantise one key group (32 tokens of channel 0) holding `values` (padded)."""
+    vals = list(values) + [values[0]] * (32 - len(values))
+    N = 32 + 0
+    d = oracle.dims(B=1, Hq=1, Hkv=1, N=N, R=0, bits=bits)
+    K = np.zeros((1, 1, N, 128), np.uint16)
+    K[0, 0, :, 0] = f2b(np.array(vals, np.float32))
+    V = np.zeros_like(K)
+    qz = oracle.quantize(d, K, V, mode=mode)
+    codes = qz["kcode"][0, 0, :len(values), 0].astype(int)
+    lo, hi = qz["kmm"][0, 0, 0, 0]
+    deq = [oracle.dequant(bits, int(lo), int(hi), int(c), mode) for c in codes]
+    return codes, deq, b2f(lo), b2f(hi)
+
+
+@pytest.mark.parametrize("name,bits", [("quant_1bit_worked.txt", 1), ("quant_2bit_worked.txt", 2)])
+def test_golden_worked_examples(name, bits):
+    for (mm, vals, codes, deq) in read_golden(name):
+        lo, hi = float(mm[0]), float(mm[1])
+        values = [float(v) for v in vals]
+        # pad with min and max so the group's extremes are the stated ones
+        group = values + [lo, hi]
+        got_codes, got_deq, glo, ghi = quantize_key_group(bits, group)
+        assert (glo, ghi) == (lo, hi)
+        assert list(got_codes[:len(values)]) == [int(c) for c in codes]
+        assert got_deq[:len(values)] == [float(x) for x in deq]
+
+
+def random_bf16_group(rng, n, lo_exp=-3, hi_exp=3):
+    """bf16 values whose exponents stay within a small range (P1's premise)."""
+    mant = rng.integers(128, 256, size=n)
+    exp = rng.integers(lo_exp, hi_exp + 1, size=n)
+    sign = rng.choice([-1.0, 1.0], size=n)
+    return (sign * mant.astype(np.float64) / 128.0 * np.power(2.0, exp)).astype(np.float32)
+
+
+def test_p1_one_bit_lands_on_half_interval_centres():
+    """Page 1 section 3: values below the midpoint dequantise to the centre of
+    [min, mid), values above it to the centre of (mid, max], exactly."""
+    rng = np.random.default_rng(1)
+    for _ in range(200):
+        vals = random_bf16_group(rng, 32)
+        codes, deq, lo, hi = quantize_key_group(1, list(vals))
+        lo_f, hi_f = Fraction(lo), Fraction(hi)
+        mid = (lo_f + hi_f) / 2
+        low_centre = (lo_f + mid) / 2
+        high_centre = (mid + hi_f) / 2
+        for x, c, xd in zip(vals, codes, deq):
+            xf = Fraction(float(x))
+            want = 0 if xf <= mid else 1
+            assert c == want
+            assert Fraction(xd) == (low_centre if c == 0 else high_centre)
+
+
+def test_p1_centres_minimise_uniform_error():
+    """The page's reason for the new z, s: under a uniform distribution on
+    [min, max] the two half-interval centres minimise the mean squared error.
+    Moving either reconstruction level away from the oracle's value raises it."""
+    codes, deq, lo, hi = quantize_key_group(1, [-1.0, 3.0])
+    levels = sorted(set(deq))
+    x = np.linspace(lo, hi, 200001)
+
+    def mse(l0, l1):
+        return np.mean(np.minimum((x - l0) ** 2, (x - l1) ** 2))
+
+    base = mse(*levels)
+    for d0, d1 in [(0.05, 0), (-0.05, 0), (0, 0.05), (0, -0.05)]:
+        assert mse(levels[0] + d0, levels[1] + d1) > base
+    # original KIVI 1-bit (z = min, s = max - min) gives a strictly larger error
+    _, deq_kivi, _, _ = quantize_key_group(1, [-1.0, 3.0], mode=1)
+    assert mse(*sorted(set(deq_kivi))) > base
+
+
+def test_p2_two_bit_nearest_grid_point():
+    """KIVI 2-bit: the code is the nearest point of {min + i*s}, s=(max-min)/3."""
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        vals = random_bf16_group(rng, 32)
+        codes, deq, lo, hi = quantize_key_group(2, list(vals))
+        lo_f, hi_f = Fraction(lo), Fraction(hi)
+        for x, c in zip(vals, codes):
+            if hi_f == lo_f:
+                assert c == 0
+                continue
+            t = 3 * (Fraction(float(x)) - lo_f) / (hi_f - lo_f)
+            fl = math.floor(t)
+            if t - fl == Fraction(1, 2):
+                assert c in (fl, fl + 1)  # exact ties: either neighbour is nearest
+            else:
+                assert c == min(max(round(t), 0), 3)
+
+
+def test_p3_original_kivi_one_bit_gives_min_and_max():
+    """Page 1 section 3: with the original KIVI rule at 1 bit every X' is max X or min X."""
+    rng = np.random.default_rng(3)
+    vals = random_bf16_group(rng, 32)
+    codes, deq, lo, hi = quantize_key_group(1, list(vals), mode=1)
+    assert set(deq) <= {lo, hi}
+    two = quantize_key_group(1, [0.5, 2.0] * 16)
+    assert two[0][0] != two[0][1]  # SpeCache's rule separates a two-valued group
+
+
+def test_constant_group_and_value_axis():
+    """min == max gives code 0 and X' = the constant; value groups run over channels."""
+    d = oracle.dims(B=1, Hq=1, Hkv=1, N=32, R=0, bits=1)
+    K = np.full((1, 1, 32, 128), f2b(np.float32(0.75)), np.uint16)
+    V = np.zeros_like(K)
+    V[0, 0, 5, 32:64] = f2b(np.float32(-2.0))
+    V[0, 0, 5, 40] = f2b(np.float32(1.0))
+    qz = oracle.quantize(d, K, V)
+    assert np.all(qz["kcode"] == 0)
+    assert oracle.dequant(1, int(qz["kmm"][0, 0, 0, 3, 0]), int(qz["kmm"][0, 0, 0, 3, 1]), 0) == 0.75
+    lo, hi = qz["vmm"][0, 0, 5, 1]
+    assert (b2f(lo), b2f(hi)) == (-2.0, 1.0)
+    assert qz["vcode"][0, 0, 5, 40] == 1 and qz["vcode"][0, 0, 5, 33] == 0
+    assert tuple(qz["vmm"][0, 0, 5, 0]) == (0, 0)  # -0.0/+0.0 stored as +0.0
+
+
+def test_residual_split():
+    for N, R, want in [(1024, 32, 992), (32768, 128, 32640), (100, 64, 32), (64, 64, 0), (10, 64, 0),
+                       (2048, 128, 1920)]:
+        assert oracle.nq(oracle.dims(B=1, Hq=1, Hkv=1, N=N, R=R, bits=1)) == want
+
+
+def dequant_tensors(d, qz):
+    """Dequantised K', V' of the oracle's own codes (fp64), for library comparisons."""
+    nq = oracle.nq(d)
+    kmm = b2f(qz["kmm"])
+    vmm = b2f(qz["vmm"])
+    klo = np.repeat(kmm[..., 0], 32, axis=2)
+    khi = np.repeat(kmm[..., 1], 32, axis=2)
+    vlo = np.repeat(vmm[..., 0], 32, axis=3)
+    vhi = np.repeat(vmm[..., 1], 32, axis=3)
+    if d.bits == 1:
+        kz, ks = (3 * klo + khi) / 4, (khi - klo) / 2
+        vz, vs = (3 * vlo + vhi) / 4, (vhi - vlo) / 2
+    else:
+        kz, ks = klo, (khi - klo) / 3
+        vz, vs = vlo, (vhi - vlo) / 3
+    Kd = qz["kcode"].astype(np.float64) * ks + kz
+    Vd = qz["vcode"].astype(np.float64) * vs + vz
+    assert Kd.shape[2] == nq
+    return Kd, Vd
+
+
+def sdpa_reference(d, q, Keff, Veff):
+    """torch's attention and softmax in fp64 over the effective K, V rows."""
+    G = d.Hq // d.Hkv
+    qf = torch.from_numpy(b2f(q))  # [B,2,Hq,D]
+    Kt = torch.from_numpy(Keff).repeat_interleave(G, dim=1)  # [B,Hq,N,D]
+    Vt = torch.from_numpy(Veff).repeat_interleave(G, dim=1)
+    qh = qf.permute(0, 2, 1, 3)  # [B,Hq,2,D]
+    o = torch.nn.functional.scaled_dot_product_attention(qh, Kt, Vt, scale=d.scale)
+    logits = torch.einsum("bhid,bhnd->bhin", qh, Kt) * d.scale
+    lse = torch.logsumexp(logits, dim=-1)
+    p = torch.softmax(logits, dim=-1)
+    return o.permute(0, 2, 1, 3).numpy(), lse.permute(0, 2, 1).numpy(), p.numpy()
+
+
+@pytest.mark.parametrize("bits,B,Hq,Hkv,N,R", [(1, 1, 4, 1, 160, 64), (2, 2, 2, 2, 96, 32),
+                                               (1, 1, 8, 2, 200, 40)])
+def test_p6_attention_matches_library_on_tiny_inputs(bits, B, Hq, Hkv, N, R):
+    d = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N, R=R, bits=bits)
+    K, V = synth.kv_layer(7, 0, B, Hkv, N)
+    q = synth.queries(7, 0, B, Hq)
+    qz = oracle.quantize(d, K, V)
+    nq = oracle.nq(d)
+    Kd, Vd = dequant_tensors(d, qz)
+    Keff = np.concatenate([Kd, b2f(K)[:, :, nq:]], axis=2)
+    Veff = np.concatenate([Vd, b2f(V)[:, :, nq:]], axis=2)
+    o_ref, lse_ref, p_ref = sdpa_reference(d, q, Keff, Veff)
+    o, lse, S = oracle.attention(d, q, qz, K, V)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+    G = Hq // Hkv
+    S_ref = p_ref[:, :, 1, :nq].reshape(B, Hkv, G, nq).sum(axis=2)
+    np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-13)
+
+
+def test_p4_all_positions_fetched_equals_full_precision_attention():
+    """Page 1 section 3: C' U C_kappa replaces the low-bit rows by the 16-bit
+    ones, so fetching every position gives plain bf16 attention."""
+    B, Hq, Hkv, N, R = 1, 4, 2, 192, 64
+    d = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N, R=R, bits=1)
+    K, V = synth.kv_layer(11, 0, B, Hkv, N)
+    q = synth.queries(11, 0, B, Hq)
+    qz = oracle.quantize(d, K, V)
+    nq = oracle.nq(d)
+    idx = np.broadcast_to(np.arange(nq, dtype=np.int32), (B, Hkv, nq)).copy()
+    o, lse, S = oracle.attention(d, q, qz, K, V, idx=idx)
+    o_ref, lse_ref, _ = sdpa_reference(d, q, b2f(K), b2f(V))
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+    # and the low-bit attention is measurably different (the substitution matters)
+    o0, _, _ = oracle.attention(d, q, qz, K, V)
+    assert np.abs(o0 - o_ref).max() > 1e-3
+
+
+def test_p5_k0_is_plain_low_bit_attention_and_padding_is_ignored():
+    B, Hq, Hkv, N, R = 1, 4, 1, 160, 32
+    d = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N, R=R, bits=1)
+    K, V = synth.kv_layer(5, 0, B, Hkv, N)
+    q = synth.queries(5, 0, B, Hq)
+    qz = oracle.quantize(d, K, V)
+    a = oracle.attention(d, q, qz, K, V)
+    b = oracle.attention(d, q, qz, K, V, idx=np.zeros((B, Hkv, 0), np.int32))
+    c = oracle.attention(d, q, qz, K, V, idx=np.full((B, Hkv, 4), -1, np.int32))
+    for x, y, z in zip(a, b, c):
+        assert np.array_equal(x, y) and np.array_equal(x, z)
+
+
+def test_p9_softmax_invariants():
+    B, Hq, Hkv, N = 1, 4, 1, 128
+    d = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N, R=0, bits=1)
+    K, V = synth.kv_layer(3, 0, B, Hkv, N)
+    q = synth.queries(3, 0, B, Hq)
+    qz = oracle.quantize(d, K, V)
+    o, lse, S = oracle.attention(d, q, qz, K, V)
+    # no residual: the speculative row sums to 1 per query head
+    np.testing.assert_allclose(S.sum(axis=-1), Hq // Hkv, rtol=1e-13)
+    # the same V row at every position, constant within each 32-channel value
+    # group (so quantisation is lossless), comes back exactly
+    row = np.repeat(f2b(np.array([0.5, -1.25, 3.0, 0.0], np.float32)), 32)
+    Vc = np.broadcast_to(row, V.shape).copy()
+    qzc = oracle.quantize(d, K, Vc)
+    oc, _, _ = oracle.attention(d, q, qzc, K, Vc)
+    np.testing.assert_allclose(oc, np.broadcast_to(b2f(Vc[:, 0, 0, :])[:, None, None, :], oc.shape), atol=1e-12)
+    # permuting whole 32-token groups permutes S and leaves o, lse unchanged
+    perm = np.array([2, 0, 3, 1])
+    tok = (perm[:, None] * 32 + np.arange(32)[None, :]).reshape(-1)
+    Kp, Vp = K[:, :, tok], V[:, :, tok]
+    qzp = oracle.quantize(d, Kp, Vp)
+    op, lsep, Sp = oracle.attention(d, q, qzp, Kp, Vp)
+    np.testing.assert_allclose(op, o, atol=1e-12)
+    np.testing.assert_allclose(lsep, lse, atol=1e-12)
+    np.testing.assert_allclose(Sp, S[:, :, tok], atol=1e-15)
+
+
+def test_topk_matches_library_sort_with_ties():
+    rng = np.random.default_rng(4)
+    B, Hkv, nq = 2, 3, 320
+    d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=nq, R=0, bits=1)
+    S = rng.integers(0, 40, size=(B, Hkv, nq)).astype(np.float64) / 7.0  # many ties
+    for k in (0, 1, 17, 64, 320, 400):
+        idx, bm = oracle.topk(d, S, k)
+        keff = min(k, nq)
+        for b in range(B):
+            for h in range(Hkv):
+                order = np.lexsort((np.arange(nq), -S[b, h]))
+                want = np.sort(order[:keff])
+                assert np.array_equal(idx[b, h, :keff], want)
+                assert np.all(idx[b, h, keff:] == -1)
+                bits = np.unpackbits(bm[b, h].view(np.uint8), bitorder="little")[:nq]
+                assert np.array_equal(np.flatnonzero(bits), want)
+
+
+def test_p10_single_head_topk_is_topk_by_logit():
+    B, Hq, Hkv, N, R = 1, 1, 1, 288, 32
+    d = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N, R=R, bits=1)
+    K, V = synth.kv_layer(9, 0, B, Hkv, N)
+    q = synth.queries(9, 0, B, Hq)
+    qz = oracle.quantize(d, K, V)
+    _, _, S = oracle.attention(d, q, qz, K, V)
+    Kd, _ = dequant_tensors(d, qz)
+    logits = torch.from_numpy(Kd[0, 0]) @ torch.from_numpy(b2f(q[0, 1, 0]))
+    idx, _ = oracle.topk(d, S, 20)
+    want = np.sort(np.lexsort((np.arange(len(logits)), -logits.numpy()))[:20])
+    assert np.array_equal(idx[0, 0], want)
+
+
+def test_p7_gather_is_an_exact_row_copy():
+    rng = np.random.default_rng(6)
+    B, Hkv, ncap, k = 2, 3, 500, 37
+    d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=ncap, R=0, bits=1)
+    host = rng.integers(0, 1 << 16, size=(B, Hkv, ncap, 2, 128), dtype=np.uint16)
+    idx = np.sort(rng.choice(ncap, size=(B, Hkv, k)), axis=-1).astype(np.int32)
+    st = oracle.gather(d, host, idx)
+    for b in range(B):
+        for h in range(Hkv):
+            assert st[b, h].tobytes() == host[b, h, idx[b, h]].tobytes()
+
+
+def test_p8_compression_ratio_matches_printed_values():
+    """Figure 4 caption: 0.13 (Mistral, 32k) and 0.14 (LLaMA-3, 8k) at g = 32.
+    The low-bit copy stores codes plus a bf16 (min, max) pair per 32 values."""
+    for (row,) in read_golden("compression_ratio.txt"):
+        model, ctx, resid, bits, printed = row
+        ctx, resid, bits = int(ctx), int(resid), int(bits)
+        d = oracle.dims(B=1, Hq=1, Hkv=1, N=ctx, R=resid, bits=bits)
+        nq = oracle.nq(d)
+        gpu_bytes = nq // 32 * oracle.record_bytes(bits) + (ctx - nq) * 2 * 128 * 2
+        ratio = gpu_bytes / (ctx * 2 * 128 * 2)
+        assert round(ratio, 2) == float(printed)
+    # fp32 metadata would not reproduce the printed ratios
+    assert round((32640 * (32 + 64) + 128 * 512) / (32768 * 512), 2) != 0.13
+
+
+def test_pack_places_every_bit_exactly_once():
+    """The packed layout is a bijection between (token, channel, plane) and bits."""
+    for bits in (1, 2):
+        d = oracle.dims(B=1, Hq=1, Hkv=1, N=32, R=0, bits=bits)
+        K = np.zeros((1, 1, 32, 128), np.uint16)
+        V = np.zeros_like(K)
+        base = oracle.quantize(d, K, V)
+        seen_k = set()
+        seen_v = set()
+        for p in range(bits):
+            for n in range(0, 32, 3):
+                for c in range(0, 128, 5):
+                    for which in ("kcode", "vcode"):
+                        qz = {k: v.copy() for k, v in base.items()}
+                        qz[which][0, 0, n, c] = 1 << p
+                        rec, _ = oracle.pack(d, qz, K, V)
+                        on = np.flatnonzero(np.unpackbits(rec[0, 0, 0]))
+                        assert len(on) == 1
+                        (seen_k if which == "kcode" else seen_v).add(int(on[0]))
+        assert len(seen_k) == len(seen_v) == bits * 11 * 26
