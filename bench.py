@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark of the SpeCache decode hot path on GB300.
+
+Workload: one decode step of LLaMA-3-8B's attention over all 32 layers
+(batch 8, 32 query / 8 KV heads, head dim 128, 32K context, 1-bit cache,
+top-1% = 328 fetched rows per KV head).  Per layer, the main stream runs the
+merged two-query attention over C' U C_kappa; a side stream then runs the
+speculative top-k and the gather of the selected bf16 rows from pinned host
+memory, overlapped with the following layers' attention.  A step is captured
+once as a CUDA graph and replayed.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=32, Hkv=8, D=128, "
+                         "N=32768, 1-bit, residual 128, top-1% (k=328)",
+                B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328, layers=32)
+METRIC = "decode attn steps/s at 32K ctx, 1-bit, top-1% (HBM GB/s and % of peak in roofline)"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["spc", "reference"], default="spc")
+    p.add_argument("--layers", type=int, default=WORKLOAD["layers"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-pairs", type=int, default=16, help="(b, kv-head) pairs in the oracle sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def record_external(ev, stream):
+    """Record a timing event so that it survives CUDA graph capture."""
+    ev.record(stream)
+
+
+def make_timing_event(torch):
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True), record_external
+    except TypeError:
+        pass
+    # older torch: record through the CUDA runtime with cudaEventRecordExternal
+    lib = None
+    with open("/proc/self/maps") as f:
+        for line in f:
+            if "libcudart.so" in line:
+                lib = ctypes.CDLL(line.split()[-1])
+                break
+    if lib is None:
+        lib = ctypes.CDLL("libcudart.so")
+    lib.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+    ev = torch.cuda.Event(enable_timing=True)
+    ev.record()  # create the underlying event
+    torch.cuda.synchronize()
+
+    def rec(e, stream):
+        err = lib.cudaEventRecordWithFlags(ctypes.c_void_p(e.cuda_event), ctypes.c_void_p(stream.cuda_stream), 1)
+        if err != 0:
+            raise RuntimeError(f"cudaEventRecordWithFlags failed: {err}")
+    return ev, rec
+
+
+# ------------------------------------------------------------------ the GPU workload
+
+class DecodeStep:
+    def __init__(self, W, layers, seed=0):
+        import torch
+
+        import bit_kv_cache_spc_gb300 as spc
+        import synth
+        import synth.gpu
+        self.torch, self.spc = torch, spc
+        B, Hq, Hkv, N, R, bits, k = (W[x] for x in ("B", "Hq", "Hkv", "N", "R", "bits", "k"))
+        self.W, self.L, self.k = W, layers, k
+        self.G = Hq // Hkv
+        self.d = spc.Dims(B, Hq, Hkv, N, R, bits, scale=float(np.float32(1.0 / math.sqrt(128))))
+        d = self.d
+        dev = torch.device("cuda")
+        self.nq = spc.spc_num_quantized(d)
+        self.Lcap = d.q_groups_cap * 32
+        self.records = [torch.empty(spc.spc_records_bytes(d), dtype=torch.uint8, device=dev) for _ in range(layers)]
+        self.resid = [torch.empty(spc.spc_resid_bytes(d) // 2, dtype=torch.int16, device=dev) for _ in range(layers)]
+        self.host = [torch.empty((B, Hkv, N, 2, 128), dtype=torch.int16, pin_memory=True) for _ in range(layers)]
+        Kt = torch.empty((B, Hkv, N, 128), dtype=torch.int16, device=dev)
+        Vt = torch.empty_like(Kt)
+        for l in range(layers):
+            synth.gpu.kv_layer_into(seed, l, Kt, Vt)
+            spc.spc_quantize_kv(d, Kt, Vt, self.records[l], self.resid[l])
+            self.host[l].copy_(torch.stack([Kt, Vt], dim=3), non_blocking=False)
+        del Kt, Vt
+        qn = np.stack([synth.queries(seed, l, B, Hq) for l in range(layers)])
+        self.q_host = torch.from_numpy(qn.view(np.int16).copy()).pin_memory()
+        self.q = self.q_host.to(dev)
+        self.o = torch.zeros((layers, B, 2, Hq, 128), dtype=torch.int16, device=dev)
+        self.o_host = torch.empty_like(self.o, device="cpu").pin_memory()
+        self.lse = torch.zeros((layers, B, 2, Hq), dtype=torch.float32, device=dev)
+        self.logits = torch.zeros((layers, B, Hkv, self.G, self.Lcap), dtype=torch.float32, device=dev)
+        self.idx = torch.zeros((layers, B, Hkv, k), dtype=torch.int32, device=dev)
+        self.bitmap = torch.zeros((layers, B, Hkv, d.q_groups_cap), dtype=torch.int32, device=dev)
+        self.staging = torch.zeros((layers, B, Hkv, k, 2, 128), dtype=torch.int16, device=dev)
+        self.ws_bytes = spc.spc_attn_workspace_bytes(d)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.main = torch.cuda.Stream()
+        self.side = torch.cuda.Stream(priority=-1)
+        self.attn_done = [torch.cuda.Event() for _ in range(layers)]
+        self.gathered = [torch.cuda.Event() for _ in range(layers)]
+        self.t0, self.rec = make_timing_event(torch)
+        self.attn_ev = [(make_timing_event(torch)[0], make_timing_event(torch)[0]) for _ in range(layers)]
+        # pre-decoding step: plain low-bit attention, first top-k and prefetch
+        with torch.cuda.stream(self.main):
+            for l in range(layers):
+                spc.spc_decode_attn2(d, self.records[l], self.resid[l], self.q[l], self.o[l], self.lse[l],
+                                     self.logits[l], self.ws, self.ws_bytes, stream=self.main)
+                spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l],
+                                    stream=self.main)
+                spc.spc_host_gather(d, self.host[l], N, self.idx[l], k, self.staging[l], stream=self.main)
+        torch.cuda.synchronize()
+        self.launches_per_step = layers * (3 + 2)  # low-bit scan, bf16 rows, combine, top-k, gather
+        self.graph = None
+
+    def enqueue(self, timed=False):
+        spc, d, k = self.spc, self.d, self.k
+        main, side = self.main, self.side
+        for l in range(self.L):
+            if timed:
+                self.rec(self.attn_ev[l][0], main)
+            spc.spc_merged_attn(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
+                                self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws, self.ws_bytes,
+                                stream=main)
+            if timed:
+                self.rec(self.attn_ev[l][1], main)
+            self.attn_done[l].record(main)
+            side.wait_event(self.attn_done[l])
+            spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=side)
+            spc.spc_host_gather(d, self.host[l], self.W["N"], self.idx[l], k, self.staging[l], stream=side)
+            self.gathered[l].record(side)
+        for l in range(self.L):
+            main.wait_event(self.gathered[l])
+
+    def capture(self):
+        torch = self.torch
+        self.main.wait_stream(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.main):
+            g.capture_begin(capture_error_mode="relaxed")
+            self.enqueue(timed=True)
+            g.capture_end()
+        self.graph = g
+        torch.cuda.synchronize()
+
+    def replay(self):
+        with self.torch.cuda.stream(self.main):
+            self.graph.replay()
+
+    def attn_ms(self):
+        return [s.elapsed_time(e) for (s, e) in self.attn_ev]
+
+
+def attention_bytes_per_layer(W, nq):
+    """Algorithmic HBM bytes of one merged-attention call (one layer)."""
+    beta = 64 if W["bits"] == 1 else 96
+    bh = W["B"] * W["Hkv"]
+    r = W["N"] - nq
+    qo = W["B"] * 2 * W["Hq"] * 128 * 2 * 2  # q read + o written
+    return bh * (nq * beta + r * 512 + W["k"] * 512) + qo
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+class OracleSample:
+    """The oracle's per-layer decode work (merged attention, top-k, gather) on
+    `pairs` (b, kv-head) pairs of one layer of the workload.  Inputs, the
+    quantisation and the first selection are prepared once; run() times the rest."""
+
+    def __init__(self, W, pairs, seed=0, layer=0):
+        import oracle
+        import synth
+        self.oracle = oracle
+        B, Hq, Hkv, N = W["B"], W["Hq"], W["Hkv"], W["N"]
+        G = Hq // Hkv
+        sel = [(p // Hkv, p % Hkv) for p in range(min(pairs, B * Hkv))]
+        qall = synth.queries(seed, layer, B, Hq)
+        Ks, Vs, qs = [], [], []
+        for (b, h) in sel:
+            kk, vv = synth.kv_slice(seed, layer, B, Hkv, N, 128, b, h)
+            Ks.append(kk)
+            Vs.append(vv)
+            qs.append(qall[b, :, h * G:(h + 1) * G])
+        self.P = len(sel)
+        self.K = np.stack(Ks)[:, None]  # the pairs as P sequences with one KV head each
+        self.V = np.stack(Vs)[:, None]
+        self.q = np.stack(qs)
+        self.d = oracle.dims(B=self.P, Hq=G, Hkv=1, N=N, R=W["R"], bits=W["bits"],
+                             scale=float(np.float32(1 / math.sqrt(128))))
+        self.qz = oracle.quantize(self.d, self.K, self.V)
+        _, _, S0 = oracle.attention(self.d, self.q, self.qz, self.K, self.V)
+        self.k = W["k"]
+        self.idx, _ = oracle.topk(self.d, S0, self.k)
+        self.host = np.stack([self.K, self.V], axis=3)
+        self.scale_to_step = (B * Hkv / self.P) * W["layers"]
+        self.threads = min(self.P, os.cpu_count() or 1)
+
+    def run(self):
+        o = self.oracle
+        t = time.perf_counter()
+        o.gather(self.d, self.host, self.idx)
+        _, _, S1 = o.attention(self.d, self.q, self.qz, self.K, self.V, idx=self.idx)
+        o.topk(self.d, S1, self.k)
+        return time.perf_counter() - t
+
+    def steps_per_s(self, seconds):
+        return 1.0 / (seconds * self.scale_to_step)
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    W = dict(WORKLOAD)
+    W["layers"] = args.layers
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        ref = OracleSample(W, args.cpu_pairs)
+        for _ in range(args.warmup):
+            ref.run()
+        secs = [ref.run() for _ in range(max(1, args.steps))]
+        v = ref.steps_per_s(statistics.median(secs))
+        sample = (f"per step: merged attention + top-k + gather of the CPU oracle on {ref.P} of "
+                  f"{W['B'] * W['Hkv']} (b, kv-head) pairs of one layer ({statistics.median(secs):.2f} s), "
+                  f"scaled x{W['B'] * W['Hkv'] // ref.P} pairs x {W['layers']} layers")
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": W["workload"]},
+                "cpu_baseline": {"value": v, "unit": "steps/s", "cores": ref.threads, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    peaks, peak_src = measured_peaks()
+
+    step = DecodeStep(W, args.layers)
+    step.capture()
+    for _ in range(max(3, args.warmup)):
+        step.replay()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region ----
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        start.record(step.main)
+        for _ in range(args.steps):
+            step.replay()
+        end.record(step.main)
+        barrier()
+    # the per-layer attention events inside the graph hold the last timed step
+    per_layer = step.attn_ms()
+    total_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1000.0)
+
+    # ---- end to end: queries in from pinned host memory, outputs back, every step ----
+    h2d = step.q_host.numel() * step.q_host.element_size()
+    d2h = step.o.numel() * step.o.element_size()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(step.main)
+    for _ in range(args.steps):
+        with torch.cuda.stream(step.main):
+            step.q.copy_(step.q_host, non_blocking=True)
+            step.graph.replay()
+            step.o_host.copy_(step.o, non_blocking=True)
+    e1.record(step.main)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    # ---- roofline of the dominant call (merged attention, one layer per launch) ----
+    bytes_layer = attention_bytes_per_layer(W, step.nq)
+    attn_avg_ms = statistics.mean(per_layer)
+    achieved = bytes_layer / (attn_avg_ms / 1000.0) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "kernel": "spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer",
+            "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,
+            "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+            "step_hbm_gbs": bytes_layer * W["layers"] / (ms_per_step / 1000.0) / 1e9}
+
+    line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16-mma/f32", "data": "synthetic",
+            "config": {"workload": W["workload"], "layers": W["layers"], "batch": W["B"], "context": W["N"],
+                       "bits": W["bits"], "k": W["k"], "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (4.3 GB low-bit cache per step, 129 MB L2); no flush",
+                       "graph": "one CUDA graph per step, main + side stream"},
+            "roofline": roof, "clocks": clk.summary(), "e2e": e2e,
+            "gpu_launches": step.launches_per_step * args.steps}
+    if rank == 0 and not args.no_cpu_baseline:
+        ref = OracleSample(W, args.cpu_pairs)
+        dt = ref.run()
+        line["cpu_baseline"] = {"value": ref.steps_per_s(dt), "unit": "steps/s", "cores": ref.threads,
+                                "kind": "oracle",
+                                "sample": f"merged attention + top-k + gather of {ref.P} (b, kv-head) pairs of one "
+                                          f"layer in {dt:.1f} s, scaled to {W['B'] * W['Hkv']} pairs x "
+                                          f"{W['layers']} layers"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

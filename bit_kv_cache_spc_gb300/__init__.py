@@ -1,0 +1,153 @@
+"""Python binding of libspc, the GB300 decode-time hot path of SpeCache.
+
+Every ``spc_*`` function here has the name and arguments of the C entry point
+in ``include/spc.h`` and only marshals arguments: torch tensors become device
+pointers, the stream defaults to torch's current stream, and a non-OK status
+raises ``SpcError``.  All computation runs in the CUDA kernels of
+``libspc.so``; there is no other implementation behind these names.  If the
+library has not been built the import fails: build it with
+``python -c "import __graft_entry__ as g; g.build()"``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+
+import torch
+
+__all__ = [
+    "Dims", "SpcError", "spc_abi_version", "spc_num_quantized", "spc_records_bytes", "spc_resid_bytes",
+    "spc_quantize_kv", "spc_attn_workspace_bytes", "spc_decode_attn2", "spc_merged_attn", "spc_topk_select",
+    "spc_host_gather", "lib_path",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "libspc.so")
+
+if not os.path.exists(lib_path):
+    raise ImportError(f"{lib_path} is missing: the CUDA library must be built (see __graft_entry__.build())")
+_lib = C.CDLL(lib_path)
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "CUDA error",
+          4: "host pointer is not mapped pinned memory", 5: "workspace too small"}
+
+
+class SpcError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = f"{fn}: {STATUS.get(status, status)}"
+        if status == 3:
+            msg += f" (cudaError {_lib.spc_last_cuda_error()})"
+        super().__init__(msg)
+
+
+class spc_dims(C.Structure):
+    _fields_ = [("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("D", C.c_int32),
+                ("bits", C.c_int32), ("group", C.c_int32), ("N", C.c_int32), ("R", C.c_int32),
+                ("q_groups_cap", C.c_int32), ("resid_cap", C.c_int32), ("scale", C.c_float)]
+
+
+def Dims(B, Hq, Hkv, N, R, bits, q_groups_cap=None, resid_cap=None, scale=None, D=128) -> spc_dims:
+    """Shape of one layer's cache (see spc_dims in include/spc.h)."""
+    nq = ((N - R) // 32) * 32 if N > R else 0
+    if q_groups_cap is None:
+        q_groups_cap = nq // 32
+    if resid_cap is None:
+        resid_cap = N - nq
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    return spc_dims(B, Hq, Hkv, D, bits, 32, N, R, q_groups_cap, resid_cap, scale)
+
+
+_P = C.c_void_p
+_D = C.POINTER(spc_dims)
+_sig = {
+    "spc_abi_version": (C.c_int32, []),
+    "spc_status_string": (C.c_char_p, [C.c_int]),
+    "spc_last_cuda_error": (C.c_int32, []),
+    "spc_num_quantized": (C.c_int32, [_D]),
+    "spc_records_bytes": (C.c_size_t, [_D]),
+    "spc_resid_bytes": (C.c_size_t, [_D]),
+    "spc_quantize_kv": (C.c_int, [_D, _P, _P, _P, _P, _P]),
+    "spc_attn_workspace_bytes": (C.c_size_t, [_D]),
+    "spc_decode_attn2": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "spc_merged_attn": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
+    "spc_topk_select": (C.c_int, [_D, _P, _P, C.c_int32, _P, _P, _P]),
+    "spc_host_gather": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, C.c_int32, _P]),
+}
+for _name, (_res, _args) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn, st):
+    if st != 0:
+        raise SpcError(fn, st)
+
+
+def spc_abi_version() -> int:
+    return int(_lib.spc_abi_version())
+
+
+def spc_num_quantized(d) -> int:
+    return int(_lib.spc_num_quantized(C.byref(d)))
+
+
+def spc_records_bytes(d) -> int:
+    return int(_lib.spc_records_bytes(C.byref(d)))
+
+
+def spc_resid_bytes(d) -> int:
+    return int(_lib.spc_resid_bytes(C.byref(d)))
+
+
+def spc_attn_workspace_bytes(d) -> int:
+    return int(_lib.spc_attn_workspace_bytes(C.byref(d)))
+
+
+def spc_quantize_kv(d, k, v, records, resid, stream=None):
+    _check("spc_quantize_kv", _lib.spc_quantize_kv(C.byref(d), _ptr(k), _ptr(v), _ptr(records), _ptr(resid),
+                                                   _stream(stream)))
+
+
+def spc_decode_attn2(d, records, resid, q, o, lse, spec_logits, ws, ws_bytes=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("spc_decode_attn2", _lib.spc_decode_attn2(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(o),
+                                                     _ptr(lse), _ptr(spec_logits), _ptr(ws), ws_bytes,
+                                                     _stream(stream)))
+
+
+def spc_merged_attn(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes=None,
+                    stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("spc_merged_attn", _lib.spc_merged_attn(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(idx),
+                                                   _ptr(bitmap), _ptr(staging), int(k), _ptr(o), _ptr(lse),
+                                                   _ptr(spec_logits), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def spc_topk_select(d, spec_logits, lse, k, idx, bitmap, stream=None):
+    _check("spc_topk_select", _lib.spc_topk_select(C.byref(d), _ptr(spec_logits), _ptr(lse), int(k), _ptr(idx),
+                                                   _ptr(bitmap), _stream(stream)))
+
+
+def spc_host_gather(d, host_kv, n_cap, idx, k, staging, max_ctas=0, stream=None):
+    _check("spc_host_gather", _lib.spc_host_gather(C.byref(d), _ptr(host_kv), int(n_cap), _ptr(idx), int(k),
+                                                   _ptr(staging), int(max_ctas), _stream(stream)))

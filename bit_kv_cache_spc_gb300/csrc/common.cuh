@@ -1,0 +1,101 @@
+// Shared device helpers of libspc (sm_103a).  Nothing here is method
+// arithmetic; the kernels in quantize.cu, attention.cu, topk.cu and gather.cu
+// carry the SpeCache steps.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spc.h"
+
+namespace spc {
+
+constexpr int kD = 128;       // head dimension handled by this build
+constexpr int kGroup = 32;    // tokens (keys) / channels (values) per quantisation group
+constexpr int kMaxRows = 8;   // 2 queries x G query heads per KV head, G <= 4
+
+__host__ __device__ inline int32_t num_quantized(int32_t N, int32_t R) {
+  return N > R ? ((N - R) / kGroup) * kGroup : 0;
+}
+
+__host__ __device__ inline int64_t record_bytes(int32_t bits) { return 1024 * (int64_t)(bits + 1); }
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// Round binary32 to bf16, nearest-even (finite inputs).
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte global->shared copy that bypasses L1 (cp.async.cg).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// D = A(16x16, f16, row) * B(16x8, f16, col) + C, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 values packed as f16x2 (x in the low half), round to nearest.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  float2 r;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(v));
+  return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+  return r;
+}
+
+}  // namespace spc
+
+// Host-side helpers shared by the entry points.
+namespace spc_host {
+
+void set_cuda_error(cudaError_t e);
+int sm_count();  // SMs of the current device (cached per device)
+bool aligned16(const void* p);
+int current_device();
+
+// Raises a kernel's dynamic shared-memory limit once per device (the attribute
+// is per context); later calls are free, so launches inside a stream capture
+// make no runtime configuration calls.  `done` holds one bit per device < 64
+// and must be a distinct static of the caller for every kernel.
+template <typename Kernel>
+cudaError_t ensure_smem_limit(unsigned long long& done, Kernel* fn, int bytes) {
+  const int dev = current_device();
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) __atomic_fetch_or(&done, bit, __ATOMIC_ACQ_REL);
+  return e;
+}
+
+}  // namespace spc_host

@@ -1,0 +1,194 @@
+// extern "C" entry points of libspc (declared in include/spc.h): argument
+// validation, then one launch sequence per call on the caller's stream.
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace spc {
+spc_status launch_quantize(const spc_dims*, const uint16_t*, const uint16_t*, void*, uint16_t*, cudaStream_t);
+size_t attn_workspace_bytes(const spc_dims*);
+spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const uint16_t*, const int32_t*,
+                            const uint32_t*, const uint16_t*, int32_t, uint16_t*, float*, float*, void*,
+                            cudaStream_t);
+spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t);
+spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
+                              int32_t, cudaStream_t);
+}  // namespace spc
+
+namespace spc_host {
+
+static thread_local int32_t g_last_cuda_error = 0;
+
+void set_cuda_error(cudaError_t e) { g_last_cuda_error = (int32_t)e; }
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+}  // namespace spc_host
+
+namespace {
+
+using spc_host::aligned16;
+
+// Shape checks shared by every call.
+spc_status check_dims(const spc_dims* d) {
+  if (d == nullptr) return SPC_ERR_INVALID;
+  if (d->B <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->D <= 0 || d->N < 0 || d->R < 0 || d->q_groups_cap < 0 ||
+      d->resid_cap < 0)
+    return SPC_ERR_INVALID;
+  if (d->Hq % d->Hkv != 0) return SPC_ERR_INVALID;
+  if (d->bits != 1 && d->bits != 2) return SPC_ERR_INVALID;
+  if (!(std::isfinite(d->scale) && d->scale > 0.f)) return SPC_ERR_INVALID;
+  const int G = d->Hq / d->Hkv;
+  if (d->D != spc::kD || d->group != spc::kGroup) return SPC_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4) return SPC_ERR_UNSUPPORTED;
+  const int32_t nq = spc::num_quantized(d->N, d->R);
+  if (nq / spc::kGroup > d->q_groups_cap) return SPC_ERR_INVALID;
+  if (d->N - nq > d->resid_cap) return SPC_ERR_INVALID;
+  return SPC_OK;
+}
+
+spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                       const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                       uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
+                       spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  const int32_t nq = spc::num_quantized(d->N, d->R);
+  if (q == nullptr || o == nullptr || ws == nullptr) return SPC_ERR_INVALID;
+  if (nq > 0 && records == nullptr) return SPC_ERR_INVALID;
+  if (d->N - nq > 0 && resid == nullptr) return SPC_ERR_INVALID;
+  if (!aligned16(records) || !aligned16(resid) || !aligned16(q) || !aligned16(o) || !aligned16(ws) ||
+      !aligned16(lse) || !aligned16(spec_logits))
+    return SPC_ERR_INVALID;
+  if (k < 0) return SPC_ERR_INVALID;
+  if (k > 0) {
+    if (idx == nullptr || bitmap == nullptr || staging == nullptr || !aligned16(staging)) return SPC_ERR_INVALID;
+    if ((int64_t)k > (int64_t)d->q_groups_cap * spc::kGroup) return SPC_ERR_INVALID;
+  }
+  if (ws_bytes < spc::attn_workspace_bytes(d)) return SPC_ERR_WORKSPACE;
+  return spc::launch_attention(d, records, resid, q, k > 0 ? idx : nullptr, k > 0 ? bitmap : nullptr,
+                               k > 0 ? staging : nullptr, k, o, lse, spec_logits, ws,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t spc_abi_version(void) { return SPC_ABI_VERSION; }
+
+const char* spc_status_string(spc_status s) {
+  switch (s) {
+    case SPC_OK: return "ok";
+    case SPC_ERR_INVALID: return "invalid argument";
+    case SPC_ERR_UNSUPPORTED: return "unsupported shape";
+    case SPC_ERR_CUDA: return "CUDA error";
+    case SPC_ERR_NOT_MAPPED: return "host pointer is not mapped pinned memory";
+    case SPC_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+int32_t spc_last_cuda_error(void) { return spc_host::g_last_cuda_error; }
+
+int32_t spc_num_quantized(const spc_dims* d) {
+  if (check_dims(d) == SPC_ERR_INVALID) return -1;
+  return spc::num_quantized(d->N, d->R);
+}
+
+size_t spc_records_bytes(const spc_dims* d) {
+  if (d == nullptr || d->B <= 0 || d->Hkv <= 0 || d->q_groups_cap < 0 || (d->bits != 1 && d->bits != 2)) return 0;
+  return (size_t)d->B * d->Hkv * d->q_groups_cap * (size_t)spc::record_bytes(d->bits);
+}
+
+size_t spc_resid_bytes(const spc_dims* d) {
+  if (d == nullptr || d->B <= 0 || d->Hkv <= 0 || d->resid_cap < 0 || d->D <= 0) return 0;
+  return (size_t)d->B * d->Hkv * d->resid_cap * 2 * d->D * sizeof(uint16_t);
+}
+
+spc_status spc_quantize_kv(const spc_dims* d, const uint16_t* k, const uint16_t* v, void* records,
+                           uint16_t* resid, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  const int32_t nq = spc::num_quantized(d->N, d->R);
+  if (d->N > 0 && (k == nullptr || v == nullptr)) return SPC_ERR_INVALID;
+  if (nq > 0 && records == nullptr) return SPC_ERR_INVALID;
+  if (d->N - nq > 0 && resid == nullptr) return SPC_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(records) || !aligned16(resid)) return SPC_ERR_INVALID;
+  return spc::launch_quantize(d, k, v, records, resid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t spc_attn_workspace_bytes(const spc_dims* d) {
+  if (check_dims(d) != SPC_OK) return 0;
+  return spc::attn_workspace_bytes(d);
+}
+
+spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                            uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
+                            spc_stream stream) {
+  return attn_common(d, records, resid, q, nullptr, nullptr, nullptr, 0, o, lse, spec_logits, ws, ws_bytes,
+                     stream);
+}
+
+spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                           const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                           uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
+                           spc_stream stream) {
+  return attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream);
+}
+
+spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse, int32_t k,
+                           int32_t* idx, uint32_t* bitmap, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  const int32_t nq = spc::num_quantized(d->N, d->R);
+  if (k < 0 || (int64_t)k > (int64_t)d->q_groups_cap * spc::kGroup) return SPC_ERR_INVALID;
+  if (bitmap == nullptr || (k > 0 && idx == nullptr)) return SPC_ERR_INVALID;
+  if (nq > 0 && (spec_logits == nullptr || lse == nullptr)) return SPC_ERR_INVALID;
+  if (nq > 262144) return SPC_ERR_UNSUPPORTED;
+  if (d->q_groups_cap == 0 && k == 0) return SPC_OK;
+  return spc::launch_topk(d, spec_logits, lse, k, idx, bitmap, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spc_status spc_host_gather(const spc_dims* d, const uint16_t* host_kv, int64_t n_cap, const int32_t* idx,
+                           int32_t k, uint16_t* staging, int32_t max_ctas, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  if (k < 0 || n_cap < 0 || max_ctas < 0) return SPC_ERR_INVALID;
+  if (k == 0) return SPC_OK;
+  if (host_kv == nullptr || idx == nullptr || staging == nullptr) return SPC_ERR_INVALID;
+  if (!aligned16(host_kv) || !aligned16(staging)) return SPC_ERR_INVALID;
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, host_kv);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of the query
+    return SPC_ERR_NOT_MAPPED;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return SPC_ERR_NOT_MAPPED;
+  return spc::launch_host_gather(d, static_cast<const uint16_t*>(attr.devicePointer), n_cap, idx, k, staging,
+                                 max_ctas, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

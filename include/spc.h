@@ -1,0 +1,188 @@
+/*
+ * spc.h -- C ABI of libspc, the GB300 (sm_103a) decode-time hot path of
+ * SpeCache ("SpeCache: Speculative Key-Value Caching for Efficient Generation
+ * of LLMs", arXiv 2503.16163).
+ *
+ * The library implements the per-layer primitives the page's Algorithms 1-3
+ * name: Quant (section 3), Attn over [T_t, T'_{t+1}] with C' U C_kappa
+ * (section 3 "Decoding", Algorithm 3), ArgTopK over the speculative token's
+ * attention row (Algorithm 3; Algorithm 2 for the pre-decoding step) and
+ * Pre-fetch of the selected 16-bit rows from CPU memory (Algorithm 3).
+ *
+ * Conventions for every call:
+ *   - Pointers are device pointers unless stated otherwise; bf16 values are
+ *     passed as their 16-bit patterns (uint16_t).  All tensors are dense,
+ *     row-major, and 16-byte aligned.
+ *   - The caller owns and allocates every buffer.  The library never
+ *     allocates, frees or synchronises; each call enqueues its kernels on the
+ *     given stream (NULL = the legacy default stream) and returns.
+ *   - Calls are stateless and may be made from several host threads.
+ *   - Argument errors return SPC_ERR_INVALID / SPC_ERR_UNSUPPORTED before
+ *     anything is launched; a failed launch returns SPC_ERR_CUDA (the CUDA
+ *     error is left for cudaGetLastError / spc_last_cuda_error).
+ */
+#ifndef SPC_H
+#define SPC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPC_ABI_VERSION 1
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* spc_stream;
+
+typedef enum spc_status {
+  SPC_OK = 0,
+  SPC_ERR_INVALID = 1,     /* bad argument (null pointer, size, alignment) */
+  SPC_ERR_UNSUPPORTED = 2, /* valid shape this build does not handle */
+  SPC_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  SPC_ERR_NOT_MAPPED = 4,  /* host pointer is not device-mapped pinned memory */
+  SPC_ERR_WORKSPACE = 5    /* workspace smaller than the size query returns */
+} spc_status;
+
+/*
+ * Shape of one layer's cache.  D must be 128 and group 32 (the page's group
+ * size g = 32, section 4).  G = Hq / Hkv query heads share a KV head; this
+ * build handles G in {1, 2, 4}.
+ * The quantised prefix has N_q = floor(max(N - R, 0) / 32) * 32 tokens and
+ * the residual window the last r = N - N_q tokens (KIVI keeps the most recent
+ * tokens in 16 bits; page 1 section 4).  Capacities bound the buffers:
+ * N_q / 32 <= q_groups_cap and r <= resid_cap.
+ */
+typedef struct spc_dims {
+  int32_t B, Hq, Hkv, D;
+  int32_t bits;         /* 1 or 2 */
+  int32_t group;        /* 32 */
+  int32_t N;            /* visible tokens of this layer */
+  int32_t R;            /* residual window target */
+  int32_t q_groups_cap; /* 32-token groups the record array can hold per (b,hkv) */
+  int32_t resid_cap;    /* residual rows the residual buffer can hold per (b,hkv) */
+  float scale;          /* softmax scale applied to q.k, e.g. 1/sqrt(128) */
+} spc_dims;
+
+int32_t spc_abi_version(void);
+const char* spc_status_string(spc_status s);
+/* The cudaError_t of the last SPC_ERR_CUDA on this host thread (0 if none). */
+int32_t spc_last_cuda_error(void);
+
+/* N_q of the shape (see spc_dims).  Returns -1 for an invalid shape. */
+int32_t spc_num_quantized(const spc_dims* d);
+
+/*
+ * Low-bit copy C' of one layer ("records").  Per (b, hkv) there are
+ * q_groups_cap records of 1024*(bits+1) bytes; record g holds tokens
+ * 32g .. 32g+31.  Bytes spc_records_bytes(d) in all, row-major
+ * [B][Hkv][q_groups_cap][1024*(bits+1)].  A record is, in order:
+ *   K codes  : `bits` planes of 128 u32 words (plane p holds bit p of each code)
+ *   K minmax : 128 u32 words, min in bits 0..15 and max in bits 16..31 (bf16)
+ *   V codes  : `bits` planes of 128 u32 words
+ *   V minmax : 128 u32 words
+ * With L = 4a + t (a in 0..7, t in 0..3), j in 0..3 and bit b in 0..31:
+ *   K code word 4L+j, bit b : token 8j + a,
+ *                             channel 16*((b&15)>>1) + 2t + 8*(b&1) + (b>>4)
+ *   K minmax word 32t+m     : channel 16*(m>>2) + 2t + 8*((m>>1)&1) + (m&1)
+ *   V code word 4L+j, bit b : token 16*(j>>1) + 8*(j&1) + 2t + (b>>4),
+ *                             channel 16*((b&15)>>1) + 8*(b&1) + a
+ *   V minmax word 32t+m     : token 16*(m>>4) + 8*((m>>3)&1) + 2t + ((m>>2)&1),
+ *                             channel group m&3
+ * Keys are grouped per channel over the 32 tokens of a record, values per
+ * token over 32 consecutive channels (KIVI's axes).  min/max are the group's
+ * exact bf16 extremes (-0.0 stored as +0.0); the zero point and scale are
+ * derived from them (page 1 section 3): 1-bit z = (3min+max)/4, s = (max-min)/2;
+ * 2-bit z = min, s = (max-min)/3.  This is 64 (1-bit) or 96 (2-bit) bytes per
+ * token and KV head, 1/8 or 3/16 of bf16.
+ */
+size_t spc_records_bytes(const spc_dims* d);
+
+/* Residual window: bf16 [B][Hkv][resid_cap][2][D]; row j holds the key then
+ * the value of token N_q + j.  The same [.., 2, D] row format is used for the
+ * full 16-bit host cache and for the staging buffer of fetched rows. */
+size_t spc_resid_bytes(const spc_dims* d);
+
+/*
+ * Quant (page 1 section 3; Algorithm 1, K' = Quant(K), V' = Quant(V)).
+ * k, v: bf16 [B][Hkv][N][D] (device).  Writes records 0 .. N_q/32-1 of every
+ * (b,hkv) and residual rows 0 .. r-1.  Codes are
+ *   clamp(rint((x - z) / s), 0, 2^bits - 1), code 0 when s == 0,
+ * with z, s and (x - z) / s evaluated in IEEE binary32, round to nearest even,
+ * without fused multiply-add.
+ */
+spc_status spc_quantize_kv(const spc_dims* d, const uint16_t* k, const uint16_t* v,
+                           void* records, uint16_t* resid, spc_stream stream);
+
+/* Bytes of device workspace spc_decode_attn2 / spc_merged_attn need for this
+ * shape on the current device (split-K partials). */
+size_t spc_attn_workspace_bytes(const spc_dims* d);
+
+/*
+ * Attn([T_t, T'_{t+1}], C') -- the two-query decode attention over the
+ * low-bit copy (page 1 section 3 "Decoding"; with no fetched rows this is also
+ * the pre-decoding attention of Algorithm 2).
+ *   q     : bf16 [B][2][Hq][D]; row 0 is the output token T_t, row 1 the
+ *           speculative token T'_{t+1}.  Query head h uses KV head h / G.
+ *   o     : bf16 [B][2][Hq][D], softmax(scale * q.K^T) V over all N tokens,
+ *           keys/values dequantised from C' for n < N_q, residual rows after.
+ *   lse   : fp32 [B][2][Hq] or NULL, natural log of the softmax normaliser.
+ *   spec_logits : fp32 [B][Hkv][G][q_groups_cap*32] or NULL: the speculative
+ *           token's scaled logits scale*q.k at the quantised positions, the
+ *           input of spc_topk_select.
+ *   ws    : device workspace of at least spc_attn_workspace_bytes(d) bytes.
+ */
+spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16_t* resid,
+                            const uint16_t* q, uint16_t* o, float* lse, float* spec_logits,
+                            void* ws, size_t ws_bytes, spc_stream stream);
+
+/*
+ * Attn([T_t, T'_{t+1}], C' U C_kappa) (page 1 section 3 "Decoding",
+ * Algorithm 3): as spc_decode_attn2, but at the k positions idx[b][hkv][0..k-1]
+ * (ascending, < N_q, -1 entries ignored) both the key and the value are the
+ * fetched 16-bit rows staging[b][hkv][j] (bf16 [B][Hkv][k][2][D]) instead of
+ * the low-bit rows.  bitmap (u32 [B][Hkv][q_groups_cap], bit n%32 of word
+ * n/32) must mark exactly the listed positions.  spec_logits at a fetched
+ * position holds the logit of the fetched row.  k = 0 is spc_decode_attn2.
+ */
+spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_t* resid,
+                           const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
+                           const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
+                           float* spec_logits, void* ws, size_t ws_bytes, spc_stream stream);
+
+/*
+ * ArgTopK(A_{1,:}) (Algorithm 3): per (b, hkv), the k_eff = min(k, N_q)
+ * quantised positions n with the largest score
+ *   S(n) = sum over the G query heads h of KV head hkv of
+ *          exp(spec_logits[b][hkv][h%G][n] - lse[b][1][h]),
+ * i.e. the speculative token's attention probability summed over the group.
+ * Ties go to the lower position.  Outputs: idx int32 [B][Hkv][k], ascending,
+ * entries k_eff..k-1 set to -1; bitmap u32 [B][Hkv][q_groups_cap] with
+ * exactly the selected bits set (words past N_q/32 are zeroed).
+ * k <= 32 * q_groups_cap; N_q <= 262144.
+ */
+spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse,
+                           int32_t k, int32_t* idx, uint32_t* bitmap, spc_stream stream);
+
+/*
+ * Pre-fetch(C_kappa) (Algorithm 3): copies the selected 16-bit rows from the
+ * full-precision cache in CPU memory into HBM,
+ *   staging[b][hkv][j][t][:] = host_kv[b][hkv][idx[b][hkv][j]][t][:], t in {K, V},
+ * for j < k with idx >= 0 (other staging rows are left untouched).
+ *   host_kv : HOST pointer, bf16 [B][Hkv][n_cap][2][D], pinned and mapped
+ *             into the device address space (cudaHostAlloc / cudaHostRegister
+ *             with mapping); otherwise SPC_ERR_NOT_MAPPED.
+ *   max_ctas: bound on the copy kernel's grid (0 = library default), so the
+ *             copy can share the GPU with attention running on another stream.
+ * Indices must be < n_cap.  The copy is issued on `stream`, typically a side
+ * stream ordered after spc_topk_select by an event.
+ */
+spc_status spc_host_gather(const spc_dims* d, const uint16_t* host_kv, int64_t n_cap,
+                           const int32_t* idx, int32_t k, uint16_t* staging, int32_t max_ctas,
+                           spc_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPC_H */

@@ -1,0 +1,69 @@
+"""The C-ABI library loads and exports every entry point its header declares.
+Only host-side calls are made here (no GPU in this environment)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spc.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spc_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def spc():
+    import bit_kv_cache_spc_gb300 as m
+    return m
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for fn in ("spc_quantize_kv", "spc_decode_attn2", "spc_topk_select", "spc_host_gather", "spc_merged_attn"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(spc):
+    lib = C.CDLL(spc.lib_path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_side_queries(spc):
+    assert spc.spc_abi_version() == 1
+    d = spc.Dims(1, 32, 8, 32768, 128, 1)
+    assert spc.spc_num_quantized(d) == 32640
+    assert spc.spc_records_bytes(d) == 8 * 1020 * 2048
+    assert spc.spc_resid_bytes(d) == 8 * 128 * 2 * 128 * 2
+    d2 = spc.Dims(16, 32, 32, 2048, 128, 2)
+    assert spc.spc_records_bytes(d2) == 16 * 32 * 60 * 3072  # 96 B per token and KV head
+    bad = spc.Dims(1, 32, 8, 1024, 32, 3)
+    assert spc.spc_num_quantized(bad) == -1
+
+
+def test_validation_happens_before_any_launch(spc):
+    """Argument errors come back as status codes; nothing reaches the GPU."""
+    bad_bits = spc.Dims(1, 32, 8, 1024, 32, 3)
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_quantize_kv(bad_bits, 16, 16, 16, 16, stream=0)
+    assert e.value.status == 1
+    g8 = spc.Dims(1, 64, 8, 1024, 32, 1)
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_topk_select(g8, 16, 16, 4, 16, 16, stream=0)
+    assert e.value.status == 2
+    d = spc.Dims(1, 32, 8, 1024, 32, 1)
+    with pytest.raises(spc.SpcError) as e:  # misaligned query pointer
+        spc.spc_decode_attn2(d, 16, 16, 18, 16, None, None, 16, 1 << 30, stream=0)
+    assert e.value.status == 1
+    small_cap = spc.Dims(1, 32, 8, 1024, 32, 1, q_groups_cap=3)
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_quantize_kv(small_cap, 16, 16, 16, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # negative k
+        spc.spc_topk_select(d, 16, 16, -1, 16, 16, stream=0)
+    assert e.value.status == 1

@@ -1,0 +1,266 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small shapes are compared element by element; the full-size configurations
+are compared on sampled (batch, KV head) pairs, which the oracle computes as
+independent 1 x 1 sub-problems on the same seeded inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from spc_cases import (CONFIGS, OUT_TOL, GpuLayer, b2f, bitmap_from_idx, c5_cases, check_topk_sets, odims,
+                       oracle_pair)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    dict(B=1, Hq=1, Hkv=1, N=1024, R=32, bits=1, k=16),        # configuration 1
+    dict(B=2, Hq=8, Hkv=2, N=1000, R=40, bits=1, k=33),        # ragged: N_q = 960, r = 40
+    dict(B=2, Hq=4, Hkv=2, N=2080, R=128, bits=2, k=20),       # G = 2, 2-bit
+    dict(B=1, Hq=4, Hkv=4, N=300, R=64, bits=2, k=7),          # MHA, 2-bit, r = 44
+    dict(B=1, Hq=4, Hkv=1, N=96, R=32, bits=1, k=200),         # k > N_q (padding), tiny
+    dict(B=1, Hq=4, Hkv=1, N=40, R=64, bits=1, k=4),           # N < R: no quantised tokens
+]
+
+
+def small_id(c):
+    return f"B{c['B']}_Hq{c['Hq']}_Hkv{c['Hkv']}_N{c['N']}_R{c['R']}_b{c['bits']}_k{c['k']}"
+
+
+def run_small(cfg, seed=1):
+    K, V = synth.kv_layer(seed, 0, cfg["B"], cfg["Hkv"], cfg["N"])
+    q = synth.queries(seed, 0, cfg["B"], cfg["Hq"])
+    g = GpuLayer(cfg, K=K, V=V, q=q)
+    d = odims(cfg)
+    qz = oracle.quantize(d, K, V)
+    return g, d, K, V, q, qz
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=small_id)
+def test_small_full_pipeline(cfg):
+    g, d, K, V, q, qz = run_small(cfg)
+    nq = oracle.nq(d)
+    assert g.nq == nq
+    # Quant: packed codes, min/max and residual rows bit-exact
+    rec, res = oracle.pack(d, qz, K, V)
+    torch.cuda.synchronize()
+    got_rec = g.records.cpu().numpy()[:rec.size]
+    assert np.array_equal(got_rec, rec.reshape(-1))
+    r = cfg["N"] - nq
+    got_res = g.resid.cpu().numpy().view(np.uint16).reshape(cfg["B"], cfg["Hkv"], -1, 2, 128)[:, :, :r]
+    assert np.array_equal(got_res, res[:, :, :r])
+
+    # Attn over C' (k = 0)
+    o, lse, lg = g.attn2()
+    oo, lo, So = oracle.attention(d, q, qz, K, V)
+    got = b2f(o.cpu().numpy())
+    assert np.abs(got - oo).max() <= OUT_TOL
+    np.testing.assert_allclose(lse.cpu().numpy(), lo, rtol=0, atol=1e-4)
+
+    # ArgTopK over the speculative row
+    k = cfg["k"]
+    idx, bm = g.topk(lg, lse, k)
+    io, bo = oracle.topk(d, So, k)
+    idx_np = idx.cpu().numpy()
+    bm_np = bm.cpu().numpy().view(np.uint32)
+    for b in range(cfg["B"]):
+        for h in range(cfg["Hkv"]):
+            check_topk_sets(idx_np[b, h], io[b, h], So[b, h], k)
+            assert np.array_equal(bm_np[b, h], bitmap_from_idx(idx_np[b, h], d_words(g)))
+
+    # Pre-fetch of the oracle's selection, then Attn over C' U C_kappa
+    idx_o = torch.from_numpy(io).cuda()
+    bm_o = torch.from_numpy(bo.view(np.int32)).cuda()
+    bm_full = torch.zeros((cfg["B"], cfg["Hkv"], max(g.d.q_groups_cap, 1)), dtype=torch.int32, device="cuda")
+    bm_full[..., :bm_o.shape[-1]] = bm_o
+    if k > 0 and nq > 0:
+        g.gather(idx_o, k)
+        st = oracle.gather(d, np.stack([K, V], axis=3), io)
+        torch.cuda.synchronize()
+        assert np.array_equal(g.staging.cpu().numpy().view(np.uint16)[:, :, :k], st)
+        o1, lse1, lg1 = g.merged(idx_o, bm_full, k)
+        oo1, lo1, So1 = oracle.attention(d, q, qz, K, V, idx=io)
+        assert np.abs(b2f(o1.cpu().numpy()) - oo1).max() <= OUT_TOL
+        np.testing.assert_allclose(lse1.cpu().numpy(), lo1, rtol=0, atol=1e-4)
+        idx2, _ = g.topk(lg1, lse1, k)
+        io2, _ = oracle.topk(d, So1, k)
+        idx2_np = idx2.cpu().numpy()
+        for b in range(cfg["B"]):
+            for h in range(cfg["Hkv"]):
+                check_topk_sets(idx2_np[b, h], io2[b, h], So1[b, h], k)
+
+
+def d_words(g):
+    return g.d.q_groups_cap
+
+
+def test_k0_merged_is_attn2_and_all_fetched_is_bf16_attention():
+    cfg = dict(B=1, Hq=4, Hkv=1, N=512, R=64, bits=1, k=448)
+    g, d, K, V, q, qz = run_small(cfg, seed=3)
+    o0, lse0, lg0 = g.attn2()
+    empty_idx = torch.zeros((1, 1, 1), dtype=torch.int32, device="cuda")
+    bm0 = torch.zeros((1, 1, g.d.q_groups_cap), dtype=torch.int32, device="cuda")
+    o1, lse1, lg1 = g.merged(empty_idx, bm0, 0)
+    assert torch.equal(o0, o1) and torch.equal(lse0, lse1)
+    # every quantised position fetched: plain bf16 attention (oracle and library routine)
+    nq = g.nq
+    idx = torch.arange(nq, dtype=torch.int32, device="cuda").view(1, 1, nq)
+    bm = torch.full((1, 1, g.d.q_groups_cap), -1, dtype=torch.int32, device="cuda")
+    g.gather(idx, nq)
+    o2, lse2, _ = g.merged(idx, bm, nq)
+    oo, lo, _ = oracle.attention(d, q, qz, K, V, idx=idx.cpu().numpy())
+    assert np.abs(b2f(o2.cpu().numpy()) - oo).max() <= OUT_TOL
+    qf = torch.from_numpy(b2f(q)).permute(0, 2, 1, 3)
+    Kf = torch.from_numpy(b2f(K)).repeat_interleave(4, dim=1)
+    Vf = torch.from_numpy(b2f(V)).repeat_interleave(4, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qf, Kf, Vf, scale=d.scale).permute(0, 2, 1, 3)
+    assert np.abs(b2f(o2.cpu().numpy()) - ref.numpy()).max() <= OUT_TOL
+
+
+def test_topk_selection_exact_with_ties_across_cluster():
+    """Selection alone, on logits whose order is unambiguous in fp32 (spacing
+    0.01 in the exponent), with many exact ties, over rows spanning 1..8 CTAs."""
+    import bit_kv_cache_spc_gb300 as spc
+    rng = np.random.default_rng(0)
+    for N, k in [(4224, 41), (40128, 401), (130944 + 128, 1311), (65536 + 128, 5000)]:
+        d = spc.Dims(2, 2, 2, N, 128, 1)
+        nq = spc.spc_num_quantized(d)
+        lg = (rng.integers(0, 300, size=(2, 2, 1, nq)) * 0.01).astype(np.float32)
+        lse = np.full((2, 2, 2), 3.0, np.float32)
+        idx = torch.full((2, 2, k), -7, dtype=torch.int32, device="cuda")
+        bm = torch.zeros((2, 2, d.q_groups_cap), dtype=torch.int32, device="cuda")
+        spc.spc_topk_select(d, torch.from_numpy(lg).cuda(), torch.from_numpy(lse).cuda(), k, idx, bm)
+        got = idx.cpu().numpy()
+        for b in range(2):
+            for h in range(2):
+                order = np.lexsort((np.arange(nq), -lg[b, h, 0].astype(np.float64)))
+                want = np.sort(order[:k])
+                assert np.array_equal(got[b, h], want)
+                assert np.array_equal(bm.cpu().numpy().view(np.uint32)[b, h], bitmap_from_idx(want, d.q_groups_cap))
+
+
+def test_gather_exact_and_unmapped_pointer_refused():
+    import bit_kv_cache_spc_gb300 as spc
+    rng = np.random.default_rng(1)
+    B, Hkv, ncap, k = 2, 3, 1000, 57
+    d = spc.Dims(B, Hkv, Hkv, ncap, 128, 1)
+    host_np = rng.integers(0, 1 << 16, size=(B, Hkv, ncap, 2, 128), dtype=np.uint16)
+    host = torch.from_numpy(host_np.view(np.int16)).pin_memory()
+    idx_np = np.sort(rng.choice(ncap, size=(B, Hkv, k)), axis=-1).astype(np.int32)
+    idx_np[1, 2, 5] = -1
+    idx = torch.from_numpy(idx_np).cuda()
+    st = torch.zeros((B, Hkv, k, 2, 128), dtype=torch.int16, device="cuda")
+    for max_ctas in (0, 1, 3):
+        st.zero_()
+        spc.spc_host_gather(d, host, ncap, idx, k, st, max_ctas)
+        got = st.cpu().numpy().view(np.uint16)
+        want = oracle.gather(oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=ncap, R=128, bits=1), host_np, idx_np)
+        assert np.array_equal(got, want)
+    unpinned = np.zeros((B, Hkv, ncap, 2, 128), np.uint16)
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_host_gather(d, unpinned.ctypes.data, ncap, idx, k, st)
+    assert e.value.status == 4
+
+
+def test_invalid_arguments_are_refused_before_launch():
+    import bit_kv_cache_spc_gb300 as spc
+    d = spc.Dims(1, 32, 8, 1024, 32, 1)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    q = torch.zeros((1, 2, 32, 128), dtype=torch.int16, device="cuda")
+    o = torch.zeros_like(q)
+    rec = torch.zeros(spc.spc_records_bytes(d), dtype=torch.uint8, device="cuda")
+    res = torch.zeros(spc.spc_resid_bytes(d) // 2, dtype=torch.int16, device="cuda")
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_decode_attn2(d, rec, res, q, o, None, None, ws)
+    assert e.value.status == 5  # workspace too small
+    bad = spc.Dims(1, 32, 8, 1024, 32, 3)
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_quantize_kv(bad, q, q, rec, res)
+    assert e.value.status == 1
+    g8 = spc.Dims(1, 64, 8, 1024, 32, 1)
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_quantize_kv(g8, q, q, rec, res)
+    assert e.value.status == 2
+
+
+def test_synth_gpu_twin_is_bit_identical():
+    import synth.gpu
+    for (B, Hkv, N) in [(2, 3, 160), (1, 8, 4096)]:
+        Kt = torch.empty((B, Hkv, N, 128), dtype=torch.int16, device="cuda")
+        Vt = torch.empty_like(Kt)
+        synth.gpu.kv_layer_into(5, 2, Kt, Vt)
+        K, V = synth.kv_layer(5, 2, B, Hkv, N)
+        assert np.array_equal(Kt.cpu().numpy().view(np.uint16), K)
+        assert np.array_equal(Vt.cpu().numpy().view(np.uint16), V)
+
+
+# ---------------------------------------------------------------- full size
+
+def full_size_check(cfg, pairs, layer=0, check_records=True):
+    """GPU pipeline over the whole configuration; oracle on sampled pairs."""
+    g = GpuLayer(cfg, layer=layer)
+    torch.cuda.synchronize()
+    o, lse, lg = g.attn2()
+    k = cfg["k"]
+    idx, bm = g.topk(lg, lse, k)
+    g.gather(idx, k)
+    o1, lse1, lg1 = g.merged(idx, bm, k)
+    idx2, _ = g.topk(lg1, lse1, k)
+    torch.cuda.synchronize()
+    G = cfg["Hq"] // cfg["Hkv"]
+    rb = oracle.record_bytes(cfg["bits"])
+    ng = g.nq // 32
+    rec_all = g.records.cpu().numpy() if check_records else None
+    o_np, o1_np = b2f(o.cpu().numpy()), b2f(o1.cpu().numpy())
+    idx_np, idx2_np = idx.cpu().numpy(), idx2.cpu().numpy()
+    lse_np = lse.cpu().numpy()
+    worst = 0.0
+    for (b, hk) in pairs:
+        ref = oracle_pair(cfg, b, hk, layer=layer)
+        if check_records:
+            rec, _ = oracle.pack(ref["d"], ref["qz"], ref["K"], ref["V"])
+            bh = b * cfg["Hkv"] + hk
+            assert np.array_equal(rec_all[bh * ng * rb:(bh + 1) * ng * rb], rec.reshape(-1))
+        hs = slice(hk * G, (hk + 1) * G)
+        err = np.abs(o_np[b, :, hs] - ref["o"]).max()
+        worst = max(worst, err)
+        assert err <= OUT_TOL
+        np.testing.assert_allclose(lse_np[b, :, hs], ref["lse"], rtol=0, atol=1e-4)
+        io, _ = oracle.topk(ref["d"], ref["S"][None, None], k)
+        check_topk_sets(idx_np[b, hk], io[0, 0], ref["S"], k)
+        # merged step with the oracle's own selection
+        ref1 = oracle_pair(cfg, b, hk, layer=layer, idx=io[0, 0])
+        # the GPU used its own selection; identical except for boundary swaps
+        same = np.array_equal(idx_np[b, hk], io[0, 0])
+        tol = OUT_TOL if same else 2 * OUT_TOL
+        assert np.abs(o1_np[b, :, hs] - ref1["o"]).max() <= tol
+        io2, _ = oracle.topk(ref1["d"], ref1["S"][None, None], k)
+        if same:
+            check_topk_sets(idx2_np[b, hk], io2[0, 0], ref1["S"], k)
+    return worst
+
+
+def test_config2_full_size():
+    cfg = CONFIGS["c2"]
+    full_size_check(cfg, [(0, h) for h in range(8)])
+
+
+def test_config3_full_size_sampled():
+    cfg = CONFIGS["c3"]
+    full_size_check(cfg, [(0, 0), (5, 17), (15, 31), (9, 3)])
+
+
+def test_config4_one_layer_sampled():
+    cfg = dict(CONFIGS["c4"])
+    full_size_check(cfg, [(0, 0), (3, 5), (7, 7)], layer=17)
+
+
+@pytest.mark.parametrize("case", [c for c in c5_cases() if c["N"] in (4096, 131072) and
+                                  abs(c["k"] - math.ceil(0.01 * c["N"])) <= 1],
+                         ids=lambda c: f"B{c['B']}_N{c['N']}_b{c['bits']}_k{c['k']}")
+def test_config5_sweep_sampled(case):
+    full_size_check(case, [(case["B"] - 1, 7), (0, 2)], check_records=case["N"] <= 4096)
