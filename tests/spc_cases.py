@@ -24,6 +24,21 @@ OUT_TOL = 2e-3     # max-abs on bf16 outputs against the fp64 oracle
 TOPK_REL = 1e-5    # boundary band for top-k set differences
 
 
+def bf16_half_ulp(x) -> np.ndarray:
+    """Half a bf16 unit in the last place at |x| (bf16 keeps 8 significant bits)."""
+    ax = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return 0.5 * np.power(2.0, e - 7)
+
+
+def out_err(got_bf16_as_f64, ref) -> float:
+    """Error of a bf16 output against the fp64 oracle beyond the output format's
+    own rounding: max(|got - ref| - half_ulp_bf16(ref)).  The bound OUT_TOL
+    applies to this quantity (2e-3 on the kernel's fp32 result; the bf16 store
+    adds up to half an ulp, which alone exceeds 2e-3 once |o| >= 1)."""
+    return float(np.max(np.abs(got_bf16_as_f64 - ref) - bf16_half_ulp(ref)))
+
+
 def k_from_fraction(p: float, N: int) -> int:
     return int(math.ceil(round(p * N, 6)))
 

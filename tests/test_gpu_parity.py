@@ -13,7 +13,7 @@ import torch
 import oracle
 import synth
 from spc_cases import (CONFIGS, OUT_TOL, GpuLayer, b2f, bitmap_from_idx, c5_cases, check_topk_sets, odims,
-                       oracle_pair)
+                       oracle_pair, out_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +58,7 @@ def test_small_full_pipeline(cfg):
     o, lse, lg = g.attn2()
     oo, lo, So = oracle.attention(d, q, qz, K, V)
     got = b2f(o.cpu().numpy())
-    assert np.abs(got - oo).max() <= OUT_TOL
+    assert out_err(got, oo) <= OUT_TOL
     np.testing.assert_allclose(lse.cpu().numpy(), lo, rtol=0, atol=1e-4)
 
     # ArgTopK over the speculative row
@@ -84,7 +84,7 @@ def test_small_full_pipeline(cfg):
         assert np.array_equal(g.staging.cpu().numpy().view(np.uint16)[:, :, :k], st)
         o1, lse1, lg1 = g.merged(idx_o, bm_full, k)
         oo1, lo1, So1 = oracle.attention(d, q, qz, K, V, idx=io)
-        assert np.abs(b2f(o1.cpu().numpy()) - oo1).max() <= OUT_TOL
+        assert out_err(b2f(o1.cpu().numpy()), oo1) <= OUT_TOL
         np.testing.assert_allclose(lse1.cpu().numpy(), lo1, rtol=0, atol=1e-4)
         idx2, _ = g.topk(lg1, lse1, k)
         io2, _ = oracle.topk(d, So1, k)
@@ -113,12 +113,12 @@ def test_k0_merged_is_attn2_and_all_fetched_is_bf16_attention():
     g.gather(idx, nq)
     o2, lse2, _ = g.merged(idx, bm, nq)
     oo, lo, _ = oracle.attention(d, q, qz, K, V, idx=idx.cpu().numpy())
-    assert np.abs(b2f(o2.cpu().numpy()) - oo).max() <= OUT_TOL
+    assert out_err(b2f(o2.cpu().numpy()), oo) <= OUT_TOL
     qf = torch.from_numpy(b2f(q)).permute(0, 2, 1, 3)
     Kf = torch.from_numpy(b2f(K)).repeat_interleave(4, dim=1)
     Vf = torch.from_numpy(b2f(V)).repeat_interleave(4, dim=1)
     ref = torch.nn.functional.scaled_dot_product_attention(qf, Kf, Vf, scale=d.scale).permute(0, 2, 1, 3)
-    assert np.abs(b2f(o2.cpu().numpy()) - ref.numpy()).max() <= OUT_TOL
+    assert out_err(b2f(o2.cpu().numpy()), ref.numpy()) <= OUT_TOL
 
 
 def test_topk_selection_exact_with_ties_across_cluster():
@@ -226,7 +226,7 @@ def full_size_check(cfg, pairs, layer=0, check_records=True):
             bh = b * cfg["Hkv"] + hk
             assert np.array_equal(rec_all[bh * ng * rb:(bh + 1) * ng * rb], rec.reshape(-1))
         hs = slice(hk * G, (hk + 1) * G)
-        err = np.abs(o_np[b, :, hs] - ref["o"]).max()
+        err = out_err(o_np[b, :, hs], ref["o"])
         worst = max(worst, err)
         assert err <= OUT_TOL
         np.testing.assert_allclose(lse_np[b, :, hs], ref["lse"], rtol=0, atol=1e-4)
@@ -237,7 +237,7 @@ def full_size_check(cfg, pairs, layer=0, check_records=True):
         # the GPU used its own selection; identical except for boundary swaps
         same = np.array_equal(idx_np[b, hk], io[0, 0])
         tol = OUT_TOL if same else 2 * OUT_TOL
-        assert np.abs(o1_np[b, :, hs] - ref1["o"]).max() <= tol
+        assert out_err(o1_np[b, :, hs], ref1["o"]) <= tol
         io2, _ = oracle.topk(ref1["d"], ref1["S"][None, None], k)
         if same:
             check_topk_sets(idx2_np[b, hk], io2[0, 0], ref1["S"], k)
