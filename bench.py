@@ -173,8 +173,8 @@ class DecodeStep:
         self.idx = torch.zeros((layers, B, Hkv, k), dtype=torch.int32, device=dev)
         self.bitmap = torch.zeros((layers, B, Hkv, d.q_groups_cap), dtype=torch.int32, device=dev)
         self.staging = torch.zeros((layers, B, Hkv, k, 2, 128), dtype=torch.int16, device=dev)
-        self.ws_bytes = spc.spc_attn_workspace_bytes(d)
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.ws_bytes = spc.spc_attn_workspace_bytes(d, k)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
         self.main = torch.cuda.Stream()
         self.side = torch.cuda.Stream(priority=-1)
         self.attn_done = [torch.cuda.Event() for _ in range(layers)]
@@ -190,7 +190,7 @@ class DecodeStep:
                                     stream=self.main)
                 spc.spc_host_gather(d, self.host[l], N, self.idx[l], k, self.staging[l], stream=self.main)
         torch.cuda.synchronize()
-        self.launches_per_step = layers * (3 + 2)  # low-bit scan, bf16 rows, combine, top-k, gather
+        self.launches_per_step = layers * 3  # attention (one launch), top-k, gather
         self.graph = None
 
     def enqueue(self, timed=False):
@@ -230,6 +230,44 @@ class DecodeStep:
 
     def attn_ms(self):
         return [s.elapsed_time(e) for (s, e) in self.attn_ev]
+
+
+def host_link_probe(step, reps=20):
+    """The pre-fetch alone against the host link: one layer's gather of the
+    selected 16-bit rows (zero-copy loads from pinned host memory) timed in
+    isolation, next to a contiguous pinned host-to-device copy of 1 GiB (the
+    copy engines' rate, taken as the link's measured peak)."""
+    torch = step.torch
+    W, d, k = step.W, step.d, step.k
+    s = step.main
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            step.spc.spc_host_gather(d, step.host[0], W["N"], step.idx[0], k, step.staging[0], stream=s)
+        e0.record(s)
+        for _ in range(reps):
+            step.spc.spc_host_gather(d, step.host[0], W["N"], step.idx[0], k, step.staging[0], stream=s)
+        e1.record(s)
+    torch.cuda.synchronize()
+    g_ms = e0.elapsed_time(e1) / reps
+    g_bytes = W["B"] * W["Hkv"] * k * 512
+    src = step.host[0].view(-1)
+    dst = torch.empty(src.numel(), dtype=src.dtype, device="cuda")
+    with torch.cuda.stream(s):
+        dst.copy_(src, non_blocking=True)
+        e0.record(s)
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize()
+    c_ms = e0.elapsed_time(e1) / 3
+    c_gbs = src.numel() * src.element_size() / (c_ms / 1000.0) / 1e9
+    del dst
+    g_gbs = g_bytes / (g_ms / 1000.0) / 1e9
+    return {"kernel": "spc_host_gather, one layer", "bytes_per_launch": g_bytes, "avg_launch_us": g_ms * 1000.0,
+            "achieved_gbs": g_gbs, "host_link_peak_gbs": c_gbs,
+            "peak_source": "measured: contiguous pinned host-to-device copy of 1 GiB",
+            "frac": g_gbs / c_gbs}
 
 
 def attention_bytes_per_layer(W, nq):
@@ -392,6 +430,8 @@ def main():
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
             "step_hbm_gbs": bytes_layer * W["layers"] / (ms_per_step / 1000.0) / 1e9}
 
+    gather = host_link_probe(step, reps=20)
+
     line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16-mma/f32", "data": "synthetic",
@@ -399,7 +439,7 @@ def main():
                        "bits": W["bits"], "k": W["k"], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (4.3 GB low-bit cache per step, 129 MB L2); no flush",
                        "graph": "one CUDA graph per step, main + side stream"},
-            "roofline": roof, "clocks": clk.summary(), "e2e": e2e,
+            "roofline": roof, "gather": gather, "clocks": clk.summary(), "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps}
     if rank == 0 and not args.no_cpu_baseline:
         ref = OracleSample(W, args.cpu_pairs)

@@ -70,7 +70,7 @@ _sig = {
     "spc_records_bytes": (C.c_size_t, [_D]),
     "spc_resid_bytes": (C.c_size_t, [_D]),
     "spc_quantize_kv": (C.c_int, [_D, _P, _P, _P, _P, _P]),
-    "spc_attn_workspace_bytes": (C.c_size_t, [_D]),
+    "spc_attn_workspace_bytes": (C.c_size_t, [_D, C.c_int32]),
     "spc_decode_attn2": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "spc_merged_attn": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
     "spc_topk_select": (C.c_int, [_D, _P, _P, C.c_int32, _P, _P, _P]),
@@ -119,8 +119,8 @@ def spc_resid_bytes(d) -> int:
     return int(_lib.spc_resid_bytes(C.byref(d)))
 
 
-def spc_attn_workspace_bytes(d) -> int:
-    return int(_lib.spc_attn_workspace_bytes(C.byref(d)))
+def spc_attn_workspace_bytes(d, k_max=0) -> int:
+    return int(_lib.spc_attn_workspace_bytes(C.byref(d), int(k_max)))
 
 
 def spc_quantize_kv(d, k, v, records, resid, stream=None):

@@ -3,11 +3,14 @@
 // copy C', with the fetched 16-bit rows C_kappa used in place of their
 // low-bit copies, plus the bf16 residual window.
 //
-// Work split (flash-decoding style split-K over tokens):
-//   * grid (chunks + 1, B*Hkv).  CTAs 0..chunks-1 scan 32-token groups of C';
-//     CTA `chunks` handles every 16-bit row (residual window and fetched rows).
-//   * each CTA writes one partial (running max, sum, unnormalised output) per
-//     query row to the workspace; attn_combine_kernel merges them.
+// One launch per call, split-K over tokens (flash-decoding style):
+//   * grid (chunks + bchunks, B*Hkv).  CTAs 0..chunks-1 of a (b, hkv) scan
+//     32-token groups of C'; CTAs chunks.. handle the 16-bit rows (residual
+//     window first, then the fetched rows), 128 rows per CTA.
+//   * every CTA merges its four warps and writes one partial (running max,
+//     sum, unnormalised output) per query row to the workspace; the last CTA
+//     of a (b, hkv) to finish (an atomic ticket) merges the partials into the
+//     bf16 output and the log-sum-exp, and re-zeroes the ticket.
 //
 // Low-bit tile arithmetic.  With k^ = z + s*b (b the code, z and s per key
 // group), the logit of query row q is  sum_c q_c s_c b_c + sum_c q_c z_c.  The
@@ -19,7 +22,8 @@
 // The value side o = sum_n p_n (z_n + s_n b_n) is the same product with
 // A = value bits (channels x tokens) and B = p o s (tokens x query rows); the
 // p*z term is accumulated on CUDA cores.  Softmax runs in base 2 with the
-// scale folded into q.
+// scale folded into q.  z and s of a group are computed once per warp into
+// shared memory and read back by the lanes that need them.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -29,8 +33,9 @@ namespace spc {
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = 3;
+constexpr int kRows16PerCta = 32 * kWarps;  // 16-bit rows per CTA (one 32-row batch per warp)
 constexpr float kNeg = -1e30f;  // finite "minus infinity": keeps max/rescale arithmetic NaN-free
-constexpr int kPartStride = 132; // floats per (chunk, row) partial: m, l, pad, pad, o[128]
+constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pad, o[128]
 
 struct AttnArgs {
   const uint8_t* records;
@@ -40,61 +45,63 @@ struct AttnArgs {
   const uint32_t* bitmap;
   const uint16_t* staging;
   float* spec_logits;
-  float* ws;
+  float* part;          // [BH][chunks + bchunks][kMaxRows][kPartStride]
+  uint32_t* tickets;    // [BH], zero between calls
+  uint16_t* out;        // [B][2][Hq][D]
+  float* lse;           // [B][2][Hq] or null
   int32_t k;
   int32_t Hq, Hkv, G, nq, r, q_groups_cap, resid_cap;
-  int32_t chunks, groups_per_chunk;
+  int32_t chunks, groups_per_chunk, bchunks;
   int32_t Lcap;
   float qscale;  // softmax scale * log2(e)
 };
 
-// {bit r, bit r+16} of w as an f16x2 pair of {0, v} (v = 1.0 or 2.0).
-template <uint32_t kOne>
-__device__ __forceinline__ uint32_t expand_pair(uint32_t w, int r) {
-  return ((w >> r) & 0x00010001u) * kOne;
+// Bits r and r+16 of w as an f16x2 pair, each 0 or the fp16 pattern v (1.0
+// or 2.0): isolate the two bits, then one multiply moves each onto v's
+// pattern (v is a multiple of 2^10, so v >> r is exact for r <= 10).  For
+// r >= 11 the caller passes ws = w >> 5 and the same rule applies at r - 5.
+__device__ __forceinline__ uint32_t bit_pair(uint32_t w, uint32_t ws, int r, uint32_t v) {
+  if (r <= 10) return (w & ((1u << r) | (1u << (r + 16)))) * (v >> r);
+  return (ws & ((1u << (r - 5)) | (1u << (r + 11)))) * (v >> (r - 5));
 }
 
-// Writes this warp's per-row state to shared memory, then (after a barrier)
-// the CTA's merged partial to the workspace.
+// fp16 high part of two floats (truncated to 11 significant bits, exact in
+// fp16) and the fp16 rounding of the remainder.
+__device__ __forceinline__ void split_hi_lo(float2 w, uint32_t& hi, uint32_t& lo) {
+  const float2 h = make_float2(__uint_as_float(__float_as_uint(w.x) & 0xFFFFE000u),
+                               __uint_as_float(__float_as_uint(w.y) & 0xFFFFE000u));
+  const float2 l = f2_sub(w, h);
+  hi = pack_f16x2(h.x, h.y);
+  lo = pack_f16x2(l.x, l.y);
+}
+
+// z and s of one group from its bf16 (min, max) word.
+template <int BITS>
+__device__ __forceinline__ void dequant_params(uint32_t mm, float& z, float& s) {
+  const float lo = __uint_as_float(mm << 16), hi = __uint_as_float(mm & 0xFFFF0000u);
+  if (BITS == 1) {
+    s = (hi - lo) * 0.5f;
+    z = fmaf(s, 0.5f, lo);  // (3 min + max) / 4 = min + s / 2
+  } else {
+    s = (hi - lo) * (1.f / 3.f);
+    z = lo;
+  }
+}
+
 struct CtaMerge {
   float m[kWarps][kMaxRows];
   float l[kWarps][kMaxRows];
   float o[kWarps][kMaxRows][kD];
 };
 
-__device__ void cta_merge_and_store(CtaMerge& sm, const AttnArgs& a, int64_t bh, int chunk) {
-  __syncthreads();
-  const int c = threadIdx.x;  // channel
-  const int rows = 2 * a.G;
-  float* part = a.ws + ((bh * (a.chunks + 1) + chunk) * kMaxRows) * kPartStride;
-  for (int rho = 0; rho < rows; ++rho) {
-    float M = kNeg;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][rho]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = fast_exp2(sm.m[w][rho] - M);
-      L += sm.l[w][rho] * f;
-      O += sm.o[w][rho][c] * f;
-    }
-    float* pr = part + rho * kPartStride;
-    if (c == 0) {
-      pr[0] = M;
-      pr[1] = L;
-    }
-    pr[4 + c] = O;
-  }
-}
-
+// ------------------------------------------------------------ low-bit CTA
 template <int BITS, bool MERGED>
-__global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
+__device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaMerge& merge) {
   constexpr int RB = 1024 * (BITS + 1);
   constexpr int KMETA = 512 * BITS;
   constexpr int VCODES = KMETA + 512;
   constexpr int VMETA = VCODES + 512 * BITS;
-  __shared__ CtaMerge merge;
+  constexpr int WARP_BYTES = kStages * RB + 2048;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, t = lane & 3;
@@ -104,7 +111,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
   const int G = a.G;
   const bool row_valid = gid < 2 * G;
 
-  uint8_t* stage = dyn_smem + (size_t)warp * kStages * RB;
+  uint8_t* stage = dyn + (size_t)warp * WARP_BYTES;
+  // per-group z and s: keys [t][kc][z0..3, s0..3], values [t][c16][slot][z cg0..3, s cg0..3]
+  float4* kzs = reinterpret_cast<float4*>(stage + kStages * RB);
+  float4* vzs = kzs + 64;
 
   // Scaled query of row gid at this lane's 32 channels, ordered
   // m = 4*kc + 2*h + half  <->  channel 16*kc + 2*t + 8*h + half.
@@ -138,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
   };
 
   float m_run = kNeg, l_run = 0.f;
-  float zacc[4] = {0.f, 0.f, 0.f, 0.f};
+  float2 zacc01 = make_float2(0.f, 0.f), zacc23 = make_float2(0.f, 0.f);
   float oacc[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
@@ -157,91 +167,96 @@ __global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
     const uint8_t* R = stage + (it % kStages) * RB;
     const int g = g_begin + warp + it * kWarps;
 
-    // ---- key group: A fragments (q o s, hi/lo) and the z bias ----
-    uint32_t afr[8][4];
-    float bias = 0.f;
+    // ---- z, s of the group's 128 key groups and 128 value groups, 4 + 4 per lane ----
+    {
+      const uint4 km = *reinterpret_cast<const uint4*>(R + KMETA + 16 * lane);
+      float4 z, s;
+      dequant_params<BITS>(km.x, z.x, s.x);
+      dequant_params<BITS>(km.y, z.y, s.y);
+      dequant_params<BITS>(km.z, z.z, s.z);
+      dequant_params<BITS>(km.w, z.w, s.w);
+      kzs[2 * lane] = z;  // lane covers key entries 4*lane..4*lane+3 = (t = lane/8, kc = lane%8)
+      kzs[2 * lane + 1] = s;
+      const uint4 vm = *reinterpret_cast<const uint4*>(R + VMETA + 16 * lane);
+      dequant_params<BITS>(vm.x, z.x, s.x);
+      dequant_params<BITS>(vm.y, z.y, s.y);
+      dequant_params<BITS>(vm.z, z.z, s.z);
+      dequant_params<BITS>(vm.w, z.w, s.w);
+      vzs[2 * lane] = z;  // value entries: (t, c16, slot) = (lane/8, (lane/4)%2, lane%4), cg 0..3
+      vzs[2 * lane + 1] = s;
+    }
+    __syncwarp();
+
+    // ---- QK, channel chunk outer: A = q o s (hi/lo), B = key bits ----
+    uint32_t kw[4], kwh[4], kw1[4], kwh1[4];
+    {
+      const uint4 v0 = *reinterpret_cast<const uint4*>(R + 16 * lane);
+      kw[0] = v0.x; kw[1] = v0.y; kw[2] = v0.z; kw[3] = v0.w;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) kwh[nt] = kw[nt] >> 5;
+      if (BITS == 2) {
+        const uint4 v1 = *reinterpret_cast<const uint4*>(R + 512 + 16 * lane);
+        kw1[0] = v1.x; kw1[1] = v1.y; kw1[2] = v1.z; kw1[3] = v1.w;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) kwh1[nt] = kw1[nt] >> 5;
+      }
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    float2 bias2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc) {
-      const uint4 mm = *reinterpret_cast<const uint4*>(R + KMETA + 128 * t + 16 * kc);
-      const uint32_t mw[4] = {mm.x, mm.y, mm.z, mm.w};
-      float wv[4];
+      const float4 z4 = kzs[2 * (8 * t + kc)];
+      const float4 s4 = kzs[2 * (8 * t + kc) + 1];
+      const float2 q01 = make_float2(qv[4 * kc], qv[4 * kc + 1]);
+      const float2 q23 = make_float2(qv[4 * kc + 2], qv[4 * kc + 3]);
+      bias2 = f2_fma(q01, make_float2(z4.x, z4.y), bias2);
+      bias2 = f2_fma(q23, make_float2(z4.z, z4.w), bias2);
+      uint32_t af[4];
+      split_hi_lo(f2_mul(q01, make_float2(s4.x, s4.y)), af[0], af[1]);
+      split_hi_lo(f2_mul(q23, make_float2(s4.z, s4.w)), af[2], af[3]);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = bf16_to_f32(mw[e] & 0xFFFFu), hi = bf16_to_f32(mw[e] >> 16);
-        float z, sc;
-        if (BITS == 1) {
-          z = (3.f * lo + hi) * 0.25f;
-          sc = (hi - lo) * 0.5f;
-        } else {
-          z = lo;
-          sc = (hi - lo) * (1.f / 3.f);
-        }
-        wv[e] = qv[4 * kc + e] * sc;
-        bias = fmaf(qv[4 * kc + e], z, bias);
+      for (int nt = 0; nt < 4; ++nt) {
+        if (BITS == 2)
+          mma_16816(acc[nt], af, bit_pair(kw1[nt], kwh1[nt], 2 * kc, 0x4000u),
+                    bit_pair(kw1[nt], kwh1[nt], 2 * kc + 1, 0x4000u));
+        mma_16816(acc[nt], af, bit_pair(kw[nt], kwh[nt], 2 * kc, 0x3C00u),
+                  bit_pair(kw[nt], kwh[nt], 2 * kc + 1, 0x3C00u));
       }
-      const uint32_t h01 = pack_f16x2(wv[0], wv[1]);
-      const uint32_t h23 = pack_f16x2(wv[2], wv[3]);
-      const float2 f01 = unpack_f16x2(h01), f23 = unpack_f16x2(h23);
-      afr[kc][0] = h01;
-      afr[kc][2] = h23;
-      afr[kc][1] = pack_f16x2(wv[0] - f01.x, wv[1] - f01.y);
-      afr[kc][3] = pack_f16x2(wv[2] - f23.x, wv[3] - f23.y);
     }
+    float bias = bias2.x + bias2.y;
     bias += __shfl_xor_sync(0xFFFFFFFFu, bias, 1);
     bias += __shfl_xor_sync(0xFFFFFFFFu, bias, 2);
 
-    // ---- QK: 4 token tiles of 8 ----
-    const uint4 kw0 = *reinterpret_cast<const uint4*>(R + 16 * lane);
-    const uint32_t kwords0[4] = {kw0.x, kw0.y, kw0.z, kw0.w};
-    uint32_t kwords1[4] = {0u, 0u, 0u, 0u};
-    if (BITS == 2) {
-      const uint4 kw1 = *reinterpret_cast<const uint4*>(R + 512 + 16 * lane);
-      kwords1[0] = kw1.x; kwords1[1] = kw1.y; kwords1[2] = kw1.z; kwords1[3] = kw1.w;
-    }
-    float lg[4][2];
+    // ---- logits, speculative-row output, online softmax (base 2) ----
     const uint32_t bm = MERGED ? a.bitmap[bh * a.q_groups_cap + g] : 0u;
+    float lg[4][2];
     float gmax = kNeg;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (BITS == 2) {
-#pragma unroll
-        for (int kc = 0; kc < 8; ++kc)
-          mma_16816(acc, afr[kc], expand_pair<0x4000u>(kwords1[nt], 2 * kc),
-                    expand_pair<0x4000u>(kwords1[nt], 2 * kc + 1));
-      }
-#pragma unroll
-      for (int kc = 0; kc < 8; ++kc)
-        mma_16816(acc, afr[kc], expand_pair<0x3C00u>(kwords0[nt], 2 * kc),
-                  expand_pair<0x3C00u>(kwords0[nt], 2 * kc + 1));
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int tok = 8 * nt + 2 * t + e;
-        const bool masked = MERGED && ((bm >> tok) & 1u);
-        const float l = acc[e] + acc[2 + e] + bias;
-        lg[nt][e] = masked ? kNeg : l;
-        gmax = fmaxf(gmax, lg[nt][e]);
-      }
+      const float2 l = f2_add(f2_add(make_float2(acc[nt][0], acc[nt][1]), make_float2(acc[nt][2], acc[nt][3])),
+                              make_float2(bias, bias));
+      const int tok = 8 * nt + 2 * t;
+      const bool m0 = MERGED && ((bm >> tok) & 1u), m1 = MERGED && ((bm >> (tok + 1)) & 1u);
+      lg[nt][0] = m0 ? kNeg : l.x;
+      lg[nt][1] = m1 ? kNeg : l.y;
+      gmax = fmaxf(gmax, fmaxf(lg[nt][0], lg[nt][1]));
       if (spec_row) {
-        const int tok = 8 * nt + 2 * t;
         float* dst = spec_out + (int64_t)g * kGroup + tok;
-        const bool m0 = MERGED && ((bm >> tok) & 1u), m1 = MERGED && ((bm >> (tok + 1)) & 1u);
         if (!m0 && !m1) {
-          *reinterpret_cast<float2*>(dst) =
-              make_float2(lg[nt][0] * CUDART_LN2_F, lg[nt][1] * CUDART_LN2_F);
+          *reinterpret_cast<float2*>(dst) = make_float2(l.x * CUDART_LN2_F, l.y * CUDART_LN2_F);
         } else {
-          if (!m0) dst[0] = lg[nt][0] * CUDART_LN2_F;
-          if (!m1) dst[1] = lg[nt][1] * CUDART_LN2_F;
+          if (!m0) dst[0] = l.x * CUDART_LN2_F;
+          if (!m1) dst[1] = l.y * CUDART_LN2_F;
         }
       }
     }
-
-    // ---- online softmax (base 2) ----
     gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, 1));
     gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, 2));
     const float m_new = fmaxf(m_run, gmax);
-    const float alpha = fast_exp2(m_run - m_new);
     if (__any_sync(0xFFFFFFFFu, m_new != m_run)) {
+      const float alpha = fast_exp2(m_run - m_new);
       const float al_a = __shfl_sync(0xFFFFFFFFu, alpha, (2 * t) * 4);
       const float al_b = __shfl_sync(0xFFFFFFFFu, alpha, (2 * t + 1) * 4);
 #pragma unroll
@@ -252,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
         oacc[mt][3] *= al_b;
       }
       l_run *= alpha;
-#pragma unroll
-      for (int cg = 0; cg < 4; ++cg) zacc[cg] *= alpha;
+      zacc01 = f2_mul(zacc01, make_float2(alpha, alpha));
+      zacc23 = f2_mul(zacc23, make_float2(alpha, alpha));
       m_run = m_new;
     }
     float p[4][2];
@@ -265,57 +280,58 @@ __global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
         l_run += p[nt][e];
       }
 
-    // ---- PV: two 16-token chunks ----
-    const uint4 vw0 = *reinterpret_cast<const uint4*>(R + VCODES + 16 * lane);
-    const uint32_t vwords0[4] = {vw0.x, vw0.y, vw0.z, vw0.w};
-    uint32_t vwords1[4] = {0u, 0u, 0u, 0u};
-    if (BITS == 2) {
-      const uint4 vw1 = *reinterpret_cast<const uint4*>(R + VCODES + 512 + 16 * lane);
-      vwords1[0] = vw1.x; vwords1[1] = vw1.y; vwords1[2] = vw1.z; vwords1[3] = vw1.w;
+    // ---- PV: two 16-token chunks; A = value bits, B = p o s ----
+    uint32_t vw[4], vwh[4], vw1[4], vwh1[4];
+    {
+      const uint4 v0 = *reinterpret_cast<const uint4*>(R + VCODES + 16 * lane);
+      vw[0] = v0.x; vw[1] = v0.y; vw[2] = v0.z; vw[3] = v0.w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vwh[j] = vw[j] >> 5;
+      if (BITS == 2) {
+        const uint4 v1 = *reinterpret_cast<const uint4*>(R + VCODES + 512 + 16 * lane);
+        vw1[0] = v1.x; vw1[1] = v1.y; vw1[2] = v1.z; vw1[3] = v1.w;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) vwh1[j] = vw1[j] >> 5;
+      }
     }
 #pragma unroll
     for (int c16 = 0; c16 < 2; ++c16) {
       const float ps[4] = {p[2 * c16][0], p[2 * c16][1], p[2 * c16 + 1][0], p[2 * c16 + 1][1]};
-      float sv[4][4], zv[4][4];  // [slot][cg]
+      float4 zz[4], ss[4];  // [slot] over cg
 #pragma unroll
       for (int slot = 0; slot < 4; ++slot) {
-        const uint4 mm = *reinterpret_cast<const uint4*>(R + VMETA + 128 * t + 64 * c16 + 16 * slot);
-        const uint32_t mw[4] = {mm.x, mm.y, mm.z, mm.w};
-#pragma unroll
-        for (int cg = 0; cg < 4; ++cg) {
-          const float lo = bf16_to_f32(mw[cg] & 0xFFFFu), hi = bf16_to_f32(mw[cg] >> 16);
-          if (BITS == 1) {
-            zv[slot][cg] = (3.f * lo + hi) * 0.25f;
-            sv[slot][cg] = (hi - lo) * 0.5f;
-          } else {
-            zv[slot][cg] = lo;
-            sv[slot][cg] = (hi - lo) * (1.f / 3.f);
-          }
-        }
+        zz[slot] = vzs[2 * (8 * t + 4 * c16 + slot)];
+        ss[slot] = vzs[2 * (8 * t + 4 * c16 + slot) + 1];
+        const float2 pp = make_float2(ps[slot], ps[slot]);
+        zacc01 = f2_fma(pp, make_float2(zz[slot].x, zz[slot].y), zacc01);
+        zacc23 = f2_fma(pp, make_float2(zz[slot].z, zz[slot].w), zacc23);
       }
       uint32_t bfr[4][2];
-#pragma unroll
-      for (int cg = 0; cg < 4; ++cg) {
-        bfr[cg][0] = pack_f16x2(ps[0] * sv[0][cg], ps[1] * sv[1][cg]);
-        bfr[cg][1] = pack_f16x2(ps[2] * sv[2][cg], ps[3] * sv[3][cg]);
-        zacc[cg] = fmaf(ps[0], zv[0][cg], zacc[cg]);
-        zacc[cg] = fmaf(ps[1], zv[1][cg], zacc[cg]);
-        zacc[cg] = fmaf(ps[2], zv[2][cg], zacc[cg]);
-        zacc[cg] = fmaf(ps[3], zv[3][cg], zacc[cg]);
+      {
+        const float2 p01 = make_float2(ps[0], ps[1]), p23 = make_float2(ps[2], ps[3]);
+        float2 x;
+        x = f2_mul(p01, make_float2(ss[0].x, ss[1].x)); bfr[0][0] = pack_f16x2(x.x, x.y);
+        x = f2_mul(p23, make_float2(ss[2].x, ss[3].x)); bfr[0][1] = pack_f16x2(x.x, x.y);
+        x = f2_mul(p01, make_float2(ss[0].y, ss[1].y)); bfr[1][0] = pack_f16x2(x.x, x.y);
+        x = f2_mul(p23, make_float2(ss[2].y, ss[3].y)); bfr[1][1] = pack_f16x2(x.x, x.y);
+        x = f2_mul(p01, make_float2(ss[0].z, ss[1].z)); bfr[2][0] = pack_f16x2(x.x, x.y);
+        x = f2_mul(p23, make_float2(ss[2].z, ss[3].z)); bfr[2][1] = pack_f16x2(x.x, x.y);
+        x = f2_mul(p01, make_float2(ss[0].w, ss[1].w)); bfr[3][0] = pack_f16x2(x.x, x.y);
+        x = f2_mul(p23, make_float2(ss[2].w, ss[3].w)); bfr[3][1] = pack_f16x2(x.x, x.y);
       }
-      const uint32_t wa = vwords0[2 * c16], wb = vwords0[2 * c16 + 1];
+      const uint32_t wa = vw[2 * c16], wah = vwh[2 * c16], wb = vw[2 * c16 + 1], wbh = vwh[2 * c16 + 1];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        uint32_t af[4] = {expand_pair<0x3C00u>(wa, 2 * mt), expand_pair<0x3C00u>(wa, 2 * mt + 1),
-                          expand_pair<0x3C00u>(wb, 2 * mt), expand_pair<0x3C00u>(wb, 2 * mt + 1)};
+        const uint32_t af[4] = {bit_pair(wa, wah, 2 * mt, 0x3C00u), bit_pair(wa, wah, 2 * mt + 1, 0x3C00u),
+                                bit_pair(wb, wbh, 2 * mt, 0x3C00u), bit_pair(wb, wbh, 2 * mt + 1, 0x3C00u)};
         mma_16816(oacc[mt], af, bfr[mt >> 1][0], bfr[mt >> 1][1]);
       }
       if (BITS == 2) {
-        const uint32_t wa1 = vwords1[2 * c16], wb1 = vwords1[2 * c16 + 1];
+        const uint32_t xa = vw1[2 * c16], xah = vwh1[2 * c16], xb = vw1[2 * c16 + 1], xbh = vwh1[2 * c16 + 1];
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          uint32_t af[4] = {expand_pair<0x4000u>(wa1, 2 * mt), expand_pair<0x4000u>(wa1, 2 * mt + 1),
-                            expand_pair<0x4000u>(wb1, 2 * mt), expand_pair<0x4000u>(wb1, 2 * mt + 1)};
+          const uint32_t af[4] = {bit_pair(xa, xah, 2 * mt, 0x4000u), bit_pair(xa, xah, 2 * mt + 1, 0x4000u),
+                                  bit_pair(xb, xbh, 2 * mt, 0x4000u), bit_pair(xb, xbh, 2 * mt + 1, 0x4000u)};
           mma_16816(oacc[mt], af, bfr[mt >> 1][0], bfr[mt >> 1][1]);
         }
       }
@@ -324,9 +340,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
   }
   cp_async_wait<0>();
 
-  // ---- warp partial -> shared memory ----
+  // ---- warp state -> shared memory ----
   l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
   l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 2);
+  float zacc[4] = {zacc01.x, zacc01.y, zacc23.x, zacc23.y};
 #pragma unroll
   for (int cg = 0; cg < 4; ++cg) {
     zacc[cg] += __shfl_xor_sync(0xFFFFFFFFu, zacc[cg], 1);
@@ -336,7 +353,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
     merge.m[warp][gid] = m_run;
     merge.l[warp][gid] = l_run;
   }
-  __syncwarp();
   // oacc[mt]: (channel 16mt+gid, row 2t), (16mt+gid, 2t+1), (16mt+gid+8, 2t), (16mt+gid+8, 2t+1)
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
@@ -346,20 +362,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_lowbit_kernel(AttnArgs a) {
     merge.o[warp][2 * t + 1][16 * mt + gid + 8] = oacc[mt][3];
   }
   __syncwarp();
-  // add the p*z term of row gid: zacc[cg] applies to channels 32cg .. 32cg+31
+  // the p*z term of row gid: zacc[cg] applies to channels 32cg .. 32cg+31
 #pragma unroll
   for (int cg = 0; cg < 4; ++cg)
 #pragma unroll
     for (int q8 = 0; q8 < 8; ++q8) merge.o[warp][gid][32 * cg + 8 * t + q8] += zacc[cg];
-  cta_merge_and_store(merge, a, bh, chunk);
 }
 
-// CTA `chunks` of each (b, hkv): all 16-bit rows (residual window, then the
-// fetched rows) on CUDA cores, one token per lane for the logits and four
-// channels per lane for the value product.
-__global__ void __launch_bounds__(kThreads) attn_bf16_rows_kernel(AttnArgs a) {
-  __shared__ CtaMerge merge;
-  __shared__ float qs[kMaxRows][kD];
+// ------------------------------------------------------------ 16-bit-row CTA
+// The residual window and the fetched rows on CUDA cores: one row per lane
+// for the logits, four channels per lane for the value product.
+__device__ __forceinline__ void rows16_cta(const AttnArgs& a, uint8_t* dyn, CtaMerge& merge) {
+  float (*qs)[kD] = reinterpret_cast<float (*)[kD]>(dyn);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t bh = blockIdx.y;
   const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
@@ -384,7 +398,8 @@ __global__ void __launch_bounds__(kThreads) attn_bf16_rows_kernel(AttnArgs a) {
     l_run[rho] = 0.f;
     o[rho][0] = o[rho][1] = o[rho][2] = o[rho][3] = 0.f;
   }
-  for (int bt = warp; bt < n_batches; bt += kWarps) {
+  const int first = (blockIdx.x - a.chunks) * kWarps + warp;
+  for (int bt = first; bt < n_batches; bt += a.bchunks * kWarps) {
     const int j = 32 * bt + lane;  // this lane's row for the logits
     const uint16_t* row = nullptr;
     int pos = -1;                   // quantised position of a fetched row
@@ -400,16 +415,24 @@ __global__ void __launch_bounds__(kThreads) attn_bf16_rows_kernel(AttnArgs a) {
     for (int rho = 0; rho < kMaxRows; ++rho) lg[rho] = 0.f;
     if (row != nullptr) {
       const uint4* kr = reinterpret_cast<const uint4*>(row);
-#pragma unroll 4
+#pragma unroll 2
       for (int c8 = 0; c8 < kD / 8; ++c8) {
         const uint4 kk = kr[c8];
         const uint32_t kw[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float k0 = bf16_to_f32(kw[e] & 0xFFFFu), k1 = bf16_to_f32(kw[e] >> 16);
-#pragma unroll
-          for (int rho = 0; rho < kMaxRows; ++rho)
-            lg[rho] = fmaf(qs[rho][8 * c8 + 2 * e + 1], k1, fmaf(qs[rho][8 * c8 + 2 * e], k0, lg[rho]));
+        for (int rho = 0; rho < kMaxRows; ++rho) {
+          const float4 qa = *reinterpret_cast<const float4*>(&qs[rho][8 * c8]);
+          const float4 qb = *reinterpret_cast<const float4*>(&qs[rho][8 * c8 + 4]);
+          float acc = lg[rho];
+          acc = fmaf(qa.x, bf16_to_f32(kw[0] & 0xFFFFu), acc);
+          acc = fmaf(qa.y, bf16_to_f32(kw[0] >> 16), acc);
+          acc = fmaf(qa.z, bf16_to_f32(kw[1] & 0xFFFFu), acc);
+          acc = fmaf(qa.w, bf16_to_f32(kw[1] >> 16), acc);
+          acc = fmaf(qb.x, bf16_to_f32(kw[2] & 0xFFFFu), acc);
+          acc = fmaf(qb.y, bf16_to_f32(kw[2] >> 16), acc);
+          acc = fmaf(qb.z, bf16_to_f32(kw[3] & 0xFFFFu), acc);
+          acc = fmaf(qb.w, bf16_to_f32(kw[3] >> 16), acc);
+          lg[rho] = acc;
         }
       }
     }
@@ -478,31 +501,72 @@ __global__ void __launch_bounds__(kThreads) attn_bf16_rows_kernel(AttnArgs a) {
   for (int rho = 0; rho < kMaxRows; ++rho)
 #pragma unroll
     for (int e = 0; e < 4; ++e) merge.o[warp][rho][4 * lane + e] = o[rho][e];
-  cta_merge_and_store(merge, a, bh, a.chunks);
 }
 
-// Merge the split-K partials of one (b, hkv, query row): o in bf16 and the
-// natural-log normaliser.
-__global__ void __launch_bounds__(kD) attn_combine_kernel(AttnArgs a, uint16_t* out, float* lse) {
+// ------------------------------------------------------------ merge + combine
+__device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last) {
+  __syncthreads();
+  const int c = threadIdx.x;  // channel
   const int64_t bh = blockIdx.y;
-  const int rho = blockIdx.x;
-  const int c = threadIdx.x;
-  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
-  const int G = a.G, qi = rho / G, gi = rho % G;
-  const int nparts = a.chunks + 1;
-  const float* part = a.ws + (bh * nparts * kMaxRows + rho) * kPartStride;
-  float M = kNeg;
-  for (int p = 0; p < nparts; ++p) M = fmaxf(M, part[(int64_t)p * kMaxRows * kPartStride]);
-  float L = 0.f, O = 0.f;
-  for (int p = 0; p < nparts; ++p) {
-    const float* pr = part + (int64_t)p * kMaxRows * kPartStride;
-    const float f = fast_exp2(pr[0] - M);
-    L += pr[1] * f;
-    O += pr[4 + c] * f;
+  const int rows = 2 * a.G;
+  const int nparts = a.chunks + a.bchunks;
+  float* part = a.part + ((bh * nparts + blockIdx.x) * kMaxRows) * kPartStride;
+  for (int rho = 0; rho < rows; ++rho) {
+    float M = kNeg;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][rho]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = fast_exp2(sm.m[w][rho] - M);
+      L += sm.l[w][rho] * f;
+      O += sm.o[w][rho][c] * f;
+    }
+    float* pr = part + rho * kPartStride;
+    if (c == 0) {
+      pr[0] = M;
+      pr[1] = L;
+    }
+    pr[4 + c] = O;
   }
-  const int64_t orow = ((int64_t)b * 2 + qi) * a.Hq + hk * G + gi;
-  out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O / L : 0.f);
-  if (c == 0 && lse != nullptr) lse[orow] = L > 0.f ? (M + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
+  // last CTA of this (b, hkv) merges every partial
+  __threadfence();
+  __syncthreads();
+  if (c == 0) *s_last = (atomicAdd(&a.tickets[bh], 1u) == (unsigned)(nparts - 1));
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
+  const int G = a.G;
+  const float* base = a.part + (bh * nparts * kMaxRows) * kPartStride;
+  for (int rho = 0; rho < rows; ++rho) {
+    const int qi = rho / G, gi = rho % G;
+    float M = kNeg;
+    for (int p = 0; p < nparts; ++p) M = fmaxf(M, __ldcg(base + ((int64_t)p * kMaxRows + rho) * kPartStride));
+    float L = 0.f, O = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+      const float* pr = base + ((int64_t)p * kMaxRows + rho) * kPartStride;
+      const float f = fast_exp2(__ldcg(pr) - M);
+      L += __ldcg(pr + 1) * f;
+      O += __ldcg(pr + 4 + c) * f;
+    }
+    const int64_t orow = ((int64_t)b * 2 + qi) * a.Hq + hk * G + gi;
+    a.out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O / L : 0.f);
+    if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
+  }
+  if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
+}
+
+template <int BITS, bool MERGED>
+__global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
+  extern __shared__ __align__(16) uint8_t dyn_smem[];
+  __shared__ CtaMerge merge;
+  __shared__ int s_last;
+  if ((int)blockIdx.x < a.chunks)
+    lowbit_cta<BITS, MERGED>(a, dyn_smem, merge);
+  else
+    rows16_cta(a, dyn_smem, merge);
+  merge_store_combine(merge, a, &s_last);
 }
 
 // ---------------------------------------------------------------- host side
@@ -510,34 +574,82 @@ __global__ void __launch_bounds__(kD) attn_combine_kernel(AttnArgs a, uint16_t* 
 struct AttnPlan {
   int chunks;
   int groups_per_chunk;
+  int bchunks;
 };
 
-AttnPlan attn_plan(const spc_dims* d) {
+static int attn_smem_bytes(int bits) { return kWarps * (kStages * 1024 * (bits + 1) + 2048); }
+
+// Resident attention CTAs per SM on the current device (occupancy query,
+// cached per device and bit width).
+static int resident_ctas(int bits) {
+  static int cached[2][64] = {};
+  const int dev = spc_host::current_device();
+  const int bi = bits == 1 ? 0 : 1;
+  if (dev >= 0 && dev < 64) {
+    const int c = __atomic_load_n(&cached[bi][dev], __ATOMIC_ACQUIRE);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  const int smem = attn_smem_bytes(bits);
+  cudaError_t e;
+  if (bits == 1) {
+    static unsigned long long configured = 0ull;
+    e = spc_host::ensure_smem_limit(configured, attn_kernel<1, true>, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<1, true>, kThreads, smem);
+  } else {
+    static unsigned long long configured = 0ull;
+    e = spc_host::ensure_smem_limit(configured, attn_kernel<2, true>, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<2, true>, kThreads, smem);
+  }
+  if (e != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 2;
+  }
+  if (dev >= 0 && dev < 64) __atomic_store_n(&cached[bi][dev], n, __ATOMIC_RELEASE);
+  return n;
+}
+
+static AttnPlan attn_plan(const spc_dims* d, int32_t k) {
   const int ng = num_quantized(d->N, d->R) / kGroup;
-  AttnPlan p{0, 1};
-  if (ng == 0) return p;
+  const int r = d->N - num_quantized(d->N, d->R);
   const int64_t BH = (int64_t)d->B * d->Hkv;
-  const int64_t target = (int64_t)spc_host::sm_count() * 2;  // resident CTAs at 2 per SM
-  int64_t chunks = (target + BH - 1) / BH;
-  chunks = std::max<int64_t>(1, std::min<int64_t>(chunks, (ng + kWarps - 1) / kWarps));
-  p.groups_per_chunk = (int)((ng + chunks - 1) / chunks);
-  p.chunks = (ng + p.groups_per_chunk - 1) / p.groups_per_chunk;
+  AttnPlan p{0, 1, 0};
+  const int rows16 = r + std::max(k, 0);
+  p.bchunks = (rows16 + kRows16PerCta - 1) / kRows16PerCta;
+  if (ng > 0) {
+    const int64_t slots = (int64_t)spc_host::sm_count() * resident_ctas(d->bits);
+    int64_t chunks = std::max<int64_t>(1, slots / BH);
+    chunks = std::min<int64_t>(chunks, (ng + kWarps - 1) / kWarps);
+    p.groups_per_chunk = (int)((ng + chunks - 1) / chunks);
+    p.chunks = (ng + p.groups_per_chunk - 1) / p.groups_per_chunk;
+  }
+  if (p.chunks + p.bchunks == 0) p.bchunks = 1;  // N = 0: one CTA writes the empty result
   return p;
 }
 
-size_t attn_workspace_bytes(const spc_dims* d) {
-  const AttnPlan p = attn_plan(d);
-  return (size_t)d->B * d->Hkv * (p.chunks + 1) * kMaxRows * kPartStride * sizeof(float);
+static size_t part_floats(const spc_dims* d, const AttnPlan& p) {
+  return (size_t)d->B * d->Hkv * (p.chunks + p.bchunks) * kMaxRows * kPartStride;
+}
+
+// Workspace: the per-(b, hkv) tickets first (a fixed place, whatever k is),
+// then the partials from a 256-byte boundary.
+static size_t ticket_bytes(const spc_dims* d) {
+  return (((size_t)d->B * d->Hkv * sizeof(uint32_t) + 255) / 256) * 256;
+}
+
+size_t attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
+  return ticket_bytes(d) + part_floats(d, attn_plan(d, k_max)) * sizeof(float);
 }
 
 template <int BITS, bool MERGED>
-static cudaError_t launch_lowbit(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
-  const int smem = kWarps * kStages * 1024 * (BITS + 1);
-  auto* fn = attn_lowbit_kernel<BITS, MERGED>;
+static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
+  const int smem = attn_smem_bytes(BITS);
+  static_assert(kMaxRows * kD * 4 <= kWarps * (kStages * 2048 + 2048), "16-bit-row CTA query tile fits");
+  auto* fn = attn_kernel<BITS, MERGED>;
   static unsigned long long configured = 0ull;  // one per <BITS, MERGED> instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
   if (e != cudaSuccess) return e;
-  fn<<<dim3(a.chunks, (unsigned)BH), kThreads, smem, stream>>>(a);
+  fn<<<dim3(a.chunks + a.bchunks, (unsigned)BH), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -545,7 +657,7 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
                             const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
                             const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
                             float* spec_logits, void* ws, cudaStream_t stream) {
-  const AttnPlan plan = attn_plan(d);
+  const AttnPlan plan = attn_plan(d, k);
   AttnArgs a;
   a.records = static_cast<const uint8_t*>(records);
   a.resid = resid;
@@ -554,7 +666,10 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.bitmap = bitmap;
   a.staging = staging;
   a.spec_logits = spec_logits;
-  a.ws = static_cast<float*>(ws);
+  a.tickets = static_cast<uint32_t*>(ws);
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ticket_bytes(d));
+  a.out = o;
+  a.lse = lse;
   a.k = k;
   a.Hq = d->Hq;
   a.Hkv = d->Hkv;
@@ -565,25 +680,16 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.resid_cap = d->resid_cap;
   a.chunks = plan.chunks;
   a.groups_per_chunk = plan.groups_per_chunk;
+  a.bchunks = plan.bchunks;
   a.Lcap = d->q_groups_cap * kGroup;
   a.qscale = d->scale * 1.4426950408889634f;
   const int64_t BH = (int64_t)d->B * d->Hkv;
   const bool merged = k > 0;
-  cudaError_t e = cudaSuccess;
-  if (a.chunks > 0) {
-    if (d->bits == 1)
-      e = merged ? launch_lowbit<1, true>(a, BH, stream) : launch_lowbit<1, false>(a, BH, stream);
-    else
-      e = merged ? launch_lowbit<2, true>(a, BH, stream) : launch_lowbit<2, false>(a, BH, stream);
-  }
-  if (e == cudaSuccess) {
-    attn_bf16_rows_kernel<<<dim3(1, (unsigned)BH), kThreads, 0, stream>>>(a);
-    e = cudaGetLastError();
-  }
-  if (e == cudaSuccess) {
-    attn_combine_kernel<<<dim3(2 * a.G, (unsigned)BH), kD, 0, stream>>>(a, o, lse);
-    e = cudaGetLastError();
-  }
+  cudaError_t e;
+  if (d->bits == 1)
+    e = merged ? launch_attn<1, true>(a, BH, stream) : launch_attn<1, false>(a, BH, stream);
+  else
+    e = merged ? launch_attn<2, true>(a, BH, stream) : launch_attn<2, false>(a, BH, stream);
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);
     return SPC_ERR_CUDA;

@@ -8,7 +8,7 @@
 
 namespace spc {
 spc_status launch_quantize(const spc_dims*, const uint16_t*, const uint16_t*, void*, uint16_t*, cudaStream_t);
-size_t attn_workspace_bytes(const spc_dims*);
+size_t attn_workspace_bytes(const spc_dims*, int32_t);
 spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const uint16_t*, const int32_t*,
                             const uint32_t*, const uint16_t*, int32_t, uint16_t*, float*, float*, void*,
                             cudaStream_t);
@@ -82,12 +82,11 @@ spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* r
   if (!aligned16(records) || !aligned16(resid) || !aligned16(q) || !aligned16(o) || !aligned16(ws) ||
       !aligned16(lse) || !aligned16(spec_logits))
     return SPC_ERR_INVALID;
-  if (k < 0) return SPC_ERR_INVALID;
+  if (k < 0 || k > (1 << 24)) return SPC_ERR_INVALID;
   if (k > 0) {
     if (idx == nullptr || bitmap == nullptr || staging == nullptr || !aligned16(staging)) return SPC_ERR_INVALID;
-    if ((int64_t)k > (int64_t)d->q_groups_cap * spc::kGroup) return SPC_ERR_INVALID;
   }
-  if (ws_bytes < spc::attn_workspace_bytes(d)) return SPC_ERR_WORKSPACE;
+  if (ws_bytes < spc::attn_workspace_bytes(d, k)) return SPC_ERR_WORKSPACE;
   return spc::launch_attention(d, records, resid, q, k > 0 ? idx : nullptr, k > 0 ? bitmap : nullptr,
                                k > 0 ? staging : nullptr, k, o, lse, spec_logits, ws,
                                reinterpret_cast<cudaStream_t>(stream));
@@ -140,9 +139,9 @@ spc_status spc_quantize_kv(const spc_dims* d, const uint16_t* k, const uint16_t*
   return spc::launch_quantize(d, k, v, records, resid, reinterpret_cast<cudaStream_t>(stream));
 }
 
-size_t spc_attn_workspace_bytes(const spc_dims* d) {
-  if (check_dims(d) != SPC_OK) return 0;
-  return spc::attn_workspace_bytes(d);
+size_t spc_attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
+  if (check_dims(d) != SPC_OK || k_max < 0 || k_max > (1 << 24)) return 0;
+  return spc::attn_workspace_bytes(d, k_max);
 }
 
 spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
@@ -164,7 +163,7 @@ spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const fl
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
   const int32_t nq = spc::num_quantized(d->N, d->R);
-  if (k < 0 || (int64_t)k > (int64_t)d->q_groups_cap * spc::kGroup) return SPC_ERR_INVALID;
+  if (k < 0 || k > (1 << 24)) return SPC_ERR_INVALID;
   if (bitmap == nullptr || (k > 0 && idx == nullptr)) return SPC_ERR_INVALID;
   if (nq > 0 && (spec_logits == nullptr || lse == nullptr)) return SPC_ERR_INVALID;
   if (nq > 262144) return SPC_ERR_UNSUPPORTED;

@@ -116,8 +116,13 @@ spc_status spc_quantize_kv(const spc_dims* d, const uint16_t* k, const uint16_t*
                            void* records, uint16_t* resid, spc_stream stream);
 
 /* Bytes of device workspace spc_decode_attn2 / spc_merged_attn need for this
- * shape on the current device (split-K partials). */
-size_t spc_attn_workspace_bytes(const spc_dims* d);
+ * shape on the current device with at most k_max fetched rows per (b, hkv):
+ * one ticket word per (b, hkv) followed by the split-K partials.  The caller
+ * zero-fills a workspace once after allocating it; every call leaves the
+ * ticket words zero again.  Calls that share a workspace must not overlap on
+ * the GPU (issue them on one stream, or order them with events).
+ * Returns 0 for an invalid shape. */
+size_t spc_attn_workspace_bytes(const spc_dims* d, int32_t k_max);
 
 /*
  * Attn([T_t, T'_{t+1}], C') -- the two-query decode attention over the
@@ -131,7 +136,8 @@ size_t spc_attn_workspace_bytes(const spc_dims* d);
  *   spec_logits : fp32 [B][Hkv][G][q_groups_cap*32] or NULL: the speculative
  *           token's scaled logits scale*q.k at the quantised positions, the
  *           input of spc_topk_select.
- *   ws    : device workspace of at least spc_attn_workspace_bytes(d) bytes.
+ *   ws    : zero-filled-once device workspace of at least
+ *           spc_attn_workspace_bytes(d, 0) bytes (see that function).
  */
 spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16_t* resid,
                             const uint16_t* q, uint16_t* o, float* lse, float* spec_logits,
@@ -145,6 +151,7 @@ spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16
  * the low-bit rows.  bitmap (u32 [B][Hkv][q_groups_cap], bit n%32 of word
  * n/32) must mark exactly the listed positions.  spec_logits at a fetched
  * position holds the logit of the fetched row.  k = 0 is spc_decode_attn2.
+ * ws holds at least spc_attn_workspace_bytes(d, k) bytes.
  */
 spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_t* resid,
                            const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
@@ -160,7 +167,7 @@ spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_
  * Ties go to the lower position.  Outputs: idx int32 [B][Hkv][k], ascending,
  * entries k_eff..k-1 set to -1; bitmap u32 [B][Hkv][q_groups_cap] with
  * exactly the selected bits set (words past N_q/32 are zeroed).
- * k <= 32 * q_groups_cap; N_q <= 262144.
+ * N_q <= 262144.
  */
 spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse,
                            int32_t k, int32_t* idx, uint32_t* bitmap, spc_stream stream);

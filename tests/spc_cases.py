@@ -97,9 +97,11 @@ class GpuLayer:
         qn = synth.queries(seed, layer, B, Hq) if q is None else q
         self.q_np = qn
         self.q = torch.from_numpy(qn.view(np.int16).copy()).to(dev)
-        self.ws = torch.empty(max(spc.spc_attn_workspace_bytes(self.d), 16), dtype=torch.uint8, device=dev)
         self.Lcap = self.d.q_groups_cap * 32
         self.kcap = cfg["k"] if kcap is None else kcap
+        # zero-filled once, as the workspace contract asks
+        self.ws = torch.zeros(max(spc.spc_attn_workspace_bytes(self.d, max(self.kcap, self.nq)), 16),
+                              dtype=torch.uint8, device=dev)
         self.host = None
         if host:
             self.host = torch.empty((B, Hkv, N, 2, 128), dtype=torch.int16, pin_memory=True)
