@@ -36,6 +36,9 @@ constexpr int kStages = 3;
 constexpr int kRows16PerCta = 32 * kWarps;  // 16-bit rows per CTA (one 32-row batch per warp)
 constexpr float kNeg = -1e30f;  // finite "minus infinity": keeps max/rescale arithmetic NaN-free
 constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pad, o[128]
+constexpr int kZsPitch = 17;     // float4s per t block of a z/s table (16 + 1 pad)
+constexpr int kZsBytes = 2 * 4 * kZsPitch * 16;  // key and value tables of one warp
+constexpr int kMergePitch = kD + 4;              // padded row of the CTA merge buffer
 
 struct AttnArgs {
   const uint8_t* records;
@@ -91,7 +94,7 @@ __device__ __forceinline__ void dequant_params(uint32_t mm, float& z, float& s) 
 struct CtaMerge {
   float m[kWarps][kMaxRows];
   float l[kWarps][kMaxRows];
-  float o[kWarps][kMaxRows][kD];
+  float o[kWarps][kMaxRows][kMergePitch];
 };
 
 // ------------------------------------------------------------ low-bit CTA
@@ -101,7 +104,8 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
   constexpr int KMETA = 512 * BITS;
   constexpr int VCODES = KMETA + 512;
   constexpr int VMETA = VCODES + 512 * BITS;
-  constexpr int WARP_BYTES = kStages * RB + 2048;
+  constexpr int STAGE = RB + 16;  // a record plus its bitmap word
+  constexpr int WARP_BYTES = kStages * STAGE + kZsBytes;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, t = lane & 3;
@@ -112,9 +116,11 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
   const bool row_valid = gid < 2 * G;
 
   uint8_t* stage = dyn + (size_t)warp * WARP_BYTES;
-  // per-group z and s: keys [t][kc][z0..3, s0..3], values [t][c16][slot][z cg0..3, s cg0..3]
-  float4* kzs = reinterpret_cast<float4*>(stage + kStages * RB);
-  float4* vzs = kzs + 64;
+  // per-group z and s: keys [t][kc][z0..3, s0..3], values [t][c16][slot][z cg0..3, s cg0..3],
+  // each t block padded by one float4 so that the four t rows read together
+  // fall in different banks
+  float4* kzs = reinterpret_cast<float4*>(stage + kStages * STAGE);
+  float4* vzs = kzs + kZsPitch * 4;
 
   // Scaled query of row gid at this lane's 32 channels, ordered
   // m = 4*kc + 2*h + half  <->  channel 16*kc + 2*t + 8*h + half.
@@ -140,9 +146,10 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     if (item < n_my) {
       const int g = g_begin + warp + item * kWarps;
       const uint8_t* src = rec_base + (int64_t)g * RB;
-      uint8_t* dst = stage + (item % kStages) * RB;
+      uint8_t* dst = stage + (item % kStages) * STAGE;
 #pragma unroll
       for (int u = 0; u < RB / 512; ++u) cp_async16(dst + 16 * (lane + 32 * u), src + 16 * (lane + 32 * u));
+      if (MERGED && lane == 0) cp_async4(dst + RB, a.bitmap + bh * a.q_groups_cap + g);
     }
     cp_async_commit();
   };
@@ -164,7 +171,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     issue(it + kStages - 1);
     cp_async_wait<kStages - 1>();
     __syncwarp();
-    const uint8_t* R = stage + (it % kStages) * RB;
+    const uint8_t* R = stage + (it % kStages) * STAGE;
     const int g = g_begin + warp + it * kWarps;
 
     // ---- z, s of the group's 128 key groups and 128 value groups, 4 + 4 per lane ----
@@ -175,15 +182,16 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
       dequant_params<BITS>(km.y, z.y, s.y);
       dequant_params<BITS>(km.z, z.z, s.z);
       dequant_params<BITS>(km.w, z.w, s.w);
-      kzs[2 * lane] = z;  // lane covers key entries 4*lane..4*lane+3 = (t = lane/8, kc = lane%8)
-      kzs[2 * lane + 1] = s;
+      const int zi = kZsPitch * (lane >> 3) + 2 * (lane & 7);
+      kzs[zi] = z;  // lane covers key entries 4*lane..4*lane+3 = (t = lane/8, kc = lane%8)
+      kzs[zi + 1] = s;
       const uint4 vm = *reinterpret_cast<const uint4*>(R + VMETA + 16 * lane);
       dequant_params<BITS>(vm.x, z.x, s.x);
       dequant_params<BITS>(vm.y, z.y, s.y);
       dequant_params<BITS>(vm.z, z.z, s.z);
       dequant_params<BITS>(vm.w, z.w, s.w);
-      vzs[2 * lane] = z;  // value entries: (t, c16, slot) = (lane/8, (lane/4)%2, lane%4), cg 0..3
-      vzs[2 * lane + 1] = s;
+      vzs[zi] = z;  // value entries: (t, c16, slot) = (lane/8, (lane/4)%2, lane%4), cg 0..3
+      vzs[zi + 1] = s;
     }
     __syncwarp();
 
@@ -207,8 +215,8 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     float2 bias2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc) {
-      const float4 z4 = kzs[2 * (8 * t + kc)];
-      const float4 s4 = kzs[2 * (8 * t + kc) + 1];
+      const float4 z4 = kzs[kZsPitch * t + 2 * kc];
+      const float4 s4 = kzs[kZsPitch * t + 2 * kc + 1];
       const float2 q01 = make_float2(qv[4 * kc], qv[4 * kc + 1]);
       const float2 q23 = make_float2(qv[4 * kc + 2], qv[4 * kc + 3]);
       bias2 = f2_fma(q01, make_float2(z4.x, z4.y), bias2);
@@ -230,7 +238,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     bias += __shfl_xor_sync(0xFFFFFFFFu, bias, 2);
 
     // ---- logits, speculative-row output, online softmax (base 2) ----
-    const uint32_t bm = MERGED ? a.bitmap[bh * a.q_groups_cap + g] : 0u;
+    const uint32_t bm = MERGED ? *reinterpret_cast<const uint32_t*>(R + RB) : 0u;
     float lg[4][2];
     float gmax = kNeg;
 #pragma unroll
@@ -300,8 +308,8 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
       float4 zz[4], ss[4];  // [slot] over cg
 #pragma unroll
       for (int slot = 0; slot < 4; ++slot) {
-        zz[slot] = vzs[2 * (8 * t + 4 * c16 + slot)];
-        ss[slot] = vzs[2 * (8 * t + 4 * c16 + slot) + 1];
+        zz[slot] = vzs[kZsPitch * t + 2 * (4 * c16 + slot)];
+        ss[slot] = vzs[kZsPitch * t + 2 * (4 * c16 + slot) + 1];
         const float2 pp = make_float2(ps[slot], ps[slot]);
         zacc01 = f2_fma(pp, make_float2(zz[slot].x, zz[slot].y), zacc01);
         zacc23 = f2_fma(pp, make_float2(zz[slot].z, zz[slot].w), zacc23);
@@ -577,7 +585,7 @@ struct AttnPlan {
   int bchunks;
 };
 
-static int attn_smem_bytes(int bits) { return kWarps * (kStages * 1024 * (bits + 1) + 2048); }
+static int attn_smem_bytes(int bits) { return kWarps * (kStages * (1024 * (bits + 1) + 16) + kZsBytes); }
 
 // Resident attention CTAs per SM on the current device (occupancy query,
 // cached per device and bit width).
@@ -615,10 +623,11 @@ static AttnPlan attn_plan(const spc_dims* d, int32_t k) {
   const int64_t BH = (int64_t)d->B * d->Hkv;
   AttnPlan p{0, 1, 0};
   const int rows16 = r + std::max(k, 0);
-  p.bchunks = (rows16 + kRows16PerCta - 1) / kRows16PerCta;
+  p.bchunks = (rows16 + 2 * kRows16PerCta - 1) / (2 * kRows16PerCta);  // two 32-row batches per warp
   if (ng > 0) {
+    // one wave: the low-bit chunks fill the resident slots the 16-bit CTAs leave
     const int64_t slots = (int64_t)spc_host::sm_count() * resident_ctas(d->bits);
-    int64_t chunks = std::max<int64_t>(1, slots / BH);
+    int64_t chunks = std::max<int64_t>(1, slots / BH - p.bchunks);
     chunks = std::min<int64_t>(chunks, (ng + kWarps - 1) / kWarps);
     p.groups_per_chunk = (int)((ng + chunks - 1) / chunks);
     p.chunks = (ng + p.groups_per_chunk - 1) / p.groups_per_chunk;
@@ -644,7 +653,7 @@ size_t attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
 template <int BITS, bool MERGED>
 static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
   const int smem = attn_smem_bytes(BITS);
-  static_assert(kMaxRows * kD * 4 <= kWarps * (kStages * 2048 + 2048), "16-bit-row CTA query tile fits");
+  static_assert(kMaxRows * kD * 4 <= kWarps * (kStages * 2064 + kZsBytes), "16-bit-row CTA query tile fits");
   auto* fn = attn_kernel<BITS, MERGED>;
   static unsigned long long configured = 0ull;  // one per <BITS, MERGED> instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
