@@ -159,6 +159,25 @@ spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_
                            float* spec_logits, void* ws, size_t ws_bytes, spc_stream stream);
 
 /*
+ * spc_merged_attn without a caller-provided workspace.  The SpeCache paper has
+ * no counterpart to this call; it exists for callers that cannot allocate
+ * device memory (a plug-in running inside a host that owns the device
+ * allocator, or a path where cudaMalloc's implicit synchronisation is not
+ * allowed).  Same arguments and results as spc_merged_attn minus ws/ws_bytes:
+ * the workspace is a fixed 8 MiB buffer compiled into the library, which each
+ * GPU that uses this call holds until the process exits.  Nothing is
+ * allocated.  The first call on a device looks the buffer's address up
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * Shapes whose workspace (spc_attn_workspace_bytes(d, k)) exceeds 8 MiB
+ * return SPC_ERR_WORKSPACE.  All calls share the buffer: calls that overlap
+ * on the GPU race, so issue them in order on one stream.
+ */
+spc_status spc_merged_attn_noalloc(const spc_dims* d, const void* records, const uint16_t* resid,
+                                   const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
+                                   const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
+                                   float* spec_logits, spc_stream stream);
+
+/*
  * ArgTopK(A_{1,:}) (Algorithm 3): per (b, hkv), the k_eff = min(k, N_q)
  * quantised positions n with the largest score
  *   S(n) = sum over the G query heads h of KV head hkv of
