@@ -33,6 +33,9 @@ WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=
                          "N=32768, 1-bit, residual 128, top-1% (k=328)",
                 B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328, layers=32)
 METRIC = "decode attn steps/s at 32K ctx, 1-bit, top-1% (HBM GB/s and % of peak in roofline)"
+# DRAM bytes (read + write) of one merged-attention launch of this workload, from the ncu capture
+# summarised in profiles/attn_kernel_llama3_8b_32k.md; None once the kernel changes after that capture.
+ATTN_TRAFFIC_BYTES = 168.9e6
 
 
 def parse():
@@ -424,7 +427,8 @@ def main():
     attn_avg_ms = statistics.mean(per_layer)
     achieved = bytes_layer / (attn_avg_ms / 1000.0) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "frac": achieved / peaks["hbm_gbs"], "traffic": ATTN_TRAFFIC_BYTES,
+            "traffic_source": "dram read+write of one launch, profiles/attn_kernel_llama3_8b_32k.md",
             "kernel": "spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer",
             "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
