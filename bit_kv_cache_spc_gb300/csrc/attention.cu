@@ -32,7 +32,11 @@ namespace spc {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = 3;
+template <int BITS>
+struct Stages {
+  static constexpr int value = BITS == 1 ? 4 : 3;  // cp.async pipeline depth per warp
+};
+constexpr int kMergeOffset = 4096;  // CTA merge buffer in dynamic smem, after the 16-bit CTA's query tile
 constexpr int kRows16PerCta = 32 * kWarps;  // 16-bit rows per CTA (one 32-row batch per warp)
 constexpr float kNeg = -1e30f;  // finite "minus infinity": keeps max/rescale arithmetic NaN-free
 constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pad, o[128]
@@ -66,6 +70,26 @@ struct AttnArgs {
 __device__ __forceinline__ uint32_t bit_pair(uint32_t w, uint32_t ws, int r, uint32_t v) {
   if (r <= 10) return (w & ((1u << r) | (1u << (r + 16)))) * (v >> r);
   return (ws & ((1u << (r - 5)) | (1u << (r + 11)))) * (v >> (r - 5));
+}
+
+// Bits r and r+16 of w as an f16x2 pair {0, 2^bit_exp(r)} with a single AND:
+// the word is pre-rotated so that the two bits sit on one fp16 exponent bit
+// (positions 10..14 of each half), r5/r10/r31 = w rotated left by 5/10/31.
+// The power of two is undone per channel on the accumulator at the end.
+__device__ __forceinline__ uint32_t bit_pair_exp(uint32_t w, uint32_t r5, uint32_t r10, uint32_t r31, int r) {
+  if (r >= 10 && r <= 14) return w & ((1u << r) | (1u << (r + 16)));
+  if (r >= 5 && r <= 9) return r5 & ((1u << (r + 5)) | (1u << (r + 21)));
+  if (r <= 4) return r10 & ((1u << (r + 10)) | (1u << (r + 26)));
+  return r31 & ((1u << 14) | (1u << 30));
+}
+// fp16 exponent position of bit r after the rotation, and the factor that
+// maps the accumulated 2^e * x back to x.
+__host__ __device__ constexpr int bit_pos(int r) {
+  return (r >= 10 && r <= 14) ? r : (r >= 5 && r <= 9) ? r + 5 : (r <= 4) ? r + 10 : 14;
+}
+__host__ __device__ constexpr float bit_comp(int r) {
+  return bit_pos(r) == 10 ? 16384.f : bit_pos(r) == 11 ? 8192.f : bit_pos(r) == 12 ? 2048.f
+         : bit_pos(r) == 13 ? 128.f : 0.5f;
 }
 
 // fp16 high part of two floats (truncated to 11 significant bits, exact in
@@ -105,6 +129,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
   constexpr int VCODES = KMETA + 512;
   constexpr int VMETA = VCODES + 512 * BITS;
   constexpr int STAGE = RB + 16;  // a record plus its bitmap word
+  constexpr int kStages = Stages<BITS>::value;
   constexpr int WARP_BYTES = kStages * STAGE + kZsBytes;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -289,17 +314,13 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
       }
 
     // ---- PV: two 16-token chunks; A = value bits, B = p o s ----
-    uint32_t vw[4], vwh[4], vw1[4], vwh1[4];
+    uint32_t vw[4], vw1[4];
     {
       const uint4 v0 = *reinterpret_cast<const uint4*>(R + VCODES + 16 * lane);
       vw[0] = v0.x; vw[1] = v0.y; vw[2] = v0.z; vw[3] = v0.w;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) vwh[j] = vw[j] >> 5;
       if (BITS == 2) {
         const uint4 v1 = *reinterpret_cast<const uint4*>(R + VCODES + 512 + 16 * lane);
         vw1[0] = v1.x; vw1[1] = v1.y; vw1[2] = v1.z; vw1[3] = v1.w;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) vwh1[j] = vw1[j] >> 5;
       }
     }
 #pragma unroll
@@ -327,26 +348,51 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
         x = f2_mul(p01, make_float2(ss[0].w, ss[1].w)); bfr[3][0] = pack_f16x2(x.x, x.y);
         x = f2_mul(p23, make_float2(ss[2].w, ss[3].w)); bfr[3][1] = pack_f16x2(x.x, x.y);
       }
-      const uint32_t wa = vw[2 * c16], wah = vwh[2 * c16], wb = vw[2 * c16 + 1], wbh = vwh[2 * c16 + 1];
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const uint32_t af[4] = {bit_pair(wa, wah, 2 * mt, 0x3C00u), bit_pair(wa, wah, 2 * mt + 1, 0x3C00u),
-                                bit_pair(wb, wbh, 2 * mt, 0x3C00u), bit_pair(wb, wbh, 2 * mt + 1, 0x3C00u)};
-        mma_16816(oacc[mt], af, bfr[mt >> 1][0], bfr[mt >> 1][1]);
-      }
-      if (BITS == 2) {
-        const uint32_t xa = vw1[2 * c16], xah = vwh1[2 * c16], xb = vw1[2 * c16 + 1], xbh = vwh1[2 * c16 + 1];
+      {
+        const uint32_t wa = vw[2 * c16], wb = vw[2 * c16 + 1];
+        const uint32_t a5 = __funnelshift_l(wa, wa, 5), a10 = __funnelshift_l(wa, wa, 10),
+                       a31 = __funnelshift_l(wa, wa, 31);
+        const uint32_t b5 = __funnelshift_l(wb, wb, 5), b10 = __funnelshift_l(wb, wb, 10),
+                       b31 = __funnelshift_l(wb, wb, 31);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t af[4] = {bit_pair(xa, xah, 2 * mt, 0x4000u), bit_pair(xa, xah, 2 * mt + 1, 0x4000u),
-                                  bit_pair(xb, xbh, 2 * mt, 0x4000u), bit_pair(xb, xbh, 2 * mt + 1, 0x4000u)};
+          const uint32_t af[4] = {bit_pair_exp(wa, a5, a10, a31, 2 * mt), bit_pair_exp(wa, a5, a10, a31, 2 * mt + 1),
+                                  bit_pair_exp(wb, b5, b10, b31, 2 * mt), bit_pair_exp(wb, b5, b10, b31, 2 * mt + 1)};
           mma_16816(oacc[mt], af, bfr[mt >> 1][0], bfr[mt >> 1][1]);
+        }
+      }
+      if (BITS == 2) {  // high plane: weight 2, carried by doubling B
+        uint32_t bfr2[4][2];
+#pragma unroll
+        for (int cg = 0; cg < 4; ++cg) {
+          bfr2[cg][0] = hadd2_u32(bfr[cg][0], bfr[cg][0]);
+          bfr2[cg][1] = hadd2_u32(bfr[cg][1], bfr[cg][1]);
+        }
+        const uint32_t xa = vw1[2 * c16], xb = vw1[2 * c16 + 1];
+        const uint32_t a5 = __funnelshift_l(xa, xa, 5), a10 = __funnelshift_l(xa, xa, 10),
+                       a31 = __funnelshift_l(xa, xa, 31);
+        const uint32_t b5 = __funnelshift_l(xb, xb, 5), b10 = __funnelshift_l(xb, xb, 10),
+                       b31 = __funnelshift_l(xb, xb, 31);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const uint32_t af[4] = {bit_pair_exp(xa, a5, a10, a31, 2 * mt), bit_pair_exp(xa, a5, a10, a31, 2 * mt + 1),
+                                  bit_pair_exp(xb, b5, b10, b31, 2 * mt), bit_pair_exp(xb, b5, b10, b31, 2 * mt + 1)};
+          mma_16816(oacc[mt], af, bfr2[mt >> 1][0], bfr2[mt >> 1][1]);
         }
       }
     }
     __syncwarp();
   }
   cp_async_wait<0>();
+  // undo the powers of two of the value-bit expansion, per channel
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    oacc[mt][0] *= bit_comp(2 * mt);
+    oacc[mt][1] *= bit_comp(2 * mt);
+    oacc[mt][2] *= bit_comp(2 * mt + 1);
+    oacc[mt][3] *= bit_comp(2 * mt + 1);
+  }
+  __syncthreads();  // the merge buffer overlaps the stages of every warp
 
   // ---- warp state -> shared memory ----
   l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
@@ -568,8 +614,8 @@ __device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs
 template <int BITS, bool MERGED>
 __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
-  __shared__ CtaMerge merge;
   __shared__ int s_last;
+  CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem + kMergeOffset);
   if ((int)blockIdx.x < a.chunks)
     lowbit_cta<BITS, MERGED>(a, dyn_smem, merge);
   else
@@ -585,7 +631,10 @@ struct AttnPlan {
   int bchunks;
 };
 
-static int attn_smem_bytes(int bits) { return kWarps * (kStages * (1024 * (bits + 1) + 16) + kZsBytes); }
+static int attn_smem_bytes(int bits) {
+  const int stages = bits == 1 ? Stages<1>::value : Stages<2>::value;
+  return kWarps * (stages * (1024 * (bits + 1) + 16) + kZsBytes);
+}
 
 // Resident attention CTAs per SM on the current device (occupancy query,
 // cached per device and bit width).
@@ -653,7 +702,9 @@ size_t attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
 template <int BITS, bool MERGED>
 static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
   const int smem = attn_smem_bytes(BITS);
-  static_assert(kMaxRows * kD * 4 <= kWarps * (kStages * 2064 + kZsBytes), "16-bit-row CTA query tile fits");
+  static_assert(kMergeOffset >= kMaxRows * kD * 4, "16-bit-row CTA query tile lies below the merge buffer");
+  static_assert(kMergeOffset + (int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2064 + kZsBytes),
+                "merge buffer fits in the dynamic shared memory");
   auto* fn = attn_kernel<BITS, MERGED>;
   static unsigned long long configured = 0ull;  // one per <BITS, MERGED> instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);

@@ -108,6 +108,13 @@ __device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
   return f2_unpack(r);
 }
 
+// Packed fp16 addition on the bit patterns of two f16x2 values.
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
