@@ -3,11 +3,10 @@
 
 Workload: one decode step of LLaMA-3-8B's attention over all 32 layers
 (batch 8, 32 query / 8 KV heads, head dim 128, 32K context, 1-bit cache,
-top-1% = 328 fetched rows per KV head).  Per layer, the main stream runs the
-merged two-query attention over C' U C_kappa; a side stream then runs the
-speculative top-k and the gather of the selected bf16 rows from pinned host
-memory, overlapped with the following layers' attention.  A step is captured
-once as a CUDA graph and replayed.
+top-1% = 328 fetched rows per KV head).  Per layer: the merged two-query
+attention over C' U C_kappa, which in the same launch pre-fetches the
+previous layer's newly selected bf16 rows from pinned host memory, then the
+speculative top-k.  A step is captured once as a CUDA graph and replayed.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -35,7 +34,7 @@ WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=
 METRIC = "decode attn steps/s at 32K ctx, 1-bit, top-1% (HBM GB/s and % of peak in roofline)"
 # DRAM bytes (read + write) of one merged-attention launch of this workload, from the ncu capture
 # summarised in profiles/attn_kernel_llama3_8b_32k.md; None once the kernel changes after that capture.
-ATTN_TRAFFIC_BYTES = 168.9e6
+ATTN_TRAFFIC_BYTES = None
 
 
 def parse():
@@ -179,9 +178,6 @@ class DecodeStep:
         self.ws_bytes = spc.spc_attn_workspace_bytes(d, k)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
         self.main = torch.cuda.Stream()
-        self.side = torch.cuda.Stream(priority=-1)
-        self.attn_done = [torch.cuda.Event() for _ in range(layers)]
-        self.gathered = [torch.cuda.Event() for _ in range(layers)]
         self.t0, self.rec = make_timing_event(torch)
         self.attn_ev = [(make_timing_event(torch)[0], make_timing_event(torch)[0]) for _ in range(layers)]
         # pre-decoding step: plain low-bit attention, first top-k and prefetch
@@ -193,27 +189,28 @@ class DecodeStep:
                                     stream=self.main)
                 spc.spc_host_gather(d, self.host[l], N, self.idx[l], k, self.staging[l], stream=self.main)
         torch.cuda.synchronize()
-        self.launches_per_step = layers * 3  # attention (one launch), top-k, gather
+        self.launches_per_step = layers * 2  # attention with the fused pre-fetch, top-k
         self.graph = None
 
     def enqueue(self, timed=False):
+        """One decode step on one stream.  Layer l: the merged attention over
+        C' U C_kappa, carrying the pre-fetch of layer l-1's new selection (layer
+        L-1's for l = 0, from the previous step), then the speculative top-k.
+        The rows fetched during layer l's attention are read by layer l-1's
+        attention of the next step, so the host link works behind the SMs."""
         spc, d, k = self.spc, self.d, self.k
-        main, side = self.main, self.side
-        for l in range(self.L):
+        main, L = self.main, self.L
+        for l in range(L):
+            j = (l - 1) % L  # the layer whose selection is pre-fetched now
             if timed:
                 self.rec(self.attn_ev[l][0], main)
-            spc.spc_merged_attn(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
-                                self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws, self.ws_bytes,
-                                stream=main)
+            spc.spc_merged_attn_fetch(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
+                                      self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws,
+                                      self.host[j], self.W["N"], self.idx[j], k, self.staging[j],
+                                      ws_bytes=self.ws_bytes, stream=main)
             if timed:
                 self.rec(self.attn_ev[l][1], main)
-            self.attn_done[l].record(main)
-            side.wait_event(self.attn_done[l])
-            spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=side)
-            spc.spc_host_gather(d, self.host[l], self.W["N"], self.idx[l], k, self.staging[l], stream=side)
-            self.gathered[l].record(side)
-        for l in range(self.L):
-            main.wait_event(self.gathered[l])
+            spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=main)
 
     def capture(self):
         torch = self.torch
@@ -274,12 +271,14 @@ def host_link_probe(step, reps=20):
 
 
 def attention_bytes_per_layer(W, nq):
-    """Algorithmic HBM bytes of one merged-attention call (one layer)."""
+    """Algorithmic HBM bytes of one merged-attention call (one layer): the
+    low-bit copy, the residual and fetched 16-bit rows read, q read and o
+    written, plus the HBM writes of the pre-fetched rows it carries."""
     beta = 64 if W["bits"] == 1 else 96
     bh = W["B"] * W["Hkv"]
     r = W["N"] - nq
     qo = W["B"] * 2 * W["Hq"] * 128 * 2 * 2  # q read + o written
-    return bh * (nq * beta + r * 512 + W["k"] * 512) + qo
+    return bh * (nq * beta + r * 512 + W["k"] * 512) + qo + bh * W["k"] * 512
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -429,7 +428,8 @@ def main():
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "traffic": ATTN_TRAFFIC_BYTES,
             "traffic_source": "dram read+write of one launch, profiles/attn_kernel_llama3_8b_32k.md",
-            "kernel": "spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer",
+            "kernel": "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, previous layer's pre-fetch "
+                      "riding along), one layer",
             "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
             "step_hbm_gbs": bytes_layer * W["layers"] / (ms_per_step / 1000.0) / 1e9}
@@ -442,7 +442,7 @@ def main():
             "config": {"workload": W["workload"], "layers": W["layers"], "batch": W["B"], "context": W["N"],
                        "bits": W["bits"], "k": W["k"], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (4.3 GB low-bit cache per step, 129 MB L2); no flush",
-                       "graph": "one CUDA graph per step, main + side stream"},
+                       "graph": "one CUDA graph per step; pre-fetch fused into the next layer's attention"},
             "roofline": roof, "gather": gather, "clocks": clk.summary(), "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps}
     if rank == 0 and not args.no_cpu_baseline:

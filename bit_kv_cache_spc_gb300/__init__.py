@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "Dims", "SpcError", "spc_abi_version", "spc_num_quantized", "spc_records_bytes", "spc_resid_bytes",
     "spc_quantize_kv", "spc_attn_workspace_bytes", "spc_decode_attn2", "spc_merged_attn", "spc_topk_select",
-    "spc_host_gather", "spc_merged_attn_noalloc", "lib_path",
+    "spc_host_gather", "spc_merged_attn_noalloc", "spc_merged_attn_fetch", "lib_path",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +74,8 @@ _sig = {
     "spc_decode_attn2": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
     "spc_merged_attn": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
     "spc_merged_attn_noalloc": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P]),
+    "spc_merged_attn_fetch": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P,
+                                        C.c_int64, _P, C.c_int32, _P, _P]),
     "spc_topk_select": (C.c_int, [_D, _P, _P, C.c_int32, _P, _P, _P]),
     "spc_host_gather": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, C.c_int32, _P]),
 }
@@ -142,6 +144,16 @@ def spc_merged_attn(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_
     _check("spc_merged_attn", _lib.spc_merged_attn(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(idx),
                                                    _ptr(bitmap), _ptr(staging), int(k), _ptr(o), _ptr(lse),
                                                    _ptr(spec_logits), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def spc_merged_attn_fetch(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, fetch_host_kv,
+                          fetch_n_cap, fetch_idx, fetch_k, fetch_staging, ws_bytes=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("spc_merged_attn_fetch",
+           _lib.spc_merged_attn_fetch(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(idx), _ptr(bitmap),
+                                      _ptr(staging), int(k), _ptr(o), _ptr(lse), _ptr(spec_logits), _ptr(ws),
+                                      ws_bytes, _ptr(fetch_host_kv), int(fetch_n_cap), _ptr(fetch_idx),
+                                      int(fetch_k), _ptr(fetch_staging), _stream(stream)))
 
 
 def spc_merged_attn_noalloc(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, stream=None):

@@ -4,10 +4,10 @@
 // low-bit copies, plus the bf16 residual window.
 //
 // One launch per call, split-K over tokens (flash-decoding style):
-//   * grid (chunks + bchunks, B*Hkv).  CTAs 0..chunks-1 of a (b, hkv) scan
-//     32-token groups of C'; CTAs chunks.. handle the 16-bit rows (residual
-//     window first, then the fetched rows), 128 rows per CTA.
-//   * every CTA merges its four warps and writes one partial (running max,
+//   * grid (chunks, B*Hkv).  Each CTA scans a range of 32-token groups of C',
+//     then its warps take their share of the 16-bit rows (residual window
+//     first, then the fetched rows) in 32-row batches spread over all CTAs.
+//   * every CTA merges its warps' states and writes one partial (running max,
 //     sum, unnormalised output) per query row to the workspace; the last CTA
 //     of a (b, hkv) to finish (an atomic ticket) merges the partials into the
 //     bf16 output and the log-sum-exp, and re-zeroes the ticket.
@@ -36,8 +36,8 @@ template <int BITS>
 struct Stages {
   static constexpr int value = BITS == 1 ? 4 : 3;  // cp.async pipeline depth per warp
 };
-constexpr int kMergeOffset = 4096;  // CTA merge buffer in dynamic smem, after the 16-bit CTA's query tile
-constexpr int kRows16PerCta = 32 * kWarps;  // 16-bit rows per CTA (one 32-row batch per warp)
+constexpr int kMergeOffset = 4096;  // CTA merge buffer in dynamic smem, after the 16-bit rows' query tile
+constexpr int kSlots = 2 * kWarps;  // merge slots: each warp's low-bit state, then its 16-bit-row state
 constexpr float kNeg = -1e30f;  // finite "minus infinity": keeps max/rescale arithmetic NaN-free
 constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pad, o[128]
 constexpr int kZsPitch = 17;     // float4s per t block of a z/s table (16 + 1 pad)
@@ -52,15 +52,22 @@ struct AttnArgs {
   const uint32_t* bitmap;
   const uint16_t* staging;
   float* spec_logits;
-  float* part;          // [BH][chunks + bchunks][kMaxRows][kPartStride]
+  float* part;          // [BH][chunks][kMaxRows][kPartStride]
   uint32_t* tickets;    // [BH], zero between calls
   uint16_t* out;        // [B][2][Hq][D]
   float* lse;           // [B][2][Hq] or null
   int32_t k;
   int32_t Hq, Hkv, G, nq, r, q_groups_cap, resid_cap;
-  int32_t chunks, groups_per_chunk, bchunks;
+  int32_t chunks, groups_per_chunk;
   int32_t Lcap;
   float qscale;  // softmax scale * log2(e)
+  // Pre-fetch riding on this launch (spc_merged_attn_fetch): rows pf_idx of
+  // the mapped host cache pf_host go to pf_staging; pf_rows = B*Hkv*pf_k.
+  const uint16_t* pf_host;  // device address of [B][Hkv][pf_ncap][2][D] bf16, or null
+  const int32_t* pf_idx;    // [B][Hkv][pf_k]
+  uint16_t* pf_staging;     // [B][Hkv][pf_k][2][D]
+  int64_t pf_ncap;
+  int32_t pf_k, pf_rows;
 };
 
 // Bits r and r+16 of w as an f16x2 pair, each 0 or the fp16 pattern v (1.0
@@ -116,9 +123,9 @@ __device__ __forceinline__ void dequant_params(uint32_t mm, float& z, float& s) 
 }
 
 struct CtaMerge {
-  float m[kWarps][kMaxRows];
-  float l[kWarps][kMaxRows];
-  float o[kWarps][kMaxRows][kMergePitch];
+  float m[kSlots][kMaxRows];
+  float l[kSlots][kMaxRows];
+  float o[kSlots][kMaxRows][kMergePitch];
 };
 
 // ------------------------------------------------------------ low-bit CTA
@@ -128,7 +135,9 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
   constexpr int KMETA = 512 * BITS;
   constexpr int VCODES = KMETA + 512;
   constexpr int VMETA = VCODES + 512 * BITS;
-  constexpr int STAGE = RB + 16;  // a record plus its bitmap word
+  // a stage: the record, a 16-byte slot (bitmap word, pre-fetch position), a pre-fetched 16-bit row
+  constexpr int PFROW = RB + 16;
+  constexpr int STAGE = PFROW + 512;
   constexpr int kStages = Stages<BITS>::value;
   constexpr int WARP_BYTES = kStages * STAGE + kZsBytes;
 
@@ -167,6 +176,16 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
   const int n_my = (g_end - g_begin - warp + kWarps - 1) / kWarps;  // groups of this warp
   const uint8_t* rec_base = a.records + (bh * a.q_groups_cap) * (int64_t)RB;
 
+  // Pre-fetch rows of this warp: rr = slot + n_slots * i, carried by every
+  // pf_every-th item (one 512-byte row per carried item), the rest copied
+  // after the groups.
+  const int64_t n_slots = (int64_t)gridDim.x * gridDim.y * kWarps;
+  const int64_t slot = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kWarps + warp;
+  const int n_pf = (a.pf_host != nullptr && a.pf_rows > slot) ? (int)((a.pf_rows - slot + n_slots - 1) / n_slots) : 0;
+  const int pf_every = n_pf > 0 ? max(1, n_my / n_pf) : 1;
+  const int pf_carried = n_pf > 0 ? min(n_pf, (n_my + pf_every - 1) / pf_every) : 0;
+  int pf_next = n_pf > 0 ? a.pf_idx[slot] : -1;  // position of the next row to issue
+
   auto issue = [&](int item) {
     if (item < n_my) {
       const int g = g_begin + warp + item * kWarps;
@@ -175,6 +194,17 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
 #pragma unroll
       for (int u = 0; u < RB / 512; ++u) cp_async16(dst + 16 * (lane + 32 * u), src + 16 * (lane + 32 * u));
       if (MERGED && lane == 0) cp_async4(dst + RB, a.bitmap + bh * a.q_groups_cap + g);
+      if (item % pf_every == 0 && item / pf_every < pf_carried) {
+        const int i = item / pf_every;
+        const int64_t rr = slot + n_slots * i;
+        const int n = pf_next;
+        if (lane == 0) reinterpret_cast<int*>(dst + RB)[1] = n;
+        if (n >= 0 && n < a.pf_ncap) {
+          const int64_t src_row = ((rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
+          cp_async16(dst + PFROW + 16 * lane, a.pf_host + src_row + 8 * lane);
+        }
+        pf_next = (i + 1 < n_pf) ? a.pf_idx[rr + n_slots] : -1;
+      }
     }
     cp_async_commit();
   };
@@ -198,6 +228,14 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     __syncwarp();
     const uint8_t* R = stage + (it % kStages) * STAGE;
     const int g = g_begin + warp + it * kWarps;
+    if (it % pf_every == 0 && it / pf_every < pf_carried) {
+      const int n = reinterpret_cast<const int*>(R + RB)[1];
+      if (n >= 0 && n < a.pf_ncap) {
+        const int64_t rr = slot + n_slots * (it / pf_every);
+        reinterpret_cast<uint4*>(a.pf_staging + rr * (2 * kD))[lane] =
+            reinterpret_cast<const uint4*>(R + PFROW)[lane];
+      }
+    }
 
     // ---- z, s of the group's 128 key groups and 128 value groups, 4 + 4 per lane ----
     {
@@ -384,6 +422,16 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     __syncwarp();
   }
   cp_async_wait<0>();
+  // pre-fetch rows this warp's groups did not carry
+  for (int i = pf_carried; i < n_pf; ++i) {
+    const int64_t rr = slot + n_slots * i;
+    const int n = a.pf_idx[rr];
+    if (n >= 0 && n < a.pf_ncap) {
+      const int64_t src_row = ((rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
+      reinterpret_cast<uint4*>(a.pf_staging + rr * (2 * kD))[lane] =
+          reinterpret_cast<const uint4*>(a.pf_host + src_row)[lane];
+    }
+  }
   // undo the powers of two of the value-bit expansion, per channel
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
@@ -423,10 +471,12 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     for (int q8 = 0; q8 < 8; ++q8) merge.o[warp][gid][32 * cg + 8 * t + q8] += zacc[cg];
 }
 
-// ------------------------------------------------------------ 16-bit-row CTA
+// ------------------------------------------------------------ 16-bit rows
 // The residual window and the fetched rows on CUDA cores: one row per lane
-// for the logits, four channels per lane for the value product.
-__device__ __forceinline__ void rows16_cta(const AttnArgs& a, uint8_t* dyn, CtaMerge& merge) {
+// for the logits, four channels per lane for the value product.  Runs in
+// every CTA after its low-bit groups (the stage buffers are free by then);
+// 32-row batch bt goes to CTA bt % chunks, warp (bt / chunks) % kWarps.
+__device__ __forceinline__ void rows16_phase(const AttnArgs& a, uint8_t* dyn, CtaMerge& merge) {
   float (*qs)[kD] = reinterpret_cast<float (*)[kD]>(dyn);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t bh = blockIdx.y;
@@ -452,8 +502,8 @@ __device__ __forceinline__ void rows16_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     l_run[rho] = 0.f;
     o[rho][0] = o[rho][1] = o[rho][2] = o[rho][3] = 0.f;
   }
-  const int first = (blockIdx.x - a.chunks) * kWarps + warp;
-  for (int bt = first; bt < n_batches; bt += a.bchunks * kWarps) {
+  const int first = blockIdx.x + a.chunks * warp;
+  for (int bt = first; bt < n_batches; bt += a.chunks * kWarps) {
     const int j = 32 * bt + lane;  // this lane's row for the logits
     const uint16_t* row = nullptr;
     int pos = -1;                   // quantised position of a fetched row
@@ -548,13 +598,13 @@ __device__ __forceinline__ void rows16_cta(const AttnArgs& a, uint8_t* dyn, CtaM
         mv = m_run[rho];
         lv = l_run[rho];
       }
-    merge.m[warp][lane] = mv;
-    merge.l[warp][lane] = lv;
+    merge.m[kWarps + warp][lane] = mv;
+    merge.l[kWarps + warp][lane] = lv;
   }
 #pragma unroll
   for (int rho = 0; rho < kMaxRows; ++rho)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) merge.o[warp][rho][4 * lane + e] = o[rho][e];
+    for (int e = 0; e < 4; ++e) merge.o[kWarps + warp][rho][4 * lane + e] = o[rho][e];
 }
 
 // ------------------------------------------------------------ merge + combine
@@ -563,15 +613,15 @@ __device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs
   const int c = threadIdx.x;  // channel
   const int64_t bh = blockIdx.y;
   const int rows = 2 * a.G;
-  const int nparts = a.chunks + a.bchunks;
+  const int nparts = a.chunks;
   float* part = a.part + ((bh * nparts + blockIdx.x) * kMaxRows) * kPartStride;
   for (int rho = 0; rho < rows; ++rho) {
     float M = kNeg;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][rho]);
+    for (int w = 0; w < kSlots; ++w) M = fmaxf(M, sm.m[w][rho]);
     float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kSlots; ++w) {
       const float f = fast_exp2(sm.m[w][rho] - M);
       L += sm.l[w][rho] * f;
       O += sm.o[w][rho][c] * f;
@@ -616,10 +666,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ int s_last;
   CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem + kMergeOffset);
-  if ((int)blockIdx.x < a.chunks)
-    lowbit_cta<BITS, MERGED>(a, dyn_smem, merge);
-  else
-    rows16_cta(a, dyn_smem, merge);
+  lowbit_cta<BITS, MERGED>(a, dyn_smem, merge);
+  rows16_phase(a, dyn_smem, merge);
   merge_store_combine(merge, a, &s_last);
 }
 
@@ -628,12 +676,11 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
 struct AttnPlan {
   int chunks;
   int groups_per_chunk;
-  int bchunks;
 };
 
 static int attn_smem_bytes(int bits) {
   const int stages = bits == 1 ? Stages<1>::value : Stages<2>::value;
-  return kWarps * (stages * (1024 * (bits + 1) + 16) + kZsBytes);
+  return kWarps * (stages * (1024 * (bits + 1) + 16 + 512) + kZsBytes);
 }
 
 // Resident attention CTAs per SM on the current device (occupancy query,
@@ -667,26 +714,23 @@ static int resident_ctas(int bits) {
 }
 
 static AttnPlan attn_plan(const spc_dims* d, int32_t k) {
+  (void)k;  // the 16-bit rows ride on the same CTAs, whatever their number
   const int ng = num_quantized(d->N, d->R) / kGroup;
-  const int r = d->N - num_quantized(d->N, d->R);
   const int64_t BH = (int64_t)d->B * d->Hkv;
-  AttnPlan p{0, 1, 0};
-  const int rows16 = r + std::max(k, 0);
-  p.bchunks = (rows16 + 2 * kRows16PerCta - 1) / (2 * kRows16PerCta);  // two 32-row batches per warp
+  AttnPlan p{1, 1};
   if (ng > 0) {
-    // one wave: the low-bit chunks fill the resident slots the 16-bit CTAs leave
+    // one wave of resident CTAs, at least four groups (one per warp) each
     const int64_t slots = (int64_t)spc_host::sm_count() * resident_ctas(d->bits);
-    int64_t chunks = std::max<int64_t>(1, slots / BH - p.bchunks);
+    int64_t chunks = std::max<int64_t>(1, slots / BH);
     chunks = std::min<int64_t>(chunks, (ng + kWarps - 1) / kWarps);
     p.groups_per_chunk = (int)((ng + chunks - 1) / chunks);
     p.chunks = (ng + p.groups_per_chunk - 1) / p.groups_per_chunk;
   }
-  if (p.chunks + p.bchunks == 0) p.bchunks = 1;  // N = 0: one CTA writes the empty result
   return p;
 }
 
 static size_t part_floats(const spc_dims* d, const AttnPlan& p) {
-  return (size_t)d->B * d->Hkv * (p.chunks + p.bchunks) * kMaxRows * kPartStride;
+  return (size_t)d->B * d->Hkv * p.chunks * kMaxRows * kPartStride;
 }
 
 // Workspace: the per-(b, hkv) tickets first (a fixed place, whatever k is),
@@ -703,20 +747,20 @@ template <int BITS, bool MERGED>
 static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
   const int smem = attn_smem_bytes(BITS);
   static_assert(kMergeOffset >= kMaxRows * kD * 4, "16-bit-row CTA query tile lies below the merge buffer");
-  static_assert(kMergeOffset + (int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2064 + kZsBytes),
+  static_assert(kMergeOffset + (int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
                 "merge buffer fits in the dynamic shared memory");
   auto* fn = attn_kernel<BITS, MERGED>;
   static unsigned long long configured = 0ull;  // one per <BITS, MERGED> instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
   if (e != cudaSuccess) return e;
-  fn<<<dim3(a.chunks + a.bchunks, (unsigned)BH), kThreads, smem, stream>>>(a);
+  fn<<<dim3(a.chunks, (unsigned)BH), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
 spc_status launch_attention(const spc_dims* d, const void* records, const uint16_t* resid,
                             const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
                             const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
-                            float* spec_logits, void* ws, cudaStream_t stream) {
+                            float* spec_logits, void* ws, cudaStream_t stream, const PrefetchJob* pf) {
   const AttnPlan plan = attn_plan(d, k);
   AttnArgs a;
   a.records = static_cast<const uint8_t*>(records);
@@ -740,9 +784,14 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.resid_cap = d->resid_cap;
   a.chunks = plan.chunks;
   a.groups_per_chunk = plan.groups_per_chunk;
-  a.bchunks = plan.bchunks;
   a.Lcap = d->q_groups_cap * kGroup;
   a.qscale = d->scale * 1.4426950408889634f;
+  a.pf_host = pf ? pf->host_dev : nullptr;
+  a.pf_idx = pf ? pf->idx : nullptr;
+  a.pf_staging = pf ? pf->staging : nullptr;
+  a.pf_ncap = pf ? pf->n_cap : 0;
+  a.pf_k = pf ? pf->k : 0;
+  a.pf_rows = pf ? (int32_t)((int64_t)d->B * d->Hkv * pf->k) : 0;
   const int64_t BH = (int64_t)d->B * d->Hkv;
   const bool merged = k > 0;
   cudaError_t e;

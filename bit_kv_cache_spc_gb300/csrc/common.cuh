@@ -123,6 +123,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 }  // namespace spc
 
+namespace spc {
+// A Pre-fetch job carried by an attention launch: rows idx of the mapped host
+// cache host_dev ([B][Hkv][n_cap][2][D] bf16) into staging ([B][Hkv][k][2][D]).
+struct PrefetchJob {
+  const uint16_t* host_dev;
+  int64_t n_cap;
+  const int32_t* idx;
+  int32_t k;
+  uint16_t* staging;
+};
+}  // namespace spc
+
 // Host-side helpers shared by the entry points.
 namespace spc_host {
 

@@ -11,7 +11,7 @@ spc_status launch_quantize(const spc_dims*, const uint16_t*, const uint16_t*, vo
 size_t attn_workspace_bytes(const spc_dims*, int32_t);
 spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const uint16_t*, const int32_t*,
                             const uint32_t*, const uint16_t*, int32_t, uint16_t*, float*, float*, void*,
-                            cudaStream_t);
+                            cudaStream_t, const PrefetchJob*);
 spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t);
 spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
                               int32_t, cudaStream_t);
@@ -69,10 +69,23 @@ spc_status check_dims(const spc_dims* d) {
   return SPC_OK;
 }
 
+// Device address of a pinned, mapped host buffer, or SPC_ERR_NOT_MAPPED.
+spc_status mapped_device_pointer(const void* host, const void** dev) {
+  cudaPointerAttributes attr;
+  const cudaError_t e = cudaPointerGetAttributes(&attr, host);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // the failed query leaves no sticky error; clear it
+    return SPC_ERR_NOT_MAPPED;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return SPC_ERR_NOT_MAPPED;
+  *dev = attr.devicePointer;
+  return SPC_OK;
+}
+
 spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
                        const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
                        uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
-                       spc_stream stream) {
+                       spc_stream stream, const spc::PrefetchJob* pf = nullptr) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
   const int32_t nq = spc::num_quantized(d->N, d->R);
@@ -89,7 +102,7 @@ spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* r
   if (ws_bytes < spc::attn_workspace_bytes(d, k)) return SPC_ERR_WORKSPACE;
   return spc::launch_attention(d, records, resid, q, k > 0 ? idx : nullptr, k > 0 ? bitmap : nullptr,
                                k > 0 ? staging : nullptr, k, o, lse, spec_logits, ws,
-                               reinterpret_cast<cudaStream_t>(stream));
+                               reinterpret_cast<cudaStream_t>(stream), pf);
 }
 
 }  // namespace
@@ -158,6 +171,27 @@ spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_
   return attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream);
 }
 
+spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const uint16_t* resid,
+                                 const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
+                                 const uint16_t* staging, int32_t k, uint16_t* o, float* lse, float* spec_logits,
+                                 void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv, int64_t fetch_n_cap,
+                                 const int32_t* fetch_idx, int32_t fetch_k, uint16_t* fetch_staging,
+                                 spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  if (fetch_k < 0 || fetch_k > (1 << 24) || fetch_n_cap < 0) return SPC_ERR_INVALID;
+  if (fetch_k == 0)
+    return attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream);
+  if (fetch_host_kv == nullptr || fetch_idx == nullptr || fetch_staging == nullptr) return SPC_ERR_INVALID;
+  if (!aligned16(fetch_host_kv) || !aligned16(fetch_staging)) return SPC_ERR_INVALID;
+  const void* dev = nullptr;
+  st = mapped_device_pointer(fetch_host_kv, &dev);
+  if (st != SPC_OK) return st;
+  spc::PrefetchJob job{static_cast<const uint16_t*>(dev), fetch_n_cap, fetch_idx, fetch_k, fetch_staging};
+  return attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream,
+                     &job);
+}
+
 spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse, int32_t k,
                            int32_t* idx, uint32_t* bitmap, spc_stream stream) {
   spc_status st = check_dims(d);
@@ -179,15 +213,11 @@ spc_status spc_host_gather(const spc_dims* d, const uint16_t* host_kv, int64_t n
   if (k == 0) return SPC_OK;
   if (host_kv == nullptr || idx == nullptr || staging == nullptr) return SPC_ERR_INVALID;
   if (!aligned16(host_kv) || !aligned16(staging)) return SPC_ERR_INVALID;
-  cudaPointerAttributes attr;
-  cudaError_t e = cudaPointerGetAttributes(&attr, host_kv);
-  if (e != cudaSuccess) {
-    cudaGetLastError();  // clear the sticky-free error of the query
-    return SPC_ERR_NOT_MAPPED;
-  }
-  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return SPC_ERR_NOT_MAPPED;
-  return spc::launch_host_gather(d, static_cast<const uint16_t*>(attr.devicePointer), n_cap, idx, k, staging,
-                                 max_ctas, reinterpret_cast<cudaStream_t>(stream));
+  const void* dev = nullptr;
+  st = mapped_device_pointer(host_kv, &dev);
+  if (st != SPC_OK) return st;
+  return spc::launch_host_gather(d, static_cast<const uint16_t*>(dev), n_cap, idx, k, staging, max_ctas,
+                                 reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -3,14 +3,16 @@
 // speculative-token attention probability, summed over the G query heads of
 // the KV head.
 //
-// One thread-block cluster per (b, hkv) row.  Each CTA of the cluster turns
-// its slice of the row into scores S(n) = sum_h exp(l_h(n) - lse_h) held in
-// shared memory as uint32 bit patterns (S >= 0, so integer order is float
-// order), then the cluster runs an MSB-first radix select (4 passes of 8 bits)
-// for the k-th largest key, summing the CTAs' histograms through distributed
-// shared memory.  A final ordered compaction writes the selected positions in
-// ascending order (ties at the threshold go to the lower position) and the
-// selection bitmap.
+// One thread-block cluster (up to 8 CTAs) per (b, hkv) row.  Each CTA turns
+// its slice of the row into scores S(n) = sum_h 2^(log2e * (l_h(n) - lse_h))
+// held in shared memory as uint32 bit patterns (S >= 0, so integer order is
+// float order).  The cluster then runs an MSB-first radix select (4 passes of
+// 8 bits) for the k-th largest key, summing the CTAs' histograms through
+// distributed shared memory.  The ordered compaction works one 32-position
+// word at a time: a warp's ballots give the word's bitmap and the in-word
+// ranks, and one block-wide scan over the words' counts (plus the lower CTAs'
+// totals) gives every selected position its place in the ascending output.
+// Ties at the threshold go to the lower position.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -21,6 +23,7 @@ namespace spc {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkMaxSlice = 32768;  // positions per CTA (one 32-position word per thread)
 
 struct TopkArgs {
   const float* logits;  // [BH][G][Lcap]
@@ -32,16 +35,18 @@ struct TopkArgs {
 };
 
 struct TopkShared {
-  uint32_t hist[2][256];     // this CTA's histogram, double-buffered by pass parity
-  uint32_t total[256];       // cluster-wide histogram of the current pass
-  uint32_t warp_cnt[2][kTopkWarps];
-  uint32_t counts[2];        // this CTA's (> threshold, == threshold) counts
+  uint32_t hist[2][256];  // this CTA's histogram, double-buffered by pass parity
+  uint32_t total[256];    // cluster-wide histogram of the current pass
+  uint32_t wsum[2][kTopkWarps];
+  uint32_t counts[2];     // this CTA's (> threshold, == threshold) counts
   uint32_t prefix, prefix_mask, remaining;
 };
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
-  extern __shared__ __align__(16) uint32_t keys[];
+  extern __shared__ __align__(16) uint32_t keys[];     // [slice]
+  __shared__ uint32_t wgt[kTopkMaxSlice / 32];          // per word: count, then exclusive prefix
+  __shared__ uint32_t weq[kTopkMaxSlice / 32];
   __shared__ TopkShared sh;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -50,17 +55,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   const int64_t bh = blockIdx.y;
   const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
   const int n0 = (int)rank * a.slice;
-  const int len = max(0, min(a.slice, a.nq - n0));
+  const int len = max(0, min(a.slice, a.nq - n0));  // multiple of 32
+  const int nw = len >> 5;
+  constexpr float kLog2e = 1.4426950408889634f;
 
   // ---- scores ----
-  float lse_h[4];
+  float nlse[4];
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi)
-    lse_h[gi] = gi < a.G ? a.lse[((int64_t)b * 2 + 1) * a.Hq + hk * a.G + gi] : 0.f;
+    nlse[gi] = gi < a.G ? -a.lse[((int64_t)b * 2 + 1) * a.Hq + hk * a.G + gi] * kLog2e : 0.f;
   const float* lrow = a.logits + (bh * a.G) * (int64_t)a.Lcap + n0;
   for (int i = tid; i < len; i += kTopkThreads) {
     float s = 0.f;
-    for (int gi = 0; gi < a.G; ++gi) s += expf(lrow[(int64_t)gi * a.Lcap + i] - lse_h[gi]);
+    for (int gi = 0; gi < a.G; ++gi) s += fast_exp2(fmaf(__ldcs(lrow + (int64_t)gi * a.Lcap + i), kLog2e, nlse[gi]));
     keys[i] = __float_as_uint(s);
   }
   if (tid == 0) {
@@ -80,10 +87,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
       const uint32_t prefix = sh.prefix, pmask = sh.prefix_mask;
       for (int i0 = 0; i0 < len; i0 += kTopkThreads) {
         const int i = i0 + tid;
-        const bool in = i < len && ((keys[i < len ? i : 0] ^ prefix) & pmask) == 0u;
+        const uint32_t key = i < len ? keys[i] : 0u;
+        const bool in = i < len && ((key ^ prefix) & pmask) == 0u;
         const uint32_t active = __ballot_sync(0xFFFFFFFFu, in);
         if (in) {
-          const uint32_t bin = (keys[i] >> shift) & 255u;
+          const uint32_t bin = (key >> shift) & 255u;
           const uint32_t peers = __match_any_sync(active, bin);
           if ((int)(__ffs(peers) - 1) == lane) atomicAdd(&sh.hist[buf][bin], (uint32_t)__popc(peers));
         }
@@ -103,14 +111,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
           cnt[e] = sh.total[8 * lane + e];
           own += cnt[e];
         }
-        uint32_t above = 0;  // keys in the bins of higher lanes
-        for (int l2 = 0; l2 < 32; ++l2) {
-          const uint32_t v = __shfl_sync(0xFFFFFFFFu, own, l2);
-          if (l2 > lane) above += v;
+        uint32_t above = own;  // inclusive suffix sum over lanes >= this one
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, above, off);
+          if (lane + off < 32) above += v;
         }
+        above -= own;  // keys in the bins of higher lanes
         const uint32_t rem = sh.remaining;
-        const bool mine = above < rem && rem <= above + own;
-        if (mine) {
+        if (above < rem && rem <= above + own) {
           uint32_t acc = above;
           for (int e = 7; e >= 0; --e) {
             if (acc + cnt[e] >= rem) {
@@ -127,34 +136,60 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
     }
   }
 
-  // ---- ordered compaction ----
+  // ---- ordered compaction, one 32-position word per warp step ----
   const uint32_t T = sh.prefix;
   const uint32_t need = sh.remaining;  // keys == T to take, lowest positions first
   const bool any = a.keff > 0;
-  uint32_t my_gt = 0, my_eq = 0;
-  if (any) {
-    for (int i = tid; i < len; i += kTopkThreads) {
-      my_gt += keys[i] > T;
-      my_eq += keys[i] == T;
+  for (int w = warp; w < nw; w += kTopkWarps) {
+    const uint32_t key = keys[32 * w + lane];
+    const uint32_t bgt = __ballot_sync(0xFFFFFFFFu, any && key > T);
+    const uint32_t beq = __ballot_sync(0xFFFFFFFFu, any && key == T);
+    if (lane == 0) {
+      wgt[w] = __popc(bgt);
+      weq[w] = __popc(beq);
     }
-  }
-  for (int off = 16; off > 0; off >>= 1) {
-    my_gt += __shfl_xor_sync(0xFFFFFFFFu, my_gt, off);
-    my_eq += __shfl_xor_sync(0xFFFFFFFFu, my_eq, off);
-  }
-  if (lane == 0) {
-    sh.warp_cnt[0][warp] = my_gt;
-    sh.warp_cnt[1][warp] = my_eq;
   }
   __syncthreads();
-  if (tid == 0) {
-    uint32_t g = 0, e = 0;
-    for (int w = 0; w < kTopkWarps; ++w) {
-      g += sh.warp_cnt[0][w];
-      e += sh.warp_cnt[1][w];
+  // exclusive scan of the word counts (one word per thread)
+  {
+    const uint32_t g = tid < nw ? wgt[tid] : 0u, e = tid < nw ? weq[tid] : 0u;
+    uint32_t ig = g, ie = e;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, ig, off), ve = __shfl_up_sync(0xFFFFFFFFu, ie, off);
+      if (lane >= off) {
+        ig += vg;
+        ie += ve;
+      }
     }
-    sh.counts[0] = g;
-    sh.counts[1] = e;
+    if (lane == 31) {
+      sh.wsum[0][warp] = ig;
+      sh.wsum[1][warp] = ie;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t sg = sh.wsum[0][lane], se = sh.wsum[1][lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, sg, off), ve = __shfl_up_sync(0xFFFFFFFFu, se, off);
+        if (lane >= off) {
+          sg += vg;
+          se += ve;
+        }
+      }
+      sh.wsum[0][lane] = sg;  // inclusive over warps
+      sh.wsum[1][lane] = se;
+      if (lane == 31) {
+        sh.counts[0] = sg;
+        sh.counts[1] = se;
+      }
+    }
+    __syncthreads();
+    const uint32_t wg0 = warp > 0 ? sh.wsum[0][warp - 1] : 0u, we0 = warp > 0 ? sh.wsum[1][warp - 1] : 0u;
+    if (tid < nw) {
+      wgt[tid] = wg0 + ig - g;
+      weq[tid] = we0 + ie - e;
+    }
   }
   cluster.sync();
   uint32_t base_gt = 0, base_eq = 0;
@@ -163,43 +198,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
     base_gt += pc[0];
     base_eq += pc[1];
   }
-  __syncthreads();
 
   int32_t* out = a.idx + bh * a.k;
   uint32_t* bm = a.bitmap + bh * a.q_groups_cap;
-  uint32_t run_gt = base_gt, run_eq = base_eq;
-  for (int i0 = 0; i0 < len; i0 += kTopkThreads) {
-    const int i = i0 + tid;
-    const uint32_t key = i < len ? keys[i] : 0u;
-    const bool gt = any && i < len && key > T;
-    const bool eq = any && i < len && key == T;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int w = warp; w < nw; w += kTopkWarps) {
+    const uint32_t key = keys[32 * w + lane];
+    const bool gt = any && key > T, eq = any && key == T;
     const uint32_t bgt = __ballot_sync(0xFFFFFFFFu, gt), beq = __ballot_sync(0xFFFFFFFFu, eq);
-    const uint32_t below = (1u << lane) - 1u;
-    if (lane == 0) {
-      sh.warp_cnt[0][warp] = __popc(bgt);
-      sh.warp_cnt[1][warp] = __popc(beq);
-    }
-    __syncthreads();
-    uint32_t wgt = 0, weq = 0, tgt = 0, teq = 0;
-    for (int w = 0; w < kTopkWarps; ++w) {
-      const uint32_t cg_ = sh.warp_cnt[0][w], ce = sh.warp_cnt[1][w];
-      if (w < warp) {
-        wgt += cg_;
-        weq += ce;
-      }
-      tgt += cg_;
-      teq += ce;
-    }
-    const uint32_t gt_before = run_gt + wgt + __popc(bgt & below);
-    const uint32_t eq_before = run_eq + weq + __popc(beq & below);
+    const uint32_t eq_before = base_eq + weq[w] + __popc(beq & below);
     const bool sel = gt || (eq && eq_before < need);
+    const uint32_t pos = base_gt + wgt[w] + __popc(bgt & below) + min(eq_before, need);
+    if (sel && pos < (uint32_t)a.keff) out[pos] = n0 + 32 * w + lane;
     const uint32_t bsel = __ballot_sync(0xFFFFFFFFu, sel);
-    const uint32_t pos = gt_before + min(eq_before, need);
-    if (sel && pos < (uint32_t)a.keff) out[pos] = n0 + i;
-    if (lane == 0 && i0 + 32 * warp < len) bm[(n0 + i0 + 32 * warp) >> 5] = bsel;
-    run_gt += tgt;
-    run_eq += teq;
-    __syncthreads();
+    if (lane == 0) bm[(n0 >> 5) + w] = bsel;
   }
   if (rank == 0) {
     for (int j = a.keff + tid; j < a.k; j += kTopkThreads) out[j] = -1;
@@ -223,13 +235,14 @@ spc_status launch_topk(const spc_dims* d, const float* logits, const float* lse,
   a.keff = std::min(k, a.nq);
   a.Lcap = d->q_groups_cap * kGroup;
   a.q_groups_cap = d->q_groups_cap;
-  int ncta = std::max(1, std::min(8, (a.nq + 16383) / 16384));
+  // about 8192 positions (8 per thread) per CTA, at most 8 CTAs per cluster
+  const int ncta = std::max(1, std::min(8, (a.nq + 8191) / 8192));
   a.slice = std::max(32, ((a.nq + ncta - 1) / ncta + 31) / 32 * 32);
-  if (a.slice > 32768) return SPC_ERR_UNSUPPORTED;
+  if (a.slice > kTopkMaxSlice) return SPC_ERR_UNSUPPORTED;
   const int64_t BH = (int64_t)d->B * d->Hkv;
   const size_t smem = (size_t)a.slice * sizeof(uint32_t);
   static unsigned long long configured = 0ull;
-  cudaError_t e = spc_host::ensure_smem_limit(configured, topk_kernel, 32768 * (int)sizeof(uint32_t));
+  cudaError_t e = spc_host::ensure_smem_limit(configured, topk_kernel, kTopkMaxSlice * (int)sizeof(uint32_t));
   if (e == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ncta, (unsigned)BH, 1);

@@ -159,6 +159,26 @@ spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_
                            float* spec_logits, void* ws, size_t ws_bytes, spc_stream stream);
 
 /*
+ * Attn([T_t, T'_{t+1}], C' U C_kappa) of one layer together with the
+ * Pre-fetch(C_kappa) of another layer (SpeCache page section 3, Algorithm 3:
+ * the prefetch runs "in parallel with the following layers' computation").
+ * Same as spc_merged_attn, and in the same launch the selected 16-bit rows
+ * fetch_idx ([B][Hkv][fetch_k], same B and Hkv) of the pinned, mapped host
+ * cache fetch_host_kv ([B][Hkv][fetch_n_cap][2][D], HOST pointer) are copied
+ * to fetch_staging ([B][Hkv][fetch_k][2][D]), exactly as spc_host_gather
+ * would.  The copy rides on the attention's own load pipeline, so the host
+ * link works while the SMs compute; the attention's results are unchanged.
+ * fetch_staging must not be the staging buffer this call reads.
+ * fetch_k = 0 is spc_merged_attn.  SPC_ERR_NOT_MAPPED as spc_host_gather.
+ */
+spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const uint16_t* resid,
+                                 const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
+                                 const uint16_t* staging, int32_t k, uint16_t* o, float* lse, float* spec_logits,
+                                 void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv, int64_t fetch_n_cap,
+                                 const int32_t* fetch_idx, int32_t fetch_k, uint16_t* fetch_staging,
+                                 spc_stream stream);
+
+/*
  * spc_merged_attn without a caller-provided workspace.  The SpeCache paper has
  * no counterpart to this call; it exists for callers that cannot allocate
  * device memory (a plug-in running inside a host that owns the device

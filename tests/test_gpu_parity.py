@@ -121,6 +121,41 @@ def test_k0_merged_is_attn2_and_all_fetched_is_bf16_attention():
     assert out_err(b2f(o2.cpu().numpy()), ref.numpy()) <= OUT_TOL
 
 
+@pytest.mark.parametrize("cfg", [dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41),
+                                 dict(B=1, Hq=4, Hkv=4, N=300, R=64, bits=2, k=7),
+                                 dict(B=1, Hq=4, Hkv=1, N=64, R=32, bits=1, k=24)],
+                         ids=["many_groups", "mha_2bit", "rows_exceed_groups"])
+def test_merged_attention_with_fetch_job(cfg):
+    """spc_merged_attn_fetch: the attention results equal spc_merged_attn's and the
+    pre-fetched rows equal the oracle's gather, also when the job has more rows
+    than the launch has groups to carry them."""
+    import bit_kv_cache_spc_gb300 as spc
+    g, d, K, V, q, qz = run_small(cfg, seed=6)
+    k = cfg["k"]
+    o0, lse0, lg0 = g.attn2()
+    idx, bm = g.topk(lg0, lse0, k)
+    g.gather(idx, k)
+    ref_o, ref_lse, ref_lg = g.merged(idx, bm, k)
+    # a job for "another layer": its own cache and selection (different seed), some -1 entries
+    K2, V2 = synth.kv_layer(9, 1, cfg["B"], cfg["Hkv"], cfg["N"])
+    host2 = torch.from_numpy(np.stack([K2, V2], axis=3).view(np.int16)).pin_memory()
+    rng = np.random.default_rng(2)
+    fk = 57
+    fidx = np.sort(rng.choice(cfg["N"], size=(cfg["B"], cfg["Hkv"], fk)), axis=-1).astype(np.int32)
+    fidx[0, 0, 3] = -1
+    fst = torch.zeros((cfg["B"], cfg["Hkv"], fk, 2, 128), dtype=torch.int16, device="cuda")
+    o, lse, lg = g.new_out()
+    spc.spc_merged_attn_fetch(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o, lse, lg, g.ws, host2,
+                              cfg["N"], torch.from_numpy(fidx).cuda(), fk, fst)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    nq = g.nq
+    assert torch.equal(lg[..., :nq], ref_lg[..., :nq])
+    want = oracle.gather(d, np.stack([K2, V2], axis=3), fidx)
+    got = fst.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
 def test_topk_selection_exact_with_ties_across_cluster():
     """Selection alone, on logits whose order is unambiguous in fp32 (spacing
     0.01 in the exponent), with many exact ties, over rows spanning 1..8 CTAs."""
