@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-pairs", type=int, default=16, help="(b, kv-head) pairs in the oracle sample")
+    p.add_argument("--prefetch", choices=["side", "fused"], default="fused",
+                   help="pre-fetch as a small side-stream kernel, or carried by the next layer's attention")
     return p.parse_args()
 
 
@@ -140,7 +142,7 @@ def make_timing_event(torch):
 # ------------------------------------------------------------------ the GPU workload
 
 class DecodeStep:
-    def __init__(self, W, layers, seed=0):
+    def __init__(self, W, layers, seed=0, mode="fused"):
         import torch
 
         import bit_kv_cache_spc_gb300 as spc
@@ -178,6 +180,11 @@ class DecodeStep:
         self.ws_bytes = spc.spc_attn_workspace_bytes(d, k)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
         self.main = torch.cuda.Stream()
+        self.side = torch.cuda.Stream(priority=-1)
+        self.selected = [torch.cuda.Event() for _ in range(layers)]
+        self.gathered = [torch.cuda.Event() for _ in range(layers)]
+        self.mode = mode
+        self.gather_ctas = 32
         self.t0, self.rec = make_timing_event(torch)
         self.attn_ev = [(make_timing_event(torch)[0], make_timing_event(torch)[0]) for _ in range(layers)]
         # pre-decoding step: plain low-bit attention, first top-k and prefetch
@@ -189,10 +196,42 @@ class DecodeStep:
                                     stream=self.main)
                 spc.spc_host_gather(d, self.host[l], N, self.idx[l], k, self.staging[l], stream=self.main)
         torch.cuda.synchronize()
-        self.launches_per_step = layers * 2  # attention with the fused pre-fetch, top-k
+        # attention, top-k, and the gather (its own launch, or riding on the next attention)
+        self.launches_per_step = layers * (3 if mode == "side" else 2)
         self.graph = None
 
     def enqueue(self, timed=False):
+        if self.mode == "fused":
+            return self.enqueue_fused(timed)
+        return self.enqueue_side(timed)
+
+    def enqueue_side(self, timed=False):
+        """One decode step.  Layer l: the merged attention over C' U C_kappa and
+        the speculative top-k on the main stream; the pre-fetch of layer l's new
+        selection on a high-priority side stream with a small persistent grid,
+        so that it shares the SMs with layer l+1's attention while the host link
+        works.  The next step's attention of layer l waits for that pre-fetch."""
+        spc, d, k = self.spc, self.d, self.k
+        main, side, L = self.main, self.side, self.L
+        for l in range(L):
+            main.wait_event(self.gathered[l])
+            if timed:
+                self.rec(self.attn_ev[l][0], main)
+            spc.spc_merged_attn(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
+                                self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws, self.ws_bytes,
+                                stream=main)
+            if timed:
+                self.rec(self.attn_ev[l][1], main)
+            spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=main)
+            self.selected[l].record(main)
+            side.wait_event(self.selected[l])
+            spc.spc_host_gather(d, self.host[l], self.W["N"], self.idx[l], k, self.staging[l],
+                                max_ctas=self.gather_ctas, stream=side)
+            self.gathered[l].record(side)
+        for l in range(L):  # join the side stream before the step ends
+            main.wait_event(self.gathered[l])
+
+    def enqueue_fused(self, timed=False):
         """One decode step on one stream.  Layer l: the merged attention over
         C' U C_kappa, carrying the pre-fetch of layer l-1's new selection (layer
         L-1's for l = 0, from the previous step), then the speculative top-k.
@@ -270,15 +309,15 @@ def host_link_probe(step, reps=20):
             "frac": g_gbs / c_gbs}
 
 
-def attention_bytes_per_layer(W, nq):
+def attention_bytes_per_layer(W, nq, fused=False):
     """Algorithmic HBM bytes of one merged-attention call (one layer): the
     low-bit copy, the residual and fetched 16-bit rows read, q read and o
-    written, plus the HBM writes of the pre-fetched rows it carries."""
+    written, plus (fused pre-fetch) the HBM writes of the rows it carries."""
     beta = 64 if W["bits"] == 1 else 96
     bh = W["B"] * W["Hkv"]
     r = W["N"] - nq
     qo = W["B"] * 2 * W["Hq"] * 128 * 2 * 2  # q read + o written
-    return bh * (nq * beta + r * 512 + W["k"] * 512) + qo + bh * W["k"] * 512
+    return bh * (nq * beta + r * 512 + W["k"] * 512) + qo + (bh * W["k"] * 512 if fused else 0)
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -368,7 +407,7 @@ def main():
         torch.cuda.set_device(0)
     peaks, peak_src = measured_peaks()
 
-    step = DecodeStep(W, args.layers)
+    step = DecodeStep(W, args.layers, mode=args.prefetch)
     step.capture()
     for _ in range(max(3, args.warmup)):
         step.replay()
@@ -422,14 +461,15 @@ def main():
            "d2h_bytes_per_step": d2h}
 
     # ---- roofline of the dominant call (merged attention, one layer per launch) ----
-    bytes_layer = attention_bytes_per_layer(W, step.nq)
+    bytes_layer = attention_bytes_per_layer(W, step.nq, fused=args.prefetch == "fused")
     attn_avg_ms = statistics.mean(per_layer)
     achieved = bytes_layer / (attn_avg_ms / 1000.0) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "traffic": ATTN_TRAFFIC_BYTES,
             "traffic_source": "dram read+write of one launch, profiles/attn_kernel_llama3_8b_32k.md",
-            "kernel": "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, previous layer's pre-fetch "
-                      "riding along), one layer",
+            "kernel": ("spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer" if args.prefetch == "side"
+                       else "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, previous layer's "
+                            "pre-fetch riding along), one layer"),
             "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
             "step_hbm_gbs": bytes_layer * W["layers"] / (ms_per_step / 1000.0) / 1e9}
@@ -442,7 +482,9 @@ def main():
             "config": {"workload": W["workload"], "layers": W["layers"], "batch": W["B"], "context": W["N"],
                        "bits": W["bits"], "k": W["k"], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (4.3 GB low-bit cache per step, 129 MB L2); no flush",
-                       "graph": "one CUDA graph per step; pre-fetch fused into the next layer's attention"},
+                       "graph": "one CUDA graph per step",
+                       "prefetch": ("side stream, 32 persistent CTAs" if args.prefetch == "side"
+                                    else "fused into the next layer's attention")},
             "roofline": roof, "gather": gather, "clocks": clk.summary(), "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps}
     if rank == 0 and not args.no_cpu_baseline:

@@ -2,10 +2,15 @@
 // scale (SpeCache page, section 3, "Original KIVI quantisation" and "Improved
 // 1-bit quantisation"; keys per channel, values per token, groups of 32).
 //
-// One CTA of 128 threads quantises one 32-token group of one (b, hkv) at a
-// time: 8 KB of keys and 8 KB of values in, one 2 KB (1-bit) or 3 KB (2-bit)
-// record out.  The kernel streams HBM: 512 B read and 64/96 B written per
-// token and KV head.
+// One CTA of 128 threads quantises 32-token groups of one (b, hkv) at a time:
+// 8 KB of keys and 8 KB of values in, one 2 KB (1-bit) or 3 KB (2-bit) record
+// out.  The next group's tiles stream in (cp.async, double-buffered) while the
+// current one is coded.  Per group: thread c finds key channel c's min/max and
+// parameters; then one warp per key token (and per value token pair) codes a
+// conflict-free 16-byte block per lane, and one ballot per code word yields
+// the packed word in the record's bit order directly (value groups' min/max
+// come from two xor-shuffles inside the same pass).
+// The kernel streams HBM: 512 B read and 64/96 B written per token and KV head.
 #include "common.cuh"
 
 namespace spc {
@@ -22,17 +27,24 @@ __device__ __forceinline__ void quant_params(int bits, float lo, float hi, float
   }
 }
 
-// clamp(rint(fl((x - z) / s)), 0, cmax), 0 when s == 0.  The product with the
-// correctly rounded reciprocal rs is within 1e-6 of the IEEE quotient for the
-// quotients that occur (|q| <= 3), so it decides every value whose fractional
-// part is farther than 1e-5 from one half; the IEEE division settles the rest.
-__device__ __forceinline__ uint32_t quant_code(float x, float z, float s, float rs, float cmax) {
-  if (s == 0.0f) return 0u;
+// clamp(rint(fl((x - z) / s)), 0, 2^bits - 1), 0 when s == 0 (rs == 0 then).
+// The product with the correctly rounded reciprocal rs is within 1e-6 of the
+// IEEE quotient for the quotients that occur (|q| <= 3), so it decides every
+// value whose quotient is farther than 1e-5 from a rounding boundary k + 1/2;
+// the IEEE division settles the rest.  At 1 bit the code is 1 exactly when
+// the quotient exceeds 1/2 (1/2 itself rounds to even, 0).
+template <int BITS>
+__device__ __forceinline__ uint32_t quant_code(float x, float z, float s, float rs) {
   const float d = __fsub_rn(x, z);
   float t = __fmul_rn(d, rs);
-  const float fr = __fsub_rn(t, floorf(t));
-  if (fabsf(__fsub_rn(fr, 0.5f)) < 1e-5f) t = __fdiv_rn(d, s);
-  return (uint32_t)fminf(fmaxf(rintf(t), 0.0f), cmax);
+  if (BITS == 1) {
+    if (fabsf(__fsub_rn(t, 0.5f)) < 1e-5f && s != 0.0f) t = __fdiv_rn(d, s);
+    return t > 0.5f ? 1u : 0u;
+  } else {
+    const float fr = __fsub_rn(t, floorf(t));
+    if (fabsf(__fsub_rn(fr, 0.5f)) < 1e-5f && s != 0.0f) t = __fdiv_rn(d, s);
+    return (uint32_t)fminf(fmaxf(rintf(t), 0.0f), 3.0f);
+  }
 }
 
 // min/max of bf16 values carried as floats; -0.0 is stored as +0.0.
@@ -44,79 +56,68 @@ struct QuantArgs {
   const uint16_t* k;
   const uint16_t* v;
   uint8_t* records;
-  int32_t Hkv, N, nq, bits, q_groups_cap;
+  int32_t Hkv, N, nq, q_groups_cap;
   int64_t total_groups;  // B * Hkv * (nq / 32)
 };
 
+struct QuantSmem {
+  uint16_t ks[2][kGroup * kD];  // double-buffered tiles, [token][channel]
+  uint16_t vs[2][kGroup * kD];
+  float kz[kD], krs[kD], kss[kD];  // per key channel: z, 1/s, s
+  uint32_t klohi[kD];
+  uint32_t rec[256 * 3];           // the record being assembled (up to 3 KB)
+};
+
+// Token pair p of a group (tokens 2p, 2p+1) is where value code words
+// (a, t = p & 3, j = 2 * (p >> 3) + ((p >> 2) & 1)) take their bits; the
+// (min, max) of token n, channel group cg is value-minmax word 32 t' + m with
+// t' = (n & 7) >> 1, m = 16 (n >> 4) + 4 (2 ((n & 15) >> 3) + (n & 1)) + cg.
+__device__ __forceinline__ int vmeta_word(int n, int cg) {
+  const int n16 = n & 15;
+  return 32 * ((n16 & 7) >> 1) + 16 * (n >> 4) + 4 * (2 * (n16 >> 3) + (n16 & 1)) + cg;
+}
+
+template <int BITS>
 __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
-  __shared__ __align__(16) uint16_t ks[kGroup * kD];
-  __shared__ uint32_t kmask[2][kD];          // [plane][channel]: bit n = token n
-  __shared__ uint32_t klohi[kD];             // [channel]: min | max << 16
-  __shared__ uint32_t vmask[2][kGroup][4];   // [plane][token][cg]: bit j = channel 32cg+j
-  __shared__ uint32_t vlohi[kGroup][4];      // [token][cg]
-
-  const int tid = threadIdx.x;
+  extern __shared__ __align__(16) uint8_t qsmem[];
+  QuantSmem& sm = *reinterpret_cast<QuantSmem*>(qsmem);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ng = a.nq / kGroup;
-  const int bits = a.bits;
-  const float cmax = (float)((1 << bits) - 1);
-  const int64_t rb = record_bytes(bits);
+  constexpr int rb = 1024 * (BITS + 1);
+  constexpr int KMETA = 128 * BITS, VCODES = KMETA + 128, VMETA = VCODES + 128 * BITS;  // in words
 
-  for (int64_t gi = blockIdx.x; gi < a.total_groups; gi += gridDim.x) {
-    const int64_t bh = gi / ng;
-    const int g = (int)(gi % ng);
-    const int64_t row0 = bh * a.N + (int64_t)g * kGroup;  // first token of the group
-    const uint4* ksrc = reinterpret_cast<const uint4*>(a.k + row0 * kD);
-    const uint4* vsrc = reinterpret_cast<const uint4*>(a.v + row0 * kD);
-
-    // ---- load: keys to shared memory, values kept in registers ----
-    uint4 vreg[4];
+  auto load = [&](int64_t gi, int buf) {
+    if (gi < a.total_groups) {
+      const int64_t bh = gi / ng;
+      const int g = (int)(gi % ng);
+      const int64_t row0 = bh * a.N + (int64_t)g * kGroup;
+      const uint8_t* ksrc = reinterpret_cast<const uint8_t*>(a.k + row0 * kD);
+      const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(a.v + row0 * kD);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      reinterpret_cast<uint4*>(ks)[tid + 128 * r] = __ldcs(ksrc + tid + 128 * r);
-      vreg[r] = __ldcs(vsrc + tid + 128 * r);
+      for (int r = 0; r < 4; ++r) {
+        cp_async16(reinterpret_cast<uint8_t*>(sm.ks[buf]) + 16 * (tid + 128 * r), ksrc + 16 * (tid + 128 * r));
+        cp_async16(reinterpret_cast<uint8_t*>(sm.vs[buf]) + 16 * (tid + 128 * r), vsrc + 16 * (tid + 128 * r));
+      }
     }
+    cp_async_commit();
+  };
 
-    // ---- values: group = (token, 32 channels) = 4 consecutive threads ----
-    // thread tid holds, for r = 0..3, token (tid>>4) + 8r, channels
-    // 32*cg + 8*sub .. +7 with cg = (tid&15)>>2, sub = tid&3.
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint32_t w[4] = {vreg[r].x, vreg[r].y, vreg[r].z, vreg[r].w};
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16_to_f32(w[e] & 0xFFFFu);
-        x[2 * e + 1] = bf16_to_f32(w[e] >> 16);
-      }
-      float lo = x[0], hi = x[0];
-#pragma unroll
-      for (int e = 1; e < 8; ++e) {
-        lo = fminf(lo, x[e]);
-        hi = fmaxf(hi, x[e]);
-      }
-#pragma unroll
-      for (int off = 1; off <= 2; off <<= 1) {
-        lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
-        hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
-      }
-      float z, s;
-      quant_params(bits, lo, hi, z, s);
-      const float rs = (s != 0.0f) ? __frcp_rn(s) : 0.0f;
-      uint32_t m0 = 0, m1 = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t c = quant_code(x[e], z, s, rs, cmax);
-        m0 |= (c & 1u) << e;
-        m1 |= ((c >> 1) & 1u) << e;
-      }
-      const int n = (tid >> 4) + 8 * r, cg = (tid & 15) >> 2, sub = tid & 3;
-      reinterpret_cast<uint8_t*>(&vmask[0][n][cg])[sub] = (uint8_t)m0;
-      reinterpret_cast<uint8_t*>(&vmask[1][n][cg])[sub] = (uint8_t)m1;
-      if (sub == 0) vlohi[n][cg] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
-    }
+  // Lane beta's key channels for word t are base + 2t, base = 16 k + 8 h + half
+  // with (half, k, h) = (beta >> 4, (beta >> 1) & 7, beta & 1): all four lie in
+  // the 16-byte block at channel 16 k + 8 h, at halves 2t + half.
+  const int half = lane >> 4, kk = (lane >> 1) & 7, hh = lane & 1;
+  const int kblock = 16 * kk + 8 * hh;
+
+  int buf = 0;
+  load(blockIdx.x, 0);
+  for (int64_t gi = blockIdx.x; gi < a.total_groups; gi += gridDim.x, buf ^= 1) {
+    load(gi + gridDim.x, buf ^ 1);
+    cp_async_wait<1>();
     __syncthreads();
+    const uint16_t* ks = sm.ks[buf];
+    const uint16_t* vs = sm.vs[buf];
 
-    // ---- keys: group = (32 tokens, channel), thread tid = channel ----
+    // ---- key group parameters: thread = channel ----
     {
       const int c = tid;
       float lo = bf16_to_f32(ks[c]), hi = lo;
@@ -127,47 +128,100 @@ __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
         hi = fmaxf(hi, x);
       }
       float z, s;
-      quant_params(bits, lo, hi, z, s);
-      const float rs = (s != 0.0f) ? __frcp_rn(s) : 0.0f;
-      uint32_t m0 = 0, m1 = 0;
-#pragma unroll 8
-      for (int n = 0; n < kGroup; ++n) {
-        const uint32_t code = quant_code(bf16_to_f32(ks[n * kD + c]), z, s, rs, cmax);
-        m0 |= (code & 1u) << n;
-        m1 |= ((code >> 1) & 1u) << n;
-      }
-      kmask[0][c] = m0;
-      kmask[1][c] = m1;
-      klohi[c] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
+      quant_params(BITS, lo, hi, z, s);
+      sm.kz[c] = z;
+      sm.kss[c] = s;
+      sm.krs[c] = s != 0.0f ? __frcp_rn(s) : 0.0f;
+      sm.klohi[c] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
     }
     __syncthreads();
 
-    // ---- scatter into the record layout (spc.h), thread tid = word tid ----
-    uint32_t* rec = reinterpret_cast<uint32_t*>(a.records + (bh * a.q_groups_cap + g) * rb);
-    const int w = tid, L = w >> 2, j = w & 3, aa = L >> 2, t = L & 3;
-    for (int p = 0; p < bits; ++p) {
-      uint32_t kw = 0, vw = 0;
-      const int kn = 8 * j + aa;
+    // ---- key codes: warp per token, one ballot per code word ----
+    {
+      float z[4], s[4], rs[4];
 #pragma unroll
-      for (int b = 0; b < 32; ++b) {
-        const int kc = 16 * ((b & 15) >> 1) + 2 * t + 8 * (b & 1) + (b >> 4);
-        kw |= ((kmask[p][kc] >> kn) & 1u) << b;
-        const int vn = 16 * (j >> 1) + 8 * (j & 1) + 2 * t + (b >> 4);
-        const int vc = 16 * ((b & 15) >> 1) + 8 * (b & 1) + aa;
-        vw |= ((vmask[p][vn][vc >> 5] >> (vc & 31)) & 1u) << b;
+      for (int t = 0; t < 4; ++t) {
+        const int c = kblock + 2 * t + half;
+        z[t] = sm.kz[c];
+        s[t] = sm.kss[c];
+        rs[t] = sm.krs[c];
       }
-      __stcs(rec + 128 * p + w, kw);
-      __stcs(rec + 128 * (bits + 1) + 128 * p + w, vw);
+      for (int n = 8 * warp; n < 8 * warp + 8; ++n) {  // token n = 8 j + a
+        const uint4 blk = *reinterpret_cast<const uint4*>(ks + n * kD + kblock);
+        const uint32_t wv[4] = {blk.x, blk.y, blk.z, blk.w};  // halves 2t, 2t+1 in word t
+        const int j = n >> 3, aa = n & 7;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float x = bf16_to_f32(half ? (wv[t] >> 16) : (wv[t] & 0xFFFFu));
+          const uint32_t code = quant_code<BITS>(x, z[t], s[t], rs[t]);
+          const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, code & 1u);
+          const int word = 4 * (4 * aa + t) + j;
+          if (BITS == 2) {
+            const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, code >> 1);
+            if (lane == 1) sm.rec[128 + word] = b1;
+          }
+          if (lane == 0) sm.rec[word] = b0;
+        }
+      }
+    }
+
+    // ---- value parameters and codes: warp per token pair ----
+    for (int p = 4 * warp; p < 4 * warp + 4; ++p) {
+      const int n = 2 * p + half;  // this lane's token
+      const uint4 blk = *reinterpret_cast<const uint4*>(vs + n * kD + kblock);  // channels kblock .. +7
+      const uint32_t wv[4] = {blk.x, blk.y, blk.z, blk.w};
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = bf16_to_f32(wv[e] & 0xFFFFu);
+        x[2 * e + 1] = bf16_to_f32(wv[e] >> 16);
+      }
+      float lo = x[0], hi = x[0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e) {
+        lo = fminf(lo, x[e]);
+        hi = fmaxf(hi, x[e]);
+      }
+      // the 32-channel group cg = kk >> 1 spans the four lanes that differ in bits 0..1
+#pragma unroll
+      for (int off = 1; off <= 2; off <<= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+        hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+      }
+      float z, s;
+      quant_params(BITS, lo, hi, z, s);
+      const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
+      if ((lane & 3) == 0)
+        sm.rec[VMETA + vmeta_word(n, kk >> 1)] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
+      const int t = p & 3, j = 2 * (p >> 3) + ((p >> 2) & 1);
+#pragma unroll
+      for (int aa = 0; aa < 8; ++aa) {  // channel kblock + aa = 16 k + 8 h + a
+        const uint32_t code = quant_code<BITS>(x[aa], z, s, rs);
+        const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, code & 1u);
+        const int word = 4 * (4 * aa + t) + j;
+        if (BITS == 2) {
+          const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, code >> 1);
+          if (lane == 1) sm.rec[VCODES + 128 + word] = b1;
+        }
+        if (lane == 0) sm.rec[VCODES + word] = b0;
+      }
     }
     {
-      const int tt = w >> 5, m = w & 31;
+      const int tt = tid >> 5, m = tid & 31;
       const int kc = 16 * (m >> 2) + 2 * tt + 8 * ((m >> 1) & 1) + (m & 1);
-      __stcs(rec + 128 * bits + w, klohi[kc]);
-      const int vn = 16 * (m >> 4) + 8 * ((m >> 3) & 1) + 2 * tt + ((m >> 2) & 1);
-      __stcs(rec + 128 * (2 * bits + 1) + w, vlohi[vn][m & 3]);
+      sm.rec[KMETA + tid] = sm.klohi[kc];
     }
     __syncthreads();
+
+    // ---- the record out, coalesced ----
+    const int64_t bh = gi / ng;
+    const int g = (int)(gi % ng);
+    uint4* dst = reinterpret_cast<uint4*>(a.records + (bh * a.q_groups_cap + g) * (int64_t)rb);
+    const uint4* src = reinterpret_cast<const uint4*>(sm.rec);
+    for (int i = tid; i < rb / 16; i += 128) __stcs(dst + i, src[i]);
+    __syncthreads();  // the tile buffer is refilled two iterations on, the record buffer next iteration
   }
+  cp_async_wait<0>();
 }
 
 // Residual window: rows N_q .. N-1 of K and V copied into [resid_cap][2][D].
@@ -188,11 +242,23 @@ __global__ void resid_copy_kernel(const uint16_t* k, const uint16_t* v, uint16_t
   }
 }
 
+template <int BITS>
+static cudaError_t launch_quantize_bits(const QuantArgs& a, cudaStream_t stream) {
+  const int smem = (int)sizeof(QuantSmem);
+  static unsigned long long configured = 0ull;
+  cudaError_t e = spc_host::ensure_smem_limit(configured, quantize_kernel<BITS>, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(a.total_groups, (int64_t)spc_host::sm_count() * 8);
+  quantize_kernel<BITS><<<(unsigned)grid, 128, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 spc_status launch_quantize(const spc_dims* d, const uint16_t* k, const uint16_t* v, void* records,
                            uint16_t* resid, cudaStream_t stream) {
   const int32_t nq = num_quantized(d->N, d->R);
   const int32_t r = d->N - nq;
   const int64_t BH = (int64_t)d->B * d->Hkv;
+  cudaError_t e = cudaSuccess;
   if (nq > 0) {
     QuantArgs a;
     a.k = k;
@@ -201,19 +267,17 @@ spc_status launch_quantize(const spc_dims* d, const uint16_t* k, const uint16_t*
     a.Hkv = d->Hkv;
     a.N = d->N;
     a.nq = nq;
-    a.bits = d->bits;
     a.q_groups_cap = d->q_groups_cap;
     a.total_groups = BH * (nq / kGroup);
-    const int64_t grid = std::min<int64_t>(a.total_groups, (int64_t)spc_host::sm_count() * 12);
-    quantize_kernel<<<(unsigned)grid, 128, 0, stream>>>(a);
+    e = d->bits == 1 ? launch_quantize_bits<1>(a, stream) : launch_quantize_bits<2>(a, stream);
   }
-  if (r > 0) {
+  if (e == cudaSuccess && r > 0) {
     const int64_t total_vec = BH * r * 32;
     const int64_t grid = std::min<int64_t>((total_vec + 255) / 256, (int64_t)spc_host::sm_count() * 8);
     resid_copy_kernel<<<(unsigned)grid, 256, 0, stream>>>(k, v, resid, d->Hkv, d->N, nq, d->resid_cap,
                                                          total_vec);
+    e = cudaGetLastError();
   }
-  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);
     return SPC_ERR_CUDA;
