@@ -4,9 +4,12 @@
 // low-bit copies, plus the bf16 residual window.
 //
 // One launch per call, split-K over tokens (flash-decoding style):
-//   * grid (chunks, B*Hkv).  Each CTA scans a range of 32-token groups of C',
-//     then its warps take their share of the 16-bit rows (residual window
-//     first, then the fetched rows) in 32-row batches spread over all CTAs.
+//   * grid (chunks, B*Hkv).  The 16-bit rows of a (b, hkv) (residual window
+//     first, then the fetched rows) are split into contiguous ranges over all
+//     warps of its CTAs; every warp first reduces its range on CUDA cores,
+//     while its first low-bit stages are already in flight, and the resulting
+//     softmax state seeds its low-bit accumulators.  Then each warp scans its
+//     share of the CTA's range of 32-token groups of C'.
 //   * every CTA merges its warps' states and writes one partial (running max,
 //     sum, unnormalised output) per query row to the workspace; the last CTA
 //     of a (b, hkv) to finish (an atomic ticket) merges the partials into the
@@ -36,13 +39,14 @@ template <int BITS>
 struct Stages {
   static constexpr int value = BITS == 1 ? 4 : 3;  // cp.async pipeline depth per warp
 };
-constexpr int kMergeOffset = 4096;  // CTA merge buffer in dynamic smem, after the 16-bit rows' query tile
-constexpr int kSlots = 2 * kWarps;  // merge slots: each warp's low-bit state, then its 16-bit-row state
+constexpr int kSlots = kWarps;  // CTA merge slots: one per warp
 constexpr float kNeg = -1e30f;  // finite "minus infinity": keeps max/rescale arithmetic NaN-free
 constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pad, o[128]
 constexpr int kZsPitch = 17;     // float4s per t block of a z/s table (16 + 1 pad)
 constexpr int kZsBytes = 2 * 4 * kZsPitch * 16;  // key and value tables of one warp
 constexpr int kMergePitch = kD + 4;              // padded row of the CTA merge buffer
+constexpr int kRowBatch = 8;                     // 16-bit rows staged per batch (512 bytes each)
+constexpr int kTilePitch = kD + 4;               // padded row of a warp's query / output transfer tile
 
 struct AttnArgs {
   const uint8_t* records;
@@ -128,9 +132,201 @@ struct CtaMerge {
   float o[kSlots][kMaxRows][kMergePitch];
 };
 
+// ------------------------------------------------------------ 16-bit rows
+// Reduce-scatter of 16 per-lane partial sums: returns the warp-wide sum of
+// x[lane >> 1], halving the vector at each butterfly step (16 shuffles).
+__device__ __forceinline__ float reduce_scatter16(const float (&x)[16], int lane) {
+  float y8[8], y4[4], y2[2];
+  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    y8[k] = (u16 ? x[k + 8] : x[k]) + __shfl_xor_sync(0xFFFFFFFFu, u16 ? x[k] : x[k + 8], 16);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    y4[k] = (u8 ? y8[k + 4] : y8[k]) + __shfl_xor_sync(0xFFFFFFFFu, u8 ? y8[k] : y8[k + 4], 8);
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    y2[k] = (u4 ? y4[k + 2] : y4[k]) + __shfl_xor_sync(0xFFFFFFFFu, u4 ? y4[k] : y4[k + 2], 4);
+  const float y1 = (u2 ? y2[1] : y2[0]) + __shfl_xor_sync(0xFFFFFFFFu, u2 ? y2[0] : y2[1], 2);
+  return y1 + __shfl_xor_sync(0xFFFFFFFFu, y1, 1);
+}
+
+// The residual window and the fetched rows of this warp's range, before its
+// low-bit groups.  Rows are staged kRowBatch at a time with cp.async into
+// `tail` (the warp's last stage and z/s table, free until the low-bit loop
+// starts); issue_lowbit() puts the first low-bit stages in flight behind the
+// first batch.  Logits: lane = 4 channels x 8 query rows for two rows at a
+// time, then a reduce-scatter leaves lane with row (lane >> 4), query row
+// (lane >> 1) & 7.  Value product: lane = 4 channels, p broadcast from shared
+// memory.  sq is the CTA's scaled query tile [kMaxRows][kTilePitch] (rows
+// 2G.. zero).  On return qv holds the scaled query and (m_run, l_run, oacc) the
+// softmax state of the rows, in the tensor-core fragment layouts of the
+// low-bit loop (oacc divided by the per-channel powers of two that loop
+// multiplies back at its end).
+template <bool MERGED, int STAGES, typename IssueLowbit>
+__device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* sq, uint8_t* tail,
+                                                IssueLowbit&& issue_lowbit,
+                                                float (&qv)[32], float& m_run, float& l_run,
+                                                float (&oacc)[8][4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, t = lane & 3;
+  const int64_t bh = blockIdx.y;
+  const int G = a.G;
+
+  const int n_rows = a.r + (MERGED ? a.k : 0);
+  const int n_warps = a.chunks * kWarps;
+  const int per_warp = (n_rows + n_warps - 1) / n_warps;
+  const int j0 = min(n_rows, (int)(blockIdx.x * kWarps + warp) * per_warp);
+  const int j1 = min(n_rows, j0 + per_warp);
+  float* pb = reinterpret_cast<float*>(tail + kRowBatch * 512);  // p of a batch: [row][query row]
+  const int rho_l = (lane >> 1) & 7;
+  const bool spec_lane = MERGED && a.spec_logits != nullptr && (lane & 1) == 0 && rho_l >= G && rho_l < 2 * G;
+  float* spec_out = spec_lane ? a.spec_logits + (bh * G + (rho_l - G)) * (int64_t)a.Lcap : nullptr;
+  float m_own = kNeg, l_own = 0.f;  // state of query row rho_l
+  float o16[kMaxRows][4];
+#pragma unroll
+  for (int rho = 0; rho < kMaxRows; ++rho) o16[rho][0] = o16[rho][1] = o16[rho][2] = o16[rho][3] = 0.f;
+  bool lowbit_issued = false;
+
+  for (int w0 = j0; w0 < j1; w0 += 32) {
+    const int nwin = min(32, j1 - w0);
+    int pos = -1;  // quantised position of a fetched row, -1 for the residual window
+    bool ok = false;
+    if (lane < nwin) {
+      const int j = w0 + lane;
+      if (j < a.r) {
+        ok = true;
+      } else {
+        pos = a.idx[bh * a.k + (j - a.r)];
+        ok = pos >= 0 && pos < a.nq;
+      }
+    }
+    const uint32_t valid = __ballot_sync(0xFFFFFFFFu, ok);
+    for (int b0 = 0; b0 < nwin; b0 += kRowBatch) {
+      const int nb = min(kRowBatch, nwin - b0);
+      for (int i = 0; i < nb; ++i) {
+        if ((valid >> (b0 + i)) & 1u) {
+          const int j = w0 + b0 + i;
+          const uint16_t* row = j < a.r ? a.resid + (bh * a.resid_cap + j) * 2 * kD
+                                        : a.staging + (bh * a.k + (j - a.r)) * 2 * kD;
+          cp_async16(tail + 512 * i + 16 * lane, row + 8 * lane);
+        }
+      }
+      cp_async_commit();
+      if (!lowbit_issued) {
+        issue_lowbit();  // STAGES - 1 commit groups behind this batch
+        lowbit_issued = true;
+        cp_async_wait<STAGES - 1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncwarp();
+
+      float lg[kRowBatch / 2];
+#pragma unroll
+      for (int pp = 0; pp < kRowBatch / 2; ++pp) {
+        lg[pp] = kNeg;
+        if (2 * pp < nb) {
+          float x[16];
+#pragma unroll
+          for (int jh = 0; jh < 2; ++jh) {
+            const uint2 kk = *reinterpret_cast<const uint2*>(tail + 512 * (2 * pp + jh) + 8 * lane);
+            const float k0 = bf16_to_f32(kk.x & 0xFFFFu), k1 = bf16_to_f32(kk.x >> 16);
+            const float k2 = bf16_to_f32(kk.y & 0xFFFFu), k3 = bf16_to_f32(kk.y >> 16);
+#pragma unroll
+            for (int rho = 0; rho < kMaxRows; ++rho) {
+              const float4 qq = *reinterpret_cast<const float4*>(sq + rho * kTilePitch + 4 * lane);
+              x[8 * jh + rho] = fmaf(qq.w, k3, fmaf(qq.z, k2, fmaf(qq.y, k1, qq.x * k0)));
+            }
+          }
+          const float v = reduce_scatter16(x, lane);
+          const int i = 2 * pp + (lane >> 4);
+          if (i < nb && ((valid >> (b0 + i)) & 1u)) lg[pp] = v;
+        }
+        const int pi = __shfl_sync(0xFFFFFFFFu, pos, b0 + 2 * pp + (lane >> 4));
+        if (spec_lane && lg[pp] != kNeg && pi >= 0) spec_out[pi] = lg[pp] * CUDART_LN2_F;
+      }
+
+      float mx = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+      const float m_new = fmaxf(m_own, mx);
+      const float alpha = fast_exp2(m_own - m_new);
+      float ps = 0.f, p[kRowBatch / 2];
+#pragma unroll
+      for (int pp = 0; pp < kRowBatch / 2; ++pp) {
+        p[pp] = lg[pp] == kNeg ? 0.f : fast_exp2(lg[pp] - m_new);
+        ps += p[pp];
+      }
+      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 16);
+      l_own = l_own * alpha + ps;
+      m_own = m_new;
+      if ((lane & 1) == 0) {
+#pragma unroll
+        for (int pp = 0; pp < kRowBatch / 2; ++pp) pb[(2 * pp + (lane >> 4)) * kMaxRows + rho_l] = p[pp];
+      }
+#pragma unroll
+      for (int rho = 0; rho < kMaxRows; ++rho) {
+        const float al = __shfl_sync(0xFFFFFFFFu, alpha, 2 * rho);
+        o16[rho][0] *= al;
+        o16[rho][1] *= al;
+        o16[rho][2] *= al;
+        o16[rho][3] *= al;
+      }
+      __syncwarp();
+      for (int i = 0; i < nb; ++i) {
+        if (!((valid >> (b0 + i)) & 1u)) continue;  // uniform across the warp
+        const uint2 vv = *reinterpret_cast<const uint2*>(tail + 512 * i + 2 * kD + 8 * lane);
+        const float v0 = bf16_to_f32(vv.x & 0xFFFFu), v1 = bf16_to_f32(vv.x >> 16);
+        const float v2 = bf16_to_f32(vv.y & 0xFFFFu), v3 = bf16_to_f32(vv.y >> 16);
+        const float4 pa = *reinterpret_cast<const float4*>(pb + i * kMaxRows);
+        const float4 pc = *reinterpret_cast<const float4*>(pb + i * kMaxRows + 4);
+        const float pr[kMaxRows] = {pa.x, pa.y, pa.z, pa.w, pc.x, pc.y, pc.z, pc.w};
+#pragma unroll
+        for (int rho = 0; rho < kMaxRows; ++rho) {
+          o16[rho][0] = fmaf(pr[rho], v0, o16[rho][0]);
+          o16[rho][1] = fmaf(pr[rho], v1, o16[rho][1]);
+          o16[rho][2] = fmaf(pr[rho], v2, o16[rho][2]);
+          o16[rho][3] = fmaf(pr[rho], v3, o16[rho][3]);
+        }
+      }
+      __syncwarp();
+    }
+  }
+  if (!lowbit_issued) issue_lowbit();
+
+  // qv[m], m = 4*kc + 2*h + half  <->  channel 16*kc + 2*t + 8*h + half of row gid
+#pragma unroll
+  for (int m = 0; m < 32; m += 2) {
+    const int ch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1);
+    const float2 v = *reinterpret_cast<const float2*>(sq + gid * kTilePitch + ch);
+    qv[m] = v.x;
+    qv[m + 1] = v.y;
+  }
+  // hand the state over to the fragment layout through `tail`
+  float* tile = reinterpret_cast<float*>(tail);  // [kMaxRows][kTilePitch]
+#pragma unroll
+  for (int rho = 0; rho < kMaxRows; ++rho)
+    *reinterpret_cast<float4*>(tile + rho * kTilePitch + 4 * lane) =
+        make_float4(o16[rho][0], o16[rho][1], o16[rho][2], o16[rho][3]);
+  __syncwarp();
+  // oacc[mt]: (channel 16mt+gid, row 2t), (16mt+gid, 2t+1), (16mt+gid+8, 2t), (16mt+gid+8, 2t+1)
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const float c0 = 1.f / bit_comp(2 * mt), c1 = 1.f / bit_comp(2 * mt + 1);
+    oacc[mt][0] = tile[(2 * t) * kTilePitch + 16 * mt + gid] * c0;
+    oacc[mt][1] = tile[(2 * t + 1) * kTilePitch + 16 * mt + gid] * c0;
+    oacc[mt][2] = tile[(2 * t) * kTilePitch + 16 * mt + gid + 8] * c1;
+    oacc[mt][3] = tile[(2 * t + 1) * kTilePitch + 16 * mt + gid + 8] * c1;
+  }
+  __syncwarp();
+  m_run = __shfl_sync(0xFFFFFFFFu, m_own, 2 * gid);
+  const float lr = __shfl_sync(0xFFFFFFFFu, l_own, 2 * gid);
+  l_run = t == 0 ? lr : 0.f;  // the low-bit loop sums l over the four lanes of a row at its end
+}
+
 // ------------------------------------------------------------ low-bit CTA
 template <int BITS, bool MERGED>
-__device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaMerge& merge) {
+__device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, const float* sq, CtaMerge& merge) {
   constexpr int RB = 1024 * (BITS + 1);
   constexpr int KMETA = 512 * BITS;
   constexpr int VCODES = KMETA + 512;
@@ -145,7 +341,6 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
   const int gid = lane >> 2, t = lane & 3;
   const int64_t bh = blockIdx.y;
   const int chunk = blockIdx.x;
-  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
   const int G = a.G;
   const bool row_valid = gid < 2 * G;
 
@@ -155,21 +350,6 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
   // fall in different banks
   float4* kzs = reinterpret_cast<float4*>(stage + kStages * STAGE);
   float4* vzs = kzs + kZsPitch * 4;
-
-  // Scaled query of row gid at this lane's 32 channels, ordered
-  // m = 4*kc + 2*h + half  <->  channel 16*kc + 2*t + 8*h + half.
-  float qv[32];
-#pragma unroll
-  for (int m = 0; m < 32; ++m) qv[m] = 0.f;
-  if (row_valid) {
-    const int i = gid / G, gi = gid % G;
-    const uint16_t* qrow = a.q + (((int64_t)b * 2 + i) * a.Hq + hk * G + gi) * kD;
-#pragma unroll
-    for (int m = 0; m < 32; ++m) {
-      const int ch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1);
-      qv[m] = bf16_to_f32(qrow[ch]) * a.qscale;
-    }
-  }
 
   const int g_begin = chunk * a.groups_per_chunk;
   const int g_end = min(a.nq / kGroup, g_begin + a.groups_per_chunk);
@@ -209,17 +389,23 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     cp_async_commit();
   };
 
-  float m_run = kNeg, l_run = 0.f;
-  float2 zacc01 = make_float2(0.f, 0.f), zacc23 = make_float2(0.f, 0.f);
+  // Scaled query of row gid at this lane's 32 channels, ordered
+  // m = 4*kc + 2*h + half  <->  channel 16*kc + 2*t + 8*h + half, and the
+  // state left by this warp's 16-bit rows.
+  float qv[32];
+  float m_run, l_run;
   float oacc[8][4];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+  rows16_prologue<MERGED, kStages>(
+      a, sq, stage + (kStages - 1) * STAGE,
+      [&]() {
+#pragma unroll 1
+        for (int s = 0; s < kStages - 1; ++s) issue(s);
+      },
+      qv, m_run, l_run, oacc);
+  float2 zacc01 = make_float2(0.f, 0.f), zacc23 = make_float2(0.f, 0.f);
 
   const bool spec_row = row_valid && gid >= G && a.spec_logits != nullptr;
   float* spec_out = spec_row ? a.spec_logits + ((bh * G + (gid - G)) * (int64_t)a.Lcap) : nullptr;
-
-#pragma unroll 1
-  for (int s = 0; s < kStages - 1; ++s) issue(s);
 
 #pragma unroll 1
   for (int it = 0; it < n_my; ++it) {
@@ -471,144 +657,8 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, CtaM
     for (int q8 = 0; q8 < 8; ++q8) merge.o[warp][gid][32 * cg + 8 * t + q8] += zacc[cg];
 }
 
-// ------------------------------------------------------------ 16-bit rows
-// The residual window and the fetched rows on CUDA cores: one row per lane
-// for the logits, four channels per lane for the value product.  Runs in
-// every CTA after its low-bit groups (the stage buffers are free by then);
-// 32-row batch bt goes to CTA bt % chunks, warp (bt / chunks) % kWarps.
-__device__ __forceinline__ void rows16_phase(const AttnArgs& a, uint8_t* dyn, CtaMerge& merge) {
-  float (*qs)[kD] = reinterpret_cast<float (*)[kD]>(dyn);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t bh = blockIdx.y;
-  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
-  const int G = a.G, rows = 2 * G;
-  for (int i = threadIdx.x; i < kMaxRows * kD; i += kThreads) {
-    const int rho = i / kD, c = i % kD;
-    float v = 0.f;
-    if (rho < rows) {
-      const int qi = rho / G, gi = rho % G;
-      v = bf16_to_f32(a.q[(((int64_t)b * 2 + qi) * a.Hq + hk * G + gi) * kD + c]) * a.qscale;
-    }
-    qs[rho][c] = v;
-  }
-  __syncthreads();
-
-  const int n_rows = a.r + a.k;
-  const int n_batches = (n_rows + 31) / 32;
-  float m_run[kMaxRows], l_run[kMaxRows], o[kMaxRows][4];
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho) {
-    m_run[rho] = kNeg;
-    l_run[rho] = 0.f;
-    o[rho][0] = o[rho][1] = o[rho][2] = o[rho][3] = 0.f;
-  }
-  const int first = blockIdx.x + a.chunks * warp;
-  for (int bt = first; bt < n_batches; bt += a.chunks * kWarps) {
-    const int j = 32 * bt + lane;  // this lane's row for the logits
-    const uint16_t* row = nullptr;
-    int pos = -1;                   // quantised position of a fetched row
-    if (j < a.r) {
-      row = a.resid + ((bh * a.resid_cap + j) * 2) * kD;
-    } else if (j < n_rows) {
-      const int jj = j - a.r;
-      pos = a.idx[bh * a.k + jj];
-      if (pos >= 0 && pos < a.nq) row = a.staging + ((bh * a.k + jj) * 2) * kD;
-    }
-    float lg[kMaxRows];
-#pragma unroll
-    for (int rho = 0; rho < kMaxRows; ++rho) lg[rho] = 0.f;
-    if (row != nullptr) {
-      const uint4* kr = reinterpret_cast<const uint4*>(row);
-#pragma unroll 2
-      for (int c8 = 0; c8 < kD / 8; ++c8) {
-        const uint4 kk = kr[c8];
-        const uint32_t kw[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-        for (int rho = 0; rho < kMaxRows; ++rho) {
-          const float4 qa = *reinterpret_cast<const float4*>(&qs[rho][8 * c8]);
-          const float4 qb = *reinterpret_cast<const float4*>(&qs[rho][8 * c8 + 4]);
-          float acc = lg[rho];
-          acc = fmaf(qa.x, bf16_to_f32(kw[0] & 0xFFFFu), acc);
-          acc = fmaf(qa.y, bf16_to_f32(kw[0] >> 16), acc);
-          acc = fmaf(qa.z, bf16_to_f32(kw[1] & 0xFFFFu), acc);
-          acc = fmaf(qa.w, bf16_to_f32(kw[1] >> 16), acc);
-          acc = fmaf(qb.x, bf16_to_f32(kw[2] & 0xFFFFu), acc);
-          acc = fmaf(qb.y, bf16_to_f32(kw[2] >> 16), acc);
-          acc = fmaf(qb.z, bf16_to_f32(kw[3] & 0xFFFFu), acc);
-          acc = fmaf(qb.w, bf16_to_f32(kw[3] >> 16), acc);
-          lg[rho] = acc;
-        }
-      }
-    }
-    const bool live = row != nullptr;
-    if (live && pos >= 0 && a.spec_logits != nullptr) {
-      for (int gi = 0; gi < G; ++gi)
-        a.spec_logits[(bh * G + gi) * (int64_t)a.Lcap + pos] = lg[G + gi] * CUDART_LN2_F;
-    }
-    float p[kMaxRows];
-#pragma unroll
-    for (int rho = 0; rho < kMaxRows; ++rho) {
-      float mx = live ? lg[rho] : kNeg;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-      const float m_new = fmaxf(m_run[rho], mx);
-      const float al = fast_exp2(m_run[rho] - m_new);
-      m_run[rho] = m_new;
-      p[rho] = live ? fast_exp2(lg[rho] - m_new) : 0.f;
-      float ps = p[rho];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
-      l_run[rho] = l_run[rho] * al + ps;
-      o[rho][0] *= al;
-      o[rho][1] *= al;
-      o[rho][2] *= al;
-      o[rho][3] *= al;
-    }
-    // value product: lane owns channels 4*lane .. 4*lane+3
-    const int nb = min(32, n_rows - 32 * bt);
-    for (int jj = 0; jj < nb; ++jj) {
-      const int jr = 32 * bt + jj;
-      const uint16_t* vrow = nullptr;
-      if (jr < a.r) {
-        vrow = a.resid + ((bh * a.resid_cap + jr) * 2 + 1) * kD;
-      } else {
-        const int js = jr - a.r;
-        const int pj = a.idx[bh * a.k + js];
-        if (pj >= 0 && pj < a.nq) vrow = a.staging + ((bh * a.k + js) * 2 + 1) * kD;
-      }
-      if (vrow == nullptr) continue;  // uniform across the warp
-      const uint2 vv = reinterpret_cast<const uint2*>(vrow)[lane];
-      const float v0 = bf16_to_f32(vv.x & 0xFFFFu), v1 = bf16_to_f32(vv.x >> 16);
-      const float v2 = bf16_to_f32(vv.y & 0xFFFFu), v3 = bf16_to_f32(vv.y >> 16);
-#pragma unroll
-      for (int rho = 0; rho < kMaxRows; ++rho) {
-        const float pj = __shfl_sync(0xFFFFFFFFu, p[rho], jj);
-        o[rho][0] = fmaf(pj, v0, o[rho][0]);
-        o[rho][1] = fmaf(pj, v1, o[rho][1]);
-        o[rho][2] = fmaf(pj, v2, o[rho][2]);
-        o[rho][3] = fmaf(pj, v3, o[rho][3]);
-      }
-    }
-  }
-  if (lane < kMaxRows) {
-    float mv = 0.f, lv = 0.f;
-#pragma unroll
-    for (int rho = 0; rho < kMaxRows; ++rho)
-      if (rho == lane) {
-        mv = m_run[rho];
-        lv = l_run[rho];
-      }
-    merge.m[kWarps + warp][lane] = mv;
-    merge.l[kWarps + warp][lane] = lv;
-  }
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) merge.o[kWarps + warp][rho][4 * lane + e] = o[rho][e];
-}
-
 // ------------------------------------------------------------ merge + combine
-__device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last) {
+__device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last, float* s_ml) {
   __syncthreads();
   const int c = threadIdx.x;  // channel
   const int64_t bh = blockIdx.y;
@@ -640,23 +690,57 @@ __device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs
   __syncthreads();
   if (!*s_last) return;
   __threadfence();
+  const float* base = a.part + (bh * nparts * kMaxRows) * kPartStride;
+  // (max, sum) of query row c / 16 over partials c % 16, c % 16 + 16, ..., then
+  // over the 16 lanes of the row
+  {
+    const int rho = c >> 4, sub = c & 15;
+    float m = kNeg, l = 0.f;
+    for (int p = sub; p < nparts; p += 16) {
+      const float* pr = base + ((int64_t)p * kMaxRows + rho) * kPartStride;
+      const float mp = __ldcg(pr), lp = __ldcg(pr + 1);
+      const float mn = fmaxf(m, mp);
+      l = l * fast_exp2(m - mn) + lp * fast_exp2(mp - mn);
+      m = mn;
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+      const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, off), lo = __shfl_xor_sync(0xFFFFFFFFu, l, off);
+      const float mn = fmaxf(m, mo);
+      l = l * fast_exp2(m - mn) + lo * fast_exp2(mo - mn);
+      m = mn;
+    }
+    if (sub == 0) {
+      s_ml[rho] = m;
+      s_ml[kMaxRows + rho] = l;
+    }
+  }
+  __syncthreads();
+  float M[kMaxRows], O[kMaxRows];
+#pragma unroll
+  for (int rho = 0; rho < kMaxRows; ++rho) {
+    M[rho] = s_ml[rho];
+    O[rho] = 0.f;
+  }
+  // every partial's 8 rows at once: independent loads, one round trip per partial
+#pragma unroll 2
+  for (int p = 0; p < nparts; ++p) {
+    const float* pr = base + (int64_t)p * kMaxRows * kPartStride;
+#pragma unroll
+    for (int rho = 0; rho < kMaxRows; ++rho)
+      if (rho < rows)
+        O[rho] += __ldcg(pr + rho * kPartStride + 4 + c) * fast_exp2(__ldcg(pr + rho * kPartStride) - M[rho]);
+  }
   const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
   const int G = a.G;
-  const float* base = a.part + (bh * nparts * kMaxRows) * kPartStride;
-  for (int rho = 0; rho < rows; ++rho) {
+#pragma unroll
+  for (int rho = 0; rho < kMaxRows; ++rho) {
+    if (rho >= rows) break;
+    const float L = s_ml[kMaxRows + rho];
     const int qi = rho / G, gi = rho % G;
-    float M = kNeg;
-    for (int p = 0; p < nparts; ++p) M = fmaxf(M, __ldcg(base + ((int64_t)p * kMaxRows + rho) * kPartStride));
-    float L = 0.f, O = 0.f;
-    for (int p = 0; p < nparts; ++p) {
-      const float* pr = base + ((int64_t)p * kMaxRows + rho) * kPartStride;
-      const float f = fast_exp2(__ldcg(pr) - M);
-      L += __ldcg(pr + 1) * f;
-      O += __ldcg(pr + 4 + c) * f;
-    }
     const int64_t orow = ((int64_t)b * 2 + qi) * a.Hq + hk * G + gi;
-    a.out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O / L : 0.f);
-    if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
+    a.out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O[rho] / L : 0.f);
+    if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M[rho] + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
   }
   if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
 }
@@ -665,10 +749,28 @@ template <int BITS, bool MERGED>
 __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ int s_last;
-  CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem + kMergeOffset);
-  lowbit_cta<BITS, MERGED>(a, dyn_smem, merge);
-  rows16_phase(a, dyn_smem, merge);
-  merge_store_combine(merge, a, &s_last);
+  __shared__ float s_ml[2 * kMaxRows];
+  __shared__ __align__(16) float s_q[kMaxRows * kTilePitch];
+  CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem);
+  {
+    // scaled query rows of this (b, hkv): rho = i * G + gi for token i, head gi
+    const int64_t bh = blockIdx.y;
+    const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
+    for (int e = threadIdx.x; e < kMaxRows * kD / 4; e += kThreads) {
+      const int rho = e / (kD / 4), c4 = e % (kD / 4);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (rho < 2 * G) {
+        const int qi = rho / G, gi = rho % G;
+        const uint2 qq = reinterpret_cast<const uint2*>(a.q + (((int64_t)b * 2 + qi) * a.Hq + hk * G + gi) * kD)[c4];
+        v = make_float4(bf16_to_f32(qq.x & 0xFFFFu) * a.qscale, bf16_to_f32(qq.x >> 16) * a.qscale,
+                        bf16_to_f32(qq.y & 0xFFFFu) * a.qscale, bf16_to_f32(qq.y >> 16) * a.qscale);
+      }
+      *reinterpret_cast<float4*>(s_q + rho * kTilePitch + 4 * c4) = v;
+    }
+    __syncthreads();
+  }
+  lowbit_cta<BITS, MERGED>(a, dyn_smem, s_q, merge);
+  merge_store_combine(merge, a, &s_last, s_ml);
 }
 
 // ---------------------------------------------------------------- host side
@@ -746,9 +848,11 @@ size_t attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
 template <int BITS, bool MERGED>
 static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
   const int smem = attn_smem_bytes(BITS);
-  static_assert(kMergeOffset >= kMaxRows * kD * 4, "16-bit-row CTA query tile lies below the merge buffer");
-  static_assert(kMergeOffset + (int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
+  static_assert((int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
                 "merge buffer fits in the dynamic shared memory");
+  static_assert(kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= 2576 + kZsBytes &&
+                    kMaxRows * kTilePitch * 4 <= 2576 + kZsBytes,
+                "16-bit row batch and transfer tile fit in a warp's last stage and z/s table");
   auto* fn = attn_kernel<BITS, MERGED>;
   static unsigned long long configured = 0ull;  // one per <BITS, MERGED> instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
