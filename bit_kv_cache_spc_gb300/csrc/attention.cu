@@ -325,7 +325,7 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
 }
 
 // ------------------------------------------------------------ low-bit CTA
-template <int BITS, bool MERGED>
+template <int BITS, bool MERGED, bool FETCH>
 __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, const float* sq, CtaMerge& merge) {
   constexpr int RB = 1024 * (BITS + 1);
   constexpr int KMETA = 512 * BITS;
@@ -356,15 +356,16 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   const int n_my = (g_end - g_begin - warp + kWarps - 1) / kWarps;  // groups of this warp
   const uint8_t* rec_base = a.records + (bh * a.q_groups_cap) * (int64_t)RB;
 
-  // Pre-fetch rows of this warp: rr = slot + n_slots * i, carried by every
-  // pf_every-th item (one 512-byte row per carried item), the rest copied
-  // after the groups.
+  // Pre-fetch rows of this warp: rr = slot + n_slots * i, carried by items
+  // 0, pf_every, 2 pf_every, ... (one 512-byte row per carried item), the
+  // rest copied after the groups.
   const int64_t n_slots = (int64_t)gridDim.x * gridDim.y * kWarps;
   const int64_t slot = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kWarps + warp;
-  const int n_pf = (a.pf_host != nullptr && a.pf_rows > slot) ? (int)((a.pf_rows - slot + n_slots - 1) / n_slots) : 0;
+  const int n_pf = (FETCH && a.pf_rows > slot) ? (int)((a.pf_rows - slot + n_slots - 1) / n_slots) : 0;
   const int pf_every = n_pf > 0 ? max(1, n_my / n_pf) : 1;
   const int pf_carried = n_pf > 0 ? min(n_pf, (n_my + pf_every - 1) / pf_every) : 0;
   int pf_next = n_pf > 0 ? a.pf_idx[slot] : -1;  // position of the next row to issue
+  int pf_issue_i = 0, pf_issue_item = 0;          // next carried row on the issue side and its item
 
   auto issue = [&](int item) {
     if (item < n_my) {
@@ -374,16 +375,17 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
 #pragma unroll
       for (int u = 0; u < RB / 512; ++u) cp_async16(dst + 16 * (lane + 32 * u), src + 16 * (lane + 32 * u));
       if (MERGED && lane == 0) cp_async4(dst + RB, a.bitmap + bh * a.q_groups_cap + g);
-      if (item % pf_every == 0 && item / pf_every < pf_carried) {
-        const int i = item / pf_every;
-        const int64_t rr = slot + n_slots * i;
+      if (FETCH && item == pf_issue_item && pf_issue_i < pf_carried) {
+        const int64_t rr = slot + n_slots * pf_issue_i;
         const int n = pf_next;
         if (lane == 0) reinterpret_cast<int*>(dst + RB)[1] = n;
         if (n >= 0 && n < a.pf_ncap) {
           const int64_t src_row = ((rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
           cp_async16(dst + PFROW + 16 * lane, a.pf_host + src_row + 8 * lane);
         }
-        pf_next = (i + 1 < n_pf) ? a.pf_idx[rr + n_slots] : -1;
+        pf_next = (pf_issue_i + 1 < n_pf) ? a.pf_idx[rr + n_slots] : -1;
+        ++pf_issue_i;
+        pf_issue_item += pf_every;
       }
     }
     cp_async_commit();
@@ -407,6 +409,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   const bool spec_row = row_valid && gid >= G && a.spec_logits != nullptr;
   float* spec_out = spec_row ? a.spec_logits + ((bh * G + (gid - G)) * (int64_t)a.Lcap) : nullptr;
 
+  int pf_use_i = 0, pf_use_item = 0;  // next carried row on the consuming side and its item
 #pragma unroll 1
   for (int it = 0; it < n_my; ++it) {
     issue(it + kStages - 1);
@@ -414,13 +417,15 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     __syncwarp();
     const uint8_t* R = stage + (it % kStages) * STAGE;
     const int g = g_begin + warp + it * kWarps;
-    if (it % pf_every == 0 && it / pf_every < pf_carried) {
+    if (FETCH && it == pf_use_item && pf_use_i < pf_carried) {
       const int n = reinterpret_cast<const int*>(R + RB)[1];
       if (n >= 0 && n < a.pf_ncap) {
-        const int64_t rr = slot + n_slots * (it / pf_every);
+        const int64_t rr = slot + n_slots * pf_use_i;
         reinterpret_cast<uint4*>(a.pf_staging + rr * (2 * kD))[lane] =
             reinterpret_cast<const uint4*>(R + PFROW)[lane];
       }
+      ++pf_use_i;
+      pf_use_item += pf_every;
     }
 
     // ---- z, s of the group's 128 key groups and 128 value groups, 4 + 4 per lane ----
@@ -487,28 +492,39 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     bias += __shfl_xor_sync(0xFFFFFFFFu, bias, 2);
 
     // ---- logits, speculative-row output, online softmax (base 2) ----
+    // bm: the group's tokens whose 16-bit rows were fetched (same word in every lane)
     const uint32_t bm = MERGED ? *reinterpret_cast<const uint32_t*>(R + RB) : 0u;
     float lg[4][2];
-    float gmax = kNeg;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const float2 l = f2_add(f2_add(make_float2(acc[nt][0], acc[nt][1]), make_float2(acc[nt][2], acc[nt][3])),
                               make_float2(bias, bias));
-      const int tok = 8 * nt + 2 * t;
-      const bool m0 = MERGED && ((bm >> tok) & 1u), m1 = MERGED && ((bm >> (tok + 1)) & 1u);
-      lg[nt][0] = m0 ? kNeg : l.x;
-      lg[nt][1] = m1 ? kNeg : l.y;
-      gmax = fmaxf(gmax, fmaxf(lg[nt][0], lg[nt][1]));
-      if (spec_row) {
-        float* dst = spec_out + (int64_t)g * kGroup + tok;
-        if (!m0 && !m1) {
-          *reinterpret_cast<float2*>(dst) = make_float2(l.x * CUDART_LN2_F, l.y * CUDART_LN2_F);
+      lg[nt][0] = l.x;
+      lg[nt][1] = l.y;
+    }
+    if (spec_row) {
+      float* dst = spec_out + (int64_t)g * kGroup + 2 * t;
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const uint32_t mb = MERGED ? (bm >> (8 * nt + 2 * t)) & 3u : 0u;
+        if (mb == 0u) {
+          *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(lg[nt][0] * CUDART_LN2_F, lg[nt][1] * CUDART_LN2_F);
         } else {
-          if (!m0) dst[0] = l.x * CUDART_LN2_F;
-          if (!m1) dst[1] = l.y * CUDART_LN2_F;
+          if (!(mb & 1u)) dst[8 * nt] = lg[nt][0] * CUDART_LN2_F;
+          if (!(mb & 2u)) dst[8 * nt + 1] = lg[nt][1] * CUDART_LN2_F;
         }
       }
     }
+    if (MERGED && bm != 0u) {  // uniform: most groups have no fetched token
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int tok = 8 * nt + 2 * t;
+        if ((bm >> tok) & 1u) lg[nt][0] = kNeg;
+        if ((bm >> (tok + 1)) & 1u) lg[nt][1] = kNeg;
+      }
+    }
+    float gmax = fmaxf(fmaxf(fmaxf(lg[0][0], lg[0][1]), fmaxf(lg[1][0], lg[1][1])),
+                       fmaxf(fmaxf(lg[2][0], lg[2][1]), fmaxf(lg[3][0], lg[3][1])));
     gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, 1));
     gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, 2));
     const float m_new = fmaxf(m_run, gmax);
@@ -528,12 +544,14 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
       zacc23 = f2_mul(zacc23, make_float2(alpha, alpha));
       m_run = m_new;
     }
+    // a masked logit (kNeg) gives exactly 0, also while no token has been seen yet
+    const float m_use = fmaxf(m_run, 0.5f * kNeg);
     float p[4][2];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        p[nt][e] = (lg[nt][e] == kNeg) ? 0.f : fast_exp2(lg[nt][e] - m_run);
+        p[nt][e] = fast_exp2(lg[nt][e] - m_use);
         l_run += p[nt][e];
       }
 
@@ -745,7 +763,7 @@ __device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs
   if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
 }
 
-template <int BITS, bool MERGED>
+template <int BITS, bool MERGED, bool FETCH>
 __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ int s_last;
@@ -769,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
     }
     __syncthreads();
   }
-  lowbit_cta<BITS, MERGED>(a, dyn_smem, s_q, merge);
+  lowbit_cta<BITS, MERGED, FETCH>(a, dyn_smem, s_q, merge);
   merge_store_combine(merge, a, &s_last, s_ml);
 }
 
@@ -800,12 +818,12 @@ static int resident_ctas(int bits) {
   cudaError_t e;
   if (bits == 1) {
     static unsigned long long configured = 0ull;
-    e = spc_host::ensure_smem_limit(configured, attn_kernel<1, true>, smem);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<1, true>, kThreads, smem);
+    e = spc_host::ensure_smem_limit(configured, attn_kernel<1, true, true>, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<1, true, true>, kThreads, smem);
   } else {
     static unsigned long long configured = 0ull;
-    e = spc_host::ensure_smem_limit(configured, attn_kernel<2, true>, smem);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<2, true>, kThreads, smem);
+    e = spc_host::ensure_smem_limit(configured, attn_kernel<2, true, true>, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<2, true, true>, kThreads, smem);
   }
   if (e != cudaSuccess || n <= 0) {
     cudaGetLastError();
@@ -845,7 +863,7 @@ size_t attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
   return ticket_bytes(d) + part_floats(d, attn_plan(d, k_max)) * sizeof(float);
 }
 
-template <int BITS, bool MERGED>
+template <int BITS, bool MERGED, bool FETCH>
 static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
   const int smem = attn_smem_bytes(BITS);
   static_assert((int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
@@ -853,8 +871,8 @@ static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t strea
   static_assert(kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= 2576 + kZsBytes &&
                     kMaxRows * kTilePitch * 4 <= 2576 + kZsBytes,
                 "16-bit row batch and transfer tile fit in a warp's last stage and z/s table");
-  auto* fn = attn_kernel<BITS, MERGED>;
-  static unsigned long long configured = 0ull;  // one per <BITS, MERGED> instantiation
+  auto* fn = attn_kernel<BITS, MERGED, FETCH>;
+  static unsigned long long configured = 0ull;  // one per <BITS, MERGED, FETCH> instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
   if (e != cudaSuccess) return e;
   fn<<<dim3(a.chunks, (unsigned)BH), kThreads, smem, stream>>>(a);
@@ -897,12 +915,19 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.pf_k = pf ? pf->k : 0;
   a.pf_rows = pf ? (int32_t)((int64_t)d->B * d->Hkv * pf->k) : 0;
   const int64_t BH = (int64_t)d->B * d->Hkv;
-  const bool merged = k > 0;
+  const bool merged = k > 0, fetch = a.pf_host != nullptr && a.pf_rows > 0;
   cudaError_t e;
-  if (d->bits == 1)
-    e = merged ? launch_attn<1, true>(a, BH, stream) : launch_attn<1, false>(a, BH, stream);
-  else
-    e = merged ? launch_attn<2, true>(a, BH, stream) : launch_attn<2, false>(a, BH, stream);
+  if (d->bits == 1) {
+    if (merged)
+      e = fetch ? launch_attn<1, true, true>(a, BH, stream) : launch_attn<1, true, false>(a, BH, stream);
+    else
+      e = fetch ? launch_attn<1, false, true>(a, BH, stream) : launch_attn<1, false, false>(a, BH, stream);
+  } else {
+    if (merged)
+      e = fetch ? launch_attn<2, true, true>(a, BH, stream) : launch_attn<2, true, false>(a, BH, stream);
+    else
+      e = fetch ? launch_attn<2, false, true>(a, BH, stream) : launch_attn<2, false, false>(a, BH, stream);
+  }
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);
     return SPC_ERR_CUDA;
