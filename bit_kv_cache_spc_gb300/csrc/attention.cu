@@ -39,6 +39,13 @@ template <int BITS>
 struct Stages {
   static constexpr int value = BITS == 1 ? 4 : 3;  // cp.async pipeline depth per warp
 };
+// At 1 bit the scaled query lives in registers across the low-bit loop; at 2
+// bits (twice the code words per group) it is read from shared memory to
+// keep the loop within the register budget of 4 CTAs per SM.
+template <int BITS>
+struct QueryInRegisters {
+  static constexpr bool value = BITS == 1;
+};
 constexpr int kSlots = kWarps;  // CTA merge slots: one per warp
 constexpr float kNeg = -1e30f;  // finite "minus infinity": keeps max/rescale arithmetic NaN-free
 constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pad, o[128]
@@ -159,14 +166,12 @@ __device__ __forceinline__ float reduce_scatter16(const float (&x)[16], int lane
 // time, then a reduce-scatter leaves lane with row (lane >> 4), query row
 // (lane >> 1) & 7.  Value product: lane = 4 channels, p broadcast from shared
 // memory.  sq is the CTA's scaled query tile [kMaxRows][kTilePitch] (rows
-// 2G.. zero).  On return qv holds the scaled query and (m_run, l_run, oacc) the
-// softmax state of the rows, in the tensor-core fragment layouts of the
-// low-bit loop (oacc divided by the per-channel powers of two that loop
+// 2G.. zero).  On return (m_run, l_run, oacc) hold the softmax state of the
+// rows, in the tensor-core fragment layouts of the low-bit loop (oacc divided by the per-channel powers of two that loop
 // multiplies back at its end).
 template <bool MERGED, int STAGES, typename IssueLowbit>
 __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* sq, uint8_t* tail,
-                                                IssueLowbit&& issue_lowbit,
-                                                float (&qv)[32], float& m_run, float& l_run,
+                                                IssueLowbit&& issue_lowbit, float& m_run, float& l_run,
                                                 float (&oacc)[8][4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, t = lane & 3;
@@ -294,14 +299,6 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
   }
   if (!lowbit_issued) issue_lowbit();
 
-  // qv[m], m = 4*kc + 2*h + half  <->  channel 16*kc + 2*t + 8*h + half of row gid
-#pragma unroll
-  for (int m = 0; m < 32; m += 2) {
-    const int ch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1);
-    const float2 v = *reinterpret_cast<const float2*>(sq + gid * kTilePitch + ch);
-    qv[m] = v.x;
-    qv[m + 1] = v.y;
-  }
   // hand the state over to the fragment layout through `tail`
   float* tile = reinterpret_cast<float*>(tail);  // [kMaxRows][kTilePitch]
 #pragma unroll
@@ -391,10 +388,9 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     cp_async_commit();
   };
 
-  // Scaled query of row gid at this lane's 32 channels, ordered
-  // m = 4*kc + 2*h + half  <->  channel 16*kc + 2*t + 8*h + half, and the
-  // state left by this warp's 16-bit rows.
-  float qv[32];
+  // the state left by this warp's 16-bit rows, and the scaled query of row
+  // gid at this lane's 32 channels, ordered m = 4*kc + 2*h + half <->
+  // channel 16*kc + 2*t + 8*h + half (registers at 1 bit, else read from sq)
   float m_run, l_run;
   float oacc[8][4];
   rows16_prologue<MERGED, kStages>(
@@ -403,7 +399,17 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
 #pragma unroll 1
         for (int s = 0; s < kStages - 1; ++s) issue(s);
       },
-      qv, m_run, l_run, oacc);
+      m_run, l_run, oacc);
+  constexpr bool kQvReg = QueryInRegisters<BITS>::value;
+  float qv[kQvReg ? 32 : 1];
+  if constexpr (kQvReg) {
+#pragma unroll
+    for (int m = 0; m < 32; m += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(sq + gid * kTilePitch + 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1));
+      qv[m] = v.x;
+      qv[m + 1] = v.y;
+    }
+  }
   float2 zacc01 = make_float2(0.f, 0.f), zacc23 = make_float2(0.f, 0.f);
 
   const bool spec_row = row_valid && gid >= G && a.spec_logits != nullptr;
@@ -471,8 +477,15 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     for (int kc = 0; kc < 8; ++kc) {
       const float4 z4 = kzs[kZsPitch * t + 2 * kc];
       const float4 s4 = kzs[kZsPitch * t + 2 * kc + 1];
-      const float2 q01 = make_float2(qv[4 * kc], qv[4 * kc + 1]);
-      const float2 q23 = make_float2(qv[4 * kc + 2], qv[4 * kc + 3]);
+      // query row gid at channels 16kc + 2t + {0, 1} and 16kc + 2t + 8 + {0, 1}
+      float2 q01, q23;
+      if constexpr (kQvReg) {
+        q01 = make_float2(qv[4 * kc], qv[4 * kc + 1]);
+        q23 = make_float2(qv[4 * kc + 2], qv[4 * kc + 3]);
+      } else {
+        q01 = *reinterpret_cast<const float2*>(sq + gid * kTilePitch + 16 * kc + 2 * t);
+        q23 = *reinterpret_cast<const float2*>(sq + gid * kTilePitch + 16 * kc + 2 * t + 8);
+      }
       bias2 = f2_fma(q01, make_float2(z4.x, z4.y), bias2);
       bias2 = f2_fma(q23, make_float2(z4.z, z4.w), bias2);
       uint32_t af[4];
@@ -804,43 +817,41 @@ static int attn_smem_bytes(int bits) {
 }
 
 // Resident attention CTAs per SM on the current device (occupancy query,
-// cached per device and bit width).
-static int resident_ctas(int bits) {
-  static int cached[2][64] = {};
+// cached per device, bit width and fetch variant).
+template <int BITS, bool FETCH>
+static int resident_ctas() {
+  static int cached[64] = {};
+  static unsigned long long configured = 0ull;
   const int dev = spc_host::current_device();
-  const int bi = bits == 1 ? 0 : 1;
   if (dev >= 0 && dev < 64) {
-    const int c = __atomic_load_n(&cached[bi][dev], __ATOMIC_ACQUIRE);
+    const int c = __atomic_load_n(&cached[dev], __ATOMIC_ACQUIRE);
     if (c > 0) return c;
   }
   int n = 0;
-  const int smem = attn_smem_bytes(bits);
-  cudaError_t e;
-  if (bits == 1) {
-    static unsigned long long configured = 0ull;
-    e = spc_host::ensure_smem_limit(configured, attn_kernel<1, true, true>, smem);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<1, true, true>, kThreads, smem);
-  } else {
-    static unsigned long long configured = 0ull;
-    e = spc_host::ensure_smem_limit(configured, attn_kernel<2, true, true>, smem);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<2, true, true>, kThreads, smem);
-  }
+  const int smem = attn_smem_bytes(BITS);
+  cudaError_t e = spc_host::ensure_smem_limit(configured, attn_kernel<BITS, true, FETCH>, smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<BITS, true, FETCH>, kThreads, smem);
   if (e != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = 2;
   }
-  if (dev >= 0 && dev < 64) __atomic_store_n(&cached[bi][dev], n, __ATOMIC_RELEASE);
+  if (dev >= 0 && dev < 64) __atomic_store_n(&cached[dev], n, __ATOMIC_RELEASE);
   return n;
 }
 
-static AttnPlan attn_plan(const spc_dims* d, int32_t k) {
-  (void)k;  // the 16-bit rows ride on the same CTAs, whatever their number
+static int resident_ctas(int bits, bool fetch) {
+  if (bits == 1) return fetch ? resident_ctas<1, true>() : resident_ctas<1, false>();
+  return fetch ? resident_ctas<2, true>() : resident_ctas<2, false>();
+}
+
+// One wave of resident CTAs over B*Hkv, at least four groups (one per warp)
+// each.  The 16-bit rows ride on the same CTAs, whatever their number.
+static AttnPlan attn_plan(const spc_dims* d, bool fetch) {
   const int ng = num_quantized(d->N, d->R) / kGroup;
   const int64_t BH = (int64_t)d->B * d->Hkv;
   AttnPlan p{1, 1};
   if (ng > 0) {
-    // one wave of resident CTAs, at least four groups (one per warp) each
-    const int64_t slots = (int64_t)spc_host::sm_count() * resident_ctas(d->bits);
+    const int64_t slots = (int64_t)spc_host::sm_count() * resident_ctas(d->bits, fetch);
     int64_t chunks = std::max<int64_t>(1, slots / BH);
     chunks = std::min<int64_t>(chunks, (ng + kWarps - 1) / kWarps);
     p.groups_per_chunk = (int)((ng + chunks - 1) / chunks);
@@ -860,7 +871,9 @@ static size_t ticket_bytes(const spc_dims* d) {
 }
 
 size_t attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
-  return ticket_bytes(d) + part_floats(d, attn_plan(d, k_max)) * sizeof(float);
+  (void)k_max;  // the partials do not depend on the number of fetched rows
+  const size_t parts = std::max(part_floats(d, attn_plan(d, false)), part_floats(d, attn_plan(d, true)));
+  return ticket_bytes(d) + parts * sizeof(float);
 }
 
 template <int BITS, bool MERGED, bool FETCH>
@@ -883,7 +896,8 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
                             const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
                             const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
                             float* spec_logits, void* ws, cudaStream_t stream, const PrefetchJob* pf) {
-  const AttnPlan plan = attn_plan(d, k);
+  const bool fetch = pf != nullptr && pf->host_dev != nullptr && (int64_t)d->B * d->Hkv * pf->k > 0;
+  const AttnPlan plan = attn_plan(d, fetch);
   AttnArgs a;
   a.records = static_cast<const uint8_t*>(records);
   a.resid = resid;
@@ -908,14 +922,14 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.groups_per_chunk = plan.groups_per_chunk;
   a.Lcap = d->q_groups_cap * kGroup;
   a.qscale = d->scale * 1.4426950408889634f;
-  a.pf_host = pf ? pf->host_dev : nullptr;
+  a.pf_host = fetch ? pf->host_dev : nullptr;
   a.pf_idx = pf ? pf->idx : nullptr;
   a.pf_staging = pf ? pf->staging : nullptr;
   a.pf_ncap = pf ? pf->n_cap : 0;
   a.pf_k = pf ? pf->k : 0;
   a.pf_rows = pf ? (int32_t)((int64_t)d->B * d->Hkv * pf->k) : 0;
   const int64_t BH = (int64_t)d->B * d->Hkv;
-  const bool merged = k > 0, fetch = a.pf_host != nullptr && a.pf_rows > 0;
+  const bool merged = k > 0;
   cudaError_t e;
   if (d->bits == 1) {
     if (merged)
