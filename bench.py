@@ -48,6 +48,7 @@ def parse():
     p.add_argument("--cpu-pairs", type=int, default=16, help="(b, kv-head) pairs in the oracle sample")
     p.add_argument("--prefetch", choices=["side", "fused"], default="fused",
                    help="pre-fetch as a small side-stream kernel, or carried by the next layer's attention")
+    p.add_argument("--gather-ctas", type=int, default=32, help="grid of the side-stream pre-fetch kernel")
     return p.parse_args()
 
 
@@ -142,7 +143,7 @@ def make_timing_event(torch):
 # ------------------------------------------------------------------ the GPU workload
 
 class DecodeStep:
-    def __init__(self, W, layers, seed=0, mode="fused"):
+    def __init__(self, W, layers, seed=0, mode="fused", gather_ctas=32):
         import torch
 
         import bit_kv_cache_spc_gb300 as spc
@@ -184,7 +185,7 @@ class DecodeStep:
         self.selected = [torch.cuda.Event() for _ in range(layers)]
         self.gathered = [torch.cuda.Event() for _ in range(layers)]
         self.mode = mode
-        self.gather_ctas = 32
+        self.gather_ctas = gather_ctas
         self.t0, self.rec = make_timing_event(torch)
         self.attn_ev = [(make_timing_event(torch)[0], make_timing_event(torch)[0]) for _ in range(layers)]
         # pre-decoding step: plain low-bit attention, first top-k and prefetch
@@ -407,7 +408,7 @@ def main():
         torch.cuda.set_device(0)
     peaks, peak_src = measured_peaks()
 
-    step = DecodeStep(W, args.layers, mode=args.prefetch)
+    step = DecodeStep(W, args.layers, mode=args.prefetch, gather_ctas=args.gather_ctas)
     step.capture()
     for _ in range(max(3, args.warmup)):
         step.replay()
