@@ -34,7 +34,7 @@ WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=
 METRIC = "decode attn steps/s at 32K ctx, 1-bit, top-1% (HBM GB/s and % of peak in roofline)"
 # DRAM bytes (read + write) of one merged-attention launch of this workload, from the ncu capture
 # summarised in profiles/attn_kernel_llama3_8b_32k.md; None once the kernel changes after that capture.
-ATTN_TRAFFIC_BYTES = None
+ATTN_TRAFFIC_BYTES = 175594496
 
 
 def parse():
@@ -188,6 +188,7 @@ class DecodeStep:
         self.gather_ctas = gather_ctas
         self.t0, self.rec = make_timing_event(torch)
         self.attn_ev = [(make_timing_event(torch)[0], make_timing_event(torch)[0]) for _ in range(layers)]
+        self.topk_ev = [(make_timing_event(torch)[0], make_timing_event(torch)[0]) for _ in range(layers)]
         # pre-decoding step: plain low-bit attention, first top-k and prefetch
         with torch.cuda.stream(self.main):
             for l in range(layers):
@@ -223,7 +224,10 @@ class DecodeStep:
                                 stream=main)
             if timed:
                 self.rec(self.attn_ev[l][1], main)
+                self.rec(self.topk_ev[l][0], main)
             spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=main)
+            if timed:
+                self.rec(self.topk_ev[l][1], main)
             self.selected[l].record(main)
             side.wait_event(self.selected[l])
             spc.spc_host_gather(d, self.host[l], self.W["N"], self.idx[l], k, self.staging[l],
@@ -250,7 +254,10 @@ class DecodeStep:
                                       ws_bytes=self.ws_bytes, stream=main)
             if timed:
                 self.rec(self.attn_ev[l][1], main)
+                self.rec(self.topk_ev[l][0], main)
             spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=main)
+            if timed:
+                self.rec(self.topk_ev[l][1], main)
 
     def capture(self):
         torch = self.torch
@@ -270,6 +277,9 @@ class DecodeStep:
 
     def attn_ms(self):
         return [s.elapsed_time(e) for (s, e) in self.attn_ev]
+
+    def topk_ms(self):
+        return [s.elapsed_time(e) for (s, e) in self.topk_ev]
 
 
 def host_link_probe(step, reps=20):
@@ -431,6 +441,7 @@ def main():
         barrier()
     # the per-layer attention events inside the graph hold the last timed step
     per_layer = step.attn_ms()
+    per_layer_topk = step.topk_ms()
     total_ms = start.elapsed_time(end)
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -484,9 +495,10 @@ def main():
                        "bits": W["bits"], "k": W["k"], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (4.3 GB low-bit cache per step, 129 MB L2); no flush",
                        "graph": "one CUDA graph per step",
-                       "prefetch": ("side stream, 32 persistent CTAs" if args.prefetch == "side"
+                       "prefetch": (f"side stream, {args.gather_ctas} CTAs" if args.prefetch == "side"
                                     else "fused into the next layer's attention")},
-            "roofline": roof, "gather": gather, "clocks": clk.summary(), "e2e": e2e,
+            "roofline": roof, "gather": gather,
+            "per_layer_us": {"attention": attn_avg_ms * 1000.0, "topk": statistics.mean(per_layer_topk) * 1000.0}, "clocks": clk.summary(), "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps}
     if rank == 0 and not args.no_cpu_baseline:
         ref = OracleSample(W, args.cpu_pairs)
