@@ -58,6 +58,7 @@ def lib():
                                     C.c_int32, P, P, P]
         L.orc_topk.argtypes = [C.POINTER(orc_dims), P, C.c_int32, P, P]
         L.orc_gather.argtypes = [C.POINTER(orc_dims), P, C.c_int64, P, C.c_int32, P]
+        L.orc_append.argtypes = [C.POINTER(orc_dims), C.c_int32, C.c_int32, P, P, P, P, P, C.c_int64]
         _lib = L
     return _lib
 
@@ -119,9 +120,9 @@ def pack(d: orc_dims, qz, K, V, q_groups_cap=None, resid_cap=None):
     resid_cap = (d.N - n_q) if resid_cap is None else resid_cap
     rec = np.zeros((d.B, d.Hkv, q_groups_cap, record_bytes(d.bits)), np.uint8)
     res = np.zeros((d.B, d.Hkv, max(resid_cap, 0), 2, d.D), np.uint16)
+    Kc, Vc = _c(K, np.uint16), _c(V, np.uint16)  # held until the call returns
     lib().orc_pack(C.byref(d), _p(qz["kcode"]), _p(qz["kmm"]), _p(qz["vcode"]), _p(qz["vmm"]),
-                   _p(_c(K, np.uint16)), _p(_c(V, np.uint16)), q_groups_cap, resid_cap,
-                   _p(rec), _p(res))
+                   _p(Kc), _p(Vc), q_groups_cap, resid_cap, _p(rec), _p(res))
     return rec, res
 
 
@@ -151,6 +152,17 @@ def topk(d: orc_dims, S, k: int):
     bm = np.zeros((d.B, d.Hkv, (n_q + 31) // 32), np.uint32)
     lib().orc_topk(C.byref(d), _p(S), k, _p(idx), _p(bm))
     return idx, bm
+
+
+def append(d: orc_dims, records, resid, k_new, v_new, host=None):
+    """Decode-time append of token d.N, in place on the packed cache (records
+    [B,Hkv,q_groups_cap,RB] u8, resid [B,Hkv,resid_cap,2,D] bf16) and, if
+    given, the host cache [B,Hkv,n_cap,2,D].  The caller then advances d.N."""
+    for a in (records, resid) + (() if host is None else (host,)):
+        assert a.flags["C_CONTIGUOUS"], "append works in place on contiguous arrays"
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)  # held until the call returns
+    lib().orc_append(C.byref(d), int(records.shape[2]), int(resid.shape[2]), _p(kn), _p(vn),
+                     _p(records), _p(resid), _p(host), 0 if host is None else int(host.shape[2]))
 
 
 def gather(d: orc_dims, host, idx):

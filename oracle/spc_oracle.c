@@ -373,3 +373,50 @@ void orc_gather(const orc_dims* d, const uint16_t* host, int64_t n_cap,
       }
     }
 }
+
+void orc_append(const orc_dims* d, int32_t q_groups_cap, int32_t resid_cap,
+                const uint16_t* k_new, const uint16_t* v_new,
+                uint8_t* records, uint16_t* resid, uint16_t* host, int64_t n_cap) {
+  const int32_t B = d->B, H = d->Hkv, D = d->D, N = d->N, nq = orc_nq(d), r = N - nq;
+  orc_dims next = *d;
+  next.N = N + 1;
+  const int flush = orc_nq(&next) > nq;
+  /* one 32-token group of one (b, hkv), quantised and packed on its own */
+  orc_dims one = *d;
+  one.B = 1;
+  one.Hkv = 1;
+  one.N = 32;
+  one.R = 0;
+  const int64_t RB = orc_record_bytes(d->bits);
+  uint16_t* K32 = malloc(sizeof(uint16_t) * 32 * (size_t)D);
+  uint16_t* V32 = malloc(sizeof(uint16_t) * 32 * (size_t)D);
+  uint8_t* kcode = malloc((size_t)32 * D);
+  uint8_t* vcode = malloc((size_t)32 * D);
+  uint16_t* kmm = malloc(sizeof(uint16_t) * 2 * (size_t)D);
+  uint16_t* vmm = malloc(sizeof(uint16_t) * 2 * 32 * (size_t)(D / 32));
+  for (int32_t b = 0; b < B; ++b)
+    for (int32_t h = 0; h < H; ++h) {
+      const int64_t bh = (int64_t)b * H + h;
+      uint16_t* win = resid + bh * resid_cap * 2 * D; /* row j: K at win + 2Dj, V at + D */
+      memcpy(win + (int64_t)r * 2 * D, k_new + bh * D, sizeof(uint16_t) * (size_t)D);
+      memcpy(win + (int64_t)r * 2 * D + D, v_new + bh * D, sizeof(uint16_t) * (size_t)D);
+      if (host != NULL) {
+        memcpy(host + (bh * n_cap + N) * 2 * D, k_new + bh * D, sizeof(uint16_t) * (size_t)D);
+        memcpy(host + (bh * n_cap + N) * 2 * D + D, v_new + bh * D, sizeof(uint16_t) * (size_t)D);
+      }
+      if (!flush) continue;
+      for (int32_t j = 0; j < 32; ++j) {
+        memcpy(K32 + (int64_t)j * D, win + (int64_t)j * 2 * D, sizeof(uint16_t) * (size_t)D);
+        memcpy(V32 + (int64_t)j * D, win + (int64_t)j * 2 * D + D, sizeof(uint16_t) * (size_t)D);
+      }
+      orc_quantize(&one, 0, K32, V32, kcode, kmm, vcode, vmm);
+      orc_pack(&one, kcode, kmm, vcode, vmm, K32, V32, 1, 0, records + (bh * q_groups_cap + nq / 32) * RB, NULL);
+      memmove(win, win + 32 * 2 * D, sizeof(uint16_t) * 2 * (size_t)D * (size_t)(r + 1 - 32));
+    }
+  free(K32);
+  free(V32);
+  free(kcode);
+  free(vcode);
+  free(kmm);
+  free(vmm);
+}

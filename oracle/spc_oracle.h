@@ -99,6 +99,19 @@ void orc_topk(const orc_dims* d, const double* S, int32_t k, int32_t* idx, uint3
 void orc_gather(const orc_dims* d, const uint16_t* host, int64_t n_cap,
                 const int32_t* idx, int32_t k, uint16_t* staging);
 
+/* Decode-time append (SpeCache page, section 3 "Decoding", Algorithm 3: the
+ * new token's K/V joins the cache; section 3's offload of the 16-bit cache to
+ * CPU memory).  d describes the cache before the call (d->N tokens held as
+ * records [B,Hkv,q_groups_cap,RB] and the residual window resid
+ * [B,Hkv,resid_cap,2,D], as orc_pack lays them out).  Token N's rows k_new,
+ * v_new (bf16 [B,Hkv,D]) go to window row r = N - N_q; when N+1 tokens
+ * quantise one more group, the window's oldest 32 rows are quantised as group
+ * N_q/32 (orc_quantize on those rows), packed into its record, and dropped
+ * from the window.  host (bf16 [B,Hkv,n_cap,2,D], may be NULL) receives row N. */
+void orc_append(const orc_dims* d, int32_t q_groups_cap, int32_t resid_cap,
+                const uint16_t* k_new, const uint16_t* v_new,
+                uint8_t* records, uint16_t* resid, uint16_t* host, int64_t n_cap);
+
 #ifdef __cplusplus
 }
 #endif

@@ -359,3 +359,37 @@ def test_pack_places_every_bit_exactly_once():
                         assert len(on) == 1
                         (seen_k if which == "kcode" else seen_v).add(int(on[0]))
         assert len(seen_k) == len(seen_v) == bits * 11 * 26
+
+
+@pytest.mark.parametrize("bits,R,N0,T", [(1, 8, 30, 45), (2, 8, 71, 40), (1, 0, 0, 70), (2, 128, 100, 70)])
+def test_append_one_token_at_a_time_equals_quantising_the_sequence(bits, R, N0, T):
+    """Decode-time append (SpeCache section 3, Algorithm 3): after tokens
+    N0 .. N0+T-1 join one by one, the packed cache must be the one that
+    quantising all N0+T tokens at once gives (group boundaries and codes
+    depend only on the tokens), and the host cache must hold every row.  The
+    runs cross at least one flush; R = 0 flushes the group the new row
+    completes."""
+    B, Hkv, D = 2, 2, 128
+    N1 = N0 + T
+    K, V = synth.kv_layer(11, bits, B, Hkv, N1, D)
+    cap = N1 // 32 + 1
+    rcap = R + 32
+    d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N0, R=R, bits=bits)
+    qz = oracle.quantize(d, K[:, :, :N0], V[:, :, :N0])
+    rec, res = oracle.pack(d, qz, K[:, :, :N0], V[:, :, :N0], q_groups_cap=cap, resid_cap=rcap)
+    host = np.zeros((B, Hkv, N1 + 3, 2, D), np.uint16)
+    host[:, :, :N0] = np.stack([K[:, :, :N0], V[:, :, :N0]], axis=3)
+    flushes = 0
+    for n in range(N0, N1):
+        before = oracle.nq(d)
+        oracle.append(d, rec, res, K[:, :, n], V[:, :, n], host)
+        d.N += 1
+        flushes += oracle.nq(d) > before
+    assert flushes >= 1
+    d1 = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N1, R=R, bits=bits)
+    nq1 = oracle.nq(d1)
+    rec1, res1 = oracle.pack(d1, oracle.quantize(d1, K, V), K, V, q_groups_cap=cap, resid_cap=rcap)
+    assert np.array_equal(rec[:, :, :nq1 // 32], rec1[:, :, :nq1 // 32])
+    assert np.array_equal(res[:, :, :N1 - nq1], res1[:, :, :N1 - nq1])
+    assert np.array_equal(host[:, :, :N1], np.stack([K, V], axis=3))
+    assert not host[:, :, N1:].any()
