@@ -78,6 +78,7 @@ _sig = {
                                         C.c_int64, _P, C.c_int32, _P, _P]),
     "spc_topk_select": (C.c_int, [_D, _P, _P, C.c_int32, _P, _P, _P]),
     "spc_host_gather": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, C.c_int32, _P]),
+    "spc_append_kv": (C.c_int, [_D, _P, _P, _P, _P, _P, C.c_int64, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -167,6 +168,11 @@ def spc_merged_attn_noalloc(d, records, resid, q, idx, bitmap, staging, k, o, ls
 def spc_topk_select(d, spec_logits, lse, k, idx, bitmap, stream=None):
     _check("spc_topk_select", _lib.spc_topk_select(C.byref(d), _ptr(spec_logits), _ptr(lse), int(k), _ptr(idx),
                                                    _ptr(bitmap), _stream(stream)))
+
+
+def spc_append_kv(d, k_new, v_new, records, resid, host_kv=None, n_cap=0, stream=None):
+    _check("spc_append_kv", _lib.spc_append_kv(C.byref(d), _ptr(k_new), _ptr(v_new), _ptr(records), _ptr(resid),
+                                               _ptr(host_kv), int(n_cap), _stream(stream)))
 
 
 def spc_host_gather(d, host_kv, n_cap, idx, k, staging, max_ctas=0, stream=None):

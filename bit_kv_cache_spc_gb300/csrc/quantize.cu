@@ -77,14 +77,130 @@ __device__ __forceinline__ int vmeta_word(int n, int cg) {
   return 32 * ((n16 & 7) >> 1) + 16 * (n >> 4) + 4 * (2 * (n16 >> 3) + (n16 & 1)) + cg;
 }
 
+// Codes one 32-token group from the tiles ks, vs ([token][channel] bf16 in
+// shared memory) into its record at dst.  Every thread of the 128-thread CTA
+// takes part; the tiles may be reused once this returns.
+template <int BITS>
+__device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, const uint16_t* vs, uint8_t* dst_rec) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int rb = 1024 * (BITS + 1);
+  constexpr int KMETA = 128 * BITS, VCODES = KMETA + 128, VMETA = VCODES + 128 * BITS;  // in words
+  // Lane beta's key channels for word t are base + 2t, base = 16 k + 8 h + half
+  // with (half, k, h) = (beta >> 4, (beta >> 1) & 7, beta & 1): all four lie in
+  // the 16-byte block at channel 16 k + 8 h, at halves 2t + half.
+  const int half = lane >> 4, kk = (lane >> 1) & 7, hh = lane & 1;
+  const int kblock = 16 * kk + 8 * hh;
+
+  // ---- key group parameters: thread = channel ----
+  {
+    const int c = tid;
+    float lo = bf16_to_f32(ks[c]), hi = lo;
+#pragma unroll 8
+    for (int n = 1; n < kGroup; ++n) {
+      const float x = bf16_to_f32(ks[n * kD + c]);
+      lo = fminf(lo, x);
+      hi = fmaxf(hi, x);
+    }
+    float z, s;
+    quant_params(BITS, lo, hi, z, s);
+    sm.kz[c] = z;
+    sm.kss[c] = s;
+    sm.krs[c] = s != 0.0f ? __frcp_rn(s) : 0.0f;
+    sm.klohi[c] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
+  }
+  __syncthreads();
+
+  // ---- key codes: warp per token, one ballot per code word ----
+  {
+    float z[4], s[4], rs[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int c = kblock + 2 * t + half;
+      z[t] = sm.kz[c];
+      s[t] = sm.kss[c];
+      rs[t] = sm.krs[c];
+    }
+    for (int n = 8 * warp; n < 8 * warp + 8; ++n) {  // token n = 8 j + a
+      const uint4 blk = *reinterpret_cast<const uint4*>(ks + n * kD + kblock);
+      const uint32_t wv[4] = {blk.x, blk.y, blk.z, blk.w};  // halves 2t, 2t+1 in word t
+      const int j = n >> 3, aa = n & 7;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float x = bf16_to_f32(half ? (wv[t] >> 16) : (wv[t] & 0xFFFFu));
+        const uint32_t code = quant_code<BITS>(x, z[t], s[t], rs[t]);
+        const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, code & 1u);
+        const int word = 4 * (4 * aa + t) + j;
+        if (BITS == 2) {
+          const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, code >> 1);
+          if (lane == 1) sm.rec[128 + word] = b1;
+        }
+        if (lane == 0) sm.rec[word] = b0;
+      }
+    }
+  }
+
+  // ---- value parameters and codes: warp per token pair ----
+  for (int p = 4 * warp; p < 4 * warp + 4; ++p) {
+    const int n = 2 * p + half;  // this lane's token
+    const uint4 blk = *reinterpret_cast<const uint4*>(vs + n * kD + kblock);  // channels kblock .. +7
+    const uint32_t wv[4] = {blk.x, blk.y, blk.z, blk.w};
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = bf16_to_f32(wv[e] & 0xFFFFu);
+      x[2 * e + 1] = bf16_to_f32(wv[e] >> 16);
+    }
+    float lo = x[0], hi = x[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e) {
+      lo = fminf(lo, x[e]);
+      hi = fmaxf(hi, x[e]);
+    }
+    // the 32-channel group cg = kk >> 1 spans the four lanes that differ in bits 0..1
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
+      hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
+    }
+    float z, s;
+    quant_params(BITS, lo, hi, z, s);
+    const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
+    if ((lane & 3) == 0)
+      sm.rec[VMETA + vmeta_word(n, kk >> 1)] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
+    const int t = p & 3, j = 2 * (p >> 3) + ((p >> 2) & 1);
+#pragma unroll
+    for (int aa = 0; aa < 8; ++aa) {  // channel kblock + aa = 16 k + 8 h + a
+      const uint32_t code = quant_code<BITS>(x[aa], z, s, rs);
+      const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, code & 1u);
+      const int word = 4 * (4 * aa + t) + j;
+      if (BITS == 2) {
+        const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, code >> 1);
+        if (lane == 1) sm.rec[VCODES + 128 + word] = b1;
+      }
+      if (lane == 0) sm.rec[VCODES + word] = b0;
+    }
+  }
+  {
+    const int tt = tid >> 5, m = tid & 31;
+    const int kc = 16 * (m >> 2) + 2 * tt + 8 * ((m >> 1) & 1) + (m & 1);
+    sm.rec[KMETA + tid] = sm.klohi[kc];
+  }
+  __syncthreads();
+
+  // ---- the record out, coalesced ----
+  uint4* dst = reinterpret_cast<uint4*>(dst_rec);
+  const uint4* src = reinterpret_cast<const uint4*>(sm.rec);
+  for (int i = tid; i < rb / 16; i += 128) __stcs(dst + i, src[i]);
+  __syncthreads();  // the record buffer is reused by the next group
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t qsmem[];
   QuantSmem& sm = *reinterpret_cast<QuantSmem*>(qsmem);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int ng = a.nq / kGroup;
   constexpr int rb = 1024 * (BITS + 1);
-  constexpr int KMETA = 128 * BITS, VCODES = KMETA + 128, VMETA = VCODES + 128 * BITS;  // in words
 
   auto load = [&](int64_t gi, int buf) {
     if (gi < a.total_groups) {
@@ -102,124 +218,16 @@ __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
     cp_async_commit();
   };
 
-  // Lane beta's key channels for word t are base + 2t, base = 16 k + 8 h + half
-  // with (half, k, h) = (beta >> 4, (beta >> 1) & 7, beta & 1): all four lie in
-  // the 16-byte block at channel 16 k + 8 h, at halves 2t + half.
-  const int half = lane >> 4, kk = (lane >> 1) & 7, hh = lane & 1;
-  const int kblock = 16 * kk + 8 * hh;
-
   int buf = 0;
   load(blockIdx.x, 0);
   for (int64_t gi = blockIdx.x; gi < a.total_groups; gi += gridDim.x, buf ^= 1) {
     load(gi + gridDim.x, buf ^ 1);
     cp_async_wait<1>();
     __syncthreads();
-    const uint16_t* ks = sm.ks[buf];
-    const uint16_t* vs = sm.vs[buf];
-
-    // ---- key group parameters: thread = channel ----
-    {
-      const int c = tid;
-      float lo = bf16_to_f32(ks[c]), hi = lo;
-#pragma unroll 8
-      for (int n = 1; n < kGroup; ++n) {
-        const float x = bf16_to_f32(ks[n * kD + c]);
-        lo = fminf(lo, x);
-        hi = fmaxf(hi, x);
-      }
-      float z, s;
-      quant_params(BITS, lo, hi, z, s);
-      sm.kz[c] = z;
-      sm.kss[c] = s;
-      sm.krs[c] = s != 0.0f ? __frcp_rn(s) : 0.0f;
-      sm.klohi[c] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
-    }
-    __syncthreads();
-
-    // ---- key codes: warp per token, one ballot per code word ----
-    {
-      float z[4], s[4], rs[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int c = kblock + 2 * t + half;
-        z[t] = sm.kz[c];
-        s[t] = sm.kss[c];
-        rs[t] = sm.krs[c];
-      }
-      for (int n = 8 * warp; n < 8 * warp + 8; ++n) {  // token n = 8 j + a
-        const uint4 blk = *reinterpret_cast<const uint4*>(ks + n * kD + kblock);
-        const uint32_t wv[4] = {blk.x, blk.y, blk.z, blk.w};  // halves 2t, 2t+1 in word t
-        const int j = n >> 3, aa = n & 7;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float x = bf16_to_f32(half ? (wv[t] >> 16) : (wv[t] & 0xFFFFu));
-          const uint32_t code = quant_code<BITS>(x, z[t], s[t], rs[t]);
-          const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, code & 1u);
-          const int word = 4 * (4 * aa + t) + j;
-          if (BITS == 2) {
-            const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, code >> 1);
-            if (lane == 1) sm.rec[128 + word] = b1;
-          }
-          if (lane == 0) sm.rec[word] = b0;
-        }
-      }
-    }
-
-    // ---- value parameters and codes: warp per token pair ----
-    for (int p = 4 * warp; p < 4 * warp + 4; ++p) {
-      const int n = 2 * p + half;  // this lane's token
-      const uint4 blk = *reinterpret_cast<const uint4*>(vs + n * kD + kblock);  // channels kblock .. +7
-      const uint32_t wv[4] = {blk.x, blk.y, blk.z, blk.w};
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16_to_f32(wv[e] & 0xFFFFu);
-        x[2 * e + 1] = bf16_to_f32(wv[e] >> 16);
-      }
-      float lo = x[0], hi = x[0];
-#pragma unroll
-      for (int e = 1; e < 8; ++e) {
-        lo = fminf(lo, x[e]);
-        hi = fmaxf(hi, x[e]);
-      }
-      // the 32-channel group cg = kk >> 1 spans the four lanes that differ in bits 0..1
-#pragma unroll
-      for (int off = 1; off <= 2; off <<= 1) {
-        lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
-        hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
-      }
-      float z, s;
-      quant_params(BITS, lo, hi, z, s);
-      const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
-      if ((lane & 3) == 0)
-        sm.rec[VMETA + vmeta_word(n, kk >> 1)] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
-      const int t = p & 3, j = 2 * (p >> 3) + ((p >> 2) & 1);
-#pragma unroll
-      for (int aa = 0; aa < 8; ++aa) {  // channel kblock + aa = 16 k + 8 h + a
-        const uint32_t code = quant_code<BITS>(x[aa], z, s, rs);
-        const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, code & 1u);
-        const int word = 4 * (4 * aa + t) + j;
-        if (BITS == 2) {
-          const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, code >> 1);
-          if (lane == 1) sm.rec[VCODES + 128 + word] = b1;
-        }
-        if (lane == 0) sm.rec[VCODES + word] = b0;
-      }
-    }
-    {
-      const int tt = tid >> 5, m = tid & 31;
-      const int kc = 16 * (m >> 2) + 2 * tt + 8 * ((m >> 1) & 1) + (m & 1);
-      sm.rec[KMETA + tid] = sm.klohi[kc];
-    }
-    __syncthreads();
-
-    // ---- the record out, coalesced ----
     const int64_t bh = gi / ng;
     const int g = (int)(gi % ng);
-    uint4* dst = reinterpret_cast<uint4*>(a.records + (bh * a.q_groups_cap + g) * (int64_t)rb);
-    const uint4* src = reinterpret_cast<const uint4*>(sm.rec);
-    for (int i = tid; i < rb / 16; i += 128) __stcs(dst + i, src[i]);
-    __syncthreads();  // the tile buffer is refilled two iterations on, the record buffer next iteration
+    // the tile buffer is refilled two iterations on
+    code_group<BITS>(sm, sm.ks[buf], sm.vs[buf], a.records + (bh * a.q_groups_cap + g) * (int64_t)rb);
   }
   cp_async_wait<0>();
 }
@@ -278,6 +286,105 @@ spc_status launch_quantize(const spc_dims* d, const uint16_t* k, const uint16_t*
                                                          total_vec);
     e = cudaGetLastError();
   }
+  if (e != cudaSuccess) {
+    spc_host::set_cuda_error(e);
+    return SPC_ERR_CUDA;
+  }
+  return SPC_OK;
+}
+
+// ------------------------------------------------------------ decode-time append
+// The new token's K/V joins the cache (SpeCache page, section 3 "Decoding",
+// Algorithm 3) and its 16-bit row goes to the host cache (section 3's offload
+// of the full-precision cache to CPU memory).  One CTA per (b, hkv): the row
+// goes to window row r = N - N_q (and host row N); when N+1 tokens quantise
+// one more group, the window's oldest 32 rows are coded into record N_q/32
+// by the same code_group as the prefill, and the window shifts down by 32.
+struct AppendArgs {
+  const uint16_t* k_new;  // [B][Hkv][D]
+  const uint16_t* v_new;
+  uint8_t* records;
+  uint16_t* resid;        // [B][Hkv][resid_cap][2][D]
+  uint16_t* host;         // device address of [B][Hkv][n_cap][2][D], or null
+  int64_t n_cap;
+  int32_t N, nq, r, resid_cap, q_groups_cap, flush;
+};
+
+template <int BITS>
+__global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+  extern __shared__ __align__(16) uint8_t qsmem[];
+  QuantSmem& sm = *reinterpret_cast<QuantSmem*>(qsmem);
+  const int tid = threadIdx.x;
+  const int64_t bh = blockIdx.x;
+  uint4* win = reinterpret_cast<uint4*>(a.resid + bh * a.resid_cap * 2 * kD);  // 32 uint4 per row: K then V
+  if (tid < 32) {
+    const uint4 v = tid < 16 ? reinterpret_cast<const uint4*>(a.k_new + bh * kD)[tid]
+                             : reinterpret_cast<const uint4*>(a.v_new + bh * kD)[tid - 16];
+    win[(int64_t)a.r * 32 + tid] = v;
+    if (a.host != nullptr) reinterpret_cast<uint4*>(a.host + (bh * a.n_cap + a.N) * 2 * kD)[tid] = v;
+  }
+  if (!a.flush) return;
+  __syncthreads();  // the new row may belong to the group being flushed
+  for (int i = tid; i < kGroup * 32; i += 128) {  // window rows 0..31 -> [token][channel] tiles
+    const int n = i >> 5, q = i & 31;
+    const uint4 v = win[n * 32 + q];
+    if (q < 16) reinterpret_cast<uint4*>(sm.ks[0] + n * kD)[q] = v;
+    else reinterpret_cast<uint4*>(sm.vs[0] + n * kD)[q - 16] = v;
+  }
+  __syncthreads();
+  constexpr int rb = 1024 * (BITS + 1);
+  code_group<BITS>(sm, sm.ks[0], sm.vs[0], a.records + (bh * a.q_groups_cap + a.nq / kGroup) * (int64_t)rb);
+  // rows 32 .. r move to 0 .. r-32, 32 rows at a time: a chunk's sources lie
+  // past every destination written before it, and it is read in full before
+  // it is written
+  const int keep = a.r + 1 - kGroup;
+  for (int c0 = 0; c0 < keep; c0 += kGroup) {
+    const int rows = min(kGroup, keep - c0);
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = tid + 128 * u, n = i >> 5;
+      if (n < rows) v[u] = win[(int64_t)(kGroup + c0 + n) * 32 + (i & 31)];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = tid + 128 * u, n = i >> 5;
+      if (n < rows) win[(int64_t)(c0 + n) * 32 + (i & 31)] = v[u];
+    }
+    __syncthreads();
+  }
+}
+
+spc_status launch_append(const spc_dims* d, const uint16_t* k_new, const uint16_t* v_new, void* records,
+                         uint16_t* resid, uint16_t* host_dev, int64_t n_cap, cudaStream_t stream) {
+  AppendArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.records = static_cast<uint8_t*>(records);
+  a.resid = resid;
+  a.host = host_dev;
+  a.n_cap = n_cap;
+  a.N = d->N;
+  a.nq = num_quantized(d->N, d->R);
+  a.r = d->N - a.nq;
+  a.resid_cap = d->resid_cap;
+  a.q_groups_cap = d->q_groups_cap;
+  a.flush = num_quantized(d->N + 1, d->R) > a.nq ? 1 : 0;
+  const int64_t BH = (int64_t)d->B * d->Hkv;
+  if (BH == 0) return SPC_OK;
+  const int smem = (int)sizeof(QuantSmem);
+  cudaError_t e;
+  if (d->bits == 1) {
+    static unsigned long long configured = 0ull;
+    e = spc_host::ensure_smem_limit(configured, append_kernel<1>, smem);
+    if (e == cudaSuccess) append_kernel<1><<<(unsigned)BH, 128, smem, stream>>>(a);
+  } else {
+    static unsigned long long configured = 0ull;
+    e = spc_host::ensure_smem_limit(configured, append_kernel<2>, smem);
+    if (e == cudaSuccess) append_kernel<2><<<(unsigned)BH, 128, smem, stream>>>(a);
+  }
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);
     return SPC_ERR_CUDA;

@@ -15,6 +15,8 @@ spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const
 spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t);
 spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
                               int32_t, cudaStream_t);
+spc_status launch_append(const spc_dims*, const uint16_t*, const uint16_t*, void*, uint16_t*, uint16_t*, int64_t,
+                         cudaStream_t);
 }  // namespace spc
 
 namespace spc_host {
@@ -150,6 +152,28 @@ spc_status spc_quantize_kv(const spc_dims* d, const uint16_t* k, const uint16_t*
   if (d->N - nq > 0 && resid == nullptr) return SPC_ERR_INVALID;
   if (!aligned16(k) || !aligned16(v) || !aligned16(records) || !aligned16(resid)) return SPC_ERR_INVALID;
   return spc::launch_quantize(d, k, v, records, resid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spc_status spc_append_kv(const spc_dims* d, const uint16_t* k_new, const uint16_t* v_new, void* records,
+                         uint16_t* resid, uint16_t* host_kv, int64_t n_cap, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  if (d->N >= (1 << 30)) return SPC_ERR_INVALID;
+  const int32_t nq = spc::num_quantized(d->N, d->R);
+  const int32_t nq1 = spc::num_quantized(d->N + 1, d->R);
+  if (k_new == nullptr || v_new == nullptr || resid == nullptr) return SPC_ERR_INVALID;
+  if (d->N - nq + 1 > d->resid_cap) return SPC_ERR_INVALID;  // room for the new row
+  if (nq1 > nq && (records == nullptr || nq1 / spc::kGroup > d->q_groups_cap)) return SPC_ERR_INVALID;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(records) || !aligned16(resid) || !aligned16(host_kv))
+    return SPC_ERR_INVALID;
+  const void* host_dev = nullptr;
+  if (host_kv != nullptr) {
+    if (n_cap <= d->N) return SPC_ERR_INVALID;
+    st = mapped_device_pointer(host_kv, &host_dev);
+    if (st != SPC_OK) return st;
+  }
+  return spc::launch_append(d, k_new, v_new, records, resid, static_cast<uint16_t*>(const_cast<void*>(host_dev)),
+                            n_cap, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t spc_attn_workspace_bytes(const spc_dims* d, int32_t k_max) {

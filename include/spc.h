@@ -198,6 +198,27 @@ spc_status spc_merged_attn_noalloc(const spc_dims* d, const void* records, const
                                    float* spec_logits, spc_stream stream);
 
 /*
+ * Decode-time append (SpeCache page, section 3 "Decoding", Algorithm 3: the
+ * new token's K/V joins the cache; section 3: the full-precision cache is
+ * offloaded to CPU memory).  d describes the cache BEFORE the call: N tokens
+ * held as records + resid, as spc_quantize_kv (or earlier appends) left them.
+ * Afterwards the cache holds N+1 tokens and the caller advances d->N.
+ *   k_new, v_new: bf16 [B][Hkv][D], token N's key and value rows (device).
+ *   records, resid: the cache (device), updated in place.
+ *   host_kv: HOST pointer to the pinned, mapped full-precision cache
+ *            [B][Hkv][n_cap][2][D] (row N is written), or NULL for no
+ *            offload; SPC_ERR_NOT_MAPPED if not mapped; n_cap > N.
+ * The new row goes to window row r = N - N_q.  When N+1 tokens quantise one
+ * more group (N_q' = N_q + 32), the window's oldest 32 rows are quantised
+ * into record N_q/32 and the window shifts down by 32 rows; the result is
+ * bit-identical to spc_quantize_kv over all N+1 tokens.  Needs
+ * resid_cap >= N - N_q + 1 and, at a flush, q_groups_cap >= N_q'/32
+ * (SPC_ERR_INVALID otherwise).  One launch on `stream`.
+ */
+spc_status spc_append_kv(const spc_dims* d, const uint16_t* k_new, const uint16_t* v_new, void* records,
+                         uint16_t* resid, uint16_t* host_kv, int64_t n_cap, spc_stream stream);
+
+/*
  * ArgTopK(A_{1,:}) (Algorithm 3): per (b, hkv), the k_eff = min(k, N_q)
  * quantised positions n with the largest score
  *   S(n) = sum over the G query heads h of KV head hkv of

@@ -24,7 +24,8 @@ def spc():
 
 def test_header_declares_the_hot_path():
     names = declared_functions()
-    for fn in ("spc_quantize_kv", "spc_decode_attn2", "spc_topk_select", "spc_host_gather", "spc_merged_attn"):
+    for fn in ("spc_quantize_kv", "spc_decode_attn2", "spc_topk_select", "spc_host_gather", "spc_merged_attn",
+               "spc_merged_attn_fetch", "spc_append_kv"):
         assert fn in names
 
 
@@ -66,4 +67,26 @@ def test_validation_happens_before_any_launch(spc):
     assert e.value.status == 1
     with pytest.raises(spc.SpcError) as e:  # negative k
         spc.spc_topk_select(d, 16, 16, -1, 16, 16, stream=0)
+    assert e.value.status == 1
+
+
+def test_append_validation(spc):
+    """The append needs room for the new window row and, at a flush, for the
+    new record; both are checked before any launch."""
+    d = spc.Dims(1, 32, 8, 1000, 32, 1)  # resid_cap defaults to exactly r: no room
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_append_kv(d, 16, 16, 16, 16, stream=0)
+    assert e.value.status == 1
+    # N = 1023, R = 32: the 1024th token completes group 30 (N_q 960 -> 992)
+    full = spc.Dims(1, 32, 8, 1023, 32, 1, resid_cap=64)
+    assert spc.spc_num_quantized(full) == 960
+    with pytest.raises(spc.SpcError) as e:  # q_groups_cap = 30 has no slot for record 30
+        spc.spc_append_kv(full, 16, 16, 16, 16, stream=0)
+    assert e.value.status == 1
+    ok_caps = spc.Dims(1, 32, 8, 1023, 32, 1, q_groups_cap=31, resid_cap=64)
+    with pytest.raises(spc.SpcError) as e:  # misaligned new key row
+        spc.spc_append_kv(ok_caps, 18, 16, 16, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # host cache too short for row N
+        spc.spc_append_kv(ok_caps, 16, 16, 16, 16, host_kv=16, n_cap=1023, stream=0)
     assert e.value.status == 1
