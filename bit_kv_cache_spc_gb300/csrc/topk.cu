@@ -220,6 +220,245 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   cluster.sync();  // peers may still read this CTA's counters
 }
 
+// ------------------------------------------------------------ k <= kMaxCand
+// Two-level selection for the usual small k (top 1% of a few ten thousand
+// positions).  Each CTA of the cluster selects its slice's own top-k' (k' =
+// min(k_eff, slice length), ties to the lower position) with a CTA-local radix
+// select and keeps those candidates, in ascending position, in shared memory.
+// Every globally selected position is among its slice's candidates (fewer than
+// k_eff positions of the slice precede it in the order key desc, position asc),
+// so after one cluster barrier the leader CTA selects the final k_eff from the
+// concatenated candidates (already in ascending position) and writes idx and
+// the bitmap.  Two cluster barriers in all, against six for the cluster-wide
+// radix select above.
+constexpr int kMaxCand = 2048;
+
+struct __align__(16) SelShared {
+  uint32_t hist[4][256];  // four sub-histograms (warp & 3) to spread atomic contention
+  uint32_t wsum[2][kTopkWarps];
+  uint32_t sel[2];        // digit search result: prefix, remaining
+  uint32_t count;         // candidates kept by this CTA
+  float nlse[4];          // -lse * log2(e) of the speculative row of each head of the group
+};
+
+// The kth largest (1 <= kth <= n) of keys[0..n): T, and how many keys equal
+// to T belong to the top kth (the other kth - need are > T).
+__device__ __forceinline__ void cta_radix_select(const uint32_t* keys, int n, uint32_t kth, SelShared& sh,
+                                                 uint32_t& T, uint32_t& need) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0u, pmask = 0u, rem = kth;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int j = tid; j < 4 * 256; j += kTopkThreads) (&sh.hist[0][0])[j] = 0u;
+    __syncthreads();
+    uint32_t* h = sh.hist[warp & 3];
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const uint32_t key = keys[i];
+      if (((key ^ prefix) & pmask) == 0u) atomicAdd(&h[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 8l .. 8l+7; find the bin holding the rem-th largest
+      uint32_t cnt[8], own = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int bin = 8 * lane + e;
+        cnt[e] = sh.hist[0][bin] + sh.hist[1][bin] + sh.hist[2][bin] + sh.hist[3][bin];
+        own += cnt[e];
+      }
+      uint32_t above = own;  // inclusive suffix sum over lanes >= this one
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, above, off);
+        if (lane + off < 32) above += v;
+      }
+      above -= own;
+      if (above < rem && rem <= above + own) {
+        uint32_t acc = above;
+        for (int e = 7; e >= 0; --e) {
+          if (acc + cnt[e] >= rem) {
+            sh.sel[0] = prefix | ((uint32_t)(8 * lane + e) << shift);
+            sh.sel[1] = rem - acc;
+            break;
+          }
+          acc += cnt[e];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = sh.sel[0];
+    rem = sh.sel[1];
+    pmask |= 255u << shift;
+  }
+  T = prefix;
+  need = rem;
+}
+
+// Ordered take over keys[0..n) (n <= 32 * kTopkThreads): element i is taken
+// if keys[i] > T, or keys[i] == T and fewer than `need` elements equal to T
+// precede it; emit(i, rank) is called for each taken element with its rank
+// among the taken ones (so ranks follow i).  wgt, weq: one word each per 32
+// elements.
+template <typename Emit>
+__device__ __forceinline__ void ordered_take(const uint32_t* keys, int n, uint32_t T, uint32_t need,
+                                             uint32_t* wgt, uint32_t* weq, SelShared& sh, Emit&& emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = (n + 31) >> 5;
+  for (int w = warp; w < nw; w += kTopkWarps) {
+    const int i = 32 * w + lane;
+    const uint32_t key = i < n ? keys[i] : 0u;
+    const uint32_t bgt = __ballot_sync(0xFFFFFFFFu, i < n && key > T);
+    const uint32_t beq = __ballot_sync(0xFFFFFFFFu, i < n && key == T);
+    if (lane == 0) {
+      wgt[w] = __popc(bgt);
+      weq[w] = __popc(beq);
+    }
+  }
+  __syncthreads();
+  {  // exclusive scan of the word counts, one word per thread
+    const uint32_t g = tid < nw ? wgt[tid] : 0u, e = tid < nw ? weq[tid] : 0u;
+    uint32_t ig = g, ie = e;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, ig, off), ve = __shfl_up_sync(0xFFFFFFFFu, ie, off);
+      if (lane >= off) {
+        ig += vg;
+        ie += ve;
+      }
+    }
+    if (lane == 31) {
+      sh.wsum[0][warp] = ig;
+      sh.wsum[1][warp] = ie;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t sg = sh.wsum[0][lane], se = sh.wsum[1][lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, sg, off), ve = __shfl_up_sync(0xFFFFFFFFu, se, off);
+        if (lane >= off) {
+          sg += vg;
+          se += ve;
+        }
+      }
+      sh.wsum[0][lane] = sg;
+      sh.wsum[1][lane] = se;
+    }
+    __syncthreads();
+    const uint32_t wg0 = warp > 0 ? sh.wsum[0][warp - 1] : 0u, we0 = warp > 0 ? sh.wsum[1][warp - 1] : 0u;
+    if (tid < nw) {
+      wgt[tid] = wg0 + ig - g;
+      weq[tid] = we0 + ie - e;
+    }
+  }
+  __syncthreads();
+  const uint32_t below = (1u << lane) - 1u;
+  for (int w = warp; w < nw; w += kTopkWarps) {
+    const int i = 32 * w + lane;
+    const uint32_t key = i < n ? keys[i] : 0u;
+    const bool gt = i < n && key > T, eq = i < n && key == T;
+    const uint32_t bgt = __ballot_sync(0xFFFFFFFFu, gt), beq = __ballot_sync(0xFFFFFFFFu, eq);
+    const uint32_t eq_before = weq[w] + __popc(beq & below);
+    if (gt || (eq && eq_before < need)) emit(i, wgt[w] + __popc(bgt & below) + min(eq_before, need));
+  }
+  __syncthreads();
+}
+
+// two CTAs of 1024 threads per SM (32 registers), so a cluster per (b, hkv) row fits one wave
+__global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArgs a) {
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(16) uint32_t dyn[];  // keys[slice]; the leader then reuses it for the merge
+  __shared__ uint32_t wgt[kTopkMaxSlice / 32];
+  __shared__ uint32_t weq[kTopkMaxSlice / 32];
+  __shared__ uint32_t ckey[kMaxCand], cpos[kMaxCand];  // this CTA's candidates, ascending position
+  __shared__ SelShared sh;
+
+  const int tid = threadIdx.x;
+  const unsigned rank = cluster.block_rank();
+  const unsigned ncta = cluster.num_blocks();
+  const int64_t bh = blockIdx.y;
+  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
+  const int n0 = (int)rank * a.slice;
+  const int len = max(0, min(a.slice, a.nq - n0));  // multiple of 32
+  constexpr float kLog2e = 1.4426950408889634f;
+  uint32_t* keys = dyn;
+
+  // ---- scores, four positions per thread and round, the round's loads issued up front ----
+  if (tid < 4) sh.nlse[tid] = tid < a.G ? -a.lse[((int64_t)b * 2 + 1) * a.Hq + hk * a.G + tid] * kLog2e : 0.f;
+  __syncthreads();
+  const float* lrow = a.logits + (bh * a.G) * (int64_t)a.Lcap + n0;
+  for (int i = 4 * tid; i < len; i += 4 * kTopkThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi)
+      v[gi] = gi < a.G ? __ldcs(reinterpret_cast<const float4*>(lrow + (int64_t)gi * a.Lcap + i))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      if (gi < a.G) {
+        const float nl = sh.nlse[gi];
+        sc.x += fast_exp2(fmaf(v[gi].x, kLog2e, nl));
+        sc.y += fast_exp2(fmaf(v[gi].y, kLog2e, nl));
+        sc.z += fast_exp2(fmaf(v[gi].z, kLog2e, nl));
+        sc.w += fast_exp2(fmaf(v[gi].w, kLog2e, nl));
+      }
+    }
+    *reinterpret_cast<uint4*>(keys + i) =
+        make_uint4(__float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
+  }
+  __syncthreads();
+
+  // ---- this slice's top-k' candidates ----
+  const uint32_t kloc = (uint32_t)min(a.keff, len);
+  if (kloc > 0) {
+    uint32_t T, need;
+    cta_radix_select(keys, len, kloc, sh, T, need);
+    ordered_take(keys, len, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
+      ckey[r] = keys[i];
+      cpos[r] = (uint32_t)(n0 + i);
+    });
+  }
+  if (tid == 0) sh.count = kloc;
+  cluster.sync();
+
+  if (rank == 0) {
+    // ---- merge: the candidates of every CTA, in rank (= position) order ----
+    uint32_t M = 0;
+    for (unsigned r = 0; r < ncta; ++r) M += cluster.map_shared_rank(&sh, r)->count;
+    uint32_t* mkey = dyn;
+    uint32_t* mpos = dyn + M;
+    uint32_t* sbm = dyn + 2 * M;  // bitmap of the selection, one word per 32 quantised positions
+    const int nwq = a.nq >> 5;
+    for (unsigned r = 0, off = 0; r < ncta; ++r) {
+      const uint32_t cnt = cluster.map_shared_rank(&sh, r)->count;
+      const uint32_t* rk = cluster.map_shared_rank(ckey, r);
+      const uint32_t* rp = cluster.map_shared_rank(cpos, r);
+      for (uint32_t i = tid; i < cnt; i += kTopkThreads) {
+        mkey[off + i] = rk[i];
+        mpos[off + i] = rp[i];
+      }
+      off += cnt;
+    }
+    for (int w = tid; w < nwq; w += kTopkThreads) sbm[w] = 0u;
+    __syncthreads();
+    int32_t* out = a.idx + bh * a.k;
+    if (a.keff > 0) {
+      uint32_t T, need;
+      cta_radix_select(mkey, (int)M, (uint32_t)a.keff, sh, T, need);
+      ordered_take(mkey, (int)M, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
+        const uint32_t p = mpos[i];
+        out[r] = (int32_t)p;
+        atomicOr(&sbm[p >> 5], 1u << (p & 31u));
+      });
+    }
+    for (int j = a.keff + tid; j < a.k; j += kTopkThreads) out[j] = -1;
+    uint32_t* bm = a.bitmap + bh * a.q_groups_cap;
+    for (int w = tid; w < a.q_groups_cap; w += kTopkThreads) bm[w] = w < nwq ? sbm[w] : 0u;
+  }
+  cluster.sync();  // the leader has read every CTA's candidates
+}
+
 spc_status launch_topk(const spc_dims* d, const float* logits, const float* lse, int32_t k, int32_t* idx,
                        uint32_t* bitmap, cudaStream_t stream) {
   TopkArgs a;
@@ -240,9 +479,15 @@ spc_status launch_topk(const spc_dims* d, const float* logits, const float* lse,
   a.slice = std::max(32, ((a.nq + ncta - 1) / ncta + 31) / 32 * 32);
   if (a.slice > kTopkMaxSlice) return SPC_ERR_UNSUPPORTED;
   const int64_t BH = (int64_t)d->B * d->Hkv;
-  const size_t smem = (size_t)a.slice * sizeof(uint32_t);
-  static unsigned long long configured = 0ull;
-  cudaError_t e = spc_host::ensure_smem_limit(configured, topk_kernel, kTopkMaxSlice * (int)sizeof(uint32_t));
+  // two-level selection when every CTA's candidates fit (k <= kMaxCand) and the
+  // leader's merge buffers (keys, positions, bitmap) fit in its dynamic memory
+  const size_t merge_words = 2 * (size_t)ncta * std::min(a.keff, a.slice) + (size_t)(a.nq >> 5);
+  const bool two_level = a.keff <= kMaxCand && merge_words <= (size_t)kTopkMaxSlice;
+  const size_t smem = std::max((size_t)a.slice, two_level ? merge_words : (size_t)0) * sizeof(uint32_t);
+  auto* fn = two_level ? topk_two_level_kernel : topk_kernel;
+  static unsigned long long configured_radix = 0ull, configured_two = 0ull;
+  cudaError_t e = spc_host::ensure_smem_limit(two_level ? configured_two : configured_radix, fn,
+                                              kTopkMaxSlice * (int)sizeof(uint32_t));
   if (e == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ncta, (unsigned)BH, 1);
@@ -256,7 +501,7 @@ spc_status launch_topk(const spc_dims* d, const float* logits, const float* lse,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, topk_kernel, a);
+    e = cudaLaunchKernelEx(&cfg, fn, a);
   }
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);

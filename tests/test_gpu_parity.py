@@ -176,6 +176,20 @@ def test_topk_selection_exact_with_ties_across_cluster():
                 want = np.sort(order[:k])
                 assert np.array_equal(got[b, h], want)
                 assert np.array_equal(bm.cpu().numpy().view(np.uint32)[b, h], bitmap_from_idx(want, d.q_groups_cap))
+    # every score equal: the k lowest positions (k = 2048 is the largest k of the two-level path; k > N_q pads)
+    for N, k, G in [(8320, 2048, 4), (8320, 2049, 4), (1056, 3000, 2), (33024, 328, 4)]:
+        d = spc.Dims(1, 2 * G, 2, N, 128, 1)
+        nq = spc.spc_num_quantized(d)
+        lg = np.full((1, 2, G, nq), -1.5, np.float32)
+        lse = np.full((1, 2, 2 * G), 3.0, np.float32)
+        idx = torch.full((1, 2, k), -7, dtype=torch.int32, device="cuda")
+        bm = torch.full((1, 2, d.q_groups_cap), 0x5A5A, dtype=torch.int32, device="cuda")
+        spc.spc_topk_select(d, torch.from_numpy(lg).cuda(), torch.from_numpy(lse).cuda(), k, idx, bm)
+        want = np.concatenate([np.arange(min(k, nq)), np.full(max(0, k - nq), -1)]).astype(np.int32)
+        for h in range(2):
+            assert np.array_equal(idx.cpu().numpy()[0, h], want)
+            assert np.array_equal(bm.cpu().numpy().view(np.uint32)[0, h],
+                                  bitmap_from_idx(want[want >= 0], d.q_groups_cap))
 
 
 def test_gather_exact_and_unmapped_pointer_refused():
