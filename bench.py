@@ -320,6 +320,42 @@ def host_link_probe(step, reps=20):
             "frac": g_gbs / c_gbs}
 
 
+def append_probe(W, reps=20):
+    """Decode-time append of one token to one layer of the workload's cache
+    (spc_append_kv, host offload included), timed without and with a flush:
+    at N = 32768 the window grows; at N = 32799 the new token completes a
+    group, which is quantised into a record and dropped from the window."""
+    import torch
+    import bit_kv_cache_spc_gb300 as spc
+    import synth.gpu
+    B, Hq, Hkv, R, bits = (W[x] for x in ("B", "Hq", "Hkv", "R", "bits"))
+    N1 = W["N"] + 32
+    K = torch.empty((B, Hkv, N1, 128), dtype=torch.int16, device="cuda")
+    V = torch.empty_like(K)
+    synth.gpu.kv_layer_into(0, 0, K, V)
+    host = torch.empty((B, Hkv, N1, 2, 128), dtype=torch.int16, pin_memory=True)
+    out = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for tag, N in (("no_flush", W["N"]), ("flush", W["N"] + 31)):
+        d = spc.Dims(B, Hq, Hkv, N, R, bits, q_groups_cap=N1 // 32, resid_cap=R + 32)
+        rec = torch.empty(spc.spc_records_bytes(d), dtype=torch.uint8, device="cuda")
+        res = torch.empty(spc.spc_resid_bytes(d) // 2, dtype=torch.int16, device="cuda")
+        kn, vn = K[:, :, N].contiguous(), V[:, :, N].contiguous()
+        ts = []
+        for i in range(reps + 3):
+            spc.spc_quantize_kv(d, K[:, :, :N].contiguous(), V[:, :, :N].contiguous(), rec, res)
+            e0.record()
+            spc.spc_append_kv(d, kn, vn, rec, res, host, N1)
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1) * 1000.0)
+        out[f"{tag}_us"] = statistics.median(ts)
+    del K, V, host
+    out["note"] = "one layer, B*Hkv rows of 512 B to the window and to pinned host memory; a flush codes one group per (b, kv-head)"
+    return out
+
+
 def attention_bytes_per_layer(W, nq, fused=False):
     """Algorithmic HBM bytes of one merged-attention call (one layer): the
     low-bit copy, the residual and fetched 16-bit rows read, q read and o
@@ -487,6 +523,7 @@ def main():
             "step_hbm_gbs": bytes_layer * W["layers"] / (ms_per_step / 1000.0) / 1e9}
 
     gather = host_link_probe(step, reps=20)
+    append = append_probe(W) if rank == 0 else None
 
     line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -498,7 +535,8 @@ def main():
                        "prefetch": (f"side stream, {args.gather_ctas} CTAs" if args.prefetch == "side"
                                     else "fused into the next layer's attention")},
             "roofline": roof, "gather": gather,
-            "per_layer_us": {"attention": attn_avg_ms * 1000.0, "topk": statistics.mean(per_layer_topk) * 1000.0}, "clocks": clk.summary(), "e2e": e2e,
+            "per_layer_us": {"attention": attn_avg_ms * 1000.0, "topk": statistics.mean(per_layer_topk) * 1000.0},
+            "append": append, "clocks": clk.summary(), "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps}
     if rank == 0 and not args.no_cpu_baseline:
         ref = OracleSample(W, args.cpu_pairs)
