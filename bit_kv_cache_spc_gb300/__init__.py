@@ -79,6 +79,7 @@ _sig = {
     "spc_topk_select": (C.c_int, [_D, _P, _P, C.c_int32, _P, _P, _P]),
     "spc_host_gather": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, C.c_int32, _P]),
     "spc_append_kv": (C.c_int, [_D, _P, _P, _P, _P, _P, C.c_int64, _P]),
+    "spc_offload_kv": (C.c_int, [_D, _P, _P, _P, C.c_int64, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -173,6 +174,11 @@ def spc_topk_select(d, spec_logits, lse, k, idx, bitmap, stream=None):
 def spc_append_kv(d, k_new, v_new, records, resid, host_kv=None, n_cap=0, stream=None):
     _check("spc_append_kv", _lib.spc_append_kv(C.byref(d), _ptr(k_new), _ptr(v_new), _ptr(records), _ptr(resid),
                                                _ptr(host_kv), int(n_cap), _stream(stream)))
+
+
+def spc_offload_kv(d, k, v, host_kv, n_cap, stream=None):
+    _check("spc_offload_kv", _lib.spc_offload_kv(C.byref(d), _ptr(k), _ptr(v), _ptr(host_kv), int(n_cap),
+                                                 _stream(stream)))
 
 
 def spc_host_gather(d, host_kv, n_cap, idx, k, staging, max_ctas=0, stream=None):

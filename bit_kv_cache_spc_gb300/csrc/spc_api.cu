@@ -154,6 +154,38 @@ spc_status spc_quantize_kv(const spc_dims* d, const uint16_t* k, const uint16_t*
   return spc::launch_quantize(d, k, v, records, resid, reinterpret_cast<cudaStream_t>(stream));
 }
 
+spc_status spc_offload_kv(const spc_dims* d, const uint16_t* k, const uint16_t* v, uint16_t* host_kv,
+                          int64_t n_cap, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  if (d->N == 0) return SPC_OK;
+  if (k == nullptr || v == nullptr || host_kv == nullptr || n_cap < d->N) return SPC_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(host_kv)) return SPC_ERR_INVALID;
+  const void* host_dev = nullptr;
+  st = mapped_device_pointer(host_kv, &host_dev);  // pinned host memory: the copy engines reach it directly
+  if (st != SPC_OK) return st;
+  const size_t row = (size_t)spc::kD * sizeof(uint16_t);  // 256 bytes
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // rows (b, hkv, n) of K go to host rows (b, hkv, n) at byte 0, of V at byte 256:
+  // one strided copy of all B*Hkv*N rows when n_cap == N, else one per (b, hkv)
+  // run of N rows (the host runs are n_cap rows apart)
+  const int64_t BH = (int64_t)d->B * d->Hkv;
+  const int64_t runs = n_cap == d->N ? 1 : BH;
+  const size_t height = (size_t)(n_cap == d->N ? BH * d->N : d->N);
+  for (int64_t bh = 0; bh < runs; ++bh) {
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint16_t* src = (kv == 0 ? k : v) + bh * (int64_t)d->N * spc::kD;
+      uint16_t* dst = host_kv + (bh * n_cap * 2 + kv) * spc::kD;
+      const cudaError_t e = cudaMemcpy2DAsync(dst, 2 * row, src, row, row, height, cudaMemcpyDeviceToHost, s);
+      if (e != cudaSuccess) {
+        spc_host::set_cuda_error(e);
+        return SPC_ERR_CUDA;
+      }
+    }
+  }
+  return SPC_OK;
+}
+
 spc_status spc_append_kv(const spc_dims* d, const uint16_t* k_new, const uint16_t* v_new, void* records,
                          uint16_t* resid, uint16_t* host_kv, int64_t n_cap, spc_stream stream) {
   spc_status st = check_dims(d);

@@ -198,6 +198,19 @@ spc_status spc_merged_attn_noalloc(const spc_dims* d, const void* records, const
                                    float* spec_logits, spc_stream stream);
 
 /*
+ * Offload(C) (SpeCache page, section 3 "Prefilling", Algorithm 1): after a
+ * layer's attention the full-precision K and V (device, bf16 [B][Hkv][N][D]
+ * each) are copied to the pinned host cache host_kv (HOST pointer, bf16
+ * [B][Hkv][n_cap][2][D], rows interleaved K then V; pinned and mapped,
+ * otherwise SPC_ERR_NOT_MAPPED; n_cap >= N), so that the device can release
+ * them before the next layer.  Rows n < N are written; the copy engines do
+ * the work (two strided copies per (b, hkv)), asynchronously on `stream`,
+ * typically a copy stream overlapped with the next layer's compute.
+ */
+spc_status spc_offload_kv(const spc_dims* d, const uint16_t* k, const uint16_t* v, uint16_t* host_kv,
+                          int64_t n_cap, spc_stream stream);
+
+/*
  * Decode-time append (SpeCache page, section 3 "Decoding", Algorithm 3: the
  * new token's K/V joins the cache; section 3: the full-precision cache is
  * offloaded to CPU memory).  d describes the cache BEFORE the call: N tokens
