@@ -259,6 +259,50 @@ class DecodeStep:
             if timed:
                 self.rec(self.topk_ev[l][1], main)
 
+    def enqueue_serial(self):
+        """The non-speculative decode step that SpeCache's speculation replaces
+        (the exact token's own attention decides the rows to fetch): per layer,
+        the low-bit attention of the real token (both query rows equal), its
+        ArgTopK, the gather of those rows on the critical path, then the merged
+        attention with them."""
+        spc, d, k = self.spc, self.d, self.k
+        main, L = self.main, self.L
+        for l in range(L):
+            spc.spc_decode_attn2(d, self.records[l], self.resid[l], self.q_serial[l], self.o[l], self.lse[l],
+                                 self.logits[l], self.ws, self.ws_bytes, stream=main)
+            spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=main)
+            spc.spc_host_gather(d, self.host[l], self.W["N"], self.idx[l], k, self.staging[l], stream=main)
+            spc.spc_merged_attn(d, self.records[l], self.resid[l], self.q_serial[l], self.idx[l], self.bitmap[l],
+                                self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws, self.ws_bytes,
+                                stream=main)
+
+    def time_serial(self, steps, warmup):
+        """Steps/s of the non-speculative step, captured as its own graph."""
+        torch = self.torch
+        self.q_serial = self.q[:, :, :1].expand(-1, -1, 2, -1, -1).contiguous()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.main):
+            g.capture_begin(capture_error_mode="relaxed")
+            self.enqueue_serial()
+            g.capture_end()
+        with torch.cuda.stream(self.main):
+            for _ in range(max(3, warmup)):
+                g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.main)
+        with torch.cuda.stream(self.main):
+            for _ in range(steps):
+                g.replay()
+        e1.record(self.main)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        del g
+        return {"value": 1000.0 / ms, "unit": "steps/s", "ms_per_step": ms,
+                "what": "per layer: low-bit attention of the real token, its top-k, the gather on the critical path, "
+                        "merged attention (no speculative token, no overlap)"}
+
     def capture(self):
         torch = self.torch
         self.main.wait_stream(torch.cuda.current_stream())
@@ -354,6 +398,56 @@ def append_probe(W, reps=20):
     del K, V, host
     out["note"] = "one layer, B*Hkv rows of 512 B to the window and to pinned host memory; a flush codes one group per (b, kv-head)"
     return out
+
+
+def prefill_probe(W, layers=4, reps=3):
+    """The prefill's per-layer tail (Algorithm 1): spc_quantize_kv of one
+    layer's K/V, and Offload(C) of those 16-bit rows to pinned host memory on
+    a copy stream; then `layers` layers pipelined (layer l+1's quantisation
+    while layer l's rows travel to the host)."""
+    import torch
+    import bit_kv_cache_spc_gb300 as spc
+    import synth.gpu
+    from bit_kv_cache_spc_gb300.steps import prefill_layer
+    B, Hq, Hkv, N, R, bits = (W[x] for x in ("B", "Hq", "Hkv", "N", "R", "bits"))
+    d = spc.Dims(B, Hq, Hkv, N, R, bits)
+    K = torch.empty((B, Hkv, N, 128), dtype=torch.int16, device="cuda")
+    V = torch.empty_like(K)
+    synth.gpu.kv_layer_into(0, 0, K, V)
+    rec = torch.empty(spc.spc_records_bytes(d), dtype=torch.uint8, device="cuda")
+    res = torch.empty(spc.spc_resid_bytes(d) // 2, dtype=torch.int16, device="cuda")
+    host = torch.empty((B, Hkv, N, 2, 128), dtype=torch.int16, pin_memory=True)
+    main, copy = torch.cuda.current_stream(), torch.cuda.Stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    q_us, o_us = [], []
+    for _ in range(reps + 1):
+        ev[0].record(main)
+        spc.spc_quantize_kv(d, K, V, rec, res)
+        ev[1].record(main)
+        ev[2].record(main)
+        spc.spc_offload_kv(d, K, V, host, N)
+        ev[3].record(main)
+        torch.cuda.synchronize()
+        q_us.append(ev[0].elapsed_time(ev[1]) * 1000.0)
+        o_us.append(ev[2].elapsed_time(ev[3]) * 1000.0)
+    qu, ou = statistics.median(q_us[1:]), statistics.median(o_us[1:])
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(main)
+    for _ in range(layers):
+        prefill_layer(d, K, V, rec, res, host, N, stream=main, copy_stream=copy)
+    main.wait_stream(copy)
+    t1.record(main)
+    torch.cuda.synchronize()
+    pipe_us = t0.elapsed_time(t1) * 1000.0 / layers
+    host_bytes = K.numel() * 2 * 2
+    q_bytes = host_bytes + spc.spc_records_bytes(d)
+    del K, V, host
+    return {"quantize_us": qu, "quantize_gbs": q_bytes / (qu * 1e-6) / 1e9,
+            "offload_us": ou, "offload_gbs": host_bytes / (ou * 1e-6) / 1e9,
+            "pipelined_us_per_layer": pipe_us, "layers": layers,
+            "note": "one layer of the workload: quantise (HBM) and Offload(C) of 1.07 GB to pinned host memory "
+                    "(copy engines, device-to-host); the pipeline overlaps the next layer's quantisation"}
 
 
 def attention_bytes_per_layer(W, nq, fused=False):
@@ -524,6 +618,8 @@ def main():
 
     gather = host_link_probe(step, reps=20)
     append = append_probe(W) if rank == 0 else None
+    serial = step.time_serial(max(5, args.steps // 4), args.warmup) if rank == 0 else None
+    prefill = prefill_probe(W) if rank == 0 else None
 
     line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -536,7 +632,9 @@ def main():
                                     else "fused into the next layer's attention")},
             "roofline": roof, "gather": gather,
             "per_layer_us": {"attention": attn_avg_ms * 1000.0, "topk": statistics.mean(per_layer_topk) * 1000.0},
-            "append": append, "clocks": clk.summary(), "e2e": e2e,
+            "append": append,
+            "nonspeculative_baseline": serial,
+            "prefill": prefill, "clocks": clk.summary(), "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps}
     if rank == 0 and not args.no_cpu_baseline:
         ref = OracleSample(W, args.cpu_pairs)
