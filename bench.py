@@ -33,7 +33,8 @@ WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=
                 B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328, layers=32)
 METRIC = "decode attn steps/s at 32K ctx, 1-bit, top-1% (HBM GB/s and % of peak in roofline)"
 # DRAM bytes (read + write) of one merged-attention launch of this workload, from the ncu capture
-# summarised in profiles/attn_kernel_llama3_8b_32k.md; None once the kernel changes after that capture.
+# summarised in profiles/attn_kernel_llama3_8b_32k.md (the fused pre-fetch placement); None once the kernel
+# changes after that capture.
 ATTN_TRAFFIC_BYTES = 175594496
 
 
@@ -607,7 +608,8 @@ def main():
     attn_avg_ms = statistics.mean(per_layer)
     achieved = bytes_layer / (attn_avg_ms / 1000.0) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": ATTN_TRAFFIC_BYTES,
+            "frac": achieved / peaks["hbm_gbs"],
+            "traffic": ATTN_TRAFFIC_BYTES if args.prefetch == "fused" else None,
             "traffic_source": "dram read+write of one launch, profiles/attn_kernel_llama3_8b_32k.md",
             "kernel": ("spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer" if args.prefetch == "side"
                        else "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, previous layer's "
