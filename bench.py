@@ -305,20 +305,31 @@ class DecodeStep:
                         "merged attention (no speculative token, no overlap)"}
 
     def capture(self):
+        """Two graphs of the same step: the one that is timed has nothing
+        between the kernels (so each launch may overlap its predecessor's
+        tail), the other records events around every attention and top-k for
+        the per-layer breakdown."""
         torch = self.torch
         self.main.wait_stream(torch.cuda.current_stream())
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(self.main):
-            g.capture_begin(capture_error_mode="relaxed")
-            self.enqueue(timed=True)
-            g.capture_end()
-        self.graph = g
+        graphs = []
+        for timed in (False, True):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.main):
+                g.capture_begin(capture_error_mode="relaxed")
+                self.enqueue(timed=timed)
+                g.capture_end()
+            graphs.append(g)
+        self.graph, self.graph_timed = graphs
         torch.cuda.synchronize()
 
     def replay(self):
         with self.torch.cuda.stream(self.main):
             self.graph.replay()
+
+    def replay_timed(self):
+        with self.torch.cuda.stream(self.main):
+            self.graph_timed.replay()
 
     def attn_ms(self):
         return [s.elapsed_time(e) for (s, e) in self.attn_ev]
@@ -570,7 +581,10 @@ def main():
             step.replay()
         end.record(step.main)
         barrier()
-    # the per-layer attention events inside the graph hold the last timed step
+    # per-layer breakdown: the graph with events between the kernels, replayed after the timed region
+    for _ in range(3):
+        step.replay_timed()
+    torch.cuda.synchronize()
     per_layer = step.attn_ms()
     per_layer_topk = step.topk_ms()
     total_ms = start.elapsed_time(end)

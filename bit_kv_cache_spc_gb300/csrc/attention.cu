@@ -783,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   __shared__ float s_ml[2 * kMaxRows];
   __shared__ __align__(16) float s_q[kMaxRows * kTilePitch];
   CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem);
+  grid_dependency_sync();  // nothing is read or written before the previous kernel is done
   {
     // scaled query rows of this (b, hkv): rho = i * G + gi for token i, head gi
     const int64_t bh = blockIdx.y;
@@ -888,8 +889,19 @@ static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t strea
   static unsigned long long configured = 0ull;  // one per <BITS, MERGED, FETCH> instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
   if (e != cudaSuccess) return e;
-  fn<<<dim3(a.chunks, (unsigned)BH), kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  // programmatic serialisation: the launch overlaps the previous kernel's tail
+  // (the kernel waits for it before touching any data)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.chunks, (unsigned)BH, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, a);
 }
 
 spc_status launch_attention(const spc_dims* d, const void* records, const uint16_t* resid,

@@ -115,6 +115,15 @@ __device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation waits here until the previous kernel in the stream has
+// completed and its memory is visible (immediately when there is none), then
+// lets the next kernel's CTAs be scheduled while this grid still runs.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));

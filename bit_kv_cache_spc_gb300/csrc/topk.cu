@@ -44,6 +44,7 @@ struct TopkShared {
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
+  grid_dependency_sync();  // nothing is read or written before the previous kernel is done
   extern __shared__ __align__(16) uint32_t keys[];     // [slice]
   __shared__ uint32_t wgt[kTopkMaxSlice / 32];          // per word: count, then exclusive prefix
   __shared__ uint32_t weq[kTopkMaxSlice / 32];
@@ -367,6 +368,7 @@ __device__ __forceinline__ void ordered_take(const uint32_t* keys, int n, uint32
 // two CTAs of 1024 threads per SM (32 registers), so a cluster per (b, hkv) row fits one wave
 __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
+  grid_dependency_sync();  // nothing is read or written before the previous kernel is done
   extern __shared__ __align__(16) uint32_t dyn[];  // keys[slice]; the leader then reuses it for the merge
   __shared__ uint32_t wgt[kTopkMaxSlice / 32];
   __shared__ uint32_t weq[kTopkMaxSlice / 32];
@@ -494,13 +496,17 @@ spc_status launch_topk(const spc_dims* d, const float* logits, const float* lse,
     cfg.blockDim = dim3(kTopkThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ncta;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic serialisation: the launch overlaps the previous kernel's
+    // tail (the kernel waits for it before touching any data)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, fn, a);
   }
   if (e != cudaSuccess) {
