@@ -47,8 +47,10 @@ def parse():
     p.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-pairs", type=int, default=16, help="(b, kv-head) pairs in the oracle sample")
-    p.add_argument("--prefetch", choices=["side", "fused"], default="fused",
-                   help="pre-fetch as a small side-stream kernel, or carried by the next layer's attention")
+    p.add_argument("--prefetch", choices=["side", "fused", "step"], default="fused",
+                   help="pre-fetch as a small side-stream kernel, or carried by the next layer's attention "
+                        "(then top-k as its own launch), or 'step': one spc_decode_step launch per layer "
+                        "(attention + carried pre-fetch + fused top-k)")
     p.add_argument("--gather-ctas", type=int, default=32, help="grid of the side-stream pre-fetch kernel")
     return p.parse_args()
 
@@ -181,6 +183,8 @@ class DecodeStep:
         self.staging = torch.zeros((layers, B, Hkv, k, 2, 128), dtype=torch.int16, device=dev)
         self.ws_bytes = spc.spc_attn_workspace_bytes(d, k)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
+        self.ws_step_bytes = spc.spc_step_workspace_bytes(d, k)
+        self.ws_step = torch.zeros(self.ws_step_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
         self.main = torch.cuda.Stream()
         self.side = torch.cuda.Stream(priority=-1)
         self.selected = [torch.cuda.Event() for _ in range(layers)]
@@ -200,13 +204,36 @@ class DecodeStep:
                 spc.spc_host_gather(d, self.host[l], N, self.idx[l], k, self.staging[l], stream=self.main)
         torch.cuda.synchronize()
         # attention, top-k, and the gather (its own launch, or riding on the next attention)
-        self.launches_per_step = layers * (3 if mode == "side" else 2)
+        self.launches_per_step = layers * {"side": 3, "fused": 2, "step": 1}[mode]
         self.graph = None
 
     def enqueue(self, timed=False):
         if self.mode == "fused":
             return self.enqueue_fused(timed)
+        if self.mode == "step":
+            return self.enqueue_step(timed)
         return self.enqueue_side(timed)
+
+    def enqueue_step(self, timed=False):
+        """One decode step on one stream, one launch per layer: spc_decode_step
+        runs the merged attention over C' U C_kappa, carries the pre-fetch of
+        layer l-1's selection and ends with the speculative top-k, whose
+        selection replaces idx[l] / bitmap[l] in place."""
+        spc, d, k = self.spc, self.d, self.k
+        main, L = self.main, self.L
+        for l in range(L):
+            j = (l - 1) % L
+            if timed:
+                self.rec(self.attn_ev[l][0], main)
+            spc.spc_decode_step(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
+                                self.staging[l], k, self.o[l], self.lse[l], self.logits[l], k, self.idx[l],
+                                self.bitmap[l], self.ws_step, self.ws_step_bytes, fetch_host_kv=self.host[j],
+                                fetch_n_cap=self.W["N"], fetch_idx=self.idx[j], fetch_k=k,
+                                fetch_staging=self.staging[j], stream=main)
+            if timed:
+                self.rec(self.attn_ev[l][1], main)
+                self.rec(self.topk_ev[l][0], main)
+                self.rec(self.topk_ev[l][1], main)
 
     def enqueue_side(self, timed=False):
         """One decode step.  Layer l: the merged attention over C' U C_kappa and
@@ -618,16 +645,18 @@ def main():
            "d2h_bytes_per_step": d2h}
 
     # ---- roofline of the dominant call (merged attention, one layer per launch) ----
-    bytes_layer = attention_bytes_per_layer(W, step.nq, fused=args.prefetch == "fused")
+    bytes_layer = attention_bytes_per_layer(W, step.nq, fused=args.prefetch in ("fused", "step"))
     attn_avg_ms = statistics.mean(per_layer)
     achieved = bytes_layer / (attn_avg_ms / 1000.0) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"],
             "traffic": ATTN_TRAFFIC_BYTES if args.prefetch == "fused" else None,
             "traffic_source": "dram read+write of one launch, profiles/attn_kernel_llama3_8b_32k.md",
-            "kernel": ("spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer" if args.prefetch == "side"
-                       else "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, previous layer's "
-                            "pre-fetch riding along), one layer"),
+            "kernel": {"side": "spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer",
+                       "fused": "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, previous layer's "
+                                "pre-fetch riding along), one layer",
+                       "step": "spc_decode_step (low-bit scan + 16-bit rows + combine + top-k, previous "
+                               "layer's pre-fetch riding along), one layer"}[args.prefetch],
             "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
             "step_hbm_gbs": bytes_layer * W["layers"] / (ms_per_step / 1000.0) / 1e9}
@@ -644,8 +673,10 @@ def main():
                        "bits": W["bits"], "k": W["k"], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (4.3 GB low-bit cache per step, 129 MB L2); no flush",
                        "graph": "one CUDA graph per step",
-                       "prefetch": (f"side stream, {args.gather_ctas} CTAs" if args.prefetch == "side"
-                                    else "fused into the next layer's attention")},
+                       "prefetch": {"side": f"side stream, {args.gather_ctas} CTAs",
+                                    "fused": "fused into the next layer's attention",
+                                    "step": "fused into the next layer's attention, which also ends with "
+                                            "the top-k (spc_decode_step)"}[args.prefetch]},
             "roofline": roof, "gather": gather,
             "per_layer_us": {"attention": attn_avg_ms * 1000.0, "topk": statistics.mean(per_layer_topk) * 1000.0},
             "append": append,

@@ -80,6 +80,10 @@ _sig = {
     "spc_host_gather": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, C.c_int32, _P]),
     "spc_append_kv": (C.c_int, [_D, _P, _P, _P, _P, _P, C.c_int64, _P]),
     "spc_offload_kv": (C.c_int, [_D, _P, _P, _P, C.c_int64, _P]),
+    "spc_step_workspace_bytes": (C.c_size_t, [_D, C.c_int32]),
+    "spc_decode_step": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, C.c_int32, _P, _P, _P,
+                                  C.c_size_t, _P, C.c_int64, _P, C.c_int32, _P, _P]),
+    "spc_read_device_status": (C.c_int, [_P, _D, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -126,6 +130,27 @@ def spc_resid_bytes(d) -> int:
 
 def spc_attn_workspace_bytes(d, k_max=0) -> int:
     return int(_lib.spc_attn_workspace_bytes(C.byref(d), int(k_max)))
+
+
+def spc_step_workspace_bytes(d, k_max=0) -> int:
+    return int(_lib.spc_step_workspace_bytes(C.byref(d), int(k_max)))
+
+
+def spc_decode_step(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, next_k, next_idx,
+                    next_bitmap, ws, ws_bytes=None, fetch_host_kv=None, fetch_n_cap=0, fetch_idx=None, fetch_k=0,
+                    fetch_staging=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("spc_decode_step",
+           _lib.spc_decode_step(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(idx), _ptr(bitmap),
+                                _ptr(staging), int(k), _ptr(o), _ptr(lse), _ptr(spec_logits), int(next_k),
+                                _ptr(next_idx), _ptr(next_bitmap), _ptr(ws), ws_bytes, _ptr(fetch_host_kv),
+                                int(fetch_n_cap), _ptr(fetch_idx), int(fetch_k), _ptr(fetch_staging),
+                                _stream(stream)))
+
+
+def spc_read_device_status(ws, d, stream=None) -> int:
+    """0, or SPC_ERR_TIMEOUT (6) if a bounded wait in spc_decode_step ran out (the word is cleared)."""
+    return int(_lib.spc_read_device_status(_ptr(ws), C.byref(d), _stream(stream)))
 
 
 def spc_quantize_kv(d, k, v, records, resid, stream=None):

@@ -30,6 +30,7 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "select.cuh"
 
 namespace spc {
 
@@ -79,6 +80,18 @@ struct AttnArgs {
   uint16_t* pf_staging;     // [B][Hkv][pf_k][2][D]
   int64_t pf_ncap;
   int32_t pf_k, pf_rows;
+  // Fused ArgTopK (spc_decode_step): per (b, hkv) the sel_k positions with the
+  // largest speculative probability go to sel_idx / sel_bitmap.  ready and
+  // tickets2 are per-(b, hkv) words (zero between calls); cand holds each
+  // chunk's candidates (key, position), cand_cap per chunk; fault is set when
+  // a wait ran out.
+  int32_t* sel_idx;       // [BH][sel_k]
+  uint32_t* sel_bitmap;   // [BH][q_groups_cap]
+  uint32_t* ready;
+  uint32_t* tickets2;
+  uint32_t* fault;
+  uint32_t* cand;         // [BH][chunks][cand_cap][2]
+  int32_t sel_k, sel_keff, cand_cap;
 };
 
 // Bits r and r+16 of w as an f16x2 pair, each 0 or the fp16 pattern v (1.0
@@ -689,7 +702,8 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
 }
 
 // ------------------------------------------------------------ merge + combine
-__device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last, float* s_ml) {
+// Returns whether this CTA was the last of its (b, hkv) and so combined the partials.
+__device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last, float* s_ml) {
   __syncthreads();
   const int c = threadIdx.x;  // channel
   const int64_t bh = blockIdx.y;
@@ -719,7 +733,7 @@ __device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs
   __syncthreads();
   if (c == 0) *s_last = (atomicAdd(&a.tickets[bh], 1u) == (unsigned)(nparts - 1));
   __syncthreads();
-  if (!*s_last) return;
+  if (!*s_last) return false;
   __threadfence();
   const float* base = a.part + (bh * nparts * kMaxRows) * kPartStride;
   // (max, sum) of query row c / 16 over partials c % 16, c % 16 + 16, ..., then
@@ -774,12 +788,144 @@ __device__ __forceinline__ void merge_store_combine(CtaMerge& sm, const AttnArgs
     if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M[rho] + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
   }
   if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
+  return true;
 }
 
-template <int BITS, bool MERGED, bool FETCH>
+// ------------------------------------------------------------ fused ArgTopK
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+
+constexpr uint64_t kWaitLimitNs = 20000000ull;  // 20 ms: a normal wait is a few microseconds
+
+// ArgTopK(A_{1,:}) at the end of the attention (SpeCache page, Algorithm 3):
+// the CTA that combined a (b, hkv) publishes its log-sum-exp; every CTA of the
+// (b, hkv) waits for it (bounded: on expiry it sets the fault word and goes
+// on), scores its own chunk's positions from the speculative logits it and its
+// siblings wrote, S(n) = sum_h 2^(log2e (l_h(n) - lse_h)), and keeps its
+// chunk's top-k' (k' = min(k, chunk length), ties to the lower position) as
+// candidates in the workspace.  The last CTA of the (b, hkv) to finish (a
+// second ticket) selects the final k from the candidates, which lie in
+// ascending position, and writes idx and the bitmap.  Every globally selected
+// position is among its chunk's candidates.
+template <int BITS>
+__device__ __forceinline__ void select_epilogue(const AttnArgs& a, uint8_t* dyn, SelShared<kThreads>& sh,
+                                                bool combined, int* s_flag, float* s_nlse) {
+  const int tid = threadIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
+  if (combined) {
+    if (tid == 0) {
+      __threadfence();  // the log-sum-exp this CTA wrote, then the flag
+      atomicExch(&a.ready[bh], 1u);
+    }
+  } else if (tid == 0) {
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_gpu(&a.ready[bh]) == 0u) {
+      if (global_ns() - t0 > kWaitLimitNs) {
+        atomicOr(a.fault, 1u);
+        break;
+      }
+      __nanosleep(200);
+    }
+  }
+  __syncthreads();
+  if (tid < G) s_nlse[tid] = -__ldcg(a.lse + ((int64_t)b * 2 + 1) * a.Hq + hk * G + tid) * 1.4426950408889634f;
+  __syncthreads();
+
+  // ---- scores of this chunk's positions, then its candidates ----
+  const int gpc32 = a.groups_per_chunk * kGroup;
+  const int p0 = blockIdx.x * gpc32;
+  const int len = max(0, min(a.nq, p0 + gpc32) - p0);  // multiple of 32
+  uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
+  const float* lrow = a.spec_logits + (bh * G) * (int64_t)a.Lcap + p0;
+  for (int i = 4 * tid; i < len; i += 4 * kThreads) {
+    float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int gi = 0; gi < G; ++gi) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(lrow + (int64_t)gi * a.Lcap + i));
+      const float nl = s_nlse[gi];
+      sc.x += fast_exp2(fmaf(v.x, 1.4426950408889634f, nl));
+      sc.y += fast_exp2(fmaf(v.y, 1.4426950408889634f, nl));
+      sc.z += fast_exp2(fmaf(v.z, 1.4426950408889634f, nl));
+      sc.w += fast_exp2(fmaf(v.w, 1.4426950408889634f, nl));
+    }
+    *reinterpret_cast<uint4*>(keys + i) =
+        make_uint4(__float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
+  }
+  __syncthreads();
+  const int kloc = min(a.sel_keff, len);
+  if (kloc > 0) {
+    uint32_t* wgt = keys + len;
+    uint32_t* weq = wgt + (len >> 5);
+    uint32_t* cand = a.cand + ((bh * a.chunks + blockIdx.x) * (int64_t)a.cand_cap) * 2;
+    uint32_t T, need;
+    cta_radix_select<kThreads>(keys, len, (uint32_t)kloc, sh, T, need);
+    ordered_take<kThreads>(keys, len, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
+      cand[2 * r] = keys[i];
+      cand[2 * r + 1] = (uint32_t)(p0 + i);
+    });
+  }
+
+  // ---- the last CTA of the (b, hkv) merges the chunks' candidates ----
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) *s_flag = (atomicAdd(&a.tickets2[bh], 1u) == (unsigned)(a.chunks - 1));
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  int M = 0;
+  for (int c = 0; c < a.chunks; ++c) M += min(a.sel_keff, max(0, min(a.nq, (c + 1) * gpc32) - c * gpc32));
+  const int nwq = a.nq >> 5;
+  uint32_t* mkey = reinterpret_cast<uint32_t*>(dyn);
+  uint32_t* mpos = mkey + M;
+  uint32_t* sbm = mpos + M;
+  uint32_t* wgt = sbm + nwq;
+  uint32_t* weq = wgt + ((M + 31) >> 5);
+  for (int c = 0, off = 0; c < a.chunks; ++c) {
+    const int cnt = min(a.sel_keff, max(0, min(a.nq, (c + 1) * gpc32) - c * gpc32));
+    const uint32_t* cand = a.cand + ((bh * a.chunks + c) * (int64_t)a.cand_cap) * 2;
+    for (int i = tid; i < cnt; i += kThreads) {
+      const uint2 kv = __ldcg(reinterpret_cast<const uint2*>(cand) + i);
+      mkey[off + i] = kv.x;
+      mpos[off + i] = kv.y;
+    }
+    off += cnt;
+  }
+  for (int w = tid; w < nwq; w += kThreads) sbm[w] = 0u;
+  __syncthreads();
+  int32_t* out = a.sel_idx + bh * a.sel_k;
+  if (a.sel_keff > 0) {
+    uint32_t T, need;
+    cta_radix_select<kThreads>(mkey, M, (uint32_t)a.sel_keff, sh, T, need);
+    ordered_take<kThreads>(mkey, M, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
+      const uint32_t p = mpos[i];
+      out[r] = (int32_t)p;
+      atomicOr(&sbm[p >> 5], 1u << (p & 31u));
+    });
+  }
+  for (int j = a.sel_keff + tid; j < a.sel_k; j += kThreads) out[j] = -1;
+  uint32_t* bm = a.sel_bitmap + bh * a.q_groups_cap;
+  for (int w = tid; w < a.q_groups_cap; w += kThreads) bm[w] = w < nwq ? sbm[w] : 0u;
+  if (tid == 0) {  // every CTA of this (b, hkv) is past its wait: ready for the next call
+    atomicExch(&a.ready[bh], 0u);
+    atomicExch(&a.tickets2[bh], 0u);
+  }
+}
+
+template <int BITS, bool MERGED, bool FETCH, bool TOPK>
 __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ int s_last;
+  static_assert(sizeof(SelShared<kThreads>) <= kMaxRows * kTilePitch * sizeof(float),
+                "the selection's shared state reuses the query tile");
   __shared__ float s_ml[2 * kMaxRows];
   __shared__ __align__(16) float s_q[kMaxRows * kTilePitch];
   CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem);
@@ -802,7 +948,11 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
     __syncthreads();
   }
   lowbit_cta<BITS, MERGED, FETCH>(a, dyn_smem, s_q, merge);
-  merge_store_combine(merge, a, &s_last, s_ml);
+  const bool combined = merge_store_combine(merge, a, &s_last, s_ml);
+  if constexpr (TOPK) {
+    __syncthreads();  // the query tile and the merge buffer are free from here on
+    select_epilogue<BITS>(a, dyn_smem, *reinterpret_cast<SelShared<kThreads>*>(s_q), combined, &s_last, s_ml);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -830,8 +980,8 @@ static int resident_ctas() {
   }
   int n = 0;
   const int smem = attn_smem_bytes(BITS);
-  cudaError_t e = spc_host::ensure_smem_limit(configured, attn_kernel<BITS, true, FETCH>, smem);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<BITS, true, FETCH>, kThreads, smem);
+  cudaError_t e = spc_host::ensure_smem_limit(configured, attn_kernel<BITS, true, FETCH, false>, smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<BITS, true, FETCH, false>, kThreads, smem);
   if (e != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = 2;
@@ -865,19 +1015,41 @@ static size_t part_floats(const spc_dims* d, const AttnPlan& p) {
   return (size_t)d->B * d->Hkv * p.chunks * kMaxRows * kPartStride;
 }
 
-// Workspace: the per-(b, hkv) tickets first (a fixed place, whatever k is),
-// then the partials from a 256-byte boundary.
-static size_t ticket_bytes(const spc_dims* d) {
-  return (((size_t)d->B * d->Hkv * sizeof(uint32_t) + 255) / 256) * 256;
+// Workspace: control words first (a fixed place, whatever k is): tickets
+// [BH], ready [BH], tickets2 [BH] and the fault word; then the partials from a
+// 256-byte boundary; then, for spc_decode_step, the chunks' candidates.
+static size_t control_bytes(const spc_dims* d) {
+  return ((((size_t)3 * d->B * d->Hkv + 1) * sizeof(uint32_t) + 255) / 256) * 256;
+}
+
+static size_t parts_bytes(const spc_dims* d) {
+  return std::max(part_floats(d, attn_plan(d, false)), part_floats(d, attn_plan(d, true))) * sizeof(float);
+}
+
+// candidates kept per chunk: min(k, N_q, the chunk's positions)
+static int cand_cap(const spc_dims* d, const AttnPlan& p, int32_t k) {
+  return std::max(0, std::min(std::min(k, num_quantized(d->N, d->R)), p.groups_per_chunk * kGroup));
+}
+
+static size_t cand_bytes(const spc_dims* d, int32_t k_max) {
+  size_t best = 0;
+  for (bool fetch : {false, true}) {
+    const AttnPlan p = attn_plan(d, fetch);
+    best = std::max(best, (size_t)d->B * d->Hkv * p.chunks * cand_cap(d, p, k_max) * 2 * sizeof(uint32_t));
+  }
+  return best;
 }
 
 size_t attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
   (void)k_max;  // the partials do not depend on the number of fetched rows
-  const size_t parts = std::max(part_floats(d, attn_plan(d, false)), part_floats(d, attn_plan(d, true)));
-  return ticket_bytes(d) + parts * sizeof(float);
+  return control_bytes(d) + parts_bytes(d);
 }
 
-template <int BITS, bool MERGED, bool FETCH>
+size_t step_workspace_bytes(const spc_dims* d, int32_t k_max) {
+  return control_bytes(d) + parts_bytes(d) + cand_bytes(d, k_max);
+}
+
+template <int BITS, bool MERGED, bool FETCH, bool TOPK>
 static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
   const int smem = attn_smem_bytes(BITS);
   static_assert((int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
@@ -885,8 +1057,8 @@ static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t strea
   static_assert(kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= 2576 + kZsBytes &&
                     kMaxRows * kTilePitch * 4 <= 2576 + kZsBytes,
                 "16-bit row batch and transfer tile fit in a warp's last stage and z/s table");
-  auto* fn = attn_kernel<BITS, MERGED, FETCH>;
-  static unsigned long long configured = 0ull;  // one per <BITS, MERGED, FETCH> instantiation
+  auto* fn = attn_kernel<BITS, MERGED, FETCH, TOPK>;
+  static unsigned long long configured = 0ull;  // one per instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
   if (e != cudaSuccess) return e;
   // programmatic serialisation: the launch overlaps the previous kernel's tail
@@ -904,12 +1076,34 @@ static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t strea
   return cudaLaunchKernelEx(&cfg, fn, a);
 }
 
+template <int BITS, bool MERGED, bool TOPK>
+static cudaError_t launch_attn_f(const AttnArgs& a, int64_t BH, cudaStream_t stream, bool fetch) {
+  return fetch ? launch_attn<BITS, MERGED, true, TOPK>(a, BH, stream)
+               : launch_attn<BITS, MERGED, false, TOPK>(a, BH, stream);
+}
+
+// The fused selection works in the attention's dynamic shared memory: a
+// chunk's keys and word counts, then the leader's merge of every chunk's
+// candidates and the bitmap.
+static bool select_fits(const spc_dims* d, const AttnPlan& p, int32_t k_sel) {
+  const int64_t words = attn_smem_bytes(d->bits) / 4;
+  const int64_t nq = num_quantized(d->N, d->R);
+  const int64_t len = (int64_t)p.groups_per_chunk * kGroup;
+  const int64_t M = (int64_t)p.chunks * cand_cap(d, p, k_sel);
+  return nq > 0 && len + 2 * (len / 32) <= words && 2 * M + nq / 32 + 2 * ((M + 31) / 32) <= words;
+}
+
 spc_status launch_attention(const spc_dims* d, const void* records, const uint16_t* resid,
                             const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
                             const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
-                            float* spec_logits, void* ws, cudaStream_t stream, const PrefetchJob* pf) {
+                            float* spec_logits, void* ws, cudaStream_t stream, const PrefetchJob* pf,
+                            const SelectJob* sel, bool* sel_done) {
   const bool fetch = pf != nullptr && pf->host_dev != nullptr && (int64_t)d->B * d->Hkv * pf->k > 0;
   const AttnPlan plan = attn_plan(d, fetch);
+  const int64_t BH = (int64_t)d->B * d->Hkv;
+  const bool merged = k > 0;
+  const bool topk = sel != nullptr && merged && lse != nullptr && spec_logits != nullptr && select_fits(d, plan, sel->k);
+  if (sel_done != nullptr) *sel_done = topk;
   AttnArgs a;
   a.records = static_cast<const uint8_t*>(records);
   a.resid = resid;
@@ -918,8 +1112,13 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.bitmap = bitmap;
   a.staging = staging;
   a.spec_logits = spec_logits;
-  a.tickets = static_cast<uint32_t*>(ws);
-  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ticket_bytes(d));
+  uint32_t* control = static_cast<uint32_t*>(ws);
+  a.tickets = control;
+  a.ready = control + BH;
+  a.tickets2 = control + 2 * BH;
+  a.fault = control + 3 * BH;
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + control_bytes(d));
+  a.cand = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + control_bytes(d) + parts_bytes(d));
   a.out = o;
   a.lse = lse;
   a.k = k;
@@ -940,19 +1139,26 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.pf_ncap = pf ? pf->n_cap : 0;
   a.pf_k = pf ? pf->k : 0;
   a.pf_rows = pf ? (int32_t)((int64_t)d->B * d->Hkv * pf->k) : 0;
-  const int64_t BH = (int64_t)d->B * d->Hkv;
-  const bool merged = k > 0;
+  a.sel_idx = topk ? sel->idx : nullptr;
+  a.sel_bitmap = topk ? sel->bitmap : nullptr;
+  a.sel_k = topk ? sel->k : 0;
+  a.sel_keff = topk ? std::min(sel->k, a.nq) : 0;
+  a.cand_cap = topk ? cand_cap(d, plan, sel->k) : 0;
   cudaError_t e;
   if (d->bits == 1) {
-    if (merged)
-      e = fetch ? launch_attn<1, true, true>(a, BH, stream) : launch_attn<1, true, false>(a, BH, stream);
+    if (topk)
+      e = launch_attn_f<1, true, true>(a, BH, stream, fetch);
+    else if (merged)
+      e = launch_attn_f<1, true, false>(a, BH, stream, fetch);
     else
-      e = fetch ? launch_attn<1, false, true>(a, BH, stream) : launch_attn<1, false, false>(a, BH, stream);
+      e = launch_attn_f<1, false, false>(a, BH, stream, fetch);
   } else {
-    if (merged)
-      e = fetch ? launch_attn<2, true, true>(a, BH, stream) : launch_attn<2, true, false>(a, BH, stream);
+    if (topk)
+      e = launch_attn_f<2, true, true>(a, BH, stream, fetch);
+    else if (merged)
+      e = launch_attn_f<2, true, false>(a, BH, stream, fetch);
     else
-      e = fetch ? launch_attn<2, false, true>(a, BH, stream) : launch_attn<2, false, false>(a, BH, stream);
+      e = launch_attn_f<2, false, false>(a, BH, stream, fetch);
   }
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);

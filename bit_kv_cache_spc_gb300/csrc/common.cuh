@@ -142,6 +142,13 @@ struct PrefetchJob {
   int32_t k;
   uint16_t* staging;
 };
+
+// ArgTopK fused into a merged attention launch (spc_decode_step).
+struct SelectJob {
+  int32_t* idx;      // [B][Hkv][k]
+  uint32_t* bitmap;  // [B][Hkv][q_groups_cap]
+  int32_t k;
+};
 }  // namespace spc
 
 // Host-side helpers shared by the entry points.

@@ -11,7 +11,8 @@ spc_status launch_quantize(const spc_dims*, const uint16_t*, const uint16_t*, vo
 size_t attn_workspace_bytes(const spc_dims*, int32_t);
 spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const uint16_t*, const int32_t*,
                             const uint32_t*, const uint16_t*, int32_t, uint16_t*, float*, float*, void*,
-                            cudaStream_t, const PrefetchJob*);
+                            cudaStream_t, const PrefetchJob*, const SelectJob*, bool*);
+size_t step_workspace_bytes(const spc_dims*, int32_t);
 spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t);
 spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
                               int32_t, cudaStream_t);
@@ -87,7 +88,8 @@ spc_status mapped_device_pointer(const void* host, const void** dev) {
 spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
                        const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
                        uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
-                       spc_stream stream, const spc::PrefetchJob* pf = nullptr) {
+                       spc_stream stream, const spc::PrefetchJob* pf = nullptr,
+                       const spc::SelectJob* sel = nullptr, bool* sel_done = nullptr) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
   const int32_t nq = spc::num_quantized(d->N, d->R);
@@ -101,10 +103,12 @@ spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* r
   if (k > 0) {
     if (idx == nullptr || bitmap == nullptr || staging == nullptr || !aligned16(staging)) return SPC_ERR_INVALID;
   }
-  if (ws_bytes < spc::attn_workspace_bytes(d, k)) return SPC_ERR_WORKSPACE;
+  const size_t need = sel != nullptr ? spc::step_workspace_bytes(d, std::max(k, sel->k))
+                                     : spc::attn_workspace_bytes(d, k);
+  if (ws_bytes < need) return SPC_ERR_WORKSPACE;
   return spc::launch_attention(d, records, resid, q, k > 0 ? idx : nullptr, k > 0 ? bitmap : nullptr,
                                k > 0 ? staging : nullptr, k, o, lse, spec_logits, ws,
-                               reinterpret_cast<cudaStream_t>(stream), pf);
+                               reinterpret_cast<cudaStream_t>(stream), pf, sel, sel_done);
 }
 
 }  // namespace
@@ -121,6 +125,7 @@ const char* spc_status_string(spc_status s) {
     case SPC_ERR_CUDA: return "CUDA error";
     case SPC_ERR_NOT_MAPPED: return "host pointer is not mapped pinned memory";
     case SPC_ERR_WORKSPACE: return "workspace too small";
+    case SPC_ERR_TIMEOUT: return "a kernel's bounded wait ran out (see spc_read_device_status)";
   }
   return "unknown status";
 }
@@ -246,6 +251,64 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
   spc::PrefetchJob job{static_cast<const uint16_t*>(dev), fetch_n_cap, fetch_idx, fetch_k, fetch_staging};
   return attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream,
                      &job);
+}
+
+size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max) {
+  if (check_dims(d) != SPC_OK || k_max < 0 || k_max > (1 << 24)) return 0;
+  return spc::step_workspace_bytes(d, k_max);
+}
+
+spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                           const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                           uint16_t* o, float* lse, float* spec_logits, int32_t next_k, int32_t* next_idx,
+                           uint32_t* next_bitmap, void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv,
+                           int64_t fetch_n_cap, const int32_t* fetch_idx, int32_t fetch_k,
+                           uint16_t* fetch_staging, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  const int32_t nq = spc::num_quantized(d->N, d->R);
+  if (next_k < 0 || next_k > (1 << 24)) return SPC_ERR_INVALID;
+  if (next_bitmap == nullptr || (next_k > 0 && next_idx == nullptr)) return SPC_ERR_INVALID;
+  if (nq > 0 && (spec_logits == nullptr || lse == nullptr)) return SPC_ERR_INVALID;
+  if (nq > 262144) return SPC_ERR_UNSUPPORTED;
+  spc::PrefetchJob job{nullptr, fetch_n_cap, fetch_idx, fetch_k, fetch_staging};
+  const spc::PrefetchJob* pf = nullptr;
+  if (fetch_k != 0) {
+    if (fetch_k < 0 || fetch_k > (1 << 24) || fetch_n_cap < 0) return SPC_ERR_INVALID;
+    if (fetch_host_kv == nullptr || fetch_idx == nullptr || fetch_staging == nullptr) return SPC_ERR_INVALID;
+    if (!aligned16(fetch_host_kv) || !aligned16(fetch_staging)) return SPC_ERR_INVALID;
+    const void* dev = nullptr;
+    st = mapped_device_pointer(fetch_host_kv, &dev);
+    if (st != SPC_OK) return st;
+    job.host_dev = static_cast<const uint16_t*>(dev);
+    pf = &job;
+  }
+  spc::SelectJob sel{next_idx, next_bitmap, next_k};
+  bool fused = false;
+  st = attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream, pf,
+                   &sel, &fused);
+  if (st != SPC_OK || fused) return st;
+  // the selection could not ride on this attention launch: its own launch, right after
+  if (d->q_groups_cap == 0 && next_k == 0) return SPC_OK;
+  return spc::launch_topk(d, spec_logits, lse, next_k, next_idx, next_bitmap, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spc_status spc_read_device_status(void* ws, const spc_dims* d, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  if (ws == nullptr) return SPC_ERR_INVALID;
+  uint32_t* fault = static_cast<uint32_t*>(ws) + 3 * (int64_t)d->B * d->Hkv;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, fault, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && v != 0u) e = cudaMemsetAsync(fault, 0, sizeof(v), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    spc_host::set_cuda_error(e);
+    return SPC_ERR_CUDA;
+  }
+  return v != 0u ? SPC_ERR_TIMEOUT : SPC_OK;
 }
 
 spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse, int32_t k,

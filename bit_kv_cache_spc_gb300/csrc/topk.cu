@@ -16,6 +16,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "select.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -234,137 +235,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
 // radix select above.
 constexpr int kMaxCand = 2048;
 
-struct __align__(16) SelShared {
-  uint32_t hist[4][256];  // four sub-histograms (warp & 3) to spread atomic contention
-  uint32_t wsum[2][kTopkWarps];
-  uint32_t sel[2];        // digit search result: prefix, remaining
-  uint32_t count;         // candidates kept by this CTA
-  float nlse[4];          // -lse * log2(e) of the speculative row of each head of the group
-};
-
-// The kth largest (1 <= kth <= n) of keys[0..n): T, and how many keys equal
-// to T belong to the top kth (the other kth - need are > T).
-__device__ __forceinline__ void cta_radix_select(const uint32_t* keys, int n, uint32_t kth, SelShared& sh,
-                                                 uint32_t& T, uint32_t& need) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0u, pmask = 0u, rem = kth;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int j = tid; j < 4 * 256; j += kTopkThreads) (&sh.hist[0][0])[j] = 0u;
-    __syncthreads();
-    uint32_t* h = sh.hist[warp & 3];
-    for (int i = tid; i < n; i += kTopkThreads) {
-      const uint32_t key = keys[i];
-      if (((key ^ prefix) & pmask) == 0u) atomicAdd(&h[(key >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 8l .. 8l+7; find the bin holding the rem-th largest
-      uint32_t cnt[8], own = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int bin = 8 * lane + e;
-        cnt[e] = sh.hist[0][bin] + sh.hist[1][bin] + sh.hist[2][bin] + sh.hist[3][bin];
-        own += cnt[e];
-      }
-      uint32_t above = own;  // inclusive suffix sum over lanes >= this one
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, above, off);
-        if (lane + off < 32) above += v;
-      }
-      above -= own;
-      if (above < rem && rem <= above + own) {
-        uint32_t acc = above;
-        for (int e = 7; e >= 0; --e) {
-          if (acc + cnt[e] >= rem) {
-            sh.sel[0] = prefix | ((uint32_t)(8 * lane + e) << shift);
-            sh.sel[1] = rem - acc;
-            break;
-          }
-          acc += cnt[e];
-        }
-      }
-    }
-    __syncthreads();
-    prefix = sh.sel[0];
-    rem = sh.sel[1];
-    pmask |= 255u << shift;
-  }
-  T = prefix;
-  need = rem;
-}
-
-// Ordered take over keys[0..n) (n <= 32 * kTopkThreads): element i is taken
-// if keys[i] > T, or keys[i] == T and fewer than `need` elements equal to T
-// precede it; emit(i, rank) is called for each taken element with its rank
-// among the taken ones (so ranks follow i).  wgt, weq: one word each per 32
-// elements.
-template <typename Emit>
-__device__ __forceinline__ void ordered_take(const uint32_t* keys, int n, uint32_t T, uint32_t need,
-                                             uint32_t* wgt, uint32_t* weq, SelShared& sh, Emit&& emit) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nw = (n + 31) >> 5;
-  for (int w = warp; w < nw; w += kTopkWarps) {
-    const int i = 32 * w + lane;
-    const uint32_t key = i < n ? keys[i] : 0u;
-    const uint32_t bgt = __ballot_sync(0xFFFFFFFFu, i < n && key > T);
-    const uint32_t beq = __ballot_sync(0xFFFFFFFFu, i < n && key == T);
-    if (lane == 0) {
-      wgt[w] = __popc(bgt);
-      weq[w] = __popc(beq);
-    }
-  }
-  __syncthreads();
-  {  // exclusive scan of the word counts, one word per thread
-    const uint32_t g = tid < nw ? wgt[tid] : 0u, e = tid < nw ? weq[tid] : 0u;
-    uint32_t ig = g, ie = e;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, ig, off), ve = __shfl_up_sync(0xFFFFFFFFu, ie, off);
-      if (lane >= off) {
-        ig += vg;
-        ie += ve;
-      }
-    }
-    if (lane == 31) {
-      sh.wsum[0][warp] = ig;
-      sh.wsum[1][warp] = ie;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t sg = sh.wsum[0][lane], se = sh.wsum[1][lane];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t vg = __shfl_up_sync(0xFFFFFFFFu, sg, off), ve = __shfl_up_sync(0xFFFFFFFFu, se, off);
-        if (lane >= off) {
-          sg += vg;
-          se += ve;
-        }
-      }
-      sh.wsum[0][lane] = sg;
-      sh.wsum[1][lane] = se;
-    }
-    __syncthreads();
-    const uint32_t wg0 = warp > 0 ? sh.wsum[0][warp - 1] : 0u, we0 = warp > 0 ? sh.wsum[1][warp - 1] : 0u;
-    if (tid < nw) {
-      wgt[tid] = wg0 + ig - g;
-      weq[tid] = we0 + ie - e;
-    }
-  }
-  __syncthreads();
-  const uint32_t below = (1u << lane) - 1u;
-  for (int w = warp; w < nw; w += kTopkWarps) {
-    const int i = 32 * w + lane;
-    const uint32_t key = i < n ? keys[i] : 0u;
-    const bool gt = i < n && key > T, eq = i < n && key == T;
-    const uint32_t bgt = __ballot_sync(0xFFFFFFFFu, gt), beq = __ballot_sync(0xFFFFFFFFu, eq);
-    const uint32_t eq_before = weq[w] + __popc(beq & below);
-    if (gt || (eq && eq_before < need)) emit(i, wgt[w] + __popc(bgt & below) + min(eq_before, need));
-  }
-  __syncthreads();
-}
-
 // two CTAs of 1024 threads per SM (32 registers), so a cluster per (b, hkv) row fits one wave
 __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
@@ -373,7 +243,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
   __shared__ uint32_t wgt[kTopkMaxSlice / 32];
   __shared__ uint32_t weq[kTopkMaxSlice / 32];
   __shared__ uint32_t ckey[kMaxCand], cpos[kMaxCand];  // this CTA's candidates, ascending position
-  __shared__ SelShared sh;
+  __shared__ SelShared<kTopkThreads> sh;
+  __shared__ uint32_t s_count;  // candidates kept by this CTA
+  __shared__ float s_nlse[4];   // -lse * log2(e) of the speculative row of each head of the group
 
   const int tid = threadIdx.x;
   const unsigned rank = cluster.block_rank();
@@ -386,7 +258,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
   uint32_t* keys = dyn;
 
   // ---- scores, four positions per thread and round, the round's loads issued up front ----
-  if (tid < 4) sh.nlse[tid] = tid < a.G ? -a.lse[((int64_t)b * 2 + 1) * a.Hq + hk * a.G + tid] * kLog2e : 0.f;
+  if (tid < 4) s_nlse[tid] = tid < a.G ? -a.lse[((int64_t)b * 2 + 1) * a.Hq + hk * a.G + tid] * kLog2e : 0.f;
   __syncthreads();
   const float* lrow = a.logits + (bh * a.G) * (int64_t)a.Lcap + n0;
   for (int i = 4 * tid; i < len; i += 4 * kTopkThreads) {
@@ -399,7 +271,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
 #pragma unroll
     for (int gi = 0; gi < 4; ++gi) {
       if (gi < a.G) {
-        const float nl = sh.nlse[gi];
+        const float nl = s_nlse[gi];
         sc.x += fast_exp2(fmaf(v[gi].x, kLog2e, nl));
         sc.y += fast_exp2(fmaf(v[gi].y, kLog2e, nl));
         sc.z += fast_exp2(fmaf(v[gi].z, kLog2e, nl));
@@ -421,19 +293,19 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
       cpos[r] = (uint32_t)(n0 + i);
     });
   }
-  if (tid == 0) sh.count = kloc;
+  if (tid == 0) s_count = kloc;
   cluster.sync();
 
   if (rank == 0) {
     // ---- merge: the candidates of every CTA, in rank (= position) order ----
     uint32_t M = 0;
-    for (unsigned r = 0; r < ncta; ++r) M += cluster.map_shared_rank(&sh, r)->count;
+    for (unsigned r = 0; r < ncta; ++r) M += *cluster.map_shared_rank(&s_count, r);
     uint32_t* mkey = dyn;
     uint32_t* mpos = dyn + M;
     uint32_t* sbm = dyn + 2 * M;  // bitmap of the selection, one word per 32 quantised positions
     const int nwq = a.nq >> 5;
     for (unsigned r = 0, off = 0; r < ncta; ++r) {
-      const uint32_t cnt = cluster.map_shared_rank(&sh, r)->count;
+      const uint32_t cnt = *cluster.map_shared_rank(&s_count, r);
       const uint32_t* rk = cluster.map_shared_rank(ckey, r);
       const uint32_t* rp = cluster.map_shared_rank(cpos, r);
       for (uint32_t i = tid; i < cnt; i += kTopkThreads) {

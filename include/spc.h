@@ -42,7 +42,8 @@ typedef enum spc_status {
   SPC_ERR_UNSUPPORTED = 2, /* valid shape this build does not handle */
   SPC_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
   SPC_ERR_NOT_MAPPED = 4,  /* host pointer is not device-mapped pinned memory */
-  SPC_ERR_WORKSPACE = 5    /* workspace smaller than the size query returns */
+  SPC_ERR_WORKSPACE = 5,   /* workspace smaller than the size query returns */
+  SPC_ERR_TIMEOUT = 6      /* a bounded wait inside a kernel ran out (spc_read_device_status) */
 } spc_status;
 
 /*
@@ -177,6 +178,46 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
                                  void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv, int64_t fetch_n_cap,
                                  const int32_t* fetch_idx, int32_t fetch_k, uint16_t* fetch_staging,
                                  spc_stream stream);
+
+/*
+ * One decoding step of a layer (SpeCache page, Algorithm 3) in one launch:
+ * spc_merged_attn (optionally carrying another layer's Pre-fetch, as
+ * spc_merged_attn_fetch) followed by ArgTopK(A_{1,:}), exactly as
+ * spc_topk_select(d, spec_logits, lse, next_k, next_idx, next_bitmap) would
+ * compute it.  The selection runs at the end of the attention: the CTA that
+ * combines a (b, hkv) publishes its log-sum-exp, every CTA of the (b, hkv)
+ * waits for it (bounded by a timer; on expiry it sets a fault word, reported
+ * by spc_read_device_status) and keeps its chunk's candidates, and the last
+ * CTA selects the final next_k.  So the speculative logits are re-read from
+ * L2 by the CTAs that wrote them instead of by a second kernel.
+ *   next_idx, next_bitmap: outputs as spc_topk_select's; they may be the idx
+ *            and bitmap this call reads (every CTA of a (b, hkv) has read them
+ *            before any is written).
+ *   ws, ws_bytes: at least spc_step_workspace_bytes(d, max(k, next_k)),
+ *            zero-filled once (the same contract as spc_attn_workspace_bytes).
+ *   lse and spec_logits are required (non-NULL).
+ *   fetch_*: as spc_merged_attn_fetch; fetch_k = 0 for none.
+ * Every CTA of the launch must be resident at once (the attention's grid is
+ * one wave of the GPU): if other work holds the SMs for long enough, the
+ * waits run out and the selection is wrong (SPC_ERR_TIMEOUT from
+ * spc_read_device_status; zero-fill the workspace again before reuse).  When
+ * the selection does not fit the attention's shared memory it is launched
+ * separately, right after, on the same stream, with the same results.
+ */
+size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max);
+spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                           const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                           uint16_t* o, float* lse, float* spec_logits, int32_t next_k, int32_t* next_idx,
+                           uint32_t* next_bitmap, void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv,
+                           int64_t fetch_n_cap, const int32_t* fetch_idx, int32_t fetch_k,
+                           uint16_t* fetch_staging, spc_stream stream);
+
+/*
+ * Reads and clears the fault word of an attention workspace (ws, laid out for
+ * d): SPC_ERR_TIMEOUT if a bounded wait of spc_decode_step ran out since the
+ * last read, else SPC_OK.  Synchronises `stream`.
+ */
+spc_status spc_read_device_status(void* ws, const spc_dims* d, spc_stream stream);
 
 /*
  * spc_merged_attn without a caller-provided workspace.  The SpeCache paper has
