@@ -22,7 +22,8 @@ _lib = None
 
 class orc_dims(C.Structure):
     _fields_ = [("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("D", C.c_int32),
-                ("bits", C.c_int32), ("N", C.c_int32), ("R", C.c_int32), ("scale", C.c_double)]
+                ("bits", C.c_int32), ("N", C.c_int32), ("R", C.c_int32), ("group", C.c_int32),
+                ("scale", C.c_double)]
 
 
 def build(force: bool = False) -> str:
@@ -71,10 +72,11 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
-def dims(B, Hq, Hkv, N, R, bits, D=128, scale=None) -> orc_dims:
+def dims(B, Hq, Hkv, N, R, bits, D=128, scale=None, group=32) -> orc_dims:
+    assert group in (32, 64)
     if scale is None:
         scale = float(np.float32(1.0 / np.sqrt(D)))
-    return orc_dims(B, Hq, Hkv, D, bits, N, R, scale)
+    return orc_dims(B, Hq, Hkv, D, bits, N, R, group, scale)
 
 
 def nq(d: orc_dims) -> int:
@@ -102,8 +104,8 @@ def quantize(d: orc_dims, K, V, mode: int = 0):
     n_q = nq(d)
     kcode = np.zeros((d.B, d.Hkv, n_q, d.D), np.uint8)
     vcode = np.zeros((d.B, d.Hkv, n_q, d.D), np.uint8)
-    kmm = np.zeros((d.B, d.Hkv, n_q // 32, d.D, 2), np.uint16)
-    vmm = np.zeros((d.B, d.Hkv, n_q, d.D // 32, 2), np.uint16)
+    kmm = np.zeros((d.B, d.Hkv, n_q // d.group, d.D, 2), np.uint16)
+    vmm = np.zeros((d.B, d.Hkv, n_q, d.D // d.group, 2), np.uint16)
     lib().orc_quantize(C.byref(d), mode, _p(K), _p(V), _p(kcode), _p(kmm), _p(vcode), _p(vmm))
     return {"kcode": kcode, "kmm": kmm, "vcode": vcode, "vmm": vmm}
 

@@ -10,8 +10,9 @@
  *     X' = Q(X)*s + z, z = min X, s = (max X - min X)/(2^B - 1)) and "Improved
  *     1-bit quantisation" (z = (3 min X + max X)/4, s = (max X - min X)/2);
  *   - grouping: keys per channel, values per token (KIVI, as the SemKV page
- *     section 2.1 describes it), group size 32 and a bf16 residual window
- *     (page 1 section 4, software setup);
+ *     section 2.1 describes it), group size g = 32 or 64 and a bf16 residual
+ *     window (page 1 section 4, software setup; the appendix's LongBench runs
+ *     use g = 64);
  *   - attention: O = Attn([T_t, T'_{t+1}], C' U C_kappa) of section 3
  *     ("Decoding") and Algorithm 3, where C' U C_kappa replaces the low-bit rows
  *     C'_kappa by the 16-bit rows C_kappa;
@@ -48,11 +49,12 @@ static uint16_t float_to_bf16_exact(float f) {
 }
 
 int32_t orc_nq(const orc_dims* d) {
-  /* Reading: the quantised part is a whole number of 32-token groups and the
-   * residual window holds at least R tokens (KIVI keeps the most recent tokens
-   * in 16 bits; page 1 section 4).  N_q = floor((N-R)/32)*32 when N >= R. */
+  /* Reading: the quantised part is a whole number of g-token groups and the
+   * rest (at least R tokens, fewer than R + g) stays in the bf16 residual
+   * window (KIVI keeps a full-precision window of recent tokens, page 1
+   * section 4).  N_q = floor((N-R)/g)*g when N >= R. */
   if (d->N <= d->R) return 0;
-  return ((d->N - d->R) / 32) * 32;
+  return ((d->N - d->R) / d->group) * d->group;
 }
 
 void orc_quant_params(int32_t bits, int32_t mode, float lo, float hi, float* z, float* s) {
@@ -104,18 +106,18 @@ double orc_dequant(int32_t bits, int32_t mode, uint16_t lo_b, uint16_t hi_b, int
 void orc_quantize(const orc_dims* d, int32_t mode, const uint16_t* K, const uint16_t* V,
                   uint8_t* kcode, uint16_t* kmm, uint8_t* vcode, uint16_t* vmm) {
   const int32_t B = d->B, H = d->Hkv, N = d->N, D = d->D, nq = orc_nq(d);
-  const int32_t ng = nq / 32, ncg = D / 32;
+  const int32_t g_sz = d->group, ng = nq / g_sz, ncg = D / g_sz;
 #pragma omp parallel for collapse(2) schedule(static)
   for (int32_t b = 0; b < B; ++b) {
     for (int32_t h = 0; h < H; ++h) {
       const uint16_t* Kbh = K + ((int64_t)(b * H + h) * N) * D;
       const uint16_t* Vbh = V + ((int64_t)(b * H + h) * N) * D;
-      /* Keys: one group per (32-token block g, channel c). */
+      /* Keys: one group per (g-token block g, channel c). */
       for (int32_t g = 0; g < ng; ++g) {
         for (int32_t c = 0; c < D; ++c) {
-          float lo = bf16_to_float(Kbh[(int64_t)(32 * g) * D + c]), hi = lo;
-          for (int32_t j = 1; j < 32; ++j) {
-            float x = bf16_to_float(Kbh[(int64_t)(32 * g + j) * D + c]);
+          float lo = bf16_to_float(Kbh[(int64_t)(g_sz * g) * D + c]), hi = lo;
+          for (int32_t j = 1; j < g_sz; ++j) {
+            float x = bf16_to_float(Kbh[(int64_t)(g_sz * g + j) * D + c]);
             if (x < lo) lo = x;
             if (x > hi) hi = x;
           }
@@ -124,19 +126,19 @@ void orc_quantize(const orc_dims* d, int32_t mode, const uint16_t* K, const uint
           int64_t m = (((int64_t)(b * H + h) * ng + g) * D + c) * 2;
           kmm[m] = float_to_bf16_exact(lo);
           kmm[m + 1] = float_to_bf16_exact(hi);
-          for (int32_t j = 0; j < 32; ++j) {
-            int32_t n = 32 * g + j;
+          for (int32_t j = 0; j < g_sz; ++j) {
+            int32_t n = g_sz * g + j;
             float x = bf16_to_float(Kbh[(int64_t)n * D + c]);
             kcode[((int64_t)(b * H + h) * nq + n) * D + c] = orc_quant_code(d->bits, x, z, s);
           }
         }
       }
-      /* Values: one group per (token n, 32-channel block cg). */
+      /* Values: one group per (token n, g-channel block cg). */
       for (int32_t n = 0; n < nq; ++n) {
         for (int32_t cg = 0; cg < ncg; ++cg) {
-          float lo = bf16_to_float(Vbh[(int64_t)n * D + 32 * cg]), hi = lo;
-          for (int32_t j = 1; j < 32; ++j) {
-            float x = bf16_to_float(Vbh[(int64_t)n * D + 32 * cg + j]);
+          float lo = bf16_to_float(Vbh[(int64_t)n * D + g_sz * cg]), hi = lo;
+          for (int32_t j = 1; j < g_sz; ++j) {
+            float x = bf16_to_float(Vbh[(int64_t)n * D + g_sz * cg + j]);
             if (x < lo) lo = x;
             if (x > hi) hi = x;
           }
@@ -145,8 +147,8 @@ void orc_quantize(const orc_dims* d, int32_t mode, const uint16_t* K, const uint
           int64_t m = (((int64_t)(b * H + h) * nq + n) * ncg + cg) * 2;
           vmm[m] = float_to_bf16_exact(lo);
           vmm[m + 1] = float_to_bf16_exact(hi);
-          for (int32_t j = 0; j < 32; ++j) {
-            int32_t c = 32 * cg + j;
+          for (int32_t j = 0; j < g_sz; ++j) {
+            int32_t c = g_sz * cg + j;
             float x = bf16_to_float(Vbh[(int64_t)n * D + c]);
             vcode[((int64_t)(b * H + h) * nq + n) * D + c] = orc_quant_code(d->bits, x, z, s);
           }
@@ -175,6 +177,10 @@ int64_t orc_record_bytes(int32_t bits) { return 1024 * (int64_t)(bits + 1); }
  *                             channel group m&3
  * The residual window is bf16 [resid_cap, 2, D] per (b,hkv): row j holds the
  * key then the value of token N_q + j.
+ * With g = 64 the same 32-token records are used: a record's K minmax words
+ * hold its 64-token group's (min, max), and a token's V minmax word for
+ * 32-channel group cg holds the (min, max) of its 64-channel group cg/2, so
+ * both records of a 64-token group carry the group's metadata.
  */
 void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
               const uint8_t* vcode, const uint16_t* vmm,
@@ -182,7 +188,8 @@ void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
               int32_t q_groups_cap, int32_t resid_cap,
               uint8_t* records, uint16_t* resid) {
   const int32_t B = d->B, H = d->Hkv, N = d->N, D = d->D, nq = orc_nq(d), bits = d->bits;
-  const int32_t ng = nq / 32, ncg = D / 32, r = N - nq;
+  const int32_t g_sz = d->group, ng = nq / 32, r = N - nq;
+  const int32_t kng = nq / g_sz, vncg = D / g_sz;  /* groups of the logical metadata */
   const int64_t RB = orc_record_bytes(bits);
   for (int32_t b = 0; b < B; ++b) {
     for (int32_t h = 0; h < H; ++h) {
@@ -217,11 +224,11 @@ void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
         for (int32_t t = 0; t < 4; ++t) {
           for (int32_t m = 0; m < 32; ++m) {
             int32_t kch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1);
-            int64_t km = ((bh * ng + g) * D + kch) * 2;
+            int64_t km = ((bh * kng + (32 * g) / g_sz) * D + kch) * 2;
             kmw[32 * t + m] = (uint32_t)kmm[km] | ((uint32_t)kmm[km + 1] << 16);
             int32_t vtok = 16 * (m >> 4) + 8 * ((m >> 3) & 1) + 2 * t + ((m >> 2) & 1);
             int32_t cg = m & 3;
-            int64_t vm = ((bh * nq + 32 * g + vtok) * ncg + cg) * 2;
+            int64_t vm = ((bh * nq + 32 * g + vtok) * vncg + (32 * cg) / g_sz) * 2;
             vmw[32 * t + m] = (uint32_t)vmm[vm] | ((uint32_t)vmm[vm + 1] << 16);
           }
         }
@@ -243,7 +250,7 @@ void orc_attention(const orc_dims* d, int32_t mode, const uint16_t* q,
                    const int32_t* idx, int32_t k,
                    double* o, double* lse, double* S) {
   const int32_t B = d->B, H = d->Hkv, Hq = d->Hq, N = d->N, D = d->D, nq = orc_nq(d);
-  const int32_t G = Hq / H, ng = nq / 32, ncg = D / 32;
+  const int32_t G = Hq / H, g_sz = d->group, ng = nq / g_sz, ncg = D / g_sz;
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
   for (int32_t b = 0; b < B; ++b) {
     for (int32_t hk = 0; hk < H; ++hk) {
@@ -261,8 +268,8 @@ void orc_attention(const orc_dims* d, int32_t mode, const uint16_t* q,
       for (int32_t n = 0; n < N; ++n) {
         for (int32_t c = 0; c < D; ++c) {
           if (n < nq && !sel[n]) {
-            int64_t km = ((bh * ng + n / 32) * D + c) * 2;
-            int64_t vm = ((bh * nq + n) * ncg + c / 32) * 2;
+            int64_t km = ((bh * ng + n / g_sz) * D + c) * 2;
+            int64_t vm = ((bh * nq + n) * ncg + c / g_sz) * 2;
             kr[(int64_t)n * D + c] = orc_dequant(d->bits, mode, kmm[km], kmm[km + 1],
                                                  kcode[(bh * nq + n) * D + c]);
             vr[(int64_t)n * D + c] = orc_dequant(d->bits, mode, vmm[vm], vmm[vm + 1],
@@ -377,23 +384,23 @@ void orc_gather(const orc_dims* d, const uint16_t* host, int64_t n_cap,
 void orc_append(const orc_dims* d, int32_t q_groups_cap, int32_t resid_cap,
                 const uint16_t* k_new, const uint16_t* v_new,
                 uint8_t* records, uint16_t* resid, uint16_t* host, int64_t n_cap) {
-  const int32_t B = d->B, H = d->Hkv, D = d->D, N = d->N, nq = orc_nq(d), r = N - nq;
+  const int32_t B = d->B, H = d->Hkv, D = d->D, N = d->N, nq = orc_nq(d), r = N - nq, g_sz = d->group;
   orc_dims next = *d;
   next.N = N + 1;
   const int flush = orc_nq(&next) > nq;
-  /* one 32-token group of one (b, hkv), quantised and packed on its own */
+  /* one g-token group of one (b, hkv), quantised and packed on its own */
   orc_dims one = *d;
   one.B = 1;
   one.Hkv = 1;
-  one.N = 32;
+  one.N = g_sz;
   one.R = 0;
   const int64_t RB = orc_record_bytes(d->bits);
-  uint16_t* K32 = malloc(sizeof(uint16_t) * 32 * (size_t)D);
-  uint16_t* V32 = malloc(sizeof(uint16_t) * 32 * (size_t)D);
-  uint8_t* kcode = malloc((size_t)32 * D);
-  uint8_t* vcode = malloc((size_t)32 * D);
+  uint16_t* Kg = malloc(sizeof(uint16_t) * (size_t)g_sz * D);
+  uint16_t* Vg = malloc(sizeof(uint16_t) * (size_t)g_sz * D);
+  uint8_t* kcode = malloc((size_t)g_sz * D);
+  uint8_t* vcode = malloc((size_t)g_sz * D);
   uint16_t* kmm = malloc(sizeof(uint16_t) * 2 * (size_t)D);
-  uint16_t* vmm = malloc(sizeof(uint16_t) * 2 * 32 * (size_t)(D / 32));
+  uint16_t* vmm = malloc(sizeof(uint16_t) * 2 * (size_t)g_sz * (size_t)(D / g_sz));
   for (int32_t b = 0; b < B; ++b)
     for (int32_t h = 0; h < H; ++h) {
       const int64_t bh = (int64_t)b * H + h;
@@ -405,16 +412,17 @@ void orc_append(const orc_dims* d, int32_t q_groups_cap, int32_t resid_cap,
         memcpy(host + (bh * n_cap + N) * 2 * D + D, v_new + bh * D, sizeof(uint16_t) * (size_t)D);
       }
       if (!flush) continue;
-      for (int32_t j = 0; j < 32; ++j) {
-        memcpy(K32 + (int64_t)j * D, win + (int64_t)j * 2 * D, sizeof(uint16_t) * (size_t)D);
-        memcpy(V32 + (int64_t)j * D, win + (int64_t)j * 2 * D + D, sizeof(uint16_t) * (size_t)D);
+      for (int32_t j = 0; j < g_sz; ++j) {
+        memcpy(Kg + (int64_t)j * D, win + (int64_t)j * 2 * D, sizeof(uint16_t) * (size_t)D);
+        memcpy(Vg + (int64_t)j * D, win + (int64_t)j * 2 * D + D, sizeof(uint16_t) * (size_t)D);
       }
-      orc_quantize(&one, 0, K32, V32, kcode, kmm, vcode, vmm);
-      orc_pack(&one, kcode, kmm, vcode, vmm, K32, V32, 1, 0, records + (bh * q_groups_cap + nq / 32) * RB, NULL);
-      memmove(win, win + 32 * 2 * D, sizeof(uint16_t) * 2 * (size_t)D * (size_t)(r + 1 - 32));
+      orc_quantize(&one, 0, Kg, Vg, kcode, kmm, vcode, vmm);
+      orc_pack(&one, kcode, kmm, vcode, vmm, Kg, Vg, g_sz / 32, 0,
+               records + (bh * q_groups_cap + nq / 32) * RB, NULL);
+      memmove(win, win + (int64_t)g_sz * 2 * D, sizeof(uint16_t) * 2 * (size_t)D * (size_t)(r + 1 - g_sz));
     }
-  free(K32);
-  free(V32);
+  free(Kg);
+  free(Vg);
   free(kcode);
   free(vcode);
   free(kmm);

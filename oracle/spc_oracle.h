@@ -33,7 +33,8 @@ typedef struct orc_dims {
   int32_t D;      /* head dim, multiple of 32 */
   int32_t bits;   /* 1 or 2 */
   int32_t N;      /* visible tokens */
-  int32_t R;      /* residual window: N_q = floor(max(N-R,0)/32)*32 */
+  int32_t R;      /* residual window: N_q = floor(max(N-R,0)/g)*g */
+  int32_t group;  /* g, tokens per key group and channels per value group: 32 or 64 */
   double scale;   /* softmax scale applied to q.k */
 } orc_dims;
 
@@ -107,7 +108,7 @@ void orc_gather(const orc_dims* d, const uint16_t* host, int64_t n_cap,
  * v_new (bf16 [B,Hkv,D]) go to window row r = N - N_q; when N+1 tokens
  * quantise one more group, the window's oldest 32 rows are quantised as group
  * N_q/32 (orc_quantize on those rows), packed into its record, and dropped
- * from the window.  host (bf16 [B,Hkv,n_cap,2,D], may be NULL) receives row N. */
+ * from the window (with g = 64: the oldest 64 rows, two records).  host (bf16 [B,Hkv,n_cap,2,D], may be NULL) receives row N. */
 void orc_append(const orc_dims* d, int32_t q_groups_cap, int32_t resid_cap,
                 const uint16_t* k_new, const uint16_t* v_new,
                 uint8_t* records, uint16_t* resid, uint16_t* host, int64_t n_cap);

@@ -42,11 +42,11 @@ def read_golden(name):
     return rows
 
 
-def quantize_key_group(bits, values, mode=0):
-    """Quantise one key group (32 tokens of channel 0) holding `values` (padded)."""
-    vals = list(values) + [values[0]] * (32 - len(values))
-    N = 32 + 0
-    d = oracle.dims(B=1, Hq=1, Hkv=1, N=N, R=0, bits=bits)
+def quantize_key_group(bits, values, mode=0, group=32):
+    """Quantise one key group (`group` tokens of channel 0) holding `values` (padded)."""
+    vals = list(values) + [values[0]] * (group - len(values))
+    N = group
+    d = oracle.dims(B=1, Hq=1, Hkv=1, N=N, R=0, bits=bits, group=group)
     K = np.zeros((1, 1, N, 128), np.uint16)
     K[0, 0, :, 0] = f2b(np.array(vals, np.float32))
     V = np.zeros_like(K)
@@ -115,12 +115,14 @@ def test_p1_centres_minimise_uniform_error():
     assert mse(*sorted(set(deq_kivi))) > base
 
 
-def test_p2_two_bit_nearest_grid_point():
-    """KIVI 2-bit: the code is the nearest point of {min + i*s}, s=(max-min)/3."""
+@pytest.mark.parametrize("group", [32, 64])
+def test_p2_two_bit_nearest_grid_point(group):
+    """KIVI 2-bit: the code is the nearest point of {min + i*s}, s=(max-min)/3,
+    min and max taken over the whole group (32 or 64 tokens)."""
     rng = np.random.default_rng(2)
-    for _ in range(200):
-        vals = random_bf16_group(rng, 32)
-        codes, deq, lo, hi = quantize_key_group(2, list(vals))
+    for _ in range(200 if group == 32 else 100):
+        vals = random_bf16_group(rng, group)
+        codes, deq, lo, hi = quantize_key_group(2, list(vals), group=group)
         lo_f, hi_f = Fraction(lo), Fraction(hi)
         for x, c in zip(vals, codes):
             if hi_f == lo_f:
@@ -171,10 +173,10 @@ def dequant_tensors(d, qz):
     nq = oracle.nq(d)
     kmm = b2f(qz["kmm"])
     vmm = b2f(qz["vmm"])
-    klo = np.repeat(kmm[..., 0], 32, axis=2)
-    khi = np.repeat(kmm[..., 1], 32, axis=2)
-    vlo = np.repeat(vmm[..., 0], 32, axis=3)
-    vhi = np.repeat(vmm[..., 1], 32, axis=3)
+    klo = np.repeat(kmm[..., 0], d.group, axis=2)
+    khi = np.repeat(kmm[..., 1], d.group, axis=2)
+    vlo = np.repeat(vmm[..., 0], d.group, axis=3)
+    vhi = np.repeat(vmm[..., 1], d.group, axis=3)
     if d.bits == 1:
         kz, ks = (3 * klo + khi) / 4, (khi - klo) / 2
         vz, vs = (3 * vlo + vhi) / 4, (vhi - vlo) / 2
@@ -201,10 +203,11 @@ def sdpa_reference(d, q, Keff, Veff):
     return o.permute(0, 2, 1, 3).numpy(), lse.permute(0, 2, 1).numpy(), p.numpy()
 
 
-@pytest.mark.parametrize("bits,B,Hq,Hkv,N,R", [(1, 1, 4, 1, 160, 64), (2, 2, 2, 2, 96, 32),
-                                               (1, 1, 8, 2, 200, 40)])
-def test_p6_attention_matches_library_on_tiny_inputs(bits, B, Hq, Hkv, N, R):
-    d = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N, R=R, bits=bits)
+@pytest.mark.parametrize("bits,B,Hq,Hkv,N,R,group", [(1, 1, 4, 1, 160, 64, 32), (2, 2, 2, 2, 96, 32, 32),
+                                                     (1, 1, 8, 2, 200, 40, 32), (1, 1, 4, 1, 230, 40, 64),
+                                                     (2, 1, 8, 2, 300, 64, 64)])
+def test_p6_attention_matches_library_on_tiny_inputs(bits, B, Hq, Hkv, N, R, group):
+    d = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N, R=R, bits=bits, group=group)
     K, V = synth.kv_layer(7, 0, B, Hkv, N)
     q = synth.queries(7, 0, B, Hq)
     qz = oracle.quantize(d, K, V)
@@ -361,8 +364,9 @@ def test_pack_places_every_bit_exactly_once():
         assert len(seen_k) == len(seen_v) == bits * 11 * 26
 
 
-@pytest.mark.parametrize("bits,R,N0,T", [(1, 8, 30, 45), (2, 8, 71, 40), (1, 0, 0, 70), (2, 128, 100, 70)])
-def test_append_one_token_at_a_time_equals_quantising_the_sequence(bits, R, N0, T):
+@pytest.mark.parametrize("bits,R,N0,T,group", [(1, 8, 30, 45, 32), (2, 8, 71, 40, 32), (1, 0, 0, 70, 32),
+                                               (2, 128, 100, 70, 32), (1, 16, 40, 90, 64), (2, 0, 10, 60, 64)])
+def test_append_one_token_at_a_time_equals_quantising_the_sequence(bits, R, N0, T, group):
     """Decode-time append (SpeCache section 3, Algorithm 3): after tokens
     N0 .. N0+T-1 join one by one, the packed cache must be the one that
     quantising all N0+T tokens at once gives (group boundaries and codes
@@ -372,9 +376,9 @@ def test_append_one_token_at_a_time_equals_quantising_the_sequence(bits, R, N0, 
     B, Hkv, D = 2, 2, 128
     N1 = N0 + T
     K, V = synth.kv_layer(11, bits, B, Hkv, N1, D)
-    cap = N1 // 32 + 1
-    rcap = R + 32
-    d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N0, R=R, bits=bits)
+    cap = N1 // 32 + 2
+    rcap = R + group
+    d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N0, R=R, bits=bits, group=group)
     qz = oracle.quantize(d, K[:, :, :N0], V[:, :, :N0])
     rec, res = oracle.pack(d, qz, K[:, :, :N0], V[:, :, :N0], q_groups_cap=cap, resid_cap=rcap)
     host = np.zeros((B, Hkv, N1 + 3, 2, D), np.uint16)
@@ -386,10 +390,40 @@ def test_append_one_token_at_a_time_equals_quantising_the_sequence(bits, R, N0, 
         d.N += 1
         flushes += oracle.nq(d) > before
     assert flushes >= 1
-    d1 = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N1, R=R, bits=bits)
+    d1 = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N1, R=R, bits=bits, group=group)
     nq1 = oracle.nq(d1)
     rec1, res1 = oracle.pack(d1, oracle.quantize(d1, K, V), K, V, q_groups_cap=cap, resid_cap=rcap)
     assert np.array_equal(rec[:, :, :nq1 // 32], rec1[:, :, :nq1 // 32])
     assert np.array_equal(res[:, :, :N1 - nq1], res1[:, :, :N1 - nq1])
     assert np.array_equal(host[:, :, :N1], np.stack([K, V], axis=3))
     assert not host[:, :, N1:].any()
+
+
+@pytest.mark.parametrize("bits", [1, 2])
+def test_g64_equals_g32_when_both_halves_of_every_group_span_the_same_range(bits):
+    """A 64-token key group whose two 32-token halves have the same per-channel
+    (min, max), and a 64-channel value group whose two halves share theirs,
+    quantise exactly as with g = 32 (a code depends only on the value and its
+    group's min and max): the packed records must coincide."""
+    B, Hkv, N, D = 1, 2, 256, 128
+    K, V = synth.kv_layer(13, bits, B, Hkv, N, D)
+    rng = np.random.default_rng(5)
+    for g in range(N // 64):  # second half of each 64-token block: a permutation of the first
+        perm = rng.permutation(32)
+        K[:, :, 64 * g + 32:64 * g + 64] = K[:, :, 64 * g + perm]
+    for c0 in (0, 64):  # channels c0+32..c0+63: a permutation of c0..c0+31, per token
+        perm = rng.permutation(32)
+        V[..., c0 + 32:c0 + 64] = V[..., c0 + perm]
+    recs = []
+    for group in (32, 64):
+        d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N, R=0, bits=bits, group=group)
+        rec, _ = oracle.pack(d, oracle.quantize(d, K, V), K, V)
+        recs.append(rec)
+    assert np.array_equal(recs[0], recs[1])
+    # and an ordinary input does differ (the pin is not vacuous)
+    K2, V2 = synth.kv_layer(13, bits, B, Hkv, N, D)
+    out = []
+    for group in (32, 64):
+        d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N, R=0, bits=bits, group=group)
+        out.append(oracle.pack(d, oracle.quantize(d, K2, V2), K2, V2)[0])
+    assert not np.array_equal(out[0], out[1])
