@@ -48,16 +48,16 @@ class spc_dims(C.Structure):
                 ("q_groups_cap", C.c_int32), ("resid_cap", C.c_int32), ("scale", C.c_float)]
 
 
-def Dims(B, Hq, Hkv, N, R, bits, q_groups_cap=None, resid_cap=None, scale=None, D=128) -> spc_dims:
+def Dims(B, Hq, Hkv, N, R, bits, q_groups_cap=None, resid_cap=None, scale=None, D=128, group=32) -> spc_dims:
     """Shape of one layer's cache (see spc_dims in include/spc.h)."""
-    nq = ((N - R) // 32) * 32 if N > R else 0
+    nq = ((N - R) // group) * group if N > R else 0
     if q_groups_cap is None:
         q_groups_cap = nq // 32
     if resid_cap is None:
         resid_cap = N - nq
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    return spc_dims(B, Hq, Hkv, D, bits, 32, N, R, q_groups_cap, resid_cap, scale)
+    return spc_dims(B, Hq, Hkv, D, bits, group, N, R, q_groups_cap, resid_cap, scale)
 
 
 _P = C.c_void_p

@@ -998,7 +998,7 @@ static int resident_ctas(int bits, bool fetch) {
 // One wave of resident CTAs over B*Hkv, at least four groups (one per warp)
 // each.  The 16-bit rows ride on the same CTAs, whatever their number.
 static AttnPlan attn_plan(const spc_dims* d, bool fetch) {
-  const int ng = num_quantized(d->N, d->R) / kGroup;
+  const int ng = num_quantized(d->N, d->R, d->group) / kGroup;
   const int64_t BH = (int64_t)d->B * d->Hkv;
   AttnPlan p{1, 1};
   if (ng > 0) {
@@ -1028,7 +1028,7 @@ static size_t parts_bytes(const spc_dims* d) {
 
 // candidates kept per chunk: min(k, N_q, the chunk's positions)
 static int cand_cap(const spc_dims* d, const AttnPlan& p, int32_t k) {
-  return std::max(0, std::min(std::min(k, num_quantized(d->N, d->R)), p.groups_per_chunk * kGroup));
+  return std::max(0, std::min(std::min(k, num_quantized(d->N, d->R, d->group)), p.groups_per_chunk * kGroup));
 }
 
 static size_t cand_bytes(const spc_dims* d, int32_t k_max) {
@@ -1087,7 +1087,7 @@ static cudaError_t launch_attn_f(const AttnArgs& a, int64_t BH, cudaStream_t str
 // candidates and the bitmap.
 static bool select_fits(const spc_dims* d, const AttnPlan& p, int32_t k_sel) {
   const int64_t words = attn_smem_bytes(d->bits) / 4;
-  const int64_t nq = num_quantized(d->N, d->R);
+  const int64_t nq = num_quantized(d->N, d->R, d->group);
   const int64_t len = (int64_t)p.groups_per_chunk * kGroup;
   const int64_t M = (int64_t)p.chunks * cand_cap(d, p, k_sel);
   return nq > 0 && len + 2 * (len / 32) <= words && 2 * M + nq / 32 + 2 * ((M + 31) / 32) <= words;
@@ -1125,7 +1125,7 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.Hq = d->Hq;
   a.Hkv = d->Hkv;
   a.G = d->Hq / d->Hkv;
-  a.nq = num_quantized(d->N, d->R);
+  a.nq = num_quantized(d->N, d->R, d->group);
   a.r = d->N - a.nq;
   a.q_groups_cap = d->q_groups_cap;
   a.resid_cap = d->resid_cap;

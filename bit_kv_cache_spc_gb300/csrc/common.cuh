@@ -11,11 +11,13 @@
 namespace spc {
 
 constexpr int kD = 128;       // head dimension handled by this build
-constexpr int kGroup = 32;    // tokens (keys) / channels (values) per quantisation group
+constexpr int kGroup = 32;    // tokens per record; tokens (keys) / channels (values) per group at g = 32
 constexpr int kMaxRows = 8;   // 2 queries x G query heads per KV head, G <= 4
 
-__host__ __device__ inline int32_t num_quantized(int32_t N, int32_t R) {
-  return N > R ? ((N - R) / kGroup) * kGroup : 0;
+// Quantised tokens: whole groups of `group` (32 or 64) tokens, leaving at
+// least R (and fewer than R + group) tokens in the bf16 residual window.
+__host__ __device__ inline int32_t num_quantized(int32_t N, int32_t R, int32_t group) {
+  return N > R ? ((N - R) / group) * group : 0;
 }
 
 __host__ __device__ inline int64_t record_bytes(int32_t bits) { return 1024 * (int64_t)(bits + 1); }

@@ -57,7 +57,7 @@ struct QuantArgs {
   const uint16_t* v;
   uint8_t* records;
   int32_t Hkv, N, nq, q_groups_cap;
-  int64_t total_groups;  // B * Hkv * (nq / 32)
+  int64_t total_groups;  // B * Hkv * (nq / group): the kernel's units of work
 };
 
 struct QuantSmem {
@@ -80,8 +80,9 @@ __device__ __forceinline__ int vmeta_word(int n, int cg) {
 // Codes one 32-token group from the tiles ks, vs ([token][channel] bf16 in
 // shared memory) into its record at dst.  Every thread of the 128-thread CTA
 // takes part; the tiles may be reused once this returns.
-template <int BITS>
-__device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, const uint16_t* vs, uint8_t* dst_rec) {
+template <int BITS, int GROUP>
+__device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, const uint16_t* vs,
+                                           const uint16_t* ks_other, uint8_t* dst_rec) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int rb = 1024 * (BITS + 1);
   constexpr int KMETA = 128 * BITS, VCODES = KMETA + 128, VMETA = VCODES + 128 * BITS;  // in words
@@ -100,6 +101,14 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
       const float x = bf16_to_f32(ks[n * kD + c]);
       lo = fminf(lo, x);
       hi = fmaxf(hi, x);
+    }
+    if (GROUP == 64) {  // the group's other 32 tokens
+#pragma unroll 8
+      for (int n = 0; n < kGroup; ++n) {
+        const float x = bf16_to_f32(ks_other[n * kD + c]);
+        lo = fminf(lo, x);
+        hi = fmaxf(hi, x);
+      }
     }
     float z, s;
     quant_params(BITS, lo, hi, z, s);
@@ -156,9 +165,10 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
       lo = fminf(lo, x[e]);
       hi = fmaxf(hi, x[e]);
     }
-    // the 32-channel group cg = kk >> 1 spans the four lanes that differ in bits 0..1
+    // the 32-channel group cg = kk >> 1 spans the four lanes that differ in bits
+    // 0..1, the 64-channel group kk >> 2 the eight that differ in bits 0..2
 #pragma unroll
-    for (int off = 1; off <= 2; off <<= 1) {
+    for (int off = 1; off <= (GROUP == 64 ? 4 : 2); off <<= 1) {
       lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, off));
       hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, off));
     }
@@ -194,13 +204,39 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
   __syncthreads();  // the record buffer is reused by the next group
 }
 
-template <int BITS>
+template <int BITS, int GROUP>
 __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
   extern __shared__ __align__(16) uint8_t qsmem[];
   QuantSmem& sm = *reinterpret_cast<QuantSmem*>(qsmem);
   const int tid = threadIdx.x;
   const int ng = a.nq / kGroup;
   constexpr int rb = 1024 * (BITS + 1);
+  if constexpr (GROUP == 64) {
+    // a 64-token group per iteration: both tile buffers, two records with the
+    // group's shared parameters
+    const int ng64 = a.nq / 64;
+    for (int64_t gi = blockIdx.x; gi < a.total_groups; gi += gridDim.x) {
+      const int64_t bh = gi / ng64;
+      const int g = (int)(gi % ng64);
+      for (int half = 0; half < 2; ++half) {
+        const int64_t row0 = bh * a.N + (int64_t)(2 * g + half) * kGroup;
+        const uint8_t* ksrc = reinterpret_cast<const uint8_t*>(a.k + row0 * kD);
+        const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(a.v + row0 * kD);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          cp_async16(reinterpret_cast<uint8_t*>(sm.ks[half]) + 16 * (tid + 128 * r), ksrc + 16 * (tid + 128 * r));
+          cp_async16(reinterpret_cast<uint8_t*>(sm.vs[half]) + 16 * (tid + 128 * r), vsrc + 16 * (tid + 128 * r));
+        }
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
+      uint8_t* rec = a.records + (bh * a.q_groups_cap + 2 * g) * (int64_t)rb;
+      code_group<BITS, 64>(sm, sm.ks[0], sm.vs[0], sm.ks[1], rec);
+      code_group<BITS, 64>(sm, sm.ks[1], sm.vs[1], sm.ks[0], rec + rb);  // ends with a barrier: tiles free
+    }
+    return;
+  }
 
   auto load = [&](int64_t gi, int buf) {
     if (gi < a.total_groups) {
@@ -227,7 +263,7 @@ __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
     const int64_t bh = gi / ng;
     const int g = (int)(gi % ng);
     // the tile buffer is refilled two iterations on
-    code_group<BITS>(sm, sm.ks[buf], sm.vs[buf], a.records + (bh * a.q_groups_cap + g) * (int64_t)rb);
+    code_group<BITS, 32>(sm, sm.ks[buf], sm.vs[buf], nullptr, a.records + (bh * a.q_groups_cap + g) * (int64_t)rb);
   }
   cp_async_wait<0>();
 }
@@ -250,20 +286,20 @@ __global__ void resid_copy_kernel(const uint16_t* k, const uint16_t* v, uint16_t
   }
 }
 
-template <int BITS>
+template <int BITS, int GROUP>
 static cudaError_t launch_quantize_bits(const QuantArgs& a, cudaStream_t stream) {
   const int smem = (int)sizeof(QuantSmem);
   static unsigned long long configured = 0ull;
-  cudaError_t e = spc_host::ensure_smem_limit(configured, quantize_kernel<BITS>, smem);
+  cudaError_t e = spc_host::ensure_smem_limit(configured, quantize_kernel<BITS, GROUP>, smem);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(a.total_groups, (int64_t)spc_host::sm_count() * 8);
-  quantize_kernel<BITS><<<(unsigned)grid, 128, smem, stream>>>(a);
+  quantize_kernel<BITS, GROUP><<<(unsigned)grid, 128, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
 spc_status launch_quantize(const spc_dims* d, const uint16_t* k, const uint16_t* v, void* records,
                            uint16_t* resid, cudaStream_t stream) {
-  const int32_t nq = num_quantized(d->N, d->R);
+  const int32_t nq = num_quantized(d->N, d->R, d->group);
   const int32_t r = d->N - nq;
   const int64_t BH = (int64_t)d->B * d->Hkv;
   cudaError_t e = cudaSuccess;
@@ -276,8 +312,11 @@ spc_status launch_quantize(const spc_dims* d, const uint16_t* k, const uint16_t*
     a.N = d->N;
     a.nq = nq;
     a.q_groups_cap = d->q_groups_cap;
-    a.total_groups = BH * (nq / kGroup);
-    e = d->bits == 1 ? launch_quantize_bits<1>(a, stream) : launch_quantize_bits<2>(a, stream);
+    a.total_groups = BH * (nq / d->group);
+    if (d->group == 64)
+      e = d->bits == 1 ? launch_quantize_bits<1, 64>(a, stream) : launch_quantize_bits<2, 64>(a, stream);
+    else
+      e = d->bits == 1 ? launch_quantize_bits<1, 32>(a, stream) : launch_quantize_bits<2, 32>(a, stream);
   }
   if (e == cudaSuccess && r > 0) {
     const int64_t total_vec = BH * r * 32;
@@ -298,8 +337,8 @@ spc_status launch_quantize(const spc_dims* d, const uint16_t* k, const uint16_t*
 // Algorithm 3) and its 16-bit row goes to the host cache (section 3's offload
 // of the full-precision cache to CPU memory).  One CTA per (b, hkv): the row
 // goes to window row r = N - N_q (and host row N); when N+1 tokens quantise
-// one more group, the window's oldest 32 rows are coded into record N_q/32
-// by the same code_group as the prefill, and the window shifts down by 32.
+// one more group, the window's oldest g rows are coded into records N_q/32 ..
+// by the same code_group as the prefill, and the window shifts down by g.
 struct AppendArgs {
   const uint16_t* k_new;  // [B][Hkv][D]
   const uint16_t* v_new;
@@ -310,7 +349,7 @@ struct AppendArgs {
   int32_t N, nq, r, resid_cap, q_groups_cap, flush;
 };
 
-template <int BITS>
+template <int BITS, int GROUP>
 __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
   extern __shared__ __align__(16) uint8_t qsmem[];
   QuantSmem& sm = *reinterpret_cast<QuantSmem*>(qsmem);
@@ -325,26 +364,28 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
   }
   if (!a.flush) return;
   __syncthreads();  // the new row may belong to the group being flushed
-  for (int i = tid; i < kGroup * 32; i += 128) {  // window rows 0..31 -> [token][channel] tiles
-    const int n = i >> 5, q = i & 31;
+  for (int i = tid; i < GROUP * 32; i += 128) {  // window rows 0..g-1 -> [token][channel] tiles of 32 rows
+    const int n = i >> 5, q = i & 31, tile = n >> 5, row = n & 31;
     const uint4 v = win[n * 32 + q];
-    if (q < 16) reinterpret_cast<uint4*>(sm.ks[0] + n * kD)[q] = v;
-    else reinterpret_cast<uint4*>(sm.vs[0] + n * kD)[q - 16] = v;
+    if (q < 16) reinterpret_cast<uint4*>(sm.ks[tile] + row * kD)[q] = v;
+    else reinterpret_cast<uint4*>(sm.vs[tile] + row * kD)[q - 16] = v;
   }
   __syncthreads();
   constexpr int rb = 1024 * (BITS + 1);
-  code_group<BITS>(sm, sm.ks[0], sm.vs[0], a.records + (bh * a.q_groups_cap + a.nq / kGroup) * (int64_t)rb);
-  // rows 32 .. r move to 0 .. r-32, 32 rows at a time: a chunk's sources lie
+  uint8_t* rec = a.records + (bh * a.q_groups_cap + a.nq / kGroup) * (int64_t)rb;
+  code_group<BITS, GROUP>(sm, sm.ks[0], sm.vs[0], sm.ks[1], rec);
+  if (GROUP == 64) code_group<BITS, GROUP>(sm, sm.ks[1], sm.vs[1], sm.ks[0], rec + rb);
+  // rows g .. r move to 0 .. r-g, 32 rows at a time: a chunk's sources lie
   // past every destination written before it, and it is read in full before
   // it is written
-  const int keep = a.r + 1 - kGroup;
+  const int keep = a.r + 1 - GROUP;
   for (int c0 = 0; c0 < keep; c0 += kGroup) {
     const int rows = min(kGroup, keep - c0);
     uint4 v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = tid + 128 * u, n = i >> 5;
-      if (n < rows) v[u] = win[(int64_t)(kGroup + c0 + n) * 32 + (i & 31)];
+      if (n < rows) v[u] = win[(int64_t)(GROUP + c0 + n) * 32 + (i & 31)];
     }
     __syncthreads();
 #pragma unroll
@@ -354,6 +395,15 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
     }
     __syncthreads();
   }
+}
+
+template <int BITS, int GROUP>
+static cudaError_t launch_append_k(const AppendArgs& a, int64_t BH, cudaStream_t stream) {
+  const int smem = (int)sizeof(QuantSmem);
+  static unsigned long long configured = 0ull;
+  cudaError_t e = spc_host::ensure_smem_limit(configured, append_kernel<BITS, GROUP>, smem);
+  if (e == cudaSuccess) append_kernel<BITS, GROUP><<<(unsigned)BH, 128, smem, stream>>>(a);
+  return e;
 }
 
 spc_status launch_append(const spc_dims* d, const uint16_t* k_new, const uint16_t* v_new, void* records,
@@ -366,24 +416,18 @@ spc_status launch_append(const spc_dims* d, const uint16_t* k_new, const uint16_
   a.host = host_dev;
   a.n_cap = n_cap;
   a.N = d->N;
-  a.nq = num_quantized(d->N, d->R);
+  a.nq = num_quantized(d->N, d->R, d->group);
   a.r = d->N - a.nq;
   a.resid_cap = d->resid_cap;
   a.q_groups_cap = d->q_groups_cap;
-  a.flush = num_quantized(d->N + 1, d->R) > a.nq ? 1 : 0;
+  a.flush = num_quantized(d->N + 1, d->R, d->group) > a.nq ? 1 : 0;
   const int64_t BH = (int64_t)d->B * d->Hkv;
   if (BH == 0) return SPC_OK;
-  const int smem = (int)sizeof(QuantSmem);
   cudaError_t e;
-  if (d->bits == 1) {
-    static unsigned long long configured = 0ull;
-    e = spc_host::ensure_smem_limit(configured, append_kernel<1>, smem);
-    if (e == cudaSuccess) append_kernel<1><<<(unsigned)BH, 128, smem, stream>>>(a);
-  } else {
-    static unsigned long long configured = 0ull;
-    e = spc_host::ensure_smem_limit(configured, append_kernel<2>, smem);
-    if (e == cudaSuccess) append_kernel<2><<<(unsigned)BH, 128, smem, stream>>>(a);
-  }
+  if (d->bits == 1)
+    e = d->group == 64 ? launch_append_k<1, 64>(a, BH, stream) : launch_append_k<1, 32>(a, BH, stream);
+  else
+    e = d->group == 64 ? launch_append_k<2, 64>(a, BH, stream) : launch_append_k<2, 32>(a, BH, stream);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);

@@ -64,9 +64,9 @@ spc_status check_dims(const spc_dims* d) {
   if (d->bits != 1 && d->bits != 2) return SPC_ERR_INVALID;
   if (!(std::isfinite(d->scale) && d->scale > 0.f)) return SPC_ERR_INVALID;
   const int G = d->Hq / d->Hkv;
-  if (d->D != spc::kD || d->group != spc::kGroup) return SPC_ERR_UNSUPPORTED;
+  if (d->D != spc::kD || (d->group != 32 && d->group != 64)) return SPC_ERR_UNSUPPORTED;
   if (G != 1 && G != 2 && G != 4) return SPC_ERR_UNSUPPORTED;
-  const int32_t nq = spc::num_quantized(d->N, d->R);
+  const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
   if (nq / spc::kGroup > d->q_groups_cap) return SPC_ERR_INVALID;
   if (d->N - nq > d->resid_cap) return SPC_ERR_INVALID;
   return SPC_OK;
@@ -92,7 +92,7 @@ spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* r
                        const spc::SelectJob* sel = nullptr, bool* sel_done = nullptr) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
-  const int32_t nq = spc::num_quantized(d->N, d->R);
+  const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
   if (q == nullptr || o == nullptr || ws == nullptr) return SPC_ERR_INVALID;
   if (nq > 0 && records == nullptr) return SPC_ERR_INVALID;
   if (d->N - nq > 0 && resid == nullptr) return SPC_ERR_INVALID;
@@ -134,7 +134,7 @@ int32_t spc_last_cuda_error(void) { return spc_host::g_last_cuda_error; }
 
 int32_t spc_num_quantized(const spc_dims* d) {
   if (check_dims(d) == SPC_ERR_INVALID) return -1;
-  return spc::num_quantized(d->N, d->R);
+  return spc::num_quantized(d->N, d->R, d->group);
 }
 
 size_t spc_records_bytes(const spc_dims* d) {
@@ -151,7 +151,7 @@ spc_status spc_quantize_kv(const spc_dims* d, const uint16_t* k, const uint16_t*
                            uint16_t* resid, spc_stream stream) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
-  const int32_t nq = spc::num_quantized(d->N, d->R);
+  const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
   if (d->N > 0 && (k == nullptr || v == nullptr)) return SPC_ERR_INVALID;
   if (nq > 0 && records == nullptr) return SPC_ERR_INVALID;
   if (d->N - nq > 0 && resid == nullptr) return SPC_ERR_INVALID;
@@ -196,8 +196,8 @@ spc_status spc_append_kv(const spc_dims* d, const uint16_t* k_new, const uint16_
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
   if (d->N >= (1 << 30)) return SPC_ERR_INVALID;
-  const int32_t nq = spc::num_quantized(d->N, d->R);
-  const int32_t nq1 = spc::num_quantized(d->N + 1, d->R);
+  const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
+  const int32_t nq1 = spc::num_quantized(d->N + 1, d->R, d->group);
   if (k_new == nullptr || v_new == nullptr || resid == nullptr) return SPC_ERR_INVALID;
   if (d->N - nq + 1 > d->resid_cap) return SPC_ERR_INVALID;  // room for the new row
   if (nq1 > nq && (records == nullptr || nq1 / spc::kGroup > d->q_groups_cap)) return SPC_ERR_INVALID;
@@ -266,7 +266,7 @@ spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_
                            uint16_t* fetch_staging, spc_stream stream) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
-  const int32_t nq = spc::num_quantized(d->N, d->R);
+  const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
   if (next_k < 0 || next_k > (1 << 24)) return SPC_ERR_INVALID;
   if (next_bitmap == nullptr || (next_k > 0 && next_idx == nullptr)) return SPC_ERR_INVALID;
   if (nq > 0 && (spec_logits == nullptr || lse == nullptr)) return SPC_ERR_INVALID;
@@ -315,7 +315,7 @@ spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const fl
                            int32_t* idx, uint32_t* bitmap, spc_stream stream) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
-  const int32_t nq = spc::num_quantized(d->N, d->R);
+  const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
   if (k < 0 || k > (1 << 24)) return SPC_ERR_INVALID;
   if (bitmap == nullptr || (k > 0 && idx == nullptr)) return SPC_ERR_INVALID;
   if (nq > 0 && (spec_logits == nullptr || lse == nullptr)) return SPC_ERR_INVALID;

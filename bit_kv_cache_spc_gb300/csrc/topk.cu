@@ -343,7 +343,7 @@ spc_status launch_topk(const spc_dims* d, const float* logits, const float* lse,
   a.Hq = d->Hq;
   a.Hkv = d->Hkv;
   a.G = d->Hq / d->Hkv;
-  a.nq = num_quantized(d->N, d->R);
+  a.nq = num_quantized(d->N, d->R, d->group);
   a.k = k;
   a.keff = std::min(k, a.nq);
   a.Lcap = d->q_groups_cap * kGroup;

@@ -47,18 +47,18 @@ typedef enum spc_status {
 } spc_status;
 
 /*
- * Shape of one layer's cache.  D must be 128 and group 32 (the page's group
- * size g = 32, section 4).  G = Hq / Hkv query heads share a KV head; this
- * build handles G in {1, 2, 4}.
- * The quantised prefix has N_q = floor(max(N - R, 0) / 32) * 32 tokens and
- * the residual window the last r = N - N_q tokens (KIVI keeps the most recent
+ * Shape of one layer's cache.  D must be 128 and group g 32 or 64 (the page's
+ * group sizes, section 4 and the appendix's LongBench runs).  G = Hq / Hkv
+ * query heads share a KV head; this build handles G in {1, 2, 4}.
+ * The quantised prefix has N_q = floor(max(N - R, 0) / g) * g tokens and the
+ * residual window the last r = N - N_q tokens (KIVI keeps the most recent
  * tokens in 16 bits; page 1 section 4).  Capacities bound the buffers:
  * N_q / 32 <= q_groups_cap and r <= resid_cap.
  */
 typedef struct spc_dims {
   int32_t B, Hq, Hkv, D;
   int32_t bits;         /* 1 or 2 */
-  int32_t group;        /* 32 */
+  int32_t group;        /* g: 32 or 64 */
   int32_t N;            /* visible tokens of this layer */
   int32_t R;            /* residual window target */
   int32_t q_groups_cap; /* 32-token groups the record array can hold per (b,hkv) */
@@ -91,8 +91,12 @@ int32_t spc_num_quantized(const spc_dims* d);
  *                             channel 16*((b&15)>>1) + 8*(b&1) + a
  *   V minmax word 32t+m     : token 16*(m>>4) + 8*((m>>3)&1) + 2t + ((m>>2)&1),
  *                             channel group m&3
- * Keys are grouped per channel over the 32 tokens of a record, values per
- * token over 32 consecutive channels (KIVI's axes).  min/max are the group's
+ * Keys are grouped per channel over g tokens, values per token over g
+ * consecutive channels (KIVI's axes); with g = 64 a record's K minmax words
+ * hold its 64-token group's extremes and a token's V minmax word for
+ * 32-channel group cg those of its 64-channel group cg/2, so the two records
+ * of a group repeat its metadata (the codes are the g = 64 codes; the layout
+ * is shared with g = 32, which lets every kernel read either).  min/max are the group's
  * exact bf16 extremes (-0.0 stored as +0.0); the zero point and scale are
  * derived from them (page 1 section 3): 1-bit z = (3min+max)/4, s = (max-min)/2;
  * 2-bit z = min, s = (max-min)/3.  This is 64 (1-bit) or 96 (2-bit) bytes per

@@ -62,7 +62,7 @@ def odims(cfg, B=None, Hkv=None, Hq=None):
     Hkv = cfg["Hkv"] if Hkv is None else Hkv
     Hq = cfg["Hq"] if Hq is None else Hq
     return oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=cfg["N"], R=cfg["R"], bits=cfg["bits"],
-                       scale=float(np.float32(1.0 / math.sqrt(128))))
+                       scale=float(np.float32(1.0 / math.sqrt(128))), group=cfg.get("group", 32))
 
 
 def interleave_host(K: np.ndarray, V: np.ndarray) -> np.ndarray:
@@ -79,7 +79,8 @@ class GpuLayer:
         self.cfg = cfg
         B, Hq, Hkv, N, R, bits = (cfg[x] for x in ("B", "Hq", "Hkv", "N", "R", "bits"))
         self.G = Hq // Hkv
-        self.d = spc.Dims(B, Hq, Hkv, N, R, bits, scale=float(np.float32(1.0 / math.sqrt(128))))
+        self.d = spc.Dims(B, Hq, Hkv, N, R, bits, scale=float(np.float32(1.0 / math.sqrt(128))),
+                          group=cfg.get("group", 32))
         self.nq = spc.spc_num_quantized(self.d)
         dev = torch.device("cuda")
         if K is None:

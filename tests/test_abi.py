@@ -90,3 +90,15 @@ def test_append_validation(spc):
     with pytest.raises(spc.SpcError) as e:  # host cache too short for row N
         spc.spc_append_kv(ok_caps, 16, 16, 16, 16, host_kv=16, n_cap=1023, stream=0)
     assert e.value.status == 1
+
+
+def test_group_size_validation(spc):
+    """g = 32 and 64 are accepted (N_q is a whole number of groups); other sizes are refused."""
+    assert spc.spc_num_quantized(spc.Dims(1, 32, 8, 1000, 40, 1, group=64)) == 960
+    assert spc.spc_num_quantized(spc.Dims(1, 32, 8, 1000, 40, 1)) == 960
+    assert spc.spc_num_quantized(spc.Dims(1, 32, 8, 1100, 40, 1, group=64)) == 1024
+    d48 = spc.Dims(1, 32, 8, 1000, 40, 1)
+    d48.group = 48
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_quantize_kv(d48, 16, 16, 16, 16, stream=0)
+    assert e.value.status == 2

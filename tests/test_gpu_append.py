@@ -23,6 +23,8 @@ CASES = [
     dict(B=2, Hkv=3, Hq=6, R=16, bits=2, N0=75, T=40),
     dict(B=1, Hkv=2, Hq=8, R=0, bits=1, N0=20, T=50),     # R = 0: the new row completes the flushed group
     dict(B=1, Hkv=2, Hq=8, R=128, bits=2, N0=100, T=70),  # starts with no quantised token
+    dict(B=2, Hkv=2, Hq=8, R=16, bits=1, N0=40, T=90, group=64),  # g = 64: 64-row flushes
+    dict(B=1, Hkv=3, Hq=6, R=0, bits=2, N0=10, T=60, group=64),
 ]
 
 
@@ -30,16 +32,17 @@ def dev16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
 
 
-@pytest.mark.parametrize("c", CASES, ids=lambda c: f"b{c['bits']}_R{c['R']}_N{c['N0']}+{c['T']}")
+@pytest.mark.parametrize("c", CASES, ids=lambda c: f"b{c['bits']}_R{c['R']}_N{c['N0']}+{c['T']}_g{c.get('group', 32)}")
 def test_append_sequence_matches_oracle(c):
     import bit_kv_cache_spc_gb300 as spc
     B, Hkv, Hq, R, bits, N0, T = (c[x] for x in ("B", "Hkv", "Hq", "R", "bits", "N0", "T"))
+    group = c.get("group", 32)
     N1 = N0 + T
     D = 128
     K, V = synth.kv_layer(5, bits, B, Hkv, N1)
-    cap, rcap, n_cap = N1 // 32 + 1, R + 32, N1 + 2
+    cap, rcap, n_cap = N1 // 32 + 2, R + group, N1 + 2
     scale = float(np.float32(1.0 / math.sqrt(D)))
-    d = spc.Dims(B, Hq, Hkv, N0, R, bits, q_groups_cap=cap, resid_cap=rcap, scale=scale)
+    d = spc.Dims(B, Hq, Hkv, N0, R, bits, q_groups_cap=cap, resid_cap=rcap, scale=scale, group=group)
     rec = torch.zeros(spc.spc_records_bytes(d), dtype=torch.uint8, device="cuda")
     res = torch.zeros(spc.spc_resid_bytes(d) // 2, dtype=torch.int16, device="cuda")
     spc.spc_quantize_kv(d, dev16(K[:, :, :N0]), dev16(V[:, :, :N0]), rec, res)
@@ -48,7 +51,7 @@ def test_append_sequence_matches_oracle(c):
     Kn = dev16(K.transpose(2, 0, 1, 3))  # [N1, B, Hkv, D]: token n's rows contiguous
     Vn = dev16(V.transpose(2, 0, 1, 3))
 
-    od = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N0, R=R, bits=bits, scale=scale)
+    od = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N0, R=R, bits=bits, scale=scale, group=group)
     qz = oracle.quantize(od, K[:, :, :N0], V[:, :, :N0])
     orec, ores = oracle.pack(od, qz, K[:, :, :N0], V[:, :, :N0], q_groups_cap=cap, resid_cap=rcap)
     ohost = np.zeros((B, Hkv, n_cap, 2, D), np.uint16)
@@ -80,7 +83,7 @@ def test_append_sequence_matches_oracle(c):
     lg = torch.zeros((B, Hkv, G, cap * 32), dtype=torch.float32, device="cuda")
     ws = torch.zeros(spc.spc_attn_workspace_bytes(d, 0), dtype=torch.uint8, device="cuda")
     spc.spc_decode_attn2(d, rec, res, dev16(q), o, lse, lg, ws)
-    od1 = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N1, R=R, bits=bits, scale=scale)
+    od1 = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N1, R=R, bits=bits, scale=scale, group=group)
     oo, lo, _ = oracle.attention(od1, q, oracle.quantize(od1, K, V), K, V)
     torch.cuda.synchronize()
     assert out_err(b2f(o.cpu().numpy()), oo) <= OUT_TOL
