@@ -4,9 +4,10 @@
 Workload: one decode step of LLaMA-3-8B's attention over all 32 layers
 (batch 8, 32 query / 8 KV heads, head dim 128, 32K context, 1-bit cache,
 top-1% = 328 fetched rows per KV head).  Per layer: the merged two-query
-attention over C' U C_kappa, which in the same launch pre-fetches the
-previous layer's newly selected bf16 rows from pinned host memory, then the
-speculative top-k.  A step is captured once as a CUDA graph and replayed.
+attention over C' U C_kappa, which in the same launch pre-fetches the bf16
+rows that layer l-2's top-k selected from pinned host memory, and the
+speculative top-k, which runs on a low-priority second stream beside the next
+layer's attention.  A step is captured once as a CUDA graph and replayed.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -47,7 +48,7 @@ def parse():
     p.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-pairs", type=int, default=16, help="(b, kv-head) pairs in the oracle sample")
-    p.add_argument("--prefetch", choices=["side", "fused", "step"], default="fused",
+    p.add_argument("--prefetch", choices=["side", "fused", "step", "overlap"], default="overlap",
                    help="pre-fetch as a small side-stream kernel, or carried by the next layer's attention "
                         "(then top-k as its own launch), or 'step': one spc_decode_step launch per layer "
                         "(attention + carried pre-fetch + fused top-k)")
@@ -185,8 +186,10 @@ class DecodeStep:
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
         self.ws_step_bytes = spc.spc_step_workspace_bytes(d, k)
         self.ws_step = torch.zeros(self.ws_step_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
-        self.main = torch.cuda.Stream()
+        self.main = torch.cuda.Stream(priority=-1 if mode == "overlap" else 0)
         self.side = torch.cuda.Stream(priority=-1)
+        self.side_lo = torch.cuda.Stream(priority=0)
+        self.attended = [torch.cuda.Event() for _ in range(layers)]
         self.selected = [torch.cuda.Event() for _ in range(layers)]
         self.gathered = [torch.cuda.Event() for _ in range(layers)]
         self.mode = mode
@@ -204,7 +207,7 @@ class DecodeStep:
                 spc.spc_host_gather(d, self.host[l], N, self.idx[l], k, self.staging[l], stream=self.main)
         torch.cuda.synchronize()
         # attention, top-k, and the gather (its own launch, or riding on the next attention)
-        self.launches_per_step = layers * {"side": 3, "fused": 2, "step": 1}[mode]
+        self.launches_per_step = layers * {"side": 3, "fused": 2, "step": 1, "overlap": 2}[mode]
         self.graph = None
 
     def enqueue(self, timed=False):
@@ -212,7 +215,41 @@ class DecodeStep:
             return self.enqueue_fused(timed)
         if self.mode == "step":
             return self.enqueue_step(timed)
+        if self.mode == "overlap":
+            return self.enqueue_overlap(timed)
         return self.enqueue_side(timed)
+
+    def enqueue_overlap(self, timed=False):
+        """One decode step on two streams.  Layer l's merged attention (main
+        stream, high priority) carries the pre-fetch of layer l-2's selection,
+        so it does not wait for layer l-1's top-k; that top-k runs on a
+        low-priority stream after layer l-1's attention and fills the SMs the
+        attention leaves idle in its tail.  Layer l's attention waits only for
+        layer l-2's top-k, long done."""
+        spc, d, k = self.spc, self.d, self.k
+        main, side, L = self.main, self.side_lo, self.L
+        for l in range(L):
+            j = (l - 2) % L
+            if l >= 2:  # layers L-2, L-1 were selected by the previous replay, which has completed
+                main.wait_event(self.selected[j])
+            if timed:
+                self.rec(self.attn_ev[l][0], main)
+            spc.spc_merged_attn_fetch(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
+                                      self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws,
+                                      self.host[j], self.W["N"], self.idx[j], k, self.staging[j],
+                                      ws_bytes=self.ws_bytes, stream=main)
+            if timed:
+                self.rec(self.attn_ev[l][1], main)
+            self.attended[l].record(main)
+            side.wait_event(self.attended[l])
+            if timed:
+                self.rec(self.topk_ev[l][0], side)
+            spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=side)
+            if timed:
+                self.rec(self.topk_ev[l][1], side)
+            self.selected[l].record(side)
+        for l in range(L):  # join the side stream before the step ends
+            main.wait_event(self.selected[l])
 
     def enqueue_step(self, timed=False):
         """One decode step on one stream, one launch per layer: spc_decode_step
@@ -645,16 +682,18 @@ def main():
            "d2h_bytes_per_step": d2h}
 
     # ---- roofline of the dominant call (merged attention, one layer per launch) ----
-    bytes_layer = attention_bytes_per_layer(W, step.nq, fused=args.prefetch in ("fused", "step"))
+    bytes_layer = attention_bytes_per_layer(W, step.nq, fused=args.prefetch in ("fused", "step", "overlap"))
     attn_avg_ms = statistics.mean(per_layer)
     achieved = bytes_layer / (attn_avg_ms / 1000.0) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"],
-            "traffic": ATTN_TRAFFIC_BYTES if args.prefetch == "fused" else None,
+            "traffic": ATTN_TRAFFIC_BYTES if args.prefetch in ("fused", "overlap") else None,
             "traffic_source": "dram read+write of one launch, profiles/attn_kernel_llama3_8b_32k.md",
             "kernel": {"side": "spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer",
                        "fused": "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, previous layer's "
                                 "pre-fetch riding along), one layer",
+                       "overlap": "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, the pre-fetch of "
+                                  "the layer two before riding along), one layer",
                        "step": "spc_decode_step (low-bit scan + 16-bit rows + combine + top-k, previous "
                                "layer's pre-fetch riding along), one layer"}[args.prefetch],
             "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,
@@ -676,7 +715,9 @@ def main():
                        "prefetch": {"side": f"side stream, {args.gather_ctas} CTAs",
                                     "fused": "fused into the next layer's attention",
                                     "step": "fused into the next layer's attention, which also ends with "
-                                            "the top-k (spc_decode_step)"}[args.prefetch]},
+                                            "the top-k (spc_decode_step)",
+                                    "overlap": "fused into the attention two layers on; top-k on a "
+                                               "low-priority stream beside the next attention"}[args.prefetch]},
             "roofline": roof, "gather": gather,
             "per_layer_us": {"attention": attn_avg_ms * 1000.0, "topk": statistics.mean(per_layer_topk) * 1000.0},
             "append": append,
