@@ -27,6 +27,7 @@
 // p*z term is accumulated on CUDA cores.  Softmax runs in base 2 with the
 // scale folded into q.  z and s of a group are computed once per warp into
 // shared memory and read back by the lanes that need them.
+#include <cooperative_groups.h>
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -48,6 +49,7 @@ struct QueryInRegisters {
   static constexpr bool value = BITS == 1;
 };
 constexpr int kSlots = kWarps;  // CTA merge slots: one per warp
+constexpr int kMaxCluster = 16;  // CTAs of one (b, hkv) that the clustered combine accepts
 constexpr float kNeg = -1e30f;  // finite "minus infinity": keeps max/rescale arithmetic NaN-free
 constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pad, o[128]
 constexpr int kZsPitch = 17;     // float4s per t block of a z/s table (16 + 1 pad)
@@ -151,6 +153,8 @@ struct CtaMerge {
   float l[kSlots][kMaxRows];
   float o[kSlots][kMaxRows][kMergePitch];
 };
+// the clustered combine's partial (kMaxRows x kPartStride floats) follows the merge buffer
+constexpr int kClusterPartOffset = (int)((sizeof(CtaMerge) + 15) / 16 * 16);
 
 // ------------------------------------------------------------ 16-bit rows
 // Reduce-scatter of 16 per-lane partial sums: returns the warp-wide sum of
@@ -736,45 +740,79 @@ __device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs
   if (!*s_last) return false;
   __threadfence();
   const float* base = a.part + (bh * nparts * kMaxRows) * kPartStride;
-  // (max, sum) of query row c / 16 over partials c % 16, c % 16 + 16, ..., then
-  // over the 16 lanes of the row
-  {
-    const int rho = c >> 4, sub = c & 15;
-    float m = kNeg, l = 0.f;
-    for (int p = sub; p < nparts; p += 16) {
-      const float* pr = base + ((int64_t)p * kMaxRows + rho) * kPartStride;
-      const float mp = __ldcg(pr), lp = __ldcg(pr + 1);
-      const float mn = fmaxf(m, mp);
-      l = l * fast_exp2(m - mn) + lp * fast_exp2(mp - mn);
-      m = mn;
-    }
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) {
-      const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, off), lo = __shfl_xor_sync(0xFFFFFFFFu, l, off);
-      const float mn = fmaxf(m, mo);
-      l = l * fast_exp2(m - mn) + lo * fast_exp2(mo - mn);
-      m = mn;
-    }
-    if (sub == 0) {
-      s_ml[rho] = m;
-      s_ml[kMaxRows + rho] = l;
-    }
-  }
-  __syncthreads();
+  // The (max, sum) words of every partial into shared memory (the merge
+  // buffer, free now) in one round trip, 2 * kPCap (p, row) pairs at a time.
+  // Then, per query row c: the max and the sum over the partials in partial
+  // order (the same arithmetic as the clustered combine, so both give
+  // identical results); then every partial's output words, 4 partials' worth
+  // of independent loads at a time.
+  constexpr int kPCap = kSlots * kMaxRows * kMergePitch / (2 * kMaxRows);  // partials per block
+  float* sml = &sm.o[0][0][0];  // [p][row][2]
   float M[kMaxRows], O[kMaxRows];
 #pragma unroll
   for (int rho = 0; rho < kMaxRows; ++rho) {
-    M[rho] = s_ml[rho];
+    M[rho] = kNeg;
     O[rho] = 0.f;
   }
-  // every partial's 8 rows at once: independent loads, one round trip per partial
-#pragma unroll 2
-  for (int p = 0; p < nparts; ++p) {
-    const float* pr = base + (int64_t)p * kMaxRows * kPartStride;
+  // pass 1: the maxima
+  for (int p0 = 0; p0 < nparts; p0 += kPCap) {
+    const int np = min(kPCap, nparts - p0);
+    for (int i = c; i < np * kMaxRows; i += kThreads) {
+      const float* pr = base + ((int64_t)(p0 + i / kMaxRows) * kMaxRows + i % kMaxRows) * kPartStride;
+      sml[2 * i] = __ldcg(pr);
+      sml[2 * i + 1] = __ldcg(pr + 1);
+    }
+    __syncthreads();
+    if (c < rows) {
+      float m = p0 == 0 ? kNeg : s_ml[c];
+      for (int p = 0; p < np; ++p) m = fmaxf(m, sml[2 * (p * kMaxRows + c)]);
+      s_ml[c] = m;
+    }
+    __syncthreads();
+  }
+  if (nparts > kPCap) {  // the maxima are final only now: the sums in a second pass over the blocks
+    if (c < rows) s_ml[kMaxRows + c] = 0.f;
+    for (int p0 = 0; p0 < nparts; p0 += kPCap) {
+      const int np = min(kPCap, nparts - p0);
+      __syncthreads();
+      for (int i = c; i < np * kMaxRows; i += kThreads) {
+        const float* pr = base + ((int64_t)(p0 + i / kMaxRows) * kMaxRows + i % kMaxRows) * kPartStride;
+        sml[2 * i] = __ldcg(pr);
+        sml[2 * i + 1] = __ldcg(pr + 1);
+      }
+      __syncthreads();
+      if (c < rows) {
+        float l = s_ml[kMaxRows + c];
+        const float m = s_ml[c];
+        for (int p = 0; p < np; ++p) l += sml[2 * (p * kMaxRows + c) + 1] * fast_exp2(sml[2 * (p * kMaxRows + c)] - m);
+        s_ml[kMaxRows + c] = l;
+      }
+    }
+  } else if (c < rows) {
+    float l = 0.f;
+    const float m = s_ml[c];
+    for (int p = 0; p < nparts; ++p) l += sml[2 * (p * kMaxRows + c) + 1] * fast_exp2(sml[2 * (p * kMaxRows + c)] - m);
+    s_ml[kMaxRows + c] = l;
+  }
+  __syncthreads();
 #pragma unroll
-    for (int rho = 0; rho < kMaxRows; ++rho)
-      if (rho < rows)
-        O[rho] += __ldcg(pr + rho * kPartStride + 4 + c) * fast_exp2(__ldcg(pr + rho * kPartStride) - M[rho]);
+  for (int rho = 0; rho < kMaxRows; ++rho) M[rho] = s_ml[rho];
+  for (int p0 = 0; p0 < nparts; p0 += 4) {
+    float ov[4][kMaxRows], mv[4][kMaxRows];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int rho = 0; rho < kMaxRows; ++rho) {
+        const bool in = p0 + u < nparts && rho < rows;
+        const float* pr = base + ((int64_t)(p0 + u) * kMaxRows + rho) * kPartStride;
+        ov[u][rho] = in ? __ldcg(pr + 4 + c) : 0.f;
+        mv[u][rho] = in ? __ldcg(pr) : kNeg;
+      }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int rho = 0; rho < kMaxRows; ++rho)
+        if (p0 + u < nparts && rho < rows) O[rho] += ov[u][rho] * fast_exp2(mv[u][rho] - M[rho]);
   }
   const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
   const int G = a.G;
@@ -920,7 +958,59 @@ __device__ __forceinline__ void select_epilogue(const AttnArgs& a, uint8_t* dyn,
   }
 }
 
-template <int BITS, bool MERGED, bool FETCH, bool TOPK>
+// Clustered combine: when all CTAs of a (b, hkv) form one thread-block
+// cluster, each keeps its partial in shared memory and, after a cluster
+// barrier, CTA r merges query row r (r, r + chunks, ...) from every CTA's
+// partial through distributed shared memory: no partials in global memory,
+// no fences, no ticket.
+__device__ __forceinline__ void cluster_combine(CtaMerge& sm, const AttnArgs& a, float* cpart) {
+  namespace cgx = cooperative_groups;
+  cgx::cluster_group cluster = cgx::this_cluster();
+  __syncthreads();
+  const int c = threadIdx.x;  // channel
+  const int rows = 2 * a.G;
+  for (int rho = 0; rho < rows; ++rho) {
+    float M = kNeg;
+#pragma unroll
+    for (int w = 0; w < kSlots; ++w) M = fmaxf(M, sm.m[w][rho]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSlots; ++w) {
+      const float f = fast_exp2(sm.m[w][rho] - M);
+      L += sm.l[w][rho] * f;
+      O += sm.o[w][rho][c] * f;
+    }
+    float* pr = cpart + rho * kPartStride;
+    if (c == 0) {
+      pr[0] = M;
+      pr[1] = L;
+    }
+    pr[4 + c] = O;
+  }
+  cluster.sync();
+  const unsigned n = cluster.num_blocks();
+  const int64_t bh = blockIdx.y;
+  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
+  for (int rho = (int)cluster.block_rank(); rho < rows; rho += (int)n) {
+    float M = kNeg;
+    for (unsigned p = 0; p < n; ++p) M = fmaxf(M, cluster.map_shared_rank(cpart, p)[rho * kPartStride]);
+    float L = 0.f, O = 0.f;
+#pragma unroll 4
+    for (unsigned p = 0; p < n; ++p) {
+      const float* pr = cluster.map_shared_rank(cpart, p) + rho * kPartStride;
+      const float f = fast_exp2(pr[0] - M);
+      L += pr[1] * f;
+      O += pr[4 + c] * f;
+    }
+    const int qi = rho / G, gi = rho % G;
+    const int64_t orow = ((int64_t)b * 2 + qi) * a.Hq + hk * G + gi;
+    a.out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O / L : 0.f);
+    if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
+  }
+  cluster.sync();  // every CTA's partial stays readable until all rows are merged
+}
+
+template <int BITS, bool MERGED, bool FETCH, bool TOPK, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ int s_last;
@@ -948,6 +1038,10 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
     __syncthreads();
   }
   lowbit_cta<BITS, MERGED, FETCH>(a, dyn_smem, s_q, merge);
+  if constexpr (CLUSTER) {
+    cluster_combine(merge, a, reinterpret_cast<float*>(dyn_smem + kClusterPartOffset));
+    return;
+  }
   const bool combined = merge_store_combine(merge, a, &s_last, s_ml);
   if constexpr (TOPK) {
     __syncthreads();  // the query tile and the merge buffer are free from here on
@@ -980,8 +1074,8 @@ static int resident_ctas() {
   }
   int n = 0;
   const int smem = attn_smem_bytes(BITS);
-  cudaError_t e = spc_host::ensure_smem_limit(configured, attn_kernel<BITS, true, FETCH, false>, smem);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<BITS, true, FETCH, false>, kThreads, smem);
+  cudaError_t e = spc_host::ensure_smem_limit(configured, attn_kernel<BITS, true, FETCH, false, false>, smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<BITS, true, FETCH, false, false>, kThreads, smem);
   if (e != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = 2;
@@ -1049,37 +1143,94 @@ size_t step_workspace_bytes(const spc_dims* d, int32_t k_max) {
   return control_bytes(d) + parts_bytes(d) + cand_bytes(d, k_max);
 }
 
-template <int BITS, bool MERGED, bool FETCH, bool TOPK>
+template <int BITS, bool MERGED, bool FETCH, bool TOPK, bool CLUSTER>
 static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
   const int smem = attn_smem_bytes(BITS);
   static_assert((int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
                 "merge buffer fits in the dynamic shared memory");
+  static_assert(kClusterPartOffset + kMaxRows * kPartStride * 4 <= kWarps * (Stages<2>::value * 3600 + kZsBytes) &&
+                    kClusterPartOffset + kMaxRows * kPartStride * 4 <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
+                "the clustered combine's partial fits behind the merge buffer");
   static_assert(kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= 2576 + kZsBytes &&
                     kMaxRows * kTilePitch * 4 <= 2576 + kZsBytes,
                 "16-bit row batch and transfer tile fit in a warp's last stage and z/s table");
-  auto* fn = attn_kernel<BITS, MERGED, FETCH, TOPK>;
+  auto* fn = attn_kernel<BITS, MERGED, FETCH, TOPK, CLUSTER>;
   static unsigned long long configured = 0ull;  // one per instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
   if (e != cudaSuccess) return e;
   // programmatic serialisation: the launch overlaps the previous kernel's tail
-  // (the kernel waits for it before touching any data)
+  // (the kernel waits for it before touching any data); clustered: the CTAs of
+  // a (b, hkv) form one cluster
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.chunks, (unsigned)BH, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)a.chunks;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CLUSTER ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, fn, a);
+}
+
+// Whether the CTAs of every (b, hkv) can form one cluster (at most
+// kMaxCluster CTAs) with all B*Hkv clusters resident at once (occupancy query,
+// cached per device and cluster size).
+template <int BITS, bool MERGED, bool FETCH>
+static bool cluster_fits(int chunks, int64_t BH) {
+  if (chunks < 2 || chunks > kMaxCluster) return false;
+  static int cached[64][kMaxCluster + 1] = {};  // 0 unknown, else 1 + resident clusters
+  static unsigned long long configured = 0ull, nonportable = 0ull;
+  const int dev = spc_host::current_device();
+  if (dev >= 0 && dev < 64) {
+    const int c = __atomic_load_n(&cached[dev][chunks], __ATOMIC_ACQUIRE);
+    if (c > 0) return (int64_t)(c - 1) >= BH;
+  }
+  auto* fn = attn_kernel<BITS, MERGED, FETCH, false, true>;
+  const int smem = attn_smem_bytes(BITS);
+  int n = 0;
+  cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (e == cudaSuccess && chunks > 8 && !(__atomic_load_n(&nonportable, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess && bit != 0ull) __atomic_fetch_or(&nonportable, bit, __ATOMIC_ACQ_REL);
+  }
+  if (e == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)chunks, (unsigned)BH, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)chunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (dev >= 0 && dev < 64) __atomic_store_n(&cached[dev][chunks], n + 1, __ATOMIC_RELEASE);
+  return (int64_t)n >= BH;
 }
 
 template <int BITS, bool MERGED, bool TOPK>
 static cudaError_t launch_attn_f(const AttnArgs& a, int64_t BH, cudaStream_t stream, bool fetch) {
-  return fetch ? launch_attn<BITS, MERGED, true, TOPK>(a, BH, stream)
-               : launch_attn<BITS, MERGED, false, TOPK>(a, BH, stream);
+  if (!TOPK) {  // the clustered combine, when every (b, hkv)'s CTAs fit one cluster in one wave
+    if (fetch ? cluster_fits<BITS, MERGED, true>(a.chunks, BH) : cluster_fits<BITS, MERGED, false>(a.chunks, BH))
+      return fetch ? launch_attn<BITS, MERGED, true, false, true>(a, BH, stream)
+                   : launch_attn<BITS, MERGED, false, false, true>(a, BH, stream);
+  }
+  return fetch ? launch_attn<BITS, MERGED, true, TOPK, false>(a, BH, stream)
+               : launch_attn<BITS, MERGED, false, TOPK, false>(a, BH, stream);
 }
 
 // The fused selection works in the attention's dynamic shared memory: a

@@ -24,6 +24,8 @@ SMALL = [
     dict(B=1, Hq=4, Hkv=4, N=300, R=64, bits=2, k=7),          # MHA, 2-bit, r = 44
     dict(B=1, Hq=4, Hkv=1, N=96, R=32, bits=1, k=200),         # k > N_q (padding), tiny
     dict(B=1, Hq=4, Hkv=1, N=40, R=64, bits=1, k=4),           # N < R: no quantised tokens
+    dict(B=16, Hq=32, Hkv=8, N=4096, R=128, bits=1, k=41),     # B*Hkv = 128: 4 CTAs per (b, kv-head), clustered combine
+    dict(B=16, Hq=16, Hkv=8, N=3000, R=96, bits=2, k=19),      # the same at 2 bits, G = 2
     dict(B=2, Hq=8, Hkv=2, N=1000, R=40, bits=1, k=33, group=64),   # g = 64: N_q = 960, r = 40
     dict(B=1, Hq=4, Hkv=2, N=2100, R=128, bits=2, k=20, group=64),  # g = 64, 2-bit, r = 180
 ]
