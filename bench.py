@@ -584,6 +584,25 @@ class OracleSample:
         return 1.0 / (seconds * self.scale_to_step)
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(value_ms, world, device):
+    """The slowest rank's time: every rank's value reduced with MAX (one rank: itself)."""
+    if world <= 1:
+        return value_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, steps, total_ms):
+    """Whole-job steps/s: each of the `world` ranks runs `steps` steps of its own
+    replica of the workload (weak scaling; the path has no exchange step)."""
+    return world * steps / (total_ms / 1000.0)
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -651,13 +670,9 @@ def main():
     torch.cuda.synchronize()
     per_layer = step.attn_ms()
     per_layer_topk = step.topk_ms()
-    total_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
     ms_per_step = total_ms / args.steps
-    value = world * args.steps / (total_ms / 1000.0)
+    value = job_throughput(world, args.steps, total_ms)
 
     # ---- end to end: queries in from pinned host memory, outputs back, every step ----
     h2d = step.q_host.numel() * step.q_host.element_size()
@@ -673,12 +688,8 @@ def main():
             step.o_host.copy_(step.o, non_blocking=True)
     e1.record(step.main)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
+    e2e = {"value": job_throughput(world, args.steps, e2e_ms), "unit": "steps/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
     # ---- roofline of the dominant call (merged attention, one layer per launch) ----
