@@ -21,7 +21,10 @@
 //   A = (q o s) for the 8 query rows (2 tokens x G <= 4 heads), split into an
 //       fp16 high part (rows 0..7) and the fp16 residual (rows 8..15), so the
 //       speculative logits keep ~22 significant bits;
-//   B = the key bits, exact {0, 1} (or {0, 2} for the high plane at 2 bits).
+//   B = the key bits, exact: each an fp16 power of two that depends only on
+//       the token column (one AND of a rotated record word, see key_frag),
+//       divided out of the logit per column; the high plane at 2 bits
+//       multiplies a doubled A.
 // The value side o = sum_n p_n (z_n + s_n b_n) is the same product with
 // A = value bits (channels x tokens) and B = p o s (tokens x query rows); the
 // p*z term is accumulated on CUDA cores.  Softmax runs in base 2 with the
@@ -55,6 +58,12 @@ constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pa
 constexpr int kZsPitch = 17;     // float4s per t block of a z/s table (16 + 1 pad)
 constexpr int kZsBytes = 2 * 4 * kZsPitch * 16;  // key and value tables of one warp
 constexpr int kMergePitch = kD + 4;              // padded row of the CTA merge buffer
+// Dynamic shared memory of one CTA: per warp, the low-bit stages (a record, a
+// 16-byte slot, a pre-fetched 16-bit row) and the z/s tables.
+template <int BITS>
+__host__ __device__ constexpr int attn_dyn_bytes() {
+  return kWarps * (Stages<BITS>::value * (1024 * (BITS + 1) + 16 + 512) + kZsBytes);
+}
 constexpr int kRowBatch = 8;                     // 16-bit rows staged per batch (512 bytes each)
 constexpr int kTilePitch = kD + 4;               // padded row of a warp's query / output transfer tile
 
@@ -96,14 +105,22 @@ struct AttnArgs {
   int32_t sel_k, sel_keff, cand_cap;
 };
 
-// Bits r and r+16 of w as an f16x2 pair, each 0 or the fp16 pattern v (1.0
-// or 2.0): isolate the two bits, then one multiply moves each onto v's
-// pattern (v is a multiple of 2^10, so v >> r is exact for r <= 10).  For
-// r >= 11 the caller passes ws = w >> 5 and the same rule applies at r - 5.
-__device__ __forceinline__ uint32_t bit_pair(uint32_t w, uint32_t ws, int r, uint32_t v) {
-  if (r <= 10) return (w & ((1u << r) | (1u << (r + 16)))) * (v >> r);
-  return (ws & ((1u << (r - 5)) | (1u << (r + 11)))) * (v >> (r - 5));
+// A lone set bit at position p of an fp16 half (p = 10..14, the exponent
+// field) is the power of two 2^(2^(p-10) - 15); pos_comp(p) is its inverse.
+__host__ __device__ constexpr float pos_comp(int p) {
+  return p == 10 ? 16384.f : p == 11 ? 8192.f : p == 12 ? 2048.f : p == 13 ? 128.f : 0.5f;
 }
+
+// Key bits.  Record word j of lane (gid, t) holds, for token 8 nt + gid and
+// channel pair e = 4j + i (channels 16 (e >> 1) + 8 (e & 1) + 2t + {0, 1}),
+// the two bits that a left rotation by 4i brings to bits 11 + nt and 27 + nt:
+// so one AND of the rotated word is the B fragment {0, 2^-13 .. 2} of token
+// column nt, the same power of two for all its channels, which the logit
+// multiplies back per column (key_comp).
+__device__ __forceinline__ uint32_t key_frag(uint32_t rotated, int nt) {
+  return rotated & ((1u << (11 + nt)) | (1u << (27 + nt)));
+}
+__host__ __device__ constexpr float key_comp(int nt) { return pos_comp(11 + nt); }
 
 // Bits r and r+16 of w as an f16x2 pair {0, 2^bit_exp(r)} with a single AND:
 // the word is pre-rotated so that the two bits sit on one fp16 exponent bit
@@ -120,10 +137,7 @@ __device__ __forceinline__ uint32_t bit_pair_exp(uint32_t w, uint32_t r5, uint32
 __host__ __device__ constexpr int bit_pos(int r) {
   return (r >= 10 && r <= 14) ? r : (r >= 5 && r <= 9) ? r + 5 : (r <= 4) ? r + 10 : 14;
 }
-__host__ __device__ constexpr float bit_comp(int r) {
-  return bit_pos(r) == 10 ? 16384.f : bit_pos(r) == 11 ? 8192.f : bit_pos(r) == 12 ? 2048.f
-         : bit_pos(r) == 13 ? 128.f : 0.5f;
-}
+__host__ __device__ constexpr float bit_comp(int r) { return pos_comp(bit_pos(r)); }
 
 // fp16 high part of two floats (truncated to 11 significant bits, exact in
 // fp16) and the fp16 rounding of the remainder.
@@ -176,19 +190,20 @@ __device__ __forceinline__ float reduce_scatter16(const float (&x)[16], int lane
 }
 
 // The residual window and the fetched rows of this warp's range, before its
-// low-bit groups.  Rows are staged kRowBatch at a time with cp.async into
-// `tail` (the warp's last stage and z/s table, free until the low-bit loop
-// starts); issue_lowbit() puts the first low-bit stages in flight behind the
-// first batch.  Logits: lane = 4 channels x 8 query rows for two rows at a
+// low-bit groups (whose first stages are already in flight).  Rows are staged
+// kRowBatch at a time with cp.async into `tail` (the warp's last stage and z/s
+// table, free until the low-bit loop starts).  fill_query() is the CTA-wide
+// fill of sq (it ends with a barrier); the positions of the warp's first
+// fetched rows are loaded before it, so that both latencies overlap.  Logits: lane = 4 channels x 8 query rows for two rows at a
 // time, then a reduce-scatter leaves lane with row (lane >> 4), query row
 // (lane >> 1) & 7.  Value product: lane = 4 channels, p broadcast from shared
 // memory.  sq is the CTA's scaled query tile [kMaxRows][kTilePitch] (rows
 // 2G.. zero).  On return (m_run, l_run, oacc) hold the softmax state of the
 // rows, in the tensor-core fragment layouts of the low-bit loop (oacc divided by the per-channel powers of two that loop
 // multiplies back at its end).
-template <bool MERGED, int STAGES, typename IssueLowbit>
+template <bool MERGED, typename FillQuery>
 __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* sq, uint8_t* tail,
-                                                IssueLowbit&& issue_lowbit, float& m_run, float& l_run,
+                                                FillQuery&& fill_query, float& m_run, float& l_run,
                                                 float (&oacc)[8][4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, t = lane & 3;
@@ -208,21 +223,18 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
   float o16[kMaxRows][4];
 #pragma unroll
   for (int rho = 0; rho < kMaxRows; ++rho) o16[rho][0] = o16[rho][1] = o16[rho][2] = o16[rho][3] = 0.f;
-  bool lowbit_issued = false;
+  // quantised position of the fetched row of lane (window w0), -1 for the residual window
+  auto row_pos = [&](int w0) {
+    const int j = w0 + lane;
+    return (lane < min(32, j1 - w0) && j >= a.r) ? a.idx[bh * a.k + (j - a.r)] : -1;
+  };
+  const int pos_first = row_pos(j0);
+  fill_query();
 
   for (int w0 = j0; w0 < j1; w0 += 32) {
     const int nwin = min(32, j1 - w0);
-    int pos = -1;  // quantised position of a fetched row, -1 for the residual window
-    bool ok = false;
-    if (lane < nwin) {
-      const int j = w0 + lane;
-      if (j < a.r) {
-        ok = true;
-      } else {
-        pos = a.idx[bh * a.k + (j - a.r)];
-        ok = pos >= 0 && pos < a.nq;
-      }
-    }
+    const int pos = w0 == j0 ? pos_first : row_pos(w0);
+    const bool ok = lane < nwin && (w0 + lane < a.r || (pos >= 0 && pos < a.nq));
     const uint32_t valid = __ballot_sync(0xFFFFFFFFu, ok);
     for (int b0 = 0; b0 < nwin; b0 += kRowBatch) {
       const int nb = min(kRowBatch, nwin - b0);
@@ -235,13 +247,7 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
         }
       }
       cp_async_commit();
-      if (!lowbit_issued) {
-        issue_lowbit();  // STAGES - 1 commit groups behind this batch
-        lowbit_issued = true;
-        cp_async_wait<STAGES - 1>();
-      } else {
-        cp_async_wait<0>();
-      }
+      cp_async_wait<0>();  // with the first batch, also the low-bit stages issued before it
       __syncwarp();
 
       float lg[kRowBatch / 2];
@@ -314,8 +320,6 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
       __syncwarp();
     }
   }
-  if (!lowbit_issued) issue_lowbit();
-
   // hand the state over to the fragment layout through `tail`
   float* tile = reinterpret_cast<float*>(tail);  // [kMaxRows][kTilePitch]
 #pragma unroll
@@ -339,8 +343,9 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
 }
 
 // ------------------------------------------------------------ low-bit CTA
-template <int BITS, bool MERGED, bool FETCH>
-__device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, const float* sq, CtaMerge& merge) {
+template <int BITS, bool MERGED, bool FETCH, typename FillQuery>
+__device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, const float* sq, CtaMerge& merge,
+                                           FillQuery&& fill_query) {
   constexpr int RB = 1024 * (BITS + 1);
   constexpr int KMETA = 512 * BITS;
   constexpr int VCODES = KMETA + 512;
@@ -350,6 +355,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   constexpr int STAGE = PFROW + 512;
   constexpr int kStages = Stages<BITS>::value;
   constexpr int WARP_BYTES = kStages * STAGE + kZsBytes;
+  static_assert(kWarps * WARP_BYTES == attn_dyn_bytes<BITS>(), "stage layout and launch size disagree");
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, t = lane & 3;
@@ -410,13 +416,9 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   // channel 16*kc + 2*t + 8*h + half (registers at 1 bit, else read from sq)
   float m_run, l_run;
   float oacc[8][4];
-  rows16_prologue<MERGED, kStages>(
-      a, sq, stage + (kStages - 1) * STAGE,
-      [&]() {
 #pragma unroll 1
-        for (int s = 0; s < kStages - 1; ++s) issue(s);
-      },
-      m_run, l_run, oacc);
+  for (int s = 0; s < kStages - 1; ++s) issue(s);  // in flight behind the query fill and the 16-bit rows
+  rows16_prologue<MERGED>(a, sq, stage + (kStages - 1) * STAGE, fill_query, m_run, l_run, oacc);
   constexpr bool kQvReg = QueryInRegisters<BITS>::value;
   float qv[kQvReg ? 32 : 1];
   if constexpr (kQvReg) {
@@ -473,17 +475,13 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     __syncwarp();
 
     // ---- QK, channel chunk outer: A = q o s (hi/lo), B = key bits ----
-    uint32_t kw[4], kwh[4], kw1[4], kwh1[4];
+    uint32_t kw[4], kw1[4];  // word j: channel pairs 4j .. 4j+3 of the lane's four tokens
     {
       const uint4 v0 = *reinterpret_cast<const uint4*>(R + 16 * lane);
       kw[0] = v0.x; kw[1] = v0.y; kw[2] = v0.z; kw[3] = v0.w;
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) kwh[nt] = kw[nt] >> 5;
       if (BITS == 2) {
         const uint4 v1 = *reinterpret_cast<const uint4*>(R + 512 + 16 * lane);
         kw1[0] = v1.x; kw1[1] = v1.y; kw1[2] = v1.z; kw1[3] = v1.w;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) kwh1[nt] = kw1[nt] >> 5;
       }
     }
     float acc[4][4];
@@ -508,14 +506,20 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
       uint32_t af[4];
       split_hi_lo(f2_mul(q01, make_float2(s4.x, s4.y)), af[0], af[1]);
       split_hi_lo(f2_mul(q23, make_float2(s4.z, s4.w)), af[2], af[3]);
+      // channel pairs e = 2kc (b0) and 2kc + 1 (b1): word kc/2 rotated by 4i, i = e mod 4
+      const int rot = 8 * (kc & 1);
+      const uint32_t r0 = __funnelshift_l(kw[kc >> 1], kw[kc >> 1], rot);
+      const uint32_t r1 = __funnelshift_l(kw[kc >> 1], kw[kc >> 1], rot + 4);
+      if (BITS == 2) {  // high plane: weight 2, carried by doubling A (exact in fp16)
+        const uint32_t x0 = __funnelshift_l(kw1[kc >> 1], kw1[kc >> 1], rot);
+        const uint32_t x1 = __funnelshift_l(kw1[kc >> 1], kw1[kc >> 1], rot + 4);
+        const uint32_t af2[4] = {hadd2_u32(af[0], af[0]), hadd2_u32(af[1], af[1]), hadd2_u32(af[2], af[2]),
+                                 hadd2_u32(af[3], af[3])};
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        if (BITS == 2)
-          mma_16816(acc[nt], af, bit_pair(kw1[nt], kwh1[nt], 2 * kc, 0x4000u),
-                    bit_pair(kw1[nt], kwh1[nt], 2 * kc + 1, 0x4000u));
-        mma_16816(acc[nt], af, bit_pair(kw[nt], kwh[nt], 2 * kc, 0x3C00u),
-                  bit_pair(kw[nt], kwh[nt], 2 * kc + 1, 0x3C00u));
+        for (int nt = 0; nt < 4; ++nt) mma_16816(acc[nt], af2, key_frag(x0, nt), key_frag(x1, nt));
       }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) mma_16816(acc[nt], af, key_frag(r0, nt), key_frag(r1, nt));
     }
     float bias = bias2.x + bias2.y;
     bias += __shfl_xor_sync(0xFFFFFFFFu, bias, 1);
@@ -527,8 +531,8 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     float lg[4][2];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      const float2 l = f2_add(f2_add(make_float2(acc[nt][0], acc[nt][1]), make_float2(acc[nt][2], acc[nt][3])),
-                              make_float2(bias, bias));
+      const float2 l = f2_fma(f2_add(make_float2(acc[nt][0], acc[nt][1]), make_float2(acc[nt][2], acc[nt][3])),
+                              make_float2(key_comp(nt), key_comp(nt)), make_float2(bias, bias));
       lg[nt][0] = l.x;
       lg[nt][1] = l.y;
     }
@@ -706,8 +710,21 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
 }
 
 // ------------------------------------------------------------ merge + combine
-// Returns whether this CTA was the last of its (b, hkv) and so combined the partials.
-__device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last, float* s_ml) {
+// Output row and log-sum-exp of query row rho of (b, hkv) bh from its merged
+// softmax state (max M, sum L, unnormalised output O at channel c).
+__device__ __forceinline__ void write_row(const AttnArgs& a, int64_t bh, int rho, float M, float L, float O, int c) {
+  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
+  const int qi = rho / G, gi = rho % G;
+  const int64_t orow = ((int64_t)b * 2 + qi) * a.Hq + hk * G + gi;
+  a.out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O / L : 0.f);
+  if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
+}
+
+// Returns whether this CTA was the last of its (b, hkv) and so combined the
+// partials.  part_cap: partials that fit in the CTA's dynamic shared memory
+// (which starts with the merge buffer `sm`).
+__device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last, float* s_ml,
+                                                    int part_cap) {
   __syncthreads();
   const int c = threadIdx.x;  // channel
   const int64_t bh = blockIdx.y;
@@ -740,6 +757,37 @@ __device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs
   if (!*s_last) return false;
   __threadfence();
   const float* base = a.part + (bh * nparts * kMaxRows) * kPartStride;
+  if (nparts <= part_cap) {
+    // Every partial's used rows into shared memory (the merge buffer and the
+    // stages, free now) with one round of copies, then per query row the
+    // arithmetic of the clustered combine in the same order, so that both
+    // give identical results.
+    float* sp = reinterpret_cast<float*>(&sm);
+    const int per_part = rows * (kPartStride / 4);  // 16-byte pieces of one partial's used rows
+    for (int i = c; i < nparts * per_part; i += kThreads) {
+      const int p = i / per_part, e = i - p * per_part;
+      cp_async16(sp + (p * kMaxRows * kPartStride) + 4 * e, base + (int64_t)p * kMaxRows * kPartStride + 4 * e);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int rho = 0; rho < rows; ++rho) {
+      float M = kNeg;
+      for (int p = 0; p < nparts; ++p) M = fmaxf(M, sp[(p * kMaxRows + rho) * kPartStride]);
+      float L = 0.f, O = 0.f;
+#pragma unroll 4
+      for (int p = 0; p < nparts; ++p) {
+        const float* pr = sp + (p * kMaxRows + rho) * kPartStride;
+        const float f = fast_exp2(pr[0] - M);
+        L += pr[1] * f;
+        O += pr[4 + c] * f;
+      }
+      write_row(a, bh, rho, M, L, O, c);
+    }
+    if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
+    return true;
+  }
+  // More partials than shared memory holds: two passes over (max, sum) blocks.
   // The (max, sum) words of every partial into shared memory (the merge
   // buffer, free now) in one round trip, 2 * kPCap (p, row) pairs at a time.
   // Then, per query row c: the max and the sum over the partials in partial
@@ -814,16 +862,10 @@ __device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs
       for (int rho = 0; rho < kMaxRows; ++rho)
         if (p0 + u < nparts && rho < rows) O[rho] += ov[u][rho] * fast_exp2(mv[u][rho] - M[rho]);
   }
-  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv);
-  const int G = a.G;
 #pragma unroll
   for (int rho = 0; rho < kMaxRows; ++rho) {
     if (rho >= rows) break;
-    const float L = s_ml[kMaxRows + rho];
-    const int qi = rho / G, gi = rho % G;
-    const int64_t orow = ((int64_t)b * 2 + qi) * a.Hq + hk * G + gi;
-    a.out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O[rho] / L : 0.f);
-    if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M[rho] + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
+    write_row(a, bh, rho, M[rho], s_ml[kMaxRows + rho], O[rho], c);
   }
   if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
   return true;
@@ -990,7 +1032,6 @@ __device__ __forceinline__ void cluster_combine(CtaMerge& sm, const AttnArgs& a,
   cluster.sync();
   const unsigned n = cluster.num_blocks();
   const int64_t bh = blockIdx.y;
-  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
   for (int rho = (int)cluster.block_rank(); rho < rows; rho += (int)n) {
     float M = kNeg;
     for (unsigned p = 0; p < n; ++p) M = fmaxf(M, cluster.map_shared_rank(cpart, p)[rho * kPartStride]);
@@ -1002,10 +1043,7 @@ __device__ __forceinline__ void cluster_combine(CtaMerge& sm, const AttnArgs& a,
       L += pr[1] * f;
       O += pr[4 + c] * f;
     }
-    const int qi = rho / G, gi = rho % G;
-    const int64_t orow = ((int64_t)b * 2 + qi) * a.Hq + hk * G + gi;
-    a.out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O / L : 0.f);
-    if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
+    write_row(a, bh, rho, M, L, O, c);
   }
   cluster.sync();  // every CTA's partial stays readable until all rows are merged
 }
@@ -1020,7 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   __shared__ __align__(16) float s_q[kMaxRows * kTilePitch];
   CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem);
   grid_dependency_sync();  // nothing is read or written before the previous kernel is done
-  {
+  auto fill_query = [&]() {
     // scaled query rows of this (b, hkv): rho = i * G + gi for token i, head gi
     const int64_t bh = blockIdx.y;
     const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
@@ -1036,13 +1074,14 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
       *reinterpret_cast<float4*>(s_q + rho * kTilePitch + 4 * c4) = v;
     }
     __syncthreads();
-  }
-  lowbit_cta<BITS, MERGED, FETCH>(a, dyn_smem, s_q, merge);
+  };
+  lowbit_cta<BITS, MERGED, FETCH>(a, dyn_smem, s_q, merge, fill_query);
   if constexpr (CLUSTER) {
     cluster_combine(merge, a, reinterpret_cast<float*>(dyn_smem + kClusterPartOffset));
     return;
   }
-  const bool combined = merge_store_combine(merge, a, &s_last, s_ml);
+  constexpr int kPartCap = attn_dyn_bytes<BITS>() / (int)(kMaxRows * kPartStride * sizeof(float));
+  const bool combined = merge_store_combine(merge, a, &s_last, s_ml, kPartCap);
   if constexpr (TOPK) {
     __syncthreads();  // the query tile and the merge buffer are free from here on
     select_epilogue<BITS>(a, dyn_smem, *reinterpret_cast<SelShared<kThreads>*>(s_q), combined, &s_last, s_ml);
@@ -1056,10 +1095,7 @@ struct AttnPlan {
   int groups_per_chunk;
 };
 
-static int attn_smem_bytes(int bits) {
-  const int stages = bits == 1 ? Stages<1>::value : Stages<2>::value;
-  return kWarps * (stages * (1024 * (bits + 1) + 16 + 512) + kZsBytes);
-}
+static int attn_smem_bytes(int bits) { return bits == 1 ? attn_dyn_bytes<1>() : attn_dyn_bytes<2>(); }
 
 // Resident attention CTAs per SM on the current device (occupancy query,
 // cached per device, bit width and fetch variant).

@@ -7,9 +7,10 @@
 // out.  The next group's tiles stream in (cp.async, double-buffered) while the
 // current one is coded.  Per group: thread c finds key channel c's min/max and
 // parameters; then one warp per key token (and per value token pair) codes a
-// conflict-free 16-byte block per lane, and one ballot per code word yields
-// the packed word in the record's bit order directly (value groups' min/max
-// come from two xor-shuffles inside the same pass).
+// conflict-free 16-byte block per lane, and one ballot per code word yields a
+// packed word: value words in the record's bit order directly (value groups'
+// min/max come from two xor-shuffles inside the same pass), key words token-
+// major, then rotated into the record's order in one pass over the words.
 // The kernel streams HBM: 512 B read and 64/96 B written per token and KV head.
 #include "common.cuh"
 
@@ -190,11 +191,39 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
       if (lane == 0) sm.rec[VCODES + word] = b0;
     }
   }
+  __syncthreads();  // every key code word of every warp is in place
+  // ---- key code words into the record's order ----
+  // The ballots give token-major words: word 4L + n (L = 4a + t) holds token
+  // 8n + a, bit e + 16h for channel 16 (e >> 1) + 8 (e & 1) + 2t + h.  Record
+  // word 4L + j takes bits e = 4j + i (i = 0..3) of the four tokens: bit
+  // e + 16h of word n goes to bit (11 + n + 16h - 4i) mod 32, a left rotation
+  // by (11 + n - 4j - 5i) mod 32 of the pair (e, e + 16).
+  uint32_t kperm[BITS];
+  {
+    const int L = tid >> 2, j = tid & 3;
+#pragma unroll
+    for (int p = 0; p < BITS; ++p) {
+      uint32_t w = 0u;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const uint32_t src = __funnelshift_r(sm.rec[128 * p + 4 * L + n], sm.rec[128 * p + 4 * L + n], 4 * j);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // bits i, i + 16 of src are e, e + 16 of the word
+          const int rot = (11 + n - 5 * i) & 31;
+          w |= __funnelshift_l(src, src, rot) & __funnelshift_l(0x10001u << i, 0x10001u << i, rot);
+        }
+      }
+      kperm[p] = w;
+    }
+  }
   {
     const int tt = tid >> 5, m = tid & 31;
     const int kc = 16 * (m >> 2) + 2 * tt + 8 * ((m >> 1) & 1) + (m & 1);
     sm.rec[KMETA + tid] = sm.klohi[kc];
   }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < BITS; ++p) sm.rec[128 * p + tid] = kperm[p];
   __syncthreads();
 
   // ---- the record out, coalesced ----

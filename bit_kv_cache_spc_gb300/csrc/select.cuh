@@ -17,13 +17,21 @@ struct __align__(16) SelShared {
 
 // The kth largest (1 <= kth <= n) of keys[0..n): T, and how many keys equal
 // to T belong to the top kth (the other kth - need are > T).  MSB-first radix
-// select, 4 passes of 8 bits.
+// select, 4 passes of 8 bits.  A caller that knows T's top byte (top8 >= 0)
+// and that kth counts from the largest key with that top byte (none of keys
+// with a larger top byte is among keys) skips the first pass.
 template <int THREADS>
 __device__ __forceinline__ void cta_radix_select(const uint32_t* keys, int n, uint32_t kth, SelShared<THREADS>& sh,
-                                                 uint32_t& T, uint32_t& need) {
+                                                 uint32_t& T, uint32_t& need, int top8 = -1) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t prefix = 0u, pmask = 0u, rem = kth;
-  for (int pass = 0; pass < 4; ++pass) {
+  int pass0 = 0;
+  if (top8 >= 0) {
+    prefix = (uint32_t)top8 << 24;
+    pmask = 0xFF000000u;
+    pass0 = 1;
+  }
+  for (int pass = pass0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     for (int j = tid; j < 4 * 256; j += THREADS) (&sh.hist[0][0])[j] = 0u;
     __syncthreads();

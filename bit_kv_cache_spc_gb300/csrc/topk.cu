@@ -224,16 +224,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
 
 // ------------------------------------------------------------ k <= kMaxCand
 // Two-level selection for the usual small k (top 1% of a few ten thousand
-// positions).  Each CTA of the cluster selects its slice's own top-k' (k' =
-// min(k_eff, slice length), ties to the lower position) with a CTA-local radix
-// select and keeps those candidates, in ascending position, in shared memory.
-// Every globally selected position is among its slice's candidates (fewer than
-// k_eff positions of the slice precede it in the order key desc, position asc),
-// so after one cluster barrier the leader CTA selects the final k_eff from the
-// concatenated candidates (already in ascending position) and writes idx and
-// the bitmap.  Two cluster barriers in all, against six for the cluster-wide
-// radix select above.
+// positions).  Every CTA of the cluster keeps candidates of its slice, in
+// ascending position, in shared memory; after one cluster barrier the leader
+// CTA selects the final k_eff from the concatenated candidates (already in
+// ascending position) and writes idx and the bitmap.  The candidates are
+//   * when few enough: every key whose top 12 bits (the bin) are at least
+//     those of the k_eff-th largest key of the row, which one histogram pass
+//     per CTA and the sum of the cluster's histograms through distributed
+//     shared memory find (the bin's lower bound is a threshold no selected key
+//     is below);
+//   * otherwise: the slice's own top-k' (k' = min(k_eff, slice length), ties
+//     to the lower position) from a CTA-local radix select.  Every globally
+//     selected position is among them (fewer than k_eff positions of the
+//     slice precede it in the order key desc, position asc).
 constexpr int kMaxCand = 2048;
+constexpr int kBinShift = 19;                  // bin = key >> 19: 8 exponent and 4 mantissa bits
+constexpr int kBins = 1 << (31 - kBinShift);   // keys are scores >= 0: bit 31 is clear
 
 // two CTAs of 1024 threads per SM (32 registers), so a cluster per (b, hkv) row fits one wave
 __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArgs a) {
@@ -244,8 +250,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
   __shared__ uint32_t weq[kTopkMaxSlice / 32];
   __shared__ uint32_t ckey[kMaxCand], cpos[kMaxCand];  // this CTA's candidates, ascending position
   __shared__ SelShared<kTopkThreads> sh;
-  __shared__ uint32_t s_count;  // candidates kept by this CTA
-  __shared__ float s_nlse[4];   // -lse * log2(e) of the speculative row of each head of the group
+  __shared__ uint32_t hist[kBins];  // this CTA's bin counts
+  __shared__ uint32_t s_count;      // candidates kept by this CTA
+  __shared__ uint32_t s_bin[3];     // the k_eff-th largest key's bin, keys at or above it, keys above its top byte
+  __shared__ float s_nlse[4];       // -lse * log2(e) of the speculative row of each head of the group
 
   const int tid = threadIdx.x;
   const unsigned rank = cluster.block_rank();
@@ -259,6 +267,8 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
 
   // ---- scores, four positions per thread and round, the round's loads issued up front ----
   if (tid < 4) s_nlse[tid] = tid < a.G ? -a.lse[((int64_t)b * 2 + 1) * a.Hq + hk * a.G + tid] * kLog2e : 0.f;
+  for (int j = tid; j < kBins; j += kTopkThreads) hist[j] = 0u;
+  if (tid == 0) s_count = 0u;
   __syncthreads();
   const float* lrow = a.logits + (bh * a.G) * (int64_t)a.Lcap + n0;
   for (int i = 4 * tid; i < len; i += 4 * kTopkThreads) {
@@ -280,46 +290,150 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
     }
     *reinterpret_cast<uint4*>(keys + i) =
         make_uint4(__float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
+    atomicAdd(&hist[__float_as_uint(sc.x) >> kBinShift], 1u);  // this slice's bin counts
+    atomicAdd(&hist[__float_as_uint(sc.y) >> kBinShift], 1u);
+    atomicAdd(&hist[__float_as_uint(sc.z) >> kBinShift], 1u);
+    atomicAdd(&hist[__float_as_uint(sc.w) >> kBinShift], 1u);
+  }
+  cluster.sync();  // every CTA's keys and bin counts are complete
+
+  // ---- the row's bin counts (the sum over the cluster) and the bin of the k_eff-th largest key ----
+  const int lane = tid & 31, warp = tid >> 5;
+  if (a.keff > 0) {
+    // thread t owns bins 4t .. 4t+3
+    static_assert(kBins == 4 * kTopkThreads, "four bins per thread");
+    uint32_t c[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (r < (int)ncta) {
+        const uint4 h = reinterpret_cast<const uint4*>(cluster.map_shared_rank(hist, (unsigned)r))[tid];
+        c[0] += h.x;
+        c[1] += h.y;
+        c[2] += h.z;
+        c[3] += h.w;
+      }
+    }
+    const uint32_t own = c[0] + c[1] + c[2] + c[3];
+    uint32_t suf = own;  // inclusive suffix sum over the lanes >= this one
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, suf, off);
+      if (lane + off < 32) suf += v;
+    }
+    if (lane == 0) sh.wsum[0][warp] = suf;
+    __syncthreads();
+    if (warp == 0) {  // exclusive suffix sum over the warps
+      const uint32_t wt = sh.wsum[0][lane];
+      uint32_t x = wt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, x, off);
+        if (lane + off < 32) x += v;
+      }
+      sh.wsum[1][lane] = x - wt;
+    }
+    __syncthreads();
+    const uint32_t above0 = sh.wsum[1][warp] + suf - own;  // keys in bins above 4t+3
+    const uint32_t keff = (uint32_t)a.keff;
+    if (above0 < keff && keff <= above0 + own) {
+      uint32_t above = above0;
+      for (int j = 3; j >= 0; --j) {
+        if (above + c[j] >= keff) {
+          s_bin[0] = (uint32_t)(4 * tid + j);
+          s_bin[1] = above + c[j];
+          break;
+        }
+        above += c[j];
+      }
+    }
+    __syncthreads();
+    // keys whose top byte is above that of the bin (bins from 32 (top + 1) up)
+    if (4 * tid + 4 == 32 * (int)((s_bin[0] >> 5) + 1)) s_bin[2] = above0;
   }
   __syncthreads();
 
-  // ---- this slice's top-k' candidates ----
+  // ---- this slice's candidates ----
   const uint32_t kloc = (uint32_t)min(a.keff, len);
-  if (kloc > 0) {
+  if (a.keff > 0 && s_bin[1] <= (uint32_t)kMaxCand) {  // the same decision in every CTA of the cluster
+    // every key at or above the bin's lower bound; warp w compacts words
+    // w*per .. w*per+per-1 in order: ballots first (kept in wgt), then the
+    // warp's offset from the lower warps' counts
+    const uint32_t lower = s_bin[0] << kBinShift;
+    const int nw = len >> 5, per = (nw + kTopkWarps - 1) / kTopkWarps;
+    const int w0 = min(nw, warp * per), w1 = min(nw, w0 + per);
+    uint32_t cnt = 0u;
+    for (int w = w0; w < w1; ++w) {
+      const uint32_t bits = __ballot_sync(0xFFFFFFFFu, keys[32 * w + lane] >= lower);
+      if (lane == 0) wgt[w] = bits;
+      cnt += __popc(bits);
+    }
+    if (lane == 0) sh.wsum[0][warp] = cnt;
+    __syncthreads();
+    uint32_t off = lane < warp ? sh.wsum[0][lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xFFFFFFFFu, off, o);
+    if (warp == kTopkWarps - 1 && lane == 0) s_count = off + cnt;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int w = w0; w < w1; ++w) {
+      const uint32_t bits = wgt[w];
+      if ((bits >> lane) & 1u) {
+        const uint32_t r = off + __popc(bits & below);
+        ckey[r] = keys[32 * w + lane];
+        cpos[r] = (uint32_t)(n0 + 32 * w + lane);
+      }
+      off += __popc(bits);
+    }
+  } else if (kloc > 0) {
     uint32_t T, need;
     cta_radix_select(keys, len, kloc, sh, T, need);
     ordered_take(keys, len, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
       ckey[r] = keys[i];
       cpos[r] = (uint32_t)(n0 + i);
     });
+    if (tid == 0) s_count = kloc;
   }
-  if (tid == 0) s_count = kloc;
   cluster.sync();
 
+  // ---- merge in the leader: the candidates of every CTA, in rank (= position) order ----
+  __shared__ uint32_t s_off[9];  // candidate offsets of the ranks, then the total
+  const bool filtered = a.keff > 0 && s_bin[1] <= (uint32_t)kMaxCand;
+  uint32_t M = 0;
+  uint32_t* mkey = dyn;
   if (rank == 0) {
-    // ---- merge: the candidates of every CTA, in rank (= position) order ----
-    uint32_t M = 0;
-    for (unsigned r = 0; r < ncta; ++r) M += *cluster.map_shared_rank(&s_count, r);
-    uint32_t* mkey = dyn;
+    if (tid < (int)ncta) wgt[tid] = *cluster.map_shared_rank(&s_count, (unsigned)tid);
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t o = 0;
+      for (unsigned r = 0; r < ncta; ++r) {
+        s_off[r] = o;
+        o += wgt[r];
+      }
+      s_off[ncta] = o;
+    }
+    __syncthreads();
+    M = s_off[ncta];
+    uint32_t* mpos = dyn + M;
+    for (uint32_t i = tid; i < M; i += kTopkThreads) {
+      unsigned r = 0;
+      while (i >= s_off[r + 1]) ++r;
+      mkey[i] = cluster.map_shared_rank(ckey, r)[i - s_off[r]];
+      mpos[i] = cluster.map_shared_rank(cpos, r)[i - s_off[r]];
+    }
+  }
+  cluster.sync();  // the leader has read every CTA's candidates: the others are done
+  if (rank == 0) {
     uint32_t* mpos = dyn + M;
     uint32_t* sbm = dyn + 2 * M;  // bitmap of the selection, one word per 32 quantised positions
     const int nwq = a.nq >> 5;
-    for (unsigned r = 0, off = 0; r < ncta; ++r) {
-      const uint32_t cnt = *cluster.map_shared_rank(&s_count, r);
-      const uint32_t* rk = cluster.map_shared_rank(ckey, r);
-      const uint32_t* rp = cluster.map_shared_rank(cpos, r);
-      for (uint32_t i = tid; i < cnt; i += kTopkThreads) {
-        mkey[off + i] = rk[i];
-        mpos[off + i] = rp[i];
-      }
-      off += cnt;
-    }
     for (int w = tid; w < nwq; w += kTopkThreads) sbm[w] = 0u;
     __syncthreads();
     int32_t* out = a.idx + bh * a.k;
     if (a.keff > 0) {
       uint32_t T, need;
-      cta_radix_select(mkey, (int)M, (uint32_t)a.keff, sh, T, need);
+      if (filtered)  // the threshold's top byte is the bin's; keys above that byte are all selected
+        cta_radix_select(mkey, (int)M, (uint32_t)a.keff - s_bin[2], sh, T, need, (int)(s_bin[0] >> 5));
+      else
+        cta_radix_select(mkey, (int)M, (uint32_t)a.keff, sh, T, need);
       ordered_take(mkey, (int)M, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
         const uint32_t p = mpos[i];
         out[r] = (int32_t)p;
@@ -330,7 +444,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
     uint32_t* bm = a.bitmap + bh * a.q_groups_cap;
     for (int w = tid; w < a.q_groups_cap; w += kTopkThreads) bm[w] = w < nwq ? sbm[w] : 0u;
   }
-  cluster.sync();  // the leader has read every CTA's candidates
 }
 
 spc_status launch_topk(const spc_dims* d, const float* logits, const float* lse, int32_t k, int32_t* idx,

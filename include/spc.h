@@ -84,8 +84,13 @@ int32_t spc_num_quantized(const spc_dims* d);
  *   V codes  : `bits` planes of 128 u32 words
  *   V minmax : 128 u32 words
  * With L = 4a + t (a in 0..7, t in 0..3), j in 0..3 and bit b in 0..31:
- *   K code word 4L+j, bit b : token 8j + a,
- *                             channel 16*((b&15)>>1) + 2t + 8*(b&1) + (b>>4)
+ *   K code word 4L+j, bit b : with v = (b + 21) mod 32, n = v mod 4,
+ *                             q = v div 4, i = (4 - q mod 4) mod 4,
+ *                             h = 1 if 1 <= q <= 4 else 0, e = 4j + i:
+ *                             token 8n + a, channel 16*(e>>1) + 8*(e&1) + 2t + h
+ *                             (rotated left by 4i, the word holds token 8n + a's
+ *                             bits for channels 16*(e>>1) + 8*(e&1) + 2t + {0, 1}
+ *                             at bits 11 + n and 27 + n)
  *   K minmax word 32t+m     : channel 16*(m>>2) + 2t + 8*((m>>1)&1) + (m&1)
  *   V code word 4L+j, bit b : token 16*(j>>1) + 8*(j&1) + 2t + (b>>4),
  *                             channel 16*((b&15)>>1) + 8*(b&1) + a

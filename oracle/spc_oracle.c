@@ -168,8 +168,10 @@ int64_t orc_record_bytes(int32_t bits) { return 1024 * (int64_t)(bits + 1); }
  *   V codes  : `bits` planes of 128 u32 words
  *   V minmax : 128 u32 words
  * With L = 4a + t (a in 0..7, t in 0..3), j in 0..3 and bit b in 0..31:
- *   K code word 4L+j, bit b : token 8j + a,
- *                             channel 16*((b&15)>>1) + 2t + 8*(b&1) + (b>>4)
+ *   K code word 4L+j, bit b : with v = (b + 21) mod 32, n = v mod 4,
+ *                             q = v div 4, i = (4 - q mod 4) mod 4,
+ *                             h = 1 if 1 <= q <= 4 else 0, e = 4j + i:
+ *                             token 8n + a, channel 16*(e>>1) + 8*(e&1) + 2t + h
  *   K minmax word 32t+m     : channel 16*(m>>2) + 2t + 8*((m>>1)&1) + (m&1)
  *   V code word 4L+j, bit b : token 16*(j>>1) + 8*(j&1) + 2t + (b>>4),
  *                             channel 16*((b&15)>>1) + 8*(b&1) + a
@@ -207,8 +209,10 @@ void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
             for (int32_t j = 0; j < 4; ++j) {
               uint32_t wk = 0, wv = 0;
               for (int32_t bit = 0; bit < 32; ++bit) {
-                int32_t ktok = 8 * j + a;
-                int32_t kch = 16 * ((bit & 15) >> 1) + 2 * t + 8 * (bit & 1) + (bit >> 4);
+                int32_t kv = (bit + 21) % 32, kq = kv / 4;
+                int32_t ke = 4 * j + (4 - kq % 4) % 4;
+                int32_t ktok = 8 * (kv % 4) + a;
+                int32_t kch = 16 * (ke >> 1) + 8 * (ke & 1) + 2 * t + ((kq >= 1 && kq <= 4) ? 1 : 0);
                 int32_t kcv = kcode[(bh * nq + 32 * g + ktok) * D + kch];
                 wk |= (uint32_t)((kcv >> p) & 1) << bit;
                 int32_t vtok = 16 * (j >> 1) + 8 * (j & 1) + 2 * t + (bit >> 4);
