@@ -240,6 +240,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
 constexpr int kMaxCand = 2048;
 constexpr int kBinShift = 19;                  // bin = key >> 19: 8 exponent and 4 mantissa bits
 constexpr int kBins = 1 << (31 - kBinShift);   // keys are scores >= 0: bit 31 is clear
+constexpr int kTopBytes = kBins / 32;          // values of the key's top byte
+// A key's bin; a key with bit 31 set (only a NaN score could have it) counts
+// in the top bin, as it counts above every other key in the selection.
+__device__ __forceinline__ uint32_t key_bin(uint32_t key) { return min(key >> kBinShift, (uint32_t)kBins - 1u); }
+constexpr int kSmallBin = kTopkThreads / 4;    // bins up to this size are ranked by counting
 
 // two CTAs of 1024 threads per SM (32 registers), so a cluster per (b, hkv) row fits one wave
 __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArgs a) {
@@ -250,9 +255,12 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
   __shared__ uint32_t weq[kTopkMaxSlice / 32];
   __shared__ uint32_t ckey[kMaxCand], cpos[kMaxCand];  // this CTA's candidates, ascending position
   __shared__ SelShared<kTopkThreads> sh;
-  __shared__ uint32_t hist[kBins];  // this CTA's bin counts
+  __shared__ __align__(16) uint32_t hist[kBins];  // this CTA's bin counts
   __shared__ uint32_t s_count;      // candidates kept by this CTA
-  __shared__ uint32_t s_bin[3];     // the k_eff-th largest key's bin, keys at or above it, keys above its top byte
+  __shared__ __align__(16) uint32_t htop[kTopBytes];  // this CTA's counts per top byte
+  __shared__ uint32_t s_tn[2];                         // the leader's threshold and its tie count
+  __shared__ uint32_t s_bin[4];     // the k_eff-th largest key's bin; keys at or above it; keys above its
+                                    // top byte; keys in it
   __shared__ float s_nlse[4];       // -lse * log2(e) of the speculative row of each head of the group
 
   const int tid = threadIdx.x;
@@ -290,23 +298,34 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
     }
     *reinterpret_cast<uint4*>(keys + i) =
         make_uint4(__float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
-    atomicAdd(&hist[__float_as_uint(sc.x) >> kBinShift], 1u);  // this slice's bin counts
-    atomicAdd(&hist[__float_as_uint(sc.y) >> kBinShift], 1u);
-    atomicAdd(&hist[__float_as_uint(sc.z) >> kBinShift], 1u);
-    atomicAdd(&hist[__float_as_uint(sc.w) >> kBinShift], 1u);
+    atomicAdd(&hist[key_bin(__float_as_uint(sc.x))], 1u);  // this slice's bin counts
+    atomicAdd(&hist[key_bin(__float_as_uint(sc.y))], 1u);
+    atomicAdd(&hist[key_bin(__float_as_uint(sc.z))], 1u);
+    atomicAdd(&hist[key_bin(__float_as_uint(sc.w))], 1u);
   }
-  cluster.sync();  // every CTA's keys and bin counts are complete
+  __syncthreads();
+  if (tid < kTopBytes) {  // this slice's count per top byte (32 bins each)
+    const uint4* h4 = reinterpret_cast<const uint4*>(hist + 32 * tid);
+    uint32_t t = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 h = h4[j];
+      t += h.x + h.y + h.z + h.w;
+    }
+    htop[tid] = t;
+  }
+  cluster.sync();  // every CTA's keys, bin and top-byte counts are complete
 
-  // ---- the row's bin counts (the sum over the cluster) and the bin of the k_eff-th largest key ----
+  // ---- the bin of the k_eff-th largest key of the row (counts summed over the cluster), in warp 0:
+  // first its top byte from the per-byte counts, then the bin among that byte's 32 ----
   const int lane = tid & 31, warp = tid >> 5;
-  if (a.keff > 0) {
-    // thread t owns bins 4t .. 4t+3
-    static_assert(kBins == 4 * kTopkThreads, "four bins per thread");
-    uint32_t c[4] = {0u, 0u, 0u, 0u};
+  if (a.keff > 0 && warp == 0) {
+    const uint32_t keff = (uint32_t)a.keff;
+    uint32_t c[4] = {0u, 0u, 0u, 0u};  // lane l: top bytes 4l .. 4l+3
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       if (r < (int)ncta) {
-        const uint4 h = reinterpret_cast<const uint4*>(cluster.map_shared_rank(hist, (unsigned)r))[tid];
+        const uint4 h = reinterpret_cast<const uint4*>(cluster.map_shared_rank(htop, (unsigned)r))[lane];
         c[0] += h.x;
         c[1] += h.y;
         c[2] += h.z;
@@ -320,35 +339,40 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
       const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, suf, off);
       if (lane + off < 32) suf += v;
     }
-    if (lane == 0) sh.wsum[0][warp] = suf;
-    __syncthreads();
-    if (warp == 0) {  // exclusive suffix sum over the warps
-      const uint32_t wt = sh.wsum[0][lane];
-      uint32_t x = wt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, x, off);
-        if (lane + off < 32) x += v;
-      }
-      sh.wsum[1][lane] = x - wt;
-    }
-    __syncthreads();
-    const uint32_t above0 = sh.wsum[1][warp] + suf - own;  // keys in bins above 4t+3
-    const uint32_t keff = (uint32_t)a.keff;
-    if (above0 < keff && keff <= above0 + own) {
-      uint32_t above = above0;
+    uint32_t above = suf - own;  // keys with a top byte above 4l+3
+    int top = -1;
+    uint32_t above_top = 0u;
+    if (above < keff && keff <= above + own) {
       for (int j = 3; j >= 0; --j) {
         if (above + c[j] >= keff) {
-          s_bin[0] = (uint32_t)(4 * tid + j);
-          s_bin[1] = above + c[j];
+          top = 4 * lane + j;
+          above_top = above;
           break;
         }
         above += c[j];
       }
     }
-    __syncthreads();
-    // keys whose top byte is above that of the bin (bins from 32 (top + 1) up)
-    if (4 * tid + 4 == 32 * (int)((s_bin[0] >> 5) + 1)) s_bin[2] = above0;
+    const int src = __ffs(__ballot_sync(0xFFFFFFFFu, top >= 0)) - 1;
+    top = __shfl_sync(0xFFFFFFFFu, top, src);
+    above_top = __shfl_sync(0xFFFFFFFFu, above_top, src);
+    // lane l: bin 32 top + l
+    uint32_t cb = 0u;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < (int)ncta) cb += cluster.map_shared_rank(hist, (unsigned)r)[32 * top + lane];
+    uint32_t sb = cb;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, sb, off);
+      if (lane + off < 32) sb += v;
+    }
+    const uint32_t ab = above_top + sb - cb;  // keys in bins above 32 top + l
+    if (ab < keff && keff <= ab + cb) {
+      s_bin[0] = (uint32_t)(32 * top + lane);
+      s_bin[1] = ab + cb;
+      s_bin[2] = above_top;
+      s_bin[3] = cb;
+    }
   }
   __syncthreads();
 
@@ -362,6 +386,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
     const int nw = len >> 5, per = (nw + kTopkWarps - 1) / kTopkWarps;
     const int w0 = min(nw, warp * per), w1 = min(nw, w0 + per);
     uint32_t cnt = 0u;
+#pragma unroll 4
     for (int w = w0; w < w1; ++w) {
       const uint32_t bits = __ballot_sync(0xFFFFFFFFu, keys[32 * w + lane] >= lower);
       if (lane == 0) wgt[w] = bits;
@@ -374,6 +399,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
     for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xFFFFFFFFu, off, o);
     if (warp == kTopkWarps - 1 && lane == 0) s_count = off + cnt;
     const uint32_t below = (1u << lane) - 1u;
+#pragma unroll 4
     for (int w = w0; w < w1; ++w) {
       const uint32_t bits = wgt[w];
       if ((bits >> lane) & 1u) {
@@ -430,10 +456,57 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
     int32_t* out = a.idx + bh * a.k;
     if (a.keff > 0) {
       uint32_t T, need;
-      if (filtered)  // the threshold's top byte is the bin's; keys above that byte are all selected
+      if (filtered && s_bin[3] <= (uint32_t)kSmallBin) {
+        // the threshold bin's keys ranked by counting (key desc, position asc):
+        // the (k_eff - keys above the bin)-th is T; need = its rank among equal keys + 1
+        const uint32_t bstar = s_bin[0], r = (uint32_t)a.keff - (s_bin[1] - s_bin[3]);
+        uint32_t* bk = wgt;  // the bin's keys and positions (free here)
+        uint32_t* bp = weq;
+        const int lane = tid & 31;
+        if (tid == 0) sh.sel[0] = 0u;
+        __syncthreads();
+        for (uint32_t i0 = 0; i0 < M; i0 += kTopkThreads) {  // append, one atomic per warp
+          const uint32_t i = i0 + tid;
+          const bool in = i < M && key_bin(mkey[i]) == bstar;
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, in);
+          uint32_t base = 0u;
+          if (lane == 0 && bal != 0u) base = atomicAdd(&sh.sel[0], (uint32_t)__popc(bal));
+          base = __shfl_sync(0xFFFFFFFFu, base, 0);
+          if (in) {
+            const uint32_t u = base + __popc(bal & ((1u << lane) - 1u));
+            bk[u] = mkey[i];
+            bp[u] = mpos[i];
+          }
+        }
+        __syncthreads();
+        // four threads per key: each counts a quarter of the bin, then the four sums
+        const uint32_t nb = sh.sel[0], u = (uint32_t)tid >> 2, part = (uint32_t)tid & 3u;
+        const uint32_t ku = u < nb ? bk[u] : 0u, pu = u < nb ? bp[u] : 0u;
+        uint32_t gt = 0u, eq_before = 0u;
+        if (u < nb) {
+          for (uint32_t v = part; v < nb; v += 4u) {
+            const uint32_t kv = bk[v];
+            gt += kv > ku;
+            eq_before += kv == ku && bp[v] < pu;
+          }
+        }
+        gt += __shfl_xor_sync(0xFFFFFFFFu, gt, 1);
+        gt += __shfl_xor_sync(0xFFFFFFFFu, gt, 2);
+        eq_before += __shfl_xor_sync(0xFFFFFFFFu, eq_before, 1);
+        eq_before += __shfl_xor_sync(0xFFFFFFFFu, eq_before, 2);
+        if (u < nb && part == 0u && gt + eq_before == r - 1u) {
+          s_tn[0] = ku;
+          s_tn[1] = r - gt;  // keys equal to T that are selected
+        }
+        __syncthreads();
+        T = s_tn[0];
+        need = s_tn[1];
+      } else if (filtered && (s_bin[0] >> 5) < (uint32_t)kTopBytes - 1u) {
+        // the threshold's top byte is the bin's; keys above that byte are all selected
         cta_radix_select(mkey, (int)M, (uint32_t)a.keff - s_bin[2], sh, T, need, (int)(s_bin[0] >> 5));
-      else
+      } else {
         cta_radix_select(mkey, (int)M, (uint32_t)a.keff, sh, T, need);
+      }
       ordered_take(mkey, (int)M, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
         const uint32_t p = mpos[i];
         out[r] = (int32_t)p;

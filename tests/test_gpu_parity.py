@@ -162,13 +162,18 @@ def test_merged_attention_with_fetch_job(cfg):
 
 def test_topk_selection_exact_with_ties_across_cluster():
     """Selection alone, on logits whose order is unambiguous in fp32 (spacing
-    0.01 in the exponent), with many exact ties, over rows spanning 1..8 CTAs."""
+    0.01 or 0.001 in the exponent), with many exact ties, over rows spanning
+    1..8 CTAs.  The cases reach every way the threshold is found: a threshold
+    bin of at most 256 keys ranked by counting (4224 and 16512 tokens), larger
+    bins by radix select, more candidates than the two-level path keeps, and
+    k above its limit."""
     import bit_kv_cache_spc_gb300 as spc
     rng = np.random.default_rng(0)
-    for N, k in [(4224, 41), (40128, 401), (130944 + 128, 1311), (65536 + 128, 5000)]:
+    for N, k, levels, step in [(4224, 41, 300, 0.01), (16512, 163, 3000, 0.001), (40128, 401, 300, 0.01),
+                               (130944 + 128, 1311, 300, 0.01), (65536 + 128, 5000, 300, 0.01)]:
         d = spc.Dims(2, 2, 2, N, 128, 1)
         nq = spc.spc_num_quantized(d)
-        lg = (rng.integers(0, 300, size=(2, 2, 1, nq)) * 0.01).astype(np.float32)
+        lg = (rng.integers(0, levels, size=(2, 2, 1, nq)) * step).astype(np.float32)
         lse = np.full((2, 2, 2), 3.0, np.float32)
         idx = torch.full((2, 2, k), -7, dtype=torch.int32, device="cuda")
         bm = torch.zeros((2, 2, d.q_groups_cap), dtype=torch.int32, device="cuda")
