@@ -53,6 +53,8 @@ def parse():
                         "(then top-k as its own launch), or 'step': one spc_decode_step launch per layer "
                         "(attention + carried pre-fetch + fused top-k)")
     p.add_argument("--gather-ctas", type=int, default=32, help="grid of the side-stream pre-fetch kernel")
+    p.add_argument("--prefetch-lag", type=int, default=2,
+                   help="overlap placement: layer l's attention carries the pre-fetch of layer l-LAG's selection")
     return p.parse_args()
 
 
@@ -147,7 +149,7 @@ def make_timing_event(torch):
 # ------------------------------------------------------------------ the GPU workload
 
 class DecodeStep:
-    def __init__(self, W, layers, seed=0, mode="fused", gather_ctas=32):
+    def __init__(self, W, layers, seed=0, mode="fused", gather_ctas=32, lag=2):
         import torch
 
         import bit_kv_cache_spc_gb300 as spc
@@ -194,6 +196,7 @@ class DecodeStep:
         self.gathered = [torch.cuda.Event() for _ in range(layers)]
         self.mode = mode
         self.gather_ctas = gather_ctas
+        self.lag = max(1, min(lag, layers))
         self.t0, self.rec = make_timing_event(torch)
         self.attn_ev = [(make_timing_event(torch)[0], make_timing_event(torch)[0]) for _ in range(layers)]
         self.topk_ev = [(make_timing_event(torch)[0], make_timing_event(torch)[0]) for _ in range(layers)]
@@ -221,16 +224,18 @@ class DecodeStep:
 
     def enqueue_overlap(self, timed=False):
         """One decode step on two streams.  Layer l's merged attention (main
-        stream, high priority) carries the pre-fetch of layer l-2's selection,
-        so it does not wait for layer l-1's top-k; that top-k runs on a
-        low-priority stream after layer l-1's attention and fills the SMs the
-        attention leaves idle in its tail.  Layer l's attention waits only for
-        layer l-2's top-k, long done."""
+        stream, high priority) carries the pre-fetch of layer (l - lag)'s
+        selection (lag >= 2), so it does not wait for the top-k of the layers
+        just before it; each top-k runs on a low-priority stream after its
+        layer's attention and fills the SMs the attentions leave idle.  Layer
+        l's attention waits only for layer (l - lag)'s top-k.  Every layer's
+        rows are still fetched before that layer's attention of the next step
+        (the last lag layers' rows ride on the next step's first attentions)."""
         spc, d, k = self.spc, self.d, self.k
-        main, side, L = self.main, self.side_lo, self.L
+        main, side, L, lag = self.main, self.side_lo, self.L, self.lag
         for l in range(L):
-            j = (l - 2) % L
-            if l >= 2:  # layers L-2, L-1 were selected by the previous replay, which has completed
+            j = (l - lag) % L
+            if l >= lag:  # layers L-lag .. L-1 were selected by the previous replay, which has completed
                 main.wait_event(self.selected[j])
             if timed:
                 self.rec(self.attn_ev[l][0], main)
@@ -643,7 +648,7 @@ def main():
         torch.cuda.set_device(0)
     peaks, peak_src = measured_peaks()
 
-    step = DecodeStep(W, args.layers, mode=args.prefetch, gather_ctas=args.gather_ctas)
+    step = DecodeStep(W, args.layers, mode=args.prefetch, gather_ctas=args.gather_ctas, lag=args.prefetch_lag)
     step.capture()
     for _ in range(max(3, args.warmup)):
         step.replay()
