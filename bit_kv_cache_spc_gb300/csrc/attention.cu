@@ -382,7 +382,9 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   const int64_t n_slots = (int64_t)gridDim.x * gridDim.y * kWarps;
   const int64_t slot = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kWarps + warp;
   const int n_pf = (FETCH && a.pf_rows > slot) ? (int)((a.pf_rows - slot + n_slots - 1) / n_slots) : 0;
-  const int pf_every = n_pf > 0 ? max(1, n_my / n_pf) : 1;
+  // At most one carried row per pipeline depth (a warp then waits on at most
+  // one host read at a time); the rows beyond that go after the groups.
+  const int pf_every = n_pf > 0 ? max(kStages, n_my / n_pf) : 1;
   const int pf_carried = n_pf > 0 ? min(n_pf, (n_my + pf_every - 1) / pf_every) : 0;
   int pf_next = n_pf > 0 ? a.pf_idx[slot] : -1;  // position of the next row to issue
   int pf_issue_i = 0, pf_issue_item = 0;          // next carried row on the issue side and its item
@@ -660,15 +662,23 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     __syncwarp();
   }
   cp_async_wait<0>();
-  // pre-fetch rows this warp's groups did not carry
-  for (int i = pf_carried; i < n_pf; ++i) {
-    const int64_t rr = slot + n_slots * i;
-    const int n = a.pf_idx[rr];
-    if (n >= 0 && n < a.pf_ncap) {
-      const int64_t src_row = ((rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
-      reinterpret_cast<uint4*>(a.pf_staging + rr * (2 * kD))[lane] =
-          reinterpret_cast<const uint4*>(a.pf_host + src_row)[lane];
+  // pre-fetch rows this warp's groups did not carry, four host reads in flight at a time
+  for (int i0 = pf_carried; i0 < n_pf; i0 += 4) {
+    int64_t rr[4];
+    int n[4];
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      rr[u] = slot + n_slots * (i0 + u);
+      n[u] = i0 + u < n_pf ? a.pf_idx[rr[u]] : -1;
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (n[u] >= 0 && n[u] < a.pf_ncap)
+        v[u] = reinterpret_cast<const uint4*>(a.pf_host + ((rr[u] / a.pf_k) * a.pf_ncap + n[u]) * (2 * kD))[lane];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (n[u] >= 0 && n[u] < a.pf_ncap) reinterpret_cast<uint4*>(a.pf_staging + rr[u] * (2 * kD))[lane] = v[u];
   }
   // undo the powers of two of the value-bit expansion, per channel
 #pragma unroll
