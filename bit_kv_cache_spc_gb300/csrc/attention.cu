@@ -13,7 +13,10 @@
 //   * every CTA merges its warps' states and writes one partial (running max,
 //     sum, unnormalised output) per query row to the workspace; the last CTA
 //     of a (b, hkv) to finish (an atomic ticket) merges the partials into the
-//     bf16 output and the log-sum-exp, and re-zeroes the ticket.
+//     bf16 output and the log-sum-exp, and re-zeroes the ticket.  When all
+//     CTAs of a (b, hkv) form one resident thread-block cluster, the partials
+//     stay in shared memory and are merged through distributed shared memory
+//     instead (cluster_combine).
 //
 // Low-bit tile arithmetic.  With k^ = z + s*b (b the code, z and s per key
 // group), the logit of query row q is  sum_c q_c s_c b_c + sum_c q_c z_c.  The

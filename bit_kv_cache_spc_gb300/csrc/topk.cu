@@ -6,7 +6,9 @@
 // One thread-block cluster (up to 8 CTAs) per (b, hkv) row.  Each CTA turns
 // its slice of the row into scores S(n) = sum_h 2^(log2e * (l_h(n) - lse_h))
 // held in shared memory as uint32 bit patterns (S >= 0, so integer order is
-// float order).  The cluster then runs an MSB-first radix select (4 passes of
+// float order).  For k up to 2048 the two-level kernel further down selects
+// from candidates; for larger k (topk_kernel, next) the cluster runs an
+// MSB-first radix select (4 passes of
 // 8 bits) for the k-th largest key, summing the CTAs' histograms through
 // distributed shared memory.  The ordered compaction works one 32-position
 // word at a time: a warp's ballots give the word's bitmap and the in-word
