@@ -71,17 +71,17 @@ _sig = {
     "spc_resid_bytes": (C.c_size_t, [_D]),
     "spc_quantize_kv": (C.c_int, [_D, _P, _P, _P, _P, _P]),
     "spc_attn_workspace_bytes": (C.c_size_t, [_D, C.c_int32]),
-    "spc_decode_attn2": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
-    "spc_merged_attn": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
+    "spc_decode_attn2": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]),
+    "spc_merged_attn": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
     "spc_merged_attn_noalloc": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P]),
-    "spc_merged_attn_fetch": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P,
-                                        C.c_int64, _P, C.c_int32, _P, _P]),
+    "spc_merged_attn_fetch": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t,
+                                        _P, C.c_int64, _P, C.c_int32, _P, _P]),
     "spc_topk_select": (C.c_int, [_D, _P, _P, C.c_int32, _P, _P, _P]),
     "spc_host_gather": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, C.c_int32, _P]),
     "spc_append_kv": (C.c_int, [_D, _P, _P, _P, _P, _P, C.c_int64, _P]),
     "spc_offload_kv": (C.c_int, [_D, _P, _P, _P, C.c_int64, _P]),
     "spc_step_workspace_bytes": (C.c_size_t, [_D, C.c_int32]),
-    "spc_decode_step": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, C.c_int32, _P, _P, _P,
+    "spc_decode_step": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, C.c_int32, _P, _P, _P,
                                   C.c_size_t, _P, C.c_int64, _P, C.c_int32, _P, _P]),
     "spc_read_device_status": (C.c_int, [_P, _D, _P]),
 }
@@ -138,10 +138,11 @@ def spc_step_workspace_bytes(d, k_max=0) -> int:
 
 def spc_decode_step(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, next_k, next_idx,
                     next_bitmap, ws, ws_bytes=None, fetch_host_kv=None, fetch_n_cap=0, fetch_idx=None, fetch_k=0,
-                    fetch_staging=None, stream=None):
+                    fetch_staging=None, stream=None, kv_self=None):
     ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
     _check("spc_decode_step",
-           _lib.spc_decode_step(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(idx), _ptr(bitmap),
+           _lib.spc_decode_step(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(kv_self), _ptr(idx),
+                                _ptr(bitmap),
                                 _ptr(staging), int(k), _ptr(o), _ptr(lse), _ptr(spec_logits), int(next_k),
                                 _ptr(next_idx), _ptr(next_bitmap), _ptr(ws), ws_bytes, _ptr(fetch_host_kv),
                                 int(fetch_n_cap), _ptr(fetch_idx), int(fetch_k), _ptr(fetch_staging),
@@ -158,26 +159,28 @@ def spc_quantize_kv(d, k, v, records, resid, stream=None):
                                                    _stream(stream)))
 
 
-def spc_decode_attn2(d, records, resid, q, o, lse, spec_logits, ws, ws_bytes=None, stream=None):
+def spc_decode_attn2(d, records, resid, q, o, lse, spec_logits, ws, ws_bytes=None, stream=None, kv_self=None):
     ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
-    _check("spc_decode_attn2", _lib.spc_decode_attn2(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(o),
-                                                     _ptr(lse), _ptr(spec_logits), _ptr(ws), ws_bytes,
-                                                     _stream(stream)))
+    _check("spc_decode_attn2", _lib.spc_decode_attn2(C.byref(d), _ptr(records), _ptr(resid), _ptr(q),
+                                                     _ptr(kv_self), _ptr(o), _ptr(lse), _ptr(spec_logits),
+                                                     _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def spc_merged_attn(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes=None,
-                    stream=None):
+                    stream=None, kv_self=None):
     ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
-    _check("spc_merged_attn", _lib.spc_merged_attn(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(idx),
-                                                   _ptr(bitmap), _ptr(staging), int(k), _ptr(o), _ptr(lse),
-                                                   _ptr(spec_logits), _ptr(ws), ws_bytes, _stream(stream)))
+    _check("spc_merged_attn", _lib.spc_merged_attn(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(kv_self),
+                                                   _ptr(idx), _ptr(bitmap), _ptr(staging), int(k), _ptr(o),
+                                                   _ptr(lse), _ptr(spec_logits), _ptr(ws), ws_bytes,
+                                                   _stream(stream)))
 
 
 def spc_merged_attn_fetch(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, fetch_host_kv,
-                          fetch_n_cap, fetch_idx, fetch_k, fetch_staging, ws_bytes=None, stream=None):
+                          fetch_n_cap, fetch_idx, fetch_k, fetch_staging, ws_bytes=None, stream=None, kv_self=None):
     ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
     _check("spc_merged_attn_fetch",
-           _lib.spc_merged_attn_fetch(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(idx), _ptr(bitmap),
+           _lib.spc_merged_attn_fetch(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(kv_self), _ptr(idx),
+                                      _ptr(bitmap),
                                       _ptr(staging), int(k), _ptr(o), _ptr(lse), _ptr(spec_logits), _ptr(ws),
                                       ws_bytes, _ptr(fetch_host_kv), int(fetch_n_cap), _ptr(fetch_idx),
                                       int(fetch_k), _ptr(fetch_staging), _stream(stream)))

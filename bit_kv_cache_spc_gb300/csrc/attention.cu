@@ -74,6 +74,7 @@ struct AttnArgs {
   const uint8_t* records;
   const uint16_t* resid;
   const uint16_t* q;
+  const uint16_t* kv_self;  // [B][Hkv][2][D] bf16 or null: the speculative token's own key and value
   const int32_t* idx;
   const uint32_t* bitmap;
   const uint16_t* staging;
@@ -213,7 +214,11 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
   const int64_t bh = blockIdx.y;
   const int G = a.G;
 
-  const int n_rows = a.r + (MERGED ? a.k : 0);
+  // rows: residual window [0, r), fetched rows [r, r + kk), then the
+  // speculative token's own row (seen by the speculative query rows only)
+  const int kk = MERGED ? a.k : 0;
+  const int j_self = a.kv_self != nullptr ? a.r + kk : -1;
+  const int n_rows = a.r + kk + (a.kv_self != nullptr ? 1 : 0);
   const int n_warps = a.chunks * kWarps;
   const int per_warp = (n_rows + n_warps - 1) / n_warps;
   const int j0 = min(n_rows, (int)(blockIdx.x * kWarps + warp) * per_warp);
@@ -229,7 +234,7 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
   // quantised position of the fetched row of lane (window w0), -1 for the residual window
   auto row_pos = [&](int w0) {
     const int j = w0 + lane;
-    return (lane < min(32, j1 - w0) && j >= a.r) ? a.idx[bh * a.k + (j - a.r)] : -1;
+    return (lane < min(32, j1 - w0) && j >= a.r && j < a.r + kk) ? a.idx[bh * a.k + (j - a.r)] : -1;
   };
   const int pos_first = row_pos(j0);
   fill_query();
@@ -237,15 +242,16 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
   for (int w0 = j0; w0 < j1; w0 += 32) {
     const int nwin = min(32, j1 - w0);
     const int pos = w0 == j0 ? pos_first : row_pos(w0);
-    const bool ok = lane < nwin && (w0 + lane < a.r || (pos >= 0 && pos < a.nq));
+    const bool ok = lane < nwin && (w0 + lane < a.r || w0 + lane == j_self || (pos >= 0 && pos < a.nq));
     const uint32_t valid = __ballot_sync(0xFFFFFFFFu, ok);
     for (int b0 = 0; b0 < nwin; b0 += kRowBatch) {
       const int nb = min(kRowBatch, nwin - b0);
       for (int i = 0; i < nb; ++i) {
         if ((valid >> (b0 + i)) & 1u) {
           const int j = w0 + b0 + i;
-          const uint16_t* row = j < a.r ? a.resid + (bh * a.resid_cap + j) * 2 * kD
-                                        : a.staging + (bh * a.k + (j - a.r)) * 2 * kD;
+          const uint16_t* row = j < a.r        ? a.resid + (bh * a.resid_cap + j) * 2 * kD
+                                : j == j_self ? a.kv_self + bh * 2 * kD
+                                              : a.staging + (bh * a.k + (j - a.r)) * 2 * kD;
           cp_async16(tail + 512 * i + 16 * lane, row + 8 * lane);
         }
       }
@@ -272,7 +278,8 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
           }
           const float v = reduce_scatter16(x, lane);
           const int i = 2 * pp + (lane >> 4);
-          if (i < nb && ((valid >> (b0 + i)) & 1u)) lg[pp] = v;
+          // the speculative token's own row is masked for the output token's rows
+          if (i < nb && ((valid >> (b0 + i)) & 1u) && !(w0 + b0 + i == j_self && rho_l < G)) lg[pp] = v;
         }
         const int pi = __shfl_sync(0xFFFFFFFFu, pos, b0 + 2 * pp + (lane >> 4));
         if (spec_lane && lg[pp] != kNeg && pi >= 0) spec_out[pi] = lg[pp] * CUDART_LN2_F;
@@ -1294,8 +1301,8 @@ static bool select_fits(const spc_dims* d, const AttnPlan& p, int32_t k_sel) {
 }
 
 spc_status launch_attention(const spc_dims* d, const void* records, const uint16_t* resid,
-                            const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
-                            const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
+                            const uint16_t* q, const uint16_t* kv_self, const int32_t* idx,
+                            const uint32_t* bitmap, const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
                             float* spec_logits, void* ws, cudaStream_t stream, const PrefetchJob* pf,
                             const SelectJob* sel, bool* sel_done) {
   const bool fetch = pf != nullptr && pf->host_dev != nullptr && (int64_t)d->B * d->Hkv * pf->k > 0;
@@ -1308,6 +1315,7 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.records = static_cast<const uint8_t*>(records);
   a.resid = resid;
   a.q = q;
+  a.kv_self = kv_self;
   a.idx = idx;
   a.bitmap = bitmap;
   a.staging = staging;

@@ -76,6 +76,6 @@ extern "C" spc_status spc_merged_attn_noalloc(const spc_dims* d, const void* rec
     spc_host::set_cuda_error(e);
     return SPC_ERR_CUDA;
   }
-  return spc_merged_attn(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws,
+  return spc_merged_attn(d, records, resid, q, nullptr, idx, bitmap, staging, k, o, lse, spec_logits, ws,
                          kNoAllocScratchBytes, stream);
 }

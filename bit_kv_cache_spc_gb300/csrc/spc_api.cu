@@ -9,9 +9,9 @@
 namespace spc {
 spc_status launch_quantize(const spc_dims*, const uint16_t*, const uint16_t*, void*, uint16_t*, cudaStream_t);
 size_t attn_workspace_bytes(const spc_dims*, int32_t);
-spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const uint16_t*, const int32_t*,
-                            const uint32_t*, const uint16_t*, int32_t, uint16_t*, float*, float*, void*,
-                            cudaStream_t, const PrefetchJob*, const SelectJob*, bool*);
+spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const uint16_t*, const uint16_t*,
+                            const int32_t*, const uint32_t*, const uint16_t*, int32_t, uint16_t*, float*, float*,
+                            void*, cudaStream_t, const PrefetchJob*, const SelectJob*, bool*);
 size_t step_workspace_bytes(const spc_dims*, int32_t);
 spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t);
 spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
@@ -86,7 +86,7 @@ spc_status mapped_device_pointer(const void* host, const void** dev) {
 }
 
 spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
-                       const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                       const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
                        uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
                        spc_stream stream, const spc::PrefetchJob* pf = nullptr,
                        const spc::SelectJob* sel = nullptr, bool* sel_done = nullptr) {
@@ -96,8 +96,8 @@ spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* r
   if (q == nullptr || o == nullptr || ws == nullptr) return SPC_ERR_INVALID;
   if (nq > 0 && records == nullptr) return SPC_ERR_INVALID;
   if (d->N - nq > 0 && resid == nullptr) return SPC_ERR_INVALID;
-  if (!aligned16(records) || !aligned16(resid) || !aligned16(q) || !aligned16(o) || !aligned16(ws) ||
-      !aligned16(lse) || !aligned16(spec_logits))
+  if (!aligned16(records) || !aligned16(resid) || !aligned16(q) || !aligned16(kv_self) || !aligned16(o) ||
+      !aligned16(ws) || !aligned16(lse) || !aligned16(spec_logits))
     return SPC_ERR_INVALID;
   if (k < 0 || k > (1 << 24)) return SPC_ERR_INVALID;
   if (k > 0) {
@@ -106,7 +106,7 @@ spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* r
   const size_t need = sel != nullptr ? spc::step_workspace_bytes(d, std::max(k, sel->k))
                                      : spc::attn_workspace_bytes(d, k);
   if (ws_bytes < need) return SPC_ERR_WORKSPACE;
-  return spc::launch_attention(d, records, resid, q, k > 0 ? idx : nullptr, k > 0 ? bitmap : nullptr,
+  return spc::launch_attention(d, records, resid, q, kv_self, k > 0 ? idx : nullptr, k > 0 ? bitmap : nullptr,
                                k > 0 ? staging : nullptr, k, o, lse, spec_logits, ws,
                                reinterpret_cast<cudaStream_t>(stream), pf, sel, sel_done);
 }
@@ -219,21 +219,22 @@ size_t spc_attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
 }
 
 spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
-                            uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
-                            spc_stream stream) {
-  return attn_common(d, records, resid, q, nullptr, nullptr, nullptr, 0, o, lse, spec_logits, ws, ws_bytes,
-                     stream);
+                            const uint16_t* kv_self, uint16_t* o, float* lse, float* spec_logits, void* ws,
+                            size_t ws_bytes, spc_stream stream) {
+  return attn_common(d, records, resid, q, kv_self, nullptr, nullptr, nullptr, 0, o, lse, spec_logits, ws,
+                     ws_bytes, stream);
 }
 
 spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
-                           const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
-                           uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
-                           spc_stream stream) {
-  return attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream);
+                           const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap,
+                           const uint16_t* staging, int32_t k, uint16_t* o, float* lse, float* spec_logits,
+                           void* ws, size_t ws_bytes, spc_stream stream) {
+  return attn_common(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes,
+                     stream);
 }
 
 spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const uint16_t* resid,
-                                 const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
+                                 const uint16_t* q, const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap,
                                  const uint16_t* staging, int32_t k, uint16_t* o, float* lse, float* spec_logits,
                                  void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv, int64_t fetch_n_cap,
                                  const int32_t* fetch_idx, int32_t fetch_k, uint16_t* fetch_staging,
@@ -242,15 +243,16 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
   if (st != SPC_OK) return st;
   if (fetch_k < 0 || fetch_k > (1 << 24) || fetch_n_cap < 0) return SPC_ERR_INVALID;
   if (fetch_k == 0)
-    return attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream);
+    return attn_common(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes,
+                       stream);
   if (fetch_host_kv == nullptr || fetch_idx == nullptr || fetch_staging == nullptr) return SPC_ERR_INVALID;
   if (!aligned16(fetch_host_kv) || !aligned16(fetch_staging)) return SPC_ERR_INVALID;
   const void* dev = nullptr;
   st = mapped_device_pointer(fetch_host_kv, &dev);
   if (st != SPC_OK) return st;
   spc::PrefetchJob job{static_cast<const uint16_t*>(dev), fetch_n_cap, fetch_idx, fetch_k, fetch_staging};
-  return attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream,
-                     &job);
+  return attn_common(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes,
+                     stream, &job);
 }
 
 size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max) {
@@ -259,7 +261,7 @@ size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max) {
 }
 
 spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
-                           const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                           const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
                            uint16_t* o, float* lse, float* spec_logits, int32_t next_k, int32_t* next_idx,
                            uint32_t* next_bitmap, void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv,
                            int64_t fetch_n_cap, const int32_t* fetch_idx, int32_t fetch_k,
@@ -285,8 +287,8 @@ spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_
   }
   spc::SelectJob sel{next_idx, next_bitmap, next_k};
   bool fused = false;
-  st = attn_common(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes, stream, pf,
-                   &sel, &fused);
+  st = attn_common(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes,
+                   stream, pf, &sel, &fused);
   if (st != SPC_OK || fused) return st;
   // the selection could not ride on this attention launch: its own launch, right after
   if (d->q_groups_cap == 0 && next_k == 0) return SPC_OK;

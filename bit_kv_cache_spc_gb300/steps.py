@@ -67,7 +67,7 @@ def predecode_layer(d, records, resid, host_kv, n_cap, q1, k1, v1, k, idx, bitma
 
 
 def decode_layer(d, records, resid, host_kv, n_cap, q, k_t, v_t, k, idx, bitmap, staging, next_idx, next_bitmap,
-                 next_staging, o, lse, logits, ws, ws_bytes, stream=None, fetch_stream=None):
+                 next_staging, o, lse, logits, ws, ws_bytes, stream=None, fetch_stream=None, kv_self=None):
     """Algorithm 3 for one layer.  The real token's K/V (k_t, v_t: bf16
     [B][Hkv][D]) first joins the cache and is offloaded (d.N is advanced), so
     both queries see it; q: bf16 [B][2][Hq][D] (the real token, then the
@@ -75,14 +75,16 @@ def decode_layer(d, records, resid, host_kv, n_cap, q, k_t, v_t, k, idx, bitmap,
     step (selected at the previous step); the merged attention substitutes
     them, the speculative row's probabilities select next_idx/next_bitmap,
     and their Pre-fetch into next_staging runs on `fetch_stream`.  The
-    speculative token's own K/V is not part of the cache.  Returns the event
-    that ends the Pre-fetch."""
+    speculative token's own K/V (kv_self: bf16 [B][Hkv][2][D], optional) is
+    seen by the speculative query only and is not part of the cache.  Returns
+    the event that ends the Pre-fetch."""
     stream = torch.cuda.current_stream() if stream is None else stream
     fetch_stream = stream if fetch_stream is None else fetch_stream
     s = stream.cuda_stream
     spc_append_kv(d, k_t, v_t, records, resid, host_kv, n_cap, stream=s)
     d.N += 1
-    spc_merged_attn(d, records, resid, q, idx, bitmap, staging, k, o, lse, logits, ws, ws_bytes, stream=s)
+    spc_merged_attn(d, records, resid, q, idx, bitmap, staging, k, o, lse, logits, ws, ws_bytes, stream=s,
+                    kv_self=kv_self)
     spc_topk_select(d, logits, lse, k, next_idx, next_bitmap, stream=s)
     selected = torch.cuda.Event()
     selected.record(stream)

@@ -31,7 +31,7 @@
 extern "C" {
 #endif
 
-#define SPC_ABI_VERSION 1
+#define SPC_ABI_VERSION 2
 
 /* A cudaStream_t. */
 typedef struct CUstream_st* spc_stream;
@@ -140,8 +140,17 @@ size_t spc_attn_workspace_bytes(const spc_dims* d, int32_t k_max);
  * the pre-decoding attention of Algorithm 2).
  *   q     : bf16 [B][2][Hq][D]; row 0 is the output token T_t, row 1 the
  *           speculative token T'_{t+1}.  Query head h uses KV head h / G.
- *   o     : bf16 [B][2][Hq][D], softmax(scale * q.K^T) V over all N tokens,
- *           keys/values dequantised from C' for n < N_q, residual rows after.
+ *   kv_self : bf16 [B][Hkv][2][D] (per (b, hkv) the key row, then the value
+ *           row) or NULL: the speculative token's own key and value, seen by
+ *           the speculative query only (it follows T_t, so T_t does not see
+ *           it), as one more visible row that is not a cache position (no
+ *           spec_logits entry, never selected; its probability still counts
+ *           in the speculative lse).  Algorithm 3 attends over [K, K_t] with
+ *           the new tokens' rows; the speculative token's row cannot join the
+ *           cache, so it is passed here and dropped after the call.
+ *   o     : bf16 [B][2][Hq][D], softmax(scale * q.K^T) V over all N tokens
+ *           (and the speculative row's own row for q row 1), keys/values
+ *           dequantised from C' for n < N_q, residual rows after.
  *   lse   : fp32 [B][2][Hq] or NULL, natural log of the softmax normaliser.
  *   spec_logits : fp32 [B][Hkv][G][q_groups_cap*32] or NULL: the speculative
  *           token's scaled logits scale*q.k at the quantised positions, the
@@ -150,8 +159,8 @@ size_t spc_attn_workspace_bytes(const spc_dims* d, int32_t k_max);
  *           spc_attn_workspace_bytes(d, 0) bytes (see that function).
  */
 spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16_t* resid,
-                            const uint16_t* q, uint16_t* o, float* lse, float* spec_logits,
-                            void* ws, size_t ws_bytes, spc_stream stream);
+                            const uint16_t* q, const uint16_t* kv_self, uint16_t* o, float* lse,
+                            float* spec_logits, void* ws, size_t ws_bytes, spc_stream stream);
 
 /*
  * Attn([T_t, T'_{t+1}], C' U C_kappa) (page 1 section 3 "Decoding",
@@ -164,7 +173,7 @@ spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16
  * ws holds at least spc_attn_workspace_bytes(d, k) bytes.
  */
 spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_t* resid,
-                           const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
+                           const uint16_t* q, const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap,
                            const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
                            float* spec_logits, void* ws, size_t ws_bytes, spc_stream stream);
 
@@ -182,7 +191,8 @@ spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_
  * fetch_k = 0 is spc_merged_attn.  SPC_ERR_NOT_MAPPED as spc_host_gather.
  */
 spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const uint16_t* resid,
-                                 const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
+                                 const uint16_t* q, const uint16_t* kv_self, const int32_t* idx,
+                                 const uint32_t* bitmap,
                                  const uint16_t* staging, int32_t k, uint16_t* o, float* lse, float* spec_logits,
                                  void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv, int64_t fetch_n_cap,
                                  const int32_t* fetch_idx, int32_t fetch_k, uint16_t* fetch_staging,
@@ -215,7 +225,7 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
  */
 size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max);
 spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
-                           const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                           const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
                            uint16_t* o, float* lse, float* spec_logits, int32_t next_k, int32_t* next_idx,
                            uint32_t* next_bitmap, void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv,
                            int64_t fetch_n_cap, const int32_t* fetch_idx, int32_t fetch_k,
@@ -233,7 +243,8 @@ spc_status spc_read_device_status(void* ws, const spc_dims* d, spc_stream stream
  * no counterpart to this call; it exists for callers that cannot allocate
  * device memory (a plug-in running inside a host that owns the device
  * allocator, or a path where cudaMalloc's implicit synchronisation is not
- * allowed).  Same arguments and results as spc_merged_attn minus ws/ws_bytes:
+ * allowed).  Same arguments and results as spc_merged_attn minus kv_self
+ * (none) and ws/ws_bytes:
  * the workspace is a fixed 8 MiB buffer compiled into the library, which each
  * GPU that uses this call holds until the process exits.  Nothing is
  * allocated.  The first call on a device looks the buffer's address up

@@ -56,7 +56,7 @@ def lib():
         L.orc_record_bytes.argtypes = [C.c_int32]
         L.orc_pack.argtypes = [C.POINTER(orc_dims), P, P, P, P, P, P, C.c_int32, C.c_int32, P, P]
         L.orc_attention.argtypes = [C.POINTER(orc_dims), C.c_int32, P, P, P, P, P, P, P, P,
-                                    C.c_int32, P, P, P]
+                                    C.c_int32, P, P, P, P]
         L.orc_topk.argtypes = [C.POINTER(orc_dims), P, C.c_int32, P, P]
         L.orc_gather.argtypes = [C.POINTER(orc_dims), P, C.c_int64, P, C.c_int32, P]
         L.orc_append.argtypes = [C.POINTER(orc_dims), C.c_int32, C.c_int32, P, P, P, P, P, C.c_int64]
@@ -128,11 +128,15 @@ def pack(d: orc_dims, qz, K, V, q_groups_cap=None, resid_cap=None):
     return rec, res
 
 
-def attention(d: orc_dims, q, qz, K, V, idx=None, mode: int = 0):
-    """fp64 o [B,2,Hq,D], lse [B,2,Hq], S [B,Hkv,N_q] of the two-query attention."""
+def attention(d: orc_dims, q, qz, K, V, idx=None, mode: int = 0, kv_self=None):
+    """fp64 o [B,2,Hq,D], lse [B,2,Hq], S [B,Hkv,N_q] of the two-query attention.
+    kv_self: bf16 bits [B,Hkv,2,D] or None, the speculative token's own key and
+    value row, seen by the speculative query only."""
     q = _c(q, np.uint16)
     K = _c(K, np.uint16)
     V = _c(V, np.uint16)
+    if kv_self is not None:
+        kv_self = _c(kv_self, np.uint16)
     n_q = nq(d)
     k = 0
     if idx is not None:
@@ -142,7 +146,7 @@ def attention(d: orc_dims, q, qz, K, V, idx=None, mode: int = 0):
     lse = np.zeros((d.B, 2, d.Hq), np.float64)
     S = np.zeros((d.B, d.Hkv, n_q), np.float64)
     lib().orc_attention(C.byref(d), mode, _p(q), _p(qz["kcode"]), _p(qz["kmm"]), _p(qz["vcode"]),
-                        _p(qz["vmm"]), _p(K), _p(V), _p(idx), k, _p(o), _p(lse), _p(S))
+                        _p(qz["vmm"]), _p(K), _p(V), _p(idx), k, _p(kv_self), _p(o), _p(lse), _p(S))
     return o, lse, S
 
 

@@ -251,7 +251,7 @@ void orc_attention(const orc_dims* d, int32_t mode, const uint16_t* q,
                    const uint8_t* kcode, const uint16_t* kmm,
                    const uint8_t* vcode, const uint16_t* vmm,
                    const uint16_t* K, const uint16_t* V,
-                   const int32_t* idx, int32_t k,
+                   const int32_t* idx, int32_t k, const uint16_t* kv_self,
                    double* o, double* lse, double* S) {
   const int32_t B = d->B, H = d->Hkv, Hq = d->Hq, N = d->N, D = d->D, nq = orc_nq(d);
   const int32_t G = Hq / H, g_sz = d->group, ng = nq / g_sz, ncg = D / g_sz;
@@ -291,7 +291,11 @@ void orc_attention(const orc_dims* d, int32_t mode, const uint16_t* q,
         const int32_t h = hk * G + gi;
         for (int32_t i = 0; i < 2; ++i) {
           const uint16_t* qv = q + (((int64_t)b * 2 + i) * Hq + h) * D;
-          double mx = -INFINITY;
+          /* The speculative token (i = 1) also sees its own key and value
+           * when they are given: Algorithm 3 attends over [K, K_t], and the
+           * speculative token comes after T_t, so T_t does not see its row. */
+          const uint16_t* self = (kv_self != NULL && i == 1) ? kv_self + bh * 2 * D : NULL;
+          double mx = -INFINITY, lself = -INFINITY;
           for (int32_t n = 0; n < N; ++n) {
             double acc = 0.0;
             for (int32_t c = 0; c < D; ++c)
@@ -299,8 +303,15 @@ void orc_attention(const orc_dims* d, int32_t mode, const uint16_t* q,
             logit[n] = d->scale * acc;
             if (logit[n] > mx) mx = logit[n];
           }
+          if (self != NULL) {
+            double acc = 0.0;
+            for (int32_t c = 0; c < D; ++c) acc += (double)bf16_to_float(qv[c]) * (double)bf16_to_float(self[c]);
+            lself = d->scale * acc;
+            if (lself > mx) mx = lself;
+          }
           double den = 0.0;
           for (int32_t n = 0; n < N; ++n) den += exp(logit[n] - mx);
+          if (self != NULL) den += exp(lself - mx);
           double* ov = o ? o + (((int64_t)b * 2 + i) * Hq + h) * D : NULL;
           if (ov != NULL) {
             for (int32_t c = 0; c < D; ++c) ov[c] = 0.0;
@@ -308,8 +319,13 @@ void orc_attention(const orc_dims* d, int32_t mode, const uint16_t* q,
               double p = exp(logit[n] - mx) / den;
               for (int32_t c = 0; c < D; ++c) ov[c] += p * vr[(int64_t)n * D + c];
             }
+            if (self != NULL) {
+              double p = exp(lself - mx) / den;
+              for (int32_t c = 0; c < D; ++c) ov[c] += p * (double)bf16_to_float(self[D + c]);
+            }
           }
-          if (lse != NULL) lse[((int64_t)b * 2 + i) * Hq + h] = (N > 0) ? mx + log(den) : -INFINITY;
+          if (lse != NULL)
+            lse[((int64_t)b * 2 + i) * Hq + h] = (N > 0 || self != NULL) ? mx + log(den) : -INFINITY;
           /* Reading: the score of position n for ArgTopK is the speculative
            * token's probability summed over the query heads sharing KV head hk. */
           if (S != NULL && i == 1)

@@ -78,15 +78,18 @@ void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
  * unless n is listed in idx[b,hkv,0..k-1] (then the original bf16 row of
  * K, V); positions n >= N_q are the bf16 residual rows of K, V.
  * idx may be NULL (k ignored): that is the plain low-bit attention.
+ * kv_self: bf16 [B,Hkv,2,D] (key row, value row) or NULL: the speculative
+ * token's own row, one more visible row for query row 1 only (Algorithm 3
+ * attends over [K, K_t]; T_t precedes the speculative token).
  * Outputs (fp64): o [B,2,Hq,D], lse [B,2,Hq] (natural log of the softmax
  * normaliser of the scaled logits), S [B,Hkv,N_q]: the speculative token's
- * attention probabilities summed over the G query heads of the KV head.
- * Any output pointer may be NULL. */
+ * attention probabilities (normalised over every row it sees) summed over
+ * the G query heads of the KV head.  Any output pointer may be NULL. */
 void orc_attention(const orc_dims* d, int32_t mode, const uint16_t* q,
                    const uint8_t* kcode, const uint16_t* kmm,
                    const uint8_t* vcode, const uint16_t* vmm,
                    const uint16_t* K, const uint16_t* V,
-                   const int32_t* idx, int32_t k,
+                   const int32_t* idx, int32_t k, const uint16_t* kv_self,
                    double* o, double* lse, double* S);
 
 /* ArgTopK per (b,hkv) over S[b,hkv,0..N_q-1]: the k_eff = min(k,N_q)

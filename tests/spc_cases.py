@@ -116,15 +116,15 @@ class GpuLayer:
         lg = torch.full((B, Hkv, self.G, max(self.Lcap, 1)), float("nan"), dtype=torch.float32, device="cuda")
         return o, lse, lg
 
-    def attn2(self):
+    def attn2(self, kv_self=None):
         o, lse, lg = self.new_out()
-        self.spc.spc_decode_attn2(self.d, self.records, self.resid, self.q, o, lse, lg, self.ws)
+        self.spc.spc_decode_attn2(self.d, self.records, self.resid, self.q, o, lse, lg, self.ws, kv_self=kv_self)
         return o, lse, lg
 
-    def merged(self, idx, bitmap, k):
+    def merged(self, idx, bitmap, k, kv_self=None):
         o, lse, lg = self.new_out()
         self.spc.spc_merged_attn(self.d, self.records, self.resid, self.q, idx, bitmap, self.staging, k, o, lse, lg,
-                                 self.ws)
+                                 self.ws, kv_self=kv_self)
         return o, lse, lg
 
     def topk(self, lg, lse, k):

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(spc):
 
 
 def test_host_side_queries(spc):
-    assert spc.spc_abi_version() == 1
+    assert spc.spc_abi_version() == 2
     d = spc.Dims(1, 32, 8, 32768, 128, 1)
     assert spc.spc_num_quantized(d) == 32640
     assert spc.spc_records_bytes(d) == 8 * 1020 * 2048
@@ -60,6 +60,9 @@ def test_validation_happens_before_any_launch(spc):
     d = spc.Dims(1, 32, 8, 1024, 32, 1)
     with pytest.raises(spc.SpcError) as e:  # misaligned query pointer
         spc.spc_decode_attn2(d, 16, 16, 18, 16, None, None, 16, 1 << 30, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # misaligned self row of the speculative token
+        spc.spc_merged_attn(d, 16, 16, 16, None, None, None, 0, 16, None, None, 16, 1 << 30, stream=0, kv_self=20)
     assert e.value.status == 1
     small_cap = spc.Dims(1, 32, 8, 1024, 32, 1, q_groups_cap=3)
     with pytest.raises(spc.SpcError) as e:

@@ -43,11 +43,16 @@ def prepare(cfg, seed=3):
 
 @pytest.mark.parametrize("cfg", CASES, ids=cid)
 @pytest.mark.parametrize("in_place", [False, True])
-def test_decode_step_equals_separate_calls(cfg, in_place):
+@pytest.mark.parametrize("with_self", [False, True])
+def test_decode_step_equals_separate_calls(cfg, in_place, with_self):
     import bit_kv_cache_spc_gb300 as spc
     g, idx, bm = prepare(cfg)
     k = cfg["k"]
-    ref_o, ref_lse, ref_lg = g.merged(idx, bm, k)
+    ks = None
+    if with_self:  # the speculative token's own key/value row
+        K1, V1 = synth.kv_layer(15, 0, cfg["B"], cfg["Hkv"], 1)
+        ks = torch.from_numpy(np.stack([K1[:, :, 0], V1[:, :, 0]], axis=2).view(np.int16).copy()).cuda()
+    ref_o, ref_lse, ref_lg = g.merged(idx, bm, k, kv_self=ks)
     ref_idx, ref_bm = g.topk(ref_lg, ref_lse, k)
     ws = torch.zeros(spc.spc_step_workspace_bytes(g.d, k), dtype=torch.uint8, device="cuda")
     o, lse, lg = g.new_out()
@@ -62,7 +67,8 @@ def test_decode_step_equals_separate_calls(cfg, in_place):
         if rep == 1 and in_place:
             src_idx.copy_(idx)
             src_bm.copy_(bm)
-        spc.spc_decode_step(g.d, g.records, g.resid, g.q, src_idx, src_bm, g.staging, k, o, lse, lg, k, nidx, nbm, ws)
+        spc.spc_decode_step(g.d, g.records, g.resid, g.q, src_idx, src_bm, g.staging, k, o, lse, lg, k, nidx, nbm, ws,
+                            kv_self=ks)
         torch.cuda.synchronize()
         assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
         assert torch.equal(lg[..., :g.nq], ref_lg[..., :g.nq])

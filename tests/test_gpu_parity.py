@@ -102,6 +102,45 @@ def d_words(g):
     return g.d.q_groups_cap
 
 
+SELF = [SMALL[1], SMALL[2], SMALL[3], SMALL[5], SMALL[6], SMALL[8]]
+
+
+@pytest.mark.parametrize("cfg", SELF, ids=small_id)
+def test_speculative_self_row(cfg):
+    """The speculative token's own key/value row (kv_self): the speculative
+    query sees it and the output token's does not.  attn2, top-k and the
+    merged attention against the oracle with the same row; the speculative
+    logits at cache positions are unchanged by it."""
+    g, d, K, V, q, qz = run_small(cfg, seed=4)
+    B, Hkv, k = cfg["B"], cfg["Hkv"], cfg["k"]
+    K1, V1 = synth.kv_layer(15, 0, B, Hkv, 1)
+    kv_self = np.stack([K1[:, :, 0], V1[:, :, 0]], axis=2)  # [B,Hkv,2,D]
+    ks = torch.from_numpy(kv_self.view(np.int16).copy()).cuda()
+    o0, lse0, lg0 = g.attn2()
+    o1, lse1, lg1 = g.attn2(kv_self=ks)
+    torch.cuda.synchronize()
+    oo, lo, So = oracle.attention(d, q, qz, K, V, kv_self=kv_self)
+    assert out_err(b2f(o1.cpu().numpy()), oo) <= OUT_TOL
+    assert np.max(np.abs(lse1.cpu().numpy() - lo)) <= 1e-3
+    nq = g.nq
+    assert torch.equal(lg1[..., :nq], lg0[..., :nq])
+    assert np.max(np.abs(lse1.cpu().numpy()[:, 1] - lse0.cpu().numpy()[:, 1])) > 0  # the row counts
+    if nq == 0:
+        return
+    idx, bm = g.topk(lg1, lse1, k)
+    io, _ = oracle.topk(d, So, k)
+    idx_np = idx.cpu().numpy()
+    for b in range(B):
+        for h in range(Hkv):
+            check_topk_sets(idx_np[b, h], io[b, h], So[b, h], k)
+    g.gather(idx, k)
+    om, lsem, _ = g.merged(idx.contiguous(), bm.contiguous(), k, kv_self=ks)
+    torch.cuda.synchronize()
+    oom, lom, _ = oracle.attention(d, q, qz, K, V, idx=idx_np, kv_self=kv_self)
+    assert out_err(b2f(om.cpu().numpy()), oom) <= OUT_TOL
+    assert np.max(np.abs(lsem.cpu().numpy() - lom)) <= 1e-3
+
+
 def test_k0_merged_is_attn2_and_all_fetched_is_bf16_attention():
     cfg = dict(B=1, Hq=4, Hkv=1, N=512, R=64, bits=1, k=448)
     g, d, K, V, q, qz = run_small(cfg, seed=3)

@@ -224,6 +224,44 @@ def test_p6_attention_matches_library_on_tiny_inputs(bits, B, Hq, Hkv, N, R, gro
     np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("bits,Hq,Hkv,N,R", [(1, 4, 1, 160, 64), (2, 8, 2, 200, 40)])
+def test_p11_speculative_self_row_is_seen_by_the_speculative_query_only(bits, Hq, Hkv, N, R):
+    """Algorithm 3 attends over [K, K_t] with the new tokens' rows; the
+    speculative token follows T_t, so with its own key/value row given, query
+    row 1 attends over N + 1 rows and row 0 over the N cache rows (torch's
+    fp64 attention with a causal mask), and row 0 is bit-identical to the
+    call without the row."""
+    B = 2
+    d = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=N, R=R, bits=bits)
+    K, V = synth.kv_layer(13, 0, B, Hkv, N)
+    q = synth.queries(13, 0, B, Hq)
+    K1, V1 = synth.kv_layer(14, 0, B, Hkv, 1)
+    kv_self = np.stack([K1[:, :, 0], V1[:, :, 0]], axis=2)  # [B,Hkv,2,D]
+    qz = oracle.quantize(d, K, V)
+    nq = oracle.nq(d)
+    Kd, Vd = dequant_tensors(d, qz)
+    Keff = np.concatenate([Kd, b2f(K)[:, :, nq:], b2f(kv_self)[:, :, None, 0]], axis=2)  # N + 1 rows
+    Veff = np.concatenate([Vd, b2f(V)[:, :, nq:], b2f(kv_self)[:, :, None, 1]], axis=2)
+    G = Hq // Hkv
+    qh = torch.from_numpy(b2f(q)).permute(0, 2, 1, 3)  # [B,Hq,2,D]
+    Kt = torch.from_numpy(Keff).repeat_interleave(G, dim=1)
+    Vt = torch.from_numpy(Veff).repeat_interleave(G, dim=1)
+    mask = torch.ones((2, N + 1), dtype=torch.bool)
+    mask[0, N] = False  # T_t does not see the speculative token's row
+    o_ref = torch.nn.functional.scaled_dot_product_attention(qh, Kt, Vt, attn_mask=mask, scale=d.scale)
+    logits = (torch.einsum("bhid,bhnd->bhin", qh, Kt) * d.scale).masked_fill(~mask, float("-inf"))
+    lse_ref = torch.logsumexp(logits, dim=-1).permute(0, 2, 1).numpy()
+    p_ref = torch.softmax(logits, dim=-1).numpy()
+    o, lse, S = oracle.attention(d, q, qz, K, V, kv_self=kv_self)
+    np.testing.assert_allclose(o, o_ref.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+    S_ref = p_ref[:, :, 1, :nq].reshape(B, Hkv, G, nq).sum(axis=2)
+    np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-13)
+    o0, lse0, S0 = oracle.attention(d, q, qz, K, V)
+    assert np.array_equal(o[:, 0], o0[:, 0]) and np.array_equal(lse[:, 0], lse0[:, 0])
+    assert np.abs(o[:, 1] - o0[:, 1]).max() > 1e-4 and np.all(S < S0 + 1e-15)  # the row takes probability
+
+
 def test_p4_all_positions_fetched_equals_full_precision_attention():
     """Page 1 section 3: C' U C_kappa replaces the low-bit rows by the 16-bit
     ones, so fetching every position gives plain bf16 attention."""
