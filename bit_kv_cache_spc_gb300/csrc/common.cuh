@@ -67,13 +67,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
-  float2 r;
-  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
-      : "=f"(r.x), "=f"(r.y)
-      : "r"(v));
-  return r;
-}
 
 // Packed binary32 pairs (sm_100+ f32x2 instructions): one issue for two lanes
 // of arithmetic, each rounded like the scalar instruction.
