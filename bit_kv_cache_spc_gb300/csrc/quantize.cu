@@ -321,7 +321,21 @@ static cudaError_t launch_quantize_bits(const QuantArgs& a, cudaStream_t stream)
   static unsigned long long configured = 0ull;
   cudaError_t e = spc_host::ensure_smem_limit(configured, quantize_kernel<BITS, GROUP>, smem);
   if (e != cudaSuccess) return e;
-  const int64_t grid = std::min<int64_t>(a.total_groups, (int64_t)spc_host::sm_count() * 8);
+  // One wave of resident CTAs (the kernel strides over the groups): a second,
+  // partial wave would start only when the first ends.
+  static int resident[64] = {};
+  const int dev = spc_host::current_device();
+  int per_sm = (dev >= 0 && dev < 64) ? __atomic_load_n(&resident[dev], __ATOMIC_ACQUIRE) : 0;
+  if (per_sm <= 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel<BITS, GROUP>, 128, smem) !=
+            cudaSuccess ||
+        per_sm <= 0) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    if (dev >= 0 && dev < 64) __atomic_store_n(&resident[dev], per_sm, __ATOMIC_RELEASE);
+  }
+  const int64_t grid = std::min<int64_t>(a.total_groups, (int64_t)spc_host::sm_count() * per_sm);
   quantize_kernel<BITS, GROUP><<<(unsigned)grid, 128, smem, stream>>>(a);
   return cudaGetLastError();
 }
