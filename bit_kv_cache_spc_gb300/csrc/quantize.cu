@@ -4,14 +4,17 @@
 //
 // One CTA of 128 threads quantises 32-token groups of one (b, hkv) at a time:
 // 8 KB of keys and 8 KB of values in, one 2 KB (1-bit) or 3 KB (2-bit) record
-// out.  The next group's tiles stream in (cp.async, double-buffered) while the
-// current one is coded.  Per group: thread c finds key channel c's min/max and
+// out.  A CTA loads a group's tiles (cp.async) and then codes them; the
+// other resident CTAs of the SM (one wave of them, 21 KB of shared memory
+// each) overlap one another's loads.  Per group: thread c finds key channel c's min/max and
 // parameters; then one warp per key token (and per value token pair) codes a
 // conflict-free 16-byte block per lane, and one ballot per code word yields a
 // packed word: value words in the record's bit order directly (value groups'
 // min/max come from two xor-shuffles inside the same pass), key words token-
 // major, then rotated into the record's order in one pass over the words.
 // The kernel streams HBM: 512 B read and 64/96 B written per token and KV head.
+#include <cstddef>
+
 #include "common.cuh"
 
 namespace spc {
@@ -61,12 +64,14 @@ struct QuantArgs {
   int64_t total_groups;  // B * Hkv * (nq / group): the kernel's units of work
 };
 
+// Shared memory of the quantiser and the append kernel.  The second tile pair
+// is last: the g = 32 quantiser codes one 32-token group at a time and
+// launches without it (more resident CTAs hide the loads instead).
 struct QuantSmem {
-  uint16_t ks[2][kGroup * kD];  // double-buffered tiles, [token][channel]
-  uint16_t vs[2][kGroup * kD];
   float kz[kD], krs[kD], kss[kD];  // per key channel: z, 1/s, s
   uint32_t klohi[kD];
-  uint32_t rec[256 * 3];           // the record being assembled (up to 3 KB)
+  uint32_t rec[256 * 3];             // the record being assembled (up to 3 KB)
+  uint16_t tile[2][2][kGroup * kD];  // [tile][keys, values][token][channel]
 };
 
 // Token pair p of a group (tokens 2p, 2p+1) is where value code words
@@ -253,20 +258,21 @@ __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
         const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(a.v + row0 * kD);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          cp_async16(reinterpret_cast<uint8_t*>(sm.ks[half]) + 16 * (tid + 128 * r), ksrc + 16 * (tid + 128 * r));
-          cp_async16(reinterpret_cast<uint8_t*>(sm.vs[half]) + 16 * (tid + 128 * r), vsrc + 16 * (tid + 128 * r));
+          cp_async16(reinterpret_cast<uint8_t*>(sm.tile[half][0]) + 16 * (tid + 128 * r), ksrc + 16 * (tid + 128 * r));
+          cp_async16(reinterpret_cast<uint8_t*>(sm.tile[half][1]) + 16 * (tid + 128 * r), vsrc + 16 * (tid + 128 * r));
         }
       }
       cp_async_commit();
       cp_async_wait<0>();
       __syncthreads();
       uint8_t* rec = a.records + (bh * a.q_groups_cap + 2 * g) * (int64_t)rb;
-      code_group<BITS, 64>(sm, sm.ks[0], sm.vs[0], sm.ks[1], rec);
-      code_group<BITS, 64>(sm, sm.ks[1], sm.vs[1], sm.ks[0], rec + rb);  // ends with a barrier: tiles free
+      code_group<BITS, 64>(sm, sm.tile[0][0], sm.tile[0][1], sm.tile[1][0], rec);
+      code_group<BITS, 64>(sm, sm.tile[1][0], sm.tile[1][1], sm.tile[0][0], rec + rb);  // ends with a barrier: tiles free
     }
     return;
   }
 
+  // g = 32: one group per iteration, loaded into tile 0 and coded
   auto load = [&](int64_t gi, int buf) {
     if (gi < a.total_groups) {
       const int64_t bh = gi / ng;
@@ -276,23 +282,21 @@ __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
       const uint8_t* vsrc = reinterpret_cast<const uint8_t*>(a.v + row0 * kD);
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        cp_async16(reinterpret_cast<uint8_t*>(sm.ks[buf]) + 16 * (tid + 128 * r), ksrc + 16 * (tid + 128 * r));
-        cp_async16(reinterpret_cast<uint8_t*>(sm.vs[buf]) + 16 * (tid + 128 * r), vsrc + 16 * (tid + 128 * r));
+        cp_async16(reinterpret_cast<uint8_t*>(sm.tile[buf][0]) + 16 * (tid + 128 * r), ksrc + 16 * (tid + 128 * r));
+        cp_async16(reinterpret_cast<uint8_t*>(sm.tile[buf][1]) + 16 * (tid + 128 * r), vsrc + 16 * (tid + 128 * r));
       }
     }
     cp_async_commit();
   };
 
-  int buf = 0;
-  load(blockIdx.x, 0);
-  for (int64_t gi = blockIdx.x; gi < a.total_groups; gi += gridDim.x, buf ^= 1) {
-    load(gi + gridDim.x, buf ^ 1);
-    cp_async_wait<1>();
+  for (int64_t gi = blockIdx.x; gi < a.total_groups; gi += gridDim.x) {
+    const int buf = 0;
+    load(gi, buf);
+    cp_async_wait<0>();
     __syncthreads();
     const int64_t bh = gi / ng;
     const int g = (int)(gi % ng);
-    // the tile buffer is refilled two iterations on
-    code_group<BITS, 32>(sm, sm.ks[buf], sm.vs[buf], nullptr, a.records + (bh * a.q_groups_cap + g) * (int64_t)rb);
+    code_group<BITS, 32>(sm, sm.tile[buf][0], sm.tile[buf][1], nullptr, a.records + (bh * a.q_groups_cap + g) * (int64_t)rb);
   }
   cp_async_wait<0>();
 }
@@ -317,7 +321,8 @@ __global__ void resid_copy_kernel(const uint16_t* k, const uint16_t* v, uint16_t
 
 template <int BITS, int GROUP>
 static cudaError_t launch_quantize_bits(const QuantArgs& a, cudaStream_t stream) {
-  const int smem = (int)sizeof(QuantSmem);
+  // g = 32 uses tile 0 only (see QuantSmem)
+  const int smem = GROUP == 32 ? (int)offsetof(QuantSmem, tile[1]) : (int)sizeof(QuantSmem);
   static unsigned long long configured = 0ull;
   cudaError_t e = spc_host::ensure_smem_limit(configured, quantize_kernel<BITS, GROUP>, smem);
   if (e != cudaSuccess) return e;
@@ -410,14 +415,14 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
   for (int i = tid; i < GROUP * 32; i += 128) {  // window rows 0..g-1 -> [token][channel] tiles of 32 rows
     const int n = i >> 5, q = i & 31, tile = n >> 5, row = n & 31;
     const uint4 v = win[n * 32 + q];
-    if (q < 16) reinterpret_cast<uint4*>(sm.ks[tile] + row * kD)[q] = v;
-    else reinterpret_cast<uint4*>(sm.vs[tile] + row * kD)[q - 16] = v;
+    if (q < 16) reinterpret_cast<uint4*>(sm.tile[tile][0] + row * kD)[q] = v;
+    else reinterpret_cast<uint4*>(sm.tile[tile][1] + row * kD)[q - 16] = v;
   }
   __syncthreads();
   constexpr int rb = 1024 * (BITS + 1);
   uint8_t* rec = a.records + (bh * a.q_groups_cap + a.nq / kGroup) * (int64_t)rb;
-  code_group<BITS, GROUP>(sm, sm.ks[0], sm.vs[0], sm.ks[1], rec);
-  if (GROUP == 64) code_group<BITS, GROUP>(sm, sm.ks[1], sm.vs[1], sm.ks[0], rec + rb);
+  code_group<BITS, GROUP>(sm, sm.tile[0][0], sm.tile[0][1], sm.tile[1][0], rec);
+  if (GROUP == 64) code_group<BITS, GROUP>(sm, sm.tile[1][0], sm.tile[1][1], sm.tile[0][0], rec + rb);
   // rows g .. r move to 0 .. r-g, 32 rows at a time: a chunk's sources lie
   // past every destination written before it, and it is read in full before
   // it is written
