@@ -740,35 +740,44 @@ __device__ __forceinline__ void write_row(const AttnArgs& a, int64_t bh, int rho
   if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
 }
 
+// The CTA's partial from its warps' states: per query row the max over the
+// slots, then the sum and the output at channel c in slot order.  The rows
+// are independent: unrolled, their dependent chains interleave.
+__device__ __forceinline__ void cta_merge_rows(const CtaMerge& sm, int rows, int c, float* dst) {
+#pragma unroll
+  for (int rho = 0; rho < kMaxRows; ++rho) {
+    if (rho < rows) {
+      float M = kNeg;
+#pragma unroll
+      for (int w = 0; w < kSlots; ++w) M = fmaxf(M, sm.m[w][rho]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSlots; ++w) {
+        const float f = fast_exp2(sm.m[w][rho] - M);
+        L += sm.l[w][rho] * f;
+        O += sm.o[w][rho][c] * f;
+      }
+      float* pr = dst + rho * kPartStride;
+      if (c == 0) {
+        pr[0] = M;
+        pr[1] = L;
+      }
+      pr[4 + c] = O;
+    }
+  }
+}
+
 // Returns whether this CTA was the last of its (b, hkv) and so combined the
 // partials.  part_cap: partials that fit in the CTA's dynamic shared memory
 // (which starts with the merge buffer `sm`).
 __device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last, float* s_ml,
-                                                    int part_cap) {
+                                                    float* s_w, int part_cap) {
   __syncthreads();
   const int c = threadIdx.x;  // channel
   const int64_t bh = blockIdx.y;
   const int rows = 2 * a.G;
   const int nparts = a.chunks;
-  float* part = a.part + ((bh * nparts + blockIdx.x) * kMaxRows) * kPartStride;
-  for (int rho = 0; rho < rows; ++rho) {
-    float M = kNeg;
-#pragma unroll
-    for (int w = 0; w < kSlots; ++w) M = fmaxf(M, sm.m[w][rho]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kSlots; ++w) {
-      const float f = fast_exp2(sm.m[w][rho] - M);
-      L += sm.l[w][rho] * f;
-      O += sm.o[w][rho][c] * f;
-    }
-    float* pr = part + rho * kPartStride;
-    if (c == 0) {
-      pr[0] = M;
-      pr[1] = L;
-    }
-    pr[4 + c] = O;
-  }
+  cta_merge_rows(sm, rows, c, a.part + ((bh * nparts + blockIdx.x) * kMaxRows) * kPartStride);
   // last CTA of this (b, hkv) merges every partial
   __threadfence();
   __syncthreads();
@@ -781,29 +790,40 @@ __device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs
     // Every partial's used rows into shared memory (the merge buffer and the
     // stages, free now) with one round of copies, then per query row the
     // arithmetic of the clustered combine in the same order, so that both
-    // give identical results.
+    // give identical results: thread rho finds row rho's max, sum and the
+    // partials' weights (computed once, shared), every thread its channel's
+    // output.
     float* sp = reinterpret_cast<float*>(&sm);
     const int per_part = rows * (kPartStride / 4);  // 16-byte pieces of one partial's used rows
-    for (int i = c; i < nparts * per_part; i += kThreads) {
-      const int p = i / per_part, e = i - p * per_part;
-      cp_async16(sp + (p * kMaxRows * kPartStride) + 4 * e, base + (int64_t)p * kMaxRows * kPartStride + 4 * e);
-    }
+    for (int p = 0; p < nparts; ++p)
+      for (int e = c; e < per_part; e += kThreads)
+        cp_async16(sp + (p * kMaxRows * kPartStride) + 4 * e, base + (int64_t)p * kMaxRows * kPartStride + 4 * e);
     cp_async_commit();
     cp_async_wait<0>();
     __syncthreads();
-    for (int rho = 0; rho < rows; ++rho) {
-      float M = kNeg;
-      for (int p = 0; p < nparts; ++p) M = fmaxf(M, sp[(p * kMaxRows + rho) * kPartStride]);
-      float L = 0.f, O = 0.f;
-#pragma unroll 4
+    if (c < rows) {
+      float M = kNeg, L = 0.f;
+      for (int p = 0; p < nparts; ++p) M = fmaxf(M, sp[(p * kMaxRows + c) * kPartStride]);
       for (int p = 0; p < nparts; ++p) {
-        const float* pr = sp + (p * kMaxRows + rho) * kPartStride;
+        const float* pr = sp + (p * kMaxRows + c) * kPartStride;
         const float f = fast_exp2(pr[0] - M);
         L += pr[1] * f;
-        O += pr[4 + c] * f;
+        s_w[p * kMaxRows + c] = f;
       }
-      write_row(a, bh, rho, M, L, O, c);
+      s_ml[c] = M;
+      s_ml[kMaxRows + c] = L;
     }
+    __syncthreads();
+    float O[kMaxRows];
+#pragma unroll
+    for (int rho = 0; rho < kMaxRows; ++rho) O[rho] = 0.f;
+    for (int p = 0; p < nparts; ++p)
+#pragma unroll
+      for (int rho = 0; rho < kMaxRows; ++rho)
+        if (rho < rows) O[rho] += sp[(p * kMaxRows + rho) * kPartStride + 4 + c] * s_w[p * kMaxRows + rho];
+#pragma unroll
+    for (int rho = 0; rho < kMaxRows; ++rho)
+      if (rho < rows) write_row(a, bh, rho, s_ml[rho], s_ml[kMaxRows + rho], O[rho], c);
     if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
     return true;
   }
@@ -1031,24 +1051,7 @@ __device__ __forceinline__ void cluster_combine(CtaMerge& sm, const AttnArgs& a,
   __syncthreads();
   const int c = threadIdx.x;  // channel
   const int rows = 2 * a.G;
-  for (int rho = 0; rho < rows; ++rho) {
-    float M = kNeg;
-#pragma unroll
-    for (int w = 0; w < kSlots; ++w) M = fmaxf(M, sm.m[w][rho]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kSlots; ++w) {
-      const float f = fast_exp2(sm.m[w][rho] - M);
-      L += sm.l[w][rho] * f;
-      O += sm.o[w][rho][c] * f;
-    }
-    float* pr = cpart + rho * kPartStride;
-    if (c == 0) {
-      pr[0] = M;
-      pr[1] = L;
-    }
-    pr[4 + c] = O;
-  }
+  cta_merge_rows(sm, rows, c, cpart);
   cluster.sync();
   const unsigned n = cluster.num_blocks();
   const int64_t bh = blockIdx.y;
@@ -1075,6 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   static_assert(sizeof(SelShared<kThreads>) <= kMaxRows * kTilePitch * sizeof(float),
                 "the selection's shared state reuses the query tile");
   __shared__ float s_ml[2 * kMaxRows];
+  __shared__ float s_w[kMaxCluster * kMaxRows];  // the combine's partial weights
   __shared__ __align__(16) float s_q[kMaxRows * kTilePitch];
   CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem);
   grid_dependency_sync();  // nothing is read or written before the previous kernel is done
@@ -1101,7 +1105,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
     return;
   }
   constexpr int kPartCap = attn_dyn_bytes<BITS>() / (int)(kMaxRows * kPartStride * sizeof(float));
-  const bool combined = merge_store_combine(merge, a, &s_last, s_ml, kPartCap);
+  static_assert(kPartCap <= kMaxCluster, "the combine's weight table holds kMaxCluster partials");
+  const bool combined = merge_store_combine(merge, a, &s_last, s_ml, s_w, kPartCap);
   if constexpr (TOPK) {
     __syncthreads();  // the query tile and the merge buffer are free from here on
     select_epilogue<BITS>(a, dyn_smem, *reinterpret_cast<SelShared<kThreads>*>(s_q), combined, &s_last, s_ml);
