@@ -730,6 +730,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
 }
 
 // ------------------------------------------------------------ merge + combine
+
 // Output row and log-sum-exp of query row rho of (b, hkv) bh from its merged
 // softmax state (max M, sum L, unnormalised output O at channel c).
 __device__ __forceinline__ void write_row(const AttnArgs& a, int64_t bh, int rho, float M, float L, float O, int c) {
@@ -778,13 +779,18 @@ __device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs
   const int rows = 2 * a.G;
   const int nparts = a.chunks;
   cta_merge_rows(sm, rows, c, a.part + ((bh * nparts + blockIdx.x) * kMaxRows) * kPartStride);
-  // last CTA of this (b, hkv) merges every partial
-  __threadfence();
+  // last CTA of this (b, hkv) merges every partial.  The barrier orders the
+  // CTA's partial before thread 0's fence and ticket (a fence is cumulative
+  // over what the barrier ordered before it); the fence after the ticket and
+  // the second barrier order the last CTA's reads after it.
   __syncthreads();
-  if (c == 0) *s_last = (atomicAdd(&a.tickets[bh], 1u) == (unsigned)(nparts - 1));
+  if (c == 0) {
+    __threadfence();
+    *s_last = (atomicAdd(&a.tickets[bh], 1u) == (unsigned)(nparts - 1));
+    __threadfence();
+  }
   __syncthreads();
   if (!*s_last) return false;
-  __threadfence();
   const float* base = a.part + (bh * nparts * kMaxRows) * kPartStride;
   if (nparts <= part_cap) {
     // Every partial's used rows into shared memory (the merge buffer and the
