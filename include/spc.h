@@ -52,7 +52,7 @@ typedef enum spc_status {
  * query heads share a KV head; this build handles G in {1, 2, 4}.
  * The quantised prefix has N_q = floor(max(N - R, 0) / g) * g tokens and the
  * residual window the last r = N - N_q tokens (KIVI keeps the most recent
- * tokens in 16 bits; page 1 section 4).  Capacities bound the buffers:
+ * tokens in 16 bits; SpeCache page, section 4).  Capacities bound the buffers:
  * N_q / 32 <= q_groups_cap and r <= resid_cap.
  */
 typedef struct spc_dims {
@@ -103,7 +103,7 @@ int32_t spc_num_quantized(const spc_dims* d);
  * of a group repeat its metadata (the codes are the g = 64 codes; the layout
  * is shared with g = 32, which lets every kernel read either).  min/max are the group's
  * exact bf16 extremes (-0.0 stored as +0.0); the zero point and scale are
- * derived from them (page 1 section 3): 1-bit z = (3min+max)/4, s = (max-min)/2;
+ * derived from them (SpeCache page, section 3): 1-bit z = (3min+max)/4, s = (max-min)/2;
  * 2-bit z = min, s = (max-min)/3.  This is 64 (1-bit) or 96 (2-bit) bytes per
  * token and KV head, 1/8 or 3/16 of bf16.
  */
@@ -115,7 +115,7 @@ size_t spc_records_bytes(const spc_dims* d);
 size_t spc_resid_bytes(const spc_dims* d);
 
 /*
- * Quant (page 1 section 3; Algorithm 1, K' = Quant(K), V' = Quant(V)).
+ * Quant (SpeCache page, section 3; Algorithm 1, K' = Quant(K), V' = Quant(V)).
  * k, v: bf16 [B][Hkv][N][D] (device).  Writes records 0 .. N_q/32-1 of every
  * (b,hkv) and residual rows 0 .. r-1.  Codes are
  *   clamp(rint((x - z) / s), 0, 2^bits - 1), code 0 when s == 0,
@@ -136,7 +136,7 @@ size_t spc_attn_workspace_bytes(const spc_dims* d, int32_t k_max);
 
 /*
  * Attn([T_t, T'_{t+1}], C') -- the two-query decode attention over the
- * low-bit copy (page 1 section 3 "Decoding"; with no fetched rows this is also
+ * low-bit copy (SpeCache page, section 3 "Decoding"; with no fetched rows this is also
  * the pre-decoding attention of Algorithm 2).
  *   q     : bf16 [B][2][Hq][D]; row 0 is the output token T_t, row 1 the
  *           speculative token T'_{t+1}.  Query head h uses KV head h / G.
@@ -163,7 +163,7 @@ spc_status spc_decode_attn2(const spc_dims* d, const void* records, const uint16
                             float* spec_logits, void* ws, size_t ws_bytes, spc_stream stream);
 
 /*
- * Attn([T_t, T'_{t+1}], C' U C_kappa) (page 1 section 3 "Decoding",
+ * Attn([T_t, T'_{t+1}], C' U C_kappa) (SpeCache page, section 3 "Decoding",
  * Algorithm 3): as spc_decode_attn2, but at the k positions idx[b][hkv][0..k-1]
  * (ascending, < N_q, -1 entries ignored) both the key and the value are the
  * fetched 16-bit rows staging[b][hkv][j] (bf16 [B][Hkv][k][2][D]) instead of

@@ -11,7 +11,7 @@
  *     1-bit quantisation" (z = (3 min X + max X)/4, s = (max X - min X)/2);
  *   - grouping: keys per channel, values per token (KIVI, as the SemKV page
  *     section 2.1 describes it), group size g = 32 or 64 and a bf16 residual
- *     window (page 1 section 4, software setup; the appendix's LongBench runs
+ *     window (SpeCache page, section 4, software setup; the appendix's LongBench runs
  *     use g = 64);
  *   - attention: O = Attn([T_t, T'_{t+1}], C' U C_kappa) of section 3
  *     ("Decoding") and Algorithm 3, where C' U C_kappa replaces the low-bit rows
@@ -51,7 +51,7 @@ static uint16_t float_to_bf16_exact(float f) {
 int32_t orc_nq(const orc_dims* d) {
   /* Reading: the quantised part is a whole number of g-token groups and the
    * rest (at least R tokens, fewer than R + g) stays in the bf16 residual
-   * window (KIVI keeps a full-precision window of recent tokens, page 1
+   * window (KIVI keeps a full-precision window of recent tokens, SpeCache page,
    * section 4).  N_q = floor((N-R)/g)*g when N >= R. */
   if (d->N <= d->R) return 0;
   return ((d->N - d->R) / d->group) * d->group;

@@ -50,7 +50,7 @@ void orc_quant_params(int32_t bits, int32_t mode, float lo, float hi, float* z, 
 /* Quantisation code of one value: clamp(rint((x-z)/s), 0, 2^bits-1); 0 if s==0. */
 uint8_t orc_quant_code(int32_t bits, float x, float z, float s);
 
-/* Logical quantisation of one layer (page 1 section 3, "Original KIVI" and
+/* Logical quantisation of one layer (SpeCache page, section 3, "Original KIVI" and
  * "Improved 1-bit" formulas).  Inputs K, V: bf16 [B,Hkv,N,D].  Outputs:
  *   kcode u8  [B,Hkv,N_q,D]          kmm u16 [B,Hkv,N_q/32,D,2]  (min,max bf16)
  *   vcode u8  [B,Hkv,N_q,D]          vmm u16 [B,Hkv,N_q,D/32,2]
@@ -72,7 +72,7 @@ void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
               int32_t q_groups_cap, int32_t resid_cap,
               uint8_t* records, uint16_t* resid);
 
-/* Two-query attention over C' U C_kappa (page 1 section 3 decoding, and
+/* Two-query attention over C' U C_kappa (SpeCache page, section 3 decoding, and
  * Algorithm 3).  q: bf16 [B,2,Hq,D] (row 0 the output token T_t, row 1 the
  * speculative token T'_{t+1}).  Position n < N_q uses the dequantised row
  * unless n is listed in idx[b,hkv,0..k-1] (then the original bf16 row of

@@ -22,7 +22,7 @@ Generator definition (both implementations follow it exactly):
   to 2**-63 in probability.
 
 Workload recipe (shapes of the pages' LLaMA-2-7B / LLaMA-3-8B / Mistral-7B
-attention layers, page 1 section 4):
+attention layers, SpeCache page, section 4):
 
 * K, V for layer l: bf16 [B, Hkv, N, D], element (b,h,n,c) is draw number
   ((b*Hkv + h)*N + n)*D + c of streams (seed, TID_K, l) and (seed, TID_V, l).
