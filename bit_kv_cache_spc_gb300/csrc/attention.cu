@@ -67,7 +67,7 @@ template <int BITS>
 __host__ __device__ constexpr int attn_dyn_bytes() {
   return kWarps * (Stages<BITS>::value * (1024 * (BITS + 1) + 16 + 512) + kZsBytes);
 }
-constexpr int kRowBatch = 8;                     // 16-bit rows staged per batch (512 bytes each)
+constexpr int kRowBatch = 16;                    // 16-bit rows staged per batch (512 bytes each)
 constexpr int kTilePitch = kD + 4;               // padded row of a warp's query / output transfer tile
 
 struct AttnArgs {
@@ -194,9 +194,9 @@ __device__ __forceinline__ float reduce_scatter16(const float (&x)[16], int lane
 }
 
 // The residual window and the fetched rows of this warp's range, before its
-// low-bit groups (whose first stages are already in flight).  Rows are staged
-// kRowBatch at a time with cp.async into `tail` (the warp's last stage and z/s
-// table, free until the low-bit loop starts).  fill_query() is the CTA-wide
+// low-bit groups (whose first stage is already in flight).  Rows are staged
+// kRowBatch at a time with cp.async into `tail` (the warp's stages after the
+// first and its z/s table, free until the low-bit loop starts).  fill_query() is the CTA-wide
 // fill of sq (it ends with a barrier); the positions of the warp's first
 // fetched rows are loaded before it, so that both latencies overlap.  Logits: lane = 4 channels x 8 query rows for two rows at a
 // time, then a reduce-scatter leaves lane with row (lane >> 4), query row
@@ -428,9 +428,13 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   // channel 16*kc + 2*t + 8*h + half (registers at 1 bit, else read from sq)
   float m_run, l_run;
   float oacc[8][4];
+  // The first low-bit stage is in flight behind the query fill and the 16-bit
+  // rows, which are staged in the other stages and the z/s table (a warp's
+  // rows then take one round trip); the rest of the pipeline is issued after.
+  issue(0);
+  rows16_prologue<MERGED>(a, sq, stage + STAGE, fill_query, m_run, l_run, oacc);
 #pragma unroll 1
-  for (int s = 0; s < kStages - 1; ++s) issue(s);  // in flight behind the query fill and the 16-bit rows
-  rows16_prologue<MERGED>(a, sq, stage + (kStages - 1) * STAGE, fill_query, m_run, l_run, oacc);
+  for (int s = 1; s < kStages - 1; ++s) issue(s);
   constexpr bool kQvReg = QueryInRegisters<BITS>::value;
   float qv[kQvReg ? 32 : 1];
   if constexpr (kQvReg) {
@@ -1218,9 +1222,10 @@ static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t strea
   static_assert(kClusterPartOffset + kMaxRows * kPartStride * 4 <= kWarps * (Stages<2>::value * 3600 + kZsBytes) &&
                     kClusterPartOffset + kMaxRows * kPartStride * 4 <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
                 "the clustered combine's partial fits behind the merge buffer");
-  static_assert(kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= 2576 + kZsBytes &&
+  static_assert(kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= (Stages<1>::value - 1) * 2576 + kZsBytes &&
+                    kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= (Stages<2>::value - 1) * 3600 + kZsBytes &&
                     kMaxRows * kTilePitch * 4 <= 2576 + kZsBytes,
-                "16-bit row batch and transfer tile fit in a warp's last stage and z/s table");
+                "16-bit row batch and transfer tile fit in a warp's stages after the first and its z/s table");
   auto* fn = attn_kernel<BITS, MERGED, FETCH, TOPK, CLUSTER>;
   static unsigned long long configured = 0ull;  // one per instantiation
   cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
