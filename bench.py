@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-pairs", type=int, default=16, help="(b, kv-head) pairs in the oracle sample")
+    p.add_argument("--oracle-1core", action="store_true",
+                   help="(internal) time the oracle on the two small configurations, one thread, and exit")
     p.add_argument("--prefetch", choices=["side", "fused", "step", "overlap"], default="overlap",
                    help="pre-fetch as a small side-stream kernel, or carried by the next layer's attention "
                         "(then top-k as its own launch), or 'step': one spc_decode_step launch per layer "
@@ -609,6 +611,23 @@ class OracleSample:
 
 # ------------------------------------------------------------------ ranks
 
+SMALL_CONFIGS = {  # the oracle's single-core timing (one layer each)
+    "c1": dict(B=1, Hq=1, Hkv=1, N=1024, R=32, bits=1, k=16, layers=1),
+    "c2": dict(B=1, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328, layers=1),
+}
+
+
+def oracle_single_core():
+    """The oracle's decode work (merged attention, top-k, gather) on the whole
+    of each small configuration, in a child process with one OpenMP thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-1core"], env=env,
+                       capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"exit {r.returncode}"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def max_over_ranks(value_ms, world, device):
     """The slowest rank's time: every rank's value reduced with MAX (one rank: itself)."""
     if world <= 1:
@@ -635,6 +654,16 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     W = dict(WORKLOAD)
     W["layers"] = args.layers
+
+    if args.oracle_1core:
+        out = {}
+        for name, cfg in SMALL_CONFIGS.items():
+            ref = OracleSample(cfg, cfg["B"] * cfg["Hkv"])
+            secs = [ref.run() for _ in range(5)]
+            out[f"{name}_ms_per_layer"] = 1000.0 * statistics.median(secs)
+        out["threads"] = 1
+        print(json.dumps(out))
+        return
 
     if args.impl == "reference":
         if rank != 0:
@@ -768,7 +797,8 @@ def main():
                                 "kind": "oracle",
                                 "sample": f"merged attention + top-k + gather of {ref.P} (b, kv-head) pairs of one "
                                           f"layer, {len(secs)} runs in {sum(secs):.1f} s (median {dt:.3f} s), "
-                                          f"scaled to {W['B'] * W['Hkv']} pairs x {W['layers']} layers"}
+                                          f"scaled to {W['B'] * W['Hkv']} pairs x {W['layers']} layers",
+                                "single_core": oracle_single_core()}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
