@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=32, Hkv=8, D=128, "
                          "N=32768, 1-bit, residual 128, top-1% (k=328)",
                 B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328, layers=32)
-METRIC = "decode attn steps/s at 32K ctx, 1-bit, top-1% (HBM GB/s and % of peak in roofline)"
+METRIC = "decode attn steps/s and HBM GB/s (% of peak) at 32K ctx, 1-bit, top-1%"  # value: steps/s; GB/s: roofline
 # DRAM bytes (read + write) of one merged-attention launch of this workload, from the ncu capture
 # summarised in profiles/attn_kernel_llama3_8b_32k.md (the fused pre-fetch placement); None once the kernel
 # changes after that capture.
