@@ -402,6 +402,45 @@ def test_pack_places_every_bit_exactly_once():
         assert len(seen_k) == len(seen_v) == bits * 11 * 26
 
 
+@pytest.mark.parametrize("bits", [1, 2])
+def test_pack_follows_the_documented_index_rule(bits):
+    """Every bit and metadata word of the packed records, read back with the
+    index rule as the library's header states it (restated here), equals the
+    logical codes and (min, max) of the quantiser."""
+    B, Hkv, N = 1, 1, 64
+    d = oracle.dims(B=B, Hq=1, Hkv=Hkv, N=N, R=0, bits=bits)
+    K, V = synth.kv_layer(21, 0, B, Hkv, N)
+    qz = oracle.quantize(d, K, V)
+    rec, _ = oracle.pack(d, qz, K, V)
+    kcode, vcode, kmm, vmm = qz["kcode"][0, 0], qz["vcode"][0, 0], qz["kmm"][0, 0], qz["vmm"][0, 0]
+    assert kcode.max() > 0 and vcode.max() > 0
+    for g in range(N // 32):
+        w = np.frombuffer(rec[0, 0, g].tobytes(), dtype="<u4")
+        kc, km, vc, vm = w[:128 * bits], w[128 * bits:128 * bits + 128], w[128 * bits + 128:256 * bits + 128], \
+            w[256 * bits + 128:]
+        for p in range(bits):
+            for L in range(32):
+                a, t = L >> 2, L & 3
+                for j in range(4):
+                    kw, vw = int(kc[128 * p + 4 * L + j]), int(vc[128 * p + 4 * L + j])
+                    for b in range(32):
+                        v = (b + 21) % 32
+                        n, q = v % 4, v // 4
+                        i, h = (4 - q % 4) % 4, 1 if 1 <= q <= 4 else 0
+                        e = 4 * j + i
+                        tok, ch = 8 * n + a, 16 * (e >> 1) + 8 * (e & 1) + 2 * t + h
+                        assert (kw >> b) & 1 == (int(kcode[32 * g + tok, ch]) >> p) & 1
+                        tok = 16 * (j >> 1) + 8 * (j & 1) + 2 * t + (b >> 4)
+                        ch = 16 * ((b & 15) >> 1) + 8 * (b & 1) + a
+                        assert (vw >> b) & 1 == (int(vcode[32 * g + tok, ch]) >> p) & 1
+        for t in range(4):
+            for m in range(32):
+                ch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1)
+                assert int(km[32 * t + m]) == int(kmm[g, ch, 0]) | (int(kmm[g, ch, 1]) << 16)
+                tok = 16 * (m >> 4) + 8 * ((m >> 3) & 1) + 2 * t + ((m >> 2) & 1)
+                assert int(vm[32 * t + m]) == int(vmm[32 * g + tok, m & 3, 0]) | (int(vmm[32 * g + tok, m & 3, 1]) << 16)
+
+
 @pytest.mark.parametrize("bits,R,N0,T,group", [(1, 8, 30, 45, 32), (2, 8, 71, 40, 32), (1, 0, 0, 70, 32),
                                                (2, 128, 100, 70, 32), (1, 16, 40, 90, 64), (2, 0, 10, 60, 64)])
 def test_append_one_token_at_a_time_equals_quantising_the_sequence(bits, R, N0, T, group):
