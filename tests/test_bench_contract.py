@@ -1,0 +1,30 @@
+"""The benchmark's reference arm (the oracle timed on the host cores) prints
+the one JSON line the measurement contract asks for, with the same metric and
+workload as the GPU arm, on a tiny sample (one (b, kv-head) pair, one step)."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_the_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "1", "--cpu-pairs", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    sys.path.insert(0, ROOT)
+    import bench
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
+        assert key in line, key
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == "steps/s" and line["higher_is_better"] is True
+    assert line["config"]["workload"] == bench.WORKLOAD["workload"]
+    assert line["steps"] == 1 and line["warmup"] == 1 and line["n_gpus"] == 1
+    assert line["value"] > 0 and abs(line["ms_per_step"] - 1000.0 / line["value"]) < 1e-6 * line["ms_per_step"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["h2d_bytes_per_step"] == 0
