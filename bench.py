@@ -33,10 +33,10 @@ WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=
                          "N=32768, 1-bit, residual 128, top-1% (k=328)",
                 B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328, layers=32)
 METRIC = "decode attn steps/s and HBM GB/s (% of peak) at 32K ctx, 1-bit, top-1%"  # value: steps/s; GB/s: roofline
-# DRAM bytes (read + write) of one merged-attention launch of this workload, from the ncu capture
-# summarised in profiles/attn_kernel_llama3_8b_32k.md (the fused pre-fetch placement); None once the kernel
-# changes after that capture.
-ATTN_TRAFFIC_BYTES = 175020032
+# DRAM bytes (read + write) of one merged-attention launch (attn_kernel) of this workload, from the ncu
+# capture summarised in profiles/attn_kernel_llama3_8b_32k.md (the fused pre-fetch placement); None once the
+# kernel changes after that capture.
+ATTN_TRAFFIC_BYTES = None
 
 
 def parse():
@@ -212,7 +212,11 @@ class DecodeStep:
                 spc.spc_host_gather(d, self.host[l], N, self.idx[l], k, self.staging[l], stream=self.main)
         torch.cuda.synchronize()
         # attention, top-k, and the gather (its own launch, or riding on the next attention)
-        self.launches_per_step = layers * {"side": 3, "fused": 2, "step": 1, "overlap": 2}[mode]
+        attn_f = spc.spc_attn_kernel_count(d, k, k)  # the attention call's kernels, carrying a pre-fetch
+        attn = spc.spc_attn_kernel_count(d, k, 0)
+        step = spc.spc_decode_step_kernel_count(d, k, k, k)
+        self.launches_per_step = layers * {"side": attn + 2, "fused": attn_f + 1, "step": step,
+                                           "overlap": attn_f + 1}[mode]
         self.graph = None
 
     def enqueue(self, timed=False):
@@ -752,11 +756,12 @@ def main():
             "frac": achieved / peaks["hbm_gbs"],
             "traffic": ATTN_TRAFFIC_BYTES if args.prefetch in ("fused", "overlap") else None,
             "traffic_source": "dram read+write of one launch, profiles/attn_kernel_llama3_8b_32k.md",
-            "kernel": {"side": "spc_merged_attn (low-bit scan + 16-bit rows + combine), one layer",
-                       "fused": "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, previous layer's "
-                                "pre-fetch riding along), one layer",
-                       "overlap": "spc_merged_attn_fetch (low-bit scan + 16-bit rows + combine, the pre-fetch of "
-                                  "the layer two before riding along), one layer",
+            "kernel": {"side": "spc_merged_attn (attn_kernel: low-bit scan + 16-bit rows; combine_kernel), "
+                               "one layer",
+                       "fused": "spc_merged_attn_fetch (attn_kernel: low-bit scan + 16-bit rows, previous layer's "
+                                "pre-fetch riding along; combine_kernel), one layer",
+                       "overlap": "spc_merged_attn_fetch (attn_kernel: low-bit scan + 16-bit rows, the pre-fetch "
+                                  "of the layer two before riding along; combine_kernel), one layer",
                        "step": "spc_decode_step (low-bit scan + 16-bit rows + combine + top-k, previous "
                                "layer's pre-fetch riding along), one layer"}[args.prefetch],
             "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,

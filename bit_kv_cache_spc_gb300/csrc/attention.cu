@@ -87,6 +87,7 @@ struct AttnArgs {
   int32_t Hq, Hkv, G, nq, r, q_groups_cap, resid_cap;
   int32_t chunks, groups_per_chunk;
   int32_t Lcap;
+  int32_t ext_combine;  // 1: the CTAs only store their partials; combine_kernel, launched next, merges them
   float qscale;  // softmax scale * log2(e)
   // Pre-fetch riding on this launch (spc_merged_attn_fetch): rows pf_idx of
   // the mapped host cache pf_host go to pf_staging; pf_rows = B*Hkv*pf_k.
@@ -163,6 +164,27 @@ __device__ __forceinline__ void dequant_params(uint32_t mm, float& z, float& s) 
   } else {
     s = (hi - lo) * (1.f / 3.f);
     z = lo;
+  }
+}
+
+// z and s of four groups from their bf16 (min, max) words, two groups per
+// packed instruction (the same roundings as dequant_params).
+template <int BITS>
+__device__ __forceinline__ void dequant_params4(uint4 mm, float4& z, float4& s) {
+  const float2 lo01 = make_float2(__uint_as_float(mm.x << 16), __uint_as_float(mm.y << 16));
+  const float2 lo23 = make_float2(__uint_as_float(mm.z << 16), __uint_as_float(mm.w << 16));
+  const float2 hi01 = make_float2(__uint_as_float(mm.x & 0xFFFF0000u), __uint_as_float(mm.y & 0xFFFF0000u));
+  const float2 hi23 = make_float2(__uint_as_float(mm.z & 0xFFFF0000u), __uint_as_float(mm.w & 0xFFFF0000u));
+  constexpr float f = BITS == 1 ? 0.5f : 1.f / 3.f;
+  const float2 s01 = f2_mul(f2_sub(hi01, lo01), make_float2(f, f));
+  const float2 s23 = f2_mul(f2_sub(hi23, lo23), make_float2(f, f));
+  s = make_float4(s01.x, s01.y, s23.x, s23.y);
+  if (BITS == 1) {
+    const float2 z01 = f2_fma(s01, make_float2(0.5f, 0.5f), lo01);
+    const float2 z23 = f2_fma(s23, make_float2(0.5f, 0.5f), lo23);
+    z = make_float4(z01.x, z01.y, z23.x, z23.y);
+  } else {
+    z = make_float4(lo01.x, lo01.y, lo23.x, lo23.y);
   }
 }
 
@@ -471,20 +493,12 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
 
     // ---- z, s of the group's 128 key groups and 128 value groups, 4 + 4 per lane ----
     {
-      const uint4 km = *reinterpret_cast<const uint4*>(R + KMETA + 16 * lane);
-      float4 z, s;
-      dequant_params<BITS>(km.x, z.x, s.x);
-      dequant_params<BITS>(km.y, z.y, s.y);
-      dequant_params<BITS>(km.z, z.z, s.z);
-      dequant_params<BITS>(km.w, z.w, s.w);
       const int zi = kZsPitch * (lane >> 3) + 2 * (lane & 7);
+      float4 z, s;
+      dequant_params4<BITS>(*reinterpret_cast<const uint4*>(R + KMETA + 16 * lane), z, s);
       kzs[zi] = z;  // lane covers key entries 4*lane..4*lane+3 = (t = lane/8, kc = lane%8)
       kzs[zi + 1] = s;
-      const uint4 vm = *reinterpret_cast<const uint4*>(R + VMETA + 16 * lane);
-      dequant_params<BITS>(vm.x, z.x, s.x);
-      dequant_params<BITS>(vm.y, z.y, s.y);
-      dequant_params<BITS>(vm.z, z.z, s.z);
-      dequant_params<BITS>(vm.w, z.w, s.w);
+      dequant_params4<BITS>(*reinterpret_cast<const uint4*>(R + VMETA + 16 * lane), z, s);
       vzs[zi] = z;  // value entries: (t, c16, slot) = (lane/8, (lane/4)%2, lane%4), cg 0..3
       vzs[zi + 1] = s;
     }
@@ -554,12 +568,15 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     }
     if (spec_row) {
       float* dst = spec_out + (int64_t)g * kGroup + 2 * t;
+      if (!MERGED || bm == 0u) {  // uniform: most groups have no fetched token
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const uint32_t mb = MERGED ? (bm >> (8 * nt + 2 * t)) & 3u : 0u;
-        if (mb == 0u) {
-          *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(lg[nt][0] * CUDART_LN2_F, lg[nt][1] * CUDART_LN2_F);
-        } else {
+        for (int nt = 0; nt < 4; ++nt)
+          *reinterpret_cast<float2*>(dst + 8 * nt) =
+              f2_mul(make_float2(lg[nt][0], lg[nt][1]), make_float2(CUDART_LN2_F, CUDART_LN2_F));
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const uint32_t mb = (bm >> (8 * nt + 2 * t)) & 3u;
           if (!(mb & 1u)) dst[8 * nt] = lg[nt][0] * CUDART_LN2_F;
           if (!(mb & 2u)) dst[8 * nt + 1] = lg[nt][1] * CUDART_LN2_F;
         }
@@ -783,6 +800,7 @@ __device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs
   const int rows = 2 * a.G;
   const int nparts = a.chunks;
   cta_merge_rows(sm, rows, c, a.part + ((bh * nparts + blockIdx.x) * kMaxRows) * kPartStride);
+  if (a.ext_combine) return false;  // combine_kernel runs after this grid
   // last CTA of this (b, hkv) merges every partial.  The barrier orders the
   // CTA's partial before thread 0's fence and ticket (a fence is cumulative
   // over what the barrier ordered before it); the fence after the ticket and
@@ -1123,7 +1141,77 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   }
 }
 
+// ------------------------------------------------------------ combine kernel
+// Query row blockIdx.x of (b, hkv) blockIdx.y from the partials that every
+// CTA of the attention grid before it stored, in partial order and with the
+// arithmetic of the in-kernel combines (so every path gives identical
+// results): M = the maximum of the partials' maxima, w_p = 2^(m_p - M), then
+// L = sum of l_p w_p and the output at channel threadIdx.x = sum of o_p w_p,
+// both as sequential multiply-adds over p.  kThreads threads, 2 * chunks
+// floats of dynamic shared memory.
+__global__ void __launch_bounds__(kThreads) combine_kernel(AttnArgs a) {
+  extern __shared__ float s_cw[];  // [nparts] weights (first the maxima), [nparts] sums
+  __shared__ float s_red[kWarps];
+  __shared__ float s_L;
+  grid_dependency_sync();  // the attention grid's partials are complete and visible
+  const int rho = blockIdx.x, c = threadIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int nparts = a.chunks;
+  const float* base = a.part + (bh * nparts * kMaxRows + rho) * kPartStride;
+  constexpr int64_t kStep = (int64_t)kMaxRows * kPartStride;  // from one partial's row to the next's
+  float* s_w = s_cw;
+  float* s_l = s_cw + nparts;
+  float m_loc = kNeg;
+  for (int p = c; p < nparts; p += kThreads) {
+    const float m = __ldcg(base + p * kStep);
+    s_w[p] = m;
+    s_l[p] = __ldcg(base + p * kStep + 1);
+    m_loc = fmaxf(m_loc, m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m_loc = fmaxf(m_loc, __shfl_xor_sync(0xFFFFFFFFu, m_loc, o));
+  if ((c & 31) == 0) s_red[c >> 5] = m_loc;
+  __syncthreads();
+  float M = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) M = fmaxf(M, s_red[w]);
+  for (int p = c; p < nparts; p += kThreads) s_w[p] = fast_exp2(s_w[p] - M);
+  __syncthreads();
+  if (c == 0) {
+    float L = 0.f;
+    for (int p = 0; p < nparts; ++p) L += s_l[p] * s_w[p];
+    s_L = L;
+  }
+  float O = 0.f;  // 16 partials' loads in flight at a time
+  for (int p0 = 0; p0 < nparts; p0 += 16) {
+    float ov[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) ov[u] = p0 + u < nparts ? __ldcg(base + (p0 + u) * kStep + 4 + c) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (p0 + u < nparts) O += ov[u] * s_w[p0 + u];
+  }
+  __syncthreads();
+  write_row(a, bh, rho, M, s_L, O, c);
+}
+
 // ---------------------------------------------------------------- host side
+
+static cudaError_t launch_combine(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * a.G), (unsigned)BH, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 2 * sizeof(float) * (size_t)a.chunks;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+}
+
+
 
 struct AttnPlan {
   int chunks;
@@ -1294,15 +1382,28 @@ static bool cluster_fits(int chunks, int64_t BH) {
   return (int64_t)n >= BH;
 }
 
+// The clustered combine, when every (b, hkv)'s CTAs fit one cluster and all
+// clusters are resident in one wave.
+static bool use_cluster(int bits, bool merged, bool fetch, int chunks, int64_t BH) {
+  if (bits == 1)
+    return merged ? (fetch ? cluster_fits<1, true, true>(chunks, BH) : cluster_fits<1, true, false>(chunks, BH))
+                  : (fetch ? cluster_fits<1, false, true>(chunks, BH) : cluster_fits<1, false, false>(chunks, BH));
+  return merged ? (fetch ? cluster_fits<2, true, true>(chunks, BH) : cluster_fits<2, true, false>(chunks, BH))
+                : (fetch ? cluster_fits<2, false, true>(chunks, BH) : cluster_fits<2, false, false>(chunks, BH));
+}
+
+// The attention launch: with the fused selection (its last CTA per (b, hkv)
+// combines), clustered (the CTAs combine through distributed shared memory),
+// or else followed by combine_kernel (a.ext_combine).
 template <int BITS, bool MERGED, bool TOPK>
-static cudaError_t launch_attn_f(const AttnArgs& a, int64_t BH, cudaStream_t stream, bool fetch) {
-  if (!TOPK) {  // the clustered combine, when every (b, hkv)'s CTAs fit one cluster in one wave
-    if (fetch ? cluster_fits<BITS, MERGED, true>(a.chunks, BH) : cluster_fits<BITS, MERGED, false>(a.chunks, BH))
-      return fetch ? launch_attn<BITS, MERGED, true, false, true>(a, BH, stream)
-                   : launch_attn<BITS, MERGED, false, false, true>(a, BH, stream);
-  }
-  return fetch ? launch_attn<BITS, MERGED, true, TOPK, false>(a, BH, stream)
-               : launch_attn<BITS, MERGED, false, TOPK, false>(a, BH, stream);
+static cudaError_t launch_attn_f(const AttnArgs& a, int64_t BH, cudaStream_t stream, bool fetch, bool clustered) {
+  if (!TOPK && clustered)
+    return fetch ? launch_attn<BITS, MERGED, true, false, true>(a, BH, stream)
+                 : launch_attn<BITS, MERGED, false, false, true>(a, BH, stream);
+  cudaError_t e = fetch ? launch_attn<BITS, MERGED, true, TOPK, false>(a, BH, stream)
+                        : launch_attn<BITS, MERGED, false, TOPK, false>(a, BH, stream);
+  if (e == cudaSuccess && a.ext_combine) e = launch_combine(a, BH, stream);
+  return e;
 }
 
 // The fused selection works in the attention's dynamic shared memory: a
@@ -1368,27 +1469,46 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.sel_k = topk ? sel->k : 0;
   a.sel_keff = topk ? std::min(sel->k, a.nq) : 0;
   a.cand_cap = topk ? cand_cap(d, plan, sel->k) : 0;
+  const bool clustered = !topk && use_cluster(d->bits, merged, fetch, a.chunks, BH);
+  a.ext_combine = !topk && !clustered;
   cudaError_t e;
   if (d->bits == 1) {
     if (topk)
-      e = launch_attn_f<1, true, true>(a, BH, stream, fetch);
+      e = launch_attn_f<1, true, true>(a, BH, stream, fetch, clustered);
     else if (merged)
-      e = launch_attn_f<1, true, false>(a, BH, stream, fetch);
+      e = launch_attn_f<1, true, false>(a, BH, stream, fetch, clustered);
     else
-      e = launch_attn_f<1, false, false>(a, BH, stream, fetch);
+      e = launch_attn_f<1, false, false>(a, BH, stream, fetch, clustered);
   } else {
     if (topk)
-      e = launch_attn_f<2, true, true>(a, BH, stream, fetch);
+      e = launch_attn_f<2, true, true>(a, BH, stream, fetch, clustered);
     else if (merged)
-      e = launch_attn_f<2, true, false>(a, BH, stream, fetch);
+      e = launch_attn_f<2, true, false>(a, BH, stream, fetch, clustered);
     else
-      e = launch_attn_f<2, false, false>(a, BH, stream, fetch);
+      e = launch_attn_f<2, false, false>(a, BH, stream, fetch, clustered);
   }
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);
     return SPC_ERR_CUDA;
   }
   return SPC_OK;
+}
+
+// Kernels that launch_attention enqueues without a fused selection: the
+// attention grid, then combine_kernel unless the CTAs combine in a cluster.
+int attn_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k) {
+  const int64_t BH = (int64_t)d->B * d->Hkv;
+  const bool fetch = BH * fetch_k > 0;
+  const AttnPlan plan = attn_plan(d, fetch);
+  return use_cluster(d->bits, k > 0, fetch, plan.chunks, BH) ? 1 : 2;
+}
+
+// Kernels of one spc_decode_step: one when the selection rides on the
+// attention launch, else the attention's and the separate top-k.
+int step_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k, int32_t next_k) {
+  const bool fetch = (int64_t)d->B * d->Hkv * fetch_k > 0;
+  if (k > 0 && select_fits(d, attn_plan(d, fetch), next_k)) return 1;
+  return attn_kernel_count(d, k, fetch_k) + ((d->q_groups_cap == 0 && next_k == 0) ? 0 : 1);
 }
 
 }  // namespace spc

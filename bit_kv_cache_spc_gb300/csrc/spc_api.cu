@@ -13,6 +13,8 @@ spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const
                             const int32_t*, const uint32_t*, const uint16_t*, int32_t, uint16_t*, float*, float*,
                             void*, cudaStream_t, const PrefetchJob*, const SelectJob*, bool*);
 size_t step_workspace_bytes(const spc_dims*, int32_t);
+int attn_kernel_count(const spc_dims*, int32_t, int32_t);
+int step_kernel_count(const spc_dims*, int32_t, int32_t, int32_t);
 spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t);
 spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
                               int32_t, cudaStream_t);
@@ -253,6 +255,18 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
   spc::PrefetchJob job{static_cast<const uint16_t*>(dev), fetch_n_cap, fetch_idx, fetch_k, fetch_staging};
   return attn_common(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes,
                      stream, &job);
+}
+
+int32_t spc_attn_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k) {
+  if (check_dims(d) != SPC_OK || k < 0 || k > (1 << 24) || fetch_k < 0 || fetch_k > (1 << 24)) return -1;
+  return spc::attn_kernel_count(d, k, fetch_k);
+}
+
+int32_t spc_decode_step_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k, int32_t next_k) {
+  if (check_dims(d) != SPC_OK || k < 0 || k > (1 << 24) || fetch_k < 0 || fetch_k > (1 << 24) || next_k < 0 ||
+      next_k > (1 << 24))
+    return -1;
+  return spc::step_kernel_count(d, k, fetch_k, next_k);
 }
 
 size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max) {

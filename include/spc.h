@@ -199,6 +199,18 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
                                  spc_stream stream);
 
 /*
+ * Kernels that spc_decode_attn2 (k = 0), spc_merged_attn (k > 0) or
+ * spc_merged_attn_fetch (fetch_k > 0) enqueue for this shape on the current
+ * device: 1 when the CTAs of every (b, hkv) form one resident thread-block
+ * cluster and combine their split-K partials through distributed shared
+ * memory, else 2 (the attention grid stores its partials in the workspace and
+ * a second, small kernel merges them).  A host-side query (no launch), for
+ * callers that count launches or plan CUDA graphs.  -1 for an invalid shape
+ * or a negative count.
+ */
+int32_t spc_attn_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k);
+
+/*
  * One decoding step of a layer (SpeCache page, Algorithm 3) in one launch:
  * spc_merged_attn (optionally carrying another layer's Pre-fetch, as
  * spc_merged_attn_fetch) followed by ArgTopK(A_{1,:}), exactly as
@@ -224,6 +236,11 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
  * separately, right after, on the same stream, with the same results.
  */
 size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max);
+/* Kernels one spc_decode_step with these arguments enqueues on the current
+ * device: 1 when the selection rides on the attention launch, else the
+ * attention's (spc_attn_kernel_count) plus the separate top-k.  -1 for an
+ * invalid shape or a negative count. */
+int32_t spc_decode_step_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k, int32_t next_k);
 spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
                            const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
                            uint16_t* o, float* lse, float* spec_logits, int32_t next_k, int32_t* next_idx,

@@ -73,6 +73,19 @@ def test_validation_happens_before_any_launch(spc):
     assert e.value.status == 1
 
 
+def test_kernel_count_queries_refuse_bad_arguments(spc):
+    """The launch-count queries answer -1 for an invalid shape or count (no
+    launch; their positive answers depend on the device and are checked on
+    the GPU)."""
+    bad_bits = spc.Dims(1, 32, 8, 1024, 32, 3)
+    assert spc.spc_attn_kernel_count(bad_bits, 0, 0) == -1
+    assert spc.spc_decode_step_kernel_count(bad_bits, 8, 0, 8) == -1
+    d = spc.Dims(1, 32, 8, 1024, 32, 1)
+    assert spc.spc_attn_kernel_count(d, -1, 0) == -1
+    assert spc.spc_attn_kernel_count(d, 0, -1) == -1
+    assert spc.spc_decode_step_kernel_count(d, 8, 0, -1) == -1
+
+
 def test_append_validation(spc):
     """The append needs room for the new window row and, at a flush, for the
     new record; both are checked before any launch."""

@@ -12,6 +12,7 @@ import torch
 
 import oracle
 import synth
+import bit_kv_cache_spc_gb300 as spc
 from spc_cases import (CONFIGS, OUT_TOL, GpuLayer, b2f, bitmap_from_idx, c5_cases, check_topk_sets, odims,
                        oracle_pair, out_err)
 
@@ -238,6 +239,22 @@ def test_topk_selection_exact_with_ties_across_cluster():
             assert np.array_equal(idx.cpu().numpy()[0, h], want)
             assert np.array_equal(bm.cpu().numpy().view(np.uint32)[0, h],
                                   bitmap_from_idx(want[want >= 0], d.q_groups_cap))
+
+
+def test_kernel_counts_of_the_combine_paths():
+    """Configuration 4 splits each (b, kv-head) over 9 CTAs, more than one wave
+    of resident 9-CTA clusters holds for 64 pairs, so its attention calls are
+    two kernels (the grid, then the combine kernel), and so is batch 1 at 128K
+    (76 CTAs per pair); B*Hkv = 128 at N = 4096 (4 CTAs per pair) combines in
+    clusters, one kernel; spc_decode_step at configuration 4 carries its
+    selection, one kernel."""
+    d4 = spc.Dims(8, 32, 8, 32768, 128, 1)
+    assert spc.spc_attn_kernel_count(d4, 0, 0) == 2
+    assert spc.spc_attn_kernel_count(d4, 328, 328) == 2
+    assert spc.spc_decode_step_kernel_count(d4, 328, 328, 328) == 1
+    assert spc.spc_decode_step_kernel_count(d4, 0, 0, 328) == 3  # no fetched rows: nothing to fuse with
+    assert spc.spc_attn_kernel_count(spc.Dims(1, 32, 8, 131072, 128, 1), 1311, 0) == 2
+    assert spc.spc_attn_kernel_count(spc.Dims(16, 32, 8, 4096, 128, 1), 41, 0) == 1
 
 
 def test_gather_exact_and_unmapped_pointer_refused():
