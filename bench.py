@@ -36,7 +36,7 @@ METRIC = "decode attn steps/s and HBM GB/s (% of peak) at 32K ctx, 1-bit, top-1%
 # DRAM bytes (read + write) of one merged-attention launch (attn_kernel) of this workload, from the ncu
 # capture summarised in profiles/attn_kernel_llama3_8b_32k.md (the fused pre-fetch placement); None once the
 # kernel changes after that capture.
-ATTN_TRAFFIC_BYTES = 173981696
+ATTN_TRAFFIC_BYTES = 174386176
 
 
 def parse():

@@ -397,7 +397,9 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   const bool row_valid = gid < 2 * G;
 
   uint8_t* stage = dyn + (size_t)warp * WARP_BYTES;
-  // per-group z and s: keys [t][kc][z0..3, s0..3], values [t][c16][slot][z cg0..3, s cg0..3],
+  // per-group z and s: keys [t][kc][z0..3, s0..3], values [t][c16][e][z at slot e over cg0..3,
+  // s at channel group e over slot0..3] (the scales transposed so that a B fragment's two tokens
+  // sit side by side),
   // each t block padded by one float4 so that the four t rows read together
   // fall in different banks
   float4* kzs = reinterpret_cast<float4*>(stage + kStages * STAGE);
@@ -500,7 +502,14 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
       kzs[zi + 1] = s;
       dequant_params4<BITS>(*reinterpret_cast<const uint4*>(R + VMETA + 16 * lane), z, s);
       vzs[zi] = z;  // value entries: (t, c16, slot) = (lane/8, (lane/4)%2, lane%4), cg 0..3
-      vzs[zi + 1] = s;
+      {  // scales transposed within the c16 block: entry 4 c16 + cg holds slots 0..3
+        float* st = reinterpret_cast<float*>(vzs + kZsPitch * (lane >> 3) + 2 * (lane & 4) + 1);
+        const int slot = lane & 3;
+        st[slot] = s.x;
+        st[8 + slot] = s.y;
+        st[16 + slot] = s.z;
+        st[24 + slot] = s.w;
+      }
     }
     __syncwarp();
 
@@ -635,7 +644,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
 #pragma unroll
     for (int c16 = 0; c16 < 2; ++c16) {
       const float ps[4] = {p[2 * c16][0], p[2 * c16][1], p[2 * c16 + 1][0], p[2 * c16 + 1][1]};
-      float4 zz[4], ss[4];  // [slot] over cg
+      float4 zz[4], ss[4];  // zz[slot] over cg, ss[cg] over slot
 #pragma unroll
       for (int slot = 0; slot < 4; ++slot) {
         zz[slot] = vzs[kZsPitch * t + 2 * (4 * c16 + slot)];
@@ -648,14 +657,11 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
       {
         const float2 p01 = make_float2(ps[0], ps[1]), p23 = make_float2(ps[2], ps[3]);
         float2 x;
-        x = f2_mul(p01, make_float2(ss[0].x, ss[1].x)); bfr[0][0] = pack_f16x2(x.x, x.y);
-        x = f2_mul(p23, make_float2(ss[2].x, ss[3].x)); bfr[0][1] = pack_f16x2(x.x, x.y);
-        x = f2_mul(p01, make_float2(ss[0].y, ss[1].y)); bfr[1][0] = pack_f16x2(x.x, x.y);
-        x = f2_mul(p23, make_float2(ss[2].y, ss[3].y)); bfr[1][1] = pack_f16x2(x.x, x.y);
-        x = f2_mul(p01, make_float2(ss[0].z, ss[1].z)); bfr[2][0] = pack_f16x2(x.x, x.y);
-        x = f2_mul(p23, make_float2(ss[2].z, ss[3].z)); bfr[2][1] = pack_f16x2(x.x, x.y);
-        x = f2_mul(p01, make_float2(ss[0].w, ss[1].w)); bfr[3][0] = pack_f16x2(x.x, x.y);
-        x = f2_mul(p23, make_float2(ss[2].w, ss[3].w)); bfr[3][1] = pack_f16x2(x.x, x.y);
+#pragma unroll
+        for (int cg = 0; cg < 4; ++cg) {  // ss[cg]: the scales of slots 0..3 at channel group cg
+          x = f2_mul(p01, make_float2(ss[cg].x, ss[cg].y)); bfr[cg][0] = pack_f16x2(x.x, x.y);
+          x = f2_mul(p23, make_float2(ss[cg].z, ss[cg].w)); bfr[cg][1] = pack_f16x2(x.x, x.y);
+        }
       }
       {
         const uint32_t wa = vw[2 * c16], wb = vw[2 * c16 + 1];
