@@ -806,7 +806,11 @@ __device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs
   const int rows = 2 * a.G;
   const int nparts = a.chunks;
   cta_merge_rows(sm, rows, c, a.part + ((bh * nparts + blockIdx.x) * kMaxRows) * kPartStride);
-  if (a.ext_combine) return false;  // combine_kernel runs after this grid
+  // combine_kernel runs after this grid.  A run-time flag on purpose: making
+  // it a template branch (so that the partial-only instantiations lose the
+  // code below) changed the register allocation of the pre-fetching variant
+  // and slowed it by a quarter.
+  if (a.ext_combine) return false;
   // last CTA of this (b, hkv) merges every partial.  The barrier orders the
   // CTA's partial before thread 0's fence and ticket (a fence is cumulative
   // over what the barrier ordered before it); the fence after the ticket and
