@@ -1,10 +1,13 @@
-"""The benchmark's reference arm (the oracle timed on the host cores) prints
-the one JSON line the measurement contract asks for, with the same metric and
-workload as the GPU arm, on a tiny sample (one (b, kv-head) pair, one step)."""
+"""Both arms of the benchmark print the one JSON line the measurement contract
+asks for: the reference arm (the oracle timed on the host cores, on a tiny
+sample: one (b, kv-head) pair, one step) with the same metric and workload as
+the GPU arm, and the GPU arm on a short run."""
 import json
 import os
 import subprocess
 import sys
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -28,3 +31,29 @@ def test_reference_arm_prints_the_contract_line():
     assert line["value"] > 0 and abs(line["ms_per_step"] - 1000.0 / line["value"]) < 1e-6 * line["ms_per_step"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["value"] == line["value"] and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+@pytest.mark.gpu
+def test_gpu_arm_prints_the_contract_line():
+    """The GPU arm on a short run (4 layers, 3 timed steps) prints one JSON line
+    with every key of the measurement contract, its roofline of the dominant
+    call, the end-to-end figure, the clocks and the launch count."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--layers", "4", "--steps", "3",
+                        "--warmup", "3", "--no-cpu-baseline"], capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "clocks", "gpu_launches"):
+        assert key in line, key
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["value"] > 0 and abs(line["ms_per_step"] - 1000.0 / line["value"]) < 1e-6 * line["ms_per_step"]
+    roof = line["roofline"]
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in roof, key
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and 0 < roof["frac"] == roof["achieved"] / roof["peak"]
+    e2e = line["e2e"]
+    assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(line["clocks"])
+    assert line["gpu_launches"] > 0 and line["gpu_launches"] % (3 * 4) == 0  # whole launches per layer and step
