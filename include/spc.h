@@ -127,10 +127,13 @@ spc_status spc_quantize_kv(const spc_dims* d, const uint16_t* k, const uint16_t*
 
 /* Bytes of device workspace spc_decode_attn2 / spc_merged_attn need for this
  * shape on the current device with at most k_max fetched rows per (b, hkv):
- * one ticket word per (b, hkv) followed by the split-K partials.  The caller
- * zero-fills a workspace once after allocating it; every call leaves the
- * ticket words zero again.  Calls that share a workspace must not overlap on
- * the GPU (issue them on one stream, or order them with events).
+ * control words (three per (b, hkv) and a fault word, padded to 256 bytes)
+ * followed by the split-K partials (one per CTA of the attention grid and
+ * query row, merged by the call's second kernel unless the CTAs combine in a
+ * cluster).  The caller zero-fills a workspace once after allocating it;
+ * every call leaves the control words zero again.  Calls that share a
+ * workspace must not overlap on the GPU (issue them on one stream, or order
+ * them with events).
  * Returns 0 for an invalid shape. */
 size_t spc_attn_workspace_bytes(const spc_dims* d, int32_t k_max);
 
