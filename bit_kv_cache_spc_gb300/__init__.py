@@ -31,7 +31,8 @@ if not os.path.exists(lib_path):
 _lib = C.CDLL(lib_path)
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "CUDA error",
-          4: "host pointer is not mapped pinned memory", 5: "workspace too small"}
+          4: "host pointer is not mapped pinned memory", 5: "workspace too small",
+          6: "a kernel's bounded wait ran out"}
 
 
 class SpcError(RuntimeError):
@@ -50,14 +51,17 @@ class spc_dims(C.Structure):
 
 
 def Dims(B, Hq, Hkv, N, R, bits, q_groups_cap=None, resid_cap=None, scale=None, D=128, group=32) -> spc_dims:
-    """Shape of one layer's cache (see spc_dims in include/spc.h)."""
-    nq = ((N - R) // group) * group if N > R else 0
+    """Shape of one layer's cache (see spc_dims in include/spc.h).  The default
+    capacities hold exactly the N_q quantised tokens and the r = N - N_q
+    residual rows that spc_num_quantized reports for the shape."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    probe = spc_dims(B, Hq, Hkv, D, bits, group, N, R, max(N, 0) // 32 + 1, max(N, 0), scale)
+    nq = max(int(_lib.spc_num_quantized(C.byref(probe))), 0)  # -1: an invalid shape, which every call refuses
     if q_groups_cap is None:
         q_groups_cap = nq // 32
     if resid_cap is None:
         resid_cap = N - nq
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
     return spc_dims(B, Hq, Hkv, D, bits, group, N, R, q_groups_cap, resid_cap, scale)
 
 

@@ -15,12 +15,19 @@
 // exits.  All calls share it, so calls that overlap on the GPU (different
 // streams without ordering, or several host threads) race and corrupt each
 // other's results; issue them in order on one stream.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
 
 namespace spc {
 size_t attn_workspace_bytes(const spc_dims*, int32_t);
+}
+namespace spc_host {
+spc_status check_attn_args(const spc_dims*, const void*, const uint16_t*, const uint16_t*, const uint16_t*,
+                           const int32_t*, const uint32_t*, const uint16_t*, int32_t, const uint16_t*, const float*,
+                           const float*);
 }
 
 namespace {
@@ -31,24 +38,68 @@ constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of the buffer on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// The unique id of the calling thread's current CUDA context (ids are never
+// reused within a process), through the driver entry points that the runtime
+// hands out; false when there is no current context or no such entry point.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+    cudaGetLastError();  // a failed query leaves no error behind
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return false;
+  return get_id(c, id) == CUDA_SUCCESS;
+}
+
+// Device address of the buffer in the current context.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress: once per context (the module, and so the buffer, is
+// loaded per context; a context created after a device reset gets a new id
+// and a fresh lookup), or on every call when the context id is unavailable.
 cudaError_t scratch_address(void** out) {
   static std::mutex mu;
-  static void* addr[64] = {};
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = p;
+  struct Entry {
+    unsigned long long ctx;
+    void* addr;
+  };
+  static Entry cache[16] = {};
+  static int n_cached = 0, next_slot = 0;
+  unsigned long long id = 0;
+  bool have_id = current_context_id(&id);
+  if (have_id) {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cached; ++i)
+      if (cache[i].ctx == id) {
+        *out = cache[i].addr;
+        return cudaSuccess;
+      }
   }
-  *out = addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if (!have_id) have_id = current_context_id(&id);  // the lookup made the primary context current
+  if (have_id) {
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next_slot] = Entry{id, p};
+    next_slot = (next_slot + 1) % 16;
+    if (n_cached < 16) ++n_cached;
+  }
+  *out = p;
   return cudaSuccess;
 }
 
@@ -58,9 +109,11 @@ extern "C" spc_status spc_merged_attn_noalloc(const spc_dims* d, const void* rec
                                               const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,
                                               const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
                                               float* spec_logits, spc_stream stream) {
-  const size_t need = spc_attn_workspace_bytes(d, k < 0 ? 0 : k);
-  if (need == 0) return SPC_ERR_INVALID;               // invalid shape
-  if (need > kNoAllocScratchBytes) return SPC_ERR_WORKSPACE;  // beyond the built-in buffer
+  // the statuses spc_merged_attn would return, before anything is enqueued
+  spc_status st = spc_host::check_attn_args(d, records, resid, q, nullptr, idx, bitmap, staging, k, o, lse,
+                                            spec_logits);
+  if (st != SPC_OK) return st;
+  if (spc::attn_workspace_bytes(d, k) > kNoAllocScratchBytes) return SPC_ERR_WORKSPACE;  // beyond the buffer
   void* ws = nullptr;
   cudaError_t e = scratch_address(&ws);
   if (e != cudaSuccess) {

@@ -87,24 +87,45 @@ spc_status mapped_device_pointer(const void* host, const void** dev) {
   return SPC_OK;
 }
 
-spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
-                       const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
-                       uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
-                       spc_stream stream, const spc::PrefetchJob* pf = nullptr,
-                       const spc::SelectJob* sel = nullptr, bool* sel_done = nullptr) {
+}  // namespace
+
+namespace spc_host {
+
+// Argument checks of every attention entry point other than those of its
+// workspace, in the order they apply; nothing is launched or enqueued.
+spc_status check_attn_args(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                           const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap,
+                           const uint16_t* staging, int32_t k, const uint16_t* o, const float* lse,
+                           const float* spec_logits) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
   const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
-  if (q == nullptr || o == nullptr || ws == nullptr) return SPC_ERR_INVALID;
+  if (q == nullptr || o == nullptr) return SPC_ERR_INVALID;
   if (nq > 0 && records == nullptr) return SPC_ERR_INVALID;
   if (d->N - nq > 0 && resid == nullptr) return SPC_ERR_INVALID;
   if (!aligned16(records) || !aligned16(resid) || !aligned16(q) || !aligned16(kv_self) || !aligned16(o) ||
-      !aligned16(ws) || !aligned16(lse) || !aligned16(spec_logits))
+      !aligned16(lse) || !aligned16(spec_logits))
     return SPC_ERR_INVALID;
   if (k < 0 || k > (1 << 24)) return SPC_ERR_INVALID;
   if (k > 0) {
     if (idx == nullptr || bitmap == nullptr || staging == nullptr || !aligned16(staging)) return SPC_ERR_INVALID;
   }
+  return SPC_OK;
+}
+
+}  // namespace spc_host
+
+namespace {
+
+spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                       const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                       uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
+                       spc_stream stream, const spc::PrefetchJob* pf = nullptr,
+                       const spc::SelectJob* sel = nullptr, bool* sel_done = nullptr) {
+  spc_status st = spc_host::check_attn_args(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse,
+                                            spec_logits);
+  if (st != SPC_OK) return st;
+  if (ws == nullptr || !aligned16(ws)) return SPC_ERR_INVALID;
   const size_t need = sel != nullptr ? spc::step_workspace_bytes(d, std::max(k, sel->k))
                                      : spc::attn_workspace_bytes(d, k);
   if (ws_bytes < need) return SPC_ERR_WORKSPACE;

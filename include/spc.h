@@ -267,11 +267,14 @@ spc_status spc_read_device_status(void* ws, const spc_dims* d, spc_stream stream
  * (none) and ws/ws_bytes:
  * the workspace is a fixed 8 MiB buffer compiled into the library, which each
  * GPU that uses this call holds until the process exits.  Nothing is
- * allocated.  The first call on a device looks the buffer's address up
- * (cudaGetSymbolAddress), so make that first call before any stream capture.
- * Shapes whose workspace (spc_attn_workspace_bytes(d, k)) exceeds 8 MiB
- * return SPC_ERR_WORKSPACE.  All calls share the buffer: calls that overlap
- * on the GPU race, so issue them in order on one stream.
+ * allocated.  Argument errors return the statuses spc_merged_attn returns,
+ * before anything is enqueued.  The buffer's device address is looked up
+ * (cudaGetSymbolAddress) on the first call in each CUDA context and kept for
+ * that context (a context made after a device reset gets a fresh lookup), so
+ * make that first call before any stream capture.  Shapes whose workspace
+ * (spc_attn_workspace_bytes(d, k)) exceeds 8 MiB return SPC_ERR_WORKSPACE.
+ * All calls share the buffer: calls that overlap on the GPU race, so issue
+ * them in order on one stream.
  */
 spc_status spc_merged_attn_noalloc(const spc_dims* d, const void* records, const uint16_t* resid,
                                    const uint16_t* q, const int32_t* idx, const uint32_t* bitmap,

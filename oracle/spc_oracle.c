@@ -79,6 +79,10 @@ uint8_t orc_quant_code(int32_t bits, float x, float z, float s) {
    * gets code 0, whose dequantised value z is the group's value. */
   if (s == 0.0f) return 0;
   float t = (x - z) / s;
+  /* Reading: a quotient that is not a number (an infinite x - z over an
+   * infinite s, possible only when the group's range overflows binary32)
+   * has no nearest integer; it gets the lower end of the clamp, code 0. */
+  if (isnan(t)) return 0;
   float c = rintf(t);
   float cmax = (float)((1 << bits) - 1);
   if (c < 0.0f) c = 0.0f;

@@ -138,20 +138,39 @@ class GpuLayer:
         self.spc.spc_host_gather(self.d, self.host, self.cfg["N"], idx, k, self.staging, max_ctas)
 
 
+class PairOracle:
+    """The oracle on one (b, hkv) of a configuration, as a 1 x 1 sub-problem on
+    the same seeded inputs; the pair's K/V, queries and quantisation are made
+    once and shared by every attention call."""
+
+    def __init__(self, cfg, b, hk, K=None, V=None, seed=SEED, layer=0):
+        B, Hq, Hkv, N = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"]
+        G = Hq // Hkv
+        if K is None:
+            k, v = synth.kv_slice(seed, layer, B, Hkv, N, 128, b, hk)
+        else:
+            k, v = K[b, hk], V[b, hk]
+        self.K, self.V = k[None, None], v[None, None]
+        self.q = synth.queries(seed, layer, B, Hq)[b:b + 1, :, hk * G:(hk + 1) * G]
+        self.d = odims(cfg, B=1, Hkv=1, Hq=G)
+        self.qz = oracle.quantize(self.d, self.K, self.V)
+
+    def attention(self, idx=None):
+        """(o [2, G, D], lse [2, G], S [N_q]) with the 16-bit rows at idx (or none)."""
+        o, lse, S = oracle.attention(self.d, self.q, self.qz, self.K, self.V,
+                                     idx=None if idx is None else np.asarray(idx)[None, None])
+        return o[0], lse[0], S[0, 0]
+
+    def topk(self, S, k):
+        io, _ = oracle.topk(self.d, S[None, None], k)
+        return io[0, 0]
+
+
 def oracle_pair(cfg, b, hk, K=None, V=None, idx=None, seed=SEED, layer=0):
     """Oracle outputs of one (b, hkv) of a configuration (a 1 x 1 sub-problem)."""
-    B, Hq, Hkv, N = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"]
-    G = Hq // Hkv
-    if K is None:
-        k, v = synth.kv_slice(seed, layer, B, Hkv, N, 128, b, hk)
-    else:
-        k, v = K[b, hk], V[b, hk]
-    K1, V1 = k[None, None], v[None, None]
-    q = synth.queries(seed, layer, B, Hq)[b:b + 1, :, hk * G:(hk + 1) * G]
-    d = odims(cfg, B=1, Hkv=1, Hq=G)
-    qz = oracle.quantize(d, K1, V1)
-    o, lse, S = oracle.attention(d, q, qz, K1, V1, idx=None if idx is None else idx[None, None])
-    return dict(d=d, K=K1, V=V1, qz=qz, o=o[0], lse=lse[0], S=S[0, 0])
+    p = PairOracle(cfg, b, hk, K=K, V=V, seed=seed, layer=layer)
+    o, lse, S = p.attention(idx)
+    return dict(d=p.d, K=p.K, V=p.V, qz=p.qz, o=o, lse=lse, S=S)
 
 
 def check_topk_sets(idx_gpu, idx_orc, S_orc, k):

@@ -504,3 +504,33 @@ def test_g64_equals_g32_when_both_halves_of_every_group_span_the_same_range(bits
         d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N, R=0, bits=bits, group=group)
         out.append(oracle.pack(d, oracle.quantize(d, K2, V2), K2, V2)[0])
     assert not np.array_equal(out[0], out[1])
+
+
+def test_binary32_edge_readings():
+    """Groups at the edges of binary32, worked by hand from IEEE-754 rules:
+    subnormal ranges quantise like any other; 3 min + max overflowing makes
+    z = +inf (every code 0) or -inf (every code the top code); max - min
+    overflowing makes s = +inf, so a finite x - z gives the quotient 0 and an
+    infinite one no number, which takes code 0 (the reading for a quotient
+    that is not a number)."""
+    big = float(b2f(0x7F7F))          # largest finite bf16
+    big1 = float(b2f(0x7F7E))         # the next one down
+    sub = float(b2f(0x0001))          # smallest bf16 subnormal, 2^-133
+    # lo = 0, hi = 2^-133: s = 2^-134, z = 2^-135; quotients -1/2 and 3/2
+    codes, _, lo, hi = quantize_key_group(1, [0.0, sub, 0.0, sub])
+    assert (lo, hi) == (0.0, sub) and list(codes) == [0, 1, 0, 1]
+    # 2-bit on {0, 2^-133 .. 3 * 2^-133}: s = 2^-133 exactly, codes are the multiples
+    codes, _, _, _ = quantize_key_group(2, [0.0, sub, 2 * sub, 3 * sub])
+    assert list(codes) == [0, 1, 2, 3]
+    for bits in (1, 2):
+        codes, _, _, _ = quantize_key_group(bits, [big, big1, big])
+        top = 0 if bits == 1 else 3  # 2-bit: z = min, nothing overflows, max gets the top code
+        assert list(codes) == [top, 0, top]
+    codes, _, _, _ = quantize_key_group(1, [-big, -big1, -big])  # z = -inf: x - z = +inf
+    assert list(codes) == [1, 1, 1]
+    codes, _, _, _ = quantize_key_group(1, [-big, big, -big1])    # z = -inf, s = +inf: inf / inf
+    assert list(codes) == [0, 0, 0]
+    codes, _, _, _ = quantize_key_group(2, [-big, big, 0.0])      # s = +inf: 0, inf / inf, finite / inf
+    assert list(codes) == [0, 0, 0]
+    codes, _, _, _ = quantize_key_group(1, [-float(b2f(0x7E80)), big, 1.0])  # z finite, s = +inf
+    assert list(codes) == [0, 0, 0]

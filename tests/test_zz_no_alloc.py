@@ -5,15 +5,16 @@ a host that owns the allocator, or a path that must not synchronise the way
 cudaMalloc can), so spc_merged_attn_noalloc runs the merged attention with a
 workspace built into the library.  This checks it through the C ABI against
 spc_merged_attn with a caller workspace, on two calls in a row (the built-in
-buffer keeps the previous call's contents), and that a shape too large for
-the buffer is refused.  The file is named to be collected last.
+buffer keeps the previous call's contents): both run the same kernels on the
+same workspace layout, so the results must be identical bit for bit.  Also
+that argument errors return spc_merged_attn's statuses and a shape too large
+for the buffer is refused.  The file is named to be collected last.
 """
-import numpy as np
 import pytest
 import torch
 
 import synth
-from spc_cases import OUT_TOL, GpuLayer, b2f, out_err
+from spc_cases import GpuLayer
 
 pytestmark = pytest.mark.gpu
 
@@ -31,10 +32,10 @@ def test_noalloc_matches_workspace_variant_on_two_calls():
         o, lse, lg = g.new_out()
         spc.spc_merged_attn_noalloc(g.d, g.records, g.resid, g.q, idx, bm, g.staging, cfg["k"], o, lse, lg)
         torch.cuda.synchronize()
-        assert out_err(b2f(o.cpu().numpy()), b2f(ref_o.cpu().numpy())) <= OUT_TOL
-        np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=0, atol=1e-5)
         nq = g.nq
-        np.testing.assert_allclose(lg.cpu().numpy()[..., :nq], ref_lg.cpu().numpy()[..., :nq], rtol=0, atol=1e-5)
+        assert torch.equal(o, ref_o)
+        assert torch.equal(lse, ref_lse)
+        assert torch.equal(lg[..., :nq], ref_lg[..., :nq])
 
 
 def test_noalloc_refuses_shapes_beyond_its_buffer():
@@ -44,3 +45,11 @@ def test_noalloc_refuses_shapes_beyond_its_buffer():
     with pytest.raises(spc.SpcError) as e:
         spc.spc_merged_attn_noalloc(d, 16, 16, 16, 16, 16, 16, 1, 16, 16, 16)
     assert e.value.status == 5
+    # argument errors come first, with spc_merged_attn's statuses
+    g8 = spc.Dims(1, 64, 8, 1024, 32, 1)  # G = 8: unsupported shape
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_merged_attn_noalloc(g8, 16, 16, 16, 16, 16, 16, 1, 16, 16, 16)
+    assert e.value.status == 2
+    with pytest.raises(spc.SpcError) as e:  # misaligned output
+        spc.spc_merged_attn_noalloc(spc.Dims(1, 4, 1, 1024, 32, 1), 16, 16, 16, 16, 16, 16, 1, 17, 16, 16)
+    assert e.value.status == 1
