@@ -33,10 +33,32 @@ WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=
                          "N=32768, 1-bit, residual 128, top-1% (k=328)",
                 B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328, layers=32)
 METRIC = "decode attn steps/s and HBM GB/s (% of peak) at 32K ctx, 1-bit, top-1%"  # value: steps/s; GB/s: roofline
-# DRAM bytes (read + write) of one merged-attention launch (attn_kernel) of this workload, from the ncu
-# capture summarised in profiles/attn_kernel_llama3_8b_32k.md (the fused pre-fetch placement); None once the
-# kernel changes after that capture.
-ATTN_TRAFFIC_BYTES = 174386176
+# DRAM bytes (read + write) of one merged-attention call of this workload (attn_kernel + combine_kernel, the
+# carried pre-fetch included), from an ncu capture of the attention sources whose digest is recorded beside
+# it; reported as null when the sources compiled now differ from those.
+ATTN_TRAFFIC = {"bytes_per_call": None, "sources_sha256": None}
+ATTN_SOURCES = ("attention.cu", "common.cuh", "select.cuh")
+
+
+def attention_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ATTN_SOURCES:
+        with open(os.path.join(ROOT, "bit_kv_cache_spc_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def attention_traffic():
+    """The captured DRAM traffic of one attention call, if it was taken on the sources built now."""
+    if ATTN_TRAFFIC["sources_sha256"] is not None and ATTN_TRAFFIC["sources_sha256"] == attention_sources_sha256():
+        return ATTN_TRAFFIC["bytes_per_call"]
+    return None
+
+
+def synth_queries(seed, layer, W):
+    import synth
+    return synth.queries(seed, layer, W["B"], W["Hq"])
 
 
 def parse():
@@ -47,7 +69,10 @@ def parse():
     p.add_argument("--impl", choices=["spc", "reference"], default="spc")
     p.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-pairs", type=int, default=16, help="(b, kv-head) pairs in the oracle sample")
+    p.add_argument("--cpu-pairs", type=int, default=0,
+                   help="(b, kv-head) pairs in the oracle sample (0: as many as host cores, at least 16)")
+    p.add_argument("--no-configs", dest="configs", action="store_false",
+                   help="skip the per-configuration points (configurations 1-3 and the 48 of configuration 5)")
     p.add_argument("--oracle-1core", action="store_true",
                    help="(internal) time the oracle on the two small configurations, one thread, and exit")
     p.add_argument("--prefetch", choices=["side", "fused", "step", "overlap"], default="overlap",
@@ -228,7 +253,7 @@ class DecodeStep:
             return self.enqueue_overlap(timed)
         return self.enqueue_side(timed)
 
-    def enqueue_overlap(self, timed=False):
+    def enqueue_overlap(self, timed=False, fetch=True, topk=True):
         """One decode step on two streams.  Layer l's merged attention (main
         stream, high priority) carries the pre-fetch of layer (l - lag)'s
         selection (lag >= 2), so it does not wait for the top-k of the layers
@@ -236,21 +261,31 @@ class DecodeStep:
         layer's attention and fills the SMs the attentions leave idle.  Layer
         l's attention waits only for layer (l - lag)'s top-k.  Every layer's
         rows are still fetched before that layer's attention of the next step
-        (the last lag layers' rows ride on the next step's first attentions)."""
+        (the last lag layers' rows ride on the next step's first attentions).
+        fetch=False: the same step with the staging buffers already filled and
+        no pre-fetch (the overlap test's reference).  topk=False: the merged
+        attentions alone, back to back on one stream (their kernel time)."""
         spc, d, k = self.spc, self.d, self.k
         main, side, L, lag = self.main, self.side_lo, self.L, self.lag
         for l in range(L):
             j = (l - lag) % L
-            if l >= lag:  # layers L-lag .. L-1 were selected by the previous replay, which has completed
+            if topk and l >= lag:  # layers L-lag .. L-1 were selected by the previous replay, which has completed
                 main.wait_event(self.selected[j])
             if timed:
                 self.rec(self.attn_ev[l][0], main)
-            spc.spc_merged_attn_fetch(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
-                                      self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws,
-                                      self.host[j], self.W["N"], self.idx[j], k, self.staging[j],
-                                      ws_bytes=self.ws_bytes, stream=main)
+            if fetch:
+                spc.spc_merged_attn_fetch(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
+                                          self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws,
+                                          self.host[j], self.W["N"], self.idx[j], k, self.staging[j],
+                                          ws_bytes=self.ws_bytes, stream=main)
+            else:
+                spc.spc_merged_attn(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
+                                    self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws,
+                                    self.ws_bytes, stream=main)
             if timed:
                 self.rec(self.attn_ev[l][1], main)
+            if not topk:
+                continue
             self.attended[l].record(main)
             side.wait_event(self.attended[l])
             if timed:
@@ -259,8 +294,9 @@ class DecodeStep:
             if timed:
                 self.rec(self.topk_ev[l][1], side)
             self.selected[l].record(side)
-        for l in range(L):  # join the side stream before the step ends
-            main.wait_event(self.selected[l])
+        if topk:
+            for l in range(L):  # join the side stream before the step ends
+                main.wait_event(self.selected[l])
 
     def enqueue_step(self, timed=False):
         """One decode step on one stream, one launch per layer: spc_decode_step
@@ -387,16 +423,35 @@ class DecodeStep:
         torch = self.torch
         self.main.wait_stream(torch.cuda.current_stream())
         torch.cuda.synchronize()
-        graphs = []
-        for timed in (False, True):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(self.main):
-                g.capture_begin(capture_error_mode="relaxed")
-                self.enqueue(timed=timed)
-                g.capture_end()
-            graphs.append(g)
-        self.graph, self.graph_timed = graphs
+        self.graph = self.capture_graph(lambda: self.enqueue(timed=False))
+        self.graph_timed = self.capture_graph(lambda: self.enqueue(timed=True))
+
+    def capture_graph(self, enqueue):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.main):
+            g.capture_begin(capture_error_mode="relaxed")
+            enqueue()
+            g.capture_end()
         torch.cuda.synchronize()
+        return g
+
+    def time_graph(self, g, reps, warmup=3):
+        """ms per replay of graph g: `reps` replays back to back between two
+        events on the main stream, after `warmup` replays."""
+        torch = self.torch
+        with torch.cuda.stream(self.main):
+            for _ in range(warmup):
+                g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.main)
+        with torch.cuda.stream(self.main):
+            for _ in range(reps):
+                g.replay()
+        e1.record(self.main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
 
     def replay(self):
         with self.torch.cuda.stream(self.main):
@@ -555,25 +610,47 @@ def prefill_probe(W, layers=4, reps=3):
                     "(copy engines, device-to-host); the pipeline overlaps the next layer's quantisation"}
 
 
-def attention_bytes_per_layer(W, nq, fused=False):
+def attention_bytes_per_layer(W, nq):
     """Algorithmic HBM bytes of one merged-attention call (one layer): the
     low-bit copy, the residual and fetched 16-bit rows read, q read and o
-    written, plus (fused pre-fetch) the HBM writes of the rows it carries."""
+    written."""
     beta = 64 if W["bits"] == 1 else 96
     bh = W["B"] * W["Hkv"]
     r = W["N"] - nq
     qo = W["B"] * 2 * W["Hq"] * 128 * 2 * 2  # q read + o written
-    return bh * (nq * beta + r * 512 + W["k"] * 512) + qo + (bh * W["k"] * 512 if fused else 0)
+    return bh * (nq * beta + r * 512 + W["k"] * 512) + qo
 
 
 # ------------------------------------------------------------------ CPU oracle timing
+
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+_KV_CACHE = {}
+
+
+def kv_pair(seed, layer, B, Hkv, N, b, h):
+    """The seeded K, V rows of one (b, kv-head), generated once per process."""
+    import synth
+    key = (seed, layer, B, Hkv, N, b, h)
+    if key not in _KV_CACHE:
+        if len(_KV_CACHE) > 64:
+            _KV_CACHE.clear()
+        _KV_CACHE[key] = synth.kv_slice(seed, layer, B, Hkv, N, 128, b, h)
+    return _KV_CACHE[key]
+
 
 class OracleSample:
     """The oracle's per-layer decode work (merged attention, top-k, gather) on
     `pairs` (b, kv-head) pairs of one layer of the workload.  Inputs, the
     quantisation and the first selection are prepared once; run() times the rest."""
 
-    def __init__(self, W, pairs, seed=0, layer=0):
+    def __init__(self, W, pairs, seed=0, layer=0, k=None):
         import oracle
         import synth
         self.oracle = oracle
@@ -583,11 +660,12 @@ class OracleSample:
         qall = synth.queries(seed, layer, B, Hq)
         Ks, Vs, qs = [], [], []
         for (b, h) in sel:
-            kk, vv = synth.kv_slice(seed, layer, B, Hkv, N, 128, b, h)
+            kk, vv = kv_pair(seed, layer, B, Hkv, N, b, h)
             Ks.append(kk)
             Vs.append(vv)
             qs.append(qall[b, :, h * G:(h + 1) * G])
         self.P = len(sel)
+        self.pairs_per_layer = B * Hkv
         self.K = np.stack(Ks)[:, None]  # the pairs as P sequences with one KV head each
         self.V = np.stack(Vs)[:, None]
         self.q = np.stack(qs)
@@ -595,11 +673,12 @@ class OracleSample:
                              scale=float(np.float32(1 / math.sqrt(128))))
         self.qz = oracle.quantize(self.d, self.K, self.V)
         _, _, S0 = oracle.attention(self.d, self.q, self.qz, self.K, self.V)
-        self.k = W["k"]
+        self.k = W["k"] if k is None else k
         self.idx, _ = oracle.topk(self.d, S0, self.k)
         self.host = np.stack([self.K, self.V], axis=3)
-        self.scale_to_step = (B * Hkv / self.P) * W["layers"]
-        self.threads = min(self.P, os.cpu_count() or 1)
+        self.layers = W.get("layers", 1)
+        self.scale_to_step = (B * Hkv / self.P) * self.layers
+        self.threads = min(self.P, host_cores())
 
     def run(self):
         o = self.oracle
@@ -611,6 +690,212 @@ class OracleSample:
 
     def steps_per_s(self, seconds):
         return 1.0 / (seconds * self.scale_to_step)
+
+    def layer_ms(self, seconds):
+        """ms for the whole layer (all B * Hkv pairs) at the sample's rate."""
+        return 1000.0 * seconds * self.pairs_per_layer / self.P
+
+
+# ------------------------------------------------------------------ the other configurations
+
+CONFIGS = {  # shapes of the pages' Mistral-7B / LLaMA-2-7B layers and a one-head layer
+    "c1": dict(workload="one layer, B=1, 1 query / 1 KV head, N=1024, 1-bit, residual 32, k=16",
+               B=1, Hq=1, Hkv=1, N=1024, R=32, bits=1, ks=[16], pairs=1),
+    "c2": dict(workload="Mistral-7B layer, B=1, 32 query / 8 KV heads, N=32768, 1-bit, residual 128, k=328 (1%)",
+               B=1, Hq=32, Hkv=8, N=32768, R=128, bits=1, ks=[328], pairs=8),
+    "c3": dict(workload="LLaMA-2-7B layer, B=16, 32 query / 32 KV heads (MHA), N=2048, 2-bit, residual 128, k=64",
+               B=16, Hq=32, Hkv=32, N=2048, R=128, bits=2, ks=[64], pairs=16),
+}
+
+
+def c5_points():
+    """Configuration 5: the LLaMA-3-8B layer shape at B in {1, 4}, N in {4K, 16K,
+    64K, 128K}, 1 and 2 bits, k = 0.5%, 1% and 4% of N (k = ceil(p N))."""
+    pts = []
+    for B in (1, 4):
+        for N in (4096, 16384, 65536, 131072):
+            for bits in (1, 2):
+                ks = [int(math.ceil(round(p * N, 6))) for p in (0.005, 0.01, 0.04)]
+                pts.append(dict(workload=f"LLaMA-3-8B layer, B={B}, N={N}, {bits}-bit", B=B, Hq=32, Hkv=8, N=N,
+                                R=128, bits=bits, ks=ks, pairs=1))
+    return pts
+
+
+class LayerRig:
+    """One layer of a configuration resident on the device (the low-bit cache
+    and residual window, the pinned 16-bit host cache, the queries and every
+    output buffer), driven through the library's public calls.  Each call is
+    timed alone with CUDA events after an L2 flush (a 256 MB write, more than
+    the 129 MB L2), with the host queued ahead by a short GPU spin so that no
+    launch waits for the host."""
+
+    FLUSH_BYTES = 256 << 20
+
+    def __init__(self, cfg, seed=0, layer=0):
+        import torch
+
+        import bit_kv_cache_spc_gb300 as spc
+        import synth
+        import synth.gpu
+        self.torch, self.spc = torch, spc
+        B, Hq, Hkv, N, R, bits = (cfg[x] for x in ("B", "Hq", "Hkv", "N", "R", "bits"))
+        self.cfg = cfg
+        self.kmax = max(cfg["ks"])
+        self.G = Hq // Hkv
+        self.d = spc.Dims(B, Hq, Hkv, N, R, bits, scale=float(np.float32(1.0 / math.sqrt(128))))
+        d = self.d
+        dev = torch.device("cuda")
+        self.nq = spc.spc_num_quantized(d)
+        self.K = torch.empty((B, Hkv, N, 128), dtype=torch.int16, device=dev)
+        self.V = torch.empty_like(self.K)
+        synth.gpu.kv_layer_into(seed, layer, self.K, self.V)
+        self.records = torch.empty(max(spc.spc_records_bytes(d), 16), dtype=torch.uint8, device=dev)
+        self.resid = torch.empty(max(spc.spc_resid_bytes(d) // 2, 8), dtype=torch.int16, device=dev)
+        spc.spc_quantize_kv(d, self.K, self.V, self.records, self.resid)
+        self.host = torch.empty((B, Hkv, N, 2, 128), dtype=torch.int16, pin_memory=True)
+        self.host.copy_(torch.stack([self.K, self.V], dim=3))
+        self.q = torch.from_numpy(synth.queries(seed, layer, B, Hq).view(np.int16).copy()).to(dev)
+        self.o = torch.zeros((B, 2, Hq, 128), dtype=torch.int16, device=dev)
+        self.lse = torch.zeros((B, 2, Hq), dtype=torch.float32, device=dev)
+        self.logits = torch.zeros((B, Hkv, self.G, max(d.q_groups_cap * 32, 1)), dtype=torch.float32, device=dev)
+        self.idx = torch.zeros((B, Hkv, max(self.kmax, 1)), dtype=torch.int32, device=dev)
+        self.bitmap = torch.zeros((B, Hkv, max(d.q_groups_cap, 1)), dtype=torch.int32, device=dev)
+        self.staging = torch.zeros((B, Hkv, max(self.kmax, 1), 2, 128), dtype=torch.int16, device=dev)
+        self.ws_bytes = spc.spc_attn_workspace_bytes(d, self.kmax)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
+        self.flush = torch.empty(self.FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.Stream()
+        torch.cuda.synchronize()
+
+    # the calls of one decode step of this layer
+    def quantize(self):
+        self.spc.spc_quantize_kv(self.d, self.K, self.V, self.records, self.resid, stream=self.stream)
+
+    def attn2(self):
+        self.spc.spc_decode_attn2(self.d, self.records, self.resid, self.q, self.o, self.lse, self.logits, self.ws,
+                                  self.ws_bytes, stream=self.stream)
+
+    def topk(self, k):
+        self.spc.spc_topk_select(self.d, self.logits, self.lse, k, self.idx, self.bitmap, stream=self.stream)
+
+    def gather(self, k):
+        self.spc.spc_host_gather(self.d, self.host, self.cfg["N"], self.idx, k, self.staging, stream=self.stream)
+
+    def merged(self, k):
+        self.spc.spc_merged_attn(self.d, self.records, self.resid, self.q, self.idx, self.bitmap, self.staging, k,
+                                 self.o, self.lse, self.logits, self.ws, self.ws_bytes, stream=self.stream)
+
+    def decode_step(self, k):
+        """One decode step of the layer: the merged attention over C' U C_kappa,
+        its top-k and the pre-fetch of the new selection (for the next step)."""
+        self.merged(k)
+        self.topk(k)
+        self.gather(k)
+
+    def time_us(self, fn, reps=10):
+        """Median device time of fn (its kernels back to back), one call per
+        L2 flush."""
+        torch = self.torch
+        s = self.stream
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        out = []
+        with torch.cuda.stream(s):
+            for i in range(reps + 2):
+                self.flush.fill_(i)
+                torch.cuda._sleep(200000)  # the host enqueues fn while the GPU spins
+                e0.record(s)
+                fn()
+                e1.record(s)
+                e1.synchronize()
+                if i >= 2:
+                    out.append(e0.elapsed_time(e1) * 1000.0)
+        return statistics.median(out)
+
+    def graph_us(self, fn, reps=10):
+        """Median latency of fn captured as one CUDA graph and replayed, one
+        replay per L2 flush."""
+        torch = self.torch
+        s = self.stream
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.capture_begin(capture_error_mode="relaxed")
+            fn()
+            g.capture_end()
+        us = self.time_us(g.replay, reps)
+        del g
+        return us
+
+
+def attention_bytes(cfg, nq, k):
+    """Algorithmic HBM bytes of one merged-attention call: the low-bit copy,
+    the residual and fetched 16-bit rows read, q read and o written."""
+    beta = 64 if cfg["bits"] == 1 else 96
+    bh = cfg["B"] * cfg["Hkv"]
+    r = cfg["N"] - nq
+    qo = cfg["B"] * 2 * cfg["Hq"] * 128 * 2 * 2
+    return bh * (nq * beta + r * 512 + k * 512) + qo
+
+
+def measure_config(cfg, peak_gbs, oracle_on=True, reps=10, rig=None):
+    """Per-call device times of one configuration (its layer), bytes, HBM and
+    host-link fractions, and the oracle's time on a sample of the same layer."""
+    rig = LayerRig(cfg) if rig is None else rig
+    out = []
+    q_us = rig.time_us(rig.quantize, reps=max(3, reps // 3))
+    bh = cfg["B"] * cfg["Hkv"]
+    q_bytes = bh * cfg["N"] * 512 + bh * rig.nq * (64 if cfg["bits"] == 1 else 96)
+    a2_us = rig.time_us(rig.attn2, reps)
+    for k in cfg["ks"]:
+        rig.attn2()
+        rig.topk(k)
+        rig.gather(k)
+        rig.torch.cuda.synchronize()
+        t_us = rig.time_us(lambda: rig.topk(k), reps)
+        g_us = rig.time_us(lambda: rig.gather(k), reps)
+        m_us = rig.time_us(lambda: rig.merged(k), reps)
+        step_us = rig.graph_us(lambda: rig.decode_step(k), reps)
+        mb = attention_bytes(cfg, rig.nq, k)
+        a2b = attention_bytes(cfg, rig.nq, 0)
+        gb = bh * k * 512
+        pt = {"B": cfg["B"], "N": cfg["N"], "bits": cfg["bits"], "k": k,
+              "decode_step_graph_us": step_us, "merged_us": m_us, "attn2_us": a2_us, "topk_us": t_us,
+              "gather_us": g_us, "quantize_us": q_us,
+              "merged_bytes": mb, "merged_hbm_frac": mb / (m_us * 1e-6) / 1e9 / peak_gbs,
+              "attn2_hbm_frac": a2b / (a2_us * 1e-6) / 1e9 / peak_gbs,
+              "quantize_hbm_frac": q_bytes / (q_us * 1e-6) / 1e9 / peak_gbs,
+              "gather_bytes": gb, "gather_gbs": gb / (g_us * 1e-6) / 1e9}
+        if oracle_on:
+            ref = OracleSample(dict(cfg, k=k, layers=1), cfg["pairs"], k=k)
+            secs = [ref.run() for _ in range(2 if cfg["N"] >= 65536 else 3)]
+            dt = statistics.median(secs)
+            pt["oracle_ms_per_layer"] = ref.layer_ms(dt)
+            pt["oracle_sample"] = (f"merged attention + top-k + gather of {ref.P} of {ref.pairs_per_layer} "
+                                   f"(b, kv-head) pairs, {ref.threads} threads, scaled to the layer")
+        out.append(pt)
+    return out
+
+
+def measure_configs(peak_gbs, oracle_on=True, log=None):
+    """Configurations 1-3 and the 48 points of configuration 5, one line each."""
+    import torch
+    res = {}
+    for name, cfg in CONFIGS.items():
+        try:
+            res[name] = dict(workload=cfg["workload"], points=measure_config(cfg, peak_gbs, oracle_on))
+        except Exception as e:  # a failed configuration is reported, not fatal to the bench
+            res[name] = {"workload": cfg["workload"], "error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+    pts = []
+    for cfg in c5_points():
+        try:
+            pts += measure_config(cfg, peak_gbs, oracle_on)
+        except Exception as e:
+            pts.append({"B": cfg["B"], "N": cfg["N"], "bits": cfg["bits"], "error": f"{type(e).__name__}: {e}"})
+        torch.cuda.empty_cache()
+    res["c5"] = dict(workload="LLaMA-3-8B layer (32 query / 8 KV heads), B in {1, 4}, N in {4096, 16384, 65536, "
+                              "131072}, 1 and 2 bits, k = 0.5 / 1 / 4 % of N", points=pts)
+    return res
 
 
 # ------------------------------------------------------------------ ranks
@@ -672,18 +957,26 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        ref = OracleSample(W, args.cpu_pairs)
+        pairs = args.cpu_pairs or min(W["B"] * W["Hkv"], max(16, host_cores()))
+        ref = OracleSample(W, pairs)
         for _ in range(args.warmup):
             ref.run()
         secs = [ref.run() for _ in range(max(1, args.steps))]
-        v = ref.steps_per_s(statistics.median(secs))
-        sample = (f"per step: merged attention + top-k + gather of the CPU oracle on {ref.P} of "
-                  f"{W['B'] * W['Hkv']} (b, kv-head) pairs of one layer ({statistics.median(secs):.2f} s), "
-                  f"scaled x{W['B'] * W['Hkv'] // ref.P} pairs x {W['layers']} layers")
+        dt = statistics.median(secs)
+        v = ref.steps_per_s(dt)
+        sample = (f"each of the {args.steps} timed 'steps' is one run of the CPU oracle's merged attention + top-k + "
+                  f"gather on {ref.P} of {W['B'] * W['Hkv']} (b, kv-head) pairs of one layer "
+                  f"({dt:.2f} s median), extrapolated x{ref.scale_to_step:g} "
+                  f"({W['B'] * W['Hkv']} / {ref.P} pairs x {W['layers']} layers) to a decode step")
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": W["workload"]},
+                "measured": {"seconds_per_sample": dt, "samples": len(secs), "sample_pairs": ref.P,
+                             "pairs_per_layer": W["B"] * W["Hkv"], "layers": W["layers"],
+                             "scale_to_step": ref.scale_to_step, "threads": ref.threads,
+                             "host_cores": host_cores(),
+                             "note": "value and ms_per_step are extrapolated from the sample, not timed steps"},
                 "cpu_baseline": {"value": v, "unit": "steps/s", "cores": ref.threads, "kind": "oracle",
                                  "sample": sample},
                 "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -729,49 +1022,120 @@ def main():
     total_ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
     ms_per_step = total_ms / args.steps
     value = job_throughput(world, args.steps, total_ms)
+    launches_per_step = step.launches_per_step
 
-    # ---- end to end: queries in from pinned host memory, outputs back, every step ----
+    # ---- end to end: each step's queries in from pinned host memory (a different set every step, so the
+    # selections and the fetched host rows change), outputs back, every step ----
+    n_sets = 8
+    q_sets = torch.from_numpy(np.stack([np.stack([synth_queries(s_, l, W) for l in range(args.layers)])
+                                        for s_ in range(n_sets)]).view(np.int16).copy()).pin_memory()
     h2d = step.q_host.numel() * step.q_host.element_size()
     d2h = step.o.numel() * step.o.element_size()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(step.main)
-    for _ in range(args.steps):
+    for i in range(args.steps):
         with torch.cuda.stream(step.main):
-            step.q.copy_(step.q_host, non_blocking=True)
+            step.q.copy_(q_sets[i % n_sets], non_blocking=True)
             step.graph.replay()
             step.o_host.copy_(step.o, non_blocking=True)
     e1.record(step.main)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
     e2e = {"value": job_throughput(world, args.steps, e2e_ms), "unit": "steps/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h}
+           "d2h_bytes_per_step": d2h,
+           "note": f"queries rotate over {n_sets} seeded sets, so every step selects and fetches other host rows"}
+    # the same rotation with the query sets already in HBM (a device copy per step): what fresh
+    # selections cost the step, without the host copies
+    q_dev = q_sets.to("cuda")
+    barrier()
+    e0.record(step.main)
+    for i in range(args.steps):
+        with torch.cuda.stream(step.main):
+            step.q.copy_(q_dev[i % n_sets], non_blocking=True)
+            step.graph.replay()
+    e1.record(step.main)
+    barrier()
+    fresh_ms = e0.elapsed_time(e1) / args.steps
+    step.q.copy_(q_dev[0])
+    del q_dev
+    torch.cuda.synchronize()
 
-    # ---- roofline of the dominant call (merged attention, one layer per launch) ----
-    bytes_layer = attention_bytes_per_layer(W, step.nq, fused=args.prefetch in ("fused", "step", "overlap"))
-    attn_avg_ms = statistics.mean(per_layer)
+    # ---- overlap test: the step with the pre-fetch against the same step with the staging buffers already
+    # filled and no pre-fetch; the two graphs alternate, twice each ----
+    L = args.layers
+    overlap = None
+    if args.prefetch == "overlap":
+        g_nofetch = step.capture_graph(lambda: step.enqueue_overlap(fetch=False))
+        t_f, t_n = [], []
+        for _ in range(2):
+            t_f.append(step.time_graph(step.graph, reps=max(5, args.steps)))
+            t_n.append(step.time_graph(g_nofetch, reps=max(5, args.steps)))
+        del g_nofetch
+        tf, tn = statistics.mean(t_f), statistics.mean(t_n)
+        overlap = {"steps_per_s_with_prefetch": 1000.0 / tf, "steps_per_s_staging_preloaded": 1000.0 / tn,
+                   "delta_pct": 100.0 * (tf - tn) / tn, "hidden": (tf - tn) / tn <= 0.02,
+                   "prefetch_bytes_per_step": W["B"] * W["Hkv"] * W["k"] * 512 * L,
+                   "link_bound_ms_per_step": None,
+                   "what": "the step as timed, against the same step with every layer's selected rows already in "
+                           "HBM and no pre-fetch (spc_merged_attn instead of spc_merged_attn_fetch); 'hidden' is "
+                           "a difference of 2% or less"}
+    # the host copies of e2e alone, per step
+    e0.record(step.main)
+    for i in range(args.steps):
+        with torch.cuda.stream(step.main):
+            step.q.copy_(q_sets[i % n_sets], non_blocking=True)
+            step.o_host.copy_(step.o, non_blocking=True)
+    e1.record(step.main)
+    torch.cuda.synchronize()
+    e2e["host_copies_ms_per_step"] = e0.elapsed_time(e1) / args.steps
+    step.q.copy_(q_sets[0])
+    torch.cuda.synchronize()
+
+    # ---- roofline of the dominant call (merged attention, one layer per call) ----
+    # Its live duration is taken from the timed step itself: the layers' attention calls are the only work on
+    # the step's main stream (each top-k runs beside them on a second stream), so the main stream's time per
+    # layer bounds one call's duration from above (waits for a top-k, if any, are counted against it).
+    bytes_layer = attention_bytes_per_layer(W, step.nq)
+    attn_avg_ms = ms_per_step / L
+    dur_src = (f"the timed step's main stream per layer ({ms_per_step:.4f} ms / {L}): CUDA events on the launching "
+               f"stream around {args.steps} graph replays in which the {L} attention calls are that stream's only "
+               f"work")
     achieved = bytes_layer / (attn_avg_ms / 1000.0) / 1e9
+    pf_bytes = W["B"] * W["Hkv"] * W["k"] * 512 if args.prefetch in ("fused", "step", "overlap") else 0
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"],
-            "traffic": ATTN_TRAFFIC_BYTES if args.prefetch in ("fused", "overlap") else None,
-            "traffic_source": "dram read+write of one launch, profiles/attn_kernel_llama3_8b_32k.md",
-            "kernel": {"side": "spc_merged_attn (attn_kernel: low-bit scan + 16-bit rows; combine_kernel), "
-                               "one layer",
-                       "fused": "spc_merged_attn_fetch (attn_kernel: low-bit scan + 16-bit rows, previous layer's "
-                                "pre-fetch riding along; combine_kernel), one layer",
-                       "overlap": "spc_merged_attn_fetch (attn_kernel: low-bit scan + 16-bit rows, the pre-fetch "
-                                  "of the layer two before riding along; combine_kernel), one layer",
-                       "step": "spc_decode_step (low-bit scan + 16-bit rows + combine + top-k, previous "
-                               "layer's pre-fetch riding along), one layer"}[args.prefetch],
+            "frac": achieved / peaks["hbm_gbs"], "traffic": attention_traffic(),
+            "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of attn_kernel and combine_kernel "
+                              "for one call, from an ncu capture of this build's attention sources (null when "
+                              "the sources differ from the captured ones)",
+            "kernel": {"side": "spc_merged_attn (attn_kernel + combine_kernel), one layer",
+                       "fused": "spc_merged_attn_fetch (attn_kernel + combine_kernel; the previous layer's "
+                                "pre-fetch riding along), one layer",
+                       "overlap": "spc_merged_attn_fetch (attn_kernel + combine_kernel; the pre-fetch of the layer "
+                                  "two before riding along), one layer",
+                       "step": "spc_decode_step (attention + combine + top-k, the previous layer's pre-fetch "
+                               "riding along), one layer"}[args.prefetch],
             "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,
+            "duration_source": dur_src,
+            "prefetch_bytes_per_launch": pf_bytes,
+            "prefetch_note": "the carried pre-fetch rows (read over the host link, written to HBM) are not in the "
+                             "algorithmic bytes; they are accounted against the host link in 'gather'",
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-            "step_hbm_gbs": bytes_layer * W["layers"] / (ms_per_step / 1000.0) / 1e9}
+            "step_hbm_gbs": bytes_layer * L / (ms_per_step / 1000.0) / 1e9,
+            "step_hbm_frac": bytes_layer * L / (ms_per_step / 1000.0) / 1e9 / peaks["hbm_gbs"]}
 
     gather = host_link_probe(step, reps=20)
+    if overlap is not None:
+        overlap["link_bound_ms_per_step"] = overlap["prefetch_bytes_per_step"] / (gather["host_link_peak_gbs"] * 1e6)
     append = append_probe(W) if rank == 0 else None
     serial = step.time_serial(max(5, args.steps // 4), args.warmup) if rank == 0 else None
     prefill = prefill_probe(W) if rank == 0 else None
+    peak_hbm = peaks["hbm_gbs"]
+    del step
+    torch.cuda.empty_cache()
+    configs = measure_configs(peak_hbm, oracle_on=not args.no_cpu_baseline) if (rank == 0 and args.configs) \
+        else None
 
     line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -780,33 +1144,46 @@ def main():
                        "bits": W["bits"], "k": W["k"], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (4.3 GB low-bit cache per step, 129 MB L2); no flush",
                        "graph": "one CUDA graph per step",
+                       "replay": "every timed step replays the same queries, so the same rows are selected and "
+                                 "fetched each step (see e2e and fresh_queries for changing queries); the "
+                                 "decode-time append of the new token is not in the step (see append)",
                        "prefetch": {"side": f"side stream, {args.gather_ctas} CTAs",
                                     "fused": "fused into the next layer's attention",
                                     "step": "fused into the next layer's attention, which also ends with "
                                             "the top-k (spc_decode_step)",
                                     "overlap": "fused into the attention two layers on; top-k on a "
                                                "low-priority stream beside the next attention"}[args.prefetch]},
-            "roofline": roof, "gather": gather,
-            "per_layer_us": {"attention": attn_avg_ms * 1000.0, "topk": statistics.mean(per_layer_topk) * 1000.0},
+            "roofline": roof, "overlap": overlap, "gather": gather,
+            "fresh_queries": {"value": 1000.0 / fresh_ms, "unit": "steps/s",
+                              "what": "the step with the queries rotating over 8 seeded sets already in HBM"},
+            "per_layer_us": {"attention": statistics.mean(per_layer) * 1000.0,
+                             "topk": statistics.mean(per_layer_topk) * 1000.0,
+                             "note": "CUDA events around each call inside a copy of the step's graph (the events "
+                                     "break the programmatic overlap of neighbouring launches, so these run a few "
+                                     "microseconds longer than in the timed step)"},
             "append": append,
             "nonspeculative_baseline": serial,
-            "prefill": prefill, "clocks": clk.summary(), "e2e": e2e,
-            "gpu_launches": step.launches_per_step * args.steps}
+            "prefill": prefill, "configs": configs, "clocks": clk.summary(), "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps}
     if rank == 0 and not args.no_cpu_baseline:
-        ref = OracleSample(W, args.cpu_pairs)
+        pairs = args.cpu_pairs or min(W["B"] * W["Hkv"], max(16, host_cores()))
+        ref = OracleSample(W, pairs)
         secs = []
         while sum(secs) < 10.0 and len(secs) < 1000:  # about 10 s of oracle work
             secs.append(ref.run())
         dt = statistics.median(secs)
         line["cpu_baseline"] = {"value": ref.steps_per_s(dt), "unit": "steps/s", "cores": ref.threads,
-                                "kind": "oracle",
+                                "host_cores": host_cores(), "kind": "oracle",
                                 "sample": f"merged attention + top-k + gather of {ref.P} (b, kv-head) pairs of one "
                                           f"layer, {len(secs)} runs in {sum(secs):.1f} s (median {dt:.3f} s), "
                                           f"scaled to {W['B'] * W['Hkv']} pairs x {W['layers']} layers",
+                                "sample_pairs": ref.P, "pairs_per_layer": W["B"] * W["Hkv"], "layers": W["layers"],
+                                "measured_s_per_sample": dt, "scale_to_step": ref.scale_to_step,
                                 "single_core": oracle_single_core()}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
+        torch.distributed.barrier()
         torch.distributed.destroy_process_group()
 
 

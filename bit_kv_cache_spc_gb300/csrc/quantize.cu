@@ -31,23 +31,35 @@ __device__ __forceinline__ void quant_params(int bits, float lo, float hi, float
   }
 }
 
+// The multiplier that stands in for a division by s: the correctly rounded
+// reciprocal; 0 when s == 0 (the code is then 0); NaN when 1/s overflows
+// binary32 (s below about 2^-128, a subnormal range), so that every quotient
+// of such a group is settled by the IEEE division in quant_code.
+__device__ __forceinline__ float quant_recip(float s) {
+  if (s == 0.0f) return 0.0f;
+  const float rs = __frcp_rn(s);
+  return isinf(rs) ? __int_as_float(0x7FC00000) : rs;
+}
+
 // clamp(rint(fl((x - z) / s)), 0, 2^bits - 1), 0 when s == 0 (rs == 0 then).
 // The product with the correctly rounded reciprocal rs is within 1e-6 of the
 // IEEE quotient for the quotients that occur (|q| <= 3), so it decides every
 // value whose quotient is farther than 1e-5 from a rounding boundary k + 1/2;
-// the IEEE division settles the rest.  At 1 bit the code is 1 exactly when
-// the quotient exceeds 1/2 (1/2 itself rounds to even, 0).
+// the IEEE division settles the rest, and every product that is not a number
+// (a NaN rs, or an infinite x - z times a zero rs).  At 1 bit the code is 1
+// exactly when the quotient exceeds 1/2 (1/2 itself rounds to even, 0); a
+// quotient that is not a number gets code 0.
 template <int BITS>
 __device__ __forceinline__ uint32_t quant_code(float x, float z, float s, float rs) {
   const float d = __fsub_rn(x, z);
   float t = __fmul_rn(d, rs);
   if (BITS == 1) {
-    if (fabsf(__fsub_rn(t, 0.5f)) < 1e-5f && s != 0.0f) t = __fdiv_rn(d, s);
+    if (!(fabsf(__fsub_rn(t, 0.5f)) >= 1e-5f) && s != 0.0f) t = __fdiv_rn(d, s);
     return t > 0.5f ? 1u : 0u;
   } else {
     const float fr = __fsub_rn(t, floorf(t));
-    if (fabsf(__fsub_rn(fr, 0.5f)) < 1e-5f && s != 0.0f) t = __fdiv_rn(d, s);
-    return (uint32_t)fminf(fmaxf(rintf(t), 0.0f), 3.0f);
+    if (!(fabsf(__fsub_rn(fr, 0.5f)) >= 1e-5f) && s != 0.0f) t = __fdiv_rn(d, s);
+    return (uint32_t)fminf(fmaxf(rintf(t), 0.0f), 3.0f);  // fmaxf(NaN, 0) = 0
   }
 }
 
@@ -120,7 +132,7 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
     quant_params(BITS, lo, hi, z, s);
     sm.kz[c] = z;
     sm.kss[c] = s;
-    sm.krs[c] = s != 0.0f ? __frcp_rn(s) : 0.0f;
+    sm.krs[c] = quant_recip(s);
     sm.klohi[c] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
   }
   __syncthreads();
@@ -180,7 +192,7 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
     }
     float z, s;
     quant_params(BITS, lo, hi, z, s);
-    const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
+    const float rs = quant_recip(s);
     if ((lane & 3) == 0)
       sm.rec[VMETA + vmeta_word(n, kk >> 1)] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
     const int t = p & 3, j = 2 * (p >> 3) + ((p >> 2) & 1);
