@@ -670,7 +670,7 @@ class OracleSample:
         self.V = np.stack(Vs)[:, None]
         self.q = np.stack(qs)
         self.d = oracle.dims(B=self.P, Hq=G, Hkv=1, N=N, R=W["R"], bits=W["bits"],
-                             scale=float(np.float32(1 / math.sqrt(128))))
+                             scale=float(np.float32(1 / math.sqrt(128))), group=W.get("group", 32))
         self.qz = oracle.quantize(self.d, self.K, self.V)
         _, _, S0 = oracle.attention(self.d, self.q, self.qz, self.K, self.V)
         self.k = W["k"] if k is None else k
@@ -742,7 +742,8 @@ class LayerRig:
         self.cfg = cfg
         self.kmax = max(cfg["ks"])
         self.G = Hq // Hkv
-        self.d = spc.Dims(B, Hq, Hkv, N, R, bits, scale=float(np.float32(1.0 / math.sqrt(128))))
+        self.d = spc.Dims(B, Hq, Hkv, N, R, bits, scale=float(np.float32(1.0 / math.sqrt(128))),
+                          group=cfg.get("group", 32))
         d = self.d
         dev = torch.device("cuda")
         self.nq = spc.spc_num_quantized(d)
@@ -827,10 +828,16 @@ class LayerRig:
         return us
 
 
+def low_bit_bytes_per_token(bits, group=32):
+    """Bytes per token and KV head of the low-bit copy: codes plus a bf16
+    (min, max) pair per group of keys and of values."""
+    return {(1, 32): 64, (2, 32): 96, (1, 64): 48, (2, 64): 80}[(bits, group)]
+
+
 def attention_bytes(cfg, nq, k):
     """Algorithmic HBM bytes of one merged-attention call: the low-bit copy,
     the residual and fetched 16-bit rows read, q read and o written."""
-    beta = 64 if cfg["bits"] == 1 else 96
+    beta = low_bit_bytes_per_token(cfg["bits"], cfg.get("group", 32))
     bh = cfg["B"] * cfg["Hkv"]
     r = cfg["N"] - nq
     qo = cfg["B"] * 2 * cfg["Hq"] * 128 * 2 * 2
@@ -844,7 +851,7 @@ def measure_config(cfg, peak_gbs, oracle_on=True, reps=10, rig=None):
     out = []
     q_us = rig.time_us(rig.quantize, reps=max(3, reps // 3))
     bh = cfg["B"] * cfg["Hkv"]
-    q_bytes = bh * cfg["N"] * 512 + bh * rig.nq * (64 if cfg["bits"] == 1 else 96)
+    q_bytes = bh * cfg["N"] * 512 + bh * rig.nq * low_bit_bytes_per_token(cfg["bits"], cfg.get("group", 32))
     a2_us = rig.time_us(rig.attn2, reps)
     for k in cfg["ks"]:
         rig.attn2()
@@ -858,7 +865,8 @@ def measure_config(cfg, peak_gbs, oracle_on=True, reps=10, rig=None):
         mb = attention_bytes(cfg, rig.nq, k)
         a2b = attention_bytes(cfg, rig.nq, 0)
         gb = bh * k * 512
-        pt = {"B": cfg["B"], "N": cfg["N"], "bits": cfg["bits"], "k": k,
+        pt = {"B": cfg["B"], "N": cfg["N"], "bits": cfg["bits"], "group": cfg.get("group", 32), "k": k,
+              "low_bit_bytes_per_token": low_bit_bytes_per_token(cfg["bits"], cfg.get("group", 32)),
               "decode_step_graph_us": step_us, "merged_us": m_us, "attn2_us": a2_us, "topk_us": t_us,
               "gather_us": g_us, "quantize_us": q_us,
               "merged_bytes": mb, "merged_hbm_frac": mb / (m_us * 1e-6) / 1e9 / peak_gbs,
@@ -892,6 +900,15 @@ def measure_configs(peak_gbs, oracle_on=True, log=None):
             pts += measure_config(cfg, peak_gbs, oracle_on)
         except Exception as e:
             pts.append({"B": cfg["B"], "N": cfg["N"], "bits": cfg["bits"], "error": f"{type(e).__name__}: {e}"})
+        torch.cuda.empty_cache()
+    for bits in (1, 2):  # group size 64 (the appendix's LongBench runs) on one LLaMA-3-8B decode layer
+        cfg = dict(workload=f"LLaMA-3-8B decode layer at g = 64, B=8, 32/8 heads, N=32768, {bits}-bit, k=328",
+                   B=8, Hq=32, Hkv=8, N=32768, R=128, bits=bits, ks=[328], pairs=16, group=64)
+        name = f"g64_{bits}bit"
+        try:
+            res[name] = dict(workload=cfg["workload"], points=measure_config(cfg, peak_gbs, oracle_on))
+        except Exception as e:
+            res[name] = {"workload": cfg["workload"], "error": f"{type(e).__name__}: {e}"}
         torch.cuda.empty_cache()
     res["c5"] = dict(workload="LLaMA-3-8B layer (32 query / 8 KV heads), B in {1, 4}, N in {4096, 16384, 65536, "
                               "131072}, 1 and 2 bits, k = 0.5 / 1 / 4 % of N", points=pts)

@@ -1,1155 +1,13 @@
-// Attn([T_t, T'_{t+1}], C' U C_kappa): the two-query decode attention of the
-// SpeCache page (section 3 "Decoding", Algorithm 3) over the packed low-bit
-// copy C', with the fetched 16-bit rows C_kappa used in place of their
-// low-bit copies, plus the bf16 residual window.
-//
-// One launch per call, split-K over tokens (flash-decoding style):
-//   * grid (chunks, B*Hkv).  The 16-bit rows of a (b, hkv) (residual window
-//     first, then the fetched rows) are split into contiguous ranges over all
-//     warps of its CTAs; every warp first reduces its range on CUDA cores,
-//     while its first low-bit stages are already in flight, and the resulting
-//     softmax state seeds its low-bit accumulators.  Then each warp scans its
-//     share of the CTA's range of 32-token groups of C'.
-//   * every CTA merges its warps' states and writes one partial (running max,
-//     sum, unnormalised output) per query row to the workspace; the last CTA
-//     of a (b, hkv) to finish (an atomic ticket) merges the partials into the
-//     bf16 output and the log-sum-exp, and re-zeroes the ticket.  When all
-//     CTAs of a (b, hkv) form one resident thread-block cluster, the partials
-//     stay in shared memory and are merged through distributed shared memory
-//     instead (cluster_combine).
-//
-// Low-bit tile arithmetic.  With k^ = z + s*b (b the code, z and s per key
-// group), the logit of query row q is  sum_c q_c s_c b_c + sum_c q_c z_c.  The
-// first term is a 16x8x16 tensor-core product per 8 tokens and 16 channels:
-//   A = (q o s) for the 8 query rows (2 tokens x G <= 4 heads), split into an
-//       fp16 high part (rows 0..7) and the fp16 residual (rows 8..15), so the
-//       speculative logits keep ~22 significant bits;
-//   B = the key bits, exact: each an fp16 power of two that depends only on
-//       the token column (one AND of a rotated record word, see key_frag),
-//       divided out of the logit per column; the high plane at 2 bits
-//       multiplies a doubled A.
-// The value side o = sum_n p_n (z_n + s_n b_n) is the same product with
-// A = value bits (channels x tokens) and B = p o s (tokens x query rows); the
-// p*z term is accumulated on CUDA cores.  Softmax runs in base 2 with the
-// scale folded into q.  z and s of a group are computed once per warp into
-// shared memory and read back by the lanes that need them.
-#include <cooperative_groups.h>
-#include <math_constants.h>
+// Host side of the attention entry points: the work split, the workspace
+// layout and the launch sequence (the attention grid of the shape's (bit
+// width, group size) variant, then combine_kernel unless the CTAs combine in a
+// cluster or in the fused selection).  The kernels themselves are in
+// attention.cuh, instantiated per variant in attn_b{1,2}g{32,64}.cu.
+#include <algorithm>
 
-#include "common.cuh"
-#include "select.cuh"
+#include "attention.cuh"
 
 namespace spc {
-
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
-template <int BITS>
-struct Stages {
-  static constexpr int value = BITS == 1 ? 4 : 3;  // cp.async pipeline depth per warp
-};
-// At 1 bit the scaled query lives in registers across the low-bit loop; at 2
-// bits (twice the code words per group) it is read from shared memory to
-// keep the loop within the register budget of 4 CTAs per SM.
-template <int BITS>
-struct QueryInRegisters {
-  static constexpr bool value = BITS == 1;
-};
-constexpr int kSlots = kWarps;  // CTA merge slots: one per warp
-constexpr int kMaxCluster = 16;  // CTAs of one (b, hkv) that the clustered combine accepts
-constexpr float kNeg = -1e30f;  // finite "minus infinity": keeps max/rescale arithmetic NaN-free
-constexpr int kPartStride = 132; // floats per (cta, row) partial: m, l, pad, pad, o[128]
-constexpr int kZsPitch = 17;     // float4s per t block of a z/s table (16 + 1 pad)
-constexpr int kZsBytes = 2 * 4 * kZsPitch * 16;  // key and value tables of one warp
-constexpr int kMergePitch = kD + 4;              // padded row of the CTA merge buffer
-// Dynamic shared memory of one CTA: per warp, the low-bit stages (a record, a
-// 16-byte slot, a pre-fetched 16-bit row) and the z/s tables.
-template <int BITS>
-__host__ __device__ constexpr int attn_dyn_bytes() {
-  return kWarps * (Stages<BITS>::value * (1024 * (BITS + 1) + 16 + 512) + kZsBytes);
-}
-constexpr int kRowBatch = 16;                    // 16-bit rows staged per batch (512 bytes each)
-constexpr int kTilePitch = kD + 4;               // padded row of a warp's query / output transfer tile
-
-struct AttnArgs {
-  const uint8_t* records;
-  const uint16_t* resid;
-  const uint16_t* q;
-  const uint16_t* kv_self;  // [B][Hkv][2][D] bf16 or null: the speculative token's own key and value
-  const int32_t* idx;
-  const uint32_t* bitmap;
-  const uint16_t* staging;
-  float* spec_logits;
-  float* part;          // [BH][chunks][kMaxRows][kPartStride]
-  uint32_t* tickets;    // [BH], zero between calls
-  uint16_t* out;        // [B][2][Hq][D]
-  float* lse;           // [B][2][Hq] or null
-  int32_t k;
-  int32_t Hq, Hkv, G, nq, r, q_groups_cap, resid_cap;
-  int32_t chunks, groups_per_chunk;
-  int32_t Lcap;
-  int32_t ext_combine;  // 1: the CTAs only store their partials; combine_kernel, launched next, merges them
-  float qscale;  // softmax scale * log2(e)
-  // Pre-fetch riding on this launch (spc_merged_attn_fetch): rows pf_idx of
-  // the mapped host cache pf_host go to pf_staging; pf_rows = B*Hkv*pf_k.
-  const uint16_t* pf_host;  // device address of [B][Hkv][pf_ncap][2][D] bf16, or null
-  const int32_t* pf_idx;    // [B][Hkv][pf_k]
-  uint16_t* pf_staging;     // [B][Hkv][pf_k][2][D]
-  int64_t pf_ncap;
-  int32_t pf_k, pf_rows;
-  // Fused ArgTopK (spc_decode_step): per (b, hkv) the sel_k positions with the
-  // largest speculative probability go to sel_idx / sel_bitmap.  ready and
-  // tickets2 are per-(b, hkv) words (zero between calls); cand holds each
-  // chunk's candidates (key, position), cand_cap per chunk; fault is set when
-  // a wait ran out.
-  int32_t* sel_idx;       // [BH][sel_k]
-  uint32_t* sel_bitmap;   // [BH][q_groups_cap]
-  uint32_t* ready;
-  uint32_t* tickets2;
-  uint32_t* fault;
-  uint32_t* cand;         // [BH][chunks][cand_cap][2]
-  int32_t sel_k, sel_keff, cand_cap;
-};
-
-// A lone set bit at position p of an fp16 half (p = 10..14, the exponent
-// field) is the power of two 2^(2^(p-10) - 15); pos_comp(p) is its inverse.
-__host__ __device__ constexpr float pos_comp(int p) {
-  return p == 10 ? 16384.f : p == 11 ? 8192.f : p == 12 ? 2048.f : p == 13 ? 128.f : 0.5f;
-}
-
-// Key bits.  Record word j of lane (gid, t) holds, for token 8 nt + gid and
-// channel pair e = 4j + i (channels 16 (e >> 1) + 8 (e & 1) + 2t + {0, 1}),
-// the two bits that a left rotation by 4i brings to bits 11 + nt and 27 + nt:
-// so one AND of the rotated word is the B fragment {0, 2^-13 .. 2} of token
-// column nt, the same power of two for all its channels, which the logit
-// multiplies back per column (key_comp).
-__device__ __forceinline__ uint32_t key_frag(uint32_t rotated, int nt) {
-  return rotated & ((1u << (11 + nt)) | (1u << (27 + nt)));
-}
-__host__ __device__ constexpr float key_comp(int nt) { return pos_comp(11 + nt); }
-
-// Bits r and r+16 of w as an f16x2 pair {0, 2^bit_exp(r)} with a single AND:
-// the word is pre-rotated so that the two bits sit on one fp16 exponent bit
-// (positions 10..14 of each half), r5/r10/r31 = w rotated left by 5/10/31.
-// The power of two is undone per channel on the accumulator at the end.
-__device__ __forceinline__ uint32_t bit_pair_exp(uint32_t w, uint32_t r5, uint32_t r10, uint32_t r31, int r) {
-  if (r >= 10 && r <= 14) return w & ((1u << r) | (1u << (r + 16)));
-  if (r >= 5 && r <= 9) return r5 & ((1u << (r + 5)) | (1u << (r + 21)));
-  if (r <= 4) return r10 & ((1u << (r + 10)) | (1u << (r + 26)));
-  return r31 & ((1u << 14) | (1u << 30));
-}
-// fp16 exponent position of bit r after the rotation, and the factor that
-// maps the accumulated 2^e * x back to x.
-__host__ __device__ constexpr int bit_pos(int r) {
-  return (r >= 10 && r <= 14) ? r : (r >= 5 && r <= 9) ? r + 5 : (r <= 4) ? r + 10 : 14;
-}
-__host__ __device__ constexpr float bit_comp(int r) { return pos_comp(bit_pos(r)); }
-
-// fp16 high part of two floats (truncated to 11 significant bits, exact in
-// fp16) and the fp16 rounding of the remainder.
-__device__ __forceinline__ void split_hi_lo(float2 w, uint32_t& hi, uint32_t& lo) {
-  const float2 h = make_float2(__uint_as_float(__float_as_uint(w.x) & 0xFFFFE000u),
-                               __uint_as_float(__float_as_uint(w.y) & 0xFFFFE000u));
-  const float2 l = f2_sub(w, h);
-  hi = pack_f16x2(h.x, h.y);
-  lo = pack_f16x2(l.x, l.y);
-}
-
-// z and s of one group from its bf16 (min, max) word.
-template <int BITS>
-__device__ __forceinline__ void dequant_params(uint32_t mm, float& z, float& s) {
-  const float lo = __uint_as_float(mm << 16), hi = __uint_as_float(mm & 0xFFFF0000u);
-  if (BITS == 1) {
-    s = (hi - lo) * 0.5f;
-    z = fmaf(s, 0.5f, lo);  // (3 min + max) / 4 = min + s / 2
-  } else {
-    s = (hi - lo) * (1.f / 3.f);
-    z = lo;
-  }
-}
-
-// z and s of four groups from their bf16 (min, max) words, two groups per
-// packed instruction (the same roundings as dequant_params).
-template <int BITS>
-__device__ __forceinline__ void dequant_params4(uint4 mm, float4& z, float4& s) {
-  const float2 lo01 = make_float2(__uint_as_float(mm.x << 16), __uint_as_float(mm.y << 16));
-  const float2 lo23 = make_float2(__uint_as_float(mm.z << 16), __uint_as_float(mm.w << 16));
-  const float2 hi01 = make_float2(__uint_as_float(mm.x & 0xFFFF0000u), __uint_as_float(mm.y & 0xFFFF0000u));
-  const float2 hi23 = make_float2(__uint_as_float(mm.z & 0xFFFF0000u), __uint_as_float(mm.w & 0xFFFF0000u));
-  constexpr float f = BITS == 1 ? 0.5f : 1.f / 3.f;
-  const float2 s01 = f2_mul(f2_sub(hi01, lo01), make_float2(f, f));
-  const float2 s23 = f2_mul(f2_sub(hi23, lo23), make_float2(f, f));
-  s = make_float4(s01.x, s01.y, s23.x, s23.y);
-  if (BITS == 1) {
-    const float2 z01 = f2_fma(s01, make_float2(0.5f, 0.5f), lo01);
-    const float2 z23 = f2_fma(s23, make_float2(0.5f, 0.5f), lo23);
-    z = make_float4(z01.x, z01.y, z23.x, z23.y);
-  } else {
-    z = make_float4(lo01.x, lo01.y, lo23.x, lo23.y);
-  }
-}
-
-struct CtaMerge {
-  float m[kSlots][kMaxRows];
-  float l[kSlots][kMaxRows];
-  float o[kSlots][kMaxRows][kMergePitch];
-};
-// the clustered combine's partial (kMaxRows x kPartStride floats) follows the merge buffer
-constexpr int kClusterPartOffset = (int)((sizeof(CtaMerge) + 15) / 16 * 16);
-
-// ------------------------------------------------------------ 16-bit rows
-// Reduce-scatter of 16 per-lane partial sums: returns the warp-wide sum of
-// x[lane >> 1], halving the vector at each butterfly step (16 shuffles).
-__device__ __forceinline__ float reduce_scatter16(const float (&x)[16], int lane) {
-  float y8[8], y4[4], y2[2];
-  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    y8[k] = (u16 ? x[k + 8] : x[k]) + __shfl_xor_sync(0xFFFFFFFFu, u16 ? x[k] : x[k + 8], 16);
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    y4[k] = (u8 ? y8[k + 4] : y8[k]) + __shfl_xor_sync(0xFFFFFFFFu, u8 ? y8[k] : y8[k + 4], 8);
-#pragma unroll
-  for (int k = 0; k < 2; ++k)
-    y2[k] = (u4 ? y4[k + 2] : y4[k]) + __shfl_xor_sync(0xFFFFFFFFu, u4 ? y4[k] : y4[k + 2], 4);
-  const float y1 = (u2 ? y2[1] : y2[0]) + __shfl_xor_sync(0xFFFFFFFFu, u2 ? y2[0] : y2[1], 2);
-  return y1 + __shfl_xor_sync(0xFFFFFFFFu, y1, 1);
-}
-
-// The residual window and the fetched rows of this warp's range, before its
-// low-bit groups (whose first stage is already in flight).  Rows are staged
-// kRowBatch at a time with cp.async into `tail` (the warp's stages after the
-// first and its z/s table, free until the low-bit loop starts).  fill_query() is the CTA-wide
-// fill of sq (it ends with a barrier); the positions of the warp's first
-// fetched rows are loaded before it, so that both latencies overlap.  Logits: lane = 4 channels x 8 query rows for two rows at a
-// time, then a reduce-scatter leaves lane with row (lane >> 4), query row
-// (lane >> 1) & 7.  Value product: lane = 4 channels, p broadcast from shared
-// memory.  sq is the CTA's scaled query tile [kMaxRows][kTilePitch] (rows
-// 2G.. zero).  On return (m_run, l_run, oacc) hold the softmax state of the
-// rows, in the tensor-core fragment layouts of the low-bit loop (oacc divided by the per-channel powers of two that loop
-// multiplies back at its end).
-template <bool MERGED, typename FillQuery>
-__device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* sq, uint8_t* tail,
-                                                FillQuery&& fill_query, float& m_run, float& l_run,
-                                                float (&oacc)[8][4]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int gid = lane >> 2, t = lane & 3;
-  const int64_t bh = blockIdx.y;
-  const int G = a.G;
-
-  // rows: residual window [0, r), fetched rows [r, r + kk), then the
-  // speculative token's own row (seen by the speculative query rows only)
-  const int kk = MERGED ? a.k : 0;
-  const int j_self = a.kv_self != nullptr ? a.r + kk : -1;
-  const int n_rows = a.r + kk + (a.kv_self != nullptr ? 1 : 0);
-  const int n_warps = a.chunks * kWarps;
-  const int per_warp = (n_rows + n_warps - 1) / n_warps;
-  const int j0 = min(n_rows, (int)(blockIdx.x * kWarps + warp) * per_warp);
-  const int j1 = min(n_rows, j0 + per_warp);
-  float* pb = reinterpret_cast<float*>(tail + kRowBatch * 512);  // p of a batch: [row][query row]
-  const int rho_l = (lane >> 1) & 7;
-  const bool spec_lane = MERGED && a.spec_logits != nullptr && (lane & 1) == 0 && rho_l >= G && rho_l < 2 * G;
-  float* spec_out = spec_lane ? a.spec_logits + (bh * G + (rho_l - G)) * (int64_t)a.Lcap : nullptr;
-  float m_own = kNeg, l_own = 0.f;  // state of query row rho_l
-  float o16[kMaxRows][4];
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho) o16[rho][0] = o16[rho][1] = o16[rho][2] = o16[rho][3] = 0.f;
-  // quantised position of the fetched row of lane (window w0), -1 for the residual window
-  auto row_pos = [&](int w0) {
-    const int j = w0 + lane;
-    return (lane < min(32, j1 - w0) && j >= a.r && j < a.r + kk) ? a.idx[bh * a.k + (j - a.r)] : -1;
-  };
-  const int pos_first = row_pos(j0);
-  fill_query();
-
-  for (int w0 = j0; w0 < j1; w0 += 32) {
-    const int nwin = min(32, j1 - w0);
-    const int pos = w0 == j0 ? pos_first : row_pos(w0);
-    const bool ok = lane < nwin && (w0 + lane < a.r || w0 + lane == j_self || (pos >= 0 && pos < a.nq));
-    const uint32_t valid = __ballot_sync(0xFFFFFFFFu, ok);
-    for (int b0 = 0; b0 < nwin; b0 += kRowBatch) {
-      const int nb = min(kRowBatch, nwin - b0);
-      for (int i = 0; i < nb; ++i) {
-        if ((valid >> (b0 + i)) & 1u) {
-          const int j = w0 + b0 + i;
-          const uint16_t* row = j < a.r        ? a.resid + (bh * a.resid_cap + j) * 2 * kD
-                                : j == j_self ? a.kv_self + bh * 2 * kD
-                                              : a.staging + (bh * a.k + (j - a.r)) * 2 * kD;
-          cp_async16(tail + 512 * i + 16 * lane, row + 8 * lane);
-        }
-      }
-      cp_async_commit();
-      cp_async_wait<0>();  // with the first batch, also the low-bit stages issued before it
-      __syncwarp();
-
-      float lg[kRowBatch / 2];
-#pragma unroll
-      for (int pp = 0; pp < kRowBatch / 2; ++pp) {
-        lg[pp] = kNeg;
-        if (2 * pp < nb) {
-          float x[16];
-#pragma unroll
-          for (int jh = 0; jh < 2; ++jh) {
-            const uint2 kk = *reinterpret_cast<const uint2*>(tail + 512 * (2 * pp + jh) + 8 * lane);
-            const float k0 = bf16_to_f32(kk.x & 0xFFFFu), k1 = bf16_to_f32(kk.x >> 16);
-            const float k2 = bf16_to_f32(kk.y & 0xFFFFu), k3 = bf16_to_f32(kk.y >> 16);
-#pragma unroll
-            for (int rho = 0; rho < kMaxRows; ++rho) {
-              const float4 qq = *reinterpret_cast<const float4*>(sq + rho * kTilePitch + 4 * lane);
-              x[8 * jh + rho] = fmaf(qq.w, k3, fmaf(qq.z, k2, fmaf(qq.y, k1, qq.x * k0)));
-            }
-          }
-          const float v = reduce_scatter16(x, lane);
-          const int i = 2 * pp + (lane >> 4);
-          // the speculative token's own row is masked for the output token's rows
-          if (i < nb && ((valid >> (b0 + i)) & 1u) && !(w0 + b0 + i == j_self && rho_l < G)) lg[pp] = v;
-        }
-        const int pi = __shfl_sync(0xFFFFFFFFu, pos, b0 + 2 * pp + (lane >> 4));
-        if (spec_lane && lg[pp] != kNeg && pi >= 0) spec_out[pi] = lg[pp] * CUDART_LN2_F;
-      }
-
-      float mx = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-      const float m_new = fmaxf(m_own, mx);
-      const float alpha = fast_exp2(m_own - m_new);
-      float ps = 0.f, p[kRowBatch / 2];
-#pragma unroll
-      for (int pp = 0; pp < kRowBatch / 2; ++pp) {
-        p[pp] = lg[pp] == kNeg ? 0.f : fast_exp2(lg[pp] - m_new);
-        ps += p[pp];
-      }
-      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 16);
-      l_own = l_own * alpha + ps;
-      m_own = m_new;
-      if ((lane & 1) == 0) {
-#pragma unroll
-        for (int pp = 0; pp < kRowBatch / 2; ++pp) pb[(2 * pp + (lane >> 4)) * kMaxRows + rho_l] = p[pp];
-      }
-#pragma unroll
-      for (int rho = 0; rho < kMaxRows; ++rho) {
-        const float al = __shfl_sync(0xFFFFFFFFu, alpha, 2 * rho);
-        o16[rho][0] *= al;
-        o16[rho][1] *= al;
-        o16[rho][2] *= al;
-        o16[rho][3] *= al;
-      }
-      __syncwarp();
-      for (int i = 0; i < nb; ++i) {
-        if (!((valid >> (b0 + i)) & 1u)) continue;  // uniform across the warp
-        const uint2 vv = *reinterpret_cast<const uint2*>(tail + 512 * i + 2 * kD + 8 * lane);
-        const float v0 = bf16_to_f32(vv.x & 0xFFFFu), v1 = bf16_to_f32(vv.x >> 16);
-        const float v2 = bf16_to_f32(vv.y & 0xFFFFu), v3 = bf16_to_f32(vv.y >> 16);
-        const float4 pa = *reinterpret_cast<const float4*>(pb + i * kMaxRows);
-        const float4 pc = *reinterpret_cast<const float4*>(pb + i * kMaxRows + 4);
-        const float pr[kMaxRows] = {pa.x, pa.y, pa.z, pa.w, pc.x, pc.y, pc.z, pc.w};
-#pragma unroll
-        for (int rho = 0; rho < kMaxRows; ++rho) {
-          o16[rho][0] = fmaf(pr[rho], v0, o16[rho][0]);
-          o16[rho][1] = fmaf(pr[rho], v1, o16[rho][1]);
-          o16[rho][2] = fmaf(pr[rho], v2, o16[rho][2]);
-          o16[rho][3] = fmaf(pr[rho], v3, o16[rho][3]);
-        }
-      }
-      __syncwarp();
-    }
-  }
-  // hand the state over to the fragment layout through `tail`
-  float* tile = reinterpret_cast<float*>(tail);  // [kMaxRows][kTilePitch]
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho)
-    *reinterpret_cast<float4*>(tile + rho * kTilePitch + 4 * lane) =
-        make_float4(o16[rho][0], o16[rho][1], o16[rho][2], o16[rho][3]);
-  __syncwarp();
-  // oacc[mt]: (channel 16mt+gid, row 2t), (16mt+gid, 2t+1), (16mt+gid+8, 2t), (16mt+gid+8, 2t+1)
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const float c0 = 1.f / bit_comp(2 * mt), c1 = 1.f / bit_comp(2 * mt + 1);
-    oacc[mt][0] = tile[(2 * t) * kTilePitch + 16 * mt + gid] * c0;
-    oacc[mt][1] = tile[(2 * t + 1) * kTilePitch + 16 * mt + gid] * c0;
-    oacc[mt][2] = tile[(2 * t) * kTilePitch + 16 * mt + gid + 8] * c1;
-    oacc[mt][3] = tile[(2 * t + 1) * kTilePitch + 16 * mt + gid + 8] * c1;
-  }
-  __syncwarp();
-  m_run = __shfl_sync(0xFFFFFFFFu, m_own, 2 * gid);
-  const float lr = __shfl_sync(0xFFFFFFFFu, l_own, 2 * gid);
-  l_run = t == 0 ? lr : 0.f;  // the low-bit loop sums l over the four lanes of a row at its end
-}
-
-// ------------------------------------------------------------ low-bit CTA
-template <int BITS, bool MERGED, bool FETCH, typename FillQuery>
-__device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, const float* sq, CtaMerge& merge,
-                                           FillQuery&& fill_query) {
-  constexpr int RB = 1024 * (BITS + 1);
-  constexpr int KMETA = 512 * BITS;
-  constexpr int VCODES = KMETA + 512;
-  constexpr int VMETA = VCODES + 512 * BITS;
-  // a stage: the record, a 16-byte slot (bitmap word, pre-fetch position), a pre-fetched 16-bit row
-  constexpr int PFROW = RB + 16;
-  constexpr int STAGE = PFROW + 512;
-  constexpr int kStages = Stages<BITS>::value;
-  constexpr int WARP_BYTES = kStages * STAGE + kZsBytes;
-  static_assert(kWarps * WARP_BYTES == attn_dyn_bytes<BITS>(), "stage layout and launch size disagree");
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int gid = lane >> 2, t = lane & 3;
-  const int64_t bh = blockIdx.y;
-  const int chunk = blockIdx.x;
-  const int G = a.G;
-  const bool row_valid = gid < 2 * G;
-
-  uint8_t* stage = dyn + (size_t)warp * WARP_BYTES;
-  // per-group z and s: keys [t][kc][z0..3, s0..3], values [t][c16][e][z at slot e over cg0..3,
-  // s at channel group e over slot0..3] (the scales transposed so that a B fragment's two tokens
-  // sit side by side),
-  // each t block padded by one float4 so that the four t rows read together
-  // fall in different banks
-  float4* kzs = reinterpret_cast<float4*>(stage + kStages * STAGE);
-  float4* vzs = kzs + kZsPitch * 4;
-
-  const int g_begin = chunk * a.groups_per_chunk;
-  const int g_end = min(a.nq / kGroup, g_begin + a.groups_per_chunk);
-  const int n_my = (g_end - g_begin - warp + kWarps - 1) / kWarps;  // groups of this warp
-  const uint8_t* rec_base = a.records + (bh * a.q_groups_cap) * (int64_t)RB;
-
-  // Pre-fetch rows of this warp: rr = slot + n_slots * i, carried by items
-  // 0, pf_every, 2 pf_every, ... (one 512-byte row per carried item), the
-  // rest copied after the groups.
-  const int64_t n_slots = (int64_t)gridDim.x * gridDim.y * kWarps;
-  const int64_t slot = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kWarps + warp;
-  const int n_pf = (FETCH && a.pf_rows > slot) ? (int)((a.pf_rows - slot + n_slots - 1) / n_slots) : 0;
-  // At most one carried row per pipeline depth (a warp then waits on at most
-  // one host read at a time); the rows beyond that go after the groups.
-  const int pf_every = n_pf > 0 ? max(kStages, n_my / n_pf) : 1;
-  const int pf_carried = n_pf > 0 ? min(n_pf, (n_my + pf_every - 1) / pf_every) : 0;
-  int pf_next = n_pf > 0 ? a.pf_idx[slot] : -1;  // position of the next row to issue
-  int pf_issue_i = 0, pf_issue_item = 0;          // next carried row on the issue side and its item
-
-  auto issue = [&](int item) {
-    if (item < n_my) {
-      const int g = g_begin + warp + item * kWarps;
-      const uint8_t* src = rec_base + (int64_t)g * RB;
-      uint8_t* dst = stage + (item % kStages) * STAGE;
-#pragma unroll
-      for (int u = 0; u < RB / 512; ++u) cp_async16(dst + 16 * (lane + 32 * u), src + 16 * (lane + 32 * u));
-      if (MERGED && lane == 0) cp_async4(dst + RB, a.bitmap + bh * a.q_groups_cap + g);
-      if (FETCH && item == pf_issue_item && pf_issue_i < pf_carried) {
-        const int64_t rr = slot + n_slots * pf_issue_i;
-        const int n = pf_next;
-        if (lane == 0) reinterpret_cast<int*>(dst + RB)[1] = n;
-        if (n >= 0 && n < a.pf_ncap) {
-          const int64_t src_row = ((rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
-          cp_async16(dst + PFROW + 16 * lane, a.pf_host + src_row + 8 * lane);
-        }
-        pf_next = (pf_issue_i + 1 < n_pf) ? a.pf_idx[rr + n_slots] : -1;
-        ++pf_issue_i;
-        pf_issue_item += pf_every;
-      }
-    }
-    cp_async_commit();
-  };
-
-  // the state left by this warp's 16-bit rows, and the scaled query of row
-  // gid at this lane's 32 channels, ordered m = 4*kc + 2*h + half <->
-  // channel 16*kc + 2*t + 8*h + half (registers at 1 bit, else read from sq)
-  float m_run, l_run;
-  float oacc[8][4];
-  // The first low-bit stage is in flight behind the query fill and the 16-bit
-  // rows, which are staged in the other stages and the z/s table (a warp's
-  // rows then take one round trip); the rest of the pipeline is issued after.
-  issue(0);
-  rows16_prologue<MERGED>(a, sq, stage + STAGE, fill_query, m_run, l_run, oacc);
-#pragma unroll 1
-  for (int s = 1; s < kStages - 1; ++s) issue(s);
-  constexpr bool kQvReg = QueryInRegisters<BITS>::value;
-  float qv[kQvReg ? 32 : 1];
-  if constexpr (kQvReg) {
-#pragma unroll
-    for (int m = 0; m < 32; m += 2) {
-      const float2 v = *reinterpret_cast<const float2*>(sq + gid * kTilePitch + 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1));
-      qv[m] = v.x;
-      qv[m + 1] = v.y;
-    }
-  }
-  float2 zacc01 = make_float2(0.f, 0.f), zacc23 = make_float2(0.f, 0.f);
-
-  const bool spec_row = row_valid && gid >= G && a.spec_logits != nullptr;
-  float* spec_out = spec_row ? a.spec_logits + ((bh * G + (gid - G)) * (int64_t)a.Lcap) : nullptr;
-
-  int pf_use_i = 0, pf_use_item = 0;  // next carried row on the consuming side and its item
-#pragma unroll 1
-  for (int it = 0; it < n_my; ++it) {
-    issue(it + kStages - 1);
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    const uint8_t* R = stage + (it % kStages) * STAGE;
-    const int g = g_begin + warp + it * kWarps;
-    if (FETCH && it == pf_use_item && pf_use_i < pf_carried) {
-      const int n = reinterpret_cast<const int*>(R + RB)[1];
-      if (n >= 0 && n < a.pf_ncap) {
-        const int64_t rr = slot + n_slots * pf_use_i;
-        reinterpret_cast<uint4*>(a.pf_staging + rr * (2 * kD))[lane] =
-            reinterpret_cast<const uint4*>(R + PFROW)[lane];
-      }
-      ++pf_use_i;
-      pf_use_item += pf_every;
-    }
-
-    // ---- z, s of the group's 128 key groups and 128 value groups, 4 + 4 per lane ----
-    {
-      const int zi = kZsPitch * (lane >> 3) + 2 * (lane & 7);
-      float4 z, s;
-      dequant_params4<BITS>(*reinterpret_cast<const uint4*>(R + KMETA + 16 * lane), z, s);
-      kzs[zi] = z;  // lane covers key entries 4*lane..4*lane+3 = (t = lane/8, kc = lane%8)
-      kzs[zi + 1] = s;
-      dequant_params4<BITS>(*reinterpret_cast<const uint4*>(R + VMETA + 16 * lane), z, s);
-      vzs[zi] = z;  // value entries: (t, c16, slot) = (lane/8, (lane/4)%2, lane%4), cg 0..3
-      {  // scales transposed within the c16 block: entry 4 c16 + cg holds slots 0..3
-        float* st = reinterpret_cast<float*>(vzs + kZsPitch * (lane >> 3) + 2 * (lane & 4) + 1);
-        const int slot = lane & 3;
-        st[slot] = s.x;
-        st[8 + slot] = s.y;
-        st[16 + slot] = s.z;
-        st[24 + slot] = s.w;
-      }
-    }
-    __syncwarp();
-
-    // ---- QK, channel chunk outer: A = q o s (hi/lo), B = key bits ----
-    uint32_t kw[4], kw1[4];  // word j: channel pairs 4j .. 4j+3 of the lane's four tokens
-    {
-      const uint4 v0 = *reinterpret_cast<const uint4*>(R + 16 * lane);
-      kw[0] = v0.x; kw[1] = v0.y; kw[2] = v0.z; kw[3] = v0.w;
-      if (BITS == 2) {
-        const uint4 v1 = *reinterpret_cast<const uint4*>(R + 512 + 16 * lane);
-        kw1[0] = v1.x; kw1[1] = v1.y; kw1[2] = v1.z; kw1[3] = v1.w;
-      }
-    }
-    float acc[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    float2 bias2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc) {
-      const float4 z4 = kzs[kZsPitch * t + 2 * kc];
-      const float4 s4 = kzs[kZsPitch * t + 2 * kc + 1];
-      // query row gid at channels 16kc + 2t + {0, 1} and 16kc + 2t + 8 + {0, 1}
-      float2 q01, q23;
-      if constexpr (kQvReg) {
-        q01 = make_float2(qv[4 * kc], qv[4 * kc + 1]);
-        q23 = make_float2(qv[4 * kc + 2], qv[4 * kc + 3]);
-      } else {
-        q01 = *reinterpret_cast<const float2*>(sq + gid * kTilePitch + 16 * kc + 2 * t);
-        q23 = *reinterpret_cast<const float2*>(sq + gid * kTilePitch + 16 * kc + 2 * t + 8);
-      }
-      bias2 = f2_fma(q01, make_float2(z4.x, z4.y), bias2);
-      bias2 = f2_fma(q23, make_float2(z4.z, z4.w), bias2);
-      uint32_t af[4];
-      split_hi_lo(f2_mul(q01, make_float2(s4.x, s4.y)), af[0], af[1]);
-      split_hi_lo(f2_mul(q23, make_float2(s4.z, s4.w)), af[2], af[3]);
-      // channel pairs e = 2kc (b0) and 2kc + 1 (b1): word kc/2 rotated by 4i, i = e mod 4
-      const int rot = 8 * (kc & 1);
-      const uint32_t r0 = __funnelshift_l(kw[kc >> 1], kw[kc >> 1], rot);
-      const uint32_t r1 = __funnelshift_l(kw[kc >> 1], kw[kc >> 1], rot + 4);
-      if (BITS == 2) {  // high plane: weight 2, carried by doubling A (exact in fp16)
-        const uint32_t x0 = __funnelshift_l(kw1[kc >> 1], kw1[kc >> 1], rot);
-        const uint32_t x1 = __funnelshift_l(kw1[kc >> 1], kw1[kc >> 1], rot + 4);
-        const uint32_t af2[4] = {hadd2_u32(af[0], af[0]), hadd2_u32(af[1], af[1]), hadd2_u32(af[2], af[2]),
-                                 hadd2_u32(af[3], af[3])};
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma_16816(acc[nt], af2, key_frag(x0, nt), key_frag(x1, nt));
-      }
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) mma_16816(acc[nt], af, key_frag(r0, nt), key_frag(r1, nt));
-    }
-    float bias = bias2.x + bias2.y;
-    bias += __shfl_xor_sync(0xFFFFFFFFu, bias, 1);
-    bias += __shfl_xor_sync(0xFFFFFFFFu, bias, 2);
-
-    // ---- logits, speculative-row output, online softmax (base 2) ----
-    // bm: the group's tokens whose 16-bit rows were fetched (same word in every lane)
-    const uint32_t bm = MERGED ? *reinterpret_cast<const uint32_t*>(R + RB) : 0u;
-    float lg[4][2];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const float2 l = f2_fma(f2_add(make_float2(acc[nt][0], acc[nt][1]), make_float2(acc[nt][2], acc[nt][3])),
-                              make_float2(key_comp(nt), key_comp(nt)), make_float2(bias, bias));
-      lg[nt][0] = l.x;
-      lg[nt][1] = l.y;
-    }
-    if (spec_row) {
-      float* dst = spec_out + (int64_t)g * kGroup + 2 * t;
-      if (!MERGED || bm == 0u) {  // uniform: most groups have no fetched token
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-          *reinterpret_cast<float2*>(dst + 8 * nt) =
-              f2_mul(make_float2(lg[nt][0], lg[nt][1]), make_float2(CUDART_LN2_F, CUDART_LN2_F));
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const uint32_t mb = (bm >> (8 * nt + 2 * t)) & 3u;
-          if (!(mb & 1u)) dst[8 * nt] = lg[nt][0] * CUDART_LN2_F;
-          if (!(mb & 2u)) dst[8 * nt + 1] = lg[nt][1] * CUDART_LN2_F;
-        }
-      }
-    }
-    if (MERGED && bm != 0u) {  // uniform: most groups have no fetched token
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int tok = 8 * nt + 2 * t;
-        if ((bm >> tok) & 1u) lg[nt][0] = kNeg;
-        if ((bm >> (tok + 1)) & 1u) lg[nt][1] = kNeg;
-      }
-    }
-    float gmax = fmaxf(fmaxf(fmaxf(lg[0][0], lg[0][1]), fmaxf(lg[1][0], lg[1][1])),
-                       fmaxf(fmaxf(lg[2][0], lg[2][1]), fmaxf(lg[3][0], lg[3][1])));
-    gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, 1));
-    gmax = fmaxf(gmax, __shfl_xor_sync(0xFFFFFFFFu, gmax, 2));
-    const float m_new = fmaxf(m_run, gmax);
-    if (__any_sync(0xFFFFFFFFu, m_new != m_run)) {
-      const float alpha = fast_exp2(m_run - m_new);
-      const float al_a = __shfl_sync(0xFFFFFFFFu, alpha, (2 * t) * 4);
-      const float al_b = __shfl_sync(0xFFFFFFFFu, alpha, (2 * t + 1) * 4);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        oacc[mt][0] *= al_a;
-        oacc[mt][1] *= al_b;
-        oacc[mt][2] *= al_a;
-        oacc[mt][3] *= al_b;
-      }
-      l_run *= alpha;
-      zacc01 = f2_mul(zacc01, make_float2(alpha, alpha));
-      zacc23 = f2_mul(zacc23, make_float2(alpha, alpha));
-      m_run = m_new;
-    }
-    // a masked logit (kNeg) gives exactly 0, also while no token has been seen yet
-    const float m_use = fmaxf(m_run, 0.5f * kNeg);
-    float p[4][2];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        p[nt][e] = fast_exp2(lg[nt][e] - m_use);
-        l_run += p[nt][e];
-      }
-
-    // ---- PV: two 16-token chunks; A = value bits, B = p o s ----
-    uint32_t vw[4], vw1[4];
-    {
-      const uint4 v0 = *reinterpret_cast<const uint4*>(R + VCODES + 16 * lane);
-      vw[0] = v0.x; vw[1] = v0.y; vw[2] = v0.z; vw[3] = v0.w;
-      if (BITS == 2) {
-        const uint4 v1 = *reinterpret_cast<const uint4*>(R + VCODES + 512 + 16 * lane);
-        vw1[0] = v1.x; vw1[1] = v1.y; vw1[2] = v1.z; vw1[3] = v1.w;
-      }
-    }
-#pragma unroll
-    for (int c16 = 0; c16 < 2; ++c16) {
-      const float ps[4] = {p[2 * c16][0], p[2 * c16][1], p[2 * c16 + 1][0], p[2 * c16 + 1][1]};
-      float4 zz[4], ss[4];  // zz[slot] over cg, ss[cg] over slot
-#pragma unroll
-      for (int slot = 0; slot < 4; ++slot) {
-        zz[slot] = vzs[kZsPitch * t + 2 * (4 * c16 + slot)];
-        ss[slot] = vzs[kZsPitch * t + 2 * (4 * c16 + slot) + 1];
-        const float2 pp = make_float2(ps[slot], ps[slot]);
-        zacc01 = f2_fma(pp, make_float2(zz[slot].x, zz[slot].y), zacc01);
-        zacc23 = f2_fma(pp, make_float2(zz[slot].z, zz[slot].w), zacc23);
-      }
-      uint32_t bfr[4][2];
-      {
-        const float2 p01 = make_float2(ps[0], ps[1]), p23 = make_float2(ps[2], ps[3]);
-        float2 x;
-#pragma unroll
-        for (int cg = 0; cg < 4; ++cg) {  // ss[cg]: the scales of slots 0..3 at channel group cg
-          x = f2_mul(p01, make_float2(ss[cg].x, ss[cg].y)); bfr[cg][0] = pack_f16x2(x.x, x.y);
-          x = f2_mul(p23, make_float2(ss[cg].z, ss[cg].w)); bfr[cg][1] = pack_f16x2(x.x, x.y);
-        }
-      }
-      {
-        const uint32_t wa = vw[2 * c16], wb = vw[2 * c16 + 1];
-        const uint32_t a5 = __funnelshift_l(wa, wa, 5), a10 = __funnelshift_l(wa, wa, 10),
-                       a31 = __funnelshift_l(wa, wa, 31);
-        const uint32_t b5 = __funnelshift_l(wb, wb, 5), b10 = __funnelshift_l(wb, wb, 10),
-                       b31 = __funnelshift_l(wb, wb, 31);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t af[4] = {bit_pair_exp(wa, a5, a10, a31, 2 * mt), bit_pair_exp(wa, a5, a10, a31, 2 * mt + 1),
-                                  bit_pair_exp(wb, b5, b10, b31, 2 * mt), bit_pair_exp(wb, b5, b10, b31, 2 * mt + 1)};
-          mma_16816(oacc[mt], af, bfr[mt >> 1][0], bfr[mt >> 1][1]);
-        }
-      }
-      if (BITS == 2) {  // high plane: weight 2, carried by doubling B
-        uint32_t bfr2[4][2];
-#pragma unroll
-        for (int cg = 0; cg < 4; ++cg) {
-          bfr2[cg][0] = hadd2_u32(bfr[cg][0], bfr[cg][0]);
-          bfr2[cg][1] = hadd2_u32(bfr[cg][1], bfr[cg][1]);
-        }
-        const uint32_t xa = vw1[2 * c16], xb = vw1[2 * c16 + 1];
-        const uint32_t a5 = __funnelshift_l(xa, xa, 5), a10 = __funnelshift_l(xa, xa, 10),
-                       a31 = __funnelshift_l(xa, xa, 31);
-        const uint32_t b5 = __funnelshift_l(xb, xb, 5), b10 = __funnelshift_l(xb, xb, 10),
-                       b31 = __funnelshift_l(xb, xb, 31);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t af[4] = {bit_pair_exp(xa, a5, a10, a31, 2 * mt), bit_pair_exp(xa, a5, a10, a31, 2 * mt + 1),
-                                  bit_pair_exp(xb, b5, b10, b31, 2 * mt), bit_pair_exp(xb, b5, b10, b31, 2 * mt + 1)};
-          mma_16816(oacc[mt], af, bfr2[mt >> 1][0], bfr2[mt >> 1][1]);
-        }
-      }
-    }
-    __syncwarp();
-  }
-  cp_async_wait<0>();
-  // pre-fetch rows this warp's groups did not carry, four host reads in flight at a time
-  for (int i0 = pf_carried; i0 < n_pf; i0 += 4) {
-    int64_t rr[4];
-    int n[4];
-    uint4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      rr[u] = slot + n_slots * (i0 + u);
-      n[u] = i0 + u < n_pf ? a.pf_idx[rr[u]] : -1;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (n[u] >= 0 && n[u] < a.pf_ncap)
-        v[u] = reinterpret_cast<const uint4*>(a.pf_host + ((rr[u] / a.pf_k) * a.pf_ncap + n[u]) * (2 * kD))[lane];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (n[u] >= 0 && n[u] < a.pf_ncap) reinterpret_cast<uint4*>(a.pf_staging + rr[u] * (2 * kD))[lane] = v[u];
-  }
-  // undo the powers of two of the value-bit expansion, per channel
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    oacc[mt][0] *= bit_comp(2 * mt);
-    oacc[mt][1] *= bit_comp(2 * mt);
-    oacc[mt][2] *= bit_comp(2 * mt + 1);
-    oacc[mt][3] *= bit_comp(2 * mt + 1);
-  }
-  __syncthreads();  // the merge buffer overlaps the stages of every warp
-
-  // ---- warp state -> shared memory ----
-  l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
-  l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 2);
-  float zacc[4] = {zacc01.x, zacc01.y, zacc23.x, zacc23.y};
-#pragma unroll
-  for (int cg = 0; cg < 4; ++cg) {
-    zacc[cg] += __shfl_xor_sync(0xFFFFFFFFu, zacc[cg], 1);
-    zacc[cg] += __shfl_xor_sync(0xFFFFFFFFu, zacc[cg], 2);
-  }
-  if (t == 0) {
-    merge.m[warp][gid] = m_run;
-    merge.l[warp][gid] = l_run;
-  }
-  // oacc[mt]: (channel 16mt+gid, row 2t), (16mt+gid, 2t+1), (16mt+gid+8, 2t), (16mt+gid+8, 2t+1)
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    merge.o[warp][2 * t][16 * mt + gid] = oacc[mt][0];
-    merge.o[warp][2 * t + 1][16 * mt + gid] = oacc[mt][1];
-    merge.o[warp][2 * t][16 * mt + gid + 8] = oacc[mt][2];
-    merge.o[warp][2 * t + 1][16 * mt + gid + 8] = oacc[mt][3];
-  }
-  __syncwarp();
-  // the p*z term of row gid: zacc[cg] applies to channels 32cg .. 32cg+31
-#pragma unroll
-  for (int cg = 0; cg < 4; ++cg)
-#pragma unroll
-    for (int q8 = 0; q8 < 8; ++q8) merge.o[warp][gid][32 * cg + 8 * t + q8] += zacc[cg];
-}
-
-// ------------------------------------------------------------ merge + combine
-
-// Output row and log-sum-exp of query row rho of (b, hkv) bh from its merged
-// softmax state (max M, sum L, unnormalised output O at channel c).
-__device__ __forceinline__ void write_row(const AttnArgs& a, int64_t bh, int rho, float M, float L, float O, int c) {
-  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
-  const int qi = rho / G, gi = rho % G;
-  const int64_t orow = ((int64_t)b * 2 + qi) * a.Hq + hk * G + gi;
-  a.out[orow * kD + c] = f32_to_bf16_rne(L > 0.f ? O / L : 0.f);
-  if (c == 0 && a.lse != nullptr) a.lse[orow] = L > 0.f ? (M + __log2f(L)) * CUDART_LN2_F : -CUDART_INF_F;
-}
-
-// The CTA's partial from its warps' states: per query row the max over the
-// slots, then the sum and the output at channel c in slot order.  The rows
-// are independent: unrolled, their dependent chains interleave.
-__device__ __forceinline__ void cta_merge_rows(const CtaMerge& sm, int rows, int c, float* dst) {
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho) {
-    if (rho < rows) {
-      float M = kNeg;
-#pragma unroll
-      for (int w = 0; w < kSlots; ++w) M = fmaxf(M, sm.m[w][rho]);
-      float L = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < kSlots; ++w) {
-        const float f = fast_exp2(sm.m[w][rho] - M);
-        L += sm.l[w][rho] * f;
-        O += sm.o[w][rho][c] * f;
-      }
-      float* pr = dst + rho * kPartStride;
-      if (c == 0) {
-        pr[0] = M;
-        pr[1] = L;
-      }
-      pr[4 + c] = O;
-    }
-  }
-}
-
-// Returns whether this CTA was the last of its (b, hkv) and so combined the
-// partials.  part_cap: partials that fit in the CTA's dynamic shared memory
-// (which starts with the merge buffer `sm`).
-__device__ __forceinline__ bool merge_store_combine(CtaMerge& sm, const AttnArgs& a, int* s_last, float* s_ml,
-                                                    float* s_w, int part_cap) {
-  __syncthreads();
-  const int c = threadIdx.x;  // channel
-  const int64_t bh = blockIdx.y;
-  const int rows = 2 * a.G;
-  const int nparts = a.chunks;
-  cta_merge_rows(sm, rows, c, a.part + ((bh * nparts + blockIdx.x) * kMaxRows) * kPartStride);
-  // combine_kernel runs after this grid.  A run-time flag on purpose: making
-  // it a template branch (so that the partial-only instantiations lose the
-  // code below) changed the register allocation of the pre-fetching variant
-  // and slowed it by a quarter.
-  if (a.ext_combine) return false;
-  // last CTA of this (b, hkv) merges every partial.  The barrier orders the
-  // CTA's partial before thread 0's fence and ticket (a fence is cumulative
-  // over what the barrier ordered before it); the fence after the ticket and
-  // the second barrier order the last CTA's reads after it.
-  __syncthreads();
-  if (c == 0) {
-    __threadfence();
-    *s_last = (atomicAdd(&a.tickets[bh], 1u) == (unsigned)(nparts - 1));
-    __threadfence();
-  }
-  __syncthreads();
-  if (!*s_last) return false;
-  const float* base = a.part + (bh * nparts * kMaxRows) * kPartStride;
-  if (nparts <= part_cap) {
-    // Every partial's used rows into shared memory (the merge buffer and the
-    // stages, free now) with one round of copies, then per query row the
-    // arithmetic of the clustered combine in the same order, so that both
-    // give identical results: thread rho finds row rho's max, sum and the
-    // partials' weights (computed once, shared), every thread its channel's
-    // output.
-    float* sp = reinterpret_cast<float*>(&sm);
-    const int per_part = rows * (kPartStride / 4);  // 16-byte pieces of one partial's used rows
-    for (int p = 0; p < nparts; ++p)
-      for (int e = c; e < per_part; e += kThreads)
-        cp_async16(sp + (p * kMaxRows * kPartStride) + 4 * e, base + (int64_t)p * kMaxRows * kPartStride + 4 * e);
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-    if (c < rows) {
-      float M = kNeg, L = 0.f;
-      for (int p = 0; p < nparts; ++p) M = fmaxf(M, sp[(p * kMaxRows + c) * kPartStride]);
-      for (int p = 0; p < nparts; ++p) {
-        const float* pr = sp + (p * kMaxRows + c) * kPartStride;
-        const float f = fast_exp2(pr[0] - M);
-        L += pr[1] * f;
-        s_w[p * kMaxRows + c] = f;
-      }
-      s_ml[c] = M;
-      s_ml[kMaxRows + c] = L;
-    }
-    __syncthreads();
-    float O[kMaxRows];
-#pragma unroll
-    for (int rho = 0; rho < kMaxRows; ++rho) O[rho] = 0.f;
-    for (int p = 0; p < nparts; ++p)
-#pragma unroll
-      for (int rho = 0; rho < kMaxRows; ++rho)
-        if (rho < rows) O[rho] += sp[(p * kMaxRows + rho) * kPartStride + 4 + c] * s_w[p * kMaxRows + rho];
-#pragma unroll
-    for (int rho = 0; rho < kMaxRows; ++rho)
-      if (rho < rows) write_row(a, bh, rho, s_ml[rho], s_ml[kMaxRows + rho], O[rho], c);
-    if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
-    return true;
-  }
-  // More partials than shared memory holds: two passes over (max, sum) blocks.
-  // The (max, sum) words of every partial into shared memory (the merge
-  // buffer, free now) in one round trip, 2 * kPCap (p, row) pairs at a time.
-  // Then, per query row c: the max and the sum over the partials in partial
-  // order (the same arithmetic as the clustered combine, so both give
-  // identical results); then every partial's output words, 4 partials' worth
-  // of independent loads at a time.
-  constexpr int kPCap = kSlots * kMaxRows * kMergePitch / (2 * kMaxRows);  // partials per block
-  float* sml = &sm.o[0][0][0];  // [p][row][2]
-  float M[kMaxRows], O[kMaxRows];
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho) {
-    M[rho] = kNeg;
-    O[rho] = 0.f;
-  }
-  // pass 1: the maxima
-  for (int p0 = 0; p0 < nparts; p0 += kPCap) {
-    const int np = min(kPCap, nparts - p0);
-    for (int i = c; i < np * kMaxRows; i += kThreads) {
-      const float* pr = base + ((int64_t)(p0 + i / kMaxRows) * kMaxRows + i % kMaxRows) * kPartStride;
-      sml[2 * i] = __ldcg(pr);
-      sml[2 * i + 1] = __ldcg(pr + 1);
-    }
-    __syncthreads();
-    if (c < rows) {
-      float m = p0 == 0 ? kNeg : s_ml[c];
-      for (int p = 0; p < np; ++p) m = fmaxf(m, sml[2 * (p * kMaxRows + c)]);
-      s_ml[c] = m;
-    }
-    __syncthreads();
-  }
-  if (nparts > kPCap) {  // the maxima are final only now: the sums in a second pass over the blocks
-    if (c < rows) s_ml[kMaxRows + c] = 0.f;
-    for (int p0 = 0; p0 < nparts; p0 += kPCap) {
-      const int np = min(kPCap, nparts - p0);
-      __syncthreads();
-      for (int i = c; i < np * kMaxRows; i += kThreads) {
-        const float* pr = base + ((int64_t)(p0 + i / kMaxRows) * kMaxRows + i % kMaxRows) * kPartStride;
-        sml[2 * i] = __ldcg(pr);
-        sml[2 * i + 1] = __ldcg(pr + 1);
-      }
-      __syncthreads();
-      if (c < rows) {
-        float l = s_ml[kMaxRows + c];
-        const float m = s_ml[c];
-        for (int p = 0; p < np; ++p) l += sml[2 * (p * kMaxRows + c) + 1] * fast_exp2(sml[2 * (p * kMaxRows + c)] - m);
-        s_ml[kMaxRows + c] = l;
-      }
-    }
-  } else if (c < rows) {
-    float l = 0.f;
-    const float m = s_ml[c];
-    for (int p = 0; p < nparts; ++p) l += sml[2 * (p * kMaxRows + c) + 1] * fast_exp2(sml[2 * (p * kMaxRows + c)] - m);
-    s_ml[kMaxRows + c] = l;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho) M[rho] = s_ml[rho];
-  for (int p0 = 0; p0 < nparts; p0 += 4) {
-    float ov[4][kMaxRows], mv[4][kMaxRows];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int rho = 0; rho < kMaxRows; ++rho) {
-        const bool in = p0 + u < nparts && rho < rows;
-        const float* pr = base + ((int64_t)(p0 + u) * kMaxRows + rho) * kPartStride;
-        ov[u][rho] = in ? __ldcg(pr + 4 + c) : 0.f;
-        mv[u][rho] = in ? __ldcg(pr) : kNeg;
-      }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int rho = 0; rho < kMaxRows; ++rho)
-        if (p0 + u < nparts && rho < rows) O[rho] += ov[u][rho] * fast_exp2(mv[u][rho] - M[rho]);
-  }
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho) {
-    if (rho >= rows) break;
-    write_row(a, bh, rho, M[rho], s_ml[kMaxRows + rho], O[rho], c);
-  }
-  if (c == 0) atomicExch(&a.tickets[bh], 0u);  // ready for the next call on this workspace
-  return true;
-}
-
-// ------------------------------------------------------------ fused ArgTopK
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-  return t;
-}
-
-constexpr uint64_t kWaitLimitNs = 20000000ull;  // 20 ms: a normal wait is a few microseconds
-
-// ArgTopK(A_{1,:}) at the end of the attention (SpeCache page, Algorithm 3):
-// the CTA that combined a (b, hkv) publishes its log-sum-exp; every CTA of the
-// (b, hkv) waits for it (bounded: on expiry it sets the fault word and goes
-// on), scores its own chunk's positions from the speculative logits it and its
-// siblings wrote, S(n) = sum_h 2^(log2e (l_h(n) - lse_h)), and keeps its
-// chunk's top-k' (k' = min(k, chunk length), ties to the lower position) as
-// candidates in the workspace.  The last CTA of the (b, hkv) to finish (a
-// second ticket) selects the final k from the candidates, which lie in
-// ascending position, and writes idx and the bitmap.  Every globally selected
-// position is among its chunk's candidates.
-template <int BITS>
-__device__ __forceinline__ void select_epilogue(const AttnArgs& a, uint8_t* dyn, SelShared<kThreads>& sh,
-                                                bool combined, int* s_flag, float* s_nlse) {
-  const int tid = threadIdx.x;
-  const int64_t bh = blockIdx.y;
-  const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
-  if (combined) {
-    if (tid == 0) {
-      __threadfence();  // the log-sum-exp this CTA wrote, then the flag
-      atomicExch(&a.ready[bh], 1u);
-    }
-  } else if (tid == 0) {
-    const uint64_t t0 = global_ns();
-    while (ld_acquire_gpu(&a.ready[bh]) == 0u) {
-      if (global_ns() - t0 > kWaitLimitNs) {
-        atomicOr(a.fault, 1u);
-        break;
-      }
-      __nanosleep(200);
-    }
-  }
-  __syncthreads();
-  if (tid < G) s_nlse[tid] = -__ldcg(a.lse + ((int64_t)b * 2 + 1) * a.Hq + hk * G + tid) * 1.4426950408889634f;
-  __syncthreads();
-
-  // ---- scores of this chunk's positions, then its candidates ----
-  const int gpc32 = a.groups_per_chunk * kGroup;
-  const int p0 = blockIdx.x * gpc32;
-  const int len = max(0, min(a.nq, p0 + gpc32) - p0);  // multiple of 32
-  uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
-  const float* lrow = a.spec_logits + (bh * G) * (int64_t)a.Lcap + p0;
-  for (int i = 4 * tid; i < len; i += 4 * kThreads) {
-    float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int gi = 0; gi < G; ++gi) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(lrow + (int64_t)gi * a.Lcap + i));
-      const float nl = s_nlse[gi];
-      sc.x += fast_exp2(fmaf(v.x, 1.4426950408889634f, nl));
-      sc.y += fast_exp2(fmaf(v.y, 1.4426950408889634f, nl));
-      sc.z += fast_exp2(fmaf(v.z, 1.4426950408889634f, nl));
-      sc.w += fast_exp2(fmaf(v.w, 1.4426950408889634f, nl));
-    }
-    *reinterpret_cast<uint4*>(keys + i) =
-        make_uint4(__float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
-  }
-  __syncthreads();
-  const int kloc = min(a.sel_keff, len);
-  if (kloc > 0) {
-    uint32_t* wgt = keys + len;
-    uint32_t* weq = wgt + (len >> 5);
-    uint32_t* cand = a.cand + ((bh * a.chunks + blockIdx.x) * (int64_t)a.cand_cap) * 2;
-    uint32_t T, need;
-    cta_radix_select<kThreads>(keys, len, (uint32_t)kloc, sh, T, need);
-    ordered_take<kThreads>(keys, len, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
-      cand[2 * r] = keys[i];
-      cand[2 * r + 1] = (uint32_t)(p0 + i);
-    });
-  }
-
-  // ---- the last CTA of the (b, hkv) merges the chunks' candidates ----
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) *s_flag = (atomicAdd(&a.tickets2[bh], 1u) == (unsigned)(a.chunks - 1));
-  __syncthreads();
-  if (!*s_flag) return;
-  __threadfence();
-  int M = 0;
-  for (int c = 0; c < a.chunks; ++c) M += min(a.sel_keff, max(0, min(a.nq, (c + 1) * gpc32) - c * gpc32));
-  const int nwq = a.nq >> 5;
-  uint32_t* mkey = reinterpret_cast<uint32_t*>(dyn);
-  uint32_t* mpos = mkey + M;
-  uint32_t* sbm = mpos + M;
-  uint32_t* wgt = sbm + nwq;
-  uint32_t* weq = wgt + ((M + 31) >> 5);
-  for (int c = 0, off = 0; c < a.chunks; ++c) {
-    const int cnt = min(a.sel_keff, max(0, min(a.nq, (c + 1) * gpc32) - c * gpc32));
-    const uint32_t* cand = a.cand + ((bh * a.chunks + c) * (int64_t)a.cand_cap) * 2;
-    for (int i = tid; i < cnt; i += kThreads) {
-      const uint2 kv = __ldcg(reinterpret_cast<const uint2*>(cand) + i);
-      mkey[off + i] = kv.x;
-      mpos[off + i] = kv.y;
-    }
-    off += cnt;
-  }
-  for (int w = tid; w < nwq; w += kThreads) sbm[w] = 0u;
-  __syncthreads();
-  int32_t* out = a.sel_idx + bh * a.sel_k;
-  if (a.sel_keff > 0) {
-    uint32_t T, need;
-    cta_radix_select<kThreads>(mkey, M, (uint32_t)a.sel_keff, sh, T, need);
-    ordered_take<kThreads>(mkey, M, T, need, wgt, weq, sh, [&](int i, uint32_t r) {
-      const uint32_t p = mpos[i];
-      out[r] = (int32_t)p;
-      atomicOr(&sbm[p >> 5], 1u << (p & 31u));
-    });
-  }
-  for (int j = a.sel_keff + tid; j < a.sel_k; j += kThreads) out[j] = -1;
-  uint32_t* bm = a.sel_bitmap + bh * a.q_groups_cap;
-  for (int w = tid; w < a.q_groups_cap; w += kThreads) bm[w] = w < nwq ? sbm[w] : 0u;
-  if (tid == 0) {  // every CTA of this (b, hkv) is past its wait: ready for the next call
-    atomicExch(&a.ready[bh], 0u);
-    atomicExch(&a.tickets2[bh], 0u);
-  }
-}
-
-// Clustered combine: when all CTAs of a (b, hkv) form one thread-block
-// cluster, each keeps its partial in shared memory and, after a cluster
-// barrier, CTA r merges query row r (r, r + chunks, ...) from every CTA's
-// partial through distributed shared memory: no partials in global memory,
-// no fences, no ticket.
-__device__ __forceinline__ void cluster_combine(CtaMerge& sm, const AttnArgs& a, float* cpart) {
-  namespace cgx = cooperative_groups;
-  cgx::cluster_group cluster = cgx::this_cluster();
-  __syncthreads();
-  const int c = threadIdx.x;  // channel
-  const int rows = 2 * a.G;
-  cta_merge_rows(sm, rows, c, cpart);
-  cluster.sync();
-  const unsigned n = cluster.num_blocks();
-  const int64_t bh = blockIdx.y;
-  for (int rho = (int)cluster.block_rank(); rho < rows; rho += (int)n) {
-    float M = kNeg;
-    for (unsigned p = 0; p < n; ++p) M = fmaxf(M, cluster.map_shared_rank(cpart, p)[rho * kPartStride]);
-    float L = 0.f, O = 0.f;
-#pragma unroll 4
-    for (unsigned p = 0; p < n; ++p) {
-      const float* pr = cluster.map_shared_rank(cpart, p) + rho * kPartStride;
-      const float f = fast_exp2(pr[0] - M);
-      L += pr[1] * f;
-      O += pr[4 + c] * f;
-    }
-    write_row(a, bh, rho, M, L, O, c);
-  }
-  cluster.sync();  // every CTA's partial stays readable until all rows are merged
-}
-
-template <int BITS, bool MERGED, bool FETCH, bool TOPK, bool CLUSTER>
-__global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
-  extern __shared__ __align__(16) uint8_t dyn_smem[];
-  __shared__ int s_last;
-  static_assert(sizeof(SelShared<kThreads>) <= kMaxRows * kTilePitch * sizeof(float),
-                "the selection's shared state reuses the query tile");
-  __shared__ float s_ml[2 * kMaxRows];
-  __shared__ float s_w[kMaxCluster * kMaxRows];  // the combine's partial weights
-  __shared__ __align__(16) float s_q[kMaxRows * kTilePitch];
-  CtaMerge& merge = *reinterpret_cast<CtaMerge*>(dyn_smem);
-  grid_dependency_sync();  // nothing is read or written before the previous kernel is done
-  auto fill_query = [&]() {
-    // scaled query rows of this (b, hkv): rho = i * G + gi for token i, head gi
-    const int64_t bh = blockIdx.y;
-    const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
-    for (int e = threadIdx.x; e < kMaxRows * kD / 4; e += kThreads) {
-      const int rho = e / (kD / 4), c4 = e % (kD / 4);
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (rho < 2 * G) {
-        const int qi = rho / G, gi = rho % G;
-        const uint2 qq = reinterpret_cast<const uint2*>(a.q + (((int64_t)b * 2 + qi) * a.Hq + hk * G + gi) * kD)[c4];
-        v = make_float4(bf16_to_f32(qq.x & 0xFFFFu) * a.qscale, bf16_to_f32(qq.x >> 16) * a.qscale,
-                        bf16_to_f32(qq.y & 0xFFFFu) * a.qscale, bf16_to_f32(qq.y >> 16) * a.qscale);
-      }
-      *reinterpret_cast<float4*>(s_q + rho * kTilePitch + 4 * c4) = v;
-    }
-    __syncthreads();
-  };
-  lowbit_cta<BITS, MERGED, FETCH>(a, dyn_smem, s_q, merge, fill_query);
-  if constexpr (CLUSTER) {
-    cluster_combine(merge, a, reinterpret_cast<float*>(dyn_smem + kClusterPartOffset));
-    return;
-  }
-  constexpr int kPartCap = attn_dyn_bytes<BITS>() / (int)(kMaxRows * kPartStride * sizeof(float));
-  static_assert(kPartCap <= kMaxCluster, "the combine's weight table holds kMaxCluster partials");
-  const bool combined = merge_store_combine(merge, a, &s_last, s_ml, s_w, kPartCap);
-  if constexpr (TOPK) {
-    __syncthreads();  // the query tile and the merge buffer are free from here on
-    select_epilogue<BITS>(a, dyn_smem, *reinterpret_cast<SelShared<kThreads>*>(s_q), combined, &s_last, s_ml);
-  }
-}
 
 // ------------------------------------------------------------ combine kernel
 // Query row blockIdx.x of (b, hkv) blockIdx.y from the partials that every
@@ -1221,55 +79,30 @@ static cudaError_t launch_combine(const AttnArgs& a, int64_t BH, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
-
+static const AttnVariant& variant(const spc_dims* d) {
+  if (d->bits == 1) return d->group == 64 ? attn_variant_b1g64() : attn_variant_b1g32();
+  return d->group == 64 ? attn_variant_b2g64() : attn_variant_b2g32();
+}
 
 struct AttnPlan {
   int chunks;
-  int groups_per_chunk;
+  int groups_per_chunk;  // 32-token groups per CTA (a multiple of the record's halves)
 };
 
-static int attn_smem_bytes(int bits) { return bits == 1 ? attn_dyn_bytes<1>() : attn_dyn_bytes<2>(); }
-
-// Resident attention CTAs per SM on the current device (occupancy query,
-// cached per device, bit width and fetch variant).
-template <int BITS, bool FETCH>
-static int resident_ctas() {
-  static int cached[64] = {};
-  static unsigned long long configured = 0ull;
-  const int dev = spc_host::current_device();
-  if (dev >= 0 && dev < 64) {
-    const int c = __atomic_load_n(&cached[dev], __ATOMIC_ACQUIRE);
-    if (c > 0) return c;
-  }
-  int n = 0;
-  const int smem = attn_smem_bytes(BITS);
-  cudaError_t e = spc_host::ensure_smem_limit(configured, attn_kernel<BITS, true, FETCH, false, false>, smem);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<BITS, true, FETCH, false, false>, kThreads, smem);
-  if (e != cudaSuccess || n <= 0) {
-    cudaGetLastError();
-    n = 2;
-  }
-  if (dev >= 0 && dev < 64) __atomic_store_n(&cached[dev], n, __ATOMIC_RELEASE);
-  return n;
-}
-
-static int resident_ctas(int bits, bool fetch) {
-  if (bits == 1) return fetch ? resident_ctas<1, true>() : resident_ctas<1, false>();
-  return fetch ? resident_ctas<2, true>() : resident_ctas<2, false>();
-}
-
-// One wave of resident CTAs over B*Hkv, at least four groups (one per warp)
+// One wave of resident CTAs over B*Hkv, at least four records (one per warp)
 // each.  The 16-bit rows ride on the same CTAs, whatever their number.
 static AttnPlan attn_plan(const spc_dims* d, bool fetch) {
-  const int ng = num_quantized(d->N, d->R, d->group) / kGroup;
+  const int nh = d->group / kGroup;  // 32-token halves per record
+  const int nu = num_quantized(d->N, d->R, d->group) / d->group;
   const int64_t BH = (int64_t)d->B * d->Hkv;
-  AttnPlan p{1, 1};
-  if (ng > 0) {
-    const int64_t slots = (int64_t)spc_host::sm_count() * resident_ctas(d->bits, fetch);
+  AttnPlan p{1, nh};
+  if (nu > 0) {
+    const int64_t slots = (int64_t)spc_host::sm_count() * variant(d).resident_ctas(fetch);
     int64_t chunks = std::max<int64_t>(1, slots / BH);
-    chunks = std::min<int64_t>(chunks, (ng + kWarps - 1) / kWarps);
-    p.groups_per_chunk = (int)((ng + chunks - 1) / chunks);
-    p.chunks = (ng + p.groups_per_chunk - 1) / p.groups_per_chunk;
+    chunks = std::min<int64_t>(chunks, (nu + kWarps - 1) / kWarps);
+    const int upc = (int)((nu + chunks - 1) / chunks);
+    p.chunks = (nu + upc - 1) / upc;
+    p.groups_per_chunk = upc * nh;
   }
   return p;
 }
@@ -1312,115 +145,17 @@ size_t step_workspace_bytes(const spc_dims* d, int32_t k_max) {
   return control_bytes(d) + parts_bytes(d) + cand_bytes(d, k_max);
 }
 
-template <int BITS, bool MERGED, bool FETCH, bool TOPK, bool CLUSTER>
-static cudaError_t launch_attn(const AttnArgs& a, int64_t BH, cudaStream_t stream) {
-  const int smem = attn_smem_bytes(BITS);
-  static_assert((int)sizeof(CtaMerge) <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
-                "merge buffer fits in the dynamic shared memory");
-  static_assert(kClusterPartOffset + kMaxRows * kPartStride * 4 <= kWarps * (Stages<2>::value * 3600 + kZsBytes) &&
-                    kClusterPartOffset + kMaxRows * kPartStride * 4 <= kWarps * (Stages<1>::value * 2576 + kZsBytes),
-                "the clustered combine's partial fits behind the merge buffer");
-  static_assert(kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= (Stages<1>::value - 1) * 2576 + kZsBytes &&
-                    kRowBatch * 512 + kRowBatch * kMaxRows * 4 <= (Stages<2>::value - 1) * 3600 + kZsBytes &&
-                    kMaxRows * kTilePitch * 4 <= 2576 + kZsBytes,
-                "16-bit row batch and transfer tile fit in a warp's stages after the first and its z/s table");
-  auto* fn = attn_kernel<BITS, MERGED, FETCH, TOPK, CLUSTER>;
-  static unsigned long long configured = 0ull;  // one per instantiation
-  cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
-  if (e != cudaSuccess) return e;
-  // programmatic serialisation: the launch overlaps the previous kernel's tail
-  // (the kernel waits for it before touching any data); clustered: the CTAs of
-  // a (b, hkv) form one cluster
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.chunks, (unsigned)BH, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = (unsigned)a.chunks;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = CLUSTER ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, fn, a);
-}
-
-// Whether the CTAs of every (b, hkv) can form one cluster (at most
-// kMaxCluster CTAs) with all B*Hkv clusters resident at once (occupancy query,
-// cached per device and cluster size).
-template <int BITS, bool MERGED, bool FETCH>
-static bool cluster_fits(int chunks, int64_t BH) {
-  if (chunks < 2 || chunks > kMaxCluster) return false;
-  static int cached[64][kMaxCluster + 1] = {};  // 0 unknown, else 1 + resident clusters
-  static unsigned long long configured = 0ull, nonportable = 0ull;
-  const int dev = spc_host::current_device();
-  if (dev >= 0 && dev < 64) {
-    const int c = __atomic_load_n(&cached[dev][chunks], __ATOMIC_ACQUIRE);
-    if (c > 0) return (int64_t)(c - 1) >= BH;
-  }
-  auto* fn = attn_kernel<BITS, MERGED, FETCH, false, true>;
-  const int smem = attn_smem_bytes(BITS);
-  int n = 0;
-  cudaError_t e = spc_host::ensure_smem_limit(configured, fn, smem);
-  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
-  if (e == cudaSuccess && chunks > 8 && !(__atomic_load_n(&nonportable, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess && bit != 0ull) __atomic_fetch_or(&nonportable, bit, __ATOMIC_ACQ_REL);
-  }
-  if (e == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)chunks, (unsigned)BH, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)chunks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
-  }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    n = 0;
-  }
-  if (dev >= 0 && dev < 64) __atomic_store_n(&cached[dev][chunks], n + 1, __ATOMIC_RELEASE);
-  return (int64_t)n >= BH;
-}
-
 // The clustered combine, when every (b, hkv)'s CTAs fit one cluster and all
 // clusters are resident in one wave.
-static bool use_cluster(int bits, bool merged, bool fetch, int chunks, int64_t BH) {
-  if (bits == 1)
-    return merged ? (fetch ? cluster_fits<1, true, true>(chunks, BH) : cluster_fits<1, true, false>(chunks, BH))
-                  : (fetch ? cluster_fits<1, false, true>(chunks, BH) : cluster_fits<1, false, false>(chunks, BH));
-  return merged ? (fetch ? cluster_fits<2, true, true>(chunks, BH) : cluster_fits<2, true, false>(chunks, BH))
-                : (fetch ? cluster_fits<2, false, true>(chunks, BH) : cluster_fits<2, false, false>(chunks, BH));
-}
-
-// The attention launch: with the fused selection (its last CTA per (b, hkv)
-// combines), clustered (the CTAs combine through distributed shared memory),
-// or else followed by combine_kernel (a.ext_combine).
-template <int BITS, bool MERGED, bool TOPK>
-static cudaError_t launch_attn_f(const AttnArgs& a, int64_t BH, cudaStream_t stream, bool fetch, bool clustered) {
-  if (!TOPK && clustered)
-    return fetch ? launch_attn<BITS, MERGED, true, false, true>(a, BH, stream)
-                 : launch_attn<BITS, MERGED, false, false, true>(a, BH, stream);
-  cudaError_t e = fetch ? launch_attn<BITS, MERGED, true, TOPK, false>(a, BH, stream)
-                        : launch_attn<BITS, MERGED, false, TOPK, false>(a, BH, stream);
-  if (e == cudaSuccess && a.ext_combine) e = launch_combine(a, BH, stream);
-  return e;
+static bool use_cluster(const spc_dims* d, bool merged, bool fetch, int chunks, int64_t BH) {
+  return variant(d).cluster_fits(merged, fetch, chunks, BH);
 }
 
 // The fused selection works in the attention's dynamic shared memory: a
 // chunk's keys and word counts, then the leader's merge of every chunk's
 // candidates and the bitmap.
 static bool select_fits(const spc_dims* d, const AttnPlan& p, int32_t k_sel) {
-  const int64_t words = attn_smem_bytes(d->bits) / 4;
+  const int64_t words = variant(d).smem / 4;
   const int64_t nq = num_quantized(d->N, d->R, d->group);
   const int64_t len = (int64_t)p.groups_per_chunk * kGroup;
   const int64_t M = (int64_t)p.chunks * cand_cap(d, p, k_sel);
@@ -1463,6 +198,7 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.nq = num_quantized(d->N, d->R, d->group);
   a.r = d->N - a.nq;
   a.q_groups_cap = d->q_groups_cap;
+  a.units_cap = d->group == 64 ? (d->q_groups_cap + 1) / 2 : d->q_groups_cap;
   a.resid_cap = d->resid_cap;
   a.chunks = plan.chunks;
   a.groups_per_chunk = plan.groups_per_chunk;
@@ -1479,24 +215,10 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.sel_k = topk ? sel->k : 0;
   a.sel_keff = topk ? std::min(sel->k, a.nq) : 0;
   a.cand_cap = topk ? cand_cap(d, plan, sel->k) : 0;
-  const bool clustered = !topk && use_cluster(d->bits, merged, fetch, a.chunks, BH);
+  const bool clustered = !topk && use_cluster(d, merged, fetch, a.chunks, BH);
   a.ext_combine = !topk && !clustered;
-  cudaError_t e;
-  if (d->bits == 1) {
-    if (topk)
-      e = launch_attn_f<1, true, true>(a, BH, stream, fetch, clustered);
-    else if (merged)
-      e = launch_attn_f<1, true, false>(a, BH, stream, fetch, clustered);
-    else
-      e = launch_attn_f<1, false, false>(a, BH, stream, fetch, clustered);
-  } else {
-    if (topk)
-      e = launch_attn_f<2, true, true>(a, BH, stream, fetch, clustered);
-    else if (merged)
-      e = launch_attn_f<2, true, false>(a, BH, stream, fetch, clustered);
-    else
-      e = launch_attn_f<2, false, false>(a, BH, stream, fetch, clustered);
-  }
+  cudaError_t e = variant(d).launch(a, BH, stream, merged, fetch, topk, clustered);
+  if (e == cudaSuccess && a.ext_combine) e = launch_combine(a, BH, stream);
   if (e != cudaSuccess) {
     spc_host::set_cuda_error(e);
     return SPC_ERR_CUDA;
@@ -1510,7 +232,7 @@ int attn_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k) {
   const int64_t BH = (int64_t)d->B * d->Hkv;
   const bool fetch = BH * fetch_k > 0;
   const AttnPlan plan = attn_plan(d, fetch);
-  return use_cluster(d->bits, k > 0, fetch, plan.chunks, BH) ? 1 : 2;
+  return use_cluster(d, k > 0, fetch, plan.chunks, BH) ? 1 : 2;
 }
 
 // Kernels of one spc_decode_step: one when the selection rides on the

@@ -20,7 +20,16 @@ __host__ __device__ inline int32_t num_quantized(int32_t N, int32_t R, int32_t g
   return N > R ? ((N - R) / group) * group : 0;
 }
 
-__host__ __device__ inline int64_t record_bytes(int32_t bits) { return 1024 * (int64_t)(bits + 1); }
+// Bytes of one record of the low-bit copy: a 32-token group at g = 32; a
+// 64-token group at g = 64, its two halves' code planes with the group's
+// metadata stored once.
+__host__ __device__ inline int64_t record_bytes(int32_t bits, int32_t group = 32) {
+  return group == 64 ? 2048 * (int64_t)bits + 1024 : 1024 * (int64_t)(bits + 1);
+}
+// Records per (b, hkv) for a capacity of q_groups_cap 32-token groups.
+__host__ __device__ inline int32_t records_cap(int32_t group, int32_t q_groups_cap) {
+  return group == 64 ? (q_groups_cap + 1) / 2 : q_groups_cap;
+}
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 

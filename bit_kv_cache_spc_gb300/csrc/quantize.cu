@@ -72,7 +72,7 @@ struct QuantArgs {
   const uint16_t* k;
   const uint16_t* v;
   uint8_t* records;
-  int32_t Hkv, N, nq, q_groups_cap;
+  int32_t Hkv, N, nq, q_groups_cap, units_cap;
   int64_t total_groups;  // B * Hkv * (nq / group): the kernel's units of work
 };
 
@@ -94,13 +94,22 @@ __device__ __forceinline__ int vmeta_word(int n, int cg) {
   const int n16 = n & 15;
   return 32 * ((n16 & 7) >> 1) + 16 * (n >> 4) + 4 * (2 * (n16 >> 3) + (n16 & 1)) + cg;
 }
+// At g = 64 a half's 64 value-minmax words hold token n's (min, max) of
+// channels 64c .. 64c+63 at word 2m + c, where m = 8 ((n >> 1) & 3) +
+// 4 (n >> 4) + 2 ((n >> 3) & 1) + (n & 1) is the lane that reads token n.
+__device__ __forceinline__ int vmeta64_word(int n, int c) {
+  return 2 * (8 * ((n >> 1) & 3) + 4 * (n >> 4) + 2 * ((n >> 3) & 1) + (n & 1)) + c;
+}
 
 // Codes one 32-token group from the tiles ks, vs ([token][channel] bf16 in
-// shared memory) into its record at dst.  Every thread of the 128-thread CTA
-// takes part; the tiles may be reused once this returns.
+// shared memory) into its record at dst.  At g = 64 the tiles are half `half`
+// of a 64-token group (ks_other the other half's keys) and dst its record:
+// this half's code planes go there, with the keys' (min, max) words (written
+// by half 0) and this half's value (min, max) words.  Every thread of the
+// 128-thread CTA takes part; the tiles may be reused once this returns.
 template <int BITS, int GROUP>
 __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, const uint16_t* vs,
-                                           const uint16_t* ks_other, uint8_t* dst_rec) {
+                                           const uint16_t* ks_other, uint8_t* dst_rec, int half_of_64 = 0) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int rb = 1024 * (BITS + 1);
   constexpr int KMETA = 128 * BITS, VCODES = KMETA + 128, VMETA = VCODES + 128 * BITS;  // in words
@@ -193,8 +202,10 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
     float z, s;
     quant_params(BITS, lo, hi, z, s);
     const float rs = quant_recip(s);
-    if ((lane & 3) == 0)
+    if (GROUP == 32 && (lane & 3) == 0)
       sm.rec[VMETA + vmeta_word(n, kk >> 1)] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
+    if (GROUP == 64 && (lane & 7) == 0)
+      sm.rec[VMETA + vmeta64_word(n, kk >> 2)] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
     const int t = p & 3, j = 2 * (p >> 3) + ((p >> 2) & 1);
 #pragma unroll
     for (int aa = 0; aa < 8; ++aa) {  // channel kblock + aa = 16 k + 8 h + a
@@ -246,7 +257,17 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
   // ---- the record out, coalesced ----
   uint4* dst = reinterpret_cast<uint4*>(dst_rec);
   const uint4* src = reinterpret_cast<const uint4*>(sm.rec);
-  for (int i = tid; i < rb / 16; i += 128) __stcs(dst + i, src[i]);
+  if constexpr (GROUP == 32) {
+    for (int i = tid; i < rb / 16; i += 128) __stcs(dst + i, src[i]);
+  } else {  // in 16-byte units: K codes of half h at 32 BITS h, K minmax at 64 BITS, V codes of half h at
+            // 64 BITS + 32 + 32 BITS h, V minmax of half h at 128 BITS + 32 + 16 h
+    const int h = half_of_64;
+    for (int i = tid; i < 32 * BITS; i += 128) __stcs(dst + 32 * BITS * h + i, src[i]);
+    if (h == 0)
+      for (int i = tid; i < 32; i += 128) __stcs(dst + 64 * BITS + i, src[32 * BITS + i]);
+    for (int i = tid; i < 32 * BITS; i += 128) __stcs(dst + 64 * BITS + 32 + 32 * BITS * h + i, src[32 * BITS + 32 + i]);
+    for (int i = tid; i < 16; i += 128) __stcs(dst + 128 * BITS + 32 + 16 * h + i, src[64 * BITS + 32 + i]);
+  }
   __syncthreads();  // the record buffer is reused by the next group
 }
 
@@ -277,9 +298,9 @@ __global__ void __launch_bounds__(128) quantize_kernel(QuantArgs a) {
       cp_async_commit();
       cp_async_wait<0>();
       __syncthreads();
-      uint8_t* rec = a.records + (bh * a.q_groups_cap + 2 * g) * (int64_t)rb;
-      code_group<BITS, 64>(sm, sm.tile[0][0], sm.tile[0][1], sm.tile[1][0], rec);
-      code_group<BITS, 64>(sm, sm.tile[1][0], sm.tile[1][1], sm.tile[0][0], rec + rb);  // ends with a barrier: tiles free
+      uint8_t* rec = a.records + (bh * a.units_cap + g) * record_bytes(BITS, 64);
+      code_group<BITS, 64>(sm, sm.tile[0][0], sm.tile[0][1], sm.tile[1][0], rec, 0);
+      code_group<BITS, 64>(sm, sm.tile[1][0], sm.tile[1][1], sm.tile[0][0], rec, 1);  // ends with a barrier: tiles free
     }
     return;
   }
@@ -372,6 +393,7 @@ spc_status launch_quantize(const spc_dims* d, const uint16_t* k, const uint16_t*
     a.N = d->N;
     a.nq = nq;
     a.q_groups_cap = d->q_groups_cap;
+    a.units_cap = records_cap(d->group, d->q_groups_cap);
     a.total_groups = BH * (nq / d->group);
     if (d->group == 64)
       e = d->bits == 1 ? launch_quantize_bits<1, 64>(a, stream) : launch_quantize_bits<2, 64>(a, stream);
@@ -406,7 +428,7 @@ struct AppendArgs {
   uint16_t* resid;        // [B][Hkv][resid_cap][2][D]
   uint16_t* host;         // device address of [B][Hkv][n_cap][2][D], or null
   int64_t n_cap;
-  int32_t N, nq, r, resid_cap, q_groups_cap, flush;
+  int32_t N, nq, r, resid_cap, q_groups_cap, units_cap, flush;
 };
 
 template <int BITS, int GROUP>
@@ -431,10 +453,9 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
     else reinterpret_cast<uint4*>(sm.tile[tile][1] + row * kD)[q - 16] = v;
   }
   __syncthreads();
-  constexpr int rb = 1024 * (BITS + 1);
-  uint8_t* rec = a.records + (bh * a.q_groups_cap + a.nq / kGroup) * (int64_t)rb;
-  code_group<BITS, GROUP>(sm, sm.tile[0][0], sm.tile[0][1], sm.tile[1][0], rec);
-  if (GROUP == 64) code_group<BITS, GROUP>(sm, sm.tile[1][0], sm.tile[1][1], sm.tile[0][0], rec + rb);
+  uint8_t* rec = a.records + (bh * a.units_cap + a.nq / GROUP) * record_bytes(BITS, GROUP);
+  code_group<BITS, GROUP>(sm, sm.tile[0][0], sm.tile[0][1], sm.tile[1][0], rec, 0);
+  if (GROUP == 64) code_group<BITS, GROUP>(sm, sm.tile[1][0], sm.tile[1][1], sm.tile[0][0], rec, 1);
   // rows g .. r move to 0 .. r-g, 32 rows at a time: a chunk's sources lie
   // past every destination written before it, and it is read in full before
   // it is written
@@ -480,6 +501,7 @@ spc_status launch_append(const spc_dims* d, const uint16_t* k_new, const uint16_
   a.r = d->N - a.nq;
   a.resid_cap = d->resid_cap;
   a.q_groups_cap = d->q_groups_cap;
+  a.units_cap = records_cap(d->group, d->q_groups_cap);
   a.flush = num_quantized(d->N + 1, d->R, d->group) > a.nq ? 1 : 0;
   const int64_t BH = (int64_t)d->B * d->Hkv;
   if (BH == 0) return SPC_OK;

@@ -161,8 +161,11 @@ int32_t spc_num_quantized(const spc_dims* d) {
 }
 
 size_t spc_records_bytes(const spc_dims* d) {
-  if (d == nullptr || d->B <= 0 || d->Hkv <= 0 || d->q_groups_cap < 0 || (d->bits != 1 && d->bits != 2)) return 0;
-  return (size_t)d->B * d->Hkv * d->q_groups_cap * (size_t)spc::record_bytes(d->bits);
+  if (d == nullptr || d->B <= 0 || d->Hkv <= 0 || d->q_groups_cap < 0 || (d->bits != 1 && d->bits != 2) ||
+      (d->group != 32 && d->group != 64))
+    return 0;
+  return (size_t)d->B * d->Hkv * spc::records_cap(d->group, d->q_groups_cap) *
+         (size_t)spc::record_bytes(d->bits, d->group);
 }
 
 size_t spc_resid_bytes(const spc_dims* d) {

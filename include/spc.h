@@ -75,10 +75,11 @@ int32_t spc_last_cuda_error(void);
 int32_t spc_num_quantized(const spc_dims* d);
 
 /*
- * Low-bit copy C' of one layer ("records").  Per (b, hkv) there are
- * q_groups_cap records of 1024*(bits+1) bytes; record g holds tokens
- * 32g .. 32g+31.  Bytes spc_records_bytes(d) in all, row-major
- * [B][Hkv][q_groups_cap][1024*(bits+1)].  A record is, in order:
+ * Low-bit copy C' of one layer ("records").  Bytes spc_records_bytes(d) in
+ * all, row-major [B][Hkv][records per (b, hkv)][record bytes].
+ *
+ * g = 32: per (b, hkv) q_groups_cap records of 1024*(bits+1) bytes; record g
+ * holds tokens 32g .. 32g+31 and is, in order:
  *   K codes  : `bits` planes of 128 u32 words (plane p holds bit p of each code)
  *   K minmax : 128 u32 words, min in bits 0..15 and max in bits 16..31 (bf16)
  *   V codes  : `bits` planes of 128 u32 words
@@ -96,16 +97,26 @@ int32_t spc_num_quantized(const spc_dims* d);
  *                             channel 16*((b&15)>>1) + 8*(b&1) + a
  *   V minmax word 32t+m     : token 16*(m>>4) + 8*((m>>3)&1) + 2t + ((m>>2)&1),
  *                             channel group m&3
+ * This is 64 (1-bit) or 96 (2-bit) bytes per token and KV head, 1/8 or 3/16
+ * of bf16.
+ *
+ * g = 64: per (b, hkv) (q_groups_cap + 1) / 2 records of 2048*bits + 1024
+ * bytes; record u holds the 64-token group of tokens 64u .. 64u+63 as two
+ * halves H = 0, 1 (tokens 64u + 32H ..), each group's metadata stored once:
+ *   K codes of half 0, then of half 1 (`bits` planes of 128 words each, the
+ *              code word rule above for the half's 32 tokens)
+ *   K minmax : 128 words, word 32t+m as above, extremes over the 64 tokens
+ *   V codes of half 0, then of half 1 (as above)
+ *   V minmax : 128 words; word 64H + 2m + c holds token 32H + 16*((m>>2)&1) +
+ *              8*((m>>1)&1) + 2*(m>>3) + (m&1) of the record, channels
+ *              64c .. 64c+63
+ * This is 48 (1-bit) or 80 (2-bit) bytes per token and KV head.
+ *
  * Keys are grouped per channel over g tokens, values per token over g
- * consecutive channels (KIVI's axes); with g = 64 a record's K minmax words
- * hold its 64-token group's extremes and a token's V minmax word for
- * 32-channel group cg those of its 64-channel group cg/2, so the two records
- * of a group repeat its metadata (the codes are the g = 64 codes; the layout
- * is shared with g = 32, which lets every kernel read either).  min/max are the group's
- * exact bf16 extremes (-0.0 stored as +0.0); the zero point and scale are
- * derived from them (SpeCache page, section 3): 1-bit z = (3min+max)/4, s = (max-min)/2;
- * 2-bit z = min, s = (max-min)/3.  This is 64 (1-bit) or 96 (2-bit) bytes per
- * token and KV head, 1/8 or 3/16 of bf16.
+ * consecutive channels (KIVI's axes).  min/max are the group's exact bf16
+ * extremes (-0.0 stored as +0.0); the zero point and scale are derived from
+ * them (SpeCache page, section 3): 1-bit z = (3min+max)/4, s = (max-min)/2;
+ * 2-bit z = min, s = (max-min)/3.
  */
 size_t spc_records_bytes(const spc_dims* d);
 
@@ -116,7 +127,7 @@ size_t spc_resid_bytes(const spc_dims* d);
 
 /*
  * Quant (SpeCache page, section 3; Algorithm 1, K' = Quant(K), V' = Quant(V)).
- * k, v: bf16 [B][Hkv][N][D] (device).  Writes records 0 .. N_q/32-1 of every
+ * k, v: bf16 [B][Hkv][N][D] (device).  Writes records 0 .. N_q/g-1 of every
  * (b,hkv) and residual rows 0 .. r-1.  Codes are
  *   clamp(rint((x - z) / s), 0, 2^bits - 1), code 0 when s == 0,
  * with z, s and (x - z) / s evaluated in IEEE binary32, round to nearest even,
@@ -306,8 +317,8 @@ spc_status spc_offload_kv(const spc_dims* d, const uint16_t* k, const uint16_t* 
  *            [B][Hkv][n_cap][2][D] (row N is written), or NULL for no
  *            offload; SPC_ERR_NOT_MAPPED if not mapped; n_cap > N.
  * The new row goes to window row r = N - N_q.  When N+1 tokens quantise one
- * more group (N_q' = N_q + 32), the window's oldest 32 rows are quantised
- * into record N_q/32 and the window shifts down by 32 rows; the result is
+ * more group (N_q' = N_q + g), the window's oldest g rows are quantised
+ * into record N_q/g and the window shifts down by g rows; the result is
  * bit-identical to spc_quantize_kv over all N+1 tokens.  Needs
  * resid_cap >= N - N_q + 1 and, at a flush, q_groups_cap >= N_q'/32
  * (SPC_ERR_INVALID otherwise).  One launch on `stream`.

@@ -54,6 +54,10 @@ def lib():
         L.orc_quantize.argtypes = [C.POINTER(orc_dims), C.c_int32, P, P, P, P, P, P]
         L.orc_record_bytes.restype = C.c_int64
         L.orc_record_bytes.argtypes = [C.c_int32]
+        L.orc_unit_bytes.restype = C.c_int64
+        L.orc_unit_bytes.argtypes = [C.c_int32, C.c_int32]
+        L.orc_units_cap.restype = C.c_int32
+        L.orc_units_cap.argtypes = [C.c_int32, C.c_int32]
         L.orc_pack.argtypes = [C.POINTER(orc_dims), P, P, P, P, P, P, C.c_int32, C.c_int32, P, P]
         L.orc_attention.argtypes = [C.POINTER(orc_dims), C.c_int32, P, P, P, P, P, P, P, P,
                                     C.c_int32, P, P, P, P]
@@ -110,8 +114,14 @@ def quantize(d: orc_dims, K, V, mode: int = 0):
     return {"kcode": kcode, "kmm": kmm, "vcode": vcode, "vmm": vmm}
 
 
-def record_bytes(bits: int) -> int:
-    return int(lib().orc_record_bytes(bits))
+def record_bytes(bits: int, group: int = 32) -> int:
+    """Bytes of one record: a 32-token group at g = 32, a 64-token group at g = 64."""
+    return int(lib().orc_unit_bytes(bits, group))
+
+
+def records_per_pair(group: int, q_groups_cap: int) -> int:
+    """Records per (b, hkv) for a capacity of q_groups_cap 32-token groups."""
+    return int(lib().orc_units_cap(group, q_groups_cap))
 
 
 def pack(d: orc_dims, qz, K, V, q_groups_cap=None, resid_cap=None):
@@ -120,7 +130,7 @@ def pack(d: orc_dims, qz, K, V, q_groups_cap=None, resid_cap=None):
     n_q = nq(d)
     q_groups_cap = n_q // 32 if q_groups_cap is None else q_groups_cap
     resid_cap = (d.N - n_q) if resid_cap is None else resid_cap
-    rec = np.zeros((d.B, d.Hkv, q_groups_cap, record_bytes(d.bits)), np.uint8)
+    rec = np.zeros((d.B, d.Hkv, records_per_pair(d.group, q_groups_cap), record_bytes(d.bits, d.group)), np.uint8)
     res = np.zeros((d.B, d.Hkv, max(resid_cap, 0), 2, d.D), np.uint16)
     Kc, Vc = _c(K, np.uint16), _c(V, np.uint16)  # held until the call returns
     lib().orc_pack(C.byref(d), _p(qz["kcode"]), _p(qz["kmm"]), _p(qz["vcode"]), _p(qz["vmm"]),
@@ -162,12 +172,13 @@ def topk(d: orc_dims, S, k: int):
 
 def append(d: orc_dims, records, resid, k_new, v_new, host=None):
     """Decode-time append of token d.N, in place on the packed cache (records
-    [B,Hkv,q_groups_cap,RB] u8, resid [B,Hkv,resid_cap,2,D] bf16) and, if
-    given, the host cache [B,Hkv,n_cap,2,D].  The caller then advances d.N."""
+    as pack() lays them out, resid [B,Hkv,resid_cap,2,D] bf16) and, if given,
+    the host cache [B,Hkv,n_cap,2,D].  The caller then advances d.N."""
     for a in (records, resid) + (() if host is None else (host,)):
         assert a.flags["C_CONTIGUOUS"], "append works in place on contiguous arrays"
     kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)  # held until the call returns
-    lib().orc_append(C.byref(d), int(records.shape[2]), int(resid.shape[2]), _p(kn), _p(vn),
+    q_groups_cap = int(records.shape[2]) * (2 if d.group == 64 else 1)
+    lib().orc_append(C.byref(d), q_groups_cap, int(resid.shape[2]), _p(kn), _p(vn),
                      _p(records), _p(resid), _p(host), 0 if host is None else int(host.shape[2]))
 
 

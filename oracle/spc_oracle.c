@@ -164,9 +164,46 @@ void orc_quantize(const orc_dims* d, int32_t mode, const uint16_t* K, const uint
 
 int64_t orc_record_bytes(int32_t bits) { return 1024 * (int64_t)(bits + 1); }
 
+int64_t orc_unit_bytes(int32_t bits, int32_t group) {
+  return group == 64 ? 2048 * (int64_t)bits + 1024 : orc_record_bytes(bits);
+}
+
+int32_t orc_units_cap(int32_t group, int32_t q_groups_cap) {
+  return group == 64 ? (q_groups_cap + 1) / 2 : q_groups_cap;
+}
+
+/* Code planes of the 32 tokens n0 .. n0+31 of (b, hkv) bh, by the word rule
+ * below: kc and vc receive `bits` planes of 128 words each. */
+static void pack_code_words(const uint8_t* kcode, const uint8_t* vcode, int64_t bh, int32_t nq, int32_t D,
+                            int32_t n0, int32_t bits, uint32_t* kc, uint32_t* vc) {
+  for (int32_t p = 0; p < bits; ++p) {
+    for (int32_t L = 0; L < 32; ++L) {
+      int32_t a = L >> 2, t = L & 3;
+      for (int32_t j = 0; j < 4; ++j) {
+        uint32_t wk = 0, wv = 0;
+        for (int32_t bit = 0; bit < 32; ++bit) {
+          int32_t kv = (bit + 21) % 32, kq = kv / 4;
+          int32_t ke = 4 * j + (4 - kq % 4) % 4;
+          int32_t ktok = 8 * (kv % 4) + a;
+          int32_t kch = 16 * (ke >> 1) + 8 * (ke & 1) + 2 * t + ((kq >= 1 && kq <= 4) ? 1 : 0);
+          int32_t kcv = kcode[(bh * nq + n0 + ktok) * D + kch];
+          wk |= (uint32_t)((kcv >> p) & 1) << bit;
+          int32_t vtok = 16 * (j >> 1) + 8 * (j & 1) + 2 * t + (bit >> 4);
+          int32_t vch = 16 * ((bit & 15) >> 1) + 8 * (bit & 1) + a;
+          int32_t vcv = vcode[(bh * nq + n0 + vtok) * D + vch];
+          wv |= (uint32_t)((vcv >> p) & 1) << bit;
+        }
+        kc[128 * p + 4 * L + j] = wk;
+        vc[128 * p + 4 * L + j] = wv;
+      }
+    }
+  }
+}
+
 /*
- * The library's byte layout of one 32-token group (D = 128), written out as a
- * plain index rule.  A group record is, in order:
+ * The library's byte layout of the low-bit copy (D = 128), written out as a
+ * plain index rule.  With g = 32 a record holds one 32-token group and is, in
+ * order:
  *   K codes  : `bits` planes of 128 u32 words (plane p holds bit p of each code)
  *   K minmax : 128 u32 words, min in bits 0..15 and max in bits 16..31 (bf16)
  *   V codes  : `bits` planes of 128 u32 words
@@ -181,12 +218,18 @@ int64_t orc_record_bytes(int32_t bits) { return 1024 * (int64_t)(bits + 1); }
  *                             channel 16*((b&15)>>1) + 8*(b&1) + a
  *   V minmax word 32t+m     : token 16*(m>>4) + 8*((m>>3)&1) + 2t + ((m>>2)&1),
  *                             channel group m&3
+ * With g = 64 a record holds one 64-token group, its two 32-token halves
+ * H = 0, 1 coded by the same word rules, and each group's (min, max) stored
+ * once (48 bytes per token and KV head at 1 bit, 80 at 2 bits):
+ *   K codes of half 0, K codes of half 1  (`bits` planes of 128 words each)
+ *   K minmax : 128 words, word 32t+m as above, over the 64 tokens
+ *   V codes of half 0, V codes of half 1
+ *   V minmax : 128 words; word 64H + 2m + c: token 32H + 16*((m>>2)&1) +
+ *              8*((m>>1)&1) + 2*(m>>3) + (m&1), channels 64c .. 64c+63
+ * Records follow one another, q_groups_cap of them per (b,hkv) at g = 32 and
+ * (q_groups_cap + 1) / 2 at g = 64.
  * The residual window is bf16 [resid_cap, 2, D] per (b,hkv): row j holds the
  * key then the value of token N_q + j.
- * With g = 64 the same 32-token records are used: a record's K minmax words
- * hold its 64-token group's (min, max), and a token's V minmax word for
- * 32-channel group cg holds the (min, max) of its 64-channel group cg/2, so
- * both records of a 64-token group carry the group's metadata.
  */
 void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
               const uint8_t* vcode, const uint16_t* vmm,
@@ -194,50 +237,56 @@ void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
               int32_t q_groups_cap, int32_t resid_cap,
               uint8_t* records, uint16_t* resid) {
   const int32_t B = d->B, H = d->Hkv, N = d->N, D = d->D, nq = orc_nq(d), bits = d->bits;
-  const int32_t g_sz = d->group, ng = nq / 32, r = N - nq;
+  const int32_t g_sz = d->group, r = N - nq;
   const int32_t kng = nq / g_sz, vncg = D / g_sz;  /* groups of the logical metadata */
-  const int64_t RB = orc_record_bytes(bits);
+  const int64_t UB = orc_unit_bytes(bits, g_sz);
+  const int32_t ucap = orc_units_cap(g_sz, q_groups_cap), nu = nq / g_sz;
   for (int32_t b = 0; b < B; ++b) {
     for (int32_t h = 0; h < H; ++h) {
       const int64_t bh = (int64_t)b * H + h;
-      for (int32_t g = 0; g < ng; ++g) {
-        uint32_t* rec = (uint32_t*)(records + (bh * q_groups_cap + g) * RB);
-        uint32_t* kc = rec;
-        uint32_t* kmw = rec + 128 * bits;
-        uint32_t* vc = kmw + 128;
-        uint32_t* vmw = vc + 128 * bits;
-        memset(rec, 0, (size_t)RB);
-        for (int32_t p = 0; p < bits; ++p) {
-          for (int32_t L = 0; L < 32; ++L) {
-            int32_t a = L >> 2, t = L & 3;
-            for (int32_t j = 0; j < 4; ++j) {
-              uint32_t wk = 0, wv = 0;
-              for (int32_t bit = 0; bit < 32; ++bit) {
-                int32_t kv = (bit + 21) % 32, kq = kv / 4;
-                int32_t ke = 4 * j + (4 - kq % 4) % 4;
-                int32_t ktok = 8 * (kv % 4) + a;
-                int32_t kch = 16 * (ke >> 1) + 8 * (ke & 1) + 2 * t + ((kq >= 1 && kq <= 4) ? 1 : 0);
-                int32_t kcv = kcode[(bh * nq + 32 * g + ktok) * D + kch];
-                wk |= (uint32_t)((kcv >> p) & 1) << bit;
-                int32_t vtok = 16 * (j >> 1) + 8 * (j & 1) + 2 * t + (bit >> 4);
-                int32_t vch = 16 * ((bit & 15) >> 1) + 8 * (bit & 1) + a;
-                int32_t vcv = vcode[(bh * nq + 32 * g + vtok) * D + vch];
-                wv |= (uint32_t)((vcv >> p) & 1) << bit;
-              }
-              kc[128 * p + 4 * L + j] = wk;
-              vc[128 * p + 4 * L + j] = wv;
+      for (int32_t u = 0; u < nu; ++u) {
+        uint32_t* rec = (uint32_t*)(records + (bh * ucap + u) * UB);
+        memset(rec, 0, (size_t)UB);
+        if (g_sz == 32) {
+          uint32_t* kc = rec;
+          uint32_t* kmw = rec + 128 * bits;
+          uint32_t* vc = kmw + 128;
+          uint32_t* vmw = vc + 128 * bits;
+          pack_code_words(kcode, vcode, bh, nq, D, 32 * u, bits, kc, vc);
+          for (int32_t t = 0; t < 4; ++t) {
+            for (int32_t m = 0; m < 32; ++m) {
+              int32_t vtok = 16 * (m >> 4) + 8 * ((m >> 3) & 1) + 2 * t + ((m >> 2) & 1);
+              int64_t vm = ((bh * nq + 32 * u + vtok) * vncg + (m & 3)) * 2;
+              vmw[32 * t + m] = (uint32_t)vmm[vm] | ((uint32_t)vmm[vm + 1] << 16);
             }
           }
-        }
-        for (int32_t t = 0; t < 4; ++t) {
-          for (int32_t m = 0; m < 32; ++m) {
-            int32_t kch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1);
-            int64_t km = ((bh * kng + (32 * g) / g_sz) * D + kch) * 2;
-            kmw[32 * t + m] = (uint32_t)kmm[km] | ((uint32_t)kmm[km + 1] << 16);
-            int32_t vtok = 16 * (m >> 4) + 8 * ((m >> 3) & 1) + 2 * t + ((m >> 2) & 1);
-            int32_t cg = m & 3;
-            int64_t vm = ((bh * nq + 32 * g + vtok) * vncg + (32 * cg) / g_sz) * 2;
-            vmw[32 * t + m] = (uint32_t)vmm[vm] | ((uint32_t)vmm[vm + 1] << 16);
+          for (int32_t t = 0; t < 4; ++t) {
+            for (int32_t m = 0; m < 32; ++m) {
+              int32_t kch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1);
+              int64_t km = ((bh * kng + u) * D + kch) * 2;
+              kmw[32 * t + m] = (uint32_t)kmm[km] | ((uint32_t)kmm[km + 1] << 16);
+            }
+          }
+        } else {
+          uint32_t* kmw = rec + 256 * bits;
+          uint32_t* vmw = kmw + 128 + 256 * bits;
+          for (int32_t hf = 0; hf < 2; ++hf) {
+            pack_code_words(kcode, vcode, bh, nq, D, 64 * u + 32 * hf, bits, rec + 128 * bits * hf,
+                            kmw + 128 + 128 * bits * hf);
+            for (int32_t m = 0; m < 32; ++m) {
+              int32_t vtok = 16 * ((m >> 2) & 1) + 8 * ((m >> 1) & 1) + 2 * (m >> 3) + (m & 1);
+              for (int32_t c = 0; c < 2; ++c) {
+                int64_t vm = ((bh * nq + 64 * u + 32 * hf + vtok) * vncg + c) * 2;
+                vmw[64 * hf + 2 * m + c] = (uint32_t)vmm[vm] | ((uint32_t)vmm[vm + 1] << 16);
+              }
+            }
+          }
+          for (int32_t t = 0; t < 4; ++t) {
+            for (int32_t m = 0; m < 32; ++m) {
+              int32_t kch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1);
+              int64_t km = ((bh * kng + u) * D + kch) * 2;
+              kmw[32 * t + m] = (uint32_t)kmm[km] | ((uint32_t)kmm[km + 1] << 16);
+            }
           }
         }
       }
@@ -418,7 +467,8 @@ void orc_append(const orc_dims* d, int32_t q_groups_cap, int32_t resid_cap,
   one.Hkv = 1;
   one.N = g_sz;
   one.R = 0;
-  const int64_t RB = orc_record_bytes(d->bits);
+  const int64_t UB = orc_unit_bytes(d->bits, g_sz);
+  const int32_t ucap = orc_units_cap(g_sz, q_groups_cap);
   uint16_t* Kg = malloc(sizeof(uint16_t) * (size_t)g_sz * D);
   uint16_t* Vg = malloc(sizeof(uint16_t) * (size_t)g_sz * D);
   uint8_t* kcode = malloc((size_t)g_sz * D);
@@ -442,7 +492,7 @@ void orc_append(const orc_dims* d, int32_t q_groups_cap, int32_t resid_cap,
       }
       orc_quantize(&one, 0, Kg, Vg, kcode, kmm, vcode, vmm);
       orc_pack(&one, kcode, kmm, vcode, vmm, Kg, Vg, g_sz / 32, 0,
-               records + (bh * q_groups_cap + nq / 32) * RB, NULL);
+               records + (bh * ucap + nq / g_sz) * UB, NULL);
       memmove(win, win + (int64_t)g_sz * 2 * D, sizeof(uint16_t) * 2 * (size_t)D * (size_t)(r + 1 - g_sz));
     }
   free(Kg);

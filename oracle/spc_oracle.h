@@ -64,8 +64,12 @@ double orc_dequant(int32_t bits, int32_t mode, uint16_t lo, uint16_t hi, int32_t
 
 /* Byte layout of the low-bit copy C' and the residual window as the library
  * stores them (the index rule is spelled out in spc_oracle.c, orc_pack).
- * records: u8 [B,Hkv,q_groups_cap, 1024*(bits+1)];  resid: bf16 [B,Hkv,resid_cap,2,D]. */
+ * records: u8 [B,Hkv,orc_units_cap(g, q_groups_cap), orc_unit_bytes(bits, g)]
+ * (a record per 32-token group at g = 32, per 64-token group at g = 64);
+ * resid: bf16 [B,Hkv,resid_cap,2,D]. */
 int64_t orc_record_bytes(int32_t bits);
+int64_t orc_unit_bytes(int32_t bits, int32_t group);
+int32_t orc_units_cap(int32_t group, int32_t q_groups_cap);
 void orc_pack(const orc_dims* d, const uint8_t* kcode, const uint16_t* kmm,
               const uint8_t* vcode, const uint16_t* vmm,
               const uint16_t* K, const uint16_t* V,
@@ -106,7 +110,7 @@ void orc_gather(const orc_dims* d, const uint16_t* host, int64_t n_cap,
 /* Decode-time append (SpeCache page, section 3 "Decoding", Algorithm 3: the
  * new token's K/V joins the cache; section 3's offload of the 16-bit cache to
  * CPU memory).  d describes the cache before the call (d->N tokens held as
- * records [B,Hkv,q_groups_cap,RB] and the residual window resid
+ * records (as orc_pack lays them out for q_groups_cap) and the residual window resid
  * [B,Hkv,resid_cap,2,D], as orc_pack lays them out).  Token N's rows k_new,
  * v_new (bf16 [B,Hkv,D]) go to window row r = N - N_q; when N+1 tokens
  * quantise one more group, the window's oldest 32 rows are quantised as group

@@ -69,8 +69,8 @@ def test_append_sequence_matches_oracle(c):
     nq1 = oracle.nq(od)
     assert spc.spc_num_quantized(d) == nq1
     r1 = N1 - nq1
-    got_rec = rec.cpu().numpy().reshape(B, Hkv, cap, -1)
-    assert np.array_equal(got_rec[:, :, :nq1 // 32], orec[:, :, :nq1 // 32])
+    got_rec = rec.cpu().numpy().reshape(B, Hkv, oracle.records_per_pair(group, cap), -1)
+    assert np.array_equal(got_rec[:, :, :nq1 // group], orec[:, :, :nq1 // group])
     got_res = res.cpu().numpy().view(np.uint16).reshape(B, Hkv, rcap, 2, D)
     assert np.array_equal(got_res[:, :, :r1], ores[:, :, :r1])
     assert np.array_equal(host.numpy().view(np.uint16), ohost)

@@ -23,11 +23,13 @@ CASES = [
     dict(B=1, Hq=4, Hkv=1, N=96, R=32, bits=1, k=200),        # k > N_q
     dict(B=2, Hq=8, Hkv=2, N=40000, R=128, bits=1, k=400),    # many chunks
     dict(B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328),   # the LLaMA-3-8B decode shape
+    dict(B=2, Hq=8, Hkv=2, N=4200, R=40, bits=1, k=41, group=64),   # g = 64 records
+    dict(B=1, Hq=4, Hkv=2, N=2100, R=64, bits=2, k=20, group=64),   # g = 64, 2-bit
 ]
 
 
 def cid(c):
-    return f"B{c['B']}_Hq{c['Hq']}_Hkv{c['Hkv']}_N{c['N']}_b{c['bits']}_k{c['k']}"
+    return f"B{c['B']}_Hq{c['Hq']}_Hkv{c['Hkv']}_N{c['N']}_b{c['bits']}_k{c['k']}_g{c.get('group', 32)}"
 
 
 def prepare(cfg, seed=3):

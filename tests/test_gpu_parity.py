@@ -167,8 +167,9 @@ def test_k0_merged_is_attn2_and_all_fetched_is_bf16_attention():
 
 @pytest.mark.parametrize("cfg", [dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41),
                                  dict(B=1, Hq=4, Hkv=4, N=300, R=64, bits=2, k=7),
-                                 dict(B=1, Hq=4, Hkv=1, N=64, R=32, bits=1, k=24)],
-                         ids=["many_groups", "mha_2bit", "rows_exceed_groups"])
+                                 dict(B=1, Hq=4, Hkv=1, N=64, R=32, bits=1, k=24),
+                                 dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41, group=64)],
+                         ids=["many_groups", "mha_2bit", "rows_exceed_groups", "g64"])
 def test_merged_attention_with_fetch_job(cfg):
     """spc_merged_attn_fetch: the attention results equal spc_merged_attn's and the
     pre-fetched rows equal the oracle's gather, also when the job has more rows
@@ -326,8 +327,9 @@ def full_size_check(cfg, pairs, layer=0, ks=None, check_records=True):
     g = GpuLayer(cfg, layer=layer, kcap=max(ks))
     torch.cuda.synchronize()
     G = cfg["Hq"] // cfg["Hkv"]
-    rb = oracle.record_bytes(cfg["bits"])
-    ng = g.nq // 32
+    group = cfg.get("group", 32)
+    rb = oracle.record_bytes(cfg["bits"], group)
+    ng = g.nq // group  # records per (b, kv-head)
     o, lse, lg = g.attn2()
     torch.cuda.synchronize()
     o_np, lse_np = b2f(o.cpu().numpy()), lse.cpu().numpy()
@@ -398,3 +400,12 @@ def test_config5_sweep(shape):
     2 bits, k = 0.5%, 1% and 4% of N): records, attention over C', both top-k
     and the merged attention on two sampled (b, kv-head) pairs each."""
     full_size_check(shape, [(shape["B"] - 1, 7), (0, 2)], ks=shape["ks"])
+
+
+@pytest.mark.parametrize("bits", [1, 2])
+def test_group64_layer_sampled(bits):
+    """g = 64 (SpeCache appendix: LongBench at g = 64) on the LLaMA-3-8B layer
+    shape at batch 4, 16K context: records (48 or 80 bytes per token and KV
+    head), attention, both top-k and the merged attention on sampled pairs."""
+    cfg = dict(B=4, Hq=32, Hkv=8, N=16384, R=128, bits=bits, k=164, group=64)
+    full_size_check(cfg, [(3, 7), (0, 2), (2, 5)])

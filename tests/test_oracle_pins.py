@@ -402,6 +402,25 @@ def test_pack_places_every_bit_exactly_once():
         assert len(seen_k) == len(seen_v) == bits * 11 * 26
 
 
+def code_word_rule(p, kc, vc, kcode, vcode, n0):
+    """The code-word rule of the header, restated: every bit of the K and V code
+    planes kc, vc of the 32 tokens n0 .. n0+31 against the logical codes."""
+    for L in range(32):
+        a, t = L >> 2, L & 3
+        for j in range(4):
+            kw, vw = int(kc[128 * p + 4 * L + j]), int(vc[128 * p + 4 * L + j])
+            for b in range(32):
+                v = (b + 21) % 32
+                n, q = v % 4, v // 4
+                i, h = (4 - q % 4) % 4, 1 if 1 <= q <= 4 else 0
+                e = 4 * j + i
+                tok, ch = 8 * n + a, 16 * (e >> 1) + 8 * (e & 1) + 2 * t + h
+                assert (kw >> b) & 1 == (int(kcode[n0 + tok, ch]) >> p) & 1
+                tok = 16 * (j >> 1) + 8 * (j & 1) + 2 * t + (b >> 4)
+                ch = 16 * ((b & 15) >> 1) + 8 * (b & 1) + a
+                assert (vw >> b) & 1 == (int(vcode[n0 + tok, ch]) >> p) & 1
+
+
 @pytest.mark.parametrize("bits", [1, 2])
 def test_pack_follows_the_documented_index_rule(bits):
     """Every bit and metadata word of the packed records, read back with the
@@ -419,26 +438,46 @@ def test_pack_follows_the_documented_index_rule(bits):
         kc, km, vc, vm = w[:128 * bits], w[128 * bits:128 * bits + 128], w[128 * bits + 128:256 * bits + 128], \
             w[256 * bits + 128:]
         for p in range(bits):
-            for L in range(32):
-                a, t = L >> 2, L & 3
-                for j in range(4):
-                    kw, vw = int(kc[128 * p + 4 * L + j]), int(vc[128 * p + 4 * L + j])
-                    for b in range(32):
-                        v = (b + 21) % 32
-                        n, q = v % 4, v // 4
-                        i, h = (4 - q % 4) % 4, 1 if 1 <= q <= 4 else 0
-                        e = 4 * j + i
-                        tok, ch = 8 * n + a, 16 * (e >> 1) + 8 * (e & 1) + 2 * t + h
-                        assert (kw >> b) & 1 == (int(kcode[32 * g + tok, ch]) >> p) & 1
-                        tok = 16 * (j >> 1) + 8 * (j & 1) + 2 * t + (b >> 4)
-                        ch = 16 * ((b & 15) >> 1) + 8 * (b & 1) + a
-                        assert (vw >> b) & 1 == (int(vcode[32 * g + tok, ch]) >> p) & 1
+            code_word_rule(p, kc, vc, kcode, vcode, 32 * g)
         for t in range(4):
             for m in range(32):
                 ch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1)
                 assert int(km[32 * t + m]) == int(kmm[g, ch, 0]) | (int(kmm[g, ch, 1]) << 16)
                 tok = 16 * (m >> 4) + 8 * ((m >> 3) & 1) + 2 * t + ((m >> 2) & 1)
                 assert int(vm[32 * t + m]) == int(vmm[32 * g + tok, m & 3, 0]) | (int(vmm[32 * g + tok, m & 3, 1]) << 16)
+
+
+@pytest.mark.parametrize("bits", [1, 2])
+def test_pack_follows_the_documented_index_rule_g64(bits):
+    """The same for g = 64, whose records hold a 64-token group each with its
+    metadata once: both halves' code planes by the 32-token word rule, the keys'
+    (min, max) over 64 tokens, two value (min, max) words per token (channels
+    0..63 and 64..127), 48 (1 bit) or 80 (2 bits) bytes per token."""
+    B, Hkv, N = 1, 1, 128
+    d = oracle.dims(B=B, Hq=1, Hkv=Hkv, N=N, R=0, bits=bits, group=64)
+    K, V = synth.kv_layer(23, 0, B, Hkv, N)
+    qz = oracle.quantize(d, K, V)
+    rec, _ = oracle.pack(d, qz, K, V)
+    assert rec.shape[2] == N // 64 and rec.shape[3] == 64 * (48 if bits == 1 else 80)
+    kcode, vcode, kmm, vmm = qz["kcode"][0, 0], qz["vcode"][0, 0], qz["kmm"][0, 0], qz["vmm"][0, 0]
+    for u in range(N // 64):
+        w = np.frombuffer(rec[0, 0, u].tobytes(), dtype="<u4")
+        P = 128 * bits  # words of one half's code planes
+        km = w[2 * P:2 * P + 128]
+        vm = w[2 * P + 128 + 2 * P:]
+        for hf in range(2):
+            kc = w[hf * P:(hf + 1) * P]
+            vc = w[2 * P + 128 + hf * P:2 * P + 128 + (hf + 1) * P]
+            for p in range(bits):
+                code_word_rule(p, kc, vc, kcode, vcode, 64 * u + 32 * hf)
+            for m in range(32):
+                tok = 64 * u + 32 * hf + 16 * ((m >> 2) & 1) + 8 * ((m >> 1) & 1) + 2 * (m >> 3) + (m & 1)
+                for c in range(2):
+                    assert int(vm[64 * hf + 2 * m + c]) == int(vmm[tok, c, 0]) | (int(vmm[tok, c, 1]) << 16)
+        for t in range(4):
+            for m in range(32):
+                ch = 16 * (m >> 2) + 2 * t + 8 * ((m >> 1) & 1) + (m & 1)
+                assert int(km[32 * t + m]) == int(kmm[u, ch, 0]) | (int(kmm[u, ch, 1]) << 16)
 
 
 @pytest.mark.parametrize("bits,R,N0,T,group", [(1, 8, 30, 45, 32), (2, 8, 71, 40, 32), (1, 0, 0, 70, 32),
@@ -470,7 +509,7 @@ def test_append_one_token_at_a_time_equals_quantising_the_sequence(bits, R, N0, 
     d1 = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N1, R=R, bits=bits, group=group)
     nq1 = oracle.nq(d1)
     rec1, res1 = oracle.pack(d1, oracle.quantize(d1, K, V), K, V, q_groups_cap=cap, resid_cap=rcap)
-    assert np.array_equal(rec[:, :, :nq1 // 32], rec1[:, :, :nq1 // 32])
+    assert np.array_equal(rec[:, :, :nq1 // group], rec1[:, :, :nq1 // group])
     assert np.array_equal(res[:, :, :N1 - nq1], res1[:, :, :N1 - nq1])
     assert np.array_equal(host[:, :, :N1], np.stack([K, V], axis=3))
     assert not host[:, :, N1:].any()
@@ -481,7 +520,8 @@ def test_g64_equals_g32_when_both_halves_of_every_group_span_the_same_range(bits
     """A 64-token key group whose two 32-token halves have the same per-channel
     (min, max), and a 64-channel value group whose two halves share theirs,
     quantise exactly as with g = 32 (a code depends only on the value and its
-    group's min and max): the packed records must coincide."""
+    group's min and max): the codes must coincide and each 64-group's (min, max)
+    must be both of its 32-groups'."""
     B, Hkv, N, D = 1, 2, 256, 128
     K, V = synth.kv_layer(13, bits, B, Hkv, N, D)
     rng = np.random.default_rng(5)
@@ -491,18 +531,21 @@ def test_g64_equals_g32_when_both_halves_of_every_group_span_the_same_range(bits
     for c0 in (0, 64):  # channels c0+32..c0+63: a permutation of c0..c0+31, per token
         perm = rng.permutation(32)
         V[..., c0 + 32:c0 + 64] = V[..., c0 + perm]
-    recs = []
+    qz = {}
     for group in (32, 64):
         d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N, R=0, bits=bits, group=group)
-        rec, _ = oracle.pack(d, oracle.quantize(d, K, V), K, V)
-        recs.append(rec)
-    assert np.array_equal(recs[0], recs[1])
+        qz[group] = oracle.quantize(d, K, V)
+    assert np.array_equal(qz[32]["kcode"], qz[64]["kcode"]) and np.array_equal(qz[32]["vcode"], qz[64]["vcode"])
+    assert np.array_equal(qz[32]["kmm"][:, :, 0::2], qz[64]["kmm"])
+    assert np.array_equal(qz[32]["kmm"][:, :, 1::2], qz[64]["kmm"])
+    assert np.array_equal(qz[32]["vmm"][:, :, :, 0::2], qz[64]["vmm"])
+    assert np.array_equal(qz[32]["vmm"][:, :, :, 1::2], qz[64]["vmm"])
     # and an ordinary input does differ (the pin is not vacuous)
     K2, V2 = synth.kv_layer(13, bits, B, Hkv, N, D)
     out = []
     for group in (32, 64):
         d = oracle.dims(B=B, Hq=Hkv, Hkv=Hkv, N=N, R=0, bits=bits, group=group)
-        out.append(oracle.pack(d, oracle.quantize(d, K2, V2), K2, V2)[0])
+        out.append(oracle.quantize(d, K2, V2)["kcode"])
     assert not np.array_equal(out[0], out[1])
 
 
