@@ -214,6 +214,8 @@ class DecodeStep:
         self.ws_bytes = spc.spc_attn_workspace_bytes(d, k)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
         self.ws_step_bytes = spc.spc_step_workspace_bytes(d, k)
+        # the fused step keeps the speculative logits on chip (TMEM) when the shape allows it
+        self.step_onchip = spc.spc_decode_step_on_chip(d, k, k, k) == 1
         self.ws_step = torch.zeros(self.ws_step_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
         self.main = torch.cuda.Stream(priority=-1 if mode == "overlap" else 0)
         self.side = torch.cuda.Stream(priority=-1)
@@ -310,7 +312,8 @@ class DecodeStep:
             if timed:
                 self.rec(self.attn_ev[l][0], main)
             spc.spc_decode_step(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
-                                self.staging[l], k, self.o[l], self.lse[l], self.logits[l], k, self.idx[l],
+                                self.staging[l], k, self.o[l], self.lse[l],
+                                None if self.step_onchip else self.logits[l], k, self.idx[l],
                                 self.bitmap[l], self.ws_step, self.ws_step_bytes, fetch_host_kv=self.host[j],
                                 fetch_n_cap=self.W["N"], fetch_idx=self.idx[j], fetch_k=k,
                                 fetch_staging=self.staging[j], stream=main)
@@ -1167,7 +1170,7 @@ def main():
                        "prefetch": {"side": f"side stream, {args.gather_ctas} CTAs",
                                     "fused": "fused into the next layer's attention",
                                     "step": "fused into the next layer's attention, which also ends with "
-                                            "the top-k (spc_decode_step)",
+                                            "the top-k (spc_decode_step, speculative logits kept in TMEM)",
                                     "overlap": "fused into the attention two layers on; top-k on a "
                                                "low-priority stream beside the next attention"}[args.prefetch]},
             "roofline": roof, "overlap": overlap, "gather": gather,

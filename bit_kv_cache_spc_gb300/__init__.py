@@ -20,7 +20,8 @@ __all__ = [
     "Dims", "SpcError", "spc_abi_version", "spc_num_quantized", "spc_records_bytes", "spc_resid_bytes",
     "spc_quantize_kv", "spc_attn_workspace_bytes", "spc_decode_attn2", "spc_merged_attn", "spc_topk_select",
     "spc_host_gather", "spc_merged_attn_noalloc", "spc_merged_attn_fetch", "spc_attn_kernel_count",
-    "spc_decode_step_kernel_count", "lib_path",
+    "spc_decode_step_kernel_count", "spc_decode_step_on_chip", "spc_decode_step", "spc_step_workspace_bytes",
+    "spc_read_device_status", "spc_append_kv", "spc_offload_kv", "lib_path",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -88,6 +89,7 @@ _sig = {
     "spc_step_workspace_bytes": (C.c_size_t, [_D, C.c_int32]),
     "spc_attn_kernel_count": (C.c_int32, [_D, C.c_int32, C.c_int32]),
     "spc_decode_step_kernel_count": (C.c_int32, [_D, C.c_int32, C.c_int32, C.c_int32]),
+    "spc_decode_step_on_chip": (C.c_int32, [_D, C.c_int32, C.c_int32, C.c_int32]),
     "spc_decode_step": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, C.c_int32, _P, _P, _P,
                                   C.c_size_t, _P, C.c_int64, _P, C.c_int32, _P, _P]),
     "spc_read_device_status": (C.c_int, [_P, _D, _P]),
@@ -149,6 +151,11 @@ def spc_attn_kernel_count(d, k=0, fetch_k=0) -> int:
 
 def spc_decode_step_kernel_count(d, k, fetch_k, next_k) -> int:
     return int(_lib.spc_decode_step_kernel_count(C.byref(d), int(k), int(fetch_k), int(next_k)))
+
+
+def spc_decode_step_on_chip(d, k, fetch_k, next_k) -> int:
+    """1 if spc_decode_step may be called with spec_logits=None (logits kept in TMEM)."""
+    return int(_lib.spc_decode_step_on_chip(C.byref(d), int(k), int(fetch_k), int(next_k)))
 
 
 def spc_decode_step(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, next_k, next_idx,

@@ -141,8 +141,13 @@ size_t attn_workspace_bytes(const spc_dims* d, int32_t k_max) {
   return control_bytes(d) + parts_bytes(d);
 }
 
+// the fetched rows' speculative logits of the on-chip selection: [BH][k][4] floats
+static size_t rowlog_bytes(const spc_dims* d, int32_t k_max) {
+  return (size_t)d->B * d->Hkv * std::max(k_max, 0) * 4 * sizeof(float);
+}
+
 size_t step_workspace_bytes(const spc_dims* d, int32_t k_max) {
-  return control_bytes(d) + parts_bytes(d) + cand_bytes(d, k_max);
+  return control_bytes(d) + parts_bytes(d) + cand_bytes(d, k_max) + rowlog_bytes(d, k_max);
 }
 
 // The clustered combine, when every (b, hkv)'s CTAs fit one cluster and all
@@ -162,6 +167,21 @@ static bool select_fits(const spc_dims* d, const AttnPlan& p, int32_t k_sel) {
   return nq > 0 && len + 2 * (len / 32) <= words && 2 * M + nq / 32 + 2 * ((M + 31) / 32) <= words;
 }
 
+// The fused selection keeps the speculative logits of every warp's records in
+// its TMEM lanes: 4 columns (heads) per 32-token half, kTmemCols per CTA.
+static bool onchip_fits(const spc_dims* d, const AttnPlan& p) {
+  const int nh = d->group / kGroup;
+  const int units_per_warp = (p.groups_per_chunk / nh + kWarps - 1) / kWarps;
+  return 4 * nh * units_per_warp <= (int)kTmemCols;
+}
+
+// Whether spc_decode_step can keep the speculative logits on chip (spec_logits == nullptr).
+bool step_onchip(const spc_dims* d, int32_t k, int32_t fetch_k, int32_t next_k) {
+  const bool fetch = (int64_t)d->B * d->Hkv * fetch_k > 0;
+  const AttnPlan plan = attn_plan(d, fetch);
+  return k > 0 && select_fits(d, plan, next_k) && onchip_fits(d, plan);
+}
+
 spc_status launch_attention(const spc_dims* d, const void* records, const uint16_t* resid,
                             const uint16_t* q, const uint16_t* kv_self, const int32_t* idx,
                             const uint32_t* bitmap, const uint16_t* staging, int32_t k, uint16_t* o, float* lse,
@@ -171,7 +191,8 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   const AttnPlan plan = attn_plan(d, fetch);
   const int64_t BH = (int64_t)d->B * d->Hkv;
   const bool merged = k > 0;
-  const bool topk = sel != nullptr && merged && lse != nullptr && spec_logits != nullptr && select_fits(d, plan, sel->k);
+  const bool topk = sel != nullptr && merged && lse != nullptr && select_fits(d, plan, sel->k) &&
+                    (spec_logits != nullptr || onchip_fits(d, plan));
   if (sel_done != nullptr) *sel_done = topk;
   AttnArgs a;
   a.records = static_cast<const uint8_t*>(records);
@@ -215,6 +236,10 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.sel_k = topk ? sel->k : 0;
   a.sel_keff = topk ? std::min(sel->k, a.nq) : 0;
   a.cand_cap = topk ? cand_cap(d, plan, sel->k) : 0;
+  a.sel_onchip = topk && spec_logits == nullptr ? 1 : 0;
+  a.sel_rowlog = a.sel_onchip ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + control_bytes(d) + parts_bytes(d) +
+                                                         cand_bytes(d, std::max(k, sel->k)))
+                              : nullptr;
   const bool clustered = !topk && use_cluster(d, merged, fetch, a.chunks, BH);
   a.ext_combine = !topk && !clustered;
   cudaError_t e = variant(d).launch(a, BH, stream, merged, fetch, topk, clustered);

@@ -50,6 +50,51 @@
 
 namespace spc {
 
+// ---- tensor memory (TMEM) as on-chip storage of the speculative logits ----
+// (spc_decode_step without a global spec_logits buffer).  A CTA allocates
+// kTmemCols columns of its SM's tensor memory (128 lanes x 512 columns of 32
+// bits); warp w may touch lanes 32 (w % 4) .. 32 (w % 4) + 31 only.
+constexpr uint32_t kTmemCols = 128;
+// One whole warp: allocate, write the base address to *smem_dst, and give up
+// the right to allocate more (so that other CTAs on the SM can allocate).
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(smem_dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+// One whole warp (the allocating one), after every access has completed.
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Lane l of the warp writes 4 consecutive columns of TMEM lane (taddr lane + l),
+// waited for in the same statement (the source registers are then free).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, float4 v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n"
+      "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)), "r"(__float_as_uint(v.w))
+      : "memory");
+}
+// The matching read, waited for in the same statement (its registers are
+// undefined until the wait).
+__device__ __forceinline__ float4 tmem_ld4(uint32_t taddr) {
+  uint32_t x, y, z, w;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
+      : "r"(taddr)
+      : "memory");
+  return make_float4(__uint_as_float(x), __uint_as_float(y), __uint_as_float(z), __uint_as_float(w));
+}
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 // At 1 bit the scaled query lives in registers across the low-bit loop; at 2
@@ -132,6 +177,10 @@ struct AttnArgs {
   uint32_t* fault;
   uint32_t* cand;         // [BH][chunks][cand_cap][2]
   int32_t sel_k, sel_keff, cand_cap;
+  // On-chip selection (spec_logits == nullptr): the speculative logits stay in
+  // TMEM; the fetched rows' logits go to sel_rowlog [BH][k][4] instead.
+  int32_t sel_onchip;
+  float* sel_rowlog;
 };
 
 // A lone set bit at position p of an fp16 half (p = 10..14, the exponent
@@ -251,7 +300,7 @@ __device__ __forceinline__ float reduce_scatter16(const float (&x)[16], int lane
 // 2G.. zero).  On return (m_run, l_run, oacc) hold the softmax state of the
 // rows, in the tensor-core fragment layouts of the low-bit loop (oacc divided by the per-channel powers of two that loop
 // multiplies back at its end).
-template <bool MERGED, int ROWB, typename FillQuery>
+template <bool MERGED, bool TOPK, int ROWB, typename FillQuery>
 __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* sq, uint8_t* tail,
                                                 FillQuery&& fill_query, float& m_run, float& l_run,
                                                 float (&oacc)[8][4]) {
@@ -273,6 +322,7 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
   const int rho_l = (lane >> 1) & 7;
   const bool spec_lane = MERGED && a.spec_logits != nullptr && (lane & 1) == 0 && rho_l >= G && rho_l < 2 * G;
   float* spec_out = spec_lane ? a.spec_logits + (bh * G + (rho_l - G)) * (int64_t)a.Lcap : nullptr;
+  const bool rowlog_lane = TOPK && MERGED && a.sel_rowlog != nullptr && (lane & 1) == 0 && rho_l >= G && rho_l < 2 * G;
   float m_own = kNeg, l_own = 0.f;  // state of query row rho_l
   float o16[kMaxRows][4];
 #pragma unroll
@@ -329,6 +379,8 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
         }
         const int pi = __shfl_sync(0xFFFFFFFFu, pos, b0 + 2 * pp + (lane >> 4));
         if (spec_lane && lg[pp] != kNeg && pi >= 0) spec_out[pi] = lg[pp] * CUDART_LN2_F;
+        if (TOPK && rowlog_lane && lg[pp] != kNeg && pi >= 0)  // fetched row j of this (b, hkv), head rho_l - G
+          a.sel_rowlog[(bh * a.k + (w0 + b0 + 2 * pp + (lane >> 4) - a.r)) * 4 + (rho_l - G)] = lg[pp] * CUDART_LN2_F;
       }
 
       float mx = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
@@ -399,9 +451,9 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
 }
 
 // ------------------------------------------------------------ low-bit CTA
-template <int BITS, int GROUP, bool MERGED, bool FETCH, typename FillQuery>
+template <int BITS, int GROUP, bool MERGED, bool FETCH, bool TOPK, typename FillQuery>
 __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, const float* sq, CtaMerge& merge,
-                                           FillQuery&& fill_query) {
+                                           const uint32_t* s_tmem, FillQuery&& fill_query) {
   using LY = Layout<BITS, GROUP>;
   constexpr int NH = LY::H;  // 32-token halves per record
   constexpr int RB = LY::RB;
@@ -482,7 +534,15 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   // rows, which are staged in the other stages and the z/s table (a warp's
   // rows then take one round trip); the rest of the pipeline is issued after.
   issue(0);
-  rows16_prologue<MERGED, LY::ROWB>(a, sq, stage + STAGE, fill_query, m_run, l_run, oacc);
+  rows16_prologue<MERGED, TOPK, LY::ROWB>(a, sq, stage + STAGE, fill_query, m_run, l_run, oacc);
+  // on-chip selection: this warp's TMEM lanes (its 32-lane quarter), read after the CTA barrier of the query fill
+  uint32_t tmem_warp = 0;
+  if constexpr (TOPK) {
+    if (a.sel_onchip) {
+      tmem_fence_after_sync();
+      tmem_warp = *s_tmem + ((uint32_t)(32 * warp) << 16);
+    }
+  }
 #pragma unroll 1
   for (int s = 1; s < kStages - 1; ++s) issue(s);
   constexpr bool kQvReg = QueryInRegisters<BITS>::value;
@@ -615,6 +675,20 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
                                 make_float2(key_comp(nt), key_comp(nt)), make_float2(bias, bias));
         lg[nt][0] = l.x;
         lg[nt][1] = l.y;
+      }
+      if (TOPK && a.sel_onchip) {
+        // the half's speculative logits into TMEM, lane = token, column 4 (NH it + hf) + head: transposed
+        // through the half's key-code planes, which are in registers since the QK step began
+        float* tx = reinterpret_cast<float*>(const_cast<uint8_t*>(R) + 512 * BITS * hf);  // [token][4]
+        if (row_valid && gid >= G) {
+  #pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            tx[(8 * nt + 2 * t) * 4 + (gid - G)] = lg[nt][0] * CUDART_LN2_F;
+            tx[(8 * nt + 2 * t + 1) * 4 + (gid - G)] = lg[nt][1] * CUDART_LN2_F;
+          }
+        }
+        __syncwarp();
+        tmem_st4(tmem_warp + 4 * (NH * it + hf), reinterpret_cast<const float4*>(tx)[lane]);
       }
       if (spec_row) {
         float* dst = spec_out + (int64_t)g * kGroup + 2 * t;
@@ -1017,9 +1091,9 @@ constexpr uint64_t kWaitLimitNs = 20000000ull;  // 20 ms: a normal wait is a few
 // second ticket) selects the final k from the candidates, which lie in
 // ascending position, and writes idx and the bitmap.  Every globally selected
 // position is among its chunk's candidates.
-template <int BITS>
+template <int BITS, int GROUP>
 __device__ __forceinline__ void select_epilogue(const AttnArgs& a, uint8_t* dyn, SelShared<kThreads>& sh,
-                                                bool combined, int* s_flag, float* s_nlse) {
+                                                bool combined, int* s_flag, float* s_nlse, uint32_t tmem_base) {
   const int tid = threadIdx.x;
   const int64_t bh = blockIdx.y;
   const int b = (int)(bh / a.Hkv), hk = (int)(bh % a.Hkv), G = a.G;
@@ -1047,19 +1121,60 @@ __device__ __forceinline__ void select_epilogue(const AttnArgs& a, uint8_t* dyn,
   const int p0 = blockIdx.x * gpc32;
   const int len = max(0, min(a.nq, p0 + gpc32) - p0);  // multiple of 32
   uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
-  const float* lrow = a.spec_logits + (bh * G) * (int64_t)a.Lcap + p0;
-  for (int i = 4 * tid; i < len; i += 4 * kThreads) {
-    float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int gi = 0; gi < G; ++gi) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(lrow + (int64_t)gi * a.Lcap + i));
-      const float nl = s_nlse[gi];
-      sc.x += fast_exp2(fmaf(v.x, 1.4426950408889634f, nl));
-      sc.y += fast_exp2(fmaf(v.y, 1.4426950408889634f, nl));
-      sc.z += fast_exp2(fmaf(v.z, 1.4426950408889634f, nl));
-      sc.w += fast_exp2(fmaf(v.w, 1.4426950408889634f, nl));
+  if (a.sel_onchip) {
+    // From TMEM: warp w holds its records' halves, lane = token, column 4 (NH it + hf) + head, the
+    // logits as the separate path stores them (natural-log units); the fetched positions' logits are
+    // the prologue's, in sel_rowlog, and replace the low-bit ones below.
+    constexpr int NH = GROUP / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int u_begin = blockIdx.x * (a.groups_per_chunk / NH);
+    const int u_end = min(a.nq / GROUP, u_begin + a.groups_per_chunk / NH);
+    const int n_my = (u_end - u_begin - warp + kWarps - 1) / kWarps;
+    const uint32_t tw = tmem_base + ((uint32_t)(32 * warp) << 16);
+    for (int it = 0; it < n_my; ++it)
+      for (int hf = 0; hf < NH; ++hf) {
+        const float4 v = tmem_ld4(tw + 4 * (NH * it + hf));
+        const float l[4] = {v.x, v.y, v.z, v.w};
+        float sc = 0.f;
+        for (int gi = 0; gi < G; ++gi) sc += fast_exp2(fmaf(l[gi], 1.4426950408889634f, s_nlse[gi]));
+        const int g = NH * (u_begin + warp + it * kWarps) + hf;
+        keys[32 * g + lane - p0] = __float_as_uint(sc);
+      }
+    // TMEM is released here, before the candidates, by the warp that allocated it
+    tmem_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+      tmem_fence_after_sync();
+      tmem_dealloc(tmem_base, kTmemCols);
     }
-    *reinterpret_cast<uint4*>(keys + i) =
-        make_uint4(__float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
+    if (a.k > 0) {
+      // the fetched positions in [p0, p0 + len): idx is ascending (then -1 padding)
+      const int32_t* ix = a.idx + bh * a.k;
+      for (int j = tid; j < a.k; j += kThreads) {
+        const int p = ix[j];
+        if (p >= p0 && p < p0 + len) {
+          const float* lr = a.sel_rowlog + (bh * a.k + j) * 4;
+          float sc = 0.f;
+          for (int gi = 0; gi < G; ++gi) sc += fast_exp2(fmaf(lr[gi], 1.4426950408889634f, s_nlse[gi]));
+          keys[p - p0] = __float_as_uint(sc);
+        }
+      }
+    }
+  } else {
+    const float* lrow = a.spec_logits + (bh * G) * (int64_t)a.Lcap + p0;
+    for (int i = 4 * tid; i < len; i += 4 * kThreads) {
+      float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int gi = 0; gi < G; ++gi) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(lrow + (int64_t)gi * a.Lcap + i));
+        const float nl = s_nlse[gi];
+        sc.x += fast_exp2(fmaf(v.x, 1.4426950408889634f, nl));
+        sc.y += fast_exp2(fmaf(v.y, 1.4426950408889634f, nl));
+        sc.z += fast_exp2(fmaf(v.z, 1.4426950408889634f, nl));
+        sc.w += fast_exp2(fmaf(v.w, 1.4426950408889634f, nl));
+      }
+      *reinterpret_cast<uint4*>(keys + i) =
+          make_uint4(__float_as_uint(sc.x), __float_as_uint(sc.y), __float_as_uint(sc.z), __float_as_uint(sc.w));
+    }
   }
   __syncthreads();
   const int kloc = min(a.sel_keff, len);
@@ -1156,6 +1271,7 @@ template <int BITS, int GROUP, bool MERGED, bool FETCH, bool TOPK, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   extern __shared__ __align__(16) uint8_t dyn_smem[];
   __shared__ int s_last;
+  __shared__ uint32_t s_tmem;  // TMEM base of the on-chip selection
   static_assert(sizeof(SelShared<kThreads>) <= kMaxRows * kTilePitch * sizeof(float),
                 "the selection's shared state reuses the query tile");
   __shared__ float s_ml[2 * kMaxRows];
@@ -1180,7 +1296,13 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
     }
     __syncthreads();
   };
-  lowbit_cta<BITS, GROUP, MERGED, FETCH>(a, dyn_smem, s_q, merge, fill_query);
+  if constexpr (TOPK) {
+    if (a.sel_onchip && threadIdx.x < 32) {  // warp 0 allocates; the query fill's barrier publishes it
+      tmem_alloc(&s_tmem, kTmemCols);
+      tmem_fence_before_sync();
+    }
+  }
+  lowbit_cta<BITS, GROUP, MERGED, FETCH, TOPK>(a, dyn_smem, s_q, merge, &s_tmem, fill_query);
   if constexpr (CLUSTER) {
     cluster_combine(merge, a, reinterpret_cast<float*>(dyn_smem + kClusterPartOffset));
     return;
@@ -1190,7 +1312,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(AttnArgs a) {
   const bool combined = merge_store_combine(merge, a, &s_last, s_ml, s_w, kPartCap);
   if constexpr (TOPK) {
     __syncthreads();  // the query tile and the merge buffer are free from here on
-    select_epilogue<BITS>(a, dyn_smem, *reinterpret_cast<SelShared<kThreads>*>(s_q), combined, &s_last, s_ml);
+    select_epilogue<BITS, GROUP>(a, dyn_smem, *reinterpret_cast<SelShared<kThreads>*>(s_q), combined, &s_last, s_ml,
+                                 s_tmem);
   }
 }
 

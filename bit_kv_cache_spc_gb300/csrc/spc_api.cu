@@ -15,6 +15,7 @@ spc_status launch_attention(const spc_dims*, const void*, const uint16_t*, const
 size_t step_workspace_bytes(const spc_dims*, int32_t);
 int attn_kernel_count(const spc_dims*, int32_t, int32_t);
 int step_kernel_count(const spc_dims*, int32_t, int32_t, int32_t);
+bool step_onchip(const spc_dims*, int32_t, int32_t, int32_t);
 spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t);
 spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
                               int32_t, cudaStream_t);
@@ -293,6 +294,13 @@ int32_t spc_decode_step_kernel_count(const spc_dims* d, int32_t k, int32_t fetch
   return spc::step_kernel_count(d, k, fetch_k, next_k);
 }
 
+int32_t spc_decode_step_on_chip(const spc_dims* d, int32_t k, int32_t fetch_k, int32_t next_k) {
+  if (check_dims(d) != SPC_OK || k < 0 || k > (1 << 24) || fetch_k < 0 || fetch_k > (1 << 24) || next_k < 0 ||
+      next_k > (1 << 24))
+    return -1;
+  return spc::step_onchip(d, k, fetch_k, next_k) ? 1 : 0;
+}
+
 size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max) {
   if (check_dims(d) != SPC_OK || k_max < 0 || k_max > (1 << 24)) return 0;
   return spc::step_workspace_bytes(d, k_max);
@@ -309,8 +317,12 @@ spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_
   const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
   if (next_k < 0 || next_k > (1 << 24)) return SPC_ERR_INVALID;
   if (next_bitmap == nullptr || (next_k > 0 && next_idx == nullptr)) return SPC_ERR_INVALID;
-  if (nq > 0 && (spec_logits == nullptr || lse == nullptr)) return SPC_ERR_INVALID;
+  if (nq > 0 && lse == nullptr) return SPC_ERR_INVALID;
   if (nq > 262144) return SPC_ERR_UNSUPPORTED;
+  // without a logits buffer the selection must ride on the attention with the logits on chip
+  if (nq > 0 && spec_logits == nullptr &&
+      (fetch_k < 0 || fetch_k > (1 << 24) || k < 0 || k > (1 << 24) || !spc::step_onchip(d, k, fetch_k, next_k)))
+    return SPC_ERR_UNSUPPORTED;
   spc::PrefetchJob job{nullptr, fetch_n_cap, fetch_idx, fetch_k, fetch_staging};
   const spc::PrefetchJob* pf = nullptr;
   if (fetch_k != 0) {

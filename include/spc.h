@@ -240,7 +240,16 @@ int32_t spc_attn_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k);
  *            before any is written).
  *   ws, ws_bytes: at least spc_step_workspace_bytes(d, max(k, next_k)),
  *            zero-filled once (the same contract as spc_attn_workspace_bytes).
- *   lse and spec_logits are required (non-NULL).
+ *   lse is required (non-NULL).
+ *   spec_logits: as spc_merged_attn's, or NULL to keep the speculative
+ *            logits on chip: every CTA then holds its chunk's logits in its
+ *            SM's tensor memory (TMEM, 128 of the SM's 512 columns, lane =
+ *            token, column = head) from the low-bit loop to its selection, so
+ *            they are neither written to nor read back from device memory;
+ *            only the fetched rows' logits (k x 4 floats per (b, hkv)) pass
+ *            through the workspace.  The selection is identical.  NULL is
+ *            accepted when spc_decode_step_on_chip returns 1 for the same
+ *            arguments, else the call returns SPC_ERR_UNSUPPORTED.
  *   fetch_*: as spc_merged_attn_fetch; fetch_k = 0 for none.
  * Every CTA of the launch must be resident at once (the attention's grid is
  * one wave of the GPU): if other work holds the SMs for long enough, the
@@ -250,6 +259,11 @@ int32_t spc_attn_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k);
  * separately, right after, on the same stream, with the same results.
  */
 size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max);
+/* 1 when spc_decode_step with these arguments can keep the speculative logits
+ * on chip (spec_logits == NULL): the selection rides on the attention launch
+ * (k > 0) and each warp's 32-token groups need at most 32 x 4 TMEM columns.
+ * 0 otherwise, -1 for an invalid shape or a negative count.  A host-side query. */
+int32_t spc_decode_step_on_chip(const spc_dims* d, int32_t k, int32_t fetch_k, int32_t next_k);
 /* Kernels one spc_decode_step with these arguments enqueues on the current
  * device: 1 when the selection rides on the attention launch, else the
  * attention's (spc_attn_kernel_count) plus the separate top-k.  -1 for an

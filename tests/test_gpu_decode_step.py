@@ -141,3 +141,107 @@ def test_decode_step_wait_that_nothing_releases_runs_out():
     torch.cuda.synchronize()
     assert spc.spc_read_device_status(ws, g.d) == 6  # SPC_ERR_TIMEOUT
     assert spc.spc_read_device_status(ws, g.d) == 0  # cleared by the read
+
+
+ONCHIP = [c for c in CASES if c["k"] > 0]
+
+
+@pytest.mark.parametrize("cfg", ONCHIP, ids=cid)
+@pytest.mark.parametrize("with_self", [False, True])
+def test_decode_step_with_logits_on_chip_equals_separate_calls(cfg, with_self):
+    """spec_logits=None: each CTA keeps its chunk's speculative logits in TMEM
+    from the low-bit loop to its selection.  Outputs, selection and bitmap
+    must equal the separate calls' bit for bit."""
+    import bit_kv_cache_spc_gb300 as spc
+    g, idx, bm = prepare(cfg, seed=8)
+    k = cfg["k"]
+    if spc.spc_decode_step_on_chip(g.d, k, 0, k) != 1:
+        pytest.skip("this shape keeps its logits in device memory")
+    ks = None
+    if with_self:
+        K1, V1 = synth.kv_layer(16, 0, cfg["B"], cfg["Hkv"], 1)
+        ks = torch.from_numpy(np.stack([K1[:, :, 0], V1[:, :, 0]], axis=2).view(np.int16).copy()).cuda()
+    ref_o, ref_lse, ref_lg = g.merged(idx, bm, k, kv_self=ks)
+    ref_idx, ref_bm = g.topk(ref_lg, ref_lse, k)
+    ws = torch.zeros(spc.spc_step_workspace_bytes(g.d, k), dtype=torch.uint8, device="cuda")
+    o, lse, _ = g.new_out()
+    nidx = torch.full_like(idx, -9)
+    nbm = torch.full_like(bm, 0x77)
+    for _ in range(2):  # the workspace's control words are reset by each call
+        spc.spc_decode_step(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o, lse, None, k, nidx, nbm, ws,
+                            kv_self=ks)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+        assert torch.equal(nidx, ref_idx) and torch.equal(nbm, ref_bm)
+    assert spc.spc_read_device_status(ws, g.d) == 0
+
+
+def test_decode_step_on_chip_with_fetch_job_and_limits():
+    """On-chip logits with a pre-fetch riding along; the LLaMA-3-8B decode
+    shape qualifies, a shape whose warps hold more than 32 groups does not
+    and refuses spec_logits=None."""
+    import bit_kv_cache_spc_gb300 as spc
+    d4 = spc.Dims(8, 32, 8, 32768, 128, 1)
+    assert spc.spc_decode_step_on_chip(d4, 328, 328, 328) == 1
+    big = spc.Dims(4, 32, 8, 131072, 128, 1)
+    assert spc.spc_decode_step_on_chip(big, 1311, 0, 1311) == 0
+    cfg = dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41)
+    g, idx, bm = prepare(cfg, seed=9)
+    k = cfg["k"]
+    ref_o, ref_lse, ref_lg = g.merged(idx, bm, k)
+    ref_idx, ref_bm = g.topk(ref_lg, ref_lse, k)
+    K2, V2 = synth.kv_layer(10, 1, cfg["B"], cfg["Hkv"], 500)
+    host2 = torch.from_numpy(np.stack([K2, V2], axis=3).view(np.int16)).pin_memory()
+    rng = np.random.default_rng(6)
+    fk = 70
+    fidx = np.sort(rng.choice(500, size=(cfg["B"], cfg["Hkv"], fk)), axis=-1).astype(np.int32)
+    fst = torch.zeros((cfg["B"], cfg["Hkv"], fk, 2, 128), dtype=torch.int16, device="cuda")
+    assert spc.spc_decode_step_on_chip(g.d, k, fk, k) == 1
+    ws = torch.zeros(spc.spc_step_workspace_bytes(g.d, k), dtype=torch.uint8, device="cuda")
+    o, lse, _ = g.new_out()
+    nidx, nbm = torch.empty_like(idx), torch.empty_like(bm)
+    spc.spc_decode_step(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o, lse, None, k, nidx, nbm, ws,
+                        fetch_host_kv=host2, fetch_n_cap=500, fetch_idx=torch.from_numpy(fidx).cuda(), fetch_k=fk,
+                        fetch_staging=fst)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    assert torch.equal(nidx, ref_idx) and torch.equal(nbm, ref_bm)
+    d2 = oracle.dims(B=cfg["B"], Hq=cfg["Hq"], Hkv=cfg["Hkv"], N=500, R=0, bits=1)
+    assert np.array_equal(fst.cpu().numpy().view(np.uint16), oracle.gather(d2, np.stack([K2, V2], axis=3), fidx))
+    # a shape that cannot keep its logits on chip refuses a missing logits buffer
+    cfgb = dict(B=4, Hq=32, Hkv=8, N=131072, R=128, bits=1, k=1311)
+    gb = GpuLayer(cfgb, host=False)
+    wsb = torch.zeros(spc.spc_step_workspace_bytes(gb.d, cfgb["k"]), dtype=torch.uint8, device="cuda")
+    ob, lseb, _ = gb.new_out()
+    ib = torch.zeros((4, 8, cfgb["k"]), dtype=torch.int32, device="cuda")
+    bb = torch.zeros((4, 8, gb.d.q_groups_cap), dtype=torch.int32, device="cuda")
+    with pytest.raises(spc.SpcError) as e:
+        spc.spc_decode_step(gb.d, gb.records, gb.resid, gb.q, ib, bb, gb.staging, cfgb["k"], ob, lseb, None, cfgb["k"],
+                            ib, bb, wsb)
+    assert e.value.status == 2
+
+
+def test_decode_step_on_chip_wait_that_nothing_releases_runs_out():
+    """The same run-out with the logits on chip: the CTAs that waited still
+    score their chunk from tensor memory and release it, and the fault is
+    reported once."""
+    import bit_kv_cache_spc_gb300 as spc
+    cfg = dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41)
+    g, idx, bm = prepare(cfg, seed=7)
+    k = cfg["k"]
+    assert spc.spc_decode_step_on_chip(g.d, k, 0, k) == 1
+    ws = torch.zeros(spc.spc_step_workspace_bytes(g.d, k), dtype=torch.uint8, device="cuda")
+    ws.view(torch.int32)[0] = 1 << 20  # ticket of (b, hkv) 0
+    o, lse, _ = g.new_out()
+    nidx, nbm = torch.empty_like(idx), torch.empty_like(bm)
+    spc.spc_decode_step(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o, lse, None, k, nidx, nbm, ws)
+    torch.cuda.synchronize()
+    assert spc.spc_read_device_status(ws, g.d) == 6  # SPC_ERR_TIMEOUT
+    assert spc.spc_read_device_status(ws, g.d) == 0
+    # the device is still usable: a clean call on a fresh workspace matches the separate calls
+    ref_o, ref_lse, ref_lg = g.merged(idx, bm, k)
+    ref_idx, ref_bm = g.topk(ref_lg, ref_lse, k)
+    ws2 = torch.zeros_like(ws)
+    spc.spc_decode_step(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o, lse, None, k, nidx, nbm, ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(nidx, ref_idx) and torch.equal(nbm, ref_bm)
