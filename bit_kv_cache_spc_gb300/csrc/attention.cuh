@@ -130,11 +130,10 @@ struct Layout {
   static constexpr int WARP_BYTES = STAGES * STAGE + kZsBytes;
   static constexpr int DYN = kWarps * WARP_BYTES;  // dynamic shared memory of one CTA
   // 16-bit rows staged per batch in a warp's stages after the first and its
-  // z/s table (512 bytes and kMaxRows probabilities each; an even number)
+  // z/s table: 16, or 8 when 16 padded rows do not fit
   static constexpr int TAIL = (STAGES - 1) * STAGE + kZsBytes;
-  static constexpr int ROWB = (TAIL / (512 + kMaxRows * 4)) >= 16 ? 16 : (TAIL / (512 + kMaxRows * 4)) & ~1;
-  static_assert(ROWB >= 8, "a row batch of at least 8 fits a warp's free stages");
-  static_assert(kMaxRows * kTilePitch * 4 <= TAIL, "the transfer tile fits a warp's free stages");
+  static constexpr int ROWB = TAIL >= 16 * (512 + 16) ? 16 : 8;
+  static_assert(ROWB * (512 + 16) <= TAIL, "a row batch fits a warp's free stages");
   static_assert(RB % 512 == 0, "a record is streamed as whole 512-byte warp copies");
 };
 
@@ -270,40 +269,72 @@ struct CtaMerge {
 constexpr int kClusterPartOffset = (int)((sizeof(CtaMerge) + 15) / 16 * 16);
 
 // ------------------------------------------------------------ 16-bit rows
-// Reduce-scatter of 16 per-lane partial sums: returns the warp-wide sum of
-// x[lane >> 1], halving the vector at each butterfly step (16 shuffles).
-__device__ __forceinline__ float reduce_scatter16(const float (&x)[16], int lane) {
-  float y8[8], y4[4], y2[2];
-  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    y8[k] = (u16 ? x[k + 8] : x[k]) + __shfl_xor_sync(0xFFFFFFFFu, u16 ? x[k] : x[k + 8], 16);
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    y4[k] = (u8 ? y8[k + 4] : y8[k]) + __shfl_xor_sync(0xFFFFFFFFu, u8 ? y8[k] : y8[k + 4], 8);
-#pragma unroll
-  for (int k = 0; k < 2; ++k)
-    y2[k] = (u4 ? y4[k + 2] : y4[k]) + __shfl_xor_sync(0xFFFFFFFFu, u4 ? y4[k] : y4[k + 2], 4);
-  const float y1 = (u2 ? y2[1] : y2[0]) + __shfl_xor_sync(0xFFFFFFFFu, u2 ? y2[0] : y2[1], 2);
-  return y1 + __shfl_xor_sync(0xFFFFFFFFu, y1, 1);
+// bf16 tensor-core product D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_16816_bf16(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// Four 8x8 b16 matrices from shared memory; lane l gives the row address of
+// matrix l / 8, row l % 8.  .trans delivers each matrix transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(row)));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(row)));
+}
+// Two floats as bf16x2 (x in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+// x = l1 + l2 + l3 in bf16 (each the rounding of what the previous ones leave;
+// the first two remainders are exact in binary32), for two values at once.
+__device__ __forceinline__ void split3_bf16(float2 x, uint32_t& l1, uint32_t& l2, uint32_t& l3) {
+  l1 = pack_bf16x2(x.x, x.y);
+  const float2 r1 = f2_sub(x, unpack_bf16x2(l1));
+  l2 = pack_bf16x2(r1.x, r1.y);
+  const float2 r2 = f2_sub(r1, unpack_bf16x2(l2));
+  l3 = pack_bf16x2(r2.x, r2.y);
+}
+constexpr int kRowPitch = 512 + 16;  // bytes per staged 16-bit row (K then V, padded: conflict-free ldmatrix)
 
 // The residual window and the fetched rows of this warp's range, before its
-// low-bit groups (whose first stage is already in flight).  Rows are staged
-// ROWB at a time with cp.async into `tail` (the warp's stages after the
-// first and its z/s table, free until the low-bit loop starts).  fill_query() is the CTA-wide
-// fill of sq (it ends with a barrier); the positions of the warp's first
-// fetched rows are loaded before it, so that both latencies overlap.  Logits: lane = 4 channels x 8 query rows for two rows at a
-// time, then a reduce-scatter leaves lane with row (lane >> 4), query row
-// (lane >> 1) & 7.  Value product: lane = 4 channels, p broadcast from shared
-// memory.  sq is the CTA's scaled query tile [kMaxRows][kTilePitch] (rows
-// 2G.. zero).  On return (m_run, l_run, oacc) hold the softmax state of the
-// rows, in the tensor-core fragment layouts of the low-bit loop (oacc divided by the per-channel powers of two that loop
-// multiplies back at its end).
+// low-bit groups (whose first stage is already in flight), on the tensor
+// cores with exact bf16 operands.  Rows are staged ROWB at a time (a multiple
+// of 8) with cp.async into `tail` (the warp's stages after the first and its
+// z/s table, free until the low-bit loop starts), kRowPitch bytes apart.
+// fill_query() is the CTA-wide fill of sq (it ends with a barrier); the
+// positions of the warp's first fetched rows are loaded before it, so that
+// both latencies overlap.
+//   Logits: D(16 x 8 rows) = A (scaled query, the 8 query rows' three bf16
+//   limbs: limbs 1 and 2 as rows 0..7 and 8..15 of one product, limb 3 in a
+//   second) x B (the rows' keys, straight from shared memory by ldmatrix);
+//   lane (gid, t) then holds query row gid's logits of rows 2t, 2t+1 (and
+//   8 + ...) of each 8-row tile: the softmax layout of the low-bit loop.
+//   Values: oacc (channels x query rows) += A (V^T, ldmatrix.trans) x B (the
+//   probabilities in two bf16 limbs, two products), B being the lane's own
+//   probabilities.
+// sq is the CTA's scaled query tile [kMaxRows][kTilePitch] (rows 2G.. zero).
+// On return (m_run, l_run, oacc) hold the softmax state of the rows in the
+// fragment layouts of the low-bit loop (oacc divided by the per-channel powers
+// of two that loop multiplies back at its end; l_run this lane's share).
 template <bool MERGED, bool TOPK, int ROWB, typename FillQuery>
 __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* sq, uint8_t* tail,
                                                 FillQuery&& fill_query, float& m_run, float& l_run,
                                                 float (&oacc)[8][4]) {
+  constexpr int NT = ROWB / 8;  // 8-row tiles per batch
+  static_assert(ROWB % 8 == 0 && NT >= 1 && NT <= 2, "batches of 8 or 16 rows");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, t = lane & 3;
   const int64_t bh = blockIdx.y;
@@ -318,15 +349,14 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
   const int per_warp = (n_rows + n_warps - 1) / n_warps;
   const int j0 = min(n_rows, (int)(blockIdx.x * kWarps + warp) * per_warp);
   const int j1 = min(n_rows, j0 + per_warp);
-  float* pb = reinterpret_cast<float*>(tail + ROWB * 512);  // p of a batch: [row][query row]
-  const int rho_l = (lane >> 1) & 7;
-  const bool spec_lane = MERGED && a.spec_logits != nullptr && (lane & 1) == 0 && rho_l >= G && rho_l < 2 * G;
-  float* spec_out = spec_lane ? a.spec_logits + (bh * G + (rho_l - G)) * (int64_t)a.Lcap : nullptr;
-  const bool rowlog_lane = TOPK && MERGED && a.sel_rowlog != nullptr && (lane & 1) == 0 && rho_l >= G && rho_l < 2 * G;
-  float m_own = kNeg, l_own = 0.f;  // state of query row rho_l
-  float o16[kMaxRows][4];
+  const bool spec_lane = MERGED && a.spec_logits != nullptr && gid >= G && gid < 2 * G;
+  float* spec_out = spec_lane ? a.spec_logits + (bh * G + (gid - G)) * (int64_t)a.Lcap : nullptr;
+  const bool rowlog_lane = TOPK && MERGED && a.sel_rowlog != nullptr && gid >= G && gid < 2 * G;
+
+  m_run = kNeg;
+  l_run = 0.f;
 #pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho) o16[rho][0] = o16[rho][1] = o16[rho][2] = o16[rho][3] = 0.f;
+  for (int mt = 0; mt < 8; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
   // quantised position of the fetched row of lane (window w0), -1 for the residual window
   auto row_pos = [&](int w0) {
     const int j = w0 + lane;
@@ -334,6 +364,10 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
   };
   const int pos_first = row_pos(j0);
   fill_query();
+  if (j0 >= j1) return;
+
+  // the scaled query's three bf16 limbs, as A fragments: lane row gid, channels 16 kc + 2t (+1, +8, +9)
+  const float* qrow = sq + gid * kTilePitch;
 
   for (int w0 = j0; w0 < j1; w0 += 32) {
     const int nwin = min(32, j1 - w0);
@@ -342,112 +376,130 @@ __device__ __forceinline__ void rows16_prologue(const AttnArgs& a, const float* 
     const uint32_t valid = __ballot_sync(0xFFFFFFFFu, ok);
     for (int b0 = 0; b0 < nwin; b0 += ROWB) {
       const int nb = min(ROWB, nwin - b0);
-      for (int i = 0; i < nb; ++i) {
-        if ((valid >> (b0 + i)) & 1u) {
+      for (int i = 0; i < ROWB; ++i) {
+        uint8_t* dst = tail + kRowPitch * i + 16 * lane;
+        if (i < nb && ((valid >> (b0 + i)) & 1u)) {
           const int j = w0 + b0 + i;
           const uint16_t* row = j < a.r        ? a.resid + (bh * a.resid_cap + j) * 2 * kD
                                 : j == j_self ? a.kv_self + bh * 2 * kD
                                               : a.staging + (bh * a.k + (j - a.r)) * 2 * kD;
-          cp_async16(tail + 512 * i + 16 * lane, row + 8 * lane);
+          cp_async16(dst, row + 8 * lane);
+        } else {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);  // no stale bits under a zero probability
         }
       }
       cp_async_commit();
       cp_async_wait<0>();  // with the first batch, also the low-bit stages issued before it
       __syncwarp();
 
-      float lg[ROWB / 2];
+      // ---- logits: query rows x the batch's rows ----
+      float c12[NT][4], c3[NT][4];
 #pragma unroll
-      for (int pp = 0; pp < ROWB / 2; ++pp) {
-        lg[pp] = kNeg;
-        if (2 * pp < nb) {
-          float x[16];
+      for (int nt = 0; nt < NT; ++nt) c12[nt][0] = c12[nt][1] = c12[nt][2] = c12[nt][3] = c3[nt][0] = c3[nt][1] =
+          c3[nt][2] = c3[nt][3] = 0.f;
 #pragma unroll
-          for (int jh = 0; jh < 2; ++jh) {
-            const uint2 kk = *reinterpret_cast<const uint2*>(tail + 512 * (2 * pp + jh) + 8 * lane);
-            const float k0 = bf16_to_f32(kk.x & 0xFFFFu), k1 = bf16_to_f32(kk.x >> 16);
-            const float k2 = bf16_to_f32(kk.y & 0xFFFFu), k3 = bf16_to_f32(kk.y >> 16);
+      for (int kc = 0; kc < 8; ++kc) {
+        uint32_t a12[4], a3[4];
+        {
+          const float2 x01 = *reinterpret_cast<const float2*>(qrow + 16 * kc + 2 * t);
+          const float2 x89 = *reinterpret_cast<const float2*>(qrow + 16 * kc + 2 * t + 8);
+          split3_bf16(x01, a12[0], a12[1], a3[0]);
+          split3_bf16(x89, a12[2], a12[3], a3[2]);
+          a3[1] = a3[3] = 0u;
+        }
+        // keys: matrices (tile nt, channels 16kc + 8h) for h = 0, 1; lane l addresses row 8 (l >> 4) + (l & 7)
+        uint32_t kb[4];
+        ldsm_x4(kb, tail + kRowPitch * (8 * (NT == 2 ? (lane >> 4) : 0) + (lane & 7)) + 2 * (16 * kc + 8 * ((lane >> 3) & 1)));
 #pragma unroll
-            for (int rho = 0; rho < kMaxRows; ++rho) {
-              const float4 qq = *reinterpret_cast<const float4*>(sq + rho * kTilePitch + 4 * lane);
-              x[8 * jh + rho] = fmaf(qq.w, k3, fmaf(qq.z, k2, fmaf(qq.y, k1, qq.x * k0)));
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_16816_bf16(c12[nt], a12, kb[2 * nt], kb[2 * nt + 1]);
+          mma_16816_bf16(c3[nt], a3, kb[2 * nt], kb[2 * nt + 1]);
+        }
+      }
+      // lane: query row gid, batch rows 8 nt + 2t + e
+      float lg[NT][2];
+      int posr[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int i = 8 * nt + 2 * t + e;
+          const float v = (c12[nt][e] + c12[nt][2 + e]) + c3[nt][e];
+          const int j = w0 + b0 + i;
+          posr[nt][e] = __shfl_sync(0xFFFFFFFFu, pos, (b0 + i) & 31);
+          const bool seen = i < nb && ((valid >> ((b0 + i) & 31)) & 1u) && !(j == j_self && gid < G);
+          lg[nt][e] = seen ? v : kNeg;
+        }
+      if (spec_lane || rowlog_lane) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int pi = posr[nt][e];
+            if (lg[nt][e] != kNeg && pi >= 0) {
+              if (spec_lane) spec_out[pi] = lg[nt][e] * CUDART_LN2_F;
+              if (TOPK && rowlog_lane)  // fetched row j of this (b, hkv), head gid - G
+                a.sel_rowlog[(bh * a.k + (w0 + b0 + 8 * nt + 2 * t + e - a.r)) * 4 + (gid - G)] =
+                    lg[nt][e] * CUDART_LN2_F;
             }
           }
-          const float v = reduce_scatter16(x, lane);
-          const int i = 2 * pp + (lane >> 4);
-          // the speculative token's own row is masked for the output token's rows
-          if (i < nb && ((valid >> (b0 + i)) & 1u) && !(w0 + b0 + i == j_self && rho_l < G)) lg[pp] = v;
+      }
+      // ---- online softmax (base 2): query row gid's max over the four lanes of the row ----
+      float mx = lg[0][0] > lg[0][1] ? lg[0][0] : lg[0][1];
+      if (NT == 2) mx = fmaxf(mx, fmaxf(lg[NT - 1][0], lg[NT - 1][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      if (__any_sync(0xFFFFFFFFu, m_new != m_run)) {
+        const float alpha = fast_exp2(m_run - m_new);
+        const float al_a = __shfl_sync(0xFFFFFFFFu, alpha, (2 * t) * 4);
+        const float al_b = __shfl_sync(0xFFFFFFFFu, alpha, (2 * t + 1) * 4);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          oacc[mt][0] *= al_a;
+          oacc[mt][1] *= al_b;
+          oacc[mt][2] *= al_a;
+          oacc[mt][3] *= al_b;
         }
-        const int pi = __shfl_sync(0xFFFFFFFFu, pos, b0 + 2 * pp + (lane >> 4));
-        if (spec_lane && lg[pp] != kNeg && pi >= 0) spec_out[pi] = lg[pp] * CUDART_LN2_F;
-        if (TOPK && rowlog_lane && lg[pp] != kNeg && pi >= 0)  // fetched row j of this (b, hkv), head rho_l - G
-          a.sel_rowlog[(bh * a.k + (w0 + b0 + 2 * pp + (lane >> 4) - a.r)) * 4 + (rho_l - G)] = lg[pp] * CUDART_LN2_F;
+        l_run *= alpha;
+        m_run = m_new;
       }
-
-      float mx = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-      const float m_new = fmaxf(m_own, mx);
-      const float alpha = fast_exp2(m_own - m_new);
-      float ps = 0.f, p[ROWB / 2];
+      const float m_use = fmaxf(m_run, 0.5f * kNeg);  // a masked logit gives exactly 0
+      uint32_t ph[NT], pl[NT];
 #pragma unroll
-      for (int pp = 0; pp < ROWB / 2; ++pp) {
-        p[pp] = lg[pp] == kNeg ? 0.f : fast_exp2(lg[pp] - m_new);
-        ps += p[pp];
+      for (int nt = 0; nt < NT; ++nt) {
+        const float p0 = fast_exp2(lg[nt][0] - m_use), p1 = fast_exp2(lg[nt][1] - m_use);
+        l_run += p0 + p1;
+        ph[nt] = pack_bf16x2(p0, p1);
+        const float2 rem = f2_sub(make_float2(p0, p1), unpack_bf16x2(ph[nt]));
+        pl[nt] = pack_bf16x2(rem.x, rem.y);
       }
-      ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 16);
-      l_own = l_own * alpha + ps;
-      m_own = m_new;
-      if ((lane & 1) == 0) {
+      // ---- values: oacc += V^T (channels x rows) x P (rows x query rows), P in two bf16 limbs ----
+      // B fragment: k = rows 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1), n = query row gid -- this lane's p
+      const uint32_t bh0 = ph[0], bh1 = NT == 2 ? ph[NT - 1] : 0u;
+      const uint32_t bl0 = pl[0], bl1 = NT == 2 ? pl[NT - 1] : 0u;
 #pragma unroll
-        for (int pp = 0; pp < ROWB / 2; ++pp) pb[(2 * pp + (lane >> 4)) * kMaxRows + rho_l] = p[pp];
+      for (int mt = 0; mt < 8; ++mt) {
+        // matrices (rows 8 (l >> 4) .., channels 16 mt + 8 ((l >> 3) & 1)), transposed
+        uint32_t va[4];
+        ldsm_x4_trans(va, tail + kRowPitch * (8 * (NT == 2 ? (lane >> 4) : 0) + (lane & 7)) + 2 * kD +
+                              2 * (16 * mt + 8 * ((lane >> 3) & 1)));
+        if (NT == 1) va[2] = va[3] = 0u;  // rows 8..15 do not exist in an 8-row batch
+        mma_16816_bf16(oacc[mt], va, bh0, bh1);
+        mma_16816_bf16(oacc[mt], va, bl0, bl1);
       }
-#pragma unroll
-      for (int rho = 0; rho < kMaxRows; ++rho) {
-        const float al = __shfl_sync(0xFFFFFFFFu, alpha, 2 * rho);
-        o16[rho][0] *= al;
-        o16[rho][1] *= al;
-        o16[rho][2] *= al;
-        o16[rho][3] *= al;
-      }
-      __syncwarp();
-      for (int i = 0; i < nb; ++i) {
-        if (!((valid >> (b0 + i)) & 1u)) continue;  // uniform across the warp
-        const uint2 vv = *reinterpret_cast<const uint2*>(tail + 512 * i + 2 * kD + 8 * lane);
-        const float v0 = bf16_to_f32(vv.x & 0xFFFFu), v1 = bf16_to_f32(vv.x >> 16);
-        const float v2 = bf16_to_f32(vv.y & 0xFFFFu), v3 = bf16_to_f32(vv.y >> 16);
-        const float4 pa = *reinterpret_cast<const float4*>(pb + i * kMaxRows);
-        const float4 pc = *reinterpret_cast<const float4*>(pb + i * kMaxRows + 4);
-        const float pr[kMaxRows] = {pa.x, pa.y, pa.z, pa.w, pc.x, pc.y, pc.z, pc.w};
-#pragma unroll
-        for (int rho = 0; rho < kMaxRows; ++rho) {
-          o16[rho][0] = fmaf(pr[rho], v0, o16[rho][0]);
-          o16[rho][1] = fmaf(pr[rho], v1, o16[rho][1]);
-          o16[rho][2] = fmaf(pr[rho], v2, o16[rho][2]);
-          o16[rho][3] = fmaf(pr[rho], v3, o16[rho][3]);
-        }
-      }
-      __syncwarp();
+      __syncwarp();  // the batch's rows are read before the next batch is staged
     }
   }
-  // hand the state over to the fragment layout through `tail`
-  float* tile = reinterpret_cast<float*>(tail);  // [kMaxRows][kTilePitch]
-#pragma unroll
-  for (int rho = 0; rho < kMaxRows; ++rho)
-    *reinterpret_cast<float4*>(tile + rho * kTilePitch + 4 * lane) =
-        make_float4(o16[rho][0], o16[rho][1], o16[rho][2], o16[rho][3]);
-  __syncwarp();
-  // oacc[mt]: (channel 16mt+gid, row 2t), (16mt+gid, 2t+1), (16mt+gid+8, 2t), (16mt+gid+8, 2t+1)
+  // the low-bit loop multiplies its accumulators by per-channel powers of two at its end
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     const float c0 = 1.f / bit_comp(2 * mt), c1 = 1.f / bit_comp(2 * mt + 1);
-    oacc[mt][0] = tile[(2 * t) * kTilePitch + 16 * mt + gid] * c0;
-    oacc[mt][1] = tile[(2 * t + 1) * kTilePitch + 16 * mt + gid] * c0;
-    oacc[mt][2] = tile[(2 * t) * kTilePitch + 16 * mt + gid + 8] * c1;
-    oacc[mt][3] = tile[(2 * t + 1) * kTilePitch + 16 * mt + gid + 8] * c1;
+    oacc[mt][0] *= c0;
+    oacc[mt][1] *= c0;
+    oacc[mt][2] *= c1;
+    oacc[mt][3] *= c1;
   }
-  __syncwarp();
-  m_run = __shfl_sync(0xFFFFFFFFu, m_own, 2 * gid);
-  const float lr = __shfl_sync(0xFFFFFFFFu, l_own, 2 * gid);
-  l_run = t == 0 ? lr : 0.f;  // the low-bit loop sums l over the four lanes of a row at its end
 }
 
 // ------------------------------------------------------------ low-bit CTA
