@@ -539,18 +539,23 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   const int n_my = (u_end - u_begin - warp + kWarps - 1) / kWarps;  // records of this warp
   const uint8_t* rec_base = a.records + (bh * a.units_cap) * (int64_t)RB;
 
-  // Pre-fetch rows of this warp: rr = slot + n_slots * i, carried by items
-  // 0, pf_every, 2 pf_every, ... (one 512-byte row per carried item), the
-  // rest copied after the groups.
-  const int64_t n_slots = (int64_t)gridDim.x * gridDim.y * kWarps;
-  const int64_t slot = ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * kWarps + warp;
-  const int n_pf = (FETCH && a.pf_rows > slot) ? (int)((a.pf_rows - slot + n_slots - 1) / n_slots) : 0;
-  // At most one carried row per pipeline depth (a warp then waits on at most
-  // one host read at a time); the rows beyond that go after the groups.
+  // Pre-fetch rows of this warp: rr = pf_slot + pf_nslots * i.  Row 0 rides
+  // on item 0 (the first low-bit stage, which the 16-bit-row prologue waits
+  // for); row i > 0 on item i * pf_every + pf_ph, at most one per pipeline
+  // depth, so that a warp waits on at most one host read at a time.  The
+  // phase pf_ph (the warp's slot modulo the spacing) spreads the host reads
+  // of neighbouring warps over consecutive items: the warps of the grid
+  // advance in step, and reads that they all issue in the same item arrive at
+  // the host link as one burst.  Rows beyond the warp's items are copied
+  // after the groups.
+  const int pf_nslots = gridDim.x * gridDim.y * kWarps;
+  const int pf_slot = (blockIdx.y * gridDim.x + blockIdx.x) * kWarps + warp;
+  const int n_pf = (FETCH && a.pf_rows > pf_slot) ? (a.pf_rows - pf_slot + pf_nslots - 1) / pf_nslots : 0;
   const int pf_every = n_pf > 0 ? max(kStages, n_my / n_pf) : 1;
-  const int pf_carried = n_pf > 0 ? min(n_pf, (n_my + pf_every - 1) / pf_every) : 0;
-  int pf_next = n_pf > 0 ? a.pf_idx[slot] : -1;  // position of the next row to issue
-  int pf_issue_i = 0, pf_issue_item = 0;          // next carried row on the issue side and its item
+  const int pf_ph = pf_slot % pf_every;
+  const int pf_carried = (n_pf > 0 && n_my > 0) ? min(n_pf, 1 + max(0, (n_my - 1 - pf_ph) / pf_every)) : 0;
+  int pf_next = n_pf > 0 ? a.pf_idx[pf_slot] : -1;  // position of the next row to issue
+  int pf_issue_i = 0, pf_issue_item = 0;             // next carried row on the issue side and its item
 
   auto issue = [&](int item) {
     if (item < n_my) {
@@ -561,17 +566,21 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
       for (int w = 0; w < RB / 512; ++w) cp_async16(dst + 16 * (lane + 32 * w), src + 16 * (lane + 32 * w));
       // the record's bitmap words (one per 32-token half) into the slot's first words
       if (MERGED && lane < NH) cp_async4(dst + RB + 4 * lane, a.bitmap + bh * a.q_groups_cap + NH * u + lane);
-      if (FETCH && item == pf_issue_item && pf_issue_i < pf_carried) {
-        const int64_t rr = slot + n_slots * pf_issue_i;
-        const int n = pf_next;
-        if (lane == 0) reinterpret_cast<int*>(dst + RB)[3] = n;
-        if (n >= 0 && n < a.pf_ncap) {
-          const int64_t src_row = ((rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
-          cp_async16(dst + PFROW + 16 * lane, a.pf_host + src_row + 8 * lane);
+      if constexpr (FETCH) {
+        // the slot's words 2, 3: (row, position) of the row this item carries, else (-1, -1)
+        const bool carry = item == pf_issue_item && pf_issue_i < pf_carried;
+        const int rr = pf_slot + pf_nslots * pf_issue_i;
+        const int n = carry ? pf_next : -1;
+        if (lane == 0) reinterpret_cast<int2*>(dst + RB)[1] = make_int2(carry ? rr : -1, n);
+        if (carry) {
+          if (n >= 0 && n < a.pf_ncap) {
+            const int64_t src_row = ((int64_t)(rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
+            cp_async16(dst + PFROW + 16 * lane, a.pf_host + src_row + 8 * lane);
+          }
+          pf_next = (pf_issue_i + 1 < n_pf) ? a.pf_idx[rr + pf_nslots] : -1;
+          ++pf_issue_i;
+          pf_issue_item = pf_issue_i * pf_every + pf_ph;
         }
-        pf_next = (pf_issue_i + 1 < n_pf) ? a.pf_idx[rr + n_slots] : -1;
-        ++pf_issue_i;
-        pf_issue_item += pf_every;
       }
     }
     cp_async_commit();
@@ -612,7 +621,6 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   const bool spec_row = row_valid && gid >= G && a.spec_logits != nullptr;
   float* spec_out = spec_row ? a.spec_logits + ((bh * G + (gid - G)) * (int64_t)a.Lcap) : nullptr;
 
-  int pf_use_i = 0, pf_use_item = 0;  // next carried row on the consuming side and its item
 #pragma unroll 1
   for (int it = 0; it < n_my; ++it) {
     issue(it + kStages - 1);
@@ -620,15 +628,11 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     __syncwarp();
     const uint8_t* R = stage + (it % kStages) * STAGE;
     const int u = u_begin + warp + it * kWarps;
-    if (FETCH && it == pf_use_item && pf_use_i < pf_carried) {
-      const int n = reinterpret_cast<const int*>(R + RB)[3];
-      if (n >= 0 && n < a.pf_ncap) {
-        const int64_t rr = slot + n_slots * pf_use_i;
-        reinterpret_cast<uint4*>(a.pf_staging + rr * (2 * kD))[lane] =
+    if constexpr (FETCH) {  // the carried row, if any, to the staging buffer
+      const int2 pr = reinterpret_cast<const int2*>(R + RB)[1];
+      if (pr.x >= 0 && pr.y >= 0 && pr.y < a.pf_ncap)
+        reinterpret_cast<uint4*>(a.pf_staging + (int64_t)pr.x * (2 * kD))[lane] =
             reinterpret_cast<const uint4*>(R + PFROW)[lane];
-      }
-      ++pf_use_i;
-      pf_use_item += pf_every;
     }
 
 #pragma unroll 1
@@ -870,12 +874,12 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   cp_async_wait<0>();
   // pre-fetch rows this warp's groups did not carry, four host reads in flight at a time
   for (int i0 = pf_carried; i0 < n_pf; i0 += 4) {
-    int64_t rr[4];
+    int rr[4];
     int n[4];
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      rr[u] = slot + n_slots * (i0 + u);
+      rr[u] = pf_slot + pf_nslots * (i0 + u);
       n[u] = i0 + u < n_pf ? a.pf_idx[rr[u]] : -1;
     }
 #pragma unroll
@@ -884,7 +888,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
         v[u] = reinterpret_cast<const uint4*>(a.pf_host + ((rr[u] / a.pf_k) * a.pf_ncap + n[u]) * (2 * kD))[lane];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (n[u] >= 0 && n[u] < a.pf_ncap) reinterpret_cast<uint4*>(a.pf_staging + rr[u] * (2 * kD))[lane] = v[u];
+      if (n[u] >= 0 && n[u] < a.pf_ncap) reinterpret_cast<uint4*>(a.pf_staging + (int64_t)rr[u] * (2 * kD))[lane] = v[u];
   }
   // undo the powers of two of the value-bit expansion, per channel
 #pragma unroll
