@@ -539,23 +539,23 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   const int n_my = (u_end - u_begin - warp + kWarps - 1) / kWarps;  // records of this warp
   const uint8_t* rec_base = a.records + (bh * a.units_cap) * (int64_t)RB;
 
-  // Pre-fetch rows of this warp: rr = pf_slot + pf_nslots * i.  Row 0 rides
-  // on item 0 (the first low-bit stage, which the 16-bit-row prologue waits
-  // for); row i > 0 on item i * pf_every + pf_ph, at most one per pipeline
-  // depth, so that a warp waits on at most one host read at a time.  The
-  // phase pf_ph (the warp's slot modulo the spacing) spreads the host reads
-  // of neighbouring warps over consecutive items: the warps of the grid
-  // advance in step, and reads that they all issue in the same item arrive at
-  // the host link as one burst.  Rows beyond the warp's items are copied
-  // after the groups.
+  // Pre-fetch rows of this warp: rr = pf_slot + pf_nslots * i, row i on
+  // item i * pf_every + pf_ph, at most one per pipeline depth, so that a
+  // warp waits on at most one host read at a time.  The phase pf_ph (the
+  // warp's slot modulo the spacing) spreads the host reads of neighbouring
+  // warps over consecutive items: the warps of the grid advance in step, and
+  // reads that they all issue in the same item arrive at the host link as one
+  // burst.  (Phase 0 carries its first row on item 0, the first low-bit
+  // stage, which the 16-bit-row prologue waits for.)  Rows beyond the warp's
+  // items are copied after the groups.
   const int pf_nslots = gridDim.x * gridDim.y * kWarps;
   const int pf_slot = (blockIdx.y * gridDim.x + blockIdx.x) * kWarps + warp;
   const int n_pf = (FETCH && a.pf_rows > pf_slot) ? (a.pf_rows - pf_slot + pf_nslots - 1) / pf_nslots : 0;
   const int pf_every = n_pf > 0 ? max(kStages, n_my / n_pf) : 1;
   const int pf_ph = pf_slot % pf_every;
-  const int pf_carried = (n_pf > 0 && n_my > 0) ? min(n_pf, 1 + max(0, (n_my - 1 - pf_ph) / pf_every)) : 0;
+  const int pf_carried = (n_pf > 0 && n_my > pf_ph) ? min(n_pf, 1 + (n_my - 1 - pf_ph) / pf_every) : 0;
   int pf_next = n_pf > 0 ? a.pf_idx[pf_slot] : -1;  // position of the next row to issue
-  int pf_issue_i = 0, pf_issue_item = 0;             // next carried row on the issue side and its item
+  int pf_issue_i = 0, pf_issue_item = pf_ph;         // next carried row on the issue side and its item
 
   auto issue = [&](int item) {
     if (item < n_my) {
