@@ -63,6 +63,54 @@ __device__ __forceinline__ uint32_t quant_code(float x, float z, float s, float 
   }
 }
 
+// bf16 bit patterns in value order and back: ord increases with the value
+// (-0 just below +0, NaN patterns outside every finite and infinite value).
+__device__ __forceinline__ uint32_t bf16_ord(uint32_t b) { return (b & 0x8000u) ? (b ^ 0xFFFFu) : (b | 0x8000u); }
+__device__ __forceinline__ uint32_t bf16_unord(uint32_t o) { return (o & 0x8000u) ? (o & 0x7FFFu) : (o ^ 0xFFFFu); }
+
+// The smallest bf16 value x of a group's range [lo, hi] whose code
+// quant_code<BITS>(x, z, s, rs) is at least `level` (1 .. 2^BITS - 1), as a
+// float; NaN when no x of the range reaches it.  quant_code is the code of
+// the IEEE quotient fl(fl(x - z) / s), a non-decreasing function of x, so an
+// element of the group has code >= level exactly when x >= the threshold (a
+// NaN element compares false, code 0, as quant_code gives it).  Checked at
+// both ends of the range first (lo's code is not always 0: when 3 min + max
+// overflows binary32, z = -inf and every element codes 1), then in the
+// bracket (lo, hi]: the bf16 value at the analytic point z + (level - 1/2) s
+// and its two neighbours settle it unless binary32 absorbs x - z over a run
+// of bf16 values there (tiny x near a zero midpoint), which bisection then
+// resolves.
+template <int BITS>
+__device__ __forceinline__ float code_threshold(float lo, float hi, float z, float s, float rs, uint32_t level) {
+  auto ge = [&](uint32_t o) {
+    return quant_code<BITS>(__uint_as_float(bf16_unord(o) << 16), z, s, rs) >= level;
+  };
+  uint32_t a = bf16_ord(__float_as_uint(lo) >> 16), b = bf16_ord(__float_as_uint(hi) >> 16);
+  if (!(a <= b) || !ge(b)) return __int_as_float(0x7FC00000);
+  if (ge(a)) return __uint_as_float(bf16_unord(a) << 16);
+  // invariant: code(a) < level <= code(b)
+  const float guess = __fadd_rn(z, __fmul_rn((float)level - 0.5f, s));
+  const uint32_t og = min(max(bf16_ord(__float_as_uint(guess) >> 16), a + 1u), b);
+  if (ge(og)) {
+    b = og;
+    if (og - 1u > a) {
+      if (!ge(og - 1u)) return __uint_as_float(bf16_unord(og) << 16);
+      b = og - 1u;
+    }
+  } else {
+    a = og;
+    if (og + 1u < b) {
+      if (ge(og + 1u)) return __uint_as_float(bf16_unord(og + 1u) << 16);
+      a = og + 1u;
+    }
+  }
+  while (b - a > 1u) {
+    const uint32_t m = (a + b) >> 1;
+    if (ge(m)) b = m; else a = m;
+  }
+  return __uint_as_float(bf16_unord(b) << 16);
+}
+
 // min/max of bf16 values carried as floats; -0.0 is stored as +0.0.
 __device__ __forceinline__ uint32_t bf16_bits_canonical(float f) {
   return f == 0.0f ? 0u : (__float_as_uint(f) >> 16);
@@ -80,7 +128,7 @@ struct QuantArgs {
 // is last: the g = 32 quantiser codes one 32-token group at a time and
 // launches without it (more resident CTAs hide the loads instead).
 struct QuantSmem {
-  float kz[kD], krs[kD], kss[kD];  // per key channel: z, 1/s, s
+  float kt[3][kD];  // per key channel: 1 bit: the code threshold (code_threshold); 2 bits: z, s, 1/s
   uint32_t klohi[kD];
   uint32_t rec[256 * 3];             // the record being assembled (up to 3 KB)
   uint16_t tile[2][2][kGroup * kD];  // [tile][keys, values][token][channel]
@@ -139,22 +187,30 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
     }
     float z, s;
     quant_params(BITS, lo, hi, z, s);
-    sm.kz[c] = z;
-    sm.kss[c] = s;
-    sm.krs[c] = quant_recip(s);
+    const float rs = quant_recip(s);
+    if (BITS == 1) {
+      sm.kt[0][c] = code_threshold<1>(lo, hi, z, s, rs, 1u);
+    } else {  // three thresholds of the dearer 2-bit code cost more than the codes they replace
+      sm.kt[0][c] = z;
+      sm.kt[1][c] = s;
+      sm.kt[2][c] = rs;
+    }
     sm.klohi[c] = bf16_bits_canonical(lo) | (bf16_bits_canonical(hi) << 16);
   }
   __syncthreads();
 
-  // ---- key codes: warp per token, one ballot per code word ----
+  // ---- key codes: warp per token, one ballot per code word.  At 1 bit a
+  // code is one comparison with the channel's threshold, found once per
+  // channel for the group's tokens (a value group's 32 elements are spread
+  // over 4 lanes, 8 each, and the 2-bit code needs three thresholds: there the
+  // per-element quotient costs less) ----
   {
-    float z[4], s[4], rs[4];
+    float T[4][3];  // 1 bit: the channel's threshold; 2 bits: its z, s, 1/s
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int c = kblock + 2 * t + half;
-      z[t] = sm.kz[c];
-      s[t] = sm.kss[c];
-      rs[t] = sm.krs[c];
+#pragma unroll
+      for (int l = 0; l < (BITS == 1 ? 1 : 3); ++l) T[t][l] = sm.kt[l][c];
     }
     for (int n = 8 * warp; n < 8 * warp + 8; ++n) {  // token n = 8 j + a
       const uint4 blk = *reinterpret_cast<const uint4*>(ks + n * kD + kblock);
@@ -163,7 +219,7 @@ __device__ __forceinline__ void code_group(QuantSmem& sm, const uint16_t* ks, co
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const float x = bf16_to_f32(half ? (wv[t] >> 16) : (wv[t] & 0xFFFFu));
-        const uint32_t code = quant_code<BITS>(x, z[t], s[t], rs[t]);
+        const uint32_t code = BITS == 1 ? (x >= T[t][0] ? 1u : 0u) : quant_code<BITS>(x, T[t][0], T[t][1], T[t][2]);
         const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, code & 1u);
         const int word = 4 * (4 * aa + t) + j;
         if (BITS == 2) {
