@@ -107,12 +107,20 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        self.started = False
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        # the sampler's first line comes before the timed region and is dropped: every kept sample is
+        # taken while the timed work runs
+        import select
+        ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+        if ready:
+            self.started = bool(self.proc.stdout.readline())
         return self
 
     def __exit__(self, *exc):
@@ -133,7 +141,9 @@ class ClockSampler:
 
     def summary(self):
         if not getattr(self, "rows", None):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            why = "nvidia-smi unavailable" if self.proc is None or not self.started else \
+                "no nvidia-smi sample during the timed region"
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [why], "samples": 0}
         sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
