@@ -22,6 +22,10 @@ Patterns:
   near_max    magnitudes next to the largest finite bf16, one sign (3 min + max
               overflows) or both signs (max - min overflows)
   wide        values spanning 2^-20 .. 2^20 with both signs
+  absorbed    min = -max exactly (a zero midpoint) with tiny values of both
+              signs around 0 (2^-40 .. 2^-20 of max) and zeros: x - z
+              rounds to -z in binary32 for a run of them, so the 1-bit code
+              changes far from the midpoint in bf16 order
   normal      N(0, 1) rounded to bf16 (control)
 """
 from __future__ import annotations
@@ -110,6 +114,10 @@ def _pattern(name, rng, L):
         kind = int(rng.integers(0, 3))
         vals = pos if kind == 0 else neg if kind == 1 else pos[:3] + neg[:3]
         return _fill(rng, L, vals)
+    if name == "absorbed":
+        a = float(2.0 ** rng.integers(-6, 6) * (1 + rng.integers(0, 128) / 128.0))
+        tiny = a * np.power(2.0, rng.uniform(-40, -20, size=12)) * rng.choice([-1, 1], size=12)
+        return _fill(rng, L, list(_bf16([a, -a])) + list(_bf16(tiny)) + [0x0000, 0x8000])
     if name == "wide":
         x = np.power(2.0, rng.uniform(-20, 20, size=L)) * rng.choice([-1, 1], size=L)
         return _bf16(x)
@@ -118,7 +126,7 @@ def _pattern(name, rng, L):
 
 
 PATTERNS = ["midpoint1", "halfstep2", "third2", "constant", "zeros", "subnormal", "tiny", "near_max", "wide",
-            "normal"]
+            "absorbed", "normal"]
 
 
 def edge_kv(seed, B, Hkv, N, group=32, D=128):
