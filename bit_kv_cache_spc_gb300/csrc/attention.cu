@@ -100,6 +100,11 @@ static AttnPlan attn_plan(const spc_dims* d, bool fetch) {
     const int64_t slots = (int64_t)spc_host::sm_count() * variant(d).resident_ctas(fetch);
     int64_t chunks = std::max<int64_t>(1, slots / BH);
     chunks = std::min<int64_t>(chunks, (nu + kWarps - 1) / kWarps);
+    // A short row goes to at most kMaxCluster CTAs, whose partials then
+    // combine in one cluster (one kernel instead of two), when each CTA then
+    // holds at most 32 groups of 32 tokens: measured faster there (batch 1-4
+    // at 4K-16K tokens), slower with more groups per CTA.
+    if (chunks > kMaxCluster && ((int64_t)nu * nh + kMaxCluster - 1) / kMaxCluster <= 32) chunks = kMaxCluster;
     const int upc = (int)((nu + chunks - 1) / chunks);
     p.chunks = (nu + upc - 1) / upc;
     p.groups_per_chunk = upc * nh;

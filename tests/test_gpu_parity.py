@@ -247,8 +247,9 @@ def test_kernel_counts_of_the_combine_paths():
     of resident 9-CTA clusters holds for 64 pairs, so its attention calls are
     two kernels (the grid, then the combine kernel), and so is batch 1 at 128K
     (76 CTAs per pair); B*Hkv = 128 at N = 4096 (4 CTAs per pair) combines in
-    clusters, one kernel; spc_decode_step at configuration 4 carries its
-    selection, one kernel."""
+    clusters, one kernel, and so does B*Hkv = 32 at N = 4096, whose short rows
+    are held to 16 CTAs per pair (at most 32 groups each) so that they can;
+    spc_decode_step at configuration 4 carries its selection, one kernel."""
     d4 = spc.Dims(8, 32, 8, 32768, 128, 1)
     assert spc.spc_attn_kernel_count(d4, 0, 0) == 2
     assert spc.spc_attn_kernel_count(d4, 328, 328) == 2
@@ -256,6 +257,7 @@ def test_kernel_counts_of_the_combine_paths():
     assert spc.spc_decode_step_kernel_count(d4, 0, 0, 328) == 3  # no fetched rows: nothing to fuse with
     assert spc.spc_attn_kernel_count(spc.Dims(1, 32, 8, 131072, 128, 1), 1311, 0) == 2
     assert spc.spc_attn_kernel_count(spc.Dims(16, 32, 8, 4096, 128, 1), 41, 0) == 1
+    assert spc.spc_attn_kernel_count(spc.Dims(4, 32, 8, 4096, 128, 1), 41, 0) == 1
 
 
 def test_gather_exact_and_unmapped_pointer_refused():
