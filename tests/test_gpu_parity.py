@@ -168,8 +168,11 @@ def test_k0_merged_is_attn2_and_all_fetched_is_bf16_attention():
 @pytest.mark.parametrize("cfg", [dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41),
                                  dict(B=1, Hq=4, Hkv=4, N=300, R=64, bits=2, k=7),
                                  dict(B=1, Hq=4, Hkv=1, N=64, R=32, bits=1, k=24),
-                                 dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41, group=64)],
-                         ids=["many_groups", "mha_2bit", "rows_exceed_groups", "g64"])
+                                 dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41, group=64),
+                                 dict(B=8, Hq=32, Hkv=8, N=4224, R=128, bits=1, k=41),
+                                 dict(B=1, Hq=8, Hkv=2, N=19936, R=128, bits=1, k=200)],
+                         ids=["many_groups", "mha_2bit", "rows_exceed_groups", "g64", "unclustered_64_rows",
+                              "more_warps_than_records"])
 def test_merged_attention_with_fetch_job(cfg):
     """spc_merged_attn_fetch: the attention results equal spc_merged_attn's and the
     pre-fetched rows equal the oracle's gather, also when the job has more rows
@@ -190,6 +193,8 @@ def test_merged_attention_with_fetch_job(cfg):
     fidx[0, 0, 3] = -1
     fst = torch.zeros((cfg["B"], cfg["Hkv"], fk, 2, 128), dtype=torch.int16, device="cuda")
     o, lse, lg = g.new_out()
+    if cfg["N"] > 4200:  # 9 CTAs per row that do not fit as clusters, or 155 (with 620 warps for 619 records)
+        assert spc.spc_attn_kernel_count(g.d, k, fk) == 2
     spc.spc_merged_attn_fetch(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o, lse, lg, g.ws, host2,
                               cfg["N"], torch.from_numpy(fidx).cuda(), fk, fst)
     torch.cuda.synchronize()
