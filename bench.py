@@ -777,6 +777,8 @@ class LayerRig:
         self.staging = torch.zeros((B, Hkv, max(self.kmax, 1), 2, 128), dtype=torch.int16, device=dev)
         self.ws_bytes = spc.spc_attn_workspace_bytes(d, self.kmax)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
+        self.ws_step_bytes = spc.spc_step_workspace_bytes(d, self.kmax)
+        self.ws_step = torch.zeros(max(self.ws_step_bytes, 16), dtype=torch.uint8, device=dev)  # zero-filled once
         self.flush = torch.empty(self.FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.Stream()
         torch.cuda.synchronize()
@@ -804,6 +806,18 @@ class LayerRig:
         its top-k and the pre-fetch of the new selection (for the next step)."""
         self.merged(k)
         self.topk(k)
+        self.gather(k)
+
+    def decode_step_fused(self, k):
+        """The same step through spc_decode_step: the merged attention and its
+        top-k in one launch where the selection fits the attention's shared
+        memory (the logits kept on chip where allowed), else as the library's
+        two launches; then the pre-fetch of the new selection."""
+        spc, d = self.spc, self.d
+        logits = None if spc.spc_decode_step_on_chip(d, k, 0, k) == 1 else self.logits
+        spc.spc_decode_step(d, self.records, self.resid, self.q, self.idx, self.bitmap, self.staging, k, self.o,
+                            self.lse, logits, k, self.idx, self.bitmap, self.ws_step, self.ws_step_bytes,
+                            stream=self.stream)
         self.gather(k)
 
     def time_us(self, fn, reps=10):
@@ -875,12 +889,15 @@ def measure_config(cfg, peak_gbs, oracle_on=True, reps=10, rig=None):
         g_us = rig.time_us(lambda: rig.gather(k), reps)
         m_us = rig.time_us(lambda: rig.merged(k), reps)
         step_us = rig.graph_us(lambda: rig.decode_step(k), reps)
+        fused_us = rig.graph_us(lambda: rig.decode_step_fused(k), reps)
         mb = attention_bytes(cfg, rig.nq, k)
         a2b = attention_bytes(cfg, rig.nq, 0)
         gb = bh * k * 512
         pt = {"B": cfg["B"], "N": cfg["N"], "bits": cfg["bits"], "group": cfg.get("group", 32), "k": k,
               "low_bit_bytes_per_token": low_bit_bytes_per_token(cfg["bits"], cfg.get("group", 32)),
-              "decode_step_graph_us": step_us, "merged_us": m_us, "attn2_us": a2_us, "topk_us": t_us,
+              "decode_step_graph_us": step_us, "decode_step_fused_graph_us": fused_us,
+              "decode_step_fused_launches": rig.spc.spc_decode_step_kernel_count(rig.d, k, 0, k),
+              "merged_us": m_us, "attn2_us": a2_us, "topk_us": t_us,
               "gather_us": g_us, "quantize_us": q_us,
               "merged_bytes": mb, "merged_hbm_frac": mb / (m_us * 1e-6) / 1e9 / peak_gbs,
               "attn2_hbm_frac": a2b / (a2_us * 1e-6) / 1e9 / peak_gbs,
