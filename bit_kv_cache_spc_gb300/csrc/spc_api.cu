@@ -371,6 +371,7 @@ spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const fl
   if (k < 0 || k > (1 << 24)) return SPC_ERR_INVALID;
   if (bitmap == nullptr || (k > 0 && idx == nullptr)) return SPC_ERR_INVALID;
   if (nq > 0 && (spec_logits == nullptr || lse == nullptr)) return SPC_ERR_INVALID;
+  if (nq > 0 && !aligned16(spec_logits)) return SPC_ERR_INVALID;  // read in 16-byte pieces
   if (nq > 262144) return SPC_ERR_UNSUPPORTED;
   if (d->q_groups_cap == 0 && k == 0) return SPC_OK;
   return spc::launch_topk(d, spec_logits, lse, k, idx, bitmap, reinterpret_cast<cudaStream_t>(stream));

@@ -349,7 +349,7 @@ spc_status spc_append_kv(const spc_dims* d, const uint16_t* k_new, const uint16_
  * Ties go to the lower position.  Outputs: idx int32 [B][Hkv][k], ascending,
  * entries k_eff..k-1 set to -1; bitmap u32 [B][Hkv][q_groups_cap] with
  * exactly the selected bits set (words past N_q/32 are zeroed).
- * N_q <= 262144.
+ * N_q <= 262144; spec_logits 16-byte aligned (SPC_ERR_INVALID otherwise).
  */
 spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse,
                            int32_t k, int32_t* idx, uint32_t* bitmap, spc_stream stream);

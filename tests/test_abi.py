@@ -71,6 +71,9 @@ def test_validation_happens_before_any_launch(spc):
     with pytest.raises(spc.SpcError) as e:  # negative k
         spc.spc_topk_select(d, 16, 16, -1, 16, 16, stream=0)
     assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # speculative logits not on a 16-byte boundary
+        spc.spc_topk_select(d, 20, 16, 4, 16, 16, stream=0)
+    assert e.value.status == 1
 
 
 def test_kernel_count_queries_refuse_bad_arguments(spc):
