@@ -1191,9 +1191,11 @@ def main():
                        "bits": W["bits"], "k": W["k"], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (4.3 GB low-bit cache per step, 129 MB L2); no flush",
                        "graph": "one CUDA graph per step",
-                       "replay": "every timed step replays the same queries, so the same rows are selected and "
-                                 "fetched each step (see e2e and fresh_queries for changing queries); the "
-                                 "decode-time append of the new token is not in the step (see append)",
+                       "replay": "every timed step replays the same queries; the selection then alternates with "
+                                 "period two (a fetched row's exact logit replaces its low-bit estimate in the "
+                                 "next step): consecutive steps share 38% of their selected rows, steps two apart "
+                                 "all of them (see e2e and fresh_queries for changing queries); the decode-time "
+                                 "append of the new token is not in the step (see append)",
                        "prefetch": {"side": f"side stream, {args.gather_ctas} CTAs",
                                     "fused": "fused into the next layer's attention",
                                     "step": "fused into the next layer's attention, which also ends with "
