@@ -82,6 +82,10 @@ def parse():
     p.add_argument("--gather-ctas", type=int, default=32, help="grid of the side-stream pre-fetch kernel")
     p.add_argument("--prefetch-lag", type=int, default=2,
                    help="overlap placement: layer l's attention carries the pre-fetch of layer l-LAG's selection")
+    p.add_argument("--profile-call", choices=["attn2", "merged", "merged_fetch", "topk", "gather"], default=None,
+                   help="(profiling) one decode layer of the workload: run its calls once, then this call "
+                        "--profile-reps times, and exit; a profiler captures the call's kernels")
+    p.add_argument("--profile-reps", type=int, default=4)
     return p.parse_args()
 
 
@@ -983,6 +987,37 @@ def job_throughput(world, steps, total_ms):
 
 # ------------------------------------------------------------------ main
 
+def profile_call(W, call, reps):
+    """One decode layer of the workload resident on the device: the low-bit
+    cache, the first attention, its top-k and the gather of the selection;
+    then `call` reps times back to back (merged_fetch carries the pre-fetch of
+    a second layer's selection).  Prints one line and exits."""
+    import torch
+    cfg = dict(workload=W["workload"], B=W["B"], Hq=W["Hq"], Hkv=W["Hkv"], N=W["N"], R=W["R"], bits=W["bits"],
+               ks=[W["k"]], pairs=1)
+    k = W["k"]
+    rig = LayerRig(cfg)
+    rig.attn2()
+    rig.topk(k)
+    rig.gather(k)
+    other = None
+    if call == "merged_fetch":
+        other = LayerRig(cfg, layer=1)
+        other.attn2()
+        other.topk(k)
+    fst = torch.zeros_like(rig.staging)
+    fns = {"attn2": rig.attn2, "merged": lambda: rig.merged(k), "topk": lambda: rig.topk(k),
+           "gather": lambda: rig.gather(k),
+           "merged_fetch": lambda: rig.spc.spc_merged_attn_fetch(
+               rig.d, rig.records, rig.resid, rig.q, rig.idx, rig.bitmap, rig.staging, k, rig.o, rig.lse,
+               rig.logits, rig.ws, other.host, W["N"], other.idx, k, fst, ws_bytes=rig.ws_bytes, stream=rig.stream)}
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        fns[call]()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_call": call, "reps": reps, "workload": W["workload"]}))
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -990,6 +1025,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     W = dict(WORKLOAD)
     W["layers"] = args.layers
+
+    if args.profile_call:
+        profile_call(W, args.profile_call, args.profile_reps)
+        return
 
     if args.oracle_1core:
         out = {}
