@@ -80,6 +80,9 @@ def parse():
                         "(then top-k as its own launch), or 'step': one spc_decode_step launch per layer "
                         "(attention + carried pre-fetch + fused top-k)")
     p.add_argument("--gather-ctas", type=int, default=32, help="grid of the side-stream pre-fetch kernel")
+    p.add_argument("--refetch-all", action="store_true",
+                   help="overlap placement: fetch every selected row from the host each step, instead of keeping "
+                        "the rows that the layer's previous selection already staged")
     p.add_argument("--prefetch-lag", type=int, default=2,
                    help="overlap placement: layer l's attention carries the pre-fetch of layer l-LAG's selection")
     p.add_argument("--profile-call", choices=["attn2", "merged", "merged_fetch", "topk", "gather"], default=None,
@@ -189,8 +192,21 @@ def make_timing_event(torch):
 
 # ------------------------------------------------------------------ the GPU workload
 
+class GraphPair:
+    """The graphs of one step for the two buffer parities; each replay runs
+    the graph of the owner's current parity and flips it, so that every graph
+    pair of the owner stays in step with the buffers."""
+
+    def __init__(self, owner, graphs):
+        self.owner, self.graphs = owner, graphs
+
+    def replay(self):
+        self.graphs[self.owner.parity].replay()
+        self.owner.parity ^= 1
+
+
 class DecodeStep:
-    def __init__(self, W, layers, seed=0, mode="fused", gather_ctas=32, lag=2):
+    def __init__(self, W, layers, seed=0, mode="fused", gather_ctas=32, lag=2, keep_staged=True):
         import torch
 
         import bit_kv_cache_spc_gb300 as spc
@@ -225,6 +241,17 @@ class DecodeStep:
         self.idx = torch.zeros((layers, B, Hkv, k), dtype=torch.int32, device=dev)
         self.bitmap = torch.zeros((layers, B, Hkv, d.q_groups_cap), dtype=torch.int32, device=dev)
         self.staging = torch.zeros((layers, B, Hkv, k, 2, 128), dtype=torch.int16, device=dev)
+        # Overlap placement: the rows still staged from a layer's previous selection are kept.  Selections
+        # and staging alternate between two buffers by step parity (the previous ones are read while the
+        # next are written); src[l] says where each newly selected row of layer l sat in its previous
+        # selection (-1: read it from the host).
+        self.keep = keep_staged and mode == "overlap"
+        self.parity = 0
+        if self.keep:
+            self.idx_b = [self.idx, torch.full_like(self.idx, -1)]
+            self.bitmap_b = [self.bitmap, torch.zeros_like(self.bitmap)]
+            self.staging_b = [self.staging, torch.zeros_like(self.staging)]
+            self.src = torch.full((layers, B, Hkv, k), -1, dtype=torch.int32, device=dev)
         self.ws_bytes = spc.spc_attn_workspace_bytes(d, k)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # zero-filled once
         self.ws_step_bytes = spc.spc_step_workspace_bytes(d, k)
@@ -260,16 +287,17 @@ class DecodeStep:
                                            "overlap": attn_f + 1}[mode]
         self.graph = None
 
-    def enqueue(self, timed=False):
+    def enqueue(self, timed=False, parity=0):
+        self.capture_parity = parity
         if self.mode == "fused":
             return self.enqueue_fused(timed)
         if self.mode == "step":
             return self.enqueue_step(timed)
         if self.mode == "overlap":
-            return self.enqueue_overlap(timed)
+            return self.enqueue_overlap(timed, parity=self.capture_parity)
         return self.enqueue_side(timed)
 
-    def enqueue_overlap(self, timed=False, fetch=True, topk=True):
+    def enqueue_overlap(self, timed=False, fetch=True, topk=True, parity=0):
         """One decode step on two streams.  Layer l's merged attention (main
         stream, high priority) carries the pre-fetch of layer (l - lag)'s
         selection (lag >= 2), so it does not wait for the top-k of the layers
@@ -278,26 +306,44 @@ class DecodeStep:
         l's attention waits only for layer (l - lag)'s top-k.  Every layer's
         rows are still fetched before that layer's attention of the next step
         (the last lag layers' rows ride on the next step's first attentions).
+        With the staged rows kept (self.keep), the step of this parity reads
+        the selections and staging of buffer `parity` and writes the next into
+        the other; a pre-fetch copies the rows that its layer's previous
+        selection already staged from that staging, and reads the rest from
+        the host.
         fetch=False: the same step with the staging buffers already filled and
         no pre-fetch (the overlap test's reference).  topk=False: the merged
         attentions alone, back to back on one stream (their kernel time)."""
         spc, d, k = self.spc, self.d, self.k
         main, side, L, lag = self.main, self.side_lo, self.L, self.lag
+        P = parity
         for l in range(L):
             j = (l - lag) % L
+            if self.keep:
+                idx, bitmap, staging = self.idx_b[P][l], self.bitmap_b[P][l], self.staging_b[P][l]
+                if l >= lag:  # layer j's selection of this step, written to the other parity
+                    f_idx, f_out, f_prev = self.idx_b[1 - P][j], self.staging_b[1 - P][j], self.staging_b[P][j]
+                else:  # layer j's selection of the previous step
+                    f_idx, f_out, f_prev = self.idx_b[P][j], self.staging_b[P][j], self.staging_b[1 - P][j]
+            else:
+                idx, bitmap, staging = self.idx[l], self.bitmap[l], self.staging[l]
+                f_idx, f_out, f_prev = self.idx[j], self.staging[j], None
             if topk and l >= lag:  # layers L-lag .. L-1 were selected by the previous replay, which has completed
                 main.wait_event(self.selected[j])
             if timed:
                 self.rec(self.attn_ev[l][0], main)
-            if fetch:
-                spc.spc_merged_attn_fetch(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
-                                          self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws,
-                                          self.host[j], self.W["N"], self.idx[j], k, self.staging[j],
-                                          ws_bytes=self.ws_bytes, stream=main)
+            if fetch and self.keep:
+                spc.spc_merged_attn_fetch_prev(d, self.records[l], self.resid[l], self.q[l], idx, bitmap, staging, k,
+                                               self.o[l], self.lse[l], self.logits[l], self.ws, self.host[j],
+                                               self.W["N"], f_idx, k, f_out, self.src[j], f_prev, k,
+                                               ws_bytes=self.ws_bytes, stream=main)
+            elif fetch:
+                spc.spc_merged_attn_fetch(d, self.records[l], self.resid[l], self.q[l], idx, bitmap, staging, k,
+                                          self.o[l], self.lse[l], self.logits[l], self.ws, self.host[j], self.W["N"],
+                                          f_idx, k, f_out, ws_bytes=self.ws_bytes, stream=main)
             else:
-                spc.spc_merged_attn(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
-                                    self.staging[l], k, self.o[l], self.lse[l], self.logits[l], self.ws,
-                                    self.ws_bytes, stream=main)
+                spc.spc_merged_attn(d, self.records[l], self.resid[l], self.q[l], idx, bitmap, staging, k, self.o[l],
+                                    self.lse[l], self.logits[l], self.ws, self.ws_bytes, stream=main)
             if timed:
                 self.rec(self.attn_ev[l][1], main)
             if not topk:
@@ -306,7 +352,11 @@ class DecodeStep:
             side.wait_event(self.attended[l])
             if timed:
                 self.rec(self.topk_ev[l][0], side)
-            spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=side)
+            if self.keep:
+                spc.spc_topk_select_prev(d, self.logits[l], self.lse[l], k, self.idx_b[1 - P][l],
+                                         self.bitmap_b[1 - P][l], idx, k, self.src[l], stream=side)
+            else:
+                spc.spc_topk_select(d, self.logits[l], self.lse[l], k, self.idx[l], self.bitmap[l], stream=side)
             if timed:
                 self.rec(self.topk_ev[l][1], side)
             self.selected[l].record(side)
@@ -440,8 +490,15 @@ class DecodeStep:
         torch = self.torch
         self.main.wait_stream(torch.cuda.current_stream())
         torch.cuda.synchronize()
-        self.graph = self.capture_graph(lambda: self.enqueue(timed=False))
-        self.graph_timed = self.capture_graph(lambda: self.enqueue(timed=True))
+        self.graph = self.capture_step(lambda P: self.enqueue(timed=False, parity=P))
+        self.graph_timed = self.capture_step(lambda P: self.enqueue(timed=True, parity=P))
+
+    def capture_step(self, enqueue):
+        """The step's graph; with the staged rows kept, one graph per step
+        parity, replayed in turn (GraphPair)."""
+        if not self.keep:
+            return self.capture_graph(lambda: enqueue(0))
+        return GraphPair(self, [self.capture_graph(lambda: enqueue(0)), self.capture_graph(lambda: enqueue(1))])
 
     def capture_graph(self, enqueue):
         torch = self.torch
@@ -477,6 +534,15 @@ class DecodeStep:
     def replay_timed(self):
         with self.torch.cuda.stream(self.main):
             self.graph_timed.replay()
+
+    def kept_fraction(self):
+        """Of the rows the last step's pre-fetches staged, the fraction copied
+        from the previous staging instead of read from the host (None when
+        every row is read from the host)."""
+        if not self.keep:
+            return None
+        self.torch.cuda.synchronize()
+        return float((self.src >= 0).sum().item()) / float(self.src.numel())
 
     def attn_ms(self):
         return [s.elapsed_time(e) for (s, e) in self.attn_ev]
@@ -1078,7 +1144,8 @@ def main():
         torch.cuda.set_device(0)
     peaks, peak_src = measured_peaks()
 
-    step = DecodeStep(W, args.layers, mode=args.prefetch, gather_ctas=args.gather_ctas, lag=args.prefetch_lag)
+    step = DecodeStep(W, args.layers, mode=args.prefetch, gather_ctas=args.gather_ctas, lag=args.prefetch_lag,
+                      keep_staged=not args.refetch_all)
     step.capture()
     for _ in range(max(3, args.warmup)):
         step.replay()
@@ -1107,6 +1174,7 @@ def main():
     per_layer_topk = step.topk_ms()
     total_ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
     ms_per_step = total_ms / args.steps
+    kept_timed = step.kept_fraction()
     value = job_throughput(world, args.steps, total_ms)
     launches_per_step = step.launches_per_step
 
@@ -1144,6 +1212,7 @@ def main():
     e1.record(step.main)
     barrier()
     fresh_ms = e0.elapsed_time(e1) / args.steps
+    kept_fresh = step.kept_fraction()
     step.q.copy_(q_dev[0])
     del q_dev
     torch.cuda.synchronize()
@@ -1153,7 +1222,7 @@ def main():
     L = args.layers
     overlap = None
     if args.prefetch == "overlap":
-        g_nofetch = step.capture_graph(lambda: step.enqueue_overlap(fetch=False))
+        g_nofetch = step.capture_step(lambda P: step.enqueue_overlap(fetch=False, parity=P))
         t_f, t_n = [], []
         for _ in range(2):
             t_f.append(step.time_graph(step.graph, reps=max(5, args.steps)))
@@ -1163,6 +1232,7 @@ def main():
         overlap = {"steps_per_s_with_prefetch": 1000.0 / tf, "steps_per_s_staging_preloaded": 1000.0 / tn,
                    "delta_pct": 100.0 * (tf - tn) / tn, "hidden": (tf - tn) / tn <= 0.02,
                    "prefetch_bytes_per_step": W["B"] * W["Hkv"] * W["k"] * 512 * L,
+                   "prefetch_host_bytes_per_step": W["B"] * W["Hkv"] * W["k"] * 512 * L * (1.0 - (kept_timed or 0.0)),
                    "link_bound_ms_per_step": None,
                    "what": "the step as timed, against the same step with every layer's selected rows already in "
                            "HBM and no pre-fetch (spc_merged_attn instead of spc_merged_attn_fetch); 'hidden' is "
@@ -1205,6 +1275,7 @@ def main():
             "algorithmic_bytes_per_launch": bytes_layer, "avg_launch_ms": attn_avg_ms,
             "duration_source": dur_src,
             "prefetch_bytes_per_launch": pf_bytes,
+            "prefetch_host_bytes_per_launch": pf_bytes * (1.0 - (kept_timed or 0.0)),
             "prefetch_note": "the carried pre-fetch rows (read over the host link, written to HBM) are not in the "
                              "algorithmic bytes; they are accounted against the host link in 'gather'",
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
@@ -1213,7 +1284,8 @@ def main():
 
     gather = host_link_probe(step, reps=20)
     if overlap is not None:
-        overlap["link_bound_ms_per_step"] = overlap["prefetch_bytes_per_step"] / (gather["host_link_peak_gbs"] * 1e6)
+        overlap["link_bound_ms_per_step"] = (overlap["prefetch_host_bytes_per_step"] /
+                                             (gather["host_link_peak_gbs"] * 1e6))
     append = append_probe(W) if rank == 0 else None
     serial = step.time_serial(max(5, args.steps // 4), args.warmup) if rank == 0 else None
     prefill = prefill_probe(W) if rank == 0 else None
@@ -1240,8 +1312,16 @@ def main():
                                     "step": "fused into the next layer's attention, which also ends with "
                                             "the top-k (spc_decode_step, speculative logits kept in TMEM)",
                                     "overlap": "fused into the attention two layers on; top-k on a "
-                                               "low-priority stream beside the next attention"}[args.prefetch]},
+                                               "low-priority stream beside the next attention" +
+                                               ("; the rows that the layer's previous selection already staged "
+                                                "are copied from HBM, the others read from the host"
+                                                if kept_timed is not None else "")}[args.prefetch]},
             "roofline": roof, "overlap": overlap, "gather": gather,
+            "prefetch_rows": None if kept_timed is None else {
+                "kept": kept_timed, "kept_fresh_queries": kept_fresh,
+                "what": "of the rows each step's pre-fetches stage, the fraction that the layer's previous "
+                        "selection had staged already (copied from HBM; the rest come over the host link): "
+                        "in the timed step, and with the queries rotating over unrelated seeded sets"},
             "fresh_queries": {"value": 1000.0 / fresh_ms, "unit": "steps/s",
                               "what": "the step with the queries rotating over 8 seeded sets already in HBM"},
             "per_layer_us": {"attention": statistics.mean(per_layer) * 1000.0,

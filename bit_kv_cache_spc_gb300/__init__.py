@@ -19,6 +19,7 @@ import torch
 __all__ = [
     "Dims", "SpcError", "spc_abi_version", "spc_num_quantized", "spc_records_bytes", "spc_resid_bytes",
     "spc_quantize_kv", "spc_attn_workspace_bytes", "spc_decode_attn2", "spc_merged_attn", "spc_topk_select",
+    "spc_topk_select_prev", "spc_merged_attn_fetch_prev",
     "spc_host_gather", "spc_merged_attn_noalloc", "spc_merged_attn_fetch", "spc_attn_kernel_count",
     "spc_decode_step_kernel_count", "spc_decode_step_on_chip", "spc_decode_step", "spc_step_workspace_bytes",
     "spc_read_device_status", "spc_append_kv", "spc_offload_kv", "lib_path",
@@ -83,6 +84,9 @@ _sig = {
     "spc_merged_attn_fetch": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t,
                                         _P, C.c_int64, _P, C.c_int32, _P, _P]),
     "spc_topk_select": (C.c_int, [_D, _P, _P, C.c_int32, _P, _P, _P]),
+    "spc_topk_select_prev": (C.c_int, [_D, _P, _P, C.c_int32, _P, _P, _P, C.c_int32, _P, _P]),
+    "spc_merged_attn_fetch_prev": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t,
+                                             _P, C.c_int64, _P, C.c_int32, _P, _P, _P, C.c_int32, _P]),
     "spc_host_gather": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, C.c_int32, _P]),
     "spc_append_kv": (C.c_int, [_D, _P, _P, _P, _P, _P, C.c_int64, _P]),
     "spc_offload_kv": (C.c_int, [_D, _P, _P, _P, C.c_int64, _P]),
@@ -208,6 +212,19 @@ def spc_merged_attn_fetch(d, records, resid, q, idx, bitmap, staging, k, o, lse,
                                       int(fetch_k), _ptr(fetch_staging), _stream(stream)))
 
 
+def spc_merged_attn_fetch_prev(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, ws,
+                               fetch_host_kv, fetch_n_cap, fetch_idx, fetch_k, fetch_staging, fetch_src,
+                               fetch_prev_staging, fetch_prev_k, ws_bytes=None, stream=None, kv_self=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("spc_merged_attn_fetch_prev",
+           _lib.spc_merged_attn_fetch_prev(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(kv_self),
+                                           _ptr(idx), _ptr(bitmap), _ptr(staging), int(k), _ptr(o), _ptr(lse),
+                                           _ptr(spec_logits), _ptr(ws), ws_bytes, _ptr(fetch_host_kv),
+                                           int(fetch_n_cap), _ptr(fetch_idx), int(fetch_k), _ptr(fetch_staging),
+                                           _ptr(fetch_src), _ptr(fetch_prev_staging), int(fetch_prev_k),
+                                           _stream(stream)))
+
+
 def spc_merged_attn_noalloc(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, stream=None):
     """spc_merged_attn with the library's built-in workspace (for callers that cannot allocate)."""
     _check("spc_merged_attn_noalloc",
@@ -219,6 +236,12 @@ def spc_merged_attn_noalloc(d, records, resid, q, idx, bitmap, staging, k, o, ls
 def spc_topk_select(d, spec_logits, lse, k, idx, bitmap, stream=None):
     _check("spc_topk_select", _lib.spc_topk_select(C.byref(d), _ptr(spec_logits), _ptr(lse), int(k), _ptr(idx),
                                                    _ptr(bitmap), _stream(stream)))
+
+
+def spc_topk_select_prev(d, spec_logits, lse, k, idx, bitmap, prev_idx, prev_k, src, stream=None):
+    _check("spc_topk_select_prev",
+           _lib.spc_topk_select_prev(C.byref(d), _ptr(spec_logits), _ptr(lse), int(k), _ptr(idx), _ptr(bitmap),
+                                     _ptr(prev_idx), int(prev_k), _ptr(src), _stream(stream)))
 
 
 def spc_append_kv(d, k_new, v_new, records, resid, host_kv=None, n_cap=0, stream=None):

@@ -236,6 +236,9 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.pf_ncap = pf ? pf->n_cap : 0;
   a.pf_k = pf ? pf->k : 0;
   a.pf_rows = pf ? (int32_t)((int64_t)d->B * d->Hkv * pf->k) : 0;
+  a.pf_src = fetch ? pf->src : nullptr;
+  a.pf_prev = fetch ? pf->prev : nullptr;
+  a.pf_prev_k = fetch ? pf->prev_k : 0;
   a.sel_idx = topk ? sel->idx : nullptr;
   a.sel_bitmap = topk ? sel->bitmap : nullptr;
   a.sel_k = topk ? sel->k : 0;

@@ -164,6 +164,12 @@ struct AttnArgs {
   uint16_t* pf_staging;     // [B][Hkv][pf_k][2][D]
   int64_t pf_ncap;
   int32_t pf_k, pf_rows;
+  // Rows still staged from the previous selection: pf_src[rr] >= 0 is the
+  // row's slot in pf_prev ([B][Hkv][pf_prev_k][2][D], device), whose copy
+  // replaces the host read; null when every row comes from the host.
+  const int32_t* pf_src;
+  const uint16_t* pf_prev;
+  int32_t pf_prev_k;
   // Fused ArgTopK (spc_decode_step): per (b, hkv) the sel_k positions with the
   // largest speculative probability go to sel_idx / sel_bitmap.  ready and
   // tickets2 are per-(b, hkv) words (zero between calls); cand holds each
@@ -555,6 +561,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   const int pf_ph = pf_slot % pf_every;
   const int pf_carried = (n_pf > 0 && n_my > pf_ph) ? min(n_pf, 1 + (n_my - 1 - pf_ph) / pf_every) : 0;
   int pf_next = n_pf > 0 ? a.pf_idx[pf_slot] : -1;  // position of the next row to issue
+  int pf_next_src = (n_pf > 0 && a.pf_src != nullptr) ? a.pf_src[pf_slot] : -1;  // its previous slot, or -1
   int pf_issue_i = 0, pf_issue_item = pf_ph;         // next carried row on the issue side and its item
 
   auto issue = [&](int item) {
@@ -574,10 +581,15 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
         if (lane == 0) reinterpret_cast<int2*>(dst + RB)[1] = make_int2(carry ? rr : -1, n);
         if (carry) {
           if (n >= 0 && n < a.pf_ncap) {
-            const int64_t src_row = ((int64_t)(rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
-            cp_async16(dst + PFROW + 16 * lane, a.pf_host + src_row + 8 * lane);
+            const int sj = pf_next_src;
+            const uint16_t* row =
+                (sj >= 0 && sj < a.pf_prev_k)
+                    ? a.pf_prev + ((int64_t)(rr / a.pf_k) * a.pf_prev_k + sj) * (2 * kD)  // still staged
+                    : a.pf_host + ((int64_t)(rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
+            cp_async16(dst + PFROW + 16 * lane, row + 8 * lane);
           }
           pf_next = (pf_issue_i + 1 < n_pf) ? a.pf_idx[rr + pf_nslots] : -1;
+          pf_next_src = (a.pf_src != nullptr && pf_issue_i + 1 < n_pf) ? a.pf_src[rr + pf_nslots] : -1;
           ++pf_issue_i;
           pf_issue_item = pf_issue_i * pf_every + pf_ph;
         }
@@ -876,16 +888,20 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   for (int i0 = pf_carried; i0 < n_pf; i0 += 4) {
     int rr[4];
     int n[4];
+    int sj[4];
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       rr[u] = pf_slot + pf_nslots * (i0 + u);
       n[u] = i0 + u < n_pf ? a.pf_idx[rr[u]] : -1;
+      sj[u] = (a.pf_src != nullptr && i0 + u < n_pf) ? a.pf_src[rr[u]] : -1;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       if (n[u] >= 0 && n[u] < a.pf_ncap)
-        v[u] = reinterpret_cast<const uint4*>(a.pf_host + ((rr[u] / a.pf_k) * a.pf_ncap + n[u]) * (2 * kD))[lane];
+        v[u] = reinterpret_cast<const uint4*>(
+            (sj[u] >= 0 && sj[u] < a.pf_prev_k) ? a.pf_prev + ((rr[u] / a.pf_k) * (int64_t)a.pf_prev_k + sj[u]) * (2 * kD)
+                                                : a.pf_host + ((rr[u] / a.pf_k) * a.pf_ncap + n[u]) * (2 * kD))[lane];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       if (n[u] >= 0 && n[u] < a.pf_ncap) reinterpret_cast<uint4*>(a.pf_staging + (int64_t)rr[u] * (2 * kD))[lane] = v[u];

@@ -139,12 +139,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
 namespace spc {
 // A Pre-fetch job carried by an attention launch: rows idx of the mapped host
 // cache host_dev ([B][Hkv][n_cap][2][D] bf16) into staging ([B][Hkv][k][2][D]).
+// With src (else null), row j whose src[j] >= 0 is still staged from the
+// previous selection and is copied from prev ([B][Hkv][prev_k][2][D], device)
+// instead of the host.
 struct PrefetchJob {
   const uint16_t* host_dev;
   int64_t n_cap;
   const int32_t* idx;
   int32_t k;
   uint16_t* staging;
+  const int32_t* src;
+  const uint16_t* prev;
+  int32_t prev_k;
 };
 
 // ArgTopK fused into a merged attention launch (spc_decode_step).

@@ -16,7 +16,8 @@ size_t step_workspace_bytes(const spc_dims*, int32_t);
 int attn_kernel_count(const spc_dims*, int32_t, int32_t);
 int step_kernel_count(const spc_dims*, int32_t, int32_t, int32_t);
 bool step_onchip(const spc_dims*, int32_t, int32_t, int32_t);
-spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t);
+spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t,
+                       const int32_t* prev_idx = nullptr, int32_t prev_k = 0, int32_t* src = nullptr);
 spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
                               int32_t, cudaStream_t);
 spc_status launch_append(const spc_dims*, const uint16_t*, const uint16_t*, void*, uint16_t*, uint16_t*, int64_t,
@@ -282,6 +283,35 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
                      stream, &job);
 }
 
+spc_status spc_merged_attn_fetch_prev(const spc_dims* d, const void* records, const uint16_t* resid,
+                                      const uint16_t* q, const uint16_t* kv_self, const int32_t* idx,
+                                      const uint32_t* bitmap, const uint16_t* staging, int32_t k, uint16_t* o,
+                                      float* lse, float* spec_logits, void* ws, size_t ws_bytes,
+                                      const uint16_t* fetch_host_kv, int64_t fetch_n_cap, const int32_t* fetch_idx,
+                                      int32_t fetch_k, uint16_t* fetch_staging, const int32_t* fetch_src,
+                                      const uint16_t* fetch_prev_staging, int32_t fetch_prev_k, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  if (fetch_k < 0 || fetch_k > (1 << 24) || fetch_n_cap < 0 || fetch_prev_k < 0 || fetch_prev_k > (1 << 24))
+    return SPC_ERR_INVALID;
+  if (fetch_k == 0)
+    return attn_common(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes,
+                       stream);
+  if (fetch_host_kv == nullptr || fetch_idx == nullptr || fetch_staging == nullptr || fetch_src == nullptr)
+    return SPC_ERR_INVALID;
+  if (!aligned16(fetch_host_kv) || !aligned16(fetch_staging)) return SPC_ERR_INVALID;
+  if (fetch_prev_k > 0 && (fetch_prev_staging == nullptr || !aligned16(fetch_prev_staging) ||
+                           fetch_prev_staging == fetch_staging))
+    return SPC_ERR_INVALID;
+  const void* dev = nullptr;
+  st = mapped_device_pointer(fetch_host_kv, &dev);
+  if (st != SPC_OK) return st;
+  spc::PrefetchJob job{static_cast<const uint16_t*>(dev), fetch_n_cap, fetch_idx, fetch_k, fetch_staging,
+                       fetch_src, fetch_prev_k > 0 ? fetch_prev_staging : nullptr, fetch_prev_k};
+  return attn_common(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes,
+                     stream, &job);
+}
+
 int32_t spc_attn_kernel_count(const spc_dims* d, int32_t k, int32_t fetch_k) {
   if (check_dims(d) != SPC_OK || k < 0 || k > (1 << 24) || fetch_k < 0 || fetch_k > (1 << 24)) return -1;
   return spc::attn_kernel_count(d, k, fetch_k);
@@ -363,8 +393,9 @@ spc_status spc_read_device_status(void* ws, const spc_dims* d, spc_stream stream
   return v != 0u ? SPC_ERR_TIMEOUT : SPC_OK;
 }
 
-spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse, int32_t k,
-                           int32_t* idx, uint32_t* bitmap, spc_stream stream) {
+// The arguments of both top-k entry points; SPC_OK when they are valid.
+static spc_status check_topk_args(const spc_dims* d, const float* spec_logits, const float* lse, int32_t k,
+                                  const int32_t* idx, const uint32_t* bitmap) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
   const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
@@ -373,8 +404,27 @@ spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const fl
   if (nq > 0 && (spec_logits == nullptr || lse == nullptr)) return SPC_ERR_INVALID;
   if (nq > 0 && !aligned16(spec_logits)) return SPC_ERR_INVALID;  // read in 16-byte pieces
   if (nq > 262144) return SPC_ERR_UNSUPPORTED;
+  return SPC_OK;
+}
+
+spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse, int32_t k,
+                           int32_t* idx, uint32_t* bitmap, spc_stream stream) {
+  const spc_status st = check_topk_args(d, spec_logits, lse, k, idx, bitmap);
+  if (st != SPC_OK) return st;
   if (d->q_groups_cap == 0 && k == 0) return SPC_OK;
   return spc::launch_topk(d, spec_logits, lse, k, idx, bitmap, reinterpret_cast<cudaStream_t>(stream));
+}
+
+spc_status spc_topk_select_prev(const spc_dims* d, const float* spec_logits, const float* lse, int32_t k,
+                                int32_t* idx, uint32_t* bitmap, const int32_t* prev_idx, int32_t prev_k,
+                                int32_t* src, spc_stream stream) {
+  const spc_status st = check_topk_args(d, spec_logits, lse, k, idx, bitmap);
+  if (st != SPC_OK) return st;
+  if (prev_k < 0 || prev_k > (1 << 24)) return SPC_ERR_INVALID;
+  if (k > 0 && (src == nullptr || (prev_k > 0 && (prev_idx == nullptr || prev_idx == idx)))) return SPC_ERR_INVALID;
+  if (d->q_groups_cap == 0 && k == 0) return SPC_OK;
+  return spc::launch_topk(d, spec_logits, lse, k, idx, bitmap, reinterpret_cast<cudaStream_t>(stream), prev_idx,
+                          prev_k, k > 0 ? src : nullptr);
 }
 
 spc_status spc_host_gather(const spc_dims* d, const uint16_t* host_kv, int64_t n_cap, const int32_t* idx,

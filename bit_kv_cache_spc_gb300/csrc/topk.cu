@@ -35,7 +35,30 @@ struct TopkArgs {
   uint32_t* bitmap;     // [BH][q_groups_cap]
   int32_t Hq, Hkv, G, nq, k, keff, Lcap, q_groups_cap;
   int32_t slice;        // positions per CTA, multiple of 32
+  // Where each selected position sat in the previous selection (or null):
+  // src[j] = the index of idx[j] in prev_idx [BH][prev_k] (ascending, -1
+  // padded), else -1.
+  const int32_t* prev_idx;
+  int32_t prev_k;
+  int32_t* src;         // [BH][k]
 };
+
+// Index of position p in the ascending row prev[0..n), whose -1 padding at
+// the end counts as larger than every position (unsigned order), or -1.
+// prev is in global or shared memory.
+template <typename T>
+__device__ __forceinline__ int32_t find_in_prev(const T* prev, int n, uint32_t p) {
+  int lo = 0, hi = n;  // the first entry >= p
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((uint32_t)prev[mid] < p)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return (lo < n && (uint32_t)prev[lo] == p) ? lo : -1;
+}
+constexpr int kPrevSmem = 2048;  // a previous selection up to this long is searched in shared memory
 
 struct TopkShared {
   uint32_t hist[2][256];  // this CTA's histogram, double-buffered by pass parity
@@ -213,12 +236,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
     const uint32_t eq_before = base_eq + weq[w] + __popc(beq & below);
     const bool sel = gt || (eq && eq_before < need);
     const uint32_t pos = base_gt + wgt[w] + __popc(bgt & below) + min(eq_before, need);
-    if (sel && pos < (uint32_t)a.keff) out[pos] = n0 + 32 * w + lane;
+    if (sel && pos < (uint32_t)a.keff) {
+      out[pos] = n0 + 32 * w + lane;
+      if (a.src != nullptr)
+        a.src[bh * a.k + pos] = find_in_prev(a.prev_idx + bh * a.prev_k, a.prev_k, (uint32_t)(n0 + 32 * w + lane));
+    }
     const uint32_t bsel = __ballot_sync(0xFFFFFFFFu, sel);
     if (lane == 0) bm[(n0 >> 5) + w] = bsel;
   }
   if (rank == 0) {
-    for (int j = a.keff + tid; j < a.k; j += kTopkThreads) out[j] = -1;
+    for (int j = a.keff + tid; j < a.k; j += kTopkThreads) {
+      out[j] = -1;
+      if (a.src != nullptr) a.src[bh * a.k + j] = -1;
+    }
     for (int w = (a.nq >> 5) + tid; w < a.q_groups_cap; w += kTopkThreads) bm[w] = 0u;
   }
   cluster.sync();  // peers may still read this CTA's counters
@@ -264,6 +294,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
   __shared__ uint32_t s_bin[4];     // the k_eff-th largest key's bin; keys at or above it; keys above its
                                     // top byte; keys in it
   __shared__ float s_nlse[4];       // -lse * log2(e) of the speculative row of each head of the group
+  __shared__ int32_t s_prev[kPrevSmem];  // the leader's copy of the previous selection (src output)
 
   const int tid = threadIdx.x;
   const unsigned rank = cluster.block_rank();
@@ -277,6 +308,12 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
 
   // ---- scores, four positions per thread and round, the round's loads issued up front ----
   if (tid < 4) s_nlse[tid] = tid < a.G ? -a.lse[((int64_t)b * 2 + 1) * a.Hq + hk * a.G + tid] * kLog2e : 0.f;
+  // the previous selection, for the src output: copied by the leader now, read at its end
+  const bool prev_in_smem = a.src != nullptr && a.prev_k <= kPrevSmem;
+  if (prev_in_smem && rank == 0) {
+    for (int j = tid; j < a.prev_k; j += kTopkThreads) cp_async4(&s_prev[j], a.prev_idx + bh * a.prev_k + j);
+    cp_async_commit();
+  }
   for (int j = tid; j < kBins; j += kTopkThreads) hist[j] = 0u;
   if (tid == 0) s_count = 0u;
   __syncthreads();
@@ -449,6 +486,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
     }
   }
   cluster.sync();  // the leader has read every CTA's candidates: the others are done
+  if (prev_in_smem && rank == 0) {
+    cp_async_wait<0>();  // this thread's copies of the previous selection (issued at the start)
+    __syncthreads();     // and every other thread's
+  }
   if (rank == 0) {
     uint32_t* mpos = dyn + M;
     uint32_t* sbm = dyn + 2 * M;  // bitmap of the selection, one word per 32 quantised positions
@@ -513,21 +554,30 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
         const uint32_t p = mpos[i];
         out[r] = (int32_t)p;
         atomicOr(&sbm[p >> 5], 1u << (p & 31u));
+        if (a.src != nullptr)
+          a.src[bh * a.k + r] = prev_in_smem ? find_in_prev(s_prev, a.prev_k, p)
+                                             : find_in_prev(a.prev_idx + bh * a.prev_k, a.prev_k, p);
       });
     }
-    for (int j = a.keff + tid; j < a.k; j += kTopkThreads) out[j] = -1;
+    for (int j = a.keff + tid; j < a.k; j += kTopkThreads) {
+      out[j] = -1;
+      if (a.src != nullptr) a.src[bh * a.k + j] = -1;
+    }
     uint32_t* bm = a.bitmap + bh * a.q_groups_cap;
     for (int w = tid; w < a.q_groups_cap; w += kTopkThreads) bm[w] = w < nwq ? sbm[w] : 0u;
   }
 }
 
 spc_status launch_topk(const spc_dims* d, const float* logits, const float* lse, int32_t k, int32_t* idx,
-                       uint32_t* bitmap, cudaStream_t stream) {
+                       uint32_t* bitmap, cudaStream_t stream, const int32_t* prev_idx, int32_t prev_k, int32_t* src) {
   TopkArgs a;
   a.logits = logits;
   a.lse = lse;
   a.idx = idx;
   a.bitmap = bitmap;
+  a.prev_idx = src != nullptr ? prev_idx : nullptr;
+  a.prev_k = src != nullptr ? prev_k : 0;
+  a.src = src;
   a.Hq = d->Hq;
   a.Hkv = d->Hkv;
   a.G = d->Hq / d->Hkv;

@@ -213,6 +213,28 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
                                  spc_stream stream);
 
 /*
+ * spc_merged_attn_fetch that keeps the rows already staged (SpeCache page,
+ * section 3, pre-fetching and offloading during decoding: the 16-bit rows
+ * that are not in the new top-k are evicted, so the rows that are stay).
+ * Row j of the new selection, fetch_idx[b][hkv][j], is copied from
+ * fetch_prev_staging[b][hkv][fetch_src[b][hkv][j]] (device,
+ * [B][Hkv][fetch_prev_k][2][D]) when fetch_src[b][hkv][j] >= 0, else from
+ * the host cache; fetch_src is what spc_topk_select_prev writes for this
+ * selection against the previous one, whose rows fetch_prev_staging holds.
+ * fetch_staging is then exactly what spc_merged_attn_fetch writes, with only
+ * the new rows read over the host link.  fetch_prev_staging must not be
+ * fetch_staging (16-byte aligned; NULL only with fetch_prev_k = 0, when
+ * every row comes from the host).  Everything else as spc_merged_attn_fetch.
+ */
+spc_status spc_merged_attn_fetch_prev(const spc_dims* d, const void* records, const uint16_t* resid,
+                                      const uint16_t* q, const uint16_t* kv_self, const int32_t* idx,
+                                      const uint32_t* bitmap, const uint16_t* staging, int32_t k, uint16_t* o,
+                                      float* lse, float* spec_logits, void* ws, size_t ws_bytes,
+                                      const uint16_t* fetch_host_kv, int64_t fetch_n_cap, const int32_t* fetch_idx,
+                                      int32_t fetch_k, uint16_t* fetch_staging, const int32_t* fetch_src,
+                                      const uint16_t* fetch_prev_staging, int32_t fetch_prev_k, spc_stream stream);
+
+/*
  * Kernels that spc_decode_attn2 (k = 0), spc_merged_attn (k > 0) or
  * spc_merged_attn_fetch (fetch_k > 0) enqueue for this shape on the current
  * device: 1 when the CTAs of every (b, hkv) form one resident thread-block
@@ -353,6 +375,22 @@ spc_status spc_append_kv(const spc_dims* d, const uint16_t* k_new, const uint16_
  */
 spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const float* lse,
                            int32_t k, int32_t* idx, uint32_t* bitmap, spc_stream stream);
+
+/*
+ * spc_topk_select that also says where each selected position sat in the
+ * previous selection, so that a pre-fetch copies only the rows it does not
+ * hold yet (spc_merged_attn_fetch_prev):
+ *   prev_idx: int32 [B][Hkv][prev_k], the previous selection (ascending,
+ *             -1 padded at the end, as spc_topk_select writes it); may be NULL
+ *             when prev_k = 0.
+ *   src:      int32 [B][Hkv][k] output: src[b][hkv][j] = the index i with
+ *             prev_idx[b][hkv][i] == idx[b][hkv][j], else -1 (also for the
+ *             -1 entries j >= k_eff).
+ * idx and bitmap are exactly spc_topk_select's.  prev_idx must not be idx.
+ */
+spc_status spc_topk_select_prev(const spc_dims* d, const float* spec_logits, const float* lse,
+                                int32_t k, int32_t* idx, uint32_t* bitmap, const int32_t* prev_idx,
+                                int32_t prev_k, int32_t* src, spc_stream stream);
 
 /*
  * Pre-fetch(C_kappa) (Algorithm 3): copies the selected 16-bit rows from the

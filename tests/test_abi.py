@@ -25,7 +25,7 @@ def spc():
 def test_header_declares_the_hot_path():
     names = declared_functions()
     for fn in ("spc_quantize_kv", "spc_decode_attn2", "spc_topk_select", "spc_host_gather", "spc_merged_attn",
-               "spc_merged_attn_fetch", "spc_append_kv"):
+               "spc_merged_attn_fetch", "spc_append_kv", "spc_topk_select_prev", "spc_merged_attn_fetch_prev"):
         assert fn in names
 
 
@@ -73,6 +73,20 @@ def test_validation_happens_before_any_launch(spc):
     assert e.value.status == 1
     with pytest.raises(spc.SpcError) as e:  # speculative logits not on a 16-byte boundary
         spc.spc_topk_select(d, 20, 16, 4, 16, 16, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # the selection with its previous slots: no src output
+        spc.spc_topk_select_prev(d, 16, 16, 4, 16, 16, 32, 4, None, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # the previous selection is the output
+        spc.spc_topk_select_prev(d, 16, 16, 4, 16, 16, 16, 4, 48, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # a pre-fetch that keeps staged rows needs src
+        spc.spc_merged_attn_fetch_prev(d, 16, 16, 16, None, None, None, 0, 16, None, None, 16, 64, 1024, 16, 4, 32,
+                                       None, 48, 4, ws_bytes=1 << 30, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # ... and a previous staging other than its output
+        spc.spc_merged_attn_fetch_prev(d, 16, 16, 16, None, None, None, 0, 16, None, None, 16, 64, 1024, 16, 4, 32,
+                                       64, 32, 4, ws_bytes=1 << 30, stream=0)
     assert e.value.status == 1
 
 

@@ -1,0 +1,170 @@
+"""Pre-fetch that keeps the rows already staged (SpeCache page, section 3,
+pre-fetching and offloading during decoding: the used 16-bit rows outside the
+new top-k are evicted, so the rows inside it stay).
+
+spc_topk_select_prev says where each selected position sat in the previous
+selection; spc_merged_attn_fetch_prev copies those rows from the previous
+staging buffer and reads only the others from the host.  Checked here: src
+against a search of the previous selection (both top-k paths), the routing of
+every staged row, and a two-layer decode pipeline with double-buffered staging
+that must reproduce the pipeline that re-fetches every row, bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import bit_kv_cache_spc_gb300 as spc
+from spc_cases import GpuLayer
+
+pytestmark = pytest.mark.gpu
+
+
+def want_src(idx, prev):
+    """Index of each entry of idx in prev (ascending, -1 padded), else -1."""
+    out = np.full(idx.shape, -1, np.int32)
+    for r in np.ndindex(idx.shape[:-1]):
+        p = prev[r]
+        valid = p[p >= 0]
+        for j, v in enumerate(idx[r]):
+            if v < 0:
+                continue
+            i = np.searchsorted(valid, v)
+            if i < len(valid) and valid[i] == v:
+                out[r + (j,)] = i
+    return out
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,k,prev_k", [(2, 8, 2, 32768, 328, 328), (1, 4, 2, 16384, 164, 200),
+                                                 (1, 4, 2, 65536 + 128, 2500, 2500), (2, 4, 4, 1000, 900, 40)])
+def test_topk_prev_src(B, Hq, Hkv, N, k, prev_k):
+    """idx and bitmap as spc_topk_select's; src the previous slot of every
+    selected position.  The previous selection is the top prev_k of nearby
+    logits (partial overlap); k = 2500 takes the radix path; k = 900 of 864
+    positions pads with -1."""
+    rng = np.random.default_rng(N + k)
+    d = spc.Dims(B, Hq, Hkv, N, 128, 1)
+    G = Hq // Hkv
+    nq = spc.spc_num_quantized(d)
+    Lcap = d.q_groups_cap * 32
+    lg = np.zeros((B, Hkv, G, Lcap), np.float32)
+    lg[..., :nq] = (2.0 * rng.standard_normal((B, Hkv, G, nq))).astype(np.float32)
+    lse = (8.0 + rng.standard_normal((B, 2, Hq))).astype(np.float32)
+    lg_prev = lg.copy()
+    lg_prev[..., :nq] += (0.7 * rng.standard_normal((B, Hkv, G, nq))).astype(np.float32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    prev = torch.full((B, Hkv, prev_k), -7, dtype=torch.int32, device="cuda")
+    pbm = torch.zeros((B, Hkv, d.q_groups_cap), dtype=torch.int32, device="cuda")
+    spc.spc_topk_select(d, dev(lg_prev), dev(lse), prev_k, prev, pbm)
+    idx0 = torch.full((B, Hkv, k), -7, dtype=torch.int32, device="cuda")
+    bm0 = torch.zeros_like(pbm)
+    spc.spc_topk_select(d, dev(lg), dev(lse), k, idx0, bm0)
+    idx = torch.full_like(idx0, -7)
+    bm = torch.full_like(bm0, 0x5A5A)
+    src = torch.full((B, Hkv, k), -7, dtype=torch.int32, device="cuda")
+    spc.spc_topk_select_prev(d, dev(lg), dev(lse), k, idx, bm, prev, prev_k, src)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx0) and torch.equal(bm, bm0)
+    got = src.cpu().numpy()
+    want = want_src(idx.cpu().numpy(), prev.cpu().numpy())
+    assert np.array_equal(got, want)
+    shared = (got >= 0).sum()
+    assert 0 < shared < (idx.cpu().numpy() >= 0).sum()  # a partial overlap, both kinds of rows present
+
+
+def test_fetch_prev_routes_staged_rows():
+    """A row whose src is >= 0 comes from the previous staging buffer, every
+    other from the host cache: the previous buffer is filled from a second
+    cache, so each output row shows where it was read.  The attention's own
+    results are those of spc_merged_attn."""
+    cfg = dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41)
+    g = GpuLayer(cfg, seed=3)
+    B, Hkv, k = cfg["B"], cfg["Hkv"], cfg["k"]
+    o0, lse0, lg0 = g.attn2()
+    idx, bm = g.topk(lg0, lse0, k)
+    g.gather(idx, k)
+    ref_o, ref_lse, ref_lg = g.merged(idx, bm, k)
+    n2 = 600
+    K2, V2 = synth.kv_layer(21, 1, B, Hkv, n2)
+    K3, V3 = synth.kv_layer(22, 1, B, Hkv, n2)
+    host2 = torch.from_numpy(np.stack([K2, V2], axis=3).view(np.int16)).pin_memory()
+    other = np.stack([K3, V3], axis=3).view(np.uint16)  # [B][Hkv][n2][2][D]
+    rng = np.random.default_rng(4)
+    fk, pk = 70, 50
+    fidx = np.sort(np.stack([np.stack([rng.choice(n2, fk, replace=False) for _ in range(Hkv)]) for _ in range(B)]),
+                   axis=-1).astype(np.int32)
+    pidx = np.sort(np.stack([np.stack([rng.choice(n2, pk, replace=False) for _ in range(Hkv)]) for _ in range(B)]),
+                   axis=-1).astype(np.int32)
+    src = want_src(fidx, pidx)
+    assert (src >= 0).any() and (src < 0).any()
+    prev = np.take_along_axis(other, pidx[..., None, None], axis=2)  # the previous rows, from the second cache
+    prev_d = torch.from_numpy(prev.view(np.int16).copy()).cuda()
+    fst = torch.zeros((B, Hkv, fk, 2, 128), dtype=torch.int16, device="cuda")
+    o, lse, lg = g.new_out()
+    spc.spc_merged_attn_fetch_prev(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o, lse, lg, g.ws, host2, n2,
+                                   torch.from_numpy(fidx).cuda(), fk, fst, torch.from_numpy(src).cuda(), prev_d, pk)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+    assert torch.equal(lg[..., :g.nq], ref_lg[..., :g.nq])
+    got = fst.cpu().numpy().view(np.uint16)
+    d2 = oracle.dims(B=B, Hq=cfg["Hq"], Hkv=Hkv, N=n2, R=0, bits=1)
+    from_host = oracle.gather(d2, np.stack([K2, V2], axis=3), fidx)
+    from_prev = np.take_along_axis(other, fidx[..., None, None], axis=2)
+    want = np.where((src >= 0)[..., None, None], from_prev, from_host)
+    assert np.array_equal(got, want)
+
+
+def test_two_layer_pipeline_with_kept_rows_equals_full_refetch():
+    """Two layers, three decode steps, each layer's attention carrying the
+    other layer's pre-fetch (layer 1 carries layer 0's selection of the same
+    step, layer 0 the selection layer 1 made in the step before).  Pipeline A
+    re-fetches every row into one staging buffer per layer; pipeline B keeps
+    the staged rows: double-buffered selections and staging by step parity,
+    spc_topk_select_prev and spc_merged_attn_fetch_prev.  Outputs, speculative
+    logits and selections agree bit for bit at every call."""
+    cfg = dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41)
+    B, Hkv, k, N = cfg["B"], cfg["Hkv"], cfg["k"], cfg["N"]
+    L = [GpuLayer(cfg, seed=30 + l, layer=l) for l in range(2)]
+    d = L[0].d
+    zi = lambda: torch.full((B, Hkv, k), -1, dtype=torch.int32, device="cuda")
+    zb = lambda: torch.zeros((B, Hkv, d.q_groups_cap), dtype=torch.int32, device="cuda")
+    zs = lambda: torch.zeros((B, Hkv, k, 2, 128), dtype=torch.int16, device="cuda")
+    idxA, bmA, stA = [zi(), zi()], [zb(), zb()], [zs(), zs()]
+    idxB = [[zi(), zi()], [zi(), zi()]]  # [parity][layer]
+    bmB = [[zb(), zb()], [zb(), zb()]]
+    stB = [[zs(), zs()], [zs(), zs()]]
+    src = [zi(), zi()]
+    # pre-decoding: plain attention, the first selection and its gather (parity 0 for pipeline B)
+    for l in range(2):
+        o, lse, lg = L[l].attn2()
+        spc.spc_topk_select(d, lg, lse, k, idxA[l], bmA[l])
+        spc.spc_topk_select(d, lg, lse, k, idxB[0][l], bmB[0][l])
+        spc.spc_host_gather(d, L[l].host, N, idxA[l], k, stA[l])
+        spc.spc_host_gather(d, L[l].host, N, idxB[0][l], k, stB[0][l])
+    torch.cuda.synchronize()
+    reused = 0
+    for t in range(3):
+        P = t % 2
+        for l in range(2):
+            j = 1 - l
+            oA, lseA, lgA = L[l].new_out()
+            spc.spc_merged_attn_fetch(d, L[l].records, L[l].resid, L[l].q, idxA[l], bmA[l], stA[l], k, oA, lseA,
+                                      lgA, L[l].ws, L[j].host, N, idxA[j], k, stA[j])
+            oB, lseB, lgB = L[l].new_out()
+            if l == 1:  # layer 0's selection of this step: written to parity 1 - P
+                fidx, fout, fprev = idxB[1 - P][0], stB[1 - P][0], stB[P][0]
+            else:  # layer 1's selection of the previous step (pre-decoding at t = 0): parity P
+                fidx, fout, fprev = idxB[P][1], stB[P][1], stB[1 - P][1]
+            spc.spc_merged_attn_fetch_prev(d, L[l].records, L[l].resid, L[l].q, idxB[P][l], bmB[P][l], stB[P][l],
+                                           k, oB, lseB, lgB, L[l].ws, L[j].host, N, fidx, k, fout, src[j], fprev, k)
+            torch.cuda.synchronize()
+            assert torch.equal(oA, oB) and torch.equal(lseA, lseB), (t, l)
+            assert torch.equal(lgA[..., :L[l].nq], lgB[..., :L[l].nq]), (t, l)
+            spc.spc_topk_select(d, lgA, lseA, k, idxA[l], bmA[l])
+            spc.spc_topk_select_prev(d, lgB, lseB, k, idxB[1 - P][l], bmB[1 - P][l], idxB[P][l], k, src[l])
+            torch.cuda.synchronize()
+            assert torch.equal(idxA[l], idxB[1 - P][l]) and torch.equal(bmA[l], bmB[1 - P][l]), (t, l)
+            reused += int((src[l] >= 0).sum())
+    # layer 0's rows fetched in the last step (t = 2, written to parity 1) match the full re-fetch
+    assert torch.equal(stA[0], stB[1][0])
+    assert reused > 0
