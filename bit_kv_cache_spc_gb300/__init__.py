@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "Dims", "SpcError", "spc_abi_version", "spc_num_quantized", "spc_records_bytes", "spc_resid_bytes",
     "spc_quantize_kv", "spc_attn_workspace_bytes", "spc_decode_attn2", "spc_merged_attn", "spc_topk_select",
-    "spc_topk_select_prev", "spc_merged_attn_fetch_prev",
+    "spc_topk_select_prev", "spc_merged_attn_fetch_prev", "spc_host_gather_prev",
     "spc_host_gather", "spc_merged_attn_noalloc", "spc_merged_attn_fetch", "spc_attn_kernel_count",
     "spc_decode_step_kernel_count", "spc_decode_step_on_chip", "spc_decode_step", "spc_step_workspace_bytes",
     "spc_read_device_status", "spc_append_kv", "spc_offload_kv", "lib_path",
@@ -88,6 +88,7 @@ _sig = {
     "spc_merged_attn_fetch_prev": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t,
                                              _P, C.c_int64, _P, C.c_int32, _P, _P, _P, C.c_int32, _P]),
     "spc_host_gather": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, C.c_int32, _P]),
+    "spc_host_gather_prev": (C.c_int, [_D, _P, C.c_int64, _P, C.c_int32, _P, _P, _P, C.c_int32, C.c_int32, _P]),
     "spc_append_kv": (C.c_int, [_D, _P, _P, _P, _P, _P, C.c_int64, _P]),
     "spc_offload_kv": (C.c_int, [_D, _P, _P, _P, C.c_int64, _P]),
     "spc_step_workspace_bytes": (C.c_size_t, [_D, C.c_int32]),
@@ -257,3 +258,9 @@ def spc_offload_kv(d, k, v, host_kv, n_cap, stream=None):
 def spc_host_gather(d, host_kv, n_cap, idx, k, staging, max_ctas=0, stream=None):
     _check("spc_host_gather", _lib.spc_host_gather(C.byref(d), _ptr(host_kv), int(n_cap), _ptr(idx), int(k),
                                                    _ptr(staging), int(max_ctas), _stream(stream)))
+
+
+def spc_host_gather_prev(d, host_kv, n_cap, idx, k, staging, src, prev_staging, prev_k, max_ctas=0, stream=None):
+    _check("spc_host_gather_prev",
+           _lib.spc_host_gather_prev(C.byref(d), _ptr(host_kv), int(n_cap), _ptr(idx), int(k), _ptr(staging),
+                                     _ptr(src), _ptr(prev_staging), int(prev_k), int(max_ctas), _stream(stream)))

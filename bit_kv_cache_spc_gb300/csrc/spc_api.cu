@@ -19,7 +19,8 @@ bool step_onchip(const spc_dims*, int32_t, int32_t, int32_t);
 spc_status launch_topk(const spc_dims*, const float*, const float*, int32_t, int32_t*, uint32_t*, cudaStream_t,
                        const int32_t* prev_idx = nullptr, int32_t prev_k = 0, int32_t* src = nullptr);
 spc_status launch_host_gather(const spc_dims*, const uint16_t*, int64_t, const int32_t*, int32_t, uint16_t*,
-                              int32_t, cudaStream_t);
+                              int32_t, cudaStream_t, const int32_t* src = nullptr, const uint16_t* prev = nullptr,
+                              int32_t prev_k = 0);
 spc_status launch_append(const spc_dims*, const uint16_t*, const uint16_t*, void*, uint16_t*, uint16_t*, int64_t,
                          cudaStream_t);
 }  // namespace spc
@@ -440,6 +441,26 @@ spc_status spc_host_gather(const spc_dims* d, const uint16_t* host_kv, int64_t n
   if (st != SPC_OK) return st;
   return spc::launch_host_gather(d, static_cast<const uint16_t*>(dev), n_cap, idx, k, staging, max_ctas,
                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+
+spc_status spc_host_gather_prev(const spc_dims* d, const uint16_t* host_kv, int64_t n_cap, const int32_t* idx,
+                                int32_t k, uint16_t* staging, const int32_t* src, const uint16_t* prev_staging,
+                                int32_t prev_k, int32_t max_ctas, spc_stream stream) {
+  spc_status st = check_dims(d);
+  if (st != SPC_OK) return st;
+  if (k < 0 || n_cap < 0 || max_ctas < 0 || prev_k < 0 || prev_k > (1 << 24)) return SPC_ERR_INVALID;
+  if (k == 0) return SPC_OK;
+  if (host_kv == nullptr || idx == nullptr || staging == nullptr || src == nullptr) return SPC_ERR_INVALID;
+  if (!aligned16(host_kv) || !aligned16(staging)) return SPC_ERR_INVALID;
+  if (prev_k > 0 && (prev_staging == nullptr || !aligned16(prev_staging) || prev_staging == staging))
+    return SPC_ERR_INVALID;
+  const void* dev = nullptr;
+  st = mapped_device_pointer(host_kv, &dev);
+  if (st != SPC_OK) return st;
+  return spc::launch_host_gather(d, static_cast<const uint16_t*>(dev), n_cap, idx, k, staging, max_ctas,
+                                 reinterpret_cast<cudaStream_t>(stream), src,
+                                 prev_k > 0 ? prev_staging : nullptr, prev_k);
 }
 
 }  // extern "C"

@@ -19,8 +19,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (spc_append_kv, spc_decode_attn2, spc_host_gather, spc_merged_attn, spc_offload_kv,
-               spc_quantize_kv, spc_topk_select)
+from . import (spc_append_kv, spc_decode_attn2, spc_host_gather, spc_host_gather_prev, spc_merged_attn,
+               spc_offload_kv, spc_quantize_kv, spc_topk_select, spc_topk_select_prev)
 
 
 def prefill_layer(d, k, v, records, resid, host_kv, n_cap, stream=None, copy_stream=None):
@@ -67,7 +67,8 @@ def predecode_layer(d, records, resid, host_kv, n_cap, q1, k1, v1, k, idx, bitma
 
 
 def decode_layer(d, records, resid, host_kv, n_cap, q, k_t, v_t, k, idx, bitmap, staging, next_idx, next_bitmap,
-                 next_staging, o, lse, logits, ws, ws_bytes, stream=None, fetch_stream=None, kv_self=None):
+                 next_staging, o, lse, logits, ws, ws_bytes, stream=None, fetch_stream=None, kv_self=None,
+                 src=None):
     """Algorithm 3 for one layer.  The real token's K/V (k_t, v_t: bf16
     [B][Hkv][D]) first joins the cache and is offloaded (d.N is advanced), so
     both queries see it; q: bf16 [B][2][Hq][D] (the real token, then the
@@ -76,8 +77,12 @@ def decode_layer(d, records, resid, host_kv, n_cap, q, k_t, v_t, k, idx, bitmap,
     them, the speculative row's probabilities select next_idx/next_bitmap,
     and their Pre-fetch into next_staging runs on `fetch_stream`.  The
     speculative token's own K/V (kv_self: bf16 [B][Hkv][2][D], optional) is
-    seen by the speculative query only and is not part of the cache.  Returns
-    the event that ends the Pre-fetch."""
+    seen by the speculative query only and is not part of the cache.  With
+    src (int32 [B][Hkv][k], scratch), the rows of the new selection that this
+    step's selection already staged are copied from `staging` and only the
+    others are read from the host (the used rows outside the new top-k are
+    the ones evicted); next_staging is the same either way.  Returns the
+    event that ends the Pre-fetch."""
     stream = torch.cuda.current_stream() if stream is None else stream
     fetch_stream = stream if fetch_stream is None else fetch_stream
     s = stream.cuda_stream
@@ -85,11 +90,18 @@ def decode_layer(d, records, resid, host_kv, n_cap, q, k_t, v_t, k, idx, bitmap,
     d.N += 1
     spc_merged_attn(d, records, resid, q, idx, bitmap, staging, k, o, lse, logits, ws, ws_bytes, stream=s,
                     kv_self=kv_self)
-    spc_topk_select(d, logits, lse, k, next_idx, next_bitmap, stream=s)
+    if src is None:
+        spc_topk_select(d, logits, lse, k, next_idx, next_bitmap, stream=s)
+    else:
+        spc_topk_select_prev(d, logits, lse, k, next_idx, next_bitmap, idx, k, src, stream=s)
     selected = torch.cuda.Event()
     selected.record(stream)
     fetch_stream.wait_event(selected)
-    spc_host_gather(d, host_kv, n_cap, next_idx, k, next_staging, stream=fetch_stream.cuda_stream)
+    if src is None:
+        spc_host_gather(d, host_kv, n_cap, next_idx, k, next_staging, stream=fetch_stream.cuda_stream)
+    else:
+        spc_host_gather_prev(d, host_kv, n_cap, next_idx, k, next_staging, src, staging, k,
+                             stream=fetch_stream.cuda_stream)
     fetched = torch.cuda.Event()
     fetched.record(fetch_stream)
     return fetched

@@ -409,6 +409,22 @@ spc_status spc_host_gather(const spc_dims* d, const uint16_t* host_kv, int64_t n
                            const int32_t* idx, int32_t k, uint16_t* staging, int32_t max_ctas,
                            spc_stream stream);
 
+/*
+ * spc_host_gather that keeps the rows already staged (SpeCache page, section
+ * 3: the used 16-bit rows outside the new top-k are evicted, the others
+ * stay): row j with src[b][hkv][j] >= 0 is copied from
+ * prev_staging[b][hkv][src[b][hkv][j]] (device, [B][Hkv][prev_k][2][D]), the
+ * others from the host cache.  src is what spc_topk_select_prev writes for
+ * idx against the previous selection, whose rows prev_staging holds; staging
+ * is then exactly spc_host_gather's.  prev_staging must not be staging
+ * (16-byte aligned; NULL only with prev_k = 0).  Everything else as
+ * spc_host_gather.
+ */
+spc_status spc_host_gather_prev(const spc_dims* d, const uint16_t* host_kv, int64_t n_cap,
+                                const int32_t* idx, int32_t k, uint16_t* staging, const int32_t* src,
+                                const uint16_t* prev_staging, int32_t prev_k, int32_t max_ctas,
+                                spc_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

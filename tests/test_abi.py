@@ -84,6 +84,12 @@ def test_validation_happens_before_any_launch(spc):
         spc.spc_merged_attn_fetch_prev(d, 16, 16, 16, None, None, None, 0, 16, None, None, 16, 64, 1024, 16, 4, 32,
                                        None, 48, 4, ws_bytes=1 << 30, stream=0)
     assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # the standalone pre-fetch with kept rows needs src too
+        spc.spc_host_gather_prev(d, 64, 1024, 16, 4, 32, None, 48, 4, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # ... and a previous staging other than its output
+        spc.spc_host_gather_prev(d, 64, 1024, 16, 4, 32, 80, 32, 4, stream=0)
+    assert e.value.status == 1
     with pytest.raises(spc.SpcError) as e:  # ... and a previous staging other than its output
         spc.spc_merged_attn_fetch_prev(d, 16, 16, 16, None, None, None, 0, 16, None, None, 16, 64, 1024, 16, 4, 32,
                                        64, 32, 4, ws_bytes=1 << 30, stream=0)

@@ -114,6 +114,35 @@ def test_fetch_prev_routes_staged_rows():
     assert np.array_equal(got, want)
 
 
+def test_host_gather_prev_routes_staged_rows():
+    """The standalone pre-fetch with kept rows: rows whose src is >= 0 come
+    from the previous staging buffer (filled from a second cache), the others
+    from the host cache; a bounded grid (max_ctas) gives the same rows."""
+    B, Hq, Hkv, n2 = 2, 8, 4, 900
+    d = spc.Dims(B, Hq, Hkv, n2, 128, 1)
+    K2, V2 = synth.kv_layer(23, 0, B, Hkv, n2)
+    K3, V3 = synth.kv_layer(24, 0, B, Hkv, n2)
+    host = torch.from_numpy(np.stack([K2, V2], axis=3).view(np.int16)).pin_memory()
+    other = np.stack([K3, V3], axis=3).view(np.uint16)
+    rng = np.random.default_rng(5)
+    fk, pk = 120, 90
+    pick = lambda m: np.sort(np.stack([np.stack([rng.choice(n2, m, replace=False) for _ in range(Hkv)])
+                                       for _ in range(B)]), axis=-1).astype(np.int32)
+    fidx, pidx = pick(fk), pick(pk)
+    src = want_src(fidx, pidx)
+    assert (src >= 0).any() and (src < 0).any()
+    prev_d = torch.from_numpy(np.take_along_axis(other, pidx[..., None, None], axis=2).view(np.int16).copy()).cuda()
+    d2 = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=n2, R=0, bits=1)
+    want = np.where((src >= 0)[..., None, None], np.take_along_axis(other, fidx[..., None, None], axis=2),
+                    oracle.gather(d2, np.stack([K2, V2], axis=3), fidx))
+    for max_ctas in (0, 3):
+        st = torch.zeros((B, Hkv, fk, 2, 128), dtype=torch.int16, device="cuda")
+        spc.spc_host_gather_prev(d, host, n2, torch.from_numpy(fidx).cuda(), fk, st, torch.from_numpy(src).cuda(),
+                                 prev_d, pk, max_ctas=max_ctas)
+        torch.cuda.synchronize()
+        assert np.array_equal(st.cpu().numpy().view(np.uint16), want)
+
+
 def test_two_layer_pipeline_with_kept_rows_equals_full_refetch():
     """Two layers, three decode steps, each layer's attention carrying the
     other layer's pre-fetch (layer 1 carries layer 0's selection of the same

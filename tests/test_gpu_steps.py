@@ -48,11 +48,15 @@ def test_prefill_layer_quantises_and_offloads(n_extra):
     assert np.array_equal(res.cpu().numpy().view(np.uint16).reshape(B, Hkv, -1, 2, 128)[:, :, :r], ores[:, :, :r])
 
 
-def test_predecode_then_two_decode_steps_match_oracle():
+@pytest.mark.parametrize("keep", [False, True])
+def test_predecode_then_two_decode_steps_match_oracle(keep):
     """Algorithm 2 then Algorithm 3 twice on one layer.  Token 999 completes a
     group at the pre-decoding step (a flush).  At every step the GPU's outputs
     are compared with the oracle's attention over the same cache and the same
-    substituted rows, and its selection with the oracle's ArgTopK."""
+    substituted rows, its selection with the oracle's ArgTopK, and the staged
+    rows with the host cache at the selected positions.  keep: the rows the
+    previous selection staged are copied from its staging buffer, not
+    re-read from the host."""
     import bit_kv_cache_spc_gb300 as spc
     from bit_kv_cache_spc_gb300.steps import decode_layer, predecode_layer
     B, Hq, Hkv, R, bits, k = 2, 8, 2, 40, 1, 33
@@ -79,6 +83,7 @@ def test_predecode_then_two_decode_steps_match_oracle():
     bm = [torch.zeros((B, Hkv, cap), dtype=torch.int32, device="cuda") for _ in range(2)]
     st = [torch.zeros((B, Hkv, k, 2, 128), dtype=torch.int16, device="cuda") for _ in range(2)]
     q2 = torch.empty((B, 2, Hq, 128), dtype=torch.int16, device="cuda")
+    src = torch.full((B, Hkv, k), -1, dtype=torch.int32, device="cuda") if keep else None
 
     def oracle_check(n_tokens, q, sub_idx):
         od = oracle.dims(B=B, Hq=Hq, Hkv=Hkv, N=n_tokens, R=R, bits=bits, scale=scale)
@@ -110,7 +115,7 @@ def test_predecode_then_two_decode_steps_match_oracle():
         q = synth.queries(9, 1 + t, B, Hq)
         used = idx[cur].cpu().numpy()
         decode_layer(d, rec, res, host, n_cap, dev16(q), Kn[n], Vn[n], k, idx[cur], bm[cur], st[cur],
-                     idx[1 - cur], bm[1 - cur], st[1 - cur], o, lse, lg, ws, ws_bytes)
+                     idx[1 - cur], bm[1 - cur], st[1 - cur], o, lse, lg, ws, ws_bytes, src=src)
         torch.cuda.synchronize()
         assert d.N == n + 1
         od, oo, lo, S = oracle_check(n + 1, q, used)
@@ -118,8 +123,10 @@ def test_predecode_then_two_decode_steps_match_oracle():
         assert np.max(np.abs(lse.cpu().numpy() - lo)) <= 1e-3
         io, _ = oracle.topk(od, S, k)
         sel = idx[1 - cur].cpu().numpy()
+        staged = st[1 - cur].cpu().numpy().view(np.uint16)
         for b in range(B):
             for h in range(Hkv):
                 check_topk_sets(sel[b, h], io[b, h], S[b, h], k)
+                assert np.array_equal(staged[b, h], np.stack([K, V], axis=3)[b, h, sel[b, h]])
         cur = 1 - cur
     assert np.array_equal(host.numpy().view(np.uint16)[:, :, :N1], np.stack([K, V], axis=3))
