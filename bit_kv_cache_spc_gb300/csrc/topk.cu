@@ -309,8 +309,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
   // ---- scores, four positions per thread and round, the round's loads issued up front ----
   if (tid < 4) s_nlse[tid] = tid < a.G ? -a.lse[((int64_t)b * 2 + 1) * a.Hq + hk * a.G + tid] * kLog2e : 0.f;
   // the previous selection, for the src output: copied by the leader now, read at its end
-  const bool prev_in_smem = a.src != nullptr && a.prev_k <= kPrevSmem;
-  if (prev_in_smem && rank == 0) {
+  if (a.src != nullptr && a.prev_k <= kPrevSmem && rank == 0) {
     for (int j = tid; j < a.prev_k; j += kTopkThreads) cp_async4(&s_prev[j], a.prev_idx + bh * a.prev_k + j);
     cp_async_commit();
   }
@@ -486,7 +485,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
     }
   }
   cluster.sync();  // the leader has read every CTA's candidates: the others are done
-  if (prev_in_smem && rank == 0) {
+  if (a.src != nullptr && a.prev_k <= kPrevSmem && rank == 0) {
     cp_async_wait<0>();  // this thread's copies of the previous selection (issued at the start)
     __syncthreads();     // and every other thread's
   }
@@ -554,10 +553,14 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_two_level_kernel(TopkArg
         const uint32_t p = mpos[i];
         out[r] = (int32_t)p;
         atomicOr(&sbm[p >> 5], 1u << (p & 31u));
-        if (a.src != nullptr)
-          a.src[bh * a.k + r] = prev_in_smem ? find_in_prev(s_prev, a.prev_k, p)
-                                             : find_in_prev(a.prev_idx + bh * a.prev_k, a.prev_k, p);
       });
+      if (a.src != nullptr) {  // the selected positions' previous slots (ordered_take ends with a barrier)
+        for (int r = tid; r < a.keff; r += kTopkThreads) {
+          const uint32_t p = (uint32_t)out[r];
+          a.src[bh * a.k + r] = a.prev_k <= kPrevSmem ? find_in_prev(s_prev, a.prev_k, p)
+                                                      : find_in_prev(a.prev_idx + bh * a.prev_k, a.prev_k, p);
+        }
+      }
     }
     for (int j = a.keff + tid; j < a.k; j += kTopkThreads) {
       out[j] = -1;
