@@ -64,6 +64,10 @@ def test_gpu_arm_prints_the_contract_line():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(line["clocks"])
     assert line["gpu_launches"] > 0 and line["gpu_launches"] % (3 * 4) == 0  # whole launches per layer and step
+    # the pre-fetch keeps the rows already staged: a fraction of the rows, and the host bytes below the total
+    pr = line["prefetch_rows"]
+    assert 0.0 <= pr["kept"] <= 1.0 and 0.0 <= pr["kept_fresh_queries"] <= 1.0
+    assert ov["prefetch_host_bytes_per_step"] <= ov["prefetch_bytes_per_step"]
 
 
 @pytest.mark.gpu
