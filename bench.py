@@ -247,7 +247,7 @@ class DecodeStep:
         # and staging alternate between two buffers by step parity (the previous ones are read while the
         # next are written); src[l] says where each newly selected row of layer l sat in its previous
         # selection (-1: read it from the host).
-        self.keep = keep_staged and mode == "overlap"
+        self.keep = keep_staged and mode in ("overlap", "step")
         self.parity = 0
         if self.keep:
             self.idx_b = [self.idx, torch.full_like(self.idx, -1)]
@@ -294,7 +294,7 @@ class DecodeStep:
         if self.mode == "fused":
             return self.enqueue_fused(timed)
         if self.mode == "step":
-            return self.enqueue_step(timed)
+            return self.enqueue_step(timed, parity=self.capture_parity)
         if self.mode == "overlap":
             return self.enqueue_overlap(timed, parity=self.capture_parity)
         return self.enqueue_side(timed)
@@ -366,23 +366,39 @@ class DecodeStep:
             for l in range(L):  # join the side stream before the step ends
                 main.wait_event(self.selected[l])
 
-    def enqueue_step(self, timed=False):
+    def enqueue_step(self, timed=False, parity=0):
         """One decode step on one stream, one launch per layer: spc_decode_step
         runs the merged attention over C' U C_kappa, carries the pre-fetch of
-        layer l-1's selection and ends with the speculative top-k, whose
-        selection replaces idx[l] / bitmap[l] in place."""
+        layer l-1's selection and ends with the speculative top-k.  Without
+        kept rows the selection replaces idx[l] / bitmap[l] in place; with them
+        (self.keep, spc_decode_step_prev) the step of this parity reads buffer
+        `parity` and writes the next selection into the other, and a pre-fetch
+        copies the rows its layer's previous selection staged from HBM."""
         spc, d, k = self.spc, self.d, self.k
         main, L = self.main, self.L
+        P = parity
         for l in range(L):
             j = (l - 1) % L
             if timed:
                 self.rec(self.attn_ev[l][0], main)
-            spc.spc_decode_step(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
-                                self.staging[l], k, self.o[l], self.lse[l],
-                                None if self.step_onchip else self.logits[l], k, self.idx[l],
-                                self.bitmap[l], self.ws_step, self.ws_step_bytes, fetch_host_kv=self.host[j],
-                                fetch_n_cap=self.W["N"], fetch_idx=self.idx[j], fetch_k=k,
-                                fetch_staging=self.staging[j], stream=main)
+            logits = None if self.step_onchip else self.logits[l]
+            if self.keep:
+                if l >= 1:  # layer j's selection of this step, written to the other parity
+                    f_idx, f_out, f_prev = self.idx_b[1 - P][j], self.staging_b[1 - P][j], self.staging_b[P][j]
+                else:  # layer L-1's selection of the previous step
+                    f_idx, f_out, f_prev = self.idx_b[P][j], self.staging_b[P][j], self.staging_b[1 - P][j]
+                spc.spc_decode_step_prev(d, self.records[l], self.resid[l], self.q[l], self.idx_b[P][l],
+                                         self.bitmap_b[P][l], self.staging_b[P][l], k, self.o[l], self.lse[l], logits,
+                                         k, self.idx_b[1 - P][l], self.bitmap_b[1 - P][l], self.src[l], self.ws_step,
+                                         self.ws_step_bytes, fetch_host_kv=self.host[j], fetch_n_cap=self.W["N"],
+                                         fetch_idx=f_idx, fetch_k=k, fetch_staging=f_out, fetch_src=self.src[j],
+                                         fetch_prev_staging=f_prev, fetch_prev_k=k, stream=main)
+            else:
+                spc.spc_decode_step(d, self.records[l], self.resid[l], self.q[l], self.idx[l], self.bitmap[l],
+                                    self.staging[l], k, self.o[l], self.lse[l], logits, k, self.idx[l],
+                                    self.bitmap[l], self.ws_step, self.ws_step_bytes, fetch_host_kv=self.host[j],
+                                    fetch_n_cap=self.W["N"], fetch_idx=self.idx[j], fetch_k=k,
+                                    fetch_staging=self.staging[j], stream=main)
             if timed:
                 self.rec(self.attn_ev[l][1], main)
                 self.rec(self.topk_ev[l][0], main)
@@ -1314,10 +1330,9 @@ def main():
                                     "step": "fused into the next layer's attention, which also ends with "
                                             "the top-k (spc_decode_step, speculative logits kept in TMEM)",
                                     "overlap": "fused into the attention two layers on; top-k on a "
-                                               "low-priority stream beside the next attention" +
-                                               ("; the rows that the layer's previous selection already staged "
-                                                "are copied from HBM, the others read from the host"
-                                                if kept_timed is not None else "")}[args.prefetch]},
+                                               "low-priority stream beside the next attention"}[args.prefetch] +
+                                   ("; the rows that the layer's previous selection already staged are copied "
+                                    "from HBM, the others read from the host" if kept_timed is not None else "")},
             "roofline": roof, "overlap": overlap, "gather": gather,
             "prefetch_rows": None if kept_timed is None else {
                 "kept": kept_timed, "kept_fresh_queries": kept_fresh,

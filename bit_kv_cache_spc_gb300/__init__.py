@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "Dims", "SpcError", "spc_abi_version", "spc_num_quantized", "spc_records_bytes", "spc_resid_bytes",
     "spc_quantize_kv", "spc_attn_workspace_bytes", "spc_decode_attn2", "spc_merged_attn", "spc_topk_select",
-    "spc_topk_select_prev", "spc_merged_attn_fetch_prev", "spc_host_gather_prev",
+    "spc_topk_select_prev", "spc_merged_attn_fetch_prev", "spc_host_gather_prev", "spc_decode_step_prev",
     "spc_host_gather", "spc_merged_attn_noalloc", "spc_merged_attn_fetch", "spc_attn_kernel_count",
     "spc_decode_step_kernel_count", "spc_decode_step_on_chip", "spc_decode_step", "spc_step_workspace_bytes",
     "spc_read_device_status", "spc_append_kv", "spc_offload_kv", "lib_path",
@@ -97,6 +97,9 @@ _sig = {
     "spc_decode_step_on_chip": (C.c_int32, [_D, C.c_int32, C.c_int32, C.c_int32]),
     "spc_decode_step": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, C.c_int32, _P, _P, _P,
                                   C.c_size_t, _P, C.c_int64, _P, C.c_int32, _P, _P]),
+    "spc_decode_step_prev": (C.c_int, [_D, _P, _P, _P, _P, _P, _P, _P, C.c_int32, _P, _P, _P, C.c_int32, _P, _P,
+                                       _P, _P, C.c_size_t, _P, C.c_int64, _P, C.c_int32, _P, _P, _P, C.c_int32,
+                                       _P]),
     "spc_read_device_status": (C.c_int, [_P, _D, _P]),
 }
 for _name, (_res, _args) in _sig.items():
@@ -174,6 +177,20 @@ def spc_decode_step(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_
                                 _ptr(next_idx), _ptr(next_bitmap), _ptr(ws), ws_bytes, _ptr(fetch_host_kv),
                                 int(fetch_n_cap), _ptr(fetch_idx), int(fetch_k), _ptr(fetch_staging),
                                 _stream(stream)))
+
+
+def spc_decode_step_prev(d, records, resid, q, idx, bitmap, staging, k, o, lse, spec_logits, next_k, next_idx,
+                         next_bitmap, next_src, ws, ws_bytes=None, fetch_host_kv=None, fetch_n_cap=0, fetch_idx=None,
+                         fetch_k=0, fetch_staging=None, fetch_src=None, fetch_prev_staging=None, fetch_prev_k=0,
+                         stream=None, kv_self=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("spc_decode_step_prev",
+           _lib.spc_decode_step_prev(C.byref(d), _ptr(records), _ptr(resid), _ptr(q), _ptr(kv_self), _ptr(idx),
+                                     _ptr(bitmap), _ptr(staging), int(k), _ptr(o), _ptr(lse), _ptr(spec_logits),
+                                     int(next_k), _ptr(next_idx), _ptr(next_bitmap), _ptr(next_src), _ptr(ws),
+                                     ws_bytes, _ptr(fetch_host_kv), int(fetch_n_cap), _ptr(fetch_idx), int(fetch_k),
+                                     _ptr(fetch_staging), _ptr(fetch_src), _ptr(fetch_prev_staging),
+                                     int(fetch_prev_k), _stream(stream)))
 
 
 def spc_read_device_status(ws, d, stream=None) -> int:

@@ -240,6 +240,7 @@ spc_status launch_attention(const spc_dims* d, const void* records, const uint16
   a.pf_prev = fetch ? pf->prev : nullptr;
   a.pf_prev_k = fetch ? pf->prev_k : 0;
   a.sel_idx = topk ? sel->idx : nullptr;
+  a.sel_src = topk ? sel->src : nullptr;
   a.sel_bitmap = topk ? sel->bitmap : nullptr;
   a.sel_k = topk ? sel->k : 0;
   a.sel_keff = topk ? std::min(sel->k, a.nq) : 0;

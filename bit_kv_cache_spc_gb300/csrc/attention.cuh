@@ -176,6 +176,7 @@ struct AttnArgs {
   // chunk's candidates (key, position), cand_cap per chunk; fault is set when
   // a wait ran out.
   int32_t* sel_idx;       // [BH][sel_k]
+  int32_t* sel_src;       // [BH][sel_k] or null: each selected position's index in idx (the previous selection)
   uint32_t* sel_bitmap;   // [BH][q_groups_cap]
   uint32_t* ready;
   uint32_t* tickets2;
@@ -1300,6 +1301,11 @@ __device__ __forceinline__ void select_epilogue(const AttnArgs& a, uint8_t* dyn,
     });
   }
   for (int j = a.sel_keff + tid; j < a.sel_k; j += kThreads) out[j] = -1;
+  if (a.sel_src != nullptr) {  // where each selected position sat in this launch's idx
+    __syncthreads();           // every entry of the selection is written
+    for (int r = tid; r < a.sel_k; r += kThreads)
+      a.sel_src[bh * a.sel_k + r] = r < a.sel_keff ? find_in_prev(a.idx + bh * a.k, a.k, (uint32_t)out[r]) : -1;
+  }
   uint32_t* bm = a.sel_bitmap + bh * a.q_groups_cap;
   for (int w = tid; w < a.q_groups_cap; w += kThreads) bm[w] = w < nwq ? sbm[w] : 0u;
   if (tid == 0) {  // every CTA of this (b, hkv) is past its wait: ready for the next call

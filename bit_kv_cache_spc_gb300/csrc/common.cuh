@@ -153,11 +153,14 @@ struct PrefetchJob {
   int32_t prev_k;
 };
 
-// ArgTopK fused into a merged attention launch (spc_decode_step).
+// ArgTopK fused into a merged attention launch (spc_decode_step).  With src
+// (else null), each selected position's index in the launch's own idx (the
+// previous selection), or -1.
 struct SelectJob {
   int32_t* idx;      // [B][Hkv][k]
   uint32_t* bitmap;  // [B][Hkv][q_groups_cap]
   int32_t k;
+  int32_t* src;      // [B][Hkv][k]
 };
 }  // namespace spc
 

@@ -8,6 +8,22 @@
 
 namespace spc {
 
+// Index of position p in the ascending row prev[0..n), whose -1 padding at
+// the end counts as larger than every position (unsigned order), or -1.
+// prev is in global or shared memory.
+template <typename T>
+__device__ __forceinline__ int32_t find_in_prev(const T* prev, int n, uint32_t p) {
+  int lo = 0, hi = n;  // the first entry >= p
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((uint32_t)prev[mid] < p)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return (lo < n && (uint32_t)prev[lo] == p) ? lo : -1;
+}
+
 template <int THREADS>
 struct __align__(16) SelShared {
   uint32_t hist[4][256];  // four sub-histograms (warp & 3) to spread atomic contention

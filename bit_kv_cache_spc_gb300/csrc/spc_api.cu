@@ -337,17 +337,23 @@ size_t spc_step_workspace_bytes(const spc_dims* d, int32_t k_max) {
   return spc::step_workspace_bytes(d, k_max);
 }
 
-spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
-                           const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
-                           uint16_t* o, float* lse, float* spec_logits, int32_t next_k, int32_t* next_idx,
-                           uint32_t* next_bitmap, void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv,
-                           int64_t fetch_n_cap, const int32_t* fetch_idx, int32_t fetch_k,
-                           uint16_t* fetch_staging, spc_stream stream) {
+// spc_decode_step and spc_decode_step_prev: with next_src, the pre-fetch keeps
+// the rows already staged (fetch_src, fetch_prev) and the selection reports
+// each position's index in idx.
+static spc_status decode_step(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                              const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap,
+                              const uint16_t* staging, int32_t k, uint16_t* o, float* lse, float* spec_logits,
+                              int32_t next_k, int32_t* next_idx, uint32_t* next_bitmap, int32_t* next_src, void* ws,
+                              size_t ws_bytes, const uint16_t* fetch_host_kv, int64_t fetch_n_cap,
+                              const int32_t* fetch_idx, int32_t fetch_k, uint16_t* fetch_staging,
+                              const int32_t* fetch_src, const uint16_t* fetch_prev, int32_t fetch_prev_k,
+                              bool keep, spc_stream stream) {
   spc_status st = check_dims(d);
   if (st != SPC_OK) return st;
   const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
   if (next_k < 0 || next_k > (1 << 24)) return SPC_ERR_INVALID;
   if (next_bitmap == nullptr || (next_k > 0 && next_idx == nullptr)) return SPC_ERR_INVALID;
+  if (keep && next_k > 0 && (next_src == nullptr || (k > 0 && next_idx == idx))) return SPC_ERR_INVALID;
   if (nq > 0 && lse == nullptr) return SPC_ERR_INVALID;
   if (nq > 262144) return SPC_ERR_UNSUPPORTED;
   // without a logits buffer the selection must ride on the attention with the logits on chip
@@ -360,20 +366,54 @@ spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_
     if (fetch_k < 0 || fetch_k > (1 << 24) || fetch_n_cap < 0) return SPC_ERR_INVALID;
     if (fetch_host_kv == nullptr || fetch_idx == nullptr || fetch_staging == nullptr) return SPC_ERR_INVALID;
     if (!aligned16(fetch_host_kv) || !aligned16(fetch_staging)) return SPC_ERR_INVALID;
+    if (keep) {
+      if (fetch_src == nullptr || fetch_prev_k < 0 || fetch_prev_k > (1 << 24)) return SPC_ERR_INVALID;
+      if (fetch_prev_k > 0 &&
+          (fetch_prev == nullptr || !aligned16(fetch_prev) || fetch_prev == fetch_staging))
+        return SPC_ERR_INVALID;
+      job.src = fetch_src;
+      job.prev = fetch_prev_k > 0 ? fetch_prev : nullptr;
+      job.prev_k = fetch_prev_k;
+    }
     const void* dev = nullptr;
     st = mapped_device_pointer(fetch_host_kv, &dev);
     if (st != SPC_OK) return st;
     job.host_dev = static_cast<const uint16_t*>(dev);
     pf = &job;
   }
-  spc::SelectJob sel{next_idx, next_bitmap, next_k};
+  spc::SelectJob sel{next_idx, next_bitmap, next_k, keep && next_k > 0 ? next_src : nullptr};
   bool fused = false;
   st = attn_common(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, ws, ws_bytes,
                    stream, pf, &sel, &fused);
   if (st != SPC_OK || fused) return st;
   // the selection could not ride on this attention launch: its own launch, right after
   if (d->q_groups_cap == 0 && next_k == 0) return SPC_OK;
-  return spc::launch_topk(d, spec_logits, lse, next_k, next_idx, next_bitmap, reinterpret_cast<cudaStream_t>(stream));
+  return spc::launch_topk(d, spec_logits, lse, next_k, next_idx, next_bitmap, reinterpret_cast<cudaStream_t>(stream),
+                          idx, k, keep && next_k > 0 ? next_src : nullptr);
+}
+
+spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                           const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
+                           uint16_t* o, float* lse, float* spec_logits, int32_t next_k, int32_t* next_idx,
+                           uint32_t* next_bitmap, void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv,
+                           int64_t fetch_n_cap, const int32_t* fetch_idx, int32_t fetch_k,
+                           uint16_t* fetch_staging, spc_stream stream) {
+  return decode_step(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, next_k, next_idx,
+                     next_bitmap, nullptr, ws, ws_bytes, fetch_host_kv, fetch_n_cap, fetch_idx, fetch_k,
+                     fetch_staging, nullptr, nullptr, 0, false, stream);
+}
+
+spc_status spc_decode_step_prev(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                                const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap,
+                                const uint16_t* staging, int32_t k, uint16_t* o, float* lse, float* spec_logits,
+                                int32_t next_k, int32_t* next_idx, uint32_t* next_bitmap, int32_t* next_src,
+                                void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv, int64_t fetch_n_cap,
+                                const int32_t* fetch_idx, int32_t fetch_k, uint16_t* fetch_staging,
+                                const int32_t* fetch_src, const uint16_t* fetch_prev_staging, int32_t fetch_prev_k,
+                                spc_stream stream) {
+  return decode_step(d, records, resid, q, kv_self, idx, bitmap, staging, k, o, lse, spec_logits, next_k, next_idx,
+                     next_bitmap, next_src, ws, ws_bytes, fetch_host_kv, fetch_n_cap, fetch_idx, fetch_k,
+                     fetch_staging, fetch_src, fetch_prev_staging, fetch_prev_k, true, stream);
 }
 
 spc_status spc_read_device_status(void* ws, const spc_dims* d, spc_stream stream) {

@@ -43,21 +43,6 @@ struct TopkArgs {
   int32_t* src;         // [BH][k]
 };
 
-// Index of position p in the ascending row prev[0..n), whose -1 padding at
-// the end counts as larger than every position (unsigned order), or -1.
-// prev is in global or shared memory.
-template <typename T>
-__device__ __forceinline__ int32_t find_in_prev(const T* prev, int n, uint32_t p) {
-  int lo = 0, hi = n;  // the first entry >= p
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if ((uint32_t)prev[mid] < p)
-      lo = mid + 1;
-    else
-      hi = mid;
-  }
-  return (lo < n && (uint32_t)prev[lo] == p) ? lo : -1;
-}
 constexpr int kPrevSmem = 2048;  // a previous selection up to this long is searched in shared memory
 
 struct TopkShared {

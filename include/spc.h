@@ -299,6 +299,27 @@ spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_
                            uint16_t* fetch_staging, spc_stream stream);
 
 /*
+ * spc_decode_step with the staged rows kept, as spc_merged_attn_fetch_prev
+ * and spc_topk_select_prev do separately: the carried pre-fetch copies the
+ * rows that fetch_src places in fetch_prev_staging ([B][Hkv][fetch_prev_k][2][D],
+ * device) and reads only the others from the host, and the selection also
+ * writes next_src ([B][Hkv][next_k]): each selected position's index in idx
+ * (this call's own selection, k entries), else -1.  fetch_src is required when
+ * fetch_k > 0; fetch_prev_staging must not be fetch_staging.  next_idx must
+ * not be idx here (next_src is read against idx after next_idx is written).
+ * Everything else as spc_decode_step; outputs identical to it and to the
+ * separate calls.
+ */
+spc_status spc_decode_step_prev(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
+                                const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap,
+                                const uint16_t* staging, int32_t k, uint16_t* o, float* lse, float* spec_logits,
+                                int32_t next_k, int32_t* next_idx, uint32_t* next_bitmap, int32_t* next_src,
+                                void* ws, size_t ws_bytes, const uint16_t* fetch_host_kv, int64_t fetch_n_cap,
+                                const int32_t* fetch_idx, int32_t fetch_k, uint16_t* fetch_staging,
+                                const int32_t* fetch_src, const uint16_t* fetch_prev_staging, int32_t fetch_prev_k,
+                                spc_stream stream);
+
+/*
  * Reads and clears the fault word of an attention workspace (ws, laid out for
  * d): SPC_ERR_TIMEOUT if a bounded wait of spc_decode_step ran out since the
  * last read, else SPC_OK.  Synchronises `stream`.

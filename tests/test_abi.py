@@ -84,6 +84,14 @@ def test_validation_happens_before_any_launch(spc):
         spc.spc_merged_attn_fetch_prev(d, 16, 16, 16, None, None, None, 0, 16, None, None, 16, 64, 1024, 16, 4, 32,
                                        None, 48, 4, ws_bytes=1 << 30, stream=0)
     assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # the fused step with kept rows: no next_src
+        spc.spc_decode_step_prev(d, 16, 16, 16, 16, 16, 16, 4, 16, 16, 16, 4, 32, 48, None, 64, ws_bytes=1 << 30,
+                                 stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # ... or next_idx the same buffer as idx
+        spc.spc_decode_step_prev(d, 16, 16, 16, 16, 16, 16, 4, 16, 16, 16, 4, 16, 48, 80, 64, ws_bytes=1 << 30,
+                                 stream=0)
+    assert e.value.status == 1
     with pytest.raises(spc.SpcError) as e:  # the standalone pre-fetch with kept rows needs src too
         spc.spc_host_gather_prev(d, 64, 1024, 16, 4, 32, None, 48, 4, stream=0)
     assert e.value.status == 1

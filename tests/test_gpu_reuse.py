@@ -201,3 +201,64 @@ def test_two_layer_pipeline_with_kept_rows_equals_full_refetch():
     # layer 0's rows fetched in the last step (t = 2, written to parity 1) match the full re-fetch
     assert torch.equal(stA[0], stB[1][0])
     assert reused > 0
+
+
+@pytest.mark.parametrize("cfg,on_chip", [
+    (dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41), True),
+    (dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41), False),
+    (dict(B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328), True),   # the LLaMA-3-8B decode shape
+    (dict(B=2, Hq=8, Hkv=2, N=40000, R=128, bits=1, k=400), False),   # many chunks
+    (dict(B=1, Hq=4, Hkv=2, N=40000, R=128, bits=1, k=3000), False),  # the selection in its own launch
+], ids=lambda c: str(c) if isinstance(c, bool) else f"B{c['B']}_N{c['N']}_k{c['k']}")
+def test_decode_step_prev_equals_separate_calls(cfg, on_chip):
+    """spc_decode_step_prev against spc_merged_attn_fetch_prev followed by
+    spc_topk_select_prev on the same inputs: outputs, selection, bitmap, the
+    selection's slots in the call's own idx and the kept-row pre-fetch of
+    another layer's rows, bit for bit; with the logits on chip and in device
+    memory, and with a selection too large to ride on the attention."""
+    g = GpuLayer(cfg, seed=12)
+    B, Hkv, k = cfg["B"], cfg["Hkv"], cfg["k"]
+    o0, lse0, lg0 = g.attn2()
+    idx, bm = g.topk(lg0, lse0, k)
+    idx, bm = idx.contiguous(), bm.contiguous()
+    g.gather(idx, k)
+    n2, fk, pk = 700, 60, 45
+    if on_chip and spc.spc_decode_step_on_chip(g.d, k, fk, k) != 1:
+        pytest.skip("this shape keeps its logits in device memory")
+    K2, V2 = synth.kv_layer(25, 1, B, Hkv, n2)
+    K3, V3 = synth.kv_layer(26, 1, B, Hkv, n2)
+    host2 = torch.from_numpy(np.stack([K2, V2], axis=3).view(np.int16)).pin_memory()
+    other = np.stack([K3, V3], axis=3).view(np.uint16)
+    rng = np.random.default_rng(7)
+    pick = lambda m: np.sort(np.stack([np.stack([rng.choice(n2, m, replace=False) for _ in range(Hkv)])
+                                       for _ in range(B)]), axis=-1).astype(np.int32)
+    fidx, pidx = pick(fk), pick(pk)
+    src = torch.from_numpy(want_src(fidx, pidx)).cuda()
+    prev_d = torch.from_numpy(np.take_along_axis(other, pidx[..., None, None], axis=2).view(np.int16).copy()).cuda()
+    fidx_d = torch.from_numpy(fidx).cuda()
+    # the separate calls
+    fst_r = torch.zeros((B, Hkv, fk, 2, 128), dtype=torch.int16, device="cuda")
+    o_r, lse_r, lg_r = g.new_out()
+    spc.spc_merged_attn_fetch_prev(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o_r, lse_r, lg_r, g.ws, host2,
+                                   n2, fidx_d, fk, fst_r, src, prev_d, pk)
+    nidx_r = torch.full_like(idx, -7)
+    nbm_r = torch.full_like(bm, 0x77)
+    nsrc_r = torch.full_like(idx, -7)
+    spc.spc_topk_select_prev(g.d, lg_r, lse_r, k, nidx_r, nbm_r, idx, k, nsrc_r)
+    # the fused step
+    ws = torch.zeros(spc.spc_step_workspace_bytes(g.d, k), dtype=torch.uint8, device="cuda")
+    fst = torch.zeros_like(fst_r)
+    o, lse, lg = g.new_out()
+    nidx, nbm, nsrc = torch.full_like(idx, -9), torch.full_like(bm, 0x55), torch.full_like(idx, -9)
+    spc.spc_decode_step_prev(g.d, g.records, g.resid, g.q, idx, bm, g.staging, k, o, lse, None if on_chip else lg, k,
+                             nidx, nbm, nsrc, ws, fetch_host_kv=host2, fetch_n_cap=n2, fetch_idx=fidx_d, fetch_k=fk,
+                             fetch_staging=fst, fetch_src=src, fetch_prev_staging=prev_d, fetch_prev_k=pk)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_r) and torch.equal(lse, lse_r)
+    if not on_chip:
+        assert torch.equal(lg[..., :g.nq], lg_r[..., :g.nq])
+    assert torch.equal(nidx, nidx_r) and torch.equal(nbm, nbm_r) and torch.equal(nsrc, nsrc_r)
+    assert np.array_equal(nsrc.cpu().numpy(), want_src(nidx.cpu().numpy(), idx.cpu().numpy()))
+    assert (nsrc.cpu().numpy() >= 0).any()
+    assert torch.equal(fst, fst_r)
+    assert spc.spc_read_device_status(ws, g.d) == 0
