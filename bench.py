@@ -34,8 +34,9 @@ WORKLOAD = dict(workload="llama3-8b decode step, 32 layers x attention, B=8, Hq=
                 B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328, layers=32)
 METRIC = "decode attn steps/s and HBM GB/s (% of peak) at 32K ctx, 1-bit, top-1%"  # value: steps/s; GB/s: roofline
 # DRAM bytes (read + write) of one merged-attention call of this workload (attn_kernel + combine_kernel, the
-# carried pre-fetch included), from an ncu capture of the attention sources whose digest is recorded beside
-# it; reported as null when the sources compiled now differ from those.
+# carried pre-fetch included, as the default placement runs it), from an ncu capture of the attention sources
+# whose digest is recorded beside it; reported as null when the sources compiled now differ from those, or for
+# another placement's call.
 ATTN_TRAFFIC = {"bytes_per_call": 177463808, "sources_sha256": "12aa4ef8771d7e4f"}
 ATTN_SOURCES = ("attention.cuh", "attn_b1g32.cu", "attention.cu", "common.cuh", "select.cuh")
 
@@ -1279,7 +1280,8 @@ def main():
     achieved = bytes_layer / (attn_avg_ms / 1000.0) / 1e9
     pf_bytes = W["B"] * W["Hkv"] * W["k"] * 512 if args.prefetch in ("fused", "step", "overlap") else 0
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": attention_traffic(),
+            "frac": achieved / peaks["hbm_gbs"],
+            "traffic": attention_traffic() if args.prefetch == "overlap" else None,  # captured on that call
             "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of attn_kernel and combine_kernel "
                               "for one call, from an ncu capture of this build's attention sources (null when "
                               "the sources differ from the captured ones)",
