@@ -76,12 +76,17 @@ def test_topk_prev_src(B, Hq, Hkv, N, k, prev_k):
         assert shared < (idx.cpu().numpy() >= 0).sum()  # a partial overlap, both kinds of rows present
 
 
-def test_fetch_prev_routes_staged_rows():
+@pytest.mark.parametrize("cfg", [dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41),
+                                 dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=2, k=41),
+                                 dict(B=2, Hq=8, Hkv=2, N=4200, R=40, bits=1, k=41, group=64),
+                                 dict(B=1, Hq=4, Hkv=2, N=2100, R=64, bits=2, k=20, group=64)],
+                         ids=lambda c: f"b{c['bits']}_g{c.get('group', 32)}")
+def test_fetch_prev_routes_staged_rows(cfg):
     """A row whose src is >= 0 comes from the previous staging buffer, every
     other from the host cache: the previous buffer is filled from a second
     cache, so each output row shows where it was read.  The attention's own
-    results are those of spc_merged_attn."""
-    cfg = dict(B=2, Hq=8, Hkv=2, N=4096, R=128, bits=1, k=41)
+    results are those of spc_merged_attn.  Every bit width and group size
+    (the carried pre-fetch rides on each one's low-bit loop)."""
     g = GpuLayer(cfg, seed=3)
     B, Hkv, k = cfg["B"], cfg["Hkv"], cfg["k"]
     o0, lse0, lg0 = g.attn2()
