@@ -149,3 +149,15 @@ def test_group_size_validation(spc):
     with pytest.raises(spc.SpcError) as e:
         spc.spc_quantize_kv(d48, 16, 16, 16, 16, stream=0)
     assert e.value.status == 2
+
+
+def test_pipeline_refuses_a_schedule_that_reads_its_own_fetch(spc):
+    """DecodePipeline checks the layer count and the lag before it touches a
+    device: at lag = L a layer's attention would carry the fetch of the rows it
+    reads, and lag 0 is the same layer."""
+    from bit_kv_cache_spc_gb300.pipeline import DecodePipeline
+    d = spc.Dims(1, 4, 1, 1024, 64, 1)
+    for n_layers, lag in ((2, 2), (3, 3), (3, 0), (1, 1), (4, 7)):
+        rec = [object()] * n_layers
+        with pytest.raises(ValueError):
+            DecodePipeline(d, 24, rec, rec, rec, 1024, rec, rec, rec, rec, None, 0, lag=lag)
