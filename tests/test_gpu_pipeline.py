@@ -105,3 +105,40 @@ def test_pipeline_refuses_a_lag_that_reads_its_own_fetch():
     for n_layers, lag in ((2, 2), (3, 0), (1, 1)):
         with pytest.raises(ValueError):
             make_pipeline(cfg, n_layers, lag, True)
+
+
+def test_pipeline_at_the_llama3_8b_decode_shape():
+    """The timed schedule at the LLaMA-3-8B decode shape (B=8, 32/8 heads,
+    32K context, 1 bit, k=328: the benchmark's launch configuration), three
+    layers, kept rows, captured as graphs: outputs and selections bit-identical
+    to the layer-by-layer calls, and the staged rows of one sampled
+    (b, KV head) per step equal to the oracle's gather of the host cache."""
+    cfg = dict(B=8, Hq=32, Hkv=8, N=32768, R=128, bits=1, k=328)
+    k, n_layers = cfg["k"], 3
+    layers, pipe = make_pipeline(cfg, n_layers, 2, True, seed=60)
+    pipe.predecode()
+    torch.cuda.synchronize()
+    ref = []
+    for l, g in enumerate(layers):
+        o0, lse0, lg0 = g.attn2()
+        idx, bm = g.topk(lg0, lse0, k)
+        ref.append((idx.contiguous(), bm.contiguous()))
+    graphs = pipe.capture()
+    d1 = odims(cfg, B=1, Hkv=1, Hq=cfg["Hq"] // cfg["Hkv"])
+    for t in range(3):
+        graphs.replay()
+        torch.cuda.synchronize()
+        nidx, nbm = pipe.selection(pipe.parity)
+        for l, g in enumerate(layers):
+            g.gather(ref[l][0], k)
+            ro, rlse, rlg = g.merged(ref[l][0], ref[l][1], k)
+            assert torch.equal(pipe.o[l], ro) and torch.equal(pipe.lse[l], rlse), (t, l)
+            idx, bm = g.topk(rlg, rlse, k)
+            ref[l] = (idx.contiguous(), bm.contiguous())
+            assert torch.equal(nidx[l], ref[l][0]) and torch.equal(nbm[l], ref[l][1]), (t, l)
+        b, h = (3 * t + 1) % cfg["B"], (5 * t + 2) % cfg["Hkv"]
+        host = layers[0].host[b:b + 1, h:h + 1].numpy().view(np.uint16)
+        want = oracle.gather(d1, host, ref[0][0][b:b + 1, h:h + 1].cpu().numpy())
+        got = pipe.staging[pipe.parity][0][b:b + 1, h:h + 1].cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, want), t
+    assert 0.0 < pipe.kept_fraction() <= 1.0
