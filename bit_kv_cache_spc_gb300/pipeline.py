@@ -190,6 +190,7 @@ class DecodePipeline:
         kept rows)."""
         if not self.keep:
             return None
+        torch.cuda.current_stream().wait_stream(self.main)
         n = sum(int((s >= 0).sum().item()) for s in self.src)
         return n / float(sum(s.numel() for s in self.src))
 
