@@ -90,7 +90,12 @@ def parse():
                    help="(profiling) one decode layer of the workload: run its calls once, then this call "
                         "--profile-reps times, and exit; a profiler captures the call's kernels")
     p.add_argument("--profile-reps", type=int, default=4)
-    return p.parse_args()
+    args = p.parse_args()
+    if args.layers < 2 and args.prefetch != "side" and args.impl == "spc" and args.profile_call is None:
+        # a carried pre-fetch rides on another layer's attention: with one layer it would write the
+        # staging rows that the same attention reads
+        p.error("--prefetch fused|step|overlap needs at least 2 layers (--prefetch side runs one)")
+    return args
 
 
 # ------------------------------------------------------------------ helpers
