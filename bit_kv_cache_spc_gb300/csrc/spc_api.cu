@@ -120,6 +120,24 @@ spc_status check_attn_args(const spc_dims* d, const void* records, const uint16_
 
 namespace {
 
+// [a, a + na) and [b, b + nb) share a byte
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+// bytes of a [B][Hkv][k][2][D] bf16 staging buffer
+size_t staging_bytes(const spc_dims* d, int64_t k) { return (size_t)d->B * d->Hkv * (size_t)k * 2 * d->D * 2; }
+// A carried pre-fetch writes fetch_staging while the attention reads staging
+// (k rows) and, with kept rows, copies from prev (prev_k rows): a shared byte
+// would race.
+bool fetch_buffers_overlap(const spc_dims* d, const uint16_t* staging, int32_t k, const uint16_t* fetch_staging,
+                           int32_t fetch_k, const uint16_t* prev, int32_t prev_k) {
+  const size_t out = staging_bytes(d, fetch_k);
+  return (k > 0 && overlap(staging, staging_bytes(d, k), fetch_staging, out)) ||
+         (prev_k > 0 && overlap(prev, staging_bytes(d, prev_k), fetch_staging, out));
+}
+
 spc_status attn_common(const spc_dims* d, const void* records, const uint16_t* resid, const uint16_t* q,
                        const uint16_t* kv_self, const int32_t* idx, const uint32_t* bitmap, const uint16_t* staging, int32_t k,
                        uint16_t* o, float* lse, float* spec_logits, void* ws, size_t ws_bytes,
@@ -276,6 +294,7 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
                        stream);
   if (fetch_host_kv == nullptr || fetch_idx == nullptr || fetch_staging == nullptr) return SPC_ERR_INVALID;
   if (!aligned16(fetch_host_kv) || !aligned16(fetch_staging)) return SPC_ERR_INVALID;
+  if (fetch_buffers_overlap(d, staging, k, fetch_staging, fetch_k, nullptr, 0)) return SPC_ERR_INVALID;
   const void* dev = nullptr;
   st = mapped_device_pointer(fetch_host_kv, &dev);
   if (st != SPC_OK) return st;
@@ -301,8 +320,9 @@ spc_status spc_merged_attn_fetch_prev(const spc_dims* d, const void* records, co
   if (fetch_host_kv == nullptr || fetch_idx == nullptr || fetch_staging == nullptr || fetch_src == nullptr)
     return SPC_ERR_INVALID;
   if (!aligned16(fetch_host_kv) || !aligned16(fetch_staging)) return SPC_ERR_INVALID;
-  if (fetch_prev_k > 0 && (fetch_prev_staging == nullptr || !aligned16(fetch_prev_staging) ||
-                           fetch_prev_staging == fetch_staging))
+  if (fetch_prev_k > 0 && (fetch_prev_staging == nullptr || !aligned16(fetch_prev_staging)))
+    return SPC_ERR_INVALID;
+  if (fetch_buffers_overlap(d, staging, k, fetch_staging, fetch_k, fetch_prev_staging, fetch_prev_k))
     return SPC_ERR_INVALID;
   const void* dev = nullptr;
   st = mapped_device_pointer(fetch_host_kv, &dev);
@@ -368,13 +388,12 @@ static spc_status decode_step(const spc_dims* d, const void* records, const uint
     if (!aligned16(fetch_host_kv) || !aligned16(fetch_staging)) return SPC_ERR_INVALID;
     if (keep) {
       if (fetch_src == nullptr || fetch_prev_k < 0 || fetch_prev_k > (1 << 24)) return SPC_ERR_INVALID;
-      if (fetch_prev_k > 0 &&
-          (fetch_prev == nullptr || !aligned16(fetch_prev) || fetch_prev == fetch_staging))
-        return SPC_ERR_INVALID;
+      if (fetch_prev_k > 0 && (fetch_prev == nullptr || !aligned16(fetch_prev))) return SPC_ERR_INVALID;
       job.src = fetch_src;
       job.prev = fetch_prev_k > 0 ? fetch_prev : nullptr;
       job.prev_k = fetch_prev_k;
     }
+    if (fetch_buffers_overlap(d, staging, k, fetch_staging, fetch_k, job.prev, job.prev_k)) return SPC_ERR_INVALID;
     const void* dev = nullptr;
     st = mapped_device_pointer(fetch_host_kv, &dev);
     if (st != SPC_OK) return st;
@@ -493,7 +512,8 @@ spc_status spc_host_gather_prev(const spc_dims* d, const uint16_t* host_kv, int6
   if (k == 0) return SPC_OK;
   if (host_kv == nullptr || idx == nullptr || staging == nullptr || src == nullptr) return SPC_ERR_INVALID;
   if (!aligned16(host_kv) || !aligned16(staging)) return SPC_ERR_INVALID;
-  if (prev_k > 0 && (prev_staging == nullptr || !aligned16(prev_staging) || prev_staging == staging))
+  if (prev_k > 0 && (prev_staging == nullptr || !aligned16(prev_staging) ||
+                     overlap(prev_staging, staging_bytes(d, prev_k), staging, staging_bytes(d, k))))
     return SPC_ERR_INVALID;
   const void* dev = nullptr;
   st = mapped_device_pointer(host_kv, &dev);

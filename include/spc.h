@@ -201,7 +201,8 @@ spc_status spc_merged_attn(const spc_dims* d, const void* records, const uint16_
  * to fetch_staging ([B][Hkv][fetch_k][2][D]), exactly as spc_host_gather
  * would.  The copy rides on the attention's own load pipeline, so the host
  * link works while the SMs compute; the attention's results are unchanged.
- * fetch_staging must not be the staging buffer this call reads.
+ * fetch_staging must not share a byte with the staging rows this call reads
+ * (SPC_ERR_INVALID: the copy would race with the attention's reads).
  * fetch_k = 0 is spc_merged_attn.  SPC_ERR_NOT_MAPPED as spc_host_gather.
  */
 spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const uint16_t* resid,
@@ -222,8 +223,8 @@ spc_status spc_merged_attn_fetch(const spc_dims* d, const void* records, const u
  * the host cache; fetch_src is what spc_topk_select_prev writes for this
  * selection against the previous one, whose rows fetch_prev_staging holds.
  * fetch_staging is then exactly what spc_merged_attn_fetch writes, with only
- * the new rows read over the host link.  fetch_prev_staging must not be
- * fetch_staging (16-byte aligned; NULL only with fetch_prev_k = 0, when
+ * the new rows read over the host link.  fetch_prev_staging must not share
+ * a byte with fetch_staging (16-byte aligned; NULL only with fetch_prev_k = 0, when
  * every row comes from the host).  Everything else as spc_merged_attn_fetch.
  */
 spc_status spc_merged_attn_fetch_prev(const spc_dims* d, const void* records, const uint16_t* resid,
@@ -305,7 +306,8 @@ spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_
  * device) and reads only the others from the host, and the selection also
  * writes next_src ([B][Hkv][next_k]): each selected position's index in idx
  * (this call's own selection, k entries), else -1.  fetch_src is required when
- * fetch_k > 0; fetch_prev_staging must not be fetch_staging.  next_idx must
+ * fetch_k > 0; fetch_prev_staging must not share a byte with fetch_staging,
+ * nor fetch_staging with staging (SPC_ERR_INVALID).  next_idx must
  * not be idx here (next_src is read against idx after next_idx is written).
  * Everything else as spc_decode_step; outputs identical to it and to the
  * separate calls.
@@ -437,8 +439,8 @@ spc_status spc_host_gather(const spc_dims* d, const uint16_t* host_kv, int64_t n
  * prev_staging[b][hkv][src[b][hkv][j]] (device, [B][Hkv][prev_k][2][D]), the
  * others from the host cache.  src is what spc_topk_select_prev writes for
  * idx against the previous selection, whose rows prev_staging holds; staging
- * is then exactly spc_host_gather's.  prev_staging must not be staging
- * (16-byte aligned; NULL only with prev_k = 0).  Everything else as
+ * is then exactly spc_host_gather's.  prev_staging must not share a byte
+ * with staging (SPC_ERR_INVALID; 16-byte aligned; NULL only with prev_k = 0).  Everything else as
  * spc_host_gather.
  */
 spc_status spc_host_gather_prev(const spc_dims* d, const uint16_t* host_kv, int64_t n_cap,

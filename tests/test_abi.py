@@ -102,6 +102,24 @@ def test_validation_happens_before_any_launch(spc):
         spc.spc_merged_attn_fetch_prev(d, 16, 16, 16, None, None, None, 0, 16, None, None, 16, 64, 1024, 16, 4, 32,
                                        64, 32, 4, ws_bytes=1 << 30, stream=0)
     assert e.value.status == 1
+    # staging buffers that share bytes: one row of this shape's staging is 8 KV heads x 512 B = 4096 B per k
+    row = 8 * 512
+    with pytest.raises(spc.SpcError) as e:  # the carried copy would write rows the attention reads
+        spc.spc_merged_attn_fetch(d, 16, 16, 16, 32, 48, 1 << 20, 4, 16, None, None, 16, 64, 1024, 16, 4,
+                                  (1 << 20) + 3 * row, ws_bytes=1 << 30, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # ... also with kept rows: the previous staging overlaps the output
+        spc.spc_merged_attn_fetch_prev(d, 16, 16, 16, 32, 48, 1 << 20, 4, 16, None, None, 16, 64, 1024, 16, 4,
+                                       1 << 24, 32, (1 << 24) - 2 * row, 4, ws_bytes=1 << 30, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # the fused step: its carried copy over the rows it reads
+        spc.spc_decode_step(d, 16, 16, 16, 32, 48, 1 << 20, 4, 16, 16, 16, 4, 64, 80, 96, ws_bytes=1 << 30,
+                            fetch_host_kv=64, fetch_n_cap=1024, fetch_idx=16, fetch_k=4,
+                            fetch_staging=(1 << 20) + row, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # the standalone gather with kept rows, overlapping by one byte range
+        spc.spc_host_gather_prev(d, 64, 1024, 16, 4, 1 << 20, 32, (1 << 20) + row, 4, stream=0)
+    assert e.value.status == 1
 
 
 def test_kernel_count_queries_refuse_bad_arguments(spc):
