@@ -373,7 +373,10 @@ static spc_status decode_step(const spc_dims* d, const void* records, const uint
   const int32_t nq = spc::num_quantized(d->N, d->R, d->group);
   if (next_k < 0 || next_k > (1 << 24)) return SPC_ERR_INVALID;
   if (next_bitmap == nullptr || (next_k > 0 && next_idx == nullptr)) return SPC_ERR_INVALID;
-  if (keep && next_k > 0 && (next_src == nullptr || (k > 0 && next_idx == idx))) return SPC_ERR_INVALID;
+  if (keep && next_k > 0 &&
+      (next_src == nullptr || (k > 0 && overlap(next_idx, (size_t)d->B * d->Hkv * next_k * 4, idx,
+                                                  (size_t)d->B * d->Hkv * k * 4))))
+    return SPC_ERR_INVALID;
   if (nq > 0 && lse == nullptr) return SPC_ERR_INVALID;
   if (nq > 262144) return SPC_ERR_UNSUPPORTED;
   // without a logits buffer the selection must ride on the attention with the logits on chip
@@ -481,7 +484,10 @@ spc_status spc_topk_select_prev(const spc_dims* d, const float* spec_logits, con
   const spc_status st = check_topk_args(d, spec_logits, lse, k, idx, bitmap);
   if (st != SPC_OK) return st;
   if (prev_k < 0 || prev_k > (1 << 24)) return SPC_ERR_INVALID;
-  if (k > 0 && (src == nullptr || (prev_k > 0 && (prev_idx == nullptr || prev_idx == idx)))) return SPC_ERR_INVALID;
+  if (k > 0 && (src == nullptr ||
+                (prev_k > 0 && (prev_idx == nullptr || overlap(prev_idx, (size_t)d->B * d->Hkv * prev_k * 4, idx,
+                                                               (size_t)d->B * d->Hkv * k * 4)))))
+    return SPC_ERR_INVALID;
   if (d->q_groups_cap == 0 && k == 0) return SPC_OK;
   return spc::launch_topk(d, spec_logits, lse, k, idx, bitmap, reinterpret_cast<cudaStream_t>(stream), prev_idx,
                           prev_k, k > 0 ? src : nullptr);

@@ -307,8 +307,8 @@ spc_status spc_decode_step(const spc_dims* d, const void* records, const uint16_
  * writes next_src ([B][Hkv][next_k]): each selected position's index in idx
  * (this call's own selection, k entries), else -1.  fetch_src is required when
  * fetch_k > 0; fetch_prev_staging must not share a byte with fetch_staging,
- * nor fetch_staging with staging (SPC_ERR_INVALID).  next_idx must
- * not be idx here (next_src is read against idx after next_idx is written).
+ * nor fetch_staging with staging, and next_idx none with idx here (next_src
+ * is read against idx after next_idx is written): SPC_ERR_INVALID.
  * Everything else as spc_decode_step; outputs identical to it and to the
  * separate calls.
  */
@@ -409,7 +409,8 @@ spc_status spc_topk_select(const spc_dims* d, const float* spec_logits, const fl
  *   src:      int32 [B][Hkv][k] output: src[b][hkv][j] = the index i with
  *             prev_idx[b][hkv][i] == idx[b][hkv][j], else -1 (also for the
  *             -1 entries j >= k_eff).
- * idx and bitmap are exactly spc_topk_select's.  prev_idx must not be idx.
+ * idx and bitmap are exactly spc_topk_select's.  prev_idx must not share a
+ * byte with idx (SPC_ERR_INVALID).
  */
 spc_status spc_topk_select_prev(const spc_dims* d, const float* spec_logits, const float* lse,
                                 int32_t k, int32_t* idx, uint32_t* bitmap, const int32_t* prev_idx,

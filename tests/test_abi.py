@@ -80,6 +80,9 @@ def test_validation_happens_before_any_launch(spc):
     with pytest.raises(spc.SpcError) as e:  # the previous selection is the output
         spc.spc_topk_select_prev(d, 16, 16, 4, 16, 16, 16, 4, 48, stream=0)
     assert e.value.status == 1
+    with pytest.raises(spc.SpcError) as e:  # ... or overlaps it (8 KV heads x 4 entries x 4 B = 128 B per buffer)
+        spc.spc_topk_select_prev(d, 16, 16, 4, 1024, 16, 1024 + 64, 4, 48, stream=0)
+    assert e.value.status == 1
     with pytest.raises(spc.SpcError) as e:  # a pre-fetch that keeps staged rows needs src
         spc.spc_merged_attn_fetch_prev(d, 16, 16, 16, None, None, None, 0, 16, None, None, 16, 64, 1024, 16, 4, 32,
                                        None, 48, 4, ws_bytes=1 << 30, stream=0)
