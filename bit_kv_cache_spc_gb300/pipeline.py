@@ -88,6 +88,7 @@ class DecodePipeline:
         queries in q), the first selection and its gather, into copy 0; the
         next step reads copy 0."""
         s = self.main if stream is None else stream
+        s.wait_stream(torch.cuda.current_stream())  # the caches written on the caller's stream
         d, k = self.d, self.k
         self.parity = 0
         for l in range(self.L):

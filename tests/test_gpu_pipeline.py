@@ -142,3 +142,65 @@ def test_pipeline_at_the_llama3_8b_decode_shape():
         got = pipe.staging[pipe.parity][0][b:b + 1, h:h + 1].cpu().numpy().view(np.uint16)
         assert np.array_equal(got, want), t
     assert 0.0 < pipe.kept_fraction() <= 1.0
+
+
+def test_readme_decode_example():
+    """The README's decode example, as written there, at a small shape: the
+    prefill through steps.prefill_layer, the pipeline's pre-decoding step and
+    graph replays with new queries written in place; every layer's outputs
+    and selections then equal the layer-by-layer calls on the same caches."""
+    import synth
+    import synth.gpu
+    from bit_kv_cache_spc_gb300.steps import prefill_layer
+    B, Hq, Hkv, N, R, bits, L, T = 2, 8, 2, 4096, 128, 1, 3, 3
+    d = spc.Dims(B, Hq, Hkv, N, R, bits)
+    k = 41
+    dev = "cuda"
+    K, V = [], []
+    for l in range(L):
+        Kt = torch.empty((B, Hkv, N, 128), dtype=torch.int16, device=dev)
+        Vt = torch.empty_like(Kt)
+        synth.gpu.kv_layer_into(70, l, Kt, Vt)
+        K.append(Kt)
+        V.append(Vt)
+    # --- as in the README ---
+    records = [torch.empty(spc.spc_records_bytes(d), dtype=torch.uint8, device=dev) for _ in range(L)]
+    resid = [torch.empty(spc.spc_resid_bytes(d) // 2, dtype=torch.int16, device=dev) for _ in range(L)]
+    host = [torch.empty((B, Hkv, N, 2, 128), dtype=torch.int16, pin_memory=True) for _ in range(L)]
+    for l in range(L):
+        prefill_layer(d, K[l], V[l], records[l], resid[l], host[l], N)
+    q = [torch.empty((B, 2, Hq, 128), dtype=torch.int16, device=dev) for _ in range(L)]
+    o = [torch.empty((B, 2, Hq, 128), dtype=torch.int16, device=dev) for _ in range(L)]
+    lse = [torch.empty((B, 2, Hq), dtype=torch.float32, device=dev) for _ in range(L)]
+    logits = [torch.empty((B, Hkv, Hq // Hkv, d.q_groups_cap * 32), dtype=torch.float32, device=dev)
+              for _ in range(L)]
+    ws = torch.zeros(spc.spc_attn_workspace_bytes(d, k), dtype=torch.uint8, device=dev)
+    queries = lambda t, l: torch.from_numpy(synth.queries(80 + t, l, B, Hq).view(np.int16).copy()).to(dev)
+    for l in range(L):
+        q[l].copy_(queries(0, l))
+    pipe = DecodePipeline(d, k, records, resid, host, N, q, o, lse, logits, ws, ws.numel())
+    pipe.predecode()
+    graphs = pipe.capture()
+    # --- the reference: the same caches, one layer after another ---
+    cfg = dict(B=B, Hq=Hq, Hkv=Hkv, N=N, R=R, bits=bits, k=k)
+    ref_layers = [GpuLayer(cfg, seed=70, layer=l) for l in range(L)]
+    ref = []
+    for l, g in enumerate(ref_layers):
+        g.q.copy_(queries(0, l))
+        o0, lse0, lg0 = g.attn2()
+        idx, bm = g.topk(lg0, lse0, k)
+        ref.append((idx.contiguous(), bm.contiguous()))
+    for t in range(1, T + 1):
+        for l in range(L):
+            q[l].copy_(queries(t, l))
+        graphs.replay()
+        torch.cuda.synchronize()
+        nidx, nbm = pipe.selection(pipe.parity)
+        for l, g in enumerate(ref_layers):
+            g.q.copy_(queries(t, l))
+            g.gather(ref[l][0], k)
+            ro, rlse, rlg = g.merged(ref[l][0], ref[l][1], k)
+            assert torch.equal(o[l], ro) and torch.equal(lse[l], rlse), (t, l)
+            idx, bm = g.topk(rlg, rlse, k)
+            ref[l] = (idx.contiguous(), bm.contiguous())
+            assert torch.equal(nidx[l], ref[l][0]) and torch.equal(nbm[l], ref[l][1]), (t, l)
