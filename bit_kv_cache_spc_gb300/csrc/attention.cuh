@@ -124,7 +124,8 @@ struct Layout {
   static constexpr int VCODES = KMETA + 512;                                // value code planes
   static constexpr int VMETA = VCODES + 512 * BITS * H;                     // value (min, max) words
   static constexpr int STAGES = GROUP == 32 ? (BITS == 1 ? 4 : 3) : (BITS == 1 ? 3 : 2);  // per warp
-  // a stage: the record, a 16-byte slot (bitmap words, pre-fetch position), a pre-fetched 16-bit row
+  // a stage: the record, a 16-byte slot (bitmap words), 512 spare bytes (they keep the stages and the
+  // z/s table large enough for the 16-bit-row prologue's batches of 16 rows)
   static constexpr int PFROW = RB + 16;
   static constexpr int STAGE = PFROW + 512;
   static constexpr int WARP_BYTES = STAGES * STAGE + kZsBytes;
@@ -519,7 +520,6 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   constexpr int KMETA = LY::KMETA;
   constexpr int VCODES = LY::VCODES;
   constexpr int VMETA = LY::VMETA;
-  constexpr int PFROW = LY::PFROW;
   constexpr int STAGE = LY::STAGE;
   constexpr int kStages = LY::STAGES;
   constexpr int WARP_BYTES = LY::WARP_BYTES;
@@ -553,8 +553,11 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   // warps over consecutive items: the warps of the grid advance in step, and
   // reads that they all issue in the same item arrive at the host link as one
   // burst.  (Phase 0 carries its first row on item 0, the first low-bit
-  // stage, which the 16-bit-row prologue waits for.)  Rows beyond the warp's
-  // items are copied after the groups.
+  // stage, which the 16-bit-row prologue waits for.)  A carried row is loaded
+  // into registers (16 bytes per lane) when its item is issued and stored to
+  // the staging buffer when the next one is issued, pf_every items later, so
+  // the host read's latency stalls no stage of the record pipeline.  Rows
+  // beyond the warp's items are copied after the groups.
   const int pf_nslots = gridDim.x * gridDim.y * kWarps;
   const int pf_slot = (blockIdx.y * gridDim.x + blockIdx.x) * kWarps + warp;
   const int n_pf = (FETCH && a.pf_rows > pf_slot) ? (a.pf_rows - pf_slot + pf_nslots - 1) / pf_nslots : 0;
@@ -564,6 +567,12 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
   int pf_next = n_pf > 0 ? a.pf_idx[pf_slot] : -1;  // position of the next row to issue
   int pf_next_src = (n_pf > 0 && a.pf_src != nullptr) ? a.pf_src[pf_slot] : -1;  // its previous slot, or -1
   int pf_issue_i = 0, pf_issue_item = pf_ph;         // next carried row on the issue side and its item
+  uint4 pf_v = make_uint4(0u, 0u, 0u, 0u);  // the carried row in flight: this lane's 16 bytes
+  int pf_rr = -1;                           // its staging row, or -1
+  auto pf_store = [&]() {
+    if (pf_rr >= 0) reinterpret_cast<uint4*>(a.pf_staging + (int64_t)pf_rr * (2 * kD))[lane] = pf_v;
+    pf_rr = -1;
+  };
 
   auto issue = [&](int item) {
     if (item < n_my) {
@@ -575,19 +584,20 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
       // the record's bitmap words (one per 32-token half) into the slot's first words
       if (MERGED && lane < NH) cp_async4(dst + RB + 4 * lane, a.bitmap + bh * a.q_groups_cap + NH * u + lane);
       if constexpr (FETCH) {
-        // the slot's words 2, 3: (row, position) of the row this item carries, else (-1, -1)
+        // the row this item carries, if any
         const bool carry = item == pf_issue_item && pf_issue_i < pf_carried;
         const int rr = pf_slot + pf_nslots * pf_issue_i;
         const int n = carry ? pf_next : -1;
-        if (lane == 0) reinterpret_cast<int2*>(dst + RB)[1] = make_int2(carry ? rr : -1, n);
         if (carry) {
+          pf_store();  // the previous carried row, loaded pf_every items ago
           if (n >= 0 && n < a.pf_ncap) {
             const int sj = pf_next_src;
             const uint16_t* row =
                 (sj >= 0 && sj < a.pf_prev_k)
                     ? a.pf_prev + ((int64_t)(rr / a.pf_k) * a.pf_prev_k + sj) * (2 * kD)  // still staged
                     : a.pf_host + ((int64_t)(rr / a.pf_k) * a.pf_ncap + n) * (2 * kD);
-            cp_async16(dst + PFROW + 16 * lane, row + 8 * lane);
+            pf_v = reinterpret_cast<const uint4*>(row)[lane];
+            pf_rr = rr;
           }
           pf_next = (pf_issue_i + 1 < n_pf) ? a.pf_idx[rr + pf_nslots] : -1;
           pf_next_src = (a.pf_src != nullptr && pf_issue_i + 1 < n_pf) ? a.pf_src[rr + pf_nslots] : -1;
@@ -641,12 +651,6 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     __syncwarp();
     const uint8_t* R = stage + (it % kStages) * STAGE;
     const int u = u_begin + warp + it * kWarps;
-    if constexpr (FETCH) {  // the carried row, if any, to the staging buffer
-      const int2 pr = reinterpret_cast<const int2*>(R + RB)[1];
-      if (pr.x >= 0 && pr.y >= 0 && pr.y < a.pf_ncap)
-        reinterpret_cast<uint4*>(a.pf_staging + (int64_t)pr.x * (2 * kD))[lane] =
-            reinterpret_cast<const uint4*>(R + PFROW)[lane];
-    }
 
 #pragma unroll 1
     for (int hf = 0; hf < NH; ++hf) {
@@ -885,6 +889,7 @@ __device__ __forceinline__ void lowbit_cta(const AttnArgs& a, uint8_t* dyn, cons
     }  // halves
   }
   cp_async_wait<0>();
+  if constexpr (FETCH) pf_store();
   // pre-fetch rows this warp's groups did not carry, four host reads in flight at a time
   for (int i0 = pf_carried; i0 < n_pf; i0 += 4) {
     int rr[4];
