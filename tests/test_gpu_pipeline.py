@@ -80,6 +80,34 @@ def test_pipeline_equals_layer_by_layer(keep, graph, n_layers, lag):
     assert (frac is None) != keep and (frac is None or 0.0 < frac <= 1.0)
 
 
+@pytest.mark.parametrize("bits,group", [(2, 32), (1, 64), (2, 64)], ids=["b2g32", "b1g64", "b2g64"])
+def test_pipeline_other_codes(bits, group):
+    """The schedule with 2-bit codes and 64-token groups, kept rows, as
+    graphs: outputs and selections bit-identical to the layer-by-layer calls."""
+    cfg = dict(B=2, Hq=8, Hkv=2, N=4096 + 96, R=128, bits=bits, k=41, group=group)
+    k = cfg["k"]
+    layers, pipe = make_pipeline(cfg, 3, 2, True, seed=90)
+    pipe.predecode()
+    torch.cuda.synchronize()
+    ref = []
+    for g in layers:
+        o0, lse0, lg0 = g.attn2()
+        idx, bm = g.topk(lg0, lse0, k)
+        ref.append((idx.contiguous(), bm.contiguous()))
+    graphs = pipe.capture()
+    for t in range(3):
+        graphs.replay()
+        torch.cuda.synchronize()
+        nidx, nbm = pipe.selection(pipe.parity)
+        for l, g in enumerate(layers):
+            g.gather(ref[l][0], k)
+            ro, rlse, rlg = g.merged(ref[l][0], ref[l][1], k)
+            assert torch.equal(pipe.o[l], ro) and torch.equal(pipe.lse[l], rlse), (t, l)
+            idx, bm = g.topk(rlg, rlse, k)
+            ref[l] = (idx.contiguous(), bm.contiguous())
+            assert torch.equal(nidx[l], ref[l][0]) and torch.equal(nbm[l], ref[l][1]), (t, l)
+
+
 def test_pipeline_hooks_bracket_every_call():
     """on_attention / on_topk run before and after each layer's call, on the
     stream the call is enqueued on; without the selection no top-k hook runs."""
