@@ -80,11 +80,13 @@ def test_pipeline_equals_layer_by_layer(keep, graph, n_layers, lag):
     assert (frac is None) != keep and (frac is None or 0.0 < frac <= 1.0)
 
 
-@pytest.mark.parametrize("bits,group", [(2, 32), (1, 64), (2, 64)], ids=["b2g32", "b1g64", "b2g64"])
-def test_pipeline_other_codes(bits, group):
-    """The schedule with 2-bit codes and 64-token groups, kept rows, as
-    graphs: outputs and selections bit-identical to the layer-by-layer calls."""
-    cfg = dict(B=2, Hq=8, Hkv=2, N=4096 + 96, R=128, bits=bits, k=41, group=group)
+@pytest.mark.parametrize("bits,group,Hq", [(2, 32, 8), (1, 64, 8), (2, 64, 8), (1, 32, 4), (1, 32, 2)],
+                         ids=["b2g32", "b1g64", "b2g64", "G2", "G1"])
+def test_pipeline_other_codes(bits, group, Hq):
+    """The schedule with 2-bit codes, 64-token groups and query groups of 1
+    and 2 heads, kept rows, as graphs: outputs and selections bit-identical
+    to the layer-by-layer calls."""
+    cfg = dict(B=2, Hq=Hq, Hkv=2, N=4096 + 96, R=128, bits=bits, k=41, group=group)
     k = cfg["k"]
     layers, pipe = make_pipeline(cfg, 3, 2, True, seed=90)
     pipe.predecode()
